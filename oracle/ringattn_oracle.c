@@ -1,0 +1,451 @@
+/*
+ * ringattn_oracle.c -- float64 CPU oracle for ring attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain reference that the
+ * CUDA path is checked against.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load it.  It shares no code, header, table
+ * or helper with the CUDA library, and it never includes anything from it.
+ *
+ * Sources (web pages on ring attention; cited by page title and section):
+ *   [GRA]  "GPU Ring Attention" essay (aicassindra.com, gpu_ring_attention)
+ *   [ZQ]   "Ring attention" explainer/quiz page (zenaique.com, attn-ring-attention)
+ *   [RA-CN] "Ring Attention：把超长序列沿设备环流动" (charlestar.github.io)
+ *
+ * What it computes:
+ *   - dense attention by its plain definition (the ring reaches exactly this
+ *     result: [GRA] "Why partial results are allowed to merge"; [RA-CN]
+ *     section "局部 Softmax 为什么不能直接相加", last paragraph);
+ *   - a separate simulation of the P-step ring with per-row online-softmax
+ *     states (m, l, O~) and the exact rescale merge ([RA-CN] "环是怎样工作的"
+ *     and "局部 Softmax 为什么不能直接相加"; [GRA] "One lap around the ring");
+ *   - the per-block partial state, the standalone merge of two states, and
+ *     the (wrong) naive sum of per-block softmaxes used as a negative check.
+ *
+ * Readings where the pages are silent (their display formulas were lost):
+ *   - scale = 1/sqrt(d); lse is the natural log of the sum of exp of the
+ *     scaled scores; an empty row has state (m=-inf, l=0, O~=0) and a merge
+ *     with an m=-inf side gives that side weight 0;
+ *   - finalize: out = O~ / l, lse = m + ln(l);
+ *   - layouts: contiguous pos(r,i) = r*n + i ([RA-CN] "位置编码必须使用全局位置");
+ *     striped pos(r,i) = i*P + r (token t goes to shard t mod P);
+ *   - causal: key position <= query position.
+ *
+ * All inputs Q, K, V are bf16 bit patterns (uint16) in natural token order,
+ * laid out [BH][N][d]; they are widened exactly to double.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_LAYOUT_CONTIGUOUS 0
+#define ORACLE_LAYOUT_STRIPED 1
+
+static double widen_bf16(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+}
+
+/* Number of threads an OpenMP parallel region would use now. */
+int oracle_max_threads(int nthreads) {
+  set_threads(nthreads);
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Global token position of local row i of shard r ([RA-CN] "位置编码必须使用全局位置"
+ * for the contiguous map; the striped map sends token t to shard t mod P). */
+long oracle_position(int layout, long n, int P, int r, long i) {
+  if (layout == ORACLE_LAYOUT_STRIPED) return i * (long)P + r;
+  return (long)r * n + i;
+}
+
+/* The K/V block that rank r holds at ring step s: rank r sends to r+1 and
+ * receives from r-1, starting from its own block ([GRA] "One lap around the
+ * ring"; [RA-CN] "环是怎样工作的", the 4-device walk-through). */
+int oracle_block_at(int P, int r, int s) {
+  int j = (r - s) % P;
+  if (j < 0) j += P;
+  return j;
+}
+
+static int allowed(int causal, long pos_q, long pos_k) {
+  return !causal || pos_k <= pos_q;
+}
+
+static double dot_q_k(const uint16_t* q, const uint16_t* k, int d) {
+  double acc = 0.0;
+  for (int c = 0; c < d; ++c) acc += widen_bf16(q[c]) * widen_bf16(k[c]);
+  return acc;
+}
+
+/*
+ * Dense attention, plain definition, for a list of query positions.
+ *   s_k   = (q . k) / sqrt(d)          for every allowed key k
+ *   lse   = log sum_k exp(s_k)         (computed with the row max subtracted)
+ *   out   = sum_k exp(s_k - lse) v_k
+ * rows == NULL means every position 0..N-1 (nrows must equal N then).
+ * out is [BH][nrows][d], lse is [BH][nrows].
+ */
+int oracle_dense_rows(int BH, long N, int d, int causal, const uint16_t* q,
+                      const uint16_t* k, const uint16_t* v, long nrows,
+                      const long* rows, double* out, double* lse,
+                      int nthreads) {
+  if (BH <= 0 || N <= 0 || d <= 0 || nrows < 0) return -1;
+  set_threads(nthreads);
+  const double scale = 1.0 / sqrt((double)d);
+  long total = (long)BH * nrows;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!s) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (long idx = 0; idx < total; ++idx) {
+      if (!s) continue;
+      long bh = idx / nrows, ri = idx % nrows;
+      long t = rows ? rows[ri] : ri;
+      const uint16_t* qrow = q + ((size_t)bh * N + t) * d;
+      const uint16_t* kb = k + (size_t)bh * N * d;
+      const uint16_t* vb = v + (size_t)bh * N * d;
+      double m = -INFINITY;
+      for (long kk = 0; kk < N; ++kk) {
+        if (!allowed(causal, t, kk)) continue;
+        s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
+        if (s[kk] > m) m = s[kk];
+      }
+      double sum = 0.0;
+      for (long kk = 0; kk < N; ++kk)
+        if (allowed(causal, t, kk)) sum += exp(s[kk] - m);
+      double l = m + log(sum);
+      double* o = out + (size_t)idx * d;
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      for (long kk = 0; kk < N; ++kk) {
+        if (!allowed(causal, t, kk)) continue;
+        double w = exp(s[kk] - l);
+        const uint16_t* vr = vb + (size_t)kk * d;
+        for (int c = 0; c < d; ++c) o[c] += w * widen_bf16(vr[c]);
+      }
+      lse[idx] = l;
+    }
+    free(s);
+  }
+  return failed ? -2 : 0;
+}
+
+/*
+ * Partial state of one query row against one K/V block, by definition
+ * ([RA-CN] "局部 Softmax 为什么不能直接相加": per row the running max m, the exp
+ * sum l scaled by that max, and the unnormalised value sum O~):
+ *   m  = max over allowed keys of s_k        (-inf if none allowed)
+ *   l  = sum exp(s_k - m)
+ *   O~ = sum exp(s_k - m) v_k
+ * kpos[k] is the global position of key k of the block.
+ */
+static void row_block_state(const uint16_t* qrow, long pos_q, const uint16_t* kb,
+                            const uint16_t* vb, const long* kpos, long nk, int d,
+                            int causal, double scale, double* s, double* m_out,
+                            double* l_out, double* o_out, long* visit_row) {
+  double m = -INFINITY;
+  for (long kk = 0; kk < nk; ++kk) {
+    if (!allowed(causal, pos_q, kpos[kk])) continue;
+    s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
+    if (s[kk] > m) m = s[kk];
+  }
+  double l = 0.0;
+  for (int c = 0; c < d; ++c) o_out[c] = 0.0;
+  if (m != -INFINITY) {
+    for (long kk = 0; kk < nk; ++kk) {
+      if (!allowed(causal, pos_q, kpos[kk])) continue;
+      double w = exp(s[kk] - m);
+      l += w;
+      const uint16_t* vr = vb + (size_t)kk * d;
+      for (int c = 0; c < d; ++c) o_out[c] += w * widen_bf16(vr[c]);
+      if (visit_row) visit_row[kpos[kk]] += 1;
+    }
+  }
+  *m_out = m;
+  *l_out = l;
+}
+
+/*
+ * Merge of two online-softmax states into (m, l, O~) ([GRA] "Why partial
+ * results are allowed to merge": both accumulators are rescaled by the exp of
+ * the difference between the old and the new maximum, then added; [ZQ]: the
+ * running output is rescaled by exp(old_max - new_max)).
+ *   m = max(ma, mb); a = exp(ma - m); b = exp(mb - m)  (0 for an -inf side)
+ *   l = a la + b lb;  O~ = a O~a + b O~b
+ */
+static void merge_pair(double ma, double la, const double* oa, double mb,
+                       double lb, const double* ob, int d, double* m,
+                       double* l, double* o) {
+  double mm = ma > mb ? ma : mb;
+  double a = (ma == -INFINITY) ? 0.0 : exp(ma - mm);
+  double b = (mb == -INFINITY) ? 0.0 : exp(mb - mm);
+  *m = mm;
+  *l = a * la + b * lb;
+  for (int c = 0; c < d; ++c) o[c] = a * oa[c] + b * ob[c];
+}
+
+/*
+ * Ring simulation ([RA-CN] "环是怎样工作的": the forward as a loop over
+ * world_size steps that computes a block partial and merges it into the local
+ * state, then finalizes; [GRA] "One lap around the ring").
+ * P virtual ranks; rank r owns the query rows of shard r.  At step s it holds
+ * block j = (r - s) mod P, computes the block partial of its rows against it
+ * and merges that into its running state; after P steps it finalizes
+ *   out = O~ / l,   lse = m + ln l.
+ * rows: global query positions to simulate (NULL = all N).  out/lse are
+ * indexed like oracle_dense_rows.  visits (NULL or [BH][N][N] counters)
+ * receives +1 for every (query, key) pair the simulation used.
+ */
+int oracle_ring_rows(int BH, long N, int d, int P, int causal, int layout,
+                     const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     long nrows, const long* rows, double* out, double* lse,
+                     long* visits, int nthreads) {
+  if (BH <= 0 || N <= 0 || d <= 0 || P <= 0 || N % P != 0 || nrows < 0)
+    return -1;
+  set_threads(nthreads);
+  const long n = N / P;
+  const double scale = 1.0 / sqrt((double)d);
+  long total = (long)BH * nrows;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    long* kpos = (long*)malloc(sizeof(long) * (size_t)n);
+    uint16_t* kblk = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * d);
+    uint16_t* vblk = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * d);
+    double* ob = (double*)malloc(sizeof(double) * (size_t)d);
+    double* ost = (double*)malloc(sizeof(double) * (size_t)d);
+    double* otmp = (double*)malloc(sizeof(double) * (size_t)d);
+    int ok = s && kpos && kblk && vblk && ob && ost && otmp;
+    if (!ok) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (long idx = 0; idx < total; ++idx) {
+      if (!ok) continue;
+      long bh = idx / nrows, ri = idx % nrows;
+      long t = rows ? rows[ri] : ri;
+      /* which rank owns query position t, and its local row */
+      int r = (layout == ORACLE_LAYOUT_STRIPED) ? (int)(t % P) : (int)(t / n);
+      long i = (layout == ORACLE_LAYOUT_STRIPED) ? t / P : t % n;
+      const uint16_t* qrow =
+          q + ((size_t)bh * N + oracle_position(layout, n, P, r, i)) * d;
+      long* visit_row = visits ? visits + ((size_t)bh * N + t) * N : NULL;
+      double m = -INFINITY, l = 0.0;
+      for (int c = 0; c < d; ++c) ost[c] = 0.0;
+      for (int step = 0; step < P; ++step) {
+        int j = oracle_block_at(P, r, step);
+        /* the block as it would travel: rows of shard j, in local order */
+        for (long kk = 0; kk < n; ++kk) {
+          long pk = oracle_position(layout, n, P, j, kk);
+          kpos[kk] = pk;
+          memcpy(kblk + (size_t)kk * d, k + ((size_t)bh * N + pk) * d,
+                 sizeof(uint16_t) * d);
+          memcpy(vblk + (size_t)kk * d, v + ((size_t)bh * N + pk) * d,
+                 sizeof(uint16_t) * d);
+        }
+        double mb, lb;
+        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, scale, s, &mb,
+                        &lb, ob, visit_row);
+        double mn, ln;
+        merge_pair(m, l, ost, mb, lb, ob, d, &mn, &ln, otmp);
+        m = mn;
+        l = ln;
+        memcpy(ost, otmp, sizeof(double) * d);
+      }
+      double* o = out + (size_t)idx * d;
+      for (int c = 0; c < d; ++c) o[c] = ost[c] / l;
+      lse[idx] = m + log(l);
+    }
+    free(s);
+    free(kpos);
+    free(kblk);
+    free(vblk);
+    free(ob);
+    free(ost);
+    free(otmp);
+  }
+  return failed ? -2 : 0;
+}
+
+/*
+ * Block partial state of shard r's query rows against K/V block j, with the
+ * global-position mask ([RA-CN] "Causal Attention 让环不再完全对称": skip a
+ * strictly-future block, mask a block on the diagonal, else no mask).
+ * q_shard, k_block, v_block are shard-major [BH][n][d] bf16 bit patterns.
+ * Outputs m, l [BH][n] and o [BH][n][d] as defined in row_block_state.
+ */
+int oracle_block_partial(int BH, long n, int d, int P, int causal, int layout,
+                         int r, int j, const uint16_t* q_shard,
+                         const uint16_t* k_block, const uint16_t* v_block,
+                         double* m, double* l, double* o, int nthreads) {
+  if (BH <= 0 || n <= 0 || d <= 0 || P <= 0 || r < 0 || r >= P || j < 0 ||
+      j >= P)
+    return -1;
+  set_threads(nthreads);
+  const double scale = 1.0 / sqrt((double)d);
+  long total = (long)BH * n;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    long* kpos = (long*)malloc(sizeof(long) * (size_t)n);
+    int ok = s && kpos;
+    if (!ok) {
+#pragma omp atomic write
+      failed = 1;
+    }
+    if (ok)
+      for (long kk = 0; kk < n; ++kk)
+        kpos[kk] = oracle_position(layout, n, P, j, kk);
+#pragma omp for schedule(dynamic, 4)
+    for (long idx = 0; idx < total; ++idx) {
+      if (!ok) continue;
+      long bh = idx / n, i = idx % n;
+      row_block_state(q_shard + (size_t)idx * d,
+                      oracle_position(layout, n, P, r, i),
+                      k_block + (size_t)bh * n * d, v_block + (size_t)bh * n * d,
+                      kpos, n, d, causal, scale, s, &m[idx], &l[idx],
+                      o + (size_t)idx * d, NULL);
+    }
+    free(s);
+    free(kpos);
+  }
+  return failed ? -2 : 0;
+}
+
+/*
+ * Standalone merge of two fp32 states (as a GPU produces them), in float64.
+ * Inputs: rows x {m, l} and rows x d for O~, per side.  Outputs in double.
+ */
+int oracle_merge_states(long rows, int d, const float* ma, const float* la,
+                        const float* oa, const float* mb, const float* lb,
+                        const float* ob, double* m, double* l, double* o) {
+  if (rows < 0 || d <= 0) return -1;
+  double* ta = (double*)malloc(sizeof(double) * (size_t)d);
+  double* tb = (double*)malloc(sizeof(double) * (size_t)d);
+  if (!ta || !tb) {
+    free(ta);
+    free(tb);
+    return -2;
+  }
+  for (long x = 0; x < rows; ++x) {
+    for (int c = 0; c < d; ++c) {
+      ta[c] = (double)oa[(size_t)x * d + c];
+      tb[c] = (double)ob[(size_t)x * d + c];
+    }
+    merge_pair((double)ma[x], (double)la[x], ta, (double)mb[x], (double)lb[x],
+               tb, d, &m[x], &l[x], o + (size_t)x * d);
+  }
+  free(ta);
+  free(tb);
+  return 0;
+}
+
+/* Same merge on double states: a <- merge(a, b), in place.  Used to check that
+ * the merge is order independent (associative and commutative). */
+int oracle_merge_inplace(long rows, int d, double* ma, double* la, double* oa,
+                         const double* mb, const double* lb, const double* ob) {
+  if (rows < 0 || d <= 0) return -1;
+  double* t = (double*)malloc(sizeof(double) * (size_t)d);
+  if (!t) return -2;
+  for (long x = 0; x < rows; ++x) {
+    double m, l;
+    merge_pair(ma[x], la[x], oa + (size_t)x * d, mb[x], lb[x],
+               ob + (size_t)x * d, d, &m, &l, t);
+    ma[x] = m;
+    la[x] = l;
+    memcpy(oa + (size_t)x * d, t, sizeof(double) * d);
+  }
+  free(t);
+  return 0;
+}
+
+/* Finalize states: out = O~/l, lse = m + ln l (an empty row gives out = 0 and
+ * lse = -inf). */
+int oracle_finalize(long rows, int d, const double* m, const double* l,
+                    const double* o, double* out, double* lse) {
+  if (rows < 0 || d <= 0) return -1;
+  for (long x = 0; x < rows; ++x) {
+    if (l[x] == 0.0) {
+      for (int c = 0; c < d; ++c) out[(size_t)x * d + c] = 0.0;
+      lse[x] = -INFINITY;
+      continue;
+    }
+    for (int c = 0; c < d; ++c)
+      out[(size_t)x * d + c] = o[(size_t)x * d + c] / l[x];
+    lse[x] = m[x] + log(l[x]);
+  }
+  return 0;
+}
+
+/*
+ * The wrong combination the pages warn against ([GRA] "Why partial results
+ * are allowed to merge": naively summing partial outputs is wrong; [RA-CN]
+ * "局部 Softmax 为什么不能直接相加": a softmax per block, outputs added):
+ *   out_naive = sum over blocks j with an allowed key of softmax(S^(j)) V_j.
+ * Natural order in and out, out is [BH][N][d].
+ */
+int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, int layout,
+                           const uint16_t* q, const uint16_t* k,
+                           const uint16_t* v, double* out) {
+  if (BH <= 0 || N <= 0 || d <= 0 || P <= 0 || N % P != 0) return -1;
+  const long n = N / P;
+  const double scale = 1.0 / sqrt((double)d);
+  double* s = (double*)malloc(sizeof(double) * (size_t)n);
+  long* kpos = (long*)malloc(sizeof(long) * (size_t)n);
+  uint16_t* kblk = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * d);
+  uint16_t* vblk = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * d);
+  double* ob = (double*)malloc(sizeof(double) * (size_t)d);
+  if (!s || !kpos || !kblk || !vblk || !ob) {
+    free(s); free(kpos); free(kblk); free(vblk); free(ob);
+    return -2;
+  }
+  for (int bh = 0; bh < BH; ++bh) {
+    for (long t = 0; t < N; ++t) {
+      double* o = out + ((size_t)bh * N + t) * d;
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      const uint16_t* qrow = q + ((size_t)bh * N + t) * d;
+      for (int j = 0; j < P; ++j) {
+        for (long kk = 0; kk < n; ++kk) {
+          long pk = oracle_position(layout, n, P, j, kk);
+          kpos[kk] = pk;
+          memcpy(kblk + (size_t)kk * d, k + ((size_t)bh * N + pk) * d,
+                 sizeof(uint16_t) * d);
+          memcpy(vblk + (size_t)kk * d, v + ((size_t)bh * N + pk) * d,
+                 sizeof(uint16_t) * d);
+        }
+        double mb, lb;
+        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, scale, s, &mb,
+                        &lb, ob, NULL);
+        if (lb > 0.0)
+          for (int c = 0; c < d; ++c) o[c] += ob[c] / lb;
+      }
+    }
+  }
+  free(s); free(kpos); free(kblk); free(vblk); free(ob);
+  return 0;
+}

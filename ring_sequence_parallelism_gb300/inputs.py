@@ -1,0 +1,105 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the benchmark.
+
+This module holds no attention arithmetic: it only draws Q, K, V and picks
+sample rows.  Both the CUDA path and the float64 oracle consume exactly the
+bytes it returns.
+
+Recipe: Q, K, V are i.i.d. N(0, 1) float32 drawn on the CPU from a seeded
+``torch.Generator`` (Q for all heads, then K, then V, one head at a time) and
+rounded to bfloat16 with round-to-nearest-even.  The long-context workload
+additionally multiplies 1% of the key rows (floor(N/100) token positions, the
+same for every head, chosen by ``randperm`` of a second generator seeded
+``seed + 1``) by 8 after rounding; the multiplication is exact in bf16.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    P: int
+    causal: bool
+    layout: str  # "contiguous" | "striped"
+    seed: int
+    key_boost_frac: float = 0.0  # fraction of key rows scaled by key_boost
+    key_boost: float = 8.0
+
+    @property
+    def n(self) -> int:
+        return self.N // self.P
+
+    @property
+    def layout_id(self) -> int:
+        return 1 if self.layout == "striped" else 0
+
+    def allowed_pairs_per_head(self) -> int:
+        return self.N * (self.N + 1) // 2 if self.causal else self.N * self.N
+
+    def flops(self) -> int:
+        """Causal-adjusted FLOPs: 4*d per allowed (q, k) pair (QK^T and PV)."""
+        return 4 * self.B * self.H * self.d * self.allowed_pairs_per_head()
+
+
+WORKLOADS = {
+    w.name: w
+    for w in (
+        Workload("noncausal-512", 1, 2, 512, 64, 4, False, "contiguous", 1000),
+        Workload("contiguous-8k", 1, 8, 8192, 128, 8, True, "contiguous", 1001),
+        Workload("striped-8k", 1, 8, 8192, 128, 8, True, "striped", 1001),
+        Workload("striped-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01),
+        Workload("striped-1m", 1, 8, 1048576, 128, 64, True, "striped", 1004),
+    )
+}
+
+ROW_SAMPLE_SEED = 2004
+
+
+def make_qkv(B: int, H: int, N: int, d: int, seed: int, key_boost_frac: float = 0.0,
+             key_boost: float = 8.0, device="cpu", pin: bool = False):
+    """Return (q, k, v) bf16 tensors [B, H, N, d] drawn as the module docstring says."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    out = []
+    for _ in range(3):
+        t = torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=pin)
+        for b in range(B):
+            for h in range(H):
+                t[b, h].copy_(torch.randn((N, d), generator=g, dtype=torch.float32))
+        out.append(t)
+    q, k, v = out
+    if key_boost_frac > 0.0:
+        rows = boosted_key_rows(N, seed, key_boost_frac)
+        k[:, :, rows, :] *= key_boost
+    if device != "cpu":
+        q, k, v = (x.to(device) for x in (q, k, v))
+    return q, k, v
+
+
+def boosted_key_rows(N: int, seed: int, frac: float) -> torch.Tensor:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 1)
+    count = int(N * frac)
+    return torch.randperm(N, generator=g)[:count].sort().values
+
+
+def make_workload(w: Workload, device="cpu", pin: bool = False):
+    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.key_boost_frac, w.key_boost, device=device, pin=pin)
+
+
+def sample_rows(N: int, count: int, seed: int = ROW_SAMPLE_SEED, extra=()) -> torch.Tensor:
+    """Seeded distinct query positions (sorted), plus any ``extra`` positions."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    count = min(count, N)
+    rows = torch.randperm(N, generator=g)[:count]
+    if extra:
+        rows = torch.cat([rows, torch.tensor([e for e in extra if 0 <= e < N], dtype=torch.long)])
+    return torch.unique(rows)

@@ -1,0 +1,336 @@
+"""Pins that tie the float64 oracle to what the pages and the mathematics fix.
+
+Each pin takes an ``oracle.Oracle`` and raises AssertionError on a mismatch.
+They are run against the real oracle (tests/test_oracle.py) and against
+copies of it with planted mistakes (tests/test_oracle_mutations.py), which
+must each trip at least one pin.
+
+Sources cited by page title and section:
+  [GRA]   "GPU Ring Attention" (aicassindra.com)
+  [ZQ]    Ring attention explainer page (zenaique.com)
+  [RA-CN] "Ring Attention：把超长序列沿设备环流动" (charlestar.github.io)
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED, bits_to_f64, bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+LAYOUTS = (LAYOUT_CONTIGUOUS, LAYOUT_STRIPED)
+
+
+def rand_bits(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    t = (torch.randn(shape, generator=g, dtype=torch.float32) * scale).to(torch.bfloat16)
+    return bf16_bits(t)
+
+
+def to_bits(x: np.ndarray) -> np.ndarray:
+    """float array -> bf16 bits (values must already be bf16-representable)."""
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
+    back = t.to(torch.float32).numpy()
+    assert np.array_equal(back, np.asarray(x, np.float32)), "value not exact in bf16"
+    return bf16_bits(t)
+
+
+def allowed_matrix(N, causal):
+    if not causal:
+        return np.ones((N, N), bool)
+    return np.tril(np.ones((N, N), bool))
+
+
+def _close(a, b, tol, what):
+    err = float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+
+
+# ---------------------------------------------------------------- dense path
+def pin_equal_keys_closed_form(orc):
+    """All key rows equal: every allowed key has the same score s, so the
+    softmax is uniform: out = mean of the allowed v rows, lse = s + ln(count)."""
+    BH, N, d = 2, 24, 8
+    q = rand_bits((BH, N, d), 11)
+    k0 = rand_bits((BH, 1, d), 12)
+    k = np.ascontiguousarray(np.repeat(k0, N, axis=1))
+    v = rand_bits((BH, N, d), 13)
+    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    for causal in (False, True):
+        cnt = np.arange(1, N + 1) if causal else np.full(N, N)
+        mean_v = (np.cumsum(vf, axis=1) / cnt[None, :, None]) if causal else np.repeat(vf.mean(1, keepdims=True), N, 1)
+        s = np.einsum("bnd,bd->bn", qf, kf[:, 0, :]) / math.sqrt(d)
+        exp_lse = s + np.log(cnt)[None, :]
+        out, lse = orc.dense(q, k, v, causal)
+        _close(out, mean_v, 1e-12, "equal keys: out")
+        _close(lse, exp_lse, 1e-12, "equal keys: lse")
+        for layout in LAYOUTS:
+            out, lse = orc.ring(q, k, v, 4, causal, layout)
+            _close(out, mean_v, 1e-12, "equal keys (ring): out")
+            _close(lse, exp_lse, 1e-12, "equal keys (ring): lse")
+
+
+def pin_constant_values(orc):
+    """Every v row equal to c: any convex combination is c."""
+    BH, N, d = 2, 16, 4
+    q, k = rand_bits((BH, N, d), 21), rand_bits((BH, N, d), 22)
+    c = np.array([0.5, -1.25, 3.0, 0.0078125], np.float32)
+    v = to_bits(np.broadcast_to(c, (BH, N, d)))
+    for causal in (False, True):
+        out, _ = orc.dense(q, k, v, causal)
+        _close(out, np.broadcast_to(c, out.shape), 1e-13, "constant v (dense)")
+        out, _ = orc.ring(q, k, v, 4, causal, LAYOUT_STRIPED)
+        _close(out, np.broadcast_to(c, out.shape), 1e-13, "constant v (ring)")
+
+
+def pin_causal_first_row(orc):
+    """Causal row 0 sees only key 0: out_0 = v_0 and lse_0 = s_00."""
+    BH, N, d = 3, 12, 8
+    q, k, v = rand_bits((BH, N, d), 31), rand_bits((BH, N, d), 32), rand_bits((BH, N, d), 33)
+    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    s00 = np.einsum("bd,bd->b", qf[:, 0], kf[:, 0]) / math.sqrt(d)
+    for fn in (lambda: orc.dense(q, k, v, True),
+               lambda: orc.ring(q, k, v, 3, True, LAYOUT_CONTIGUOUS),
+               lambda: orc.ring(q, k, v, 3, True, LAYOUT_STRIPED)):
+        out, lse = fn()
+        _close(out[:, 0], vf[:, 0], 0.0, "causal row 0: out")
+        _close(lse[:, 0], s00, 1e-14, "causal row 0: lse")
+
+
+def pin_dominant_key(orc):
+    """One key outscores every other allowed key by ~2000 nats: the output is
+    that key's value (scores of 2048, whose exp overflows even float64, also
+    test that the oracle subtracts the row max; [RA-CN] "正确性测试应覆盖哪些边界": online
+    softmax stability under extreme scores)."""
+    BH, N, d = 1, 16, 4
+    q = to_bits(np.full((BH, N, d), 32.0, np.float32))
+    kv = np.full((BH, N, d), 1.0, np.float32)
+    kv[:, 5, :] = 32.0  # q.k/2 = 2048 for key 5, 64 for the others
+    k = to_bits(kv)
+    v = rand_bits((BH, N, d), 41)
+    vf = bits_to_f64(v)
+    for causal in (False, True):
+        out, lse = orc.dense(q, k, v, causal)
+        rows = np.arange(5, N) if causal else np.arange(N)
+        _close(out[:, rows], np.broadcast_to(vf[:, 5:6], (BH, rows.size, d)), 1e-20, "dominant key out")
+        assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse)), "overflow with extreme scores"
+        _close(lse[:, rows], np.full((BH, rows.size), 2048.0), 1e-12, "dominant key lse")
+        out_r, lse_r = orc.ring(q, k, v, 4, causal, LAYOUT_STRIPED)
+        _close(out_r, out, 1e-12, "dominant key ring")
+        _close(lse_r, lse, 1e-12, "dominant key ring lse")
+
+
+def pin_sdpa(orc):
+    """Reduction to a library routine: torch's scaled_dot_product_attention in
+    float64 on the CPU, and logsumexp of the masked score matrix."""
+    for (BH, N, d) in ((2, 40, 16), (1, 33, 64), (3, 7, 1)):
+        q, k, v = rand_bits((BH, N, d), 51 + N), rand_bits((BH, N, d), 52 + N), rand_bits((BH, N, d), 53 + N)
+        qt, kt, vt = (torch.from_numpy(bits_to_f64(x)) for x in (q, k, v))
+        for causal in (False, True):
+            ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=causal)
+            sc = torch.einsum("bqd,bkd->bqk", qt, kt) / math.sqrt(d)
+            if causal:
+                sc = sc.masked_fill(~torch.from_numpy(allowed_matrix(N, True)), float("-inf"))
+            ref_lse = torch.logsumexp(sc, dim=-1)
+            out, lse = orc.dense(q, k, v, causal)
+            _close(out, ref.numpy(), 1e-12, "sdpa out")
+            _close(lse, ref_lse.numpy(), 1e-12, "sdpa lse")
+
+
+# ------------------------------------------------------------------ the ring
+def pin_ring_equals_dense(orc):
+    """The ring reaches the dense result ([GRA] "Why partial results are
+    allowed to merge": exact after P merges; [RA-CN] "局部 Softmax 为什么不能直接相加")
+    for every divisor P of N, both layouts, causal and not."""
+    for (BH, N, d) in ((2, 24, 4), (1, 16, 1), (1, 12, 64)):
+        q, k, v = rand_bits((BH, N, d), 61 + d), rand_bits((BH, N, d), 62 + d), rand_bits((BH, N, d), 63 + d)
+        for causal in (False, True):
+            ref_out, ref_lse = orc.dense(q, k, v, causal)
+            for P in [p for p in range(1, N + 1) if N % p == 0]:
+                for layout in LAYOUTS:
+                    out, lse = orc.ring(q, k, v, P, causal, layout)
+                    tol = 1e-13 if P == 1 else 1e-12
+                    _close(out, ref_out, tol, f"ring=dense out P={P} layout={layout} causal={causal}")
+                    _close(lse, ref_lse, tol, f"ring=dense lse P={P} layout={layout} causal={causal}")
+
+
+def pin_layouts_agree(orc):
+    """Contiguous and striped layouts give the same natural-order result."""
+    BH, N, d = 2, 32, 8
+    q, k, v = rand_bits((BH, N, d), 71), rand_bits((BH, N, d), 72), rand_bits((BH, N, d), 73)
+    for causal in (False, True):
+        for P in (2, 4, 8):
+            a = orc.ring(q, k, v, P, causal, LAYOUT_CONTIGUOUS)
+            b = orc.ring(q, k, v, P, causal, LAYOUT_STRIPED)
+            _close(a[0], b[0], 1e-12, "layouts out")
+            _close(a[1], b[1], 1e-12, "layouts lse")
+
+
+def pin_visits_exactly_once(orc):
+    """Every allowed (q, k) pair is used exactly once and no other pair is
+    ([RA-CN] "局部 Softmax 为什么不能直接相加": every allowed Q-K pair computed)."""
+    BH, N, d = 1, 24, 2
+    q, k, v = rand_bits((BH, N, d), 81), rand_bits((BH, N, d), 82), rand_bits((BH, N, d), 83)
+    for causal in (False, True):
+        want = allowed_matrix(N, causal).astype(np.int64)
+        for P in (1, 2, 3, 4, 6, 8, 12, 24):
+            for layout in LAYOUTS:
+                _, _, cnt = orc.ring(q, k, v, P, causal, layout, visits=True)
+                assert np.array_equal(cnt[0], want), f"visits P={P} layout={layout} causal={causal}"
+
+
+def pin_shard_work_closed_forms(orc):
+    """Allowed pairs per shard under the causal mask, from the visit counts:
+    contiguous W_r = r n^2 + n(n+1)/2; striped W_r = (r+1) n(n+1)/2 +
+    (P-1-r) n(n-1)/2; both sum to N(N+1)/2 ([GRA] "The causal mask wrecks the
+    load balance": a linear ramp from one block of work to P)."""
+    BH, N, d = 1, 24, 1
+    q, k, v = rand_bits((BH, N, d), 91), rand_bits((BH, N, d), 92), rand_bits((BH, N, d), 93)
+    for P in (2, 3, 4, 6):
+        n = N // P
+        for layout in LAYOUTS:
+            _, _, cnt = orc.ring(q, k, v, P, True, layout, visits=True)
+            per_row = cnt[0].sum(axis=1)
+            for r in range(P):
+                rows = [orc.position(layout, n, P, r, i) for i in range(n)]
+                got = int(per_row[rows].sum())
+                if layout == LAYOUT_CONTIGUOUS:
+                    want = r * n * n + n * (n + 1) // 2
+                else:
+                    want = (r + 1) * n * (n + 1) // 2 + (P - 1 - r) * n * (n - 1) // 2
+                assert got == want, f"W_{r} layout={layout} P={P}: {got} != {want}"
+            assert int(per_row.sum()) == N * (N + 1) // 2
+
+
+def pin_naive_sum_differs(orc):
+    """Summing per-block softmax outputs is wrong ([GRA] "Why partial results
+    are allowed to merge"; [RA-CN] "局部 Softmax 为什么不能直接相加"): each block
+    normalises to 1 on its own, so rows with two or more non-empty blocks
+    differ from dense attention."""
+    BH, N, d = 1, 16, 8
+    q, k, v = rand_bits((BH, N, d), 101), rand_bits((BH, N, d), 102), rand_bits((BH, N, d), 103)
+    for causal in (False, True):
+        ref, _ = orc.dense(q, k, v, causal)
+        naive = orc.naive_block_sum(q, k, v, 4, causal, LAYOUT_CONTIGUOUS)
+        assert float(np.max(np.abs(naive - ref))) > 1e-2, "naive sum should differ"
+        # with one block (P = 1) the naive sum is the dense result
+        one = orc.naive_block_sum(q, k, v, 1, causal, LAYOUT_CONTIGUOUS)
+        _close(one, ref, 1e-12, "naive sum with P=1")
+
+
+def pin_merge_order_independent(orc):
+    """The merge is associative and commutative: folding the P block partials
+    of a shard in any order and bracketing gives the same state, and its
+    finalize equals dense attention."""
+    BH, N, d, P = 2, 32, 8, 4
+    n = N // P
+    q, k, v = rand_bits((BH, N, d), 111), rand_bits((BH, N, d), 112), rand_bits((BH, N, d), 113)
+    rng = np.random.default_rng(5)
+    for layout in LAYOUTS:
+        for causal in (False, True):
+            ref_out, ref_lse = orc.dense(q, k, v, causal)
+            for r in range(P):
+                pos = np.array([orc.position(layout, n, P, r, i) for i in range(n)])
+                qs = np.ascontiguousarray(q[:, pos])
+                parts = []
+                for j in range(P):
+                    kpos = np.array([orc.position(layout, n, P, j, i) for i in range(n)])
+                    parts.append(orc.block_partial(qs, np.ascontiguousarray(k[:, kpos]),
+                                                   np.ascontiguousarray(v[:, kpos]), P, causal, layout, r, j))
+                results = []
+                for trial in range(4):
+                    order = rng.permutation(P)
+                    if trial % 2 == 0:  # left fold
+                        acc = [x.copy() for x in parts[order[0]]]
+                        for j in order[1:]:
+                            orc.merge_inplace(acc, parts[j])
+                    else:  # pairwise tree
+                        items = [[x.copy() for x in parts[j]] for j in order]
+                        while len(items) > 1:
+                            nxt = []
+                            for a in range(0, len(items) - 1, 2):
+                                orc.merge_inplace(items[a], items[a + 1])
+                                nxt.append(items[a])
+                            if len(items) % 2:
+                                nxt.append(items[-1])
+                            items = nxt
+                        acc = items[0]
+                    out, lse = orc.finalize(*acc)
+                    results.append((out, lse))
+                for out, lse in results:
+                    _close(out, ref_out[:, pos], 1e-12, "merge order: out")
+                    _close(lse, ref_lse[:, pos], 1e-12, "merge order: lse")
+
+
+def pin_merge_empty_side(orc):
+    """A side with m = -inf (a block with no allowed key) contributes nothing;
+    two empty sides stay empty."""
+    d = 3
+    a = (np.array([0.5, -np.inf], np.float32), np.array([2.0, 0.0], np.float32),
+         np.array([[1, 2, 3], [0, 0, 0]], np.float32))
+    b = (np.array([-np.inf, -np.inf], np.float32), np.array([0.0, 0.0], np.float32), np.zeros((2, d), np.float32))
+    m, l, o = orc.merge_states(a, b)
+    assert m[0] == 0.5 and l[0] == 2.0 and np.array_equal(o[0], [1, 2, 3])
+    assert m[1] == -np.inf and l[1] == 0.0 and np.array_equal(o[1], [0, 0, 0]) and not np.any(np.isnan(o))
+    m2, l2, o2 = orc.merge_states(b, a)
+    assert m2[0] == 0.5 and l2[0] == 2.0 and np.array_equal(o2[0], [1, 2, 3])
+
+
+def pin_merge_two_point_example(orc):
+    """Two one-key blocks with scores 0 and ln 4 in float32 states: the merged
+    softmax weights are 1/5 and 4/5 (values chosen so the answer is known)."""
+    ln4 = np.float32(math.log(4.0))
+    a = (np.array([0.0], np.float32), np.array([1.0], np.float32), np.array([[10.0, 0.0]], np.float32))
+    b = (np.array([ln4], np.float32), np.array([1.0], np.float32), np.array([[0.0, 5.0]], np.float32))
+    m, l, o = orc.merge_states(a, b)
+    out, lse = orc.finalize(m, l, o)
+    w_b = 1.0 / (1.0 + math.exp(-float(ln4)))
+    _close(out[0], [10.0 * (1 - w_b), 5.0 * w_b], 1e-15, "two-point merge out")
+    _close(lse, [math.log(1.0 + math.exp(float(ln4)))], 1e-15, "two-point merge lse")
+    assert abs(w_b - 0.8) < 1e-7
+
+
+def pin_golden_schedule(orc):
+    """The 4-device walk-through printed in [RA-CN] "环是怎样工作的": at step 0
+    device r uses its own block; at step 1 device 0 holds block 3, device 1
+    block 0, device 2 block 1, device 3 block 2."""
+    path = os.path.join(GOLDEN, "ring_schedule_4dev.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert rows
+    for step, dev, blk in rows:
+        assert orc.block_at(4, int(dev), int(step)) == int(blk), (step, dev, blk)
+
+
+def pin_positions(orc):
+    """Global positions: contiguous device p local i -> p*n + i ([RA-CN]
+    "位置编码必须使用全局位置"); striped: token t on shard t mod P; both maps are
+    bijections onto 0..N-1."""
+    n, P = 5, 4
+    assert orc.position(LAYOUT_CONTIGUOUS, n, P, 2, 3) == 13
+    assert orc.position(LAYOUT_STRIPED, n, P, 2, 3) == 14
+    for layout in LAYOUTS:
+        seen = sorted(orc.position(layout, n, P, r, i) for r in range(P) for i in range(n))
+        assert seen == list(range(n * P))
+
+
+ALL_PINS = [
+    pin_equal_keys_closed_form,
+    pin_constant_values,
+    pin_causal_first_row,
+    pin_dominant_key,
+    pin_sdpa,
+    pin_ring_equals_dense,
+    pin_layouts_agree,
+    pin_visits_exactly_once,
+    pin_shard_work_closed_forms,
+    pin_naive_sum_differs,
+    pin_merge_order_independent,
+    pin_merge_empty_side,
+    pin_merge_two_point_example,
+    pin_golden_schedule,
+    pin_positions,
+]

@@ -1,0 +1,68 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins
+catch each one (CPU only; the planted copies live in a temporary directory,
+never in the source tree)."""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (name, text to find, replacement, which occurrence (0-based) or None = all)
+MUTATIONS = [
+    ("causal mask off by one", "return !causal || pos_k <= pos_q;", "return !causal || pos_k < pos_q;", None),
+    ("scale 1/d instead of 1/sqrt(d)", "1.0 / sqrt((double)d)", "1.0 / (double)d", None),
+    ("rescale sign flipped", "exp(ma - mm)", "exp(mm - ma)", None),
+    ("merge drops the rescale of l_a", "*l = a * la + b * lb;", "*l = la + b * lb;", None),
+    ("merge uses a for both sides of O", "o[c] = a * oa[c] + b * ob[c];", "o[c] = a * oa[c] + a * ob[c];", None),
+    ("ring rotates the wrong way", "int j = (r - s) % P;", "int j = (r + s) % P;", None),
+    ("striped positions swapped for contiguous",
+     "if (layout == ORACLE_LAYOUT_STRIPED) return i * (long)P + r;",
+     "if (layout == ORACLE_LAYOUT_STRIPED) return (long)r * n + i;", None),
+    ("lse misses the log", "double l = m + log(sum);", "double l = m + sum;", None),
+    ("finalize does not divide by l", "o[c] = ost[c] / l;", "o[c] = ost[c];", None),
+    ("scores use V instead of K (dense)",
+     "s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);",
+     "s[kk] = scale * dot_q_k(qrow, vb + (size_t)kk * d, d);", 0),
+    ("value rows reversed (dense)", "const uint16_t* vr = vb + (size_t)kk * d;",
+     "const uint16_t* vr = vb + (size_t)(N - 1 - kk) * d;", 0),
+    ("no max subtraction (dense)", "sum += exp(s[kk] - m);\n      double l = m + log(sum);",
+     "sum += exp(s[kk]);\n      double l = log(sum);", None),
+    ("block weight scaled by a constant", "double w = exp(s[kk] - m);\n      l += w;",
+     "double w = 0.5 * exp(s[kk] - m);\n      l += w;", None),
+    ("block partial ignores the mask in the sum",
+     "      if (!allowed(causal, pos_q, kpos[kk])) continue;\n      double w",
+     "      double w", None),
+]
+
+
+def _mutate(src: str, old: str, new: str, which):
+    count = src.count(old)
+    assert count >= 1, f"mutation anchor not found: {old!r}"
+    if which is None:
+        return src.replace(old, new)
+    idx = -1
+    for _ in range(which + 1):
+        idx = src.index(old, idx + 1)
+    return src[:idx] + new + src[idx + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,which", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new, which):
+    src = open(oracle.SOURCE, encoding="utf-8").read()
+    mutated = _mutate(src, old, new, which)
+    assert mutated != src
+    c_path = tmp_path / "mutant.c"
+    c_path.write_text(mutated, encoding="utf-8")
+    so_path = str(tmp_path / "libmutant.so")
+    oracle.build(str(c_path), so_path, force=True)
+    orc = oracle.Oracle(so_path)
+    failures = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError as e:
+            failures.append(f"{pin.__name__}: {str(e)[:80]}")
+    assert failures, f"no pin caught the planted mistake: {name}"
+    print(f"{name}: caught by {len(failures)} pin(s): {failures[0]}")
+    assert os.path.dirname(so_path) != os.path.dirname(oracle.LIBRARY)
