@@ -1,0 +1,364 @@
+"""Benchmark of the ring-attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload striped-128k] [--no-e2e] [--no-cpu-baseline]
+
+One step = one ring_attn_fwd over the whole workload: pack K/V, P ring steps
+(one block-partial kernel each, K/V rotated by device-to-device copies on a
+side stream), finalize fused into the last step.  Default workload: B=1,
+H=16, N=131072, d=128, P=16 striped shards, causal, Q/K/V ~ N(0,1) bf16 with
+1% of key rows scaled by 8 (synthetic, seeded).  Inputs (3 x 0.5 GB) are
+larger than the 129 MB L2, so no flush is needed between steps.
+
+Metric: causal-adjusted attention TFLOP/s = 4 d B H N(N+1)/2 / t (also
+tokens/s and % of bf16 peak).  With --gpus N (torchrun) every rank runs an
+independent replica of the workload (the ring is simulated on one device;
+no data-path collective); the value is the sum over ranks of the work
+divided by the slowest rank's time.
+
+--impl reference times the float64 CPU oracle (dense attention by
+definition) on a bounded sample of query rows of the same workload, on the
+host cores, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal-adjusted attention TFLOP/s and % of GB300 bf16 peak; tokens/s (1 GPU)"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCE = os.path.join(ROOT, "ring_sequence_parallelism_gb300", "csrc", "block_partial.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="striped-128k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(workload: str):
+    """ncu DRAM bytes per launch of the step kernel, if taken on this exact
+    kernel source (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(workload)
+    if not e or e.get("kernel_sha256_16") != source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- oracle leg
+def oracle_sample(w, q, k, v, seconds: float, seed: int = 4242):
+    """Time the float64 oracle on a bounded sample of query rows.  Returns
+    (TFLOP/s, rows per second, threads, description, wall seconds)."""
+    import oracle
+    from ring_sequence_parallelism_gb300.inputs import sample_rows
+
+    orc = oracle.default()
+    BH = w.B * w.H
+    qf, kf, vf = (oracle.bf16_bits(x.reshape(BH, w.N, w.d)) for x in (q, k, v))
+    rows_per_head = 2
+    t_used = 0.0
+    flops = 0
+    while True:
+        rows = sample_rows(w.N, rows_per_head, seed=seed).numpy()
+        t0 = time.perf_counter()
+        orc.dense(qf, kf, vf, w.causal, rows=rows)
+        t_used = time.perf_counter() - t0
+        keys = (rows + 1).sum() if w.causal else rows.size * w.N
+        flops = 4 * w.d * BH * int(keys)
+        if t_used >= seconds / 4 or rows_per_head >= w.N:
+            break
+        rows_per_head = min(w.N, max(rows_per_head * 2, int(rows_per_head * seconds / max(t_used, 1e-3) / 2)))
+    desc = (f"{rows_per_head} seeded query rows per head x {BH} heads of {w.name} "
+            f"({rows_per_head * BH} rows, {flops / 1e9:.1f} GFLOP, dense oracle, float64)")
+    return flops / t_used / 1e12, rows_per_head * BH / t_used, orc.threads(), desc, t_used, rows_per_head
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    from ring_sequence_parallelism_gb300.inputs import make_workload
+
+    q, k, v = make_workload(w)
+    per_step_seconds = max(1.0, min(20.0, 90.0 / max(1, args.steps + args.warmup)))
+    # calibrate the sample once, then time W + K steps of that sample
+    _, _, threads, desc, _, rph = oracle_sample(w, q, k, v, per_step_seconds)
+    import oracle
+    from ring_sequence_parallelism_gb300.inputs import sample_rows
+
+    orc = oracle.default()
+    BH = w.B * w.H
+    qf, kf, vf = (oracle.bf16_bits(x.reshape(BH, w.N, w.d)) for x in (q, k, v))
+    times, flops = [], 0
+    for i in range(args.warmup + args.steps):
+        rows = sample_rows(w.N, rph, seed=5000 + i).numpy()
+        keys = (rows + 1).sum() if w.causal else rows.size * w.N
+        t0 = time.perf_counter()
+        orc.dense(qf, kf, vf, w.causal, rows=rows)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            flops += 4 * w.d * BH * int(keys)
+    total = sum(times)
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc + "; each step a fresh row sample of that size"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    del torch
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "P": w.P, "layout": w.layout,
+            "causal": w.causal, "global_batch": w.B, "seq_len": w.N,
+            "inputs": "Q,K,V ~ N(0,1) rounded to bf16" + (", 1% of key rows x8" if w.key_boost_frac else ""),
+            "l2": l2_note(w)}
+
+
+def l2_note(w):
+    gb = w.B * w.H * w.N * w.d * 2 / 1e9
+    if gb * 1e3 > 129:
+        return "inputs (3 x %.2f GB bf16) larger than the 129 MB L2; no flush" % gb
+    return "inputs (3 x %.1f MB bf16) fit in L2: small case, not a timed workload" % (gb * 1e3)
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import ring_sequence_parallelism_gb300 as ra
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from ring_sequence_parallelism_gb300.inputs import make_workload
+
+    q_h, k_h, v_h = make_workload(w, pin=True)
+    q, k, v = (x.to("cuda", non_blocking=True) for x in (q_h, k_h, v_h))
+    torch.cuda.synchronize()
+    att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout)
+    out = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+    att.set_option(ra.RING_OPT_TIMING, 1)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        att.fwd(q, k, v, out, lse)
+    att.check()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: K forwards, inputs resident in HBM
+    kernel_ms, copy_ms, wait_ms, pack_ms = [], [], [], []
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            att.fwd(q, k, v, out, lse)
+        e1.record(stream)
+        barrier()
+    t = att.timing()  # events of the last forward in the timed region (launch stream)
+    kernel_ms, copy_ms, wait_ms, pack_ms = t["kernel_ms"], t["copy_ms"], t["wait_ms"], t["pack_ms"]
+    att.check()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_t = torch.tensor([ms], device="cuda")
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+
+    flops = w.flops()
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    tokens_s = world * w.B * w.N / (ms_max * 1e-3)
+    pk, pk_kind = peaks()
+
+    # ---- roofline of the dominant kernel (the block-partial step kernel)
+    step_flops = [4 * w.d * att.step_work(s)[0] for s in range(w.P)]
+    k_total_ms = sum(kernel_ms)
+    achieved = sum(step_flops) / (k_total_ms * 1e-3) / 1e12
+    peak_sus = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    traffic = traffic_for(w.name)
+
+    # ---- end to end through the public API, host buffers, copies in the timed region
+    e2e = None
+    if not args.no_e2e:
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        att.set_option(ra.RING_OPT_TIMING, 0)
+        att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
+        f1.record(stream)
+        barrier()
+        e2e_ms = f0.elapsed_time(f1) / args.steps
+        et = torch.tensor([e2e_ms], device="cuda")
+        if world > 1:
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * flops / (float(et.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": float(et.item()),
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h)),
+               "d2h_bytes_per_step": out_h.numel() * 4 + lse_h.numel() * 4}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, rows_s, threads, desc, secs, _ = oracle_sample(w, q_h, k_h, v_h, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "rows_per_s": rows_s, "seconds": secs}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+            "tokens_per_s": tokens_s,
+            "pct_of_bf16_peak": {"sustained": 100 * value / world / peak_sus, "burst": 100 * value / world / peak_burst,
+                                 "nominal_2250": 100 * value / world / 2250.0, "source": pk_kind},
+            "roofline": {"bound": "tensor", "kernel": "block_partial_kernel<128> (one launch per ring step)",
+                         "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                         "frac": achieved / peak_sus, "peak_kind": f"bf16_tflops_sustained ({pk_kind})",
+                         "frac_of_burst": achieved / peak_burst, "traffic": traffic,
+                         "launches_per_step": w.P, "avg_launch_ms": k_total_ms / w.P},
+            "ring": {"step_kernel_ms": kernel_ms, "rotation_copy_ms": copy_ms, "exposed_wait_ms": wait_ms,
+                     "pack_ms": pack_ms, "exposed_wait_total_ms": sum(wait_ms),
+                     "rotation_bytes_per_copy": 2 * w.B * w.H * w.N * w.d * 2},
+            "clocks": clocks.summary(),
+            "gpu_launches": args.steps * (1 + w.P),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    att.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from ring_sequence_parallelism_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

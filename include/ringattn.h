@@ -1,0 +1,201 @@
+/*
+ * ringattn.h -- C ABI of the GB300 (sm_103a) ring-attention library.
+ *
+ * The library runs the data-parallel hot path of ring attention on one GPU:
+ * the sequence of N tokens is split into P virtual shards; shard r keeps its
+ * queries resident while the K/V blocks travel around a ring, and step s pairs
+ * Q_r with block j = (r - s) mod P under the step's causal mask.  Each block
+ * contributes a per-row online-softmax state (m, l, O~) that is merged exactly.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [GRA]   "GPU Ring Attention" (aicassindra.com)
+ *   [ZQ]    ring-attention explainer page (zenaique.com)
+ *   [RA-CN] "Ring Attention：把超长序列沿设备环流动" (charlestar.github.io)
+ *
+ * Conventions for every call:
+ *   - Every function returns a ring_status_t; RING_OK is 0, errors are < 0.
+ *     No exception crosses the ABI.  ring_attn_last_error() gives a message
+ *     for the calling thread's last failure.
+ *   - Tensor pointers are DEVICE pointers to caller-owned memory, dense
+ *     row-major, 16-byte aligned.  bf16 tensors are passed as const void*.
+ *     The library never frees caller memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Launches are asynchronous on it; a device-side bounded wait
+ *     that runs out sets an error word that ring_attn_check() reports as
+ *     RING_ERR_TIMEOUT.
+ *   - Shapes: B batch, H heads, N tokens, d head dim (64 or 128), P shards
+ *     (N % P == 0), n = N / P.  "Natural order" tensors are [B][H][N][d]
+ *     (or [B][H][N] for per-row scalars) indexed by global token position.
+ *     "Shard-major" tensors of one shard are [B][H][n][d] (or [B][H][n])
+ *     indexed by local row i.
+ *   - Global position of local row i of shard r ([RA-CN] "位置编码必须使用全局位置";
+ *     the striped map sends token t to shard t mod P):
+ *       contiguous: pos(r, i) = r*n + i        striped: pos(r, i) = i*P + r
+ *   - Scores are s = (q . k) / sqrt(d); lse is the natural log of the sum of
+ *     exp(s) over the row's allowed keys; causal allows key pos <= query pos.
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define RINGATTN_API __attribute__((visibility("default")))
+#else
+#define RINGATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ring_attn* ring_attn_t; /* opaque handle */
+
+typedef enum {
+  RING_OK = 0,
+  RING_ERR_INVALID_ARG = -1, /* bad pointer, shape, index or alignment */
+  RING_ERR_UNSUPPORTED = -2, /* valid request the library does not implement */
+  RING_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+  RING_ERR_TIMEOUT = -4,     /* a device-side bounded wait ran out */
+  RING_ERR_OOM = -5          /* host allocation failed */
+} ring_status_t;
+
+typedef enum { RING_LAYOUT_CONTIGUOUS = 0, RING_LAYOUT_STRIPED = 1 } ring_layout_t;
+
+/* Class of the (query shard r, K/V block j) pair under the mask
+ * ([RA-CN] "Causal Attention 让环不再完全对称": skip a strictly-future block,
+ * mask a block crossing the diagonal, run the rest unmasked). */
+typedef enum { RING_BLOCK_SKIP = 0, RING_BLOCK_FULL = 1, RING_BLOCK_DIAG = 2 } ring_block_class_t;
+
+/* Per-row online-softmax state of one shard ([RA-CN] "局部 Softmax 为什么不能直接相加":
+ * running max m, exp-sum l scaled by exp(-m), unnormalised value sum O~).
+ * Device pointers, fp32, shard-major: m[B][H][n], l[B][H][n], o[B][H][n][d].
+ * An empty row is (m = -inf, l = 0, O~ = 0).  m is a reference point: any
+ * m with l and O~ scaled by exp(-m) describes the same state; m + ln(l) and
+ * O~ / l are unique. */
+typedef struct {
+  float* m;
+  float* l;
+  float* o;
+} ring_state_t;
+
+/* Options for ring_attn_set_option. */
+typedef enum {
+  /* 1 (default): ring_attn_fwd rotates K/V through the double buffer with
+   * device-to-device copies on a side stream.  0: every step reads its block
+   * straight from the packed buffer (no copies; for measuring their cost). */
+  RING_OPT_ROTATION = 0,
+  /* 1: record CUDA events around every pack, copy and step kernel of
+   * ring_attn_fwd so ring_attn_get_timing can report them.  Default 0. */
+  RING_OPT_TIMING = 1,
+  /* Upper bound, in nanoseconds, of every device-side wait.  Default 2e9. */
+  RING_OPT_WAIT_LIMIT_NS = 2
+} ring_option_t;
+
+/* Create a handle for one problem shape.  Validates the shape and builds the
+ * host plan (per step, per shard: block, class, diagonal offset, work
+ * counts).  Touches no GPU; device resources are made on first use.
+ * Errors: RING_ERR_INVALID_ARG for out == NULL or a non-positive size,
+ * causal not 0/1, layout not a ring_layout_t, P > N;
+ * RING_ERR_UNSUPPORTED for N % P != 0 or d not in {64, 128}. */
+RINGATTN_API int ring_attn_create(ring_attn_t* out, int B, int H, long long N, int d, int P, int causal, int layout);
+
+/* Release a handle (its events, side stream and plan memory).  Waits for no
+ * stream; the caller must not destroy a handle with launches in flight.
+ * NULL is accepted. */
+RINGATTN_API int ring_attn_destroy(ring_attn_t h);
+
+/* Message for the calling thread's last failed call ("" if none). */
+RINGATTN_API const char* ring_attn_last_error(void);
+
+/* Bytes of device workspace ring_attn_fwd needs: the two K/V rotation
+ * buffers A and B, each [P][B][H][n][d] bf16 for K and for V ([RA-CN]
+ * "双缓冲是重叠成立的基础": buffer A read by compute while B receives), plus
+ * the running l state [B][H][N] fp32.  256-byte aligned by the caller. */
+RINGATTN_API int ring_attn_workspace_size(ring_attn_t h, size_t* bytes);
+
+/* ---------------------------------------------------------------- planner
+ * Host-only queries of the plan (no GPU needed). */
+
+/* Block held by shard r at ring step s, j = (r - s) mod P ([GRA] "One lap
+ * around the ring"; [RA-CN] "环是怎样工作的"), its class and its diagonal
+ * offset delta: within the block a (row i, column k) pair is allowed iff
+ * k - i <= delta (contiguous delta = (r - j) n; striped delta = 0 if j <= r
+ * else -1; non-causal FULL).  Any output pointer may be NULL. */
+RINGATTN_API int ring_attn_plan_block(ring_attn_t h, int r, int step, int* j, int* cls, long long* delta);
+
+/* Per-shard totals over all P steps: allowed (q, k) pairs[P] and the
+ * 128x128 MMA tiles the kernel computes[P] (any pointer may be NULL). */
+RINGATTN_API int ring_attn_shard_work(ring_attn_t h, long long* pairs, long long* tiles);
+
+/* Totals of one step over all shards: allowed pairs and computed tiles. */
+RINGATTN_API int ring_attn_step_work(ring_attn_t h, int step, long long* pairs, long long* tiles);
+
+/* ---------------------------------------------------------------- state */
+
+/* Set a shard's state to empty: m = -inf, l = 0, O~ = 0 (the pages'
+ * empty_online_softmax_state, [RA-CN] "环是怎样工作的"). */
+RINGATTN_API int ring_attn_state_init(ring_attn_t h, ring_state_t s, void* stream);
+
+/* Block partial of ring step `step` for shard r ([RA-CN] "环是怎样工作的":
+ * block_attention(local_q, kv, mask_for(step)); "两层分块如何嵌套": the kernel
+ * can emit a mergeable state or update the local running buffer).
+ *   q_shard  shard r's queries, shard-major [B][H][n][d] bf16
+ *   k_block, v_block  block j = (r - step) mod P, shard-major [B][H][n][d] bf16
+ *   state    shard r's state (see ring_state_t)
+ *   accumulate  0: overwrite `state` with this block's partial state
+ *               1: merge this block into `state` (exact rescale merge)
+ * The mask uses global positions of shard r's rows and block j's keys.  A
+ * SKIP block leaves `state` unchanged (accumulate 1) or writes the empty
+ * state (accumulate 0).  All pointers 16-byte aligned. */
+RINGATTN_API int ring_attn_block_partial(ring_attn_t h, int r, int step, const void* q_shard, const void* k_block,
+                            const void* v_block, ring_state_t state, int accumulate, void* stream);
+
+/* a <- merge(a, b) over one shard's B*H*n rows ([GRA] "Why partial results
+ * are allowed to merge"; [ZQ]: rescale by exp(old_max - new_max)):
+ *   m = max(ma, mb); alpha = exp(ma - m), beta = exp(mb - m) (0 for an
+ *   m = -inf side); l = alpha la + beta lb; O~ = alpha O~a + beta O~b.
+ * a and b must not overlap. */
+RINGATTN_API int ring_attn_merge(ring_attn_t h, ring_state_t a, ring_state_t b, void* stream);
+
+/* Finalize shard r's state into natural-order outputs ([RA-CN] "环是怎样工作的":
+ * local_output = finalize(state)): out[b][h][pos(r,i)][:] = O~ / l and
+ * lse[b][h][pos(r,i)] = m + ln(l); an empty row gives out = 0, lse = -inf.
+ *   out  [B][H][N][d] fp32, lse [B][H][N] fp32 (only shard r's rows written) */
+RINGATTN_API int ring_attn_finalize(ring_attn_t h, int r, ring_state_t s, float* out, float* lse, void* stream);
+
+/* Whole ring forward on one device ([RA-CN] "环是怎样工作的" forward loop;
+ * "双缓冲是重叠成立的基础" double buffering):
+ *   q, k, v   natural order [B][H][N][d] bf16
+ *   out       natural order [B][H][N][d] fp32 (also holds O~ between steps)
+ *   lse       natural order [B][H][N]   fp32 (also holds m between steps)
+ *   workspace ring_attn_workspace_size() bytes, 256-byte aligned
+ * K/V are packed shard-major into buffer A; step s runs one kernel over every
+ * shard's block (r - s) mod P, reading slot r of the current buffer, while a
+ * side stream copies the rotated blocks into the other buffer for step s+1
+ * (slot r <- slot r-1), ordered with events.  The last step writes the
+ * normalised output and lse.  Returns after enqueueing; `stream` orders it
+ * with the caller's work. */
+RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
+                  void* workspace, void* stream);
+
+/* Set an option (see ring_option_t). */
+RINGATTN_API int ring_attn_set_option(ring_attn_t h, int option, long long value);
+
+/* Timings of the last ring_attn_fwd with RING_OPT_TIMING on, in ms; each
+ * array has P entries (NULL to skip): step kernel time, rotation copy time
+ * for the copy that feeds step s (0 for s = 0), and the time the compute
+ * stream waited for that copy (exposed copy time).  pack_ms: the packing
+ * kernel.  Synchronises on the recorded events. */
+RINGATTN_API int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float* wait_ms, float* pack_ms);
+
+/* Synchronise `stream` and report any device-side error recorded by this
+ * handle's kernels since the last check (RING_ERR_TIMEOUT for a wait that
+ * ran out), clearing it. */
+RINGATTN_API int ring_attn_check(ring_attn_t h, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGATTN_H */

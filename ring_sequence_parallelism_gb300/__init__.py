@@ -1,0 +1,204 @@
+"""Ring attention on one GB300: Python face of the C ABI in include/ringattn.h.
+
+The functions below carry the C names and only marshal arguments (torch
+tensors -> device pointers, the current torch stream -> cudaStream_t);
+every step runs in libringattn.so.  PyTorch provides device memory and
+streams.
+
+    ra = RingAttention(B, H, N, d, P, causal=True, layout="striped")
+    out, lse = ra.fwd(q, k, v)          # q, k, v: cuda bf16 [B, H, N, d]
+
+Layouts: "contiguous" (shard r holds tokens r*n .. r*n+n-1) or "striped"
+(token t goes to shard t mod P).
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import (RING_BLOCK_DIAG, RING_BLOCK_FULL, RING_BLOCK_SKIP, RING_LAYOUT_CONTIGUOUS,  # noqa: F401
+                   RING_LAYOUT_STRIPED, RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_WAIT_LIMIT_NS,
+                   RingAttnError, RingState)
+
+LAYOUTS = {"contiguous": RING_LAYOUT_CONTIGUOUS, "striped": RING_LAYOUT_STRIPED}
+
+
+def _layout_id(layout) -> int:
+    return LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _state(st) -> RingState:
+    m, l, o = st
+    return RingState(_ptr(m), _ptr(l), _ptr(o))
+
+
+# ------------------------------------------------------- C-named wrappers
+def ring_attn_create(B: int, H: int, N: int, d: int, P: int, causal: bool, layout) -> int:
+    lib = _lib.load()
+    h = ctypes.c_void_p()
+    _lib.check(lib.ring_attn_create(ctypes.byref(h), B, H, N, d, P, int(bool(causal)), _layout_id(layout)))
+    return h.value
+
+
+def ring_attn_destroy(h: int) -> None:
+    _lib.check(_lib.load().ring_attn_destroy(h))
+
+
+def ring_attn_block_partial(h, r, step, q_shard, k_block, v_block, state, accumulate, stream=None):
+    _lib.check(_lib.load().ring_attn_block_partial(h, r, step, _ptr(q_shard), _ptr(k_block), _ptr(v_block),
+                                                   _state(state), int(accumulate), _stream(stream)))
+
+
+def ring_attn_merge(h, state_a, state_b, stream=None):
+    _lib.check(_lib.load().ring_attn_merge(h, _state(state_a), _state(state_b), _stream(stream)))
+
+
+def ring_attn_finalize(h, r, state, out, lse, stream=None):
+    _lib.check(_lib.load().ring_attn_finalize(h, r, _state(state), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def ring_attn_state_init(h, state, stream=None):
+    _lib.check(_lib.load().ring_attn_state_init(h, _state(state), _stream(stream)))
+
+
+def ring_attn_fwd(h, q, k, v, out, lse, workspace, stream=None):
+    _lib.check(_lib.load().ring_attn_fwd(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
+                                         _stream(stream)))
+
+
+def ring_attn_check(h, stream=None):
+    _lib.check(_lib.load().ring_attn_check(h, _stream(stream)))
+
+
+# ------------------------------------------------------------ the object
+class RingAttention:
+    """One problem shape: plan, workspace and the calls of the C ABI."""
+
+    def __init__(self, B: int, H: int, N: int, d: int, P: int, causal: bool = True, layout="striped"):
+        self.B, self.H, self.N, self.d, self.P = B, H, N, d, P
+        self.causal = bool(causal)
+        self.layout = _layout_id(layout)
+        self.n = N // P
+        self.handle = ring_attn_create(B, H, N, d, P, causal, self.layout)
+        self._lib = _lib.load()
+        self._workspace = None
+
+    def close(self):
+        if self.handle:
+            ring_attn_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- planner (host only) -------------------------------------------
+    def plan_block(self, r: int, step: int):
+        j, cls, delta = ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
+        _lib.check(self._lib.ring_attn_plan_block(self.handle, r, step, ctypes.byref(j), ctypes.byref(cls),
+                                                  ctypes.byref(delta)))
+        return j.value, cls.value, delta.value
+
+    def shard_work(self):
+        pairs = (ctypes.c_longlong * self.P)()
+        tiles = (ctypes.c_longlong * self.P)()
+        _lib.check(self._lib.ring_attn_shard_work(self.handle, pairs, tiles))
+        return list(pairs), list(tiles)
+
+    def step_work(self, step: int):
+        pairs, tiles = ctypes.c_longlong(), ctypes.c_longlong()
+        _lib.check(self._lib.ring_attn_step_work(self.handle, step, ctypes.byref(pairs), ctypes.byref(tiles)))
+        return pairs.value, tiles.value
+
+    def workspace_size(self) -> int:
+        n = ctypes.c_size_t()
+        _lib.check(self._lib.ring_attn_workspace_size(self.handle, ctypes.byref(n)))
+        return n.value
+
+    def set_option(self, option: int, value: int):
+        _lib.check(self._lib.ring_attn_set_option(self.handle, option, int(value)))
+
+    # -- device calls ---------------------------------------------------
+    def workspace(self, device=None):
+        import torch
+
+        need = self.workspace_size()
+        if self._workspace is None or self._workspace.numel() < need:
+            self._workspace = torch.empty(need, dtype=torch.uint8, device=device or "cuda")
+        return self._workspace
+
+    def new_state(self, device=None):
+        import torch
+
+        dev = device or "cuda"
+        rows = (self.B, self.H, self.n)
+        return (torch.empty(rows, dtype=torch.float32, device=dev), torch.empty(rows, dtype=torch.float32, device=dev),
+                torch.empty(rows + (self.d,), dtype=torch.float32, device=dev))
+
+    def state_init(self, state, stream=None):
+        ring_attn_state_init(self.handle, state, stream)
+
+    def block_partial(self, r, step, q_shard, k_block, v_block, state, accumulate, stream=None):
+        ring_attn_block_partial(self.handle, r, step, q_shard, k_block, v_block, state, accumulate, stream)
+
+    def merge(self, state_a, state_b, stream=None):
+        ring_attn_merge(self.handle, state_a, state_b, stream)
+
+    def finalize(self, r, state, out, lse, stream=None):
+        ring_attn_finalize(self.handle, r, state, out, lse, stream)
+
+    def fwd(self, q, k, v, out=None, lse=None, stream=None):
+        import torch
+
+        for t in (q, k, v):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("q, k, v must be contiguous CUDA bfloat16 tensors [B, H, N, d]")
+            if tuple(t.shape) != (self.B, self.H, self.N, self.d):
+                raise ValueError(f"expected shape {(self.B, self.H, self.N, self.d)}, got {tuple(t.shape)}")
+        if out is None:
+            out = torch.empty((self.B, self.H, self.N, self.d), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((self.B, self.H, self.N), dtype=torch.float32, device=q.device)
+        ring_attn_fwd(self.handle, q, k, v, out, lse, self.workspace(q.device), stream)
+        return out, lse
+
+    def fwd_host(self, q_host, k_host, v_host, out_host=None, lse_host=None, stream=None):
+        """End-to-end call from host memory: copy pinned q, k, v to the device,
+        run the ring forward, copy out and lse back (the step's result)."""
+        import torch
+
+        q = q_host.to("cuda", non_blocking=True)
+        k = k_host.to("cuda", non_blocking=True)
+        v = v_host.to("cuda", non_blocking=True)
+        out, lse = self.fwd(q, k, v, stream=stream)
+        if out_host is None:
+            out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        if lse_host is None:
+            lse_host = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        out_host.copy_(out, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+        return out_host, lse_host
+
+    def timing(self):
+        P = self.P
+        k, c, w = (ctypes.c_float * P)(), (ctypes.c_float * P)(), (ctypes.c_float * P)()
+        pk = ctypes.c_float()
+        _lib.check(self._lib.ring_attn_get_timing(self.handle, k, c, w, ctypes.byref(pk)))
+        return {"kernel_ms": list(k), "copy_ms": list(c), "wait_ms": list(w), "pack_ms": pk.value}
+
+    def check(self, stream=None):
+        ring_attn_check(self.handle, stream)

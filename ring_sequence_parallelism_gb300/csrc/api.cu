@@ -1,0 +1,502 @@
+// api.cu -- the C ABI (include/ringattn.h): handle, argument checks, TMA
+// tensor maps and the P-step ring scheduler with the double-buffered K/V
+// rotation on a side stream.
+//
+// Ring forward on one device ([RA-CN] "环是怎样工作的" forward loop;
+// "双缓冲是重叠成立的基础": buffer A is read by the attention kernel while
+// buffer B receives the next block, roles swap, streams and events order the
+// two; [GRA] "Hiding the ring behind the GEMMs"):
+//
+//   compute stream: pack K,V -> X          record packed
+//   side stream:    wait packed;      Y <- rotate(X);   record landed[1]
+//   compute stream: step 0 on X;                        record released[0]
+//   side stream:    wait released[0]; X <- rotate(Y);   record landed[2]
+//   compute stream: wait landed[1]; step 1 on Y;        record released[1]
+//   ...
+// rotate(src): dst slot r <- src slot (r - 1) mod P, i.e. every shard sends
+// its block to shard r + 1 and receives from r - 1 ([GRA] "One lap around
+// the ring"), as two cudaMemcpyAsync device-to-device copies per tensor.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "internal.h"
+
+using namespace ringattn;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  std::string msg = std::string(what) + ": " + cudaGetErrorString(e);
+  cudaGetLastError();  // clear a sticky launch error where possible
+  return fail(RING_ERR_CUDA, msg);
+}
+
+#define RA_CUDA(call, what)                     \
+  do {                                          \
+    cudaError_t _e = (call);                    \
+    if (_e != cudaSuccess) return cuda_fail(_e, what); \
+  } while (0)
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder() {
+  if (g_encode) return RING_OK;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  void* fn = nullptr;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return fail(RING_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled from the driver");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return RING_OK;
+}
+
+// 4-D bf16 tensor map, box (64, b1, b2, 1), 128-byte swizzle, zero fill out
+// of bounds.  dims/strides are innermost first; strides in bytes for dims 1..3.
+int encode_map(CUtensorMap* map, const void* base, const cuuint64_t dims[4], const cuuint64_t strides[3],
+               cuuint32_t b1, cuuint32_t b2) {
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
+  cuuint32_t box[4] = {64, b1, b2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[128];
+    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return fail(RING_ERR_CUDA, buf);
+  }
+  return RING_OK;
+}
+
+}  // namespace
+
+struct ring_attn {
+  Plan plan;
+  int rotation = 1;
+  int timing = 0;
+  unsigned long long wait_limit_ns = 2000000000ULL;
+  // device resources, made on first use
+  bool ready = false;
+  int device = -1;
+  cudaStream_t side = nullptr;
+  cudaEvent_t packed = nullptr;
+  std::vector<cudaEvent_t> landed, released;
+  std::vector<cudaEvent_t> tk0, tk1, tc0, tc1, tw0, tw1;
+  cudaEvent_t tp0 = nullptr, tp1 = nullptr;
+  bool timed_valid = false;
+  int* d_err = nullptr;  // [0] flags, [1] first failing site
+};
+
+namespace {
+
+int make_events(std::vector<cudaEvent_t>& v, int n, unsigned flags) {
+  v.assign(n, nullptr);
+  for (int i = 0; i < n; ++i) RA_CUDA(cudaEventCreateWithFlags(&v[i], flags), "cudaEventCreate");
+  return RING_OK;
+}
+
+int ensure_device(ring_attn* h) {
+  int dev = -1;
+  RA_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (h->ready) {
+    if (dev != h->device) return fail(RING_ERR_INVALID_ARG, "handle used on a different device than its first use");
+    return RING_OK;
+  }
+  int major = 0, minor = 0;
+  RA_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cudaDeviceGetAttribute");
+  RA_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3) {
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "this library is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+    return fail(RING_ERR_UNSUPPORTED, buf);
+  }
+  int rc = get_encoder();
+  if (rc) return rc;
+  RA_CUDA((cudaError_t)prepare_block_partial_kernels(), "cudaFuncSetAttribute");
+  RA_CUDA(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking), "cudaStreamCreate");
+  const int P = h->plan.P;
+  RA_CUDA(cudaEventCreateWithFlags(&h->packed, cudaEventDisableTiming), "cudaEventCreate");
+  if ((rc = make_events(h->landed, P, cudaEventDisableTiming))) return rc;
+  if ((rc = make_events(h->released, P, cudaEventDisableTiming))) return rc;
+  for (auto* v : {&h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1})
+    if ((rc = make_events(*v, P, cudaEventDefault))) return rc;
+  RA_CUDA(cudaEventCreate(&h->tp0), "cudaEventCreate");
+  RA_CUDA(cudaEventCreate(&h->tp1), "cudaEventCreate");
+  RA_CUDA(cudaMalloc(&h->d_err, 2 * sizeof(int)), "cudaMalloc(error word)");
+  RA_CUDA(cudaMemset(h->d_err, 0, 2 * sizeof(int)), "cudaMemset");
+  h->device = dev;
+  h->ready = true;
+  return RING_OK;
+}
+
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+StepArgs base_args(const ring_attn* h) {
+  StepArgs a;
+  std::memset(&a, 0, sizeof a);
+  const Plan& p = h->plan;
+  a.err = h->d_err;
+  a.wait_limit_ns = h->wait_limit_ns;
+  a.n = (int)p.n;
+  a.P = p.P;
+  a.BH = p.B * p.H;
+  a.T = p.T;
+  a.KT = p.KT;
+  a.causal = p.causal;
+  a.layout = p.layout;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
+  a.fixed_r = -1;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ring_attn_last_error(void) { return g_last_error.c_str(); }
+
+int ring_attn_create(ring_attn_t* out, int B, int H, long long N, int d, int P, int causal, int layout) {
+  if (!out) return fail(RING_ERR_INVALID_ARG, "out handle pointer is NULL");
+  *out = nullptr;
+  ring_attn* h = new (std::nothrow) ring_attn();
+  if (!h) return fail(RING_ERR_OOM, "out of host memory");
+  std::string err;
+  int rc = build_plan(&h->plan, B, H, N, d, P, causal, layout, &err);
+  if (rc != RING_OK) {
+    delete h;
+    return fail(rc, err);
+  }
+  *out = h;
+  g_last_error.clear();
+  return RING_OK;
+}
+
+int ring_attn_destroy(ring_attn_t h) {
+  if (!h) return RING_OK;
+  if (h->ready) {
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != h->device) cudaSetDevice(h->device);
+    for (auto* v : {&h->landed, &h->released, &h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1})
+      for (auto e : *v)
+        if (e) cudaEventDestroy(e);
+    if (h->packed) cudaEventDestroy(h->packed);
+    if (h->tp0) cudaEventDestroy(h->tp0);
+    if (h->tp1) cudaEventDestroy(h->tp1);
+    if (h->side) cudaStreamDestroy(h->side);
+    if (h->d_err) cudaFree(h->d_err);
+    if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
+  }
+  delete h;
+  return RING_OK;
+}
+
+int ring_attn_workspace_size(ring_attn_t h, size_t* bytes) {
+  if (!h || !bytes) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  const Plan& p = h->plan;
+  const size_t elems = (size_t)p.B * p.H * (size_t)p.N * p.d;
+  const size_t rot = 4 * elems * 2;                      // X and Y, each K and V, bf16
+  const size_t lstate = (size_t)p.B * p.H * (size_t)p.N * 4;  // l rows
+  *bytes = rot + ((lstate + 255) / 256) * 256;
+  return RING_OK;
+}
+
+int ring_attn_plan_block(ring_attn_t h, int r, int step, int* j, int* cls, long long* delta) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  const Plan& p = h->plan;
+  if (r < 0 || r >= p.P || step < 0 || step >= p.P) return fail(RING_ERR_INVALID_ARG, "r or step out of range");
+  const BlockPlan& b = p.at(step, r);
+  if (j) *j = b.j;
+  if (cls) *cls = b.cls;
+  if (delta) *delta = b.delta;
+  return RING_OK;
+}
+
+int ring_attn_shard_work(ring_attn_t h, long long* pairs, long long* tiles) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  for (int r = 0; r < h->plan.P; ++r) {
+    if (pairs) pairs[r] = h->plan.shard_pairs[r];
+    if (tiles) tiles[r] = h->plan.shard_tiles[r];
+  }
+  return RING_OK;
+}
+
+int ring_attn_step_work(ring_attn_t h, int step, long long* pairs, long long* tiles) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  if (step < 0 || step >= h->plan.P) return fail(RING_ERR_INVALID_ARG, "step out of range");
+  if (pairs) *pairs = h->plan.step_pairs[step];
+  if (tiles) *tiles = h->plan.step_tiles[step];
+  return RING_OK;
+}
+
+int ring_attn_set_option(ring_attn_t h, int option, long long value) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  switch (option) {
+    case RING_OPT_ROTATION:
+      if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "rotation must be 0 or 1");
+      h->rotation = (int)value;
+      return RING_OK;
+    case RING_OPT_TIMING:
+      if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "timing must be 0 or 1");
+      h->timing = (int)value;
+      return RING_OK;
+    case RING_OPT_WAIT_LIMIT_NS:
+      if (value <= 0) return fail(RING_ERR_INVALID_ARG, "wait limit must be positive");
+      h->wait_limit_ns = (unsigned long long)value;
+      return RING_OK;
+    default:
+      return fail(RING_ERR_INVALID_ARG, "unknown option");
+  }
+}
+
+int ring_attn_state_init(ring_attn_t h, ring_state_t s, void* stream) {
+  if (!h || !s.m || !s.l || !s.o) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(s.o)) return fail(RING_ERR_INVALID_ARG, "state.o not 16-byte aligned");
+  int rc = ensure_device(h);
+  if (rc) return rc;
+  const Plan& p = h->plan;
+  RA_CUDA((cudaError_t)launch_state_init(s.m, s.l, s.o, (long long)p.B * p.H * p.n, p.d, stream),
+          "state_init launch");
+  return RING_OK;
+}
+
+int ring_attn_merge(ring_attn_t h, ring_state_t a, ring_state_t b, void* stream) {
+  if (!h || !a.m || !a.l || !a.o || !b.m || !b.l || !b.o) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(a.o) || !aligned16(b.o)) return fail(RING_ERR_INVALID_ARG, "state.o not 16-byte aligned");
+  int rc = ensure_device(h);
+  if (rc) return rc;
+  const Plan& p = h->plan;
+  RA_CUDA((cudaError_t)launch_merge(a.m, a.l, a.o, b.m, b.l, b.o, (long long)p.B * p.H * p.n, p.d, stream),
+          "merge launch");
+  return RING_OK;
+}
+
+int ring_attn_finalize(ring_attn_t h, int r, ring_state_t s, float* out, float* lse, void* stream) {
+  if (!h || !s.m || !s.l || !s.o || !out || !lse) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  const Plan& p = h->plan;
+  if (r < 0 || r >= p.P) return fail(RING_ERR_INVALID_ARG, "r out of range");
+  if (!aligned16(s.o) || !aligned16(out)) return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
+  int rc = ensure_device(h);
+  if (rc) return rc;
+  RA_CUDA((cudaError_t)launch_finalize(s.m, s.l, s.o, out, lse, p.B * p.H, p.n, p.d, p.P, r, p.layout, p.N, stream),
+          "finalize launch");
+  return RING_OK;
+}
+
+int ring_attn_block_partial(ring_attn_t h, int r, int step, const void* q_shard, const void* k_block,
+                            const void* v_block, ring_state_t state, int accumulate, void* stream) {
+  if (!h || !q_shard || !k_block || !v_block || !state.m || !state.l || !state.o)
+    return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  const Plan& p = h->plan;
+  if (r < 0 || r >= p.P || step < 0 || step >= p.P) return fail(RING_ERR_INVALID_ARG, "r or step out of range");
+  if (accumulate != 0 && accumulate != 1) return fail(RING_ERR_INVALID_ARG, "accumulate must be 0 or 1");
+  if (!aligned16(q_shard) || !aligned16(k_block) || !aligned16(v_block) || !aligned16(state.o))
+    return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
+  int rc = ensure_device(h);
+  if (rc) return rc;
+  const int BH = p.B * p.H;
+  const BlockPlan& b = p.at(step, r);
+  if (b.cls == RING_BLOCK_SKIP && accumulate) return RING_OK;  // nothing to merge
+  CUtensorMap qm, km, vm;
+  const cuuint64_t d = (cuuint64_t)p.d, n = (cuuint64_t)p.n;
+  const cuuint64_t row_b = d * 2;
+  {
+    cuuint64_t dims[4] = {d, n, 1, (cuuint64_t)BH};
+    cuuint64_t str[3] = {row_b, row_b * n, row_b * n};
+    if ((rc = encode_map(&qm, q_shard, dims, str, kTileM, 1))) return rc;
+  }
+  {
+    cuuint64_t dims[4] = {d, n, (cuuint64_t)BH, 1};
+    cuuint64_t str[3] = {row_b, row_b * n, row_b * n * BH};
+    if ((rc = encode_map(&km, k_block, dims, str, kTileN, 1))) return rc;
+    if ((rc = encode_map(&vm, v_block, dims, str, kTileN, 1))) return rc;
+  }
+  StepArgs a = base_args(h);
+  a.o_state = state.o;
+  a.m_state = state.m;
+  a.l_state = state.l;
+  a.out = nullptr;
+  a.lse = nullptr;
+  a.row_bh = (long long)p.n;
+  a.row_r = 0;
+  a.row_i = 1;
+  a.q_mode = kQShardMajor;
+  a.kv_mode = kKvSingle;
+  a.step = step;
+  a.accumulate = accumulate;
+  a.finalize = 0;
+  a.fixed_r = r;
+  a.n_active = 1;
+  const int grid = p.T * BH;
+  RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km, &vm, p.d, grid, stream), "block_partial launch");
+  return RING_OK;
+}
+
+int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
+                  void* workspace, void* stream) {
+  if (!h || !q || !k || !v || !out || !lse || !workspace) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(RING_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  int rc = ensure_device(h);
+  if (rc) return rc;
+  const Plan& p = h->plan;
+  const int P = p.P, BH = p.B * p.H;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const size_t elems = (size_t)BH * (size_t)p.N * p.d;
+  const size_t tensor_bytes = elems * 2;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* kbuf[2] = {ws, ws + 2 * tensor_bytes};
+  void* vbuf[2] = {ws + tensor_bytes, ws + 3 * tensor_bytes};
+  float* l_state = reinterpret_cast<float*>(ws + 4 * tensor_bytes);
+  const bool rotate = h->rotation && P > 1;
+
+  // tensor maps: Q in natural order (strided per shard), K/V rotation buffers
+  const cuuint64_t d = (cuuint64_t)p.d, n = (cuuint64_t)p.n, row_b = d * 2;
+  CUtensorMap qm, km[2], vm[2];
+  if (p.layout == RING_LAYOUT_STRIPED) {
+    cuuint64_t dims[4] = {d, (cuuint64_t)P, n, (cuuint64_t)BH};
+    cuuint64_t str[3] = {row_b, row_b * P, row_b * (cuuint64_t)p.N};
+    if ((rc = encode_map(&qm, q, dims, str, 1, kTileM))) return rc;
+  } else {
+    cuuint64_t dims[4] = {d, n, (cuuint64_t)P, (cuuint64_t)BH};
+    cuuint64_t str[3] = {row_b, row_b * n, row_b * (cuuint64_t)p.N};
+    if ((rc = encode_map(&qm, q, dims, str, kTileM, 1))) return rc;
+  }
+  for (int x = 0; x < 2; ++x) {
+    cuuint64_t dims[4] = {d, n, (cuuint64_t)BH, (cuuint64_t)P};
+    cuuint64_t str[3] = {row_b, row_b * n, row_b * n * BH};
+    if ((rc = encode_map(&km[x], kbuf[x], dims, str, kTileN, 1))) return rc;
+    if ((rc = encode_map(&vm[x], vbuf[x], dims, str, kTileN, 1))) return rc;
+  }
+
+  const bool timing = h->timing != 0;
+  if (timing) RA_CUDA(cudaEventRecord(h->tp0, cs), "cudaEventRecord");
+  RA_CUDA((cudaError_t)launch_pack_kv(k, v, kbuf[0], vbuf[0], BH, p.n, p.d, P, p.layout, cs), "pack launch");
+  if (timing) RA_CUDA(cudaEventRecord(h->tp1, cs), "cudaEventRecord");
+  if (rotate) RA_CUDA(cudaEventRecord(h->packed, cs), "cudaEventRecord");
+
+  const size_t slot_bytes = (size_t)BH * (size_t)p.n * p.d * 2;
+  StepArgs a = base_args(h);
+  a.o_state = out;   // O~ lives in `out` between steps
+  a.m_state = lse;   // m lives in `lse` between steps
+  a.l_state = l_state;
+  a.out = out;
+  a.lse = lse;
+  a.row_bh = p.N;
+  a.row_r = p.layout == RING_LAYOUT_STRIPED ? 1 : p.n;
+  a.row_i = p.layout == RING_LAYOUT_STRIPED ? P : 1;
+  a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : kQContiguous;
+  a.kv_mode = rotate ? kKvSlotR : kKvSlotJ;
+
+  for (int s = 0; s < P; ++s) {
+    const int cur = rotate ? (s & 1) : 0;
+    if (rotate && s >= 1) {
+      if (timing) RA_CUDA(cudaEventRecord(h->tw0[s], cs), "cudaEventRecord");
+      RA_CUDA(cudaStreamWaitEvent(cs, h->landed[s], 0), "cudaStreamWaitEvent");
+      if (timing) RA_CUDA(cudaEventRecord(h->tw1[s], cs), "cudaEventRecord");
+    }
+    const auto& act = p.active[s];
+    a.step = s;
+    a.accumulate = s > 0 ? 1 : 0;
+    a.finalize = s == P - 1 ? 1 : 0;
+    a.n_active = (int)act.size();
+    for (size_t x = 0; x < act.size(); ++x) a.active[x] = act[x];
+    const int grid = p.T * a.n_active * BH;
+    if (timing) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
+    RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km[cur], &vm[cur], p.d, grid, cs), "step kernel launch");
+    if (timing) RA_CUDA(cudaEventRecord(h->tk1[s], cs), "cudaEventRecord");
+    if (rotate) RA_CUDA(cudaEventRecord(h->released[s], cs), "cudaEventRecord");
+    if (rotate && s + 1 < P) {
+      // fill the other buffer for step s+1 once step s-1 has released it
+      RA_CUDA(cudaStreamWaitEvent(h->side, s == 0 ? h->packed : h->released[s - 1], 0), "cudaStreamWaitEvent");
+      const int nxt = cur ^ 1;
+      if (timing) RA_CUDA(cudaEventRecord(h->tc0[s + 1], h->side), "cudaEventRecord");
+      for (int t = 0; t < 2; ++t) {
+        uint8_t* dst = static_cast<uint8_t*>(t == 0 ? kbuf[nxt] : vbuf[nxt]);
+        const uint8_t* src = static_cast<const uint8_t*>(t == 0 ? kbuf[cur] : vbuf[cur]);
+        RA_CUDA(cudaMemcpyAsync(dst + slot_bytes, src, (size_t)(P - 1) * slot_bytes, cudaMemcpyDeviceToDevice,
+                                h->side),
+                "rotation copy");
+        RA_CUDA(cudaMemcpyAsync(dst, src + (size_t)(P - 1) * slot_bytes, slot_bytes, cudaMemcpyDeviceToDevice,
+                                h->side),
+                "rotation copy");
+      }
+      if (timing) RA_CUDA(cudaEventRecord(h->tc1[s + 1], h->side), "cudaEventRecord");
+      RA_CUDA(cudaEventRecord(h->landed[s + 1], h->side), "cudaEventRecord");
+    }
+  }
+  h->timed_valid = timing;
+  return RING_OK;
+}
+
+int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float* wait_ms, float* pack_ms) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  if (!h->timed_valid) return fail(RING_ERR_INVALID_ARG, "no timed ring_attn_fwd recorded (set RING_OPT_TIMING)");
+  const int P = h->plan.P;
+  const bool rotate = h->rotation && P > 1;
+  for (int s = 0; s < P; ++s) {
+    float ms = 0.f;
+    if (kernel_ms) {
+      RA_CUDA(cudaEventSynchronize(h->tk1[s]), "cudaEventSynchronize");
+      RA_CUDA(cudaEventElapsedTime(&ms, h->tk0[s], h->tk1[s]), "cudaEventElapsedTime");
+      kernel_ms[s] = ms;
+    }
+    if (copy_ms) {
+      ms = 0.f;
+      if (rotate && s >= 1) {
+        RA_CUDA(cudaEventSynchronize(h->tc1[s]), "cudaEventSynchronize");
+        RA_CUDA(cudaEventElapsedTime(&ms, h->tc0[s], h->tc1[s]), "cudaEventElapsedTime");
+      }
+      copy_ms[s] = ms;
+    }
+    if (wait_ms) {
+      ms = 0.f;
+      if (rotate && s >= 1) {
+        RA_CUDA(cudaEventSynchronize(h->tw1[s]), "cudaEventSynchronize");
+        RA_CUDA(cudaEventElapsedTime(&ms, h->tw0[s], h->tw1[s]), "cudaEventElapsedTime");
+      }
+      wait_ms[s] = ms;
+    }
+  }
+  if (pack_ms) {
+    float ms = 0.f;
+    RA_CUDA(cudaEventSynchronize(h->tp1), "cudaEventSynchronize");
+    RA_CUDA(cudaEventElapsedTime(&ms, h->tp0, h->tp1), "cudaEventElapsedTime");
+    *pack_ms = ms;
+  }
+  return RING_OK;
+}
+
+int ring_attn_check(ring_attn_t h, void* stream) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  if (!h->ready) return RING_OK;
+  RA_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
+  RA_CUDA(cudaStreamSynchronize(h->side), "cudaStreamSynchronize");
+  int words[2] = {0, 0};
+  RA_CUDA(cudaMemcpy(words, h->d_err, sizeof words, cudaMemcpyDeviceToHost), "cudaMemcpy(error word)");
+  if (words[0] != 0) {
+    RA_CUDA(cudaMemset(h->d_err, 0, sizeof words), "cudaMemset");
+    char buf[128];
+    std::snprintf(buf, sizeof buf, "device-side wait ran out (flags 0x%x, site %d)", words[0], words[1]);
+    return fail(RING_ERR_TIMEOUT, buf);
+  }
+  return RING_OK;
+}
+
+}  // extern "C"

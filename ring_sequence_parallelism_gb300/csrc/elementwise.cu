@@ -1,0 +1,180 @@
+// elementwise.cu -- HBM-bound kernels of the ring: empty state, the exact
+// merge of two states, finalize into natural order, and the shard-major
+// packing of K/V into the rotation buffer.
+//
+// All of them move 16-byte vectors with consecutive threads on consecutive
+// addresses; the per-row scalars (m, l) are read by the threads of one row
+// at the same address, which the memory system broadcasts.  Grids are a
+// multiple of the SM count with grid-stride loops.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace ringattn {
+namespace {
+
+int g_sm_count = 0;
+
+int grid_for(long long work, int threads) {
+  if (g_sm_count == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || g_sm_count <= 0)
+      g_sm_count = 1;
+  }
+  long long blocks = (work + threads - 1) / threads;
+  long long cap = (long long)g_sm_count * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (int)blocks;
+}
+
+// Empty state ([RA-CN] "环是怎样工作的": empty_online_softmax_state):
+// m = -inf, l = 0, O~ = 0.
+__global__ void state_init_kernel(float* __restrict__ m, float* __restrict__ l, float4* __restrict__ o,
+                                  long long rows, int d4) {
+  const long long total = rows * d4;
+  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < total;
+       x += (long long)gridDim.x * blockDim.x) {
+    o[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (x % d4 == 0) {
+      const long long row = x / d4;
+      m[row] = -INFINITY;
+      l[row] = 0.0f;
+    }
+  }
+}
+
+// a <- merge(a, b) ([GRA] "Why partial results are allowed to merge";
+// [ZQ]: rescale by exp(old_max - new_max)):
+//   m = max(ma, mb); alpha = e^{ma-m}, beta = e^{mb-m} (0 for an -inf side)
+//   l = alpha la + beta lb;  O~ = alpha O~a + beta O~b
+__global__ void merge_kernel(float* __restrict__ ma, float* __restrict__ la, float4* __restrict__ oa,
+                             const float* __restrict__ mb, const float* __restrict__ lb,
+                             const float4* __restrict__ ob, long long rows, int d4) {
+  // The loop runs per warp (all lanes share `base`, so every lane makes the
+  // same number of trips): the row's scalars are read by all its lanes before
+  // the __syncwarp, and only then overwritten.  d4 (16 or 32) divides 32, so
+  // a row never straddles two warps.
+  const long long total = rows * d4;
+  const int lane = threadIdx.x & 31;
+  for (long long base = blockIdx.x * (long long)blockDim.x + (threadIdx.x & ~31); base < total;
+       base += (long long)gridDim.x * blockDim.x) {
+    const long long x = base + lane;
+    const bool act = x < total;
+    const long long row = act ? x / d4 : 0;
+    float m = 0.f, alpha = 0.f, beta = 0.f, l = 0.f;
+    if (act) {
+      const float m_a = ma[row], m_b = mb[row];
+      m = fmaxf(m_a, m_b);
+      alpha = (m_a == -INFINITY) ? 0.0f : expf(m_a - m);
+      beta = (m_b == -INFINITY) ? 0.0f : expf(m_b - m);
+      l = alpha * la[row] + beta * lb[row];
+      const float4 va = oa[x], vb = ob[x];
+      float4 r;
+      r.x = alpha * va.x + beta * vb.x;
+      r.y = alpha * va.y + beta * vb.y;
+      r.z = alpha * va.z + beta * vb.z;
+      r.w = alpha * va.w + beta * vb.w;
+      oa[x] = r;
+    }
+    __syncwarp();
+    if (act && x % d4 == 0) {
+      ma[row] = m;
+      la[row] = l;
+    }
+  }
+}
+
+// Finalize shard r ([RA-CN] "环是怎样工作的": local_output = finalize(state)):
+// out = O~ / l, lse = m + ln l at natural position pos(r, i).
+__global__ void finalize_kernel(const float* __restrict__ m, const float* __restrict__ l,
+                                const float4* __restrict__ o, float4* __restrict__ out,
+                                float* __restrict__ lse, int BH, long long n, int d4, int P, int r,
+                                int layout, long long N) {
+  const long long rows = (long long)BH * n;
+  const long long total = rows * d4;
+  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < total;
+       x += (long long)gridDim.x * blockDim.x) {
+    const long long row = x / d4;
+    const int c = (int)(x % d4);
+    const long long bh = row / n, i = row % n;
+    const long long pos = layout == RING_LAYOUT_STRIPED ? i * P + r : (long long)r * n + i;
+    const long long dst_row = bh * N + pos;
+    const float lv = l[row];
+    const float inv = lv > 0.0f ? 1.0f / lv : 0.0f;
+    float4 v = o[x];
+    v.x *= inv;
+    v.y *= inv;
+    v.z *= inv;
+    v.w *= inv;
+    out[dst_row * d4 + c] = v;
+    if (c == 0) lse[dst_row] = lv > 0.0f ? m[row] + logf(lv) : -INFINITY;
+  }
+}
+
+// Pack natural-order K and V into the shard-major rotation buffer:
+// buf[r][bh][k][:] = src[bh][pos(r, k)][:]  (blockIdx.y: 0 = K, 1 = V).
+__global__ void pack_kv_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ kb,
+                               uint4* __restrict__ vb, int BH, long long n, int u16, int P, int layout) {
+  const uint4* src = blockIdx.y == 0 ? k : v;
+  uint4* dst = blockIdx.y == 0 ? kb : vb;
+  const long long N = n * P;
+  const long long total = (long long)P * BH * n * u16;
+  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < total;
+       x += (long long)gridDim.x * blockDim.x) {
+    const long long row = x / u16;  // destination row: (r, bh, kk)
+    const int c = (int)(x % u16);
+    const long long kk = row % n;
+    const long long bh = (row / n) % BH;
+    const long long r = row / (n * BH);
+    const long long pos = layout == RING_LAYOUT_STRIPED ? kk * P + r : r * n + kk;
+    dst[x] = src[(bh * N + pos) * u16 + c];
+  }
+}
+
+}  // namespace
+
+int launch_state_init(float* m, float* l, float* o, long long rows, int d, void* stream) {
+  const int d4 = d / 4;
+  if (rows <= 0) return 0;
+  state_init_kernel<<<grid_for(rows * d4, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      m, l, reinterpret_cast<float4*>(o), rows, d4);
+  return (int)cudaGetLastError();
+}
+
+int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* lb, const float* ob,
+                 long long rows, int d, void* stream) {
+  const int d4 = d / 4;
+  if (rows <= 0) return 0;
+  merge_kernel<<<grid_for(rows * d4, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      ma, la, reinterpret_cast<float4*>(oa), mb, lb, reinterpret_cast<const float4*>(ob), rows, d4);
+  return (int)cudaGetLastError();
+}
+
+int launch_finalize(const float* m, const float* l, const float* o, float* out, float* lse, int BH, long long n,
+                    int d, int P, int r, int layout, long long N, void* stream) {
+  const int d4 = d / 4;
+  const long long rows = (long long)BH * n;
+  if (rows <= 0) return 0;
+  finalize_kernel<<<grid_for(rows * d4, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      m, l, reinterpret_cast<const float4*>(o), reinterpret_cast<float4*>(out), lse, BH, n, d4, P, r, layout, N);
+  return (int)cudaGetLastError();
+}
+
+int launch_pack_kv(const void* k, const void* v, void* kbuf, void* vbuf, int BH, long long n, int d, int P,
+                   int layout, void* stream) {
+  const int u16 = d * 2 / 16;
+  const long long total = (long long)P * BH * n * u16;
+  if (total <= 0) return 0;
+  dim3 grid(grid_for(total, 256), 2);
+  pack_kv_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(kbuf),
+      static_cast<uint4*>(vbuf), BH, n, u16, P, layout);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace ringattn

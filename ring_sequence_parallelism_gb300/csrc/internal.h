@@ -1,0 +1,105 @@
+// internal.h -- definitions shared by the library's translation units.
+// Not part of the C ABI (that is include/ringattn.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/ringattn.h"
+
+namespace ringattn {
+
+constexpr int kTileM = 128;       // query rows per tile (one TMEM lane each)
+constexpr int kTileN = 128;       // keys per k-tile
+constexpr int kMaxShards = 1024;  // P limit (kernel parameter table size)
+
+// ---------------------------------------------------------------- planner
+// Unified diagonal-offset rule: inside block (query shard r, key block j) the
+// pair (local row i, local column k) is allowed iff k - i <= delta.
+//   contiguous: pos(j,k) <= pos(r,i)  <=>  k - i <= (r - j) n
+//   striped:    k P + j <= i P + r    <=>  k - i <= 0 if j <= r, else -1
+//   non-causal: every pair (delta = n, FULL).
+struct BlockPlan {
+  int j;            // key block held by shard r at this step
+  int cls;          // ring_block_class_t
+  long long delta;  // diagonal offset (see above)
+};
+
+struct Plan {
+  int B = 0, H = 0, d = 0, P = 0, causal = 0, layout = 0;
+  long long N = 0, n = 0;
+  int T = 0;   // query tiles per shard, ceil(n / kTileM)
+  int KT = 0;  // key tiles per block,  ceil(n / kTileN)
+  std::vector<BlockPlan> blocks;       // [step * P + r]
+  std::vector<long long> shard_pairs;  // [P] allowed pairs over all steps
+  std::vector<long long> shard_tiles;  // [P] computed 128x128 tiles
+  std::vector<long long> step_pairs;   // [P]
+  std::vector<long long> step_tiles;   // [P]
+  std::vector<std::vector<unsigned short>> active;  // [step] shards with work
+
+  const BlockPlan& at(int step, int r) const { return blocks[(size_t)step * P + r]; }
+};
+
+int block_of(int P, int r, int step);  // (r - step) mod P
+BlockPlan classify(int layout, int causal, long long n, int r, int j);
+long long block_pairs(long long n, const BlockPlan& b);
+// Key tiles a query tile t needs (count) and how many of them need no mask.
+void tile_range(long long n, int KT, const BlockPlan& b, int t, int* nk, int* full_kt);
+int build_plan(Plan* plan, int B, int H, long long N, int d, int P, int causal, int layout,
+               std::string* err);
+
+// ---------------------------------------------------------------- kernels
+// Query tensor addressing modes for the TMA map of Q.
+enum QMode : int {
+  kQShardMajor = 0,  // [BH][n][d], map dims (d, n, 1, BH), coords (c, i, 0, bh)
+  kQContiguous = 1,  // natural [BH][N][d] with pos = r n + i, dims (d, n, P, BH)
+  kQStriped = 2      // natural with pos = i P + r, dims (d, P, n, BH)
+};
+// Which slot of the K/V map holds the block of shard r at step s.
+enum KvMode : int {
+  kKvSlotR = 0,  // rotation buffer: slot r holds block (r - s) mod P
+  kKvSlotJ = 1,  // direct: slot j holds block j
+  kKvSingle = 2  // one block only (slot 0)
+};
+
+struct StepArgs {
+  float* o_state;  // O~ rows, d floats each
+  float* m_state;  // m rows (natural-log units of the scaled score)
+  float* l_state;  // l rows
+  float* out;      // finalize target: normalised rows
+  float* lse;      // finalize target: m + ln l
+  long long row_bh, row_r, row_i;  // state/out row = bh*row_bh + r*row_r + i*row_i
+  int* err;                        // device error words [0] flags, [1] site
+  unsigned long long wait_limit_ns;
+  int n, P, BH, T, KT;
+  int q_mode, kv_mode;
+  int causal, layout, step;
+  int accumulate;  // continue from the stored state
+  int finalize;    // write out/lse instead of the state
+  int n_active;    // shards in `active`
+  int fixed_r;     // >= 0: single shard (block partial); ignores `active`
+  float scale_log2;  // log2(e) / sqrt(d)
+  unsigned short active[kMaxShards];
+};
+
+// Device error flags.
+constexpr int kErrTimeout = 1;
+
+struct TensorMaps;  // opaque here (holds CUtensorMap values)
+
+// Launchers (return a cudaError_t as int).
+int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map, const void* v_map,
+                         int d, int grid, void* stream);
+int launch_state_init(float* m, float* l, float* o, long long rows, int d, void* stream);
+int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* lb, const float* ob,
+                 long long rows, int d, void* stream);
+int launch_finalize(const float* m, const float* l, const float* o, float* out, float* lse, int BH,
+                    long long n, int d, int P, int r, int layout, long long N, void* stream);
+int launch_pack_kv(const void* k, const void* v, void* kbuf, void* vbuf, int BH, long long n, int d,
+                   int P, int layout, void* stream);
+int block_partial_smem_bytes(int d);
+int prepare_block_partial_kernels();
+
+}  // namespace ringattn

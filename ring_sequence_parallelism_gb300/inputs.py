@@ -56,6 +56,8 @@ WORKLOADS = {
         Workload("striped-8k", 1, 8, 8192, 128, 8, True, "striped", 1001),
         Workload("striped-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01),
         Workload("striped-1m", 1, 8, 1048576, 128, 64, True, "striped", 1004),
+        # profiling size: the 128K striped workload with 4 heads (inputs 3 x 134 MB)
+        Workload("striped-128k-h4", 1, 4, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01),
     )
 }
 

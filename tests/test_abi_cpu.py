@@ -1,0 +1,178 @@
+"""C-ABI library on the CPU: it loads, exports every declared symbol, checks
+its arguments, and its host planner matches the closed forms and the
+oracle's visit counts.  No compute call is made (no GPU here)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import ring_sequence_parallelism_gb300 as ra
+from ring_sequence_parallelism_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ringattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ring_sequence_parallelism_gb300 import build
+
+    build.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER, encoding="utf-8").read()
+    return sorted(set(re.findall(r"RINGATTN_API\s+(?:const\s+)?\w+\*?\s+\*?(ring_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    for must in ("ring_attn_create", "ring_attn_block_partial", "ring_attn_merge", "ring_attn_fwd",
+                 "ring_attn_destroy"):
+        assert must in names
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def _create(lib, *args):
+    h = ctypes.c_void_p()
+    rc = lib.ring_attn_create(ctypes.byref(h), *args)
+    return rc, h
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 1, 64, 64, 1, 0, 0), _lib.RING_ERR_INVALID_ARG),      # B = 0
+    ((1, 1, 64, 64, 0, 0, 0), _lib.RING_ERR_INVALID_ARG),      # P = 0
+    ((1, 1, 64, 64, 1, 2, 0), _lib.RING_ERR_INVALID_ARG),      # causal = 2
+    ((1, 1, 64, 64, 1, 0, 7), _lib.RING_ERR_INVALID_ARG),      # bad layout
+    ((1, 1, 4, 64, 8, 0, 0), _lib.RING_ERR_INVALID_ARG),       # P > N
+    ((1, 1, 100, 64, 3, 0, 0), _lib.RING_ERR_UNSUPPORTED),     # N % P != 0
+    ((1, 1, 128, 96, 1, 0, 0), _lib.RING_ERR_UNSUPPORTED),     # d = 96
+    ((1, 1, 4096, 64, 2048, 0, 0), _lib.RING_ERR_UNSUPPORTED),  # P above the table size
+])
+def test_create_rejects(lib, args, status):
+    rc, h = _create(lib, *args)
+    assert rc == status
+    assert h.value is None
+    assert lib.ring_attn_last_error()
+
+
+def test_create_null_out(lib):
+    assert lib.ring_attn_create(None, 1, 1, 64, 64, 1, 0, 0) == _lib.RING_ERR_INVALID_ARG
+
+
+def test_calls_reject_null_arguments_without_a_gpu(lib):
+    rc, h = _create(lib, 1, 2, 256, 64, 2, 1, 1)
+    assert rc == 0
+    st = _lib.RingState(None, None, None)
+    assert lib.ring_attn_merge(h, st, st, None) == _lib.RING_ERR_INVALID_ARG
+    assert lib.ring_attn_fwd(h, None, None, None, None, None, None, None) == _lib.RING_ERR_INVALID_ARG
+    assert lib.ring_attn_block_partial(h, 0, 0, None, None, None, st, 0, None) == _lib.RING_ERR_INVALID_ARG
+    assert lib.ring_attn_set_option(h, 99, 1) == _lib.RING_ERR_INVALID_ARG
+    assert lib.ring_attn_set_option(h, _lib.RING_OPT_ROTATION, 0) == 0
+    assert lib.ring_attn_get_timing(h, None, None, None, None) == _lib.RING_ERR_INVALID_ARG
+    assert lib.ring_attn_plan_block(h, 2, 0, None, None, None) == _lib.RING_ERR_INVALID_ARG
+    assert lib.ring_attn_destroy(h) == 0
+    assert lib.ring_attn_destroy(None) == 0
+
+
+def test_workspace_size(lib):
+    att = ra.RingAttention(1, 16, 131072, 128, 16, causal=True, layout="striped")
+    elems = 16 * 131072 * 128
+    assert att.workspace_size() == 4 * elems * 2 + 16 * 131072 * 4
+    att.close()
+
+
+# -------------------------------------------------------------- planner
+def test_plan_matches_golden_schedule(lib):
+    """The 4-device walk-through in "Ring Attention：把超长序列沿设备环流动",
+    section "环是怎样工作的"."""
+    path = os.path.join(ROOT, "tests", "golden", "ring_schedule_4dev.txt")
+    att = ra.RingAttention(1, 1, 4 * 128, 64, 4, causal=False, layout="contiguous")
+    for line in open(path):
+        if line.strip() and not line.startswith("#"):
+            step, dev, blk = map(int, line.split())
+            assert att.plan_block(dev, step)[0] == blk
+    att.close()
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("P,n", [(2, 128), (4, 200), (8, 1024), (16, 8192), (64, 16384), (3, 1)])
+def test_shard_work_closed_forms(lib, layout, P, n):
+    """Allowed pairs per shard under the causal mask: contiguous
+    W_r = r n^2 + n(n+1)/2, striped W_r = (r+1) n(n+1)/2 + (P-1-r) n(n-1)/2;
+    the total is N(N+1)/2 ("GPU Ring Attention", "The causal mask wrecks the
+    load balance": work ramps from one block on rank 0 to P on the last)."""
+    B, H = 1, 2
+    N = P * n
+    att = ra.RingAttention(B, H, N, 64, P, causal=True, layout=layout)
+    pairs, tiles = att.shard_work()
+    for r in range(P):
+        if layout == "contiguous":
+            want = r * n * n + n * (n + 1) // 2
+        else:
+            want = (r + 1) * n * (n + 1) // 2 + (P - 1 - r) * n * (n - 1) // 2
+        assert pairs[r] == want * B * H, (r, pairs[r], want)
+    assert sum(pairs) == B * H * N * (N + 1) // 2
+    steps = [att.step_work(s)[0] for s in range(P)]
+    assert sum(steps) == sum(pairs)
+    # every computed 128x128 tile covers at least one allowed pair
+    assert sum(tiles) * 128 * 128 >= sum(pairs)
+    if P > 1 and n >= 128:
+        ratio = max(pairs) / min(pairs)
+        if layout == "contiguous":
+            assert ratio > P  # ~ 2P - 1
+        else:
+            assert ratio < 1.02
+    att.close()
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("P", [1, 2, 3, 6])
+def test_planner_agrees_with_oracle_visits(lib, orc, layout, causal, P):
+    """Per (shard, step) allowed-pair counts from the planner equal the
+    oracle ring simulation's visit counts."""
+    from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED
+    import oracle_pins
+
+    N, d = 24, 2
+    n = N // P
+    lid = LAYOUT_STRIPED if layout == "striped" else LAYOUT_CONTIGUOUS
+    q = oracle_pins.rand_bits((1, N, d), 1)
+    _, _, cnt = orc.ring(q, q, q, P, causal, lid, visits=True)
+    att = ra.RingAttention(1, 1, N, 64, P, causal=causal, layout=layout)
+    for r in range(P):
+        rows = [orc.position(lid, n, P, r, i) for i in range(n)]
+        for s in range(P):
+            j, cls, delta = att.plan_block(r, s)
+            assert j == orc.block_at(P, r, s)
+            cols = [orc.position(lid, n, P, j, kk) for kk in range(n)]
+            got = int(cnt[0][np.ix_(rows, cols)].sum())
+            # the planner's (class, delta) rule, enumerated
+            want = sum(1 for i in range(n) for kk in range(n) if cls != 0 and kk - i <= delta)
+            assert got == want, (r, s, j, cls, delta, got, want)
+            if cls == 0:
+                assert got == 0
+            if cls == 1:
+                assert got == n * n
+    att.close()
+
+
+def test_step_time_model_golden():
+    """Pipelined ring time P x max(T_compute, T_comm): the worked estimate in
+    "Ring Attention：把超长序列沿设备环流动", section "一个容量与时间的估算示例"."""
+    from ring_sequence_parallelism_gb300.report import pipelined_ring_ms
+
+    path = os.path.join(ROOT, "tests", "golden", "step_time_estimate.txt")
+    for line in open(path):
+        if line.strip() and not line.startswith("#"):
+            steps, tc, tm, total = map(float, line.split())
+            assert pipelined_ring_ms(int(steps), tc, tm) == pytest.approx(total)

@@ -1,0 +1,337 @@
+"""CUDA path against the float64 oracle, element by element (GPU only).
+
+Tolerances (bf16 inputs, fp32 accumulation): max|d out| <= 1e-2 and
+max|d lse| <= 1e-3; the fp32 merge of fp32 states: <= 1e-5.  Every call goes
+through the C ABI (the ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ring_sequence_parallelism_gb300 as ra
+from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED
+from ring_sequence_parallelism_gb300.inputs import WORKLOADS, make_qkv, make_workload, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 1e-2
+TOL_LSE = 1e-3
+TOL_MERGE = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from ring_sequence_parallelism_gb300 import build
+
+    build.build()
+    ra._lib.load()
+
+
+def lid(layout):
+    return LAYOUT_STRIPED if layout == "striped" else LAYOUT_CONTIGUOUS
+
+
+def flat(t, BH):
+    return t.reshape(BH, *t.shape[2:])
+
+
+def report(name, out, lse, ref_out, ref_lse):
+    d_out = float(np.max(np.abs(out - ref_out))) if out.size else 0.0
+    d_lse = float(np.max(np.abs(lse - ref_lse))) if lse.size else 0.0
+    print(f"{name}: max|dout|={d_out:.3e} max|dlse|={d_lse:.3e}")
+    return d_out, d_lse
+
+
+def run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=True):
+    att = ra.RingAttention(B, H, N, d, P, causal=causal, layout=layout)
+    att.set_option(ra.RING_OPT_ROTATION, int(rotation))
+    out, lse = att.fwd(q.cuda(), k.cuda(), v.cuda())
+    att.check()
+    torch.cuda.synchronize()
+    res = out.cpu(), lse.cpu()
+    att.close()
+    return res
+
+
+# ------------------------------------------------------------ merge et al.
+def random_state(rows, d, seed, empty_frac=0.1):
+    g = np.random.default_rng(seed)
+    m = g.normal(0, 3, rows).astype(np.float32)
+    l = g.uniform(0.5, 4.0, rows).astype(np.float32)
+    o = g.normal(0, 1, (rows, d)).astype(np.float32)
+    empty = g.random(rows) < empty_frac
+    m[empty] = -np.inf
+    l[empty] = 0.0
+    o[empty] = 0.0
+    return m, l, o
+
+
+@pytest.mark.parametrize("B,H,n,d", [(1, 2, 128, 64), (2, 3, 200, 128), (1, 8, 1024, 128)])
+def test_merge_matches_oracle(B, H, n, d):
+    P = 2
+    att = ra.RingAttention(B, H, n * P, d, P, causal=True, layout="striped")
+    rows = B * H * n
+    a = random_state(rows, d, 1)
+    b = random_state(rows, d, 2)
+    # also rows where both sides are empty, and equal maxima
+    a[0][:3] = -np.inf; a[1][:3] = 0; a[2][:3] = 0
+    b[0][:2] = -np.inf; b[1][:2] = 0; b[2][:2] = 0
+    b[0][5] = a[0][5]
+    ga = tuple(torch.from_numpy(x.reshape((B, H, n) + x.shape[1:])).cuda().contiguous() for x in a)
+    gb = tuple(torch.from_numpy(x.reshape((B, H, n) + x.shape[1:])).cuda().contiguous() for x in b)
+    att.merge(ga, gb)
+    torch.cuda.synchronize()
+    m, l, o = (x.cpu().numpy().reshape(rows, -1).squeeze() for x in ga)
+    o = ga[2].cpu().numpy().reshape(rows, d)
+    rm, rl, ro = oracle.default().merge_states(a, b)
+    both_empty = np.isneginf(rm)
+    assert np.array_equal(np.isneginf(m), both_empty)
+    assert np.all(l[both_empty] == 0) and np.all(o[both_empty] == 0)
+    ne = ~both_empty
+    assert np.max(np.abs(m[ne] - rm[ne])) <= TOL_MERGE
+    assert np.max(np.abs(l[ne] - rl[ne])) <= TOL_MERGE * max(1.0, float(np.max(rl)))
+    assert np.max(np.abs(o[ne] - ro[ne])) <= TOL_MERGE
+    att.close()
+
+
+def test_state_init_and_finalize():
+    B, H, N, d, P = 1, 2, 4 * 200, 128, 4
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped")
+    st = att.new_state()
+    att.state_init(st)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isneginf(st[0])) and torch.all(st[1] == 0) and torch.all(st[2] == 0)
+    rows = B * H * att.n
+    m, l, o = random_state(rows, d, 7)
+    st = tuple(torch.from_numpy(x.reshape((B, H, att.n) + x.shape[1:])).cuda().contiguous() for x in (m, l, o))
+    out = torch.full((B, H, N, d), 7.0, device="cuda")
+    lse = torch.full((B, H, N), 7.0, device="cuda")
+    r = 2
+    att.finalize(r, st, out, lse)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.default().finalize(m, l, o)
+    pos = [i * P + r for i in range(att.n)]
+    got_out = out.cpu().numpy().reshape(B * H, N, d)[:, pos].reshape(rows, d)
+    got_lse = lse.cpu().numpy().reshape(B * H, N)[:, pos].reshape(rows)
+    fin = np.isfinite(ref_lse)
+    assert np.max(np.abs(got_out - ref_out)) <= 1e-6
+    assert np.max(np.abs(got_lse[fin] - ref_lse[fin])) <= 1e-6
+    assert np.all(np.isneginf(got_lse[~fin]))
+    others = [t for t in range(N) if t % P != r]
+    assert torch.all(out.reshape(B * H, N, d)[:, others] == 7.0)
+    att.close()
+
+
+# ------------------------------------------------------------ block partial
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n", [128, 328])
+def test_block_partial_matches_oracle(layout, d, n):
+    """Every (shard, step) block of a small ring, fresh (accumulate 0): the
+    block state's unique parts, m + ln l and O~/l, against the oracle's block
+    partial; empty rows must come back as (m=-inf, l=0, O~=0)."""
+    B, H, P = 1, 2, 3
+    N = n * P
+    q, k, v = make_qkv(B, H, N, d, seed=n + d)
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout=layout)
+    orc = oracle.default()
+    L = lid(layout)
+    BH = B * H
+    qf, kf, vf = flat(q, BH), flat(k, BH), flat(v, BH)
+    worst_o = worst_l = 0.0
+    for r in range(P):
+        pos_r = [orc.position(L, n, P, r, i) for i in range(n)]
+        q_sh = qf[:, pos_r].contiguous()
+        for s in range(P):
+            j = orc.block_at(P, r, s)
+            pos_j = [orc.position(L, n, P, j, i) for i in range(n)]
+            k_bl, v_bl = kf[:, pos_j].contiguous(), vf[:, pos_j].contiguous()
+            st = att.new_state()
+            for x in st:
+                x.fill_(float("nan"))
+            att.block_partial(r, s, q_sh.reshape(B, H, n, d).cuda(), k_bl.reshape(B, H, n, d).cuda(),
+                              v_bl.reshape(B, H, n, d).cuda(), st, 0)
+            att.check()
+            m, l, o = (x.cpu().double().numpy().reshape(BH * n, -1) for x in st)
+            m, l = m[:, 0], l[:, 0]
+            rm, rl, ro = orc.block_partial(q_sh, k_bl, v_bl, P, True, L, r, j)
+            rm, rl, ro = rm.reshape(-1), rl.reshape(-1), ro.reshape(BH * n, d)
+            empty = np.isneginf(rm)
+            assert np.all(np.isneginf(m[empty])) and np.all(l[empty] == 0) and np.all(o[empty] == 0), (r, s)
+            ne = ~empty
+            if ne.any():
+                dl = np.abs((m[ne] + np.log(l[ne])) - (rm[ne] + np.log(rl[ne])))
+                do = np.abs(o[ne] / l[ne][:, None] - ro[ne] / rl[ne][:, None])
+                worst_l, worst_o = max(worst_l, float(dl.max())), max(worst_o, float(do.max()))
+    print(f"block partial {layout} d={d} n={n}: max|dout|={worst_o:.3e} max|dlse|={worst_l:.3e}")
+    assert worst_o <= TOL_OUT and worst_l <= TOL_LSE
+    att.close()
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_block_partial_ring_with_accumulate(layout):
+    """The pages' loop driven through the C ABI: empty state, then P block
+    partials with accumulate 1 in ring order, then finalize; equals dense
+    attention (oracle)."""
+    B, H, n, d, P = 1, 2, 256, 128, 4
+    N = n * P
+    q, k, v = make_qkv(B, H, N, d, seed=77)
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout=layout)
+    orc = oracle.default()
+    L = lid(layout)
+    BH = B * H
+    qf, kf, vf = flat(q, BH), flat(k, BH), flat(v, BH)
+    out = torch.empty((B, H, N, d), device="cuda")
+    lse = torch.empty((B, H, N), device="cuda")
+    for r in range(P):
+        pos_r = [orc.position(L, n, P, r, i) for i in range(n)]
+        st = att.new_state()
+        att.state_init(st)
+        for s in range(P):
+            j = orc.block_at(P, r, s)
+            pos_j = [orc.position(L, n, P, j, i) for i in range(n)]
+            att.block_partial(r, s, qf[:, pos_r].reshape(B, H, n, d).cuda(), kf[:, pos_j].reshape(B, H, n, d).cuda(),
+                              vf[:, pos_j].reshape(B, H, n, d).cuda(), st, 1)
+        att.finalize(r, st, out, lse)
+    att.check()
+    ref_out, ref_lse = orc.dense(qf, kf, vf, True)
+    d_out, d_lse = report(f"block ring {layout}", out.cpu().double().numpy().reshape(BH, N, d),
+                          lse.cpu().double().numpy().reshape(BH, N), ref_out, ref_lse)
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE
+    att.close()
+
+
+# ------------------------------------------------------------ ring forward
+SMALL_CASES = [
+    # (B, H, N, d, P, causal, layout)
+    (1, 2, 512, 64, 4, False, "contiguous"),    # 2 heads x 512 tokens, non-causal
+    (1, 2, 512, 64, 4, True, "striped"),
+    (2, 2, 3 * 200, 128, 3, True, "contiguous"),  # ragged tail (n = 200)
+    (2, 2, 3 * 200, 128, 3, True, "striped"),
+    (1, 3, 640, 128, 1, True, "contiguous"),      # P = 1: one block, one step
+    (1, 1, 5 * 8, 64, 5, True, "striped"),        # n = 8: tiny shards
+    (1, 2, 2048, 128, 16, True, "striped"),
+    (1, 2, 2048, 128, 2, False, "striped"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: "B{}H{}N{}d{}P{}{}{}".format(
+    c[0], c[1], c[2], c[3], c[4], "c" if c[5] else "n", c[6][0]))
+def test_fwd_small(case):
+    B, H, N, d, P, causal, layout = case
+    q, k, v = make_qkv(B, H, N, d, seed=N + P + d)
+    out, lse = run_fwd(B, H, N, d, P, causal, layout, q, k, v)
+    BH = B * H
+    ref_out, ref_lse = oracle.default().dense(flat(q, BH), flat(k, BH), flat(v, BH), causal)
+    d_out, d_lse = report(f"fwd {case}", out.double().numpy().reshape(BH, N, d),
+                          lse.double().numpy().reshape(BH, N), ref_out, ref_lse)
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE
+
+
+def test_fwd_rotation_matches_direct_indexing():
+    """The double-buffered rotation only moves bytes: results are identical
+    bit for bit to reading every block straight from the packed buffer."""
+    B, H, N, d, P = 1, 2, 8 * 256, 128, 8
+    q, k, v = make_qkv(B, H, N, d, seed=5)
+    for layout in ("contiguous", "striped"):
+        a = run_fwd(B, H, N, d, P, True, layout, q, k, v, rotation=True)
+        b = run_fwd(B, H, N, d, P, True, layout, q, k, v, rotation=False)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_fwd_noncausal_512_workload():
+    w = WORKLOADS["noncausal-512"]
+    q, k, v = make_workload(w)
+    out, lse = run_fwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v)
+    BH = w.B * w.H
+    orc = oracle.default()
+    ref_out, ref_lse = orc.dense(flat(q, BH), flat(k, BH), flat(v, BH), w.causal)
+    ring_out, ring_lse = orc.ring(flat(q, BH), flat(k, BH), flat(v, BH), w.P, w.causal, LAYOUT_CONTIGUOUS)
+    assert np.max(np.abs(ring_out - ref_out)) <= 1e-12
+    d_out, d_lse = report(w.name, out.double().numpy().reshape(BH, w.N, w.d), lse.double().numpy().reshape(BH, w.N),
+                          ref_out, ref_lse)
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE
+
+
+def test_fwd_8k_contiguous_and_striped():
+    """Both 8K causal workloads, every row, against dense; then the striped
+    result against the contiguous one (same seeded inputs; outputs are in
+    natural order, so no un-permuting is left to do)."""
+    wc, ws = WORKLOADS["contiguous-8k"], WORKLOADS["striped-8k"]
+    q, k, v = make_workload(wc)
+    BH = wc.B * wc.H
+    ref_out, ref_lse = oracle.default().dense(flat(q, BH), flat(k, BH), flat(v, BH), True)
+    res = {}
+    for w in (wc, ws):
+        out, lse = run_fwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v)
+        res[w.name] = (out, lse)
+        d_out, d_lse = report(w.name, out.double().numpy().reshape(BH, w.N, w.d),
+                              lse.double().numpy().reshape(BH, w.N), ref_out, ref_lse)
+        assert d_out <= TOL_OUT and d_lse <= TOL_LSE
+    a, b = res[wc.name], res[ws.name]
+    assert float((a[0] - b[0]).abs().max()) <= 2 * TOL_OUT
+    assert float((a[1] - b[1]).abs().max()) <= 2 * TOL_LSE
+
+
+def _sampled_check(w, rows_per_head, ring_rows=0):
+    q, k, v = make_workload(w)
+    out, lse = run_fwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v)
+    BH = w.B * w.H
+    n = w.n
+    extra = (0, 1, w.N - 1, n - 1, n, w.P - 1, w.P, w.N // 2)
+    rows = sample_rows(w.N, rows_per_head, extra=extra).numpy()
+    orc = oracle.default()
+    qf, kf, vf = flat(q, BH), flat(k, BH), flat(v, BH)
+    ref_out, ref_lse = orc.dense(qf, kf, vf, w.causal, rows=rows)
+    got_out = out.reshape(BH, w.N, w.d)[:, rows].double().numpy()
+    got_lse = lse.reshape(BH, w.N)[:, rows].double().numpy()
+    d_out, d_lse = report(f"{w.name} ({rows.size} rows/head)", got_out, got_lse, ref_out, ref_lse)
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE
+    if ring_rows:
+        rr = rows[:ring_rows]
+        r_out, r_lse = orc.ring(qf, kf, vf, w.P, w.causal, w.layout_id, rows=rr)
+        assert np.max(np.abs(r_out - ref_out[:, :ring_rows])) <= 1e-10
+        assert np.max(np.abs(r_lse - ref_lse[:, :ring_rows])) <= 1e-10
+    # properties that hold at any size: finite everywhere, lse above the
+    # diagonal score, and causal row 0 equal to v_0
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    v0 = v.reshape(BH, w.N, w.d)[:, 0].float()
+    assert float((out.reshape(BH, w.N, w.d)[:, 0] - v0).abs().max()) <= TOL_OUT
+
+
+def test_fwd_128k_striped_sampled():
+    _sampled_check(WORKLOADS["striped-128k"], 256, ring_rows=16)
+
+
+@pytest.mark.slow
+def test_fwd_1m_striped_sampled():
+    _sampled_check(WORKLOADS["striped-1m"], 256)
+
+
+def test_timing_report():
+    B, H, N, d, P = 1, 4, 8 * 512, 128, 8
+    q, k, v = make_qkv(B, H, N, d, seed=9)
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped")
+    att.set_option(ra.RING_OPT_TIMING, 1)
+    att.fwd(q.cuda(), k.cuda(), v.cuda())
+    t = att.timing()
+    att.check()
+    assert len(t["kernel_ms"]) == P and all(x > 0 for x in t["kernel_ms"])
+    assert t["copy_ms"][0] == 0 and all(x > 0 for x in t["copy_ms"][1:])
+    assert all(x >= 0 for x in t["wait_ms"]) and t["pack_ms"] > 0
+    att.close()
+
+
+def test_bad_alignment_is_rejected():
+    B, H, N, d, P = 1, 1, 256, 64, 2
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped")
+    buf = torch.zeros(B * H * N * d + 8, dtype=torch.bfloat16, device="cuda")
+    q = buf[1:1 + B * H * N * d].view(B, H, N, d)  # 2-byte offset: not 16-byte aligned
+    out = torch.empty((B, H, N, d), device="cuda")
+    lse = torch.empty((B, H, N), device="cuda")
+    with pytest.raises(ra.RingAttnError) as e:
+        ra.ring_attn_fwd(att.handle, q, q, q, out, lse, att.workspace())
+    assert e.value.status == ra._lib.RING_ERR_INVALID_ARG
+    att.close()
