@@ -194,6 +194,32 @@ RINGATTN_API int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* co
  * ran out), clearing it. */
 RINGATTN_API int ring_attn_check(ring_attn_t h, void* stream);
 
+/* ring_attn_fwd for callers that cannot allocate device memory (the pages
+ * have no counterpart: this is a packaging of ring_attn_fwd, not a step of
+ * the method).  Callers such as a plug-in inside a host application that
+ * owns all device memory through its own pool, or code on a latency-critical
+ * path where cudaMalloc/cudaFree may synchronise the device, pass only
+ * inputs and outputs; the scratch ring_attn_fwd takes as a workspace (the
+ * packed K/V and the running l state) lives in a fixed 64 MiB __device__
+ * array inside the library, which every GPU that loads the library holds
+ * until the process exits.
+ *   q, k, v, out, lse  as for ring_attn_fwd (device, 16-byte aligned)
+ *   status  optional device int (NULL to skip): receives the device-side
+ *           error flags of this call (0 = ok, nonzero = a bounded wait ran
+ *           out), written on `stream` at the end of the call
+ * Errors: RING_ERR_UNSUPPORTED when the problem's scratch
+ * (4*B*H*N*d + 4*B*H*N bytes, plus alignment) exceeds the array; otherwise
+ * as ring_attn_fwd.  Every step reads its block straight from the packed
+ * buffer (no rotation copies); the result equals ring_attn_fwd's.
+ * The call allocates nothing.  Its first call on a device, with that device
+ * current, does a one-time set-up (device check, kernel attributes, the
+ * array's device address via cudaGetSymbolAddress); make that first call
+ * before any stream capture.  All calls share the array and it keeps the
+ * last call's contents: calls that overlap on the GPU race on it, so
+ * serialise them. */
+RINGATTN_API int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k, const void* v, float* out,
+                                       float* lse, int* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -55,6 +55,7 @@ SIGNATURES = {
     "ring_attn_set_option": (_i, [_vp, _i, _ll]),
     "ring_attn_get_timing": (_i, [_vp, _pf, _pf, _pf, _pf]),
     "ring_attn_check": (_i, [_vp, _vp]),
+    "ring_attn_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
 _LIB = None

@@ -84,6 +84,20 @@ int encode_map(CUtensorMap* map, const void* base, const cuuint64_t dims[4], con
 
 }  // namespace
 
+namespace ringattn {
+// Shared with other translation units of the library (declared in internal.h).
+int report_error(int code, const char* msg) { return fail(code, msg); }
+
+int tensor_map_4d(void* map, const void* base, const unsigned long long dims[4],
+                  const unsigned long long strides[3], unsigned box1, unsigned box2) {
+  int rc = get_encoder();
+  if (rc) return rc;
+  cuuint64_t d4[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t s3[3] = {strides[0], strides[1], strides[2]};
+  return encode_map(static_cast<CUtensorMap*>(map), base, d4, s3, box1, box2);
+}
+}  // namespace ringattn
+
 struct ring_attn {
   Plan plan;
   int rotation = 1;
@@ -100,6 +114,11 @@ struct ring_attn {
   bool timed_valid = false;
   int* d_err = nullptr;  // [0] flags, [1] first failing site
 };
+
+namespace ringattn {
+const Plan& handle_plan(const ring_attn* h) { return h->plan; }
+unsigned long long handle_wait_limit(const ring_attn* h) { return h->wait_limit_ns; }
+}  // namespace ringattn
 
 namespace {
 

@@ -16,10 +16,10 @@
 // the exact merge with the incoming state is the same rescale.  The epilogue
 // writes the state back, or the normalised output O~/l and lse = m + ln l.
 //
-// Lazy rescale: the reference max m only moves when a tile's max exceeds it
-// by more than 2^8 (in the exp2 domain); below that P <= 256, which bf16 and
-// fp32 hold exactly enough.  Any reference max gives the same state (the pair
-// l, O~ is scaled by exp(-m) consistently), so the result is unchanged.
+// Rescale: the reference max m moves when a tile's max exceeds it by more
+// than kRescaleThreshold (exp2 domain), and the warp rescales O~ in TMEM only
+// when one of its rows moved.  Any reference max gives the same state (l and
+// O~ are scaled by exp(-m) consistently).
 //
 // CTA layout (192 threads, one 128-row query tile per CTA):
 //   warp 0      TMEM allocation; lane 0 issues the TMA loads (Q once, then
@@ -51,7 +51,12 @@ constexpr int kTmemS1 = 128;  // S buffer 1: columns [128, 256)
 constexpr int kTmemO = 256;   // O~: columns [256, 256 + d)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units (factor 256)
+// The reference max follows the running row max exactly (threshold 0): the
+// row's largest weight is then exp2(0) = 1, exact in bf16, so a row that one
+// key dominates loses nothing to the bf16 rounding of P.  (A lazy threshold
+// of 8 halves the rescale work but leaves the dominant weight anywhere in
+// [1, 256) with a bf16 rounding error of up to 2^-9 relative.)
+constexpr float kRescaleThreshold = 0.0f;
 
 // Shared-memory map.  Every tile starts on a 1024-byte boundary (the
 // 128-byte swizzle pattern repeats every 8 rows of 128 bytes).
@@ -532,18 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = need ? m_tile : m2;
       const float alpha = need ? fast_exp2(m2 - m_new) : 1.0f;
       const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-      // P is rounded to bf16 here (the PV operand), and l sums the rounded
-      // values, so numerator and denominator of O~/l see the same weights:
-      // a row dominated by one key then returns that key's value exactly.
+      // P is rounded to bf16 (the PV operand); l sums the fp32 values.
       float rowsum = 0.0f;
       uint32_t pb[kTileN / 2];
 #pragma unroll
       for (int e = 0; e < kTileN; e += 2) {
         const float p0 = fast_exp2(fmaf(s[e], a.scale_log2, -m_use));
         const float p1 = fast_exp2(fmaf(s[e + 1], a.scale_log2, -m_use));
-        const uint32_t packed = pack_bf16(p0, p1);
-        pb[e / 2] = packed;
-        rowsum += __uint_as_float(packed << 16) + __uint_as_float(packed & 0xFFFF0000u);
+        pb[e / 2] = pack_bf16(p0, p1);
+        rowsum += p0 + p1;
       }
       l = l * alpha + rowsum;
       m2 = m_new;

@@ -99,6 +99,16 @@ int launch_finalize(const float* m, const float* l, const float* o, float* out, 
                     long long n, int d, int P, int r, int layout, long long N, void* stream);
 int launch_pack_kv(const void* k, const void* v, void* kbuf, void* vbuf, int BH, long long n, int d,
                    int P, int layout, void* stream);
+// Error reporting and TMA descriptors shared across translation units:
+// report_error sets ring_attn_last_error() and returns `code`;
+// tensor_map_4d encodes a 4-D bf16 map (box 64 x box1 x box2 x 1, 128-byte
+// swizzle) into `map` (a CUtensorMap), dims innermost first, strides in bytes.
+int report_error(int code, const char* msg);
+int tensor_map_4d(void* map, const void* base, const unsigned long long dims[4],
+                  const unsigned long long strides[3], unsigned box1, unsigned box2);
+// The handle's plan and wait limit, for translation units outside api.cu.
+const Plan& handle_plan(const ring_attn* h);
+unsigned long long handle_wait_limit(const ring_attn* h);
 int block_partial_smem_bytes(int d);
 int prepare_block_partial_kernels();
 
