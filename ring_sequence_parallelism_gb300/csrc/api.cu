@@ -360,7 +360,7 @@ int ring_attn_block_partial(ring_attn_t h, int r, int step, const void* q_shard,
   a.finalize = 0;
   a.fixed_r = r;
   a.n_active = 1;
-  const int grid = p.T * BH;
+  const int grid = block_partial_grid(p.T, 1, BH);
   RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km, &vm, p.d, grid, stream), "block_partial launch");
   return RING_OK;
 }
@@ -436,7 +436,7 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     a.finalize = s == P - 1 ? 1 : 0;
     a.n_active = (int)act.size();
     for (size_t x = 0; x < act.size(); ++x) a.active[x] = act[x];
-    const int grid = p.T * a.n_active * BH;
+    const int grid = block_partial_grid(p.T, a.n_active, BH);
     if (timing) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
     RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km[cur], &vm[cur], p.d, grid, cs), "step kernel launch");
     if (timing) RA_CUDA(cudaEventRecord(h->tk1[s], cs), "cudaEventRecord");

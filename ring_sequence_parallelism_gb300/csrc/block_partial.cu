@@ -1,4 +1,4 @@
-// block_partial.cu -- blockwise exact attention of one query tile against one
+// block_partial.cu -- blockwise exact attention of query tiles against one
 // K/V block, continuing a per-row online-softmax state (sm_103a).
 //
 // What it computes ([RA-CN] "两层分块如何嵌套": inside a device-level block the
@@ -9,26 +9,37 @@
 //   for each key tile of the block that has an allowed pair for the tile:
 //     S  = Q K^T                                   (tcgen05, bf16 -> fp32 TMEM)
 //     S' = S masked with k - i <= delta, k < n     (only tiles that need it)
-//     m' = max(m, rowmax S' * scale)               (lazily, see below)
+//     m' = max(m, rowmax S' * scale)
 //     P  = exp(S' * scale - m'),  l = l e^{m-m'} + rowsum P
-//     O~ = O~ e^{m-m'} + P V                       (tcgen05, P bf16, fp32 TMEM)
+//     O~ = O~ e^{m-m'} + P V                       (tcgen05, P bf16 from TMEM)
 // The state (m, l, O~) is loaded from HBM first when `accumulate` is set, so
 // the exact merge with the incoming state is the same rescale.  The epilogue
 // writes the state back, or the normalised output O~/l and lse = m + ln l.
 //
-// Rescale: the reference max m moves when a tile's max exceeds it by more
-// than kRescaleThreshold (exp2 domain), and the warp rescales O~ in TMEM only
-// when one of its rows moved.  Any reference max gives the same state (l and
-// O~ are scaled by exp(-m) consistently).
+// CTA layout: 320 threads, two 128-row query tiles A and B (rows 256u ..
+// 256u+255 of one shard) against the same K/V key tiles.
+//   warp 0      TMEM allocation; lane 0 issues the TMA loads (Q_A, Q_B once,
+//               then K and V tiles through two 2-stage rings)
+//   warp 1      lane 0 issues tcgen05.mma in the order
+//                 PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+//               so the tensor core works on one tile while the other tile's
+//               softmax runs.  PV takes P from TMEM (A operand in TMEM, V from
+//               shared memory), which keeps shared-memory reads of the MMAs
+//               below the 128 B/clk the SM can serve.
+//   warps 2..5  softmax + epilogue of tile A, one query row per thread
+//   warps 6..9  softmax + epilogue of tile B
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O~_A [256,256+d),
+// O~_B [256+d, 256+2d).  P_t (bf16 pairs, 64 columns) is written over the
+// first half of S_t once the softmax has read S_t into registers; the next
+// S_t MMA is issued after the PV MMA that reads P_t, and tcgen05.mma
+// instructions from one thread execute in issue order.
 //
-// CTA layout (192 threads, one 128-row query tile per CTA):
-//   warp 0      TMEM allocation; lane 0 issues the TMA loads (Q once, then
-//               K and V tiles through a 2-stage ring)
-//   warp 1      lane 0 issues tcgen05.mma: S_j = Q K_j^T into one of two TMEM
-//               S buffers, then O += P_{j-1} V_{j-1} (software pipelined)
-//   warps 2..5  softmax + epilogue, one query row per thread (TMEM lane
-//               quadrant = warp % 4); P goes to shared memory in the
-//               128-byte-swizzled K-major layout the MMA reads
+// Rescale: the reference max follows the running row max exactly (threshold
+// 0): the row's largest weight is then exp2(0) = 1, exact in bf16, so a row
+// that one key dominates loses nothing to the bf16 rounding of P.  A warp
+// rescales its rows of O~ in TMEM only when one of them moved.  The commit
+// that signals S_t(j) ready also covers PV_t(j-1), so O~_t is stable then.
+//
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the thread
 // records the error, tells the others to stop, and all warps drain what they
 // started (TMA loads, MMAs) before TMEM is freed and the CTA exits.
@@ -39,23 +50,16 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "tmem_regs.h"
 
 namespace ringattn {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kStages = 2;
 constexpr int kTmemCols = 512;
-constexpr int kTmemS0 = 0;    // S buffer 0: columns [0, 128)
-constexpr int kTmemS1 = 128;  // S buffer 1: columns [128, 256)
-constexpr int kTmemO = 256;   // O~: columns [256, 256 + d)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// The reference max follows the running row max exactly (threshold 0): the
-// row's largest weight is then exp2(0) = 1, exact in bf16, so a row that one
-// key dominates loses nothing to the bf16 rounding of P.  (A lazy threshold
-// of 8 halves the rescale work but leaves the dominant weight anywhere in
-// [1, 256) with a bf16 rounding error of up to 2^-9 relative.)
 constexpr float kRescaleThreshold = 0.0f;
 
 // Shared-memory map.  Every tile starts on a 1024-byte boundary (the
@@ -63,24 +67,22 @@ constexpr float kRescaleThreshold = 0.0f;
 template <int D>
 struct Layout {
   static constexpr int kSub = 64;                 // bf16 columns per 128-byte row
-  static constexpr int kQBytes = kTileM * D * 2;  // Q tile
+  static constexpr int kQBytes = kTileM * D * 2;  // one Q tile
   static constexpr int kKBytes = kTileN * D * 2;  // one K tile
   static constexpr int kVBytes = kTileN * D * 2;  // one V tile
-  static constexpr int kPBytes = kTileM * kTileN * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffQ = 0;                 // Q_A, Q_B
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKBytes;
-  static constexpr int kOffP = kOffV + kStages * kVBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
-  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full, o_done, drain
+  static constexpr int kOffBar = kOffV + kStages * kVBytes;
   static constexpr int kBarQFull = 0;
   static constexpr int kBarKFull = 1;
-  static constexpr int kBarVFull = kBarKFull + kStages;
-  static constexpr int kBarKvEmpty = kBarVFull + kStages;
-  static constexpr int kBarSFull = kBarKvEmpty + kStages;
-  static constexpr int kBarPFull = kBarSFull + 2;
-  static constexpr int kBarODone = kBarPFull + 1;
-  static constexpr int kBarDrain = kBarODone + 1;
+  static constexpr int kBarKEmpty = kBarKFull + kStages;
+  static constexpr int kBarVFull = kBarKEmpty + kStages;
+  static constexpr int kBarVEmpty = kBarVFull + kStages;
+  static constexpr int kBarSFull = kBarVEmpty + kStages;  // [2]: tile A, B
+  static constexpr int kBarPFull = kBarSFull + 2;          // [2]
+  static constexpr int kBarOFull = kBarPFull + 2;          // [2]
+  static constexpr int kBarDrain = kBarOFull + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -88,6 +90,9 @@ struct Layout {
   // room to align the base to 1024; at least 120 KB so that only one CTA
   // (the owner of all 512 TMEM columns) is resident per SM
   static constexpr int kAlloc = (kBytes + 1024) > 122880 ? (kBytes + 1024) : 122880;
+  // TMEM columns of tile t
+  __device__ static constexpr uint32_t tmem_s(int t) { return t == 0 ? 0u : 128u; }
+  __device__ static constexpr uint32_t tmem_o(int t) { return t == 0 ? 256u : 256u + D; }
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -152,7 +157,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
-// Wait used only while draining after an abort: bounded, records nothing.
+// Wait used only while draining: bounded, records nothing.
 __device__ __noinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit) {
   const uint64_t t0 = global_timer();
   while (!mbar_try(bar, parity)) {
@@ -207,6 +212,7 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major)
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// D (TMEM) (+)= A (shared memory) x B (shared memory)
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
@@ -217,49 +223,48 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D (TMEM) (+)= A (TMEM: row i in lane i, two bf16 of K per column) x B (shared memory)
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
 
-#define RA_REGS32(x)                                                                                   \
-  "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),      \
-      "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]),        \
-      "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]),      \
-      "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]),      \
-      "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
-#define RA_INREGS32(x)                                                                                  \
-  "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), "r"(x[8]),   \
-      "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15]), "r"(x[16]),   \
-      "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]), "r"(x[22]), "r"(x[23]), "r"(x[24]),  \
-      "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), "r"(x[30]), "r"(x[31])
-#define RA_FIXREGS32(x)                                                                                \
-  "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]), "+r"(x[6]), "+r"(x[7]),      \
-      "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]), "+r"(x[12]), "+r"(x[13]), "+r"(x[14]),        \
-      "+r"(x[15]), "+r"(x[16]), "+r"(x[17]), "+r"(x[18]), "+r"(x[19]), "+r"(x[20]), "+r"(x[21]),      \
-      "+r"(x[22]), "+r"(x[23]), "+r"(x[24]), "+r"(x[25]), "+r"(x[26]), "+r"(x[27]), "+r"(x[28]),      \
-      "+r"(x[29]), "+r"(x[30]), "+r"(x[31])
-
-// 32 consecutive TMEM columns of this thread's lane -> registers.  The wait
-// is in the same asm block so no consumer can be scheduled before it.
+// TMEM -> registers: 32 / 128 consecutive columns of this thread's lane.
+// The wait is in the same asm block, so no consumer runs before it.
 __device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&x)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-      "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
-      "[%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : RA_REGS32(x)
-      : "r"(taddr)
-      : "memory");
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " RA_LD_REGS32 ", [%32];\n\t"
+               "tcgen05.wait::ld.sync.aligned;"
+               : RA_OUT32(x)
+               : "r"(taddr)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_load128(uint32_t taddr, uint32_t (&x)[128]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x128.b32 " RA_LD_REGS128 ", [%128];\n\t"
+               "tcgen05.wait::ld.sync.aligned;"
+               : RA_OUT128(x)
+               : "r"(taddr)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&x)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-      "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, "
-      "%31, %32};" ::"r"(taddr),
-      RA_INREGS32(x)
-      : "memory");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], " RA_ST_REGS32 ";" ::"r"(taddr), RA_IN32(x)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_store64(uint32_t taddr, const uint32_t (&x)[64]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], " RA_ST_REGS64 ";" ::"r"(taddr), RA_IN64(x)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_store_wait() {
@@ -277,66 +282,74 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ------------------------------------------------------------- the kernel
-struct WorkItem {
-  int bh, r, j, t, nk, full_kt, slot;
-  long long delta;
+// ------------------------------------------------------------- work items
+struct Tile {
+  int t;        // query tile index within the shard
+  int nk;       // key tiles to visit
+  int full_kt;  // key tiles [0, full_kt) need no mask
 };
 
+struct WorkItem {
+  int bh, r, j, slot, cls;
+  long long delta;
+  Tile tile[2];
+};
+
+__device__ __forceinline__ Tile tile_work(const StepArgs& a, int cls, long long delta, int t) {
+  Tile w{t, 0, 0};
+  const long long n = a.n;
+  if (t >= a.T || cls == RING_BLOCK_SKIP) return w;
+  const bool ragged = (n % kTileN) != 0;
+  if (cls == RING_BLOCK_FULL) {
+    w.nk = a.KT;
+    w.full_kt = ragged ? a.KT - 1 : a.KT;
+    return w;
+  }
+  const long long i_min = (long long)t * kTileM;
+  const long long i_max = min(n - 1, i_min + kTileM - 1);
+  const long long last_key = i_max + delta;
+  w.nk = last_key < 0 ? 0 : (int)min((long long)a.KT, last_key / kTileN + 1);
+  const long long first_keys = i_min + delta + 1;
+  int full = first_keys <= 0 ? 0 : (int)min((long long)w.nk, first_keys / kTileN);
+  if (ragged && full == a.KT) full = a.KT - 1;
+  w.full_kt = full;
+  return w;
+}
+
+// blockIdx.x -> (shard, head, tile pair).  CTAs of one (shard, head) group
+// are consecutive so the K/V block they share stays in L2; within a group
+// the heaviest pairs (largest u under the causal mask) start first.
 __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   WorkItem w;
+  const int U = (a.T + 1) / 2;
   const int item = blockIdx.x;
-  w.bh = item % a.BH;
-  const int rest = item / a.BH;
-  const int nact = a.fixed_r >= 0 ? 1 : a.n_active;
-  const int slot_in_list = rest % nact;
-  w.t = a.T - 1 - rest / nact;  // heaviest (largest t) tiles first
+  const int u = U - 1 - item % U;
+  const int g = item / U;
+  w.bh = g % a.BH;
+  const int slot_in_list = a.fixed_r >= 0 ? 0 : g / a.BH;
   w.r = a.fixed_r >= 0 ? a.fixed_r : (int)a.active[slot_in_list];
   int j = (w.r - a.step) % a.P;
   if (j < 0) j += a.P;
   w.j = j;
-  // class and diagonal offset (same rule as the host planner)
   const long long n = a.n;
-  int cls;
-  long long delta;
   if (!a.causal) {
-    cls = RING_BLOCK_FULL;
-    delta = n;
+    w.cls = RING_BLOCK_FULL;
+    w.delta = n;
   } else {
-    delta = (a.layout == RING_LAYOUT_STRIPED) ? (j <= w.r ? 0 : -1) : (long long)(w.r - j) * n;
-    cls = delta >= n - 1 ? RING_BLOCK_FULL : (delta <= -n ? RING_BLOCK_SKIP : RING_BLOCK_DIAG);
+    w.delta = (a.layout == RING_LAYOUT_STRIPED) ? (j <= w.r ? 0 : -1) : (long long)(w.r - j) * n;
+    w.cls = w.delta >= n - 1 ? RING_BLOCK_FULL : (w.delta <= -n ? RING_BLOCK_SKIP : RING_BLOCK_DIAG);
   }
-  w.delta = delta;
-  const bool ragged = (n % kTileN) != 0;
-  if (cls == RING_BLOCK_SKIP) {
-    w.nk = 0;
-    w.full_kt = 0;
-  } else if (cls == RING_BLOCK_FULL) {
-    w.nk = a.KT;
-    w.full_kt = ragged ? a.KT - 1 : a.KT;
-  } else {
-    const long long i_min = (long long)w.t * kTileM;
-    const long long i_max = min(n - 1, i_min + kTileM - 1);
-    const long long last_key = i_max + delta;
-    w.nk = last_key < 0 ? 0 : (int)min((long long)a.KT, last_key / kTileN + 1);
-    const long long first_keys = i_min + delta + 1;
-    int full = first_keys <= 0 ? 0 : (int)min((long long)w.nk, first_keys / kTileN);
-    if (ragged && full == a.KT) full = a.KT - 1;
-    w.full_kt = full;
-  }
+  w.tile[0] = tile_work(a, w.cls, w.delta, 2 * u);
+  w.tile[1] = tile_work(a, w.cls, w.delta, 2 * u + 1);
   w.slot = a.kv_mode == kKvSlotR ? w.r : (a.kv_mode == kKvSlotJ ? j : 0);
   return w;
 }
 
+// ------------------------------------------------------------- the kernel
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     block_partial_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ CUtensorMap q_map,
@@ -353,18 +366,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const WorkItem w = decode_item(a);
+  const int nk = max(w.tile[0].nk, w.tile[1].nk);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kBarQFull), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kBarKFull + s), 1);
+      mbar_init(bar(L::kBarKEmpty + s), 1);
       mbar_init(bar(L::kBarVFull + s), 1);
-      mbar_init(bar(L::kBarKvEmpty + s), 1);
+      mbar_init(bar(L::kBarVEmpty + s), 1);
     }
-    mbar_init(bar(L::kBarSFull + 0), 1);
-    mbar_init(bar(L::kBarSFull + 1), 1);
-    mbar_init(bar(L::kBarPFull), 128);
-    mbar_init(bar(L::kBarODone), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::kBarSFull + t), 1);
+      mbar_init(bar(L::kBarPFull + t), 128);
+      mbar_init(bar(L::kBarOFull + t), 1);
+    }
     mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -382,108 +398,127 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int nk = w.nk;
-
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0 && nk > 0) {
-      const uint32_t q_s = sbase + L::kOffQ;
-      mbar_expect_tx(bar(L::kBarQFull), L::kQBytes);
-      const int i0 = w.t * kTileM;
-      for (int c = 0; c < D / L::kSub; ++c) {
-        const uint32_t dst = q_s + c * (kTileM * 128);
-        if (a.q_mode == kQStriped)
-          tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, w.r, i0, w.bh);
-        else if (a.q_mode == kQContiguous)
-          tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, i0, w.r, w.bh);
-        else
-          tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, i0, 0, w.bh);
+      const int ntiles = w.tile[1].nk > 0 ? 2 : 1;
+      mbar_expect_tx(bar(L::kBarQFull), ntiles * L::kQBytes);
+      for (int t = 0; t < ntiles; ++t) {
+        const int i0 = w.tile[t].t * kTileM;
+        for (int c = 0; c < D / L::kSub; ++c) {
+          const uint32_t dst = sbase + L::kOffQ + t * L::kQBytes + c * (kTileM * 128);
+          if (a.q_mode == kQStriped)
+            tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, w.r, i0, w.bh);
+          else if (a.q_mode == kQContiguous)
+            tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, i0, w.r, w.bh);
+          else
+            tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, i0, 0, w.bh);
+        }
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int j = 0; j < nk && ok; ++j) {
         const int st = j % kStages;
-        if (j >= kStages) ok = mbar_wait(bar(L::kBarKvEmpty + st), ((j / kStages) - 1) & 1, abort_flag, a, 1);
+        const uint32_t par = ((j / kStages) - 1) & 1;
+        if (j >= kStages) ok = mbar_wait(bar(L::kBarKEmpty + st), par, abort_flag, a, 1);
         if (!ok) break;
-        const uint32_t k_s = sbase + L::kOffK + st * L::kKBytes;
-        const uint32_t v_s = sbase + L::kOffV + st * L::kVBytes;
         mbar_expect_tx(bar(L::kBarKFull + st), L::kKBytes);
         for (int c = 0; c < D / L::kSub; ++c)
-          tma_load_4d(k_s + c * (kTileN * 128), &k_map, bar(L::kBarKFull + st), c * L::kSub, j * kTileN, w.bh,
-                      w.slot);
+          tma_load_4d(sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), &k_map, bar(L::kBarKFull + st),
+                      c * L::kSub, j * kTileN, w.bh, w.slot);
+        k_issued = j + 1;
+        if (j >= kStages) ok = mbar_wait(bar(L::kBarVEmpty + st), par, abort_flag, a, 2);
+        if (!ok) break;
         mbar_expect_tx(bar(L::kBarVFull + st), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
-          tma_load_4d(v_s + c * (kTileN * 128), &v_map, bar(L::kBarVFull + st), c * L::kSub, j * kTileN, w.bh,
-                      w.slot);
-        issued = j + 1;
+          tma_load_4d(sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), &v_map, bar(L::kBarVFull + st),
+                      c * L::kSub, j * kTileN, w.bh, w.slot);
+        v_issued = j + 1;
       }
       // Drain: every load this thread started has landed before the CTA
       // can exit (normally these waits return at once).
       const unsigned long long lim = a.wait_limit_ns;
       mbar_drain_wait(bar(L::kBarQFull), 0, lim);
-      for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
-        const int st = j % kStages;
-        mbar_drain_wait(bar(L::kBarKFull + st), (j / kStages) & 1, lim);
-        mbar_drain_wait(bar(L::kBarVFull + st), (j / kStages) & 1, lim);
-      }
+      for (int j = (k_issued > kStages ? k_issued - kStages : 0); j < k_issued; ++j)
+        mbar_drain_wait(bar(L::kBarKFull + j % kStages), (j / kStages) & 1, lim);
+      for (int j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
+        mbar_drain_wait(bar(L::kBarVFull + j % kStages), (j / kStages) & 1, lim);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0 && nk > 0) {
       constexpr uint32_t idesc_qk = instr_desc(kTileM, kTileN, false);
       constexpr uint32_t idesc_pv = instr_desc(kTileM, D, true);
-      const uint32_t q_s = sbase + L::kOffQ;
-      const uint32_t p_s = sbase + L::kOffP;
-      bool ok = mbar_wait(bar(L::kBarQFull), 0, abort_flag, a, 2);
-      tc_fence_after();
-      auto issue_pv = [&](int jj) -> bool {
-        const int st = jj % kStages;
-        if (!mbar_wait(bar(L::kBarPFull), jj & 1, abort_flag, a, 3)) return false;
-        if (!mbar_wait(bar(L::kBarVFull + st), (jj / kStages) & 1, abort_flag, a, 4)) return false;
-        tc_fence_after();
-        const uint32_t v_s = sbase + L::kOffV + st * L::kVBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t ad = smem_desc(p_s + (kk / 4) * (kTileM * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(v_s + kk * 2048, kTileN * 128, 1024);
-          mma_bf16(tmem + kTmemO, ad, bd, idesc_pv, (jj > 0 || a.accumulate || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(L::kBarKvEmpty + st));
-        mma_commit(bar(L::kBarODone));
-        return true;
-      };
-      for (int j = 0; j < nk && ok; ++j) {
-        const int st = j % kStages;
-        ok = mbar_wait(bar(L::kBarKFull + st), (j / kStages) & 1, abort_flag, a, 5);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t k_s = sbase + L::kOffK + st * L::kKBytes;
-        const uint32_t s_t = tmem + ((j & 1) ? kTmemS1 : kTmemS0);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t q_s = sbase + L::kOffQ + t * L::kQBytes;
+        const uint32_t k_s = sbase + L::kOffK + (j % kStages) * L::kKBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = smem_desc(q_s + (kk / 4) * (kTileM * 128) + (kk % 4) * 32, 16, 1024);
           const uint64_t bd = smem_desc(k_s + (kk / 4) * (kTileN * 128) + (kk % 4) * 32, 16, 1024);
-          mma_bf16(s_t, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_bf16(tmem + L::tmem_s(t), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::kBarSFull + (j & 1)));
-        if (j > 0) ok = issue_pv(j - 1);
+        mma_commit(bar(L::kBarSFull + t));
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t v_s = sbase + L::kOffV + (j % kStages) * L::kVBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          const uint64_t bd = smem_desc(v_s + kk * 2048, kTileN * 128, 1024);
+          mma_bf16_tmem_a(tmem + L::tmem_o(t), tmem + L::tmem_s(t) + kk * 8, bd, idesc_pv,
+                          (j > 0 || a.accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar(L::kBarQFull), 0, abort_flag, a, 3) &&
+                mbar_wait(bar(L::kBarKFull), 0, abort_flag, a, 4);
+      tc_fence_after();
+      if (ok) {
+        for (int t = 0; t < 2; ++t)
+          if (w.tile[t].nk > 0) issue_s(t, 0);
+        mma_commit(bar(L::kBarKEmpty + 0));
       }
-      if (ok) issue_pv(nk - 1);
+      for (int j = 0; j < nk && ok; ++j) {
+        const int st = j % kStages;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= w.tile[t].nk) continue;
+          ok = mbar_wait(bar(L::kBarPFull + t), j & 1, abort_flag, a, 5) &&
+               mbar_wait(bar(L::kBarVFull + st), (j / kStages) & 1, abort_flag, a, 6);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < w.tile[t].nk) {
+            ok = mbar_wait(bar(L::kBarKFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag, a, 7);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(t, j + 1);
+          } else {
+            mma_commit(bar(L::kBarOFull + t));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(L::kBarVEmpty + st));
+        if (j + 1 < nk) mma_commit(bar(L::kBarKEmpty + (j + 1) % kStages));
+      }
       // Drain: all MMAs this thread issued are complete before TMEM is freed.
       mma_commit(bar(L::kBarDrain));
       mbar_drain_wait(bar(L::kBarDrain), 0, a.wait_limit_ns);
     }
   } else {
     // -------------------------------------------- softmax and epilogue
+    const int t = (warp - 2) / 4;  // 0: tile A (warps 2-5), 1: tile B (warps 6-9)
+    const Tile tw = w.tile[t];
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const long long i = (long long)w.t * kTileM + row;
+    const long long i = (long long)tw.t * kTileM + row;
     const bool valid = i < a.n;
-    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const bool in_range = tw.t < a.T;  // the tile exists (its rows may still be partly past n)
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + L::tmem_s(t);
+    const uint32_t o_addr = tmem + lane_off + L::tmem_o(t);
     const long long g = (long long)w.bh * a.row_bh + (long long)w.r * a.row_r + i * a.row_i;
     float m2 = -INFINITY;  // reference max, log2 domain
     float l = 0.0f;
-    if (a.accumulate) {
+    if (a.accumulate && in_range) {
       if (valid) {
         m2 = a.m_state[g] * kLog2e;
         l = a.l_state[g];
@@ -500,28 +535,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[q4 * 4 + 2] = __float_as_uint(v.z);
           x[q4 * 4 + 3] = __float_as_uint(v.w);
         }
-        tmem_store32(lane_base + kTmemO + c * 32, x);
+        tmem_store32(o_addr + c * 32, x);
       }
       tmem_store_wait();
     }
     bool ok = true;
-    const uint32_t p_s = sbase + L::kOffP;
-    for (int j = 0; j < nk; ++j) {
-      ok = warp_wait(bar(L::kBarSFull + (j & 1)), (j >> 1) & 1, abort_flag, a, 6);
+    for (int j = 0; j < tw.nk; ++j) {
+      ok = warp_wait(bar(L::kBarSFull + t), j & 1, abort_flag, a, 8);
       if (!ok) break;
       tc_fence_after();
       float s[kTileN];
       {
-        const uint32_t s_t = lane_base + ((j & 1) ? kTmemS1 : kTmemS0);
+        uint32_t x[kTileN];
+        tmem_load128(s_addr, x);
 #pragma unroll
-        for (int c = 0; c < kTileN / 32; ++c) {
-          uint32_t x[32];
-          tmem_load32(s_t + c * 32, x);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(x[e]);
-        }
+        for (int e = 0; e < kTileN; ++e) s[e] = __uint_as_float(x[e]);
       }
-      if (j >= w.full_kt) {
+      if (j >= tw.full_kt) {
         const long long kbase = (long long)j * kTileN;
 #pragma unroll
         for (int e = 0; e < kTileN; ++e) {
@@ -529,69 +559,61 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (key >= a.n || key - i > w.delta) s[e] = -INFINITY;
         }
       }
-      float mx = -INFINITY;
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < kTileN; ++e) mx = fmaxf(mx, s[e]);
-      const float m_tile = mx * a.scale_log2;
+      for (int e = 0; e < kTileN; e += 4) {
+        mx0 = fmaxf(mx0, s[e]);
+        mx1 = fmaxf(mx1, s[e + 1]);
+        mx2 = fmaxf(mx2, s[e + 2]);
+        mx3 = fmaxf(mx3, s[e + 3]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
       const bool need = m_tile > m2 + kRescaleThreshold;
       const float m_new = need ? m_tile : m2;
       const float alpha = need ? fast_exp2(m2 - m_new) : 1.0f;
       const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
       // P is rounded to bf16 (the PV operand); l sums the fp32 values.
-      float rowsum = 0.0f;
       uint32_t pb[kTileN / 2];
+      float sum0 = 0.0f, sum1 = 0.0f;
 #pragma unroll
       for (int e = 0; e < kTileN; e += 2) {
         const float p0 = fast_exp2(fmaf(s[e], a.scale_log2, -m_use));
         const float p1 = fast_exp2(fmaf(s[e + 1], a.scale_log2, -m_use));
         pb[e / 2] = pack_bf16(p0, p1);
-        rowsum += p0 + p1;
+        sum0 += p0;
+        sum1 += p1;
       }
-      l = l * alpha + rowsum;
+      l = l * alpha + (sum0 + sum1);
       m2 = m_new;
-      if (j > 0) {
-        ok = warp_wait(bar(L::kBarODone), (j - 1) & 1, abort_flag, a, 7);
-        if (!ok) break;
-        tc_fence_after();
-      }
+      tmem_store64(s_addr, pb);  // P_t over the first 64 columns of S_t
       if ((j > 0 || a.accumulate) && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t x[32];
-          tmem_load32(lane_base + kTmemO + c * 32, x);
+          tmem_load32(o_addr + c * 32, x);
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
-          tmem_store32(lane_base + kTmemO + c * 32, x);
+          tmem_store32(o_addr + c * 32, x);
         }
-        tmem_store_wait();
       }
-      // P (bf16) -> shared memory, K-major with the 128-byte swizzle:
-      // keys [64h, 64h+64) form sub-tile h; 16-byte chunk c of row `row`
-      // sits at chunk position c ^ (row & 7).
-#pragma unroll
-      for (int c = 0; c < kTileN / 8; ++c) {
-        const uint32_t sub = p_s + (c / 8) * (kTileM * 128) + row * 128;
-        const uint32_t addr = sub + (((c % 8) ^ (row & 7)) << 4);
-        st_shared_v4(addr, pb[c * 4 + 0], pb[c * 4 + 1], pb[c * 4 + 2], pb[c * 4 + 3]);
-      }
-      fence_async_smem();
+      tmem_store_wait();
       tc_fence_before();
-      mbar_arrive(bar(L::kBarPFull));
+      mbar_arrive(bar(L::kBarPFull + t));
     }
-    if (ok && nk > 0) {
-      ok = warp_wait(bar(L::kBarODone), (nk - 1) & 1, abort_flag, a, 8);
+    if (ok && tw.nk > 0) {
+      ok = warp_wait(bar(L::kBarOFull + t), 0, abort_flag, a, 9);
       tc_fence_after();
     }
-    if (ok) {
+    if (ok && in_range) {
       // ------------------------------------------------------ epilogue
-      const bool have_o = nk > 0 || a.accumulate;
+      const bool have_o = tw.nk > 0 || a.accumulate;
       if (a.finalize) {
         const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
         float4* dst = reinterpret_cast<float4*>(a.out + g * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t x[32];
-          if (have_o) tmem_load32(lane_base + kTmemO + c * 32, x);
+          if (have_o) tmem_load32(o_addr + c * 32, x);
           if (valid) {
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
@@ -610,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t x[32];
-          if (have_o) tmem_load32(lane_base + kTmemO + c * 32, x);
+          if (have_o) tmem_load32(o_addr + c * 32, x);
           if (valid) {
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
@@ -656,6 +678,8 @@ int prepare_block_partial_kernels() {
   if (e) return e;
   return prepare_one<128>();
 }
+
+int block_partial_grid(int T, int n_active, int BH) { return ((T + 1) / 2) * n_active * BH; }
 
 int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map, const void* v_map, int d,
                          int grid, void* stream) {

@@ -188,7 +188,7 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
     a.finalize = s == P - 1 ? 1 : 0;
     a.n_active = (int)act.size();
     for (size_t x = 0; x < act.size(); ++x) a.active[x] = act[x];
-    e = (cudaError_t)launch_block_partial(a, qm, km, vm, p.d, p.T * a.n_active * BH, cs);
+    e = (cudaError_t)launch_block_partial(a, qm, km, vm, p.d, block_partial_grid(p.T, a.n_active, BH), cs);
     if (e != cudaSuccess) return cuda_error(e, "step kernel launch");
   }
   if (status) {

@@ -110,6 +110,8 @@ int tensor_map_4d(void* map, const void* base, const unsigned long long dims[4],
 const Plan& handle_plan(const ring_attn* h);
 unsigned long long handle_wait_limit(const ring_attn* h);
 int block_partial_smem_bytes(int d);
+// CTAs of one block-partial launch: one per (pair of query tiles, shard, head).
+int block_partial_grid(int T, int n_active, int BH);
 int prepare_block_partial_kernels();
 
 }  // namespace ringattn
