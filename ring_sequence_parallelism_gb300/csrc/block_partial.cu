@@ -239,6 +239,102 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// Fused MMA issue.  One asm block issues a whole K loop from the elected lane
+// of a converged warp; the descriptors keep their high words and advance the
+// 14-bit start-address field of the low word (16-byte units) per K step.
+// Issuing MMAs one asm statement at a time, with the descriptor arithmetic
+// left to the compiler, measured about three times slower per instruction
+// than the tensor core's own rate on this part.
+//
+// S (+)= Q K^T, both operands K-major with the 128-byte swizzle: K steps of
+// 16 elements are +32 bytes within a 64-column sub-tile and +16 KB
+// (kTileM/kTileN rows x 128 B) to the next sub-tile.
+template <int D>
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc);
+template <>
+__device__ __forceinline__ void mma_qk<128>(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 0;\n\t"
+      "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "add.u32 al, %1, 1024;\n\tadd.u32 bl, %3, 1024;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "add.u32 al, %1, 1026;\n\tadd.u32 bl, %3, 1026;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "add.u32 al, %1, 1028;\n\tadd.u32 bl, %3, 1028;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "add.u32 al, %1, 1030;\n\tadd.u32 bl, %3, 1030;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"((uint32_t)a_desc), "r"((uint32_t)(a_desc >> 32)), "r"((uint32_t)b_desc),
+      "r"((uint32_t)(b_desc >> 32)), "r"(idesc)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_qk<64>(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 0;\n\t"
+      "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\tmov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, 1;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"((uint32_t)a_desc), "r"((uint32_t)(a_desc >> 32)), "r"((uint32_t)b_desc),
+      "r"((uint32_t)(b_desc >> 32)), "r"(idesc)
+      : "memory");
+}
+
+// O~ (+)= P V: P from TMEM (8 columns of bf16 pairs per K step of 16 keys),
+// V MN-major with the 128-byte swizzle (+2 KB = 16 key rows per K step).
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 at, bl;\n\t.reg .b64 bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %5, p;\n\t"
+      "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, 128;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %5, 1;\n\t"
+      "add.u32 at, %1, 16;\n\tadd.u32 bl, %2, 256;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %5, 1;\n\t"
+      "add.u32 at, %1, 24;\n\tadd.u32 bl, %2, 384;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %5, 1;\n\t"
+      "add.u32 at, %1, 32;\n\tadd.u32 bl, %2, 512;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %5, 1;\n\t"
+      "add.u32 at, %1, 40;\n\tadd.u32 bl, %2, 640;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %5, 1;\n\t"
+      "add.u32 at, %1, 48;\n\tadd.u32 bl, %2, 768;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %5, 1;\n\t"
+      "add.u32 at, %1, 56;\n\tadd.u32 bl, %2, 896;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %5, 1;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(p_tmem), "r"((uint32_t)b_desc), "r"((uint32_t)(b_desc >> 32)), "r"(0u), "r"(idesc),
+      "r"(accumulate)
+      : "memory");
+}
+
+// tcgen05.commit from the elected lane (the lane that issued the MMAs).
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
 // TMEM -> registers: 32 / 128 consecutive columns of this thread's lane.
 // The wait is in the same asm block, so no consumer runs before it.
 __device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&x)[32]) {
@@ -267,8 +363,51 @@ __device__ __forceinline__ void tmem_store64(uint32_t taddr, const uint32_t (&x)
                : "memory");
 }
 
+__device__ __forceinline__ void tmem_load64(uint32_t taddr, uint32_t (&x)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 " RA_LD_REGS64 ", [%64];\n\t"
+               "tcgen05.wait::ld.sync.aligned;"
+               : RA_OUT64(x)
+               : "r"(taddr)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_store128(uint32_t taddr, const uint32_t (&x)[128]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x128.b32 [%0], " RA_ST_REGS128 ";" ::"r"(taddr), RA_IN128(x)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_store_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic: one instruction, two lanes of work).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -446,67 +585,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0 && nk > 0) {
+    // The whole warp runs this loop (every lane waits on the barriers);
+    // one elected lane issues the MMAs and commits.
+    if (nk > 0) {
       constexpr uint32_t idesc_qk = instr_desc(kTileM, kTileN, false);
       constexpr uint32_t idesc_pv = instr_desc(kTileM, D, true);
       auto issue_s = [&](int t, int j) {
         const uint32_t q_s = sbase + L::kOffQ + t * L::kQBytes;
         const uint32_t k_s = sbase + L::kOffK + (j % kStages) * L::kKBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = smem_desc(q_s + (kk / 4) * (kTileM * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(k_s + (kk / 4) * (kTileN * 128) + (kk % 4) * 32, 16, 1024);
-          mma_bf16(tmem + L::tmem_s(t), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kBarSFull + t));
+        mma_qk<D>(tmem + L::tmem_s(t), smem_desc(q_s, 16, 1024), smem_desc(k_s, 16, 1024), idesc_qk);
+        mma_commit_elect(bar(L::kBarSFull + t));
       };
       auto issue_pv = [&](int t, int j) {
         const uint32_t v_s = sbase + L::kOffV + (j % kStages) * L::kVBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t bd = smem_desc(v_s + kk * 2048, kTileN * 128, 1024);
-          mma_bf16_tmem_a(tmem + L::tmem_o(t), tmem + L::tmem_s(t) + kk * 8, bd, idesc_pv,
-                          (j > 0 || a.accumulate || kk > 0) ? 1u : 0u);
-        }
+        mma_pv(tmem + L::tmem_o(t), tmem + L::tmem_s(t), smem_desc(v_s, kTileN * 128, 1024), idesc_pv,
+               (j > 0 || a.accumulate) ? 1u : 0u);
       };
-      bool ok = mbar_wait(bar(L::kBarQFull), 0, abort_flag, a, 3) &&
-                mbar_wait(bar(L::kBarKFull), 0, abort_flag, a, 4);
+      bool ok = warp_wait(bar(L::kBarQFull), 0, abort_flag, a, 3) &&
+                warp_wait(bar(L::kBarKFull), 0, abort_flag, a, 4);
       tc_fence_after();
       if (ok) {
-        for (int t = 0; t < 2; ++t)
-          if (w.tile[t].nk > 0) issue_s(t, 0);
-        mma_commit(bar(L::kBarKEmpty + 0));
+        if (w.tile[0].nk > 0) issue_s(0, 0);
+        if (w.tile[1].nk > 0) issue_s(1, 0);
+        mma_commit_elect(bar(L::kBarKEmpty + 0));
       }
+      const int nk_t[2] = {w.tile[0].nk, w.tile[1].nk};
       for (int j = 0; j < nk && ok; ++j) {
         const int st = j % kStages;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= w.tile[t].nk) continue;
-          ok = mbar_wait(bar(L::kBarPFull + t), j & 1, abort_flag, a, 5) &&
-               mbar_wait(bar(L::kBarVFull + st), (j / kStages) & 1, abort_flag, a, 6);
-          if (!ok) break;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || j >= nk_t[t]) continue;
+          ok = warp_wait(bar(L::kBarPFull + t), j & 1, abort_flag, a, 5) &&
+               warp_wait(bar(L::kBarVFull + st), (j / kStages) & 1, abort_flag, a, 6);
+          if (!ok) continue;
           tc_fence_after();
           issue_pv(t, j);
-          if (j + 1 < w.tile[t].nk) {
-            ok = mbar_wait(bar(L::kBarKFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag, a, 7);
-            if (!ok) break;
+          if (j + 1 < nk_t[t]) {
+            ok = warp_wait(bar(L::kBarKFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag, a, 7);
+            if (!ok) continue;
             tc_fence_after();
             issue_s(t, j + 1);
           } else {
-            mma_commit(bar(L::kBarOFull + t));
+            mma_commit_elect(bar(L::kBarOFull + t));
           }
         }
         if (!ok) break;
-        mma_commit(bar(L::kBarVEmpty + st));
-        if (j + 1 < nk) mma_commit(bar(L::kBarKEmpty + (j + 1) % kStages));
+        mma_commit_elect(bar(L::kBarVEmpty + st));
+        if (j + 1 < nk) mma_commit_elect(bar(L::kBarKEmpty + (j + 1) % kStages));
       }
-      // Drain: all MMAs this thread issued are complete before TMEM is freed.
-      mma_commit(bar(L::kBarDrain));
+      // Drain: all MMAs this warp issued are complete before TMEM is freed.
+      mma_commit_elect(bar(L::kBarDrain));
       mbar_drain_wait(bar(L::kBarDrain), 0, a.wait_limit_ns);
     }
   } else {
     // -------------------------------------------- softmax and epilogue
     const int t = (warp - 2) / 4;  // 0: tile A (warps 2-5), 1: tile B (warps 6-9)
-    const Tile tw = w.tile[t];
+    const Tile tw = t == 0 ? w.tile[0] : w.tile[1];
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const long long i = (long long)tw.t * kTileM + row;
@@ -559,42 +693,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (key >= a.n || key - i > w.delta) s[e] = -INFINITY;
         }
       }
+      // row max: four chains of 3-input max
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < kTileN; e += 4) {
-        mx0 = fmaxf(mx0, s[e]);
-        mx1 = fmaxf(mx1, s[e + 1]);
-        mx2 = fmaxf(mx2, s[e + 2]);
-        mx3 = fmaxf(mx3, s[e + 3]);
+      for (int e = 0; e < kTileN; e += 8) {
+        mx0 = fmax3(mx0, s[e], s[e + 1]);
+        mx1 = fmax3(mx1, s[e + 2], s[e + 3]);
+        mx2 = fmax3(mx2, s[e + 4], s[e + 5]);
+        mx3 = fmax3(mx3, s[e + 6], s[e + 7]);
       }
       const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
       const bool need = m_tile > m2 + kRescaleThreshold;
       const float m_new = need ? m_tile : m2;
       const float alpha = need ? fast_exp2(m2 - m_new) : 1.0f;
       const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-      // P is rounded to bf16 (the PV operand); l sums the fp32 values.
+      // p = exp2(s * scale - m): pairs through one packed FMA, two MUFU ex2,
+      // one bf16x2 convert (the PV operand) and one packed add into four
+      // independent fp32 pair sums (l sums the fp32 values).
+      const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
+      const uint64_t nm2 = f2(-m_use, -m_use);
+      uint64_t acc[4] = {0, 0, 0, 0};
       uint32_t pb[kTileN / 2];
-      float sum0 = 0.0f, sum1 = 0.0f;
 #pragma unroll
       for (int e = 0; e < kTileN; e += 2) {
-        const float p0 = fast_exp2(fmaf(s[e], a.scale_log2, -m_use));
-        const float p1 = fast_exp2(fmaf(s[e + 1], a.scale_log2, -m_use));
+        float t0, t1;
+        unf2(ffma2(f2(s[e], s[e + 1]), sc2, nm2), t0, t1);
+        const float p0 = fast_exp2(t0);
+        const float p1 = fast_exp2(t1);
         pb[e / 2] = pack_bf16(p0, p1);
-        sum0 += p0;
-        sum1 += p1;
+        acc[(e / 2) & 3] = fadd2(acc[(e / 2) & 3], f2(p0, p1));
       }
-      l = l * alpha + (sum0 + sum1);
+      float r0, r1, r2, r3;
+      unf2(fadd2(acc[0], acc[1]), r0, r1);
+      unf2(fadd2(acc[2], acc[3]), r2, r3);
+      l = l * alpha + ((r0 + r1) + (r2 + r3));
       m2 = m_new;
       tmem_store64(s_addr, pb);  // P_t over the first 64 columns of S_t
       if ((j > 0 || a.accumulate) && __any_sync(0xffffffffu, need)) {
+        const uint64_t al2 = f2(alpha, alpha);
+        uint32_t x[D];
+        if constexpr (D == 128) tmem_load128(o_addr, x);
+        else tmem_load64(o_addr, x);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t x[32];
-          tmem_load32(o_addr + c * 32, x);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
-          tmem_store32(o_addr + c * 32, x);
+        for (int e = 0; e < D; e += 2) {
+          float o0, o1;
+          unf2(fmul2(f2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), al2), o0, o1);
+          x[e] = __float_as_uint(o0);
+          x[e + 1] = __float_as_uint(o1);
         }
+        if constexpr (D == 128) tmem_store128(o_addr, x);
+        else tmem_store64(o_addr, x);
       }
       tmem_store_wait();
       tc_fence_before();
