@@ -601,9 +601,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_pv(tmem + L::tmem_o(t), tmem + L::tmem_s(t), smem_desc(v_s, kTileN * 128, 1024), idesc_pv,
                (j > 0 || a.accumulate) ? 1u : 0u);
       };
+      // Waits on TMA data (Q, K, V) need no tcgen05 fence: the mbarrier's
+      // transaction count completes only after the bytes are in shared
+      // memory.  Only the wait for P (written to TMEM by the softmax warps)
+      // is followed by tcgen05.fence::after_thread_sync; a fence issued right
+      // after commits measured ~125 cycles of tensor-pipe bubble.
       bool ok = warp_wait(bar(L::kBarQFull), 0, abort_flag, a, 3) &&
                 warp_wait(bar(L::kBarKFull), 0, abort_flag, a, 4);
-      tc_fence_after();
       if (ok) {
         if (w.tile[0].nk > 0) issue_s(0, 0);
         if (w.tile[1].nk > 0) issue_s(1, 0);
@@ -615,15 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || j >= nk_t[t]) continue;
-          ok = warp_wait(bar(L::kBarPFull + t), j & 1, abort_flag, a, 5) &&
-               warp_wait(bar(L::kBarVFull + st), (j / kStages) & 1, abort_flag, a, 6);
+          ok = warp_wait(bar(L::kBarVFull + st), (j / kStages) & 1, abort_flag, a, 6) &&
+               warp_wait(bar(L::kBarPFull + t), j & 1, abort_flag, a, 5);
           if (!ok) continue;
           tc_fence_after();
           issue_pv(t, j);
           if (j + 1 < nk_t[t]) {
             ok = warp_wait(bar(L::kBarKFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag, a, 7);
             if (!ok) continue;
-            tc_fence_after();
             issue_s(t, j + 1);
           } else {
             mma_commit_elect(bar(L::kBarOFull + t));
@@ -693,16 +696,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (key >= a.n || key - i > w.delta) s[e] = -INFINITY;
         }
       }
-      // row max: four chains of 3-input max
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      // row max: eight independent chains of 3-input max, then a tree
+      float mx[8];
 #pragma unroll
-      for (int e = 0; e < kTileN; e += 8) {
-        mx0 = fmax3(mx0, s[e], s[e + 1]);
-        mx1 = fmax3(mx1, s[e + 2], s[e + 3]);
-        mx2 = fmax3(mx2, s[e + 4], s[e + 5]);
-        mx3 = fmax3(mx3, s[e + 6], s[e + 7]);
+      for (int c = 0; c < 8; ++c) mx[c] = fmaxf(s[2 * c], s[2 * c + 1]);
+#pragma unroll
+      for (int e = 16; e < kTileN; e += 16) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mx[c] = fmax3(mx[c], s[e + 2 * c], s[e + 2 * c + 1]);
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
+      const float m_tile =
+          fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) * a.scale_log2;
       const bool need = m_tile > m2 + kRescaleThreshold;
       const float m_new = need ? m_tile : m2;
       const float alpha = need ? fast_exp2(m2 - m_new) : 1.0f;
