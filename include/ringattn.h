@@ -89,7 +89,13 @@ typedef enum {
    * ring_attn_fwd so ring_attn_get_timing can report them.  Default 0. */
   RING_OPT_TIMING = 1,
   /* Upper bound, in nanoseconds, of every device-side wait.  Default 2e9. */
-  RING_OPT_WAIT_LIMIT_NS = 2
+  RING_OPT_WAIT_LIMIT_NS = 2,
+  /* Test hook, default 0.  1: the step kernels issue no loads of V tiles,
+   * so the first wait for a V tile runs out after RING_OPT_WAIT_LIMIT_NS;
+   * the kernel then drains what it started, frees its tensor memory and
+   * returns, and ring_attn_check reports RING_ERR_TIMEOUT.  The outputs of
+   * such a call are undefined.  Exists to test the bounded-wait error path. */
+  RING_OPT_DEBUG_DROP_V_LOADS = 3
 } ring_option_t;
 
 /* Create a handle for one problem shape.  Validates the shape and builds the

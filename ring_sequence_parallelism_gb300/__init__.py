@@ -17,7 +17,8 @@ import ctypes
 
 from . import _lib
 from ._lib import (RING_BLOCK_DIAG, RING_BLOCK_FULL, RING_BLOCK_SKIP, RING_LAYOUT_CONTIGUOUS,  # noqa: F401
-                   RING_LAYOUT_STRIPED, RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_WAIT_LIMIT_NS,
+                   RING_LAYOUT_STRIPED, RING_OPT_DEBUG_DROP_V_LOADS, RING_OPT_ROTATION, RING_OPT_TIMING,
+                   RING_OPT_WAIT_LIMIT_NS,
                    RingAttnError, RingState)
 
 LAYOUTS = {"contiguous": RING_LAYOUT_CONTIGUOUS, "striped": RING_LAYOUT_STRIPED}

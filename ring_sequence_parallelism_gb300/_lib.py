@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "RING_OK", -1: "RING_ERR_INVALID_ARG", -2: "RING_ERR_UNSUPPOR
 RING_LAYOUT_CONTIGUOUS = 0
 RING_LAYOUT_STRIPED = 1
 RING_BLOCK_SKIP, RING_BLOCK_FULL, RING_BLOCK_DIAG = 0, 1, 2
-RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_WAIT_LIMIT_NS = 0, 1, 2
+RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_WAIT_LIMIT_NS, RING_OPT_DEBUG_DROP_V_LOADS = 0, 1, 2, 3
 
 # Every symbol include/ringattn.h declares, with (restype, argtypes).
 _vp = ctypes.c_void_p

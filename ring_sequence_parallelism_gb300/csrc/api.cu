@@ -102,6 +102,7 @@ struct ring_attn {
   Plan plan;
   int rotation = 1;
   int timing = 0;
+  int debug_drop_v = 0;
   unsigned long long wait_limit_ns = 2000000000ULL;
   // device resources, made on first use
   bool ready = false;
@@ -179,6 +180,7 @@ StepArgs base_args(const ring_attn* h) {
   a.layout = p.layout;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
   a.fixed_r = -1;
+  a.debug_drop_v = h->debug_drop_v;
   return a;
 }
 
@@ -276,6 +278,10 @@ int ring_attn_set_option(ring_attn_t h, int option, long long value) {
     case RING_OPT_WAIT_LIMIT_NS:
       if (value <= 0) return fail(RING_ERR_INVALID_ARG, "wait limit must be positive");
       h->wait_limit_ns = (unsigned long long)value;
+      return RING_OK;
+    case RING_OPT_DEBUG_DROP_V_LOADS:
+      if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "debug option must be 0 or 1");
+      h->debug_drop_v = (int)value;
       return RING_OK;
     default:
       return fail(RING_ERR_INVALID_ARG, "unknown option");

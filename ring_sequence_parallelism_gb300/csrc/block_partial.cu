@@ -568,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         k_issued = j + 1;
         if (j >= kStages) ok = mbar_wait(bar(L::kBarVEmpty + st), par, abort_flag, a, 2);
         if (!ok) break;
+        if (a.debug_drop_v) continue;  // test hook: nothing ever completes v_full
         mbar_expect_tx(bar(L::kBarVFull + st), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), &v_map, bar(L::kBarVFull + st),

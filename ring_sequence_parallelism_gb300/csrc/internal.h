@@ -80,6 +80,7 @@ struct StepArgs {
   int finalize;    // write out/lse instead of the state
   int n_active;    // shards in `active`
   int fixed_r;     // >= 0: single shard (block partial); ignores `active`
+  int debug_drop_v;  // test hook: issue no V loads (see RING_OPT_DEBUG_DROP_V_LOADS)
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned short active[kMaxShards];
 };
