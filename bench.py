@@ -59,6 +59,25 @@ def dist_env():
         os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank's time).
+    Uses the process group's backend: a CUDA tensor for nccl, CPU for gloo."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank_step: float, ms_max: float) -> float:
+    """Work of all ranks (each runs one replica of the step) over the slowest rank's time."""
+    return world * flops_per_rank_step / (ms_max * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -275,13 +294,10 @@ def run_ours(args, w):
     kernel_ms, copy_ms, wait_ms, pack_ms = t["kernel_ms"], t["copy_ms"], t["wait_ms"], t["pack_ms"]
     att.check()
     ms = e0.elapsed_time(e1) / args.steps
-    ms_t = torch.tensor([ms], device="cuda")
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, world)
 
     flops = w.flops()
-    value = world * flops / (ms_max * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms_max)
     tokens_s = world * w.B * w.N / (ms_max * 1e-3)
     pk, pk_kind = peaks()
 
@@ -307,12 +323,9 @@ def run_ours(args, w):
             att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
         f1.record(stream)
         barrier()
-        e2e_ms = f0.elapsed_time(f1) / args.steps
-        et = torch.tensor([e2e_ms], device="cuda")
-        if world > 1:
-            dist.all_reduce(et, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * flops / (float(et.item()) * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "ms_per_step": float(et.item()),
+        e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, world)
+        e2e = {"value": whole_job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h)),
                "d2h_bytes_per_step": out_h.numel() * 4 + lse_h.numel() * 4}
 
