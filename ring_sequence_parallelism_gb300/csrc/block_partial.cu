@@ -421,6 +421,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 256-bit global accesses (8 fp32): one full 32-byte sector per lane.
+__device__ __forceinline__ void ld_global_v8(const float* p, uint32_t* x) {
+  asm volatile("ld.global.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st_global_v8(float* p, const float* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+               "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -661,17 +673,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         m2 = a.m_state[g] * kLog2e;
         l = a.l_state[g];
       }
-      const float4* src = reinterpret_cast<const float4*>(a.o_state + g * D);
+      const float* src = a.o_state + g * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t x[32];
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          float4 v = valid ? src[c * 8 + q4] : make_float4(0.f, 0.f, 0.f, 0.f);
-          x[q4 * 4 + 0] = __float_as_uint(v.x);
-          x[q4 * 4 + 1] = __float_as_uint(v.y);
-          x[q4 * 4 + 2] = __float_as_uint(v.z);
-          x[q4 * 4 + 3] = __float_as_uint(v.w);
+        for (int q8 = 0; q8 < 4; ++q8) {
+          if (valid) {
+            ld_global_v8(src + c * 32 + q8 * 8, x + q8 * 8);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[q8 * 8 + e] = 0u;
+          }
         }
         tmem_store32(o_addr + c * 32, x);
       }
@@ -762,39 +775,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool have_o = tw.nk > 0 || a.accumulate;
       if (a.finalize) {
         const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
-        float4* dst = reinterpret_cast<float4*>(a.out + g * D);
+        float* dst = a.out + g * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t x[32];
           if (have_o) tmem_load32(o_addr + c * 32, x);
           if (valid) {
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              float4 v;
-              v.x = have_o ? __uint_as_float(x[q4 * 4 + 0]) * inv_l : 0.0f;
-              v.y = have_o ? __uint_as_float(x[q4 * 4 + 1]) * inv_l : 0.0f;
-              v.z = have_o ? __uint_as_float(x[q4 * 4 + 2]) * inv_l : 0.0f;
-              v.w = have_o ? __uint_as_float(x[q4 * 4 + 3]) * inv_l : 0.0f;
-              dst[c * 8 + q4] = v;
+            for (int q8 = 0; q8 < 4; ++q8) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = have_o ? __uint_as_float(x[q8 * 8 + e]) * inv_l : 0.0f;
+              st_global_v8(dst + c * 32 + q8 * 8, v);
             }
           }
         }
         if (valid) a.lse[g] = (l > 0.0f) ? (m2 + __log2f(l)) * kLn2 : -INFINITY;
       } else {
-        float4* dst = reinterpret_cast<float4*>(a.o_state + g * D);
+        float* dst = a.o_state + g * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t x[32];
           if (have_o) tmem_load32(o_addr + c * 32, x);
           if (valid) {
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              float4 v;
-              v.x = have_o ? __uint_as_float(x[q4 * 4 + 0]) : 0.0f;
-              v.y = have_o ? __uint_as_float(x[q4 * 4 + 1]) : 0.0f;
-              v.z = have_o ? __uint_as_float(x[q4 * 4 + 2]) : 0.0f;
-              v.w = have_o ? __uint_as_float(x[q4 * 4 + 3]) : 0.0f;
-              dst[c * 8 + q4] = v;
+            for (int q8 = 0; q8 < 4; ++q8) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = have_o ? __uint_as_float(x[q8 * 8 + e]) : 0.0f;
+              st_global_v8(dst + c * 32 + q8 * 8, v);
             }
           }
         }
