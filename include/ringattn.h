@@ -81,9 +81,16 @@ typedef struct {
 
 /* Options for ring_attn_set_option. */
 typedef enum {
-  /* 1 (default): ring_attn_fwd rotates K/V through the double buffer with
-   * device-to-device copies on a side stream.  0: every step reads its block
-   * straight from the packed buffer (no copies; for measuring their cost). */
+  /* How ring_attn_fwd moves each K/V block to the next shard between steps
+   * (every shard sends its block to shard r+1 through a double buffer).
+   * 2 (default): the step kernel sends it: the CTAs store the key/value tiles
+   *   they have loaded into slot r+1 of the other buffer (TMA stores from
+   *   shared memory); only the slots of shards with no work at that step
+   *   (skipped causal blocks) are copied on a side stream.
+   * 1: device-to-device copies of the whole buffer on a side stream.
+   * 0: no movement; every step reads its block straight from the packed
+   *   buffer (for measuring the cost of the other two).
+   * All three give bit-identical results. */
   RING_OPT_ROTATION = 0,
   /* 1: record CUDA events around every pack, copy and step kernel of
    * ring_attn_fwd so ring_attn_get_timing can report them.  Default 0. */

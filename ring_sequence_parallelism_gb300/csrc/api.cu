@@ -15,7 +15,21 @@
 //   ...
 // rotate(src): dst slot r <- src slot (r - 1) mod P, i.e. every shard sends
 // its block to shard r + 1 and receives from r - 1 ([GRA] "One lap around
-// the ring"), as two cudaMemcpyAsync device-to-device copies per tensor.
+// the ring").
+//
+// Rotation modes (RING_OPT_ROTATION):
+//   2 (default) the step kernel sends: each CTA stores the key/value tiles on
+//     its diagonal from shared memory into slot r+1 of the other buffer, so
+//     every block a step computes on is also moved by that step.  Only the
+//     slots of shards with no work at step s (skipped causal blocks) are
+//     copied, with cudaMemcpyAsync on the side stream:
+//       side stream:    wait released[s-1]; copy those slots;  record landed[s+1]
+//       compute stream: wait landed[s+1] before step s+1 (only if copied).
+//     The kernel reads buffer s&1 and writes the other one, so kernels in
+//     stream order need no events between them.
+//   1 two cudaMemcpyAsync device-to-device copies per tensor per step on the
+//     side stream (the schedule above).
+//   0 no rotation: every step reads its block straight from the packed buffer.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -100,7 +114,7 @@ int tensor_map_4d(void* map, const void* base, const unsigned long long dims[4],
 
 struct ring_attn {
   Plan plan;
-  int rotation = 1;
+  int rotation = 2;
   int timing = 0;
   int debug_drop_v = 0;
   unsigned long long wait_limit_ns = 2000000000ULL;
@@ -111,6 +125,7 @@ struct ring_attn {
   cudaEvent_t packed = nullptr;
   std::vector<cudaEvent_t> landed, released;
   std::vector<cudaEvent_t> tk0, tk1, tc0, tc1, tw0, tw1;
+  std::vector<char> copied;  // [s]: the side stream filled slots for step s (timing)
   cudaEvent_t tp0 = nullptr, tp1 = nullptr;
   bool timed_valid = false;
   int* d_err = nullptr;  // [0] flags, [1] first failing site
@@ -268,7 +283,7 @@ int ring_attn_set_option(ring_attn_t h, int option, long long value) {
   if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
   switch (option) {
     case RING_OPT_ROTATION:
-      if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "rotation must be 0 or 1");
+      if (value < 0 || value > 2) return fail(RING_ERR_INVALID_ARG, "rotation must be 0, 1 or 2");
       h->rotation = (int)value;
       return RING_OK;
     case RING_OPT_TIMING:
@@ -389,7 +404,8 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
   void* kbuf[2] = {ws, ws + 2 * tensor_bytes};
   void* vbuf[2] = {ws + tensor_bytes, ws + 3 * tensor_bytes};
   float* l_state = reinterpret_cast<float*>(ws + 4 * tensor_bytes);
-  const bool rotate = h->rotation && P > 1;
+  const int mode = P > 1 ? h->rotation : 0;
+  const bool rotate = mode != 0;
 
   // tensor maps: Q in natural order (strided per shard), K/V rotation buffers
   const cuuint64_t d = (cuuint64_t)p.d, n = (cuuint64_t)p.n, row_b = d * 2;
@@ -428,10 +444,23 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
   a.row_i = p.layout == RING_LAYOUT_STRIPED ? P : 1;
   a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : kQContiguous;
   a.kv_mode = rotate ? kKvSlotR : kKvSlotJ;
+  h->copied.assign((size_t)P, 0);
+
+  // side-stream copy of slots [r0, r0 + cnt) of buffer `cur` to [dst0, dst0 + cnt) of the other
+  auto copy_slots = [&](int cur, int r0, int dst0, int cnt) -> int {
+    for (int t = 0; t < 2; ++t) {
+      uint8_t* dst = static_cast<uint8_t*>(t == 0 ? kbuf[cur ^ 1] : vbuf[cur ^ 1]);
+      const uint8_t* src = static_cast<const uint8_t*>(t == 0 ? kbuf[cur] : vbuf[cur]);
+      RA_CUDA(cudaMemcpyAsync(dst + (size_t)dst0 * slot_bytes, src + (size_t)r0 * slot_bytes,
+                              (size_t)cnt * slot_bytes, cudaMemcpyDeviceToDevice, h->side),
+              "rotation copy");
+    }
+    return RING_OK;
+  };
 
   for (int s = 0; s < P; ++s) {
     const int cur = rotate ? (s & 1) : 0;
-    if (rotate && s >= 1) {
+    if (rotate && s >= 1 && h->copied[s]) {
       if (timing) RA_CUDA(cudaEventRecord(h->tw0[s], cs), "cudaEventRecord");
       RA_CUDA(cudaStreamWaitEvent(cs, h->landed[s], 0), "cudaStreamWaitEvent");
       if (timing) RA_CUDA(cudaEventRecord(h->tw1[s], cs), "cudaEventRecord");
@@ -440,31 +469,43 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     a.step = s;
     a.accumulate = s > 0 ? 1 : 0;
     a.finalize = s == P - 1 ? 1 : 0;
+    a.forward = (mode == 2 && s + 1 < P) ? 1 : 0;
     a.n_active = (int)act.size();
     for (size_t x = 0; x < act.size(); ++x) a.active[x] = act[x];
     const int grid = block_partial_grid(p.T, a.n_active, BH);
     if (timing) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
-    RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km[cur], &vm[cur], p.d, grid, cs), "step kernel launch");
+    RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km[cur], &vm[cur], p.d, grid, cs, &km[cur ^ 1],
+                                              &vm[cur ^ 1]),
+            "step kernel launch");
     if (timing) RA_CUDA(cudaEventRecord(h->tk1[s], cs), "cudaEventRecord");
     if (rotate) RA_CUDA(cudaEventRecord(h->released[s], cs), "cudaEventRecord");
-    if (rotate && s + 1 < P) {
-      // fill the other buffer for step s+1 once step s-1 has released it
-      RA_CUDA(cudaStreamWaitEvent(h->side, s == 0 ? h->packed : h->released[s - 1], 0), "cudaStreamWaitEvent");
-      const int nxt = cur ^ 1;
-      if (timing) RA_CUDA(cudaEventRecord(h->tc0[s + 1], h->side), "cudaEventRecord");
-      for (int t = 0; t < 2; ++t) {
-        uint8_t* dst = static_cast<uint8_t*>(t == 0 ? kbuf[nxt] : vbuf[nxt]);
-        const uint8_t* src = static_cast<const uint8_t*>(t == 0 ? kbuf[cur] : vbuf[cur]);
-        RA_CUDA(cudaMemcpyAsync(dst + slot_bytes, src, (size_t)(P - 1) * slot_bytes, cudaMemcpyDeviceToDevice,
-                                h->side),
-                "rotation copy");
-        RA_CUDA(cudaMemcpyAsync(dst, src + (size_t)(P - 1) * slot_bytes, slot_bytes, cudaMemcpyDeviceToDevice,
-                                h->side),
-                "rotation copy");
-      }
-      if (timing) RA_CUDA(cudaEventRecord(h->tc1[s + 1], h->side), "cudaEventRecord");
-      RA_CUDA(cudaEventRecord(h->landed[s + 1], h->side), "cudaEventRecord");
+    if (!rotate || s + 1 >= P) continue;
+    // slots the side stream moves for step s+1: all of them (mode 1), or
+    // those of shards the step kernel did not run (mode 2)
+    std::vector<char> send((size_t)P, mode == 1 ? 1 : 0);
+    if (mode == 2) {
+      std::vector<char> ran((size_t)P, 0);
+      for (unsigned short r : act) ran[r] = 1;
+      for (int r = 0; r < P; ++r) send[r] = !ran[r];
     }
+    bool any = false;
+    for (int r = 0; r < P; ++r) any = any || send[r];
+    if (!any) continue;
+    // fill the other buffer once step s-1 has released it (and written it)
+    RA_CUDA(cudaStreamWaitEvent(h->side, s == 0 ? h->packed : h->released[s - 1], 0), "cudaStreamWaitEvent");
+    if (timing) RA_CUDA(cudaEventRecord(h->tc0[s + 1], h->side), "cudaEventRecord");
+    // runs of consecutive slots r0..r1 (r1 < P-1) go to r0+1..r1+1; slot P-1 goes to 0
+    for (int r = 0; r < P - 1;) {
+      if (!send[r]) { ++r; continue; }
+      int r1 = r;
+      while (r1 + 1 < P - 1 && send[r1 + 1]) ++r1;
+      if ((rc = copy_slots(cur, r, r + 1, r1 - r + 1))) return rc;
+      r = r1 + 1;
+    }
+    if (send[P - 1] && (rc = copy_slots(cur, P - 1, 0, 1))) return rc;
+    if (timing) RA_CUDA(cudaEventRecord(h->tc1[s + 1], h->side), "cudaEventRecord");
+    RA_CUDA(cudaEventRecord(h->landed[s + 1], h->side), "cudaEventRecord");
+    h->copied[s + 1] = 1;
   }
   h->timed_valid = timing;
   return RING_OK;
@@ -474,8 +515,8 @@ int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float*
   if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
   if (!h->timed_valid) return fail(RING_ERR_INVALID_ARG, "no timed ring_attn_fwd recorded (set RING_OPT_TIMING)");
   const int P = h->plan.P;
-  const bool rotate = h->rotation && P > 1;
   for (int s = 0; s < P; ++s) {
+    const bool copied = s < (int)h->copied.size() && h->copied[s];
     float ms = 0.f;
     if (kernel_ms) {
       RA_CUDA(cudaEventSynchronize(h->tk1[s]), "cudaEventSynchronize");
@@ -484,7 +525,7 @@ int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float*
     }
     if (copy_ms) {
       ms = 0.f;
-      if (rotate && s >= 1) {
+      if (copied) {
         RA_CUDA(cudaEventSynchronize(h->tc1[s]), "cudaEventSynchronize");
         RA_CUDA(cudaEventElapsedTime(&ms, h->tc0[s], h->tc1[s]), "cudaEventElapsedTime");
       }
@@ -492,7 +533,7 @@ int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float*
     }
     if (wait_ms) {
       ms = 0.f;
-      if (rotate && s >= 1) {
+      if (copied) {
         RA_CUDA(cudaEventSynchronize(h->tw1[s]), "cudaEventSynchronize");
         RA_CUDA(cudaEventElapsedTime(&ms, h->tw0[s], h->tw1[s]), "cudaEventElapsedTime");
       }

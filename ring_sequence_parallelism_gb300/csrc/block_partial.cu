@@ -40,6 +40,16 @@
 // rescales its rows of O~ in TMEM only when one of them moved.  The commit
 // that signals S_t(j) ready also covers PV_t(j-1), so O~_t is stable then.
 //
+// Send along the ring (`forward`): the CTA of query tiles 2u, 2u+1 also
+// sends key tiles 2u and 2u+1 of its block to slot r+1 of the next step's
+// buffer, straight from shared memory with TMA stores, so no separate copy
+// rereads the block from HBM ([GRA] "Hiding the ring behind the GEMMs";
+// [RA-CN] "双缓冲是重叠成立的基础").  Those two tiles are the last ones the CTA
+// loads: a DIAG block ends on its diagonal tiles, and a FULL block walks its
+// key tiles in the rotated order 2u+2, .., KT-1, 0, .., 2u+1 (the order of the
+// tiles does not change the exact result; every tile's mask uses its own
+// key index).  A tile that the mask leaves unused is still loaded for sending.
+//
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the thread
 // records the error, tells the others to stop, and all warps drain what they
 // started (TMA loads, MMAs) before TMEM is freed and the CTA exits.
@@ -184,6 +194,19 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
+// Shared -> global tile store through the same kind of map (bulk group).
+__device__ __forceinline__ void tma_store_4d(const void* map, uint32_t src, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait_all() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -210,33 +233,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// D (TMEM) (+)= A (shared memory) x B (shared memory)
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D (TMEM) (+)= A (TMEM: row i in lane i, two bf16 of K per column) x B (shared memory)
-__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
 }
 
 // Fused MMA issue.  One asm block issues a whole K loop from the elected lane
@@ -448,7 +444,14 @@ struct WorkItem {
   int bh, r, j, slot, cls;
   long long delta;
   Tile tile[2];
+  int rot;             // loop index j visits key tile (j + rot) mod KT
+  int fwd_lo, fwd_hi;  // key tiles this CTA sends along the ring
 };
+
+__device__ __forceinline__ int key_tile(const StepArgs& a, const WorkItem& w, int j) {
+  const int kt = j + w.rot;
+  return kt >= a.KT ? kt - a.KT : kt;
+}
 
 __device__ __forceinline__ Tile tile_work(const StepArgs& a, int cls, long long delta, int t) {
   Tile w{t, 0, 0};
@@ -496,6 +499,9 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   }
   w.tile[0] = tile_work(a, w.cls, w.delta, 2 * u);
   w.tile[1] = tile_work(a, w.cls, w.delta, 2 * u + 1);
+  w.fwd_lo = 2 * u;
+  w.fwd_hi = min(2 * u + 2, a.KT);
+  w.rot = (w.cls == RING_BLOCK_FULL && w.fwd_hi < a.KT) ? w.fwd_hi : 0;
   w.slot = a.kv_mode == kKvSlotR ? w.r : (a.kv_mode == kKvSlotJ ? j : 0);
   return w;
 }
@@ -504,7 +510,8 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     block_partial_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ CUtensorMap q_map,
-                         const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map) {
+                         const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                         const __grid_constant__ CUtensorMap k_next, const __grid_constant__ CUtensorMap v_next) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -551,9 +558,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0 && nk > 0) {
-      const int ntiles = w.tile[1].nk > 0 ? 2 : 1;
-      mbar_expect_tx(bar(L::kBarQFull), ntiles * L::kQBytes);
+    // Loads for sending only (tiles the mask leaves unused) follow the
+    // computed ones; DIAG blocks end on the sent tiles, so np <= nk + 2 and
+    // the MMA warp has released every stage they reuse.
+    const int np = a.forward ? max(nk, w.fwd_hi) : nk;
+    if (lane == 0 && np > 0) {
+      const int ntiles = nk == 0 ? 0 : (w.tile[1].nk > 0 ? 2 : 1);
+      if (ntiles > 0) mbar_expect_tx(bar(L::kBarQFull), ntiles * L::kQBytes);
       for (int t = 0; t < ntiles; ++t) {
         const int i0 = w.tile[t].t * kTileM;
         for (int c = 0; c < D / L::kSub; ++c) {
@@ -568,15 +579,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int j = 0; j < nk && ok; ++j) {
+      for (int j = 0; j < np && ok; ++j) {
         const int st = j % kStages;
         const uint32_t par = ((j / kStages) - 1) & 1;
+        const int key0 = key_tile(a, w, j) * kTileN;
         if (j >= kStages) ok = mbar_wait(bar(L::kBarKEmpty + st), par, abort_flag, a, 1);
         if (!ok) break;
         mbar_expect_tx(bar(L::kBarKFull + st), L::kKBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), &k_map, bar(L::kBarKFull + st),
-                      c * L::kSub, j * kTileN, w.bh, w.slot);
+                      c * L::kSub, key0, w.bh, w.slot);
         k_issued = j + 1;
         if (j >= kStages) ok = mbar_wait(bar(L::kBarVEmpty + st), par, abort_flag, a, 2);
         if (!ok) break;
@@ -584,13 +596,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar(L::kBarVFull + st), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), &v_map, bar(L::kBarVFull + st),
-                      c * L::kSub, j * kTileN, w.bh, w.slot);
+                      c * L::kSub, key0, w.bh, w.slot);
         v_issued = j + 1;
+      }
+      if (a.forward && ok) {
+        // Send the last fwd_hi - fwd_lo tiles (still resident in their
+        // stages: nothing loads after them) to slot r+1 of the next buffer.
+        const int dst = w.r + 1 == a.P ? 0 : w.r + 1;
+        const int nf = w.fwd_hi - w.fwd_lo;
+        for (int j = np - nf; j < np && ok; ++j) {
+          const int st = j % kStages;
+          const uint32_t par = (j / kStages) & 1;
+          const int key0 = key_tile(a, w, j) * kTileN;
+          ok = mbar_wait(bar(L::kBarKFull + st), par, abort_flag, a, 10);
+          if (!ok) break;
+          for (int c = 0; c < D / L::kSub; ++c)
+            tma_store_4d(&k_next, sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), c * L::kSub, key0, w.bh,
+                         dst);
+          if (a.debug_drop_v) continue;
+          ok = mbar_wait(bar(L::kBarVFull + st), par, abort_flag, a, 11);
+          if (!ok) break;
+          for (int c = 0; c < D / L::kSub; ++c)
+            tma_store_4d(&v_next, sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), c * L::kSub, key0, w.bh,
+                         dst);
+        }
+        // the stores have read shared memory and written HBM before exit
+        bulk_commit_and_wait_all();
       }
       // Drain: every load this thread started has landed before the CTA
       // can exit (normally these waits return at once).
       const unsigned long long lim = a.wait_limit_ns;
-      mbar_drain_wait(bar(L::kBarQFull), 0, lim);
+      if (ntiles > 0) mbar_drain_wait(bar(L::kBarQFull), 0, lim);
       for (int j = (k_issued > kStages ? k_issued - kStages : 0); j < k_issued; ++j)
         mbar_drain_wait(bar(L::kBarKFull + j % kStages), (j / kStages) & 1, lim);
       for (int j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
@@ -657,6 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------- softmax and epilogue
     const int t = (warp - 2) / 4;  // 0: tile A (warps 2-5), 1: tile B (warps 6-9)
     const Tile tw = t == 0 ? w.tile[0] : w.tile[1];
+    // first loop index whose key tile may need the mask: in the rotated
+    // order of a FULL block the ragged last tile comes at KT - 1 - rot (the
+    // tiles after it take the mask too, which leaves them unchanged)
+    const int mask_from = w.rot == 0 ? tw.full_kt : (tw.full_kt < a.KT ? a.KT - 1 - w.rot : a.KT);
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const long long i = (long long)tw.t * kTileM + row;
@@ -702,8 +742,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < kTileN; ++e) s[e] = __uint_as_float(x[e]);
       }
-      if (j >= tw.full_kt) {
-        const long long kbase = (long long)j * kTileN;
+      if (j >= mask_from) {
+        const long long kbase = (long long)key_tile(a, w, j) * kTileN;
 #pragma unroll
         for (int e = 0; e < kTileN; ++e) {
           const long long key = kbase + e;
@@ -844,16 +884,20 @@ int prepare_block_partial_kernels() {
 int block_partial_grid(int T, int n_active, int BH) { return ((T + 1) / 2) * n_active * BH; }
 
 int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map, const void* v_map, int d,
-                         int grid, void* stream) {
+                         int grid, void* stream, const void* k_next_map, const void* v_next_map) {
   if (grid <= 0) return 0;
+  if (a.forward && (!k_next_map || !v_next_map)) return (int)cudaErrorInvalidValue;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
   const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
+  // without `forward` the kernel never touches the send maps
+  const CUtensorMap& kn = *static_cast<const CUtensorMap*>(k_next_map ? k_next_map : k_map);
+  const CUtensorMap& vn = *static_cast<const CUtensorMap*>(v_next_map ? v_next_map : v_map);
   if (d == 64) {
-    block_partial_kernel<64><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm);
+    block_partial_kernel<64><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
   } else {
-    block_partial_kernel<128><<<grid, kThreads, Layout<128>::kAlloc, s>>>(a, qm, km, vm);
+    block_partial_kernel<128><<<grid, kThreads, Layout<128>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
   }
   return (int)cudaGetLastError();
 }

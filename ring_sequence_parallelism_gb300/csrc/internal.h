@@ -81,6 +81,7 @@ struct StepArgs {
   int n_active;    // shards in `active`
   int fixed_r;     // >= 0: single shard (block partial); ignores `active`
   int debug_drop_v;  // test hook: issue no V loads (see RING_OPT_DEBUG_DROP_V_LOADS)
+  int forward;       // send the CTA's key tiles 2u, 2u+1 to slot r+1 of the next maps
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned short active[kMaxShards];
 };
@@ -91,8 +92,11 @@ constexpr int kErrTimeout = 1;
 struct TensorMaps;  // opaque here (holds CUtensorMap values)
 
 // Launchers (return a cudaError_t as int).
+// k_next_map / v_next_map: the other rotation buffer, used only when
+// a.forward is set (the kernel then sends its blocks there, slot r -> r+1).
 int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map, const void* v_map,
-                         int d, int grid, void* stream);
+                         int d, int grid, void* stream, const void* k_next_map = nullptr,
+                         const void* v_next_map = nullptr);
 int launch_state_init(float* m, float* l, float* o, long long rows, int d, void* stream);
 int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* lb, const float* ob,
                  long long rows, int d, void* stream);

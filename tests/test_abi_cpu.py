@@ -76,7 +76,9 @@ def test_calls_reject_null_arguments_without_a_gpu(lib):
     assert lib.ring_attn_fwd(h, None, None, None, None, None, None, None) == _lib.RING_ERR_INVALID_ARG
     assert lib.ring_attn_block_partial(h, 0, 0, None, None, None, st, 0, None) == _lib.RING_ERR_INVALID_ARG
     assert lib.ring_attn_set_option(h, 99, 1) == _lib.RING_ERR_INVALID_ARG
-    assert lib.ring_attn_set_option(h, _lib.RING_OPT_ROTATION, 0) == 0
+    for mode in (0, 1, 2):
+        assert lib.ring_attn_set_option(h, _lib.RING_OPT_ROTATION, mode) == 0
+    assert lib.ring_attn_set_option(h, _lib.RING_OPT_ROTATION, 3) == _lib.RING_ERR_INVALID_ARG
     assert lib.ring_attn_get_timing(h, None, None, None, None) == _lib.RING_ERR_INVALID_ARG
     assert lib.ring_attn_plan_block(h, 2, 0, None, None, None) == _lib.RING_ERR_INVALID_ARG
     assert lib.ring_attn_destroy(h) == 0

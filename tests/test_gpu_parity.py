@@ -44,9 +44,10 @@ def report(name, out, lse, ref_out, ref_lse):
     return d_out, d_lse
 
 
-def run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=True):
+def run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=None):
     att = ra.RingAttention(B, H, N, d, P, causal=causal, layout=layout)
-    att.set_option(ra.RING_OPT_ROTATION, int(rotation))
+    if rotation is not None:
+        att.set_option(ra.RING_OPT_ROTATION, rotation)
     out, lse = att.fwd(q.cuda(), k.cuda(), v.cuda())
     att.check()
     torch.cuda.synchronize()
@@ -214,6 +215,16 @@ SMALL_CASES = [
     (1, 1, 5 * 8, 64, 5, True, "striped"),        # n = 8: tiny shards
     (1, 2, 2048, 128, 16, True, "striped"),
     (1, 2, 2048, 128, 2, False, "striped"),
+    # shard lengths around the tile edges: n = 129 and 257 leave a last key
+    # tile that no query of a j > r striped block uses (it is still sent);
+    # n = 1 has no allowed pair at all in those blocks
+    (1, 2, 4 * 129, 64, 4, True, "striped"),
+    (1, 2, 3 * 257, 128, 3, True, "striped"),
+    (1, 2, 4 * 1, 64, 4, True, "striped"),
+    # FULL blocks walk their key tiles in rotated order; n = 328 puts the
+    # ragged tile first for the CTA of query tiles 0, 1
+    (1, 2, 3 * 328, 128, 3, True, "contiguous"),
+    (1, 2, 2 * 328, 64, 2, False, "striped"),
 ]
 
 
@@ -230,15 +241,20 @@ def test_fwd_small(case):
     assert d_out <= TOL_OUT and d_lse <= TOL_LSE
 
 
-def test_fwd_rotation_matches_direct_indexing():
-    """The double-buffered rotation only moves bytes: results are identical
-    bit for bit to reading every block straight from the packed buffer."""
-    B, H, N, d, P = 1, 2, 8 * 256, 128, 8
+@pytest.mark.parametrize("shape", [(1, 2, 8 * 256, 128, 8), (2, 1, 5 * 200, 64, 5)])
+def test_fwd_rotation_matches_direct_indexing(shape):
+    """The rotation only moves bytes: sending from the step kernel (mode 2)
+    and side-stream copies (mode 1) give results identical bit for bit to
+    reading every block straight from the packed buffer (mode 0), for causal
+    blocks of both layouts (contiguous skips blocks, whose slots the side
+    stream copies in mode 2) and for non-causal FULL blocks."""
+    B, H, N, d, P = shape
     q, k, v = make_qkv(B, H, N, d, seed=5)
-    for layout in ("contiguous", "striped"):
-        a = run_fwd(B, H, N, d, P, True, layout, q, k, v, rotation=True)
-        b = run_fwd(B, H, N, d, P, True, layout, q, k, v, rotation=False)
-        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for layout, causal in (("contiguous", True), ("striped", True), ("contiguous", False)):
+        ref = run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=0)
+        for mode in (1, 2):
+            got = run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=mode)
+            assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1]), (layout, causal, mode)
 
 
 def test_fwd_noncausal_512_workload():
@@ -315,12 +331,17 @@ def test_timing_report():
     q, k, v = make_qkv(B, H, N, d, seed=9)
     att = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped")
     att.set_option(ra.RING_OPT_TIMING, 1)
-    att.fwd(q.cuda(), k.cuda(), v.cuda())
-    t = att.timing()
-    att.check()
-    assert len(t["kernel_ms"]) == P and all(x > 0 for x in t["kernel_ms"])
-    assert t["copy_ms"][0] == 0 and all(x > 0 for x in t["copy_ms"][1:])
-    assert all(x >= 0 for x in t["wait_ms"]) and t["pack_ms"] > 0
+    for mode in (1, 2):
+        att.set_option(ra.RING_OPT_ROTATION, mode)
+        att.fwd(q.cuda(), k.cuda(), v.cuda())
+        t = att.timing()
+        att.check()
+        assert len(t["kernel_ms"]) == P and all(x > 0 for x in t["kernel_ms"])
+        if mode == 1:
+            assert t["copy_ms"][0] == 0 and all(x > 0 for x in t["copy_ms"][1:])
+        else:  # striped: every shard has work every step, the kernels send everything
+            assert all(x == 0 for x in t["copy_ms"]) and all(x == 0 for x in t["wait_ms"])
+        assert all(x >= 0 for x in t["wait_ms"]) and t["pack_ms"] > 0
     att.close()
 
 
