@@ -16,18 +16,24 @@
 // the exact merge with the incoming state is the same rescale.  The epilogue
 // writes the state back, or the normalised output O~/l and lse = m + ln l.
 //
-// CTA layout: 320 threads, two 128-row query tiles A and B (rows 256u ..
+// CTA layout: 352 threads, two 128-row query tiles A and B (rows 256u ..
 // 256u+255 of one shard) against the same K/V key tiles.
 //   warp 0      TMEM allocation; lane 0 issues the TMA loads (Q_A, Q_B once,
 //               then K and V tiles through two 2-stage rings)
-//   warp 1      lane 0 issues tcgen05.mma in the order
-//                 PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-//               so the tensor core works on one tile while the other tile's
-//               softmax runs.  PV takes P from TMEM (A operand in TMEM, V from
-//               shared memory), which keeps shared-memory reads of the MMAs
-//               below the 128 B/clk the SM can serve.
-//   warps 2..5  softmax + epilogue of tile A, one query row per thread
-//   warps 6..9  softmax + epilogue of tile B
+//   warp 1      issues the tcgen05.mma of tile A: S_A(0), then per key tile
+//               PV_A(j), S_A(j+1); warp 2 does the same for tile B.  The
+//               tensor core works on one tile while the other tile's softmax
+//               runs.  One issuing warp per tile waits only for its own P:
+//               an mbarrier wait costs ~140-270 cycles even on a completed
+//               phase, and with one warp serving both tiles those waits sat
+//               between one tile's P and its PV.  Each warp releases a K/V
+//               stage through its own barrier (tcgen05.commit tracks the
+//               MMAs of the issuing thread only).  PV takes P from TMEM (A
+//               operand in TMEM, V from shared memory), which keeps
+//               shared-memory reads of the MMAs below the 128 B/clk the SM
+//               can serve.
+//   warps 3..6  softmax + epilogue of tile A, one query row per thread
+//   warps 7..10 softmax + epilogue of tile B
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O~_A [256,256+d),
 // O~_B [256+d, 256+2d).  P_t (bf16 pairs, 64 columns) is written over the
 // first half of S_t once the softmax has read S_t into registers; the next
@@ -65,7 +71,7 @@
 namespace ringattn {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kStages = 2;
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -86,14 +92,14 @@ struct Layout {
   static constexpr int kOffBar = kOffV + kStages * kVBytes;
   static constexpr int kBarQFull = 0;
   static constexpr int kBarKFull = 1;
-  static constexpr int kBarKEmpty = kBarKFull + kStages;
-  static constexpr int kBarVFull = kBarKEmpty + kStages;
-  static constexpr int kBarVEmpty = kBarVFull + kStages;
-  static constexpr int kBarSFull = kBarVEmpty + kStages;  // [2]: tile A, B
-  static constexpr int kBarPFull = kBarSFull + 2;          // [2]
-  static constexpr int kBarOFull = kBarPFull + 2;          // [2]
-  static constexpr int kBarDrain = kBarOFull + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarKEmpty = kBarKFull + kStages;      // [stage][tile]
+  static constexpr int kBarVFull = kBarKEmpty + 2 * kStages;
+  static constexpr int kBarVEmpty = kBarVFull + kStages;      // [stage][tile]
+  static constexpr int kBarSFull = kBarVEmpty + 2 * kStages;  // [2]: tile A, B
+  static constexpr int kBarPFull = kBarSFull + 2;              // [2]
+  static constexpr int kBarOFull = kBarPFull + 2;              // [2]
+  static constexpr int kBarDrain = kBarOFull + 2;              // [2]
+  static constexpr int kNumBars = kBarDrain + 2;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
@@ -530,16 +536,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(L::kBarQFull), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kBarKFull + s), 1);
-      mbar_init(bar(L::kBarKEmpty + s), 1);
       mbar_init(bar(L::kBarVFull + s), 1);
-      mbar_init(bar(L::kBarVEmpty + s), 1);
+      for (int t = 0; t < 2; ++t) {
+        mbar_init(bar(L::kBarKEmpty + 2 * s + t), 1);
+        mbar_init(bar(L::kBarVEmpty + 2 * s + t), 1);
+      }
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::kBarSFull + t), 1);
       mbar_init(bar(L::kBarPFull + t), 128);
       mbar_init(bar(L::kBarOFull + t), 1);
+      mbar_init(bar(L::kBarDrain + t), 1);
     }
-    mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
@@ -583,14 +591,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % kStages;
         const uint32_t par = ((j / kStages) - 1) & 1;
         const int key0 = key_tile(a, w, j) * kTileN;
-        if (j >= kStages) ok = mbar_wait(bar(L::kBarKEmpty + st), par, abort_flag, a, 1);
+        // stage st last held tile j - 2; wait for each tile that used it
+        if (j >= kStages && j - kStages < w.tile[0].nk)
+          ok = mbar_wait(bar(L::kBarKEmpty + 2 * st), par, abort_flag, a, 1);
+        if (ok && j >= kStages && j - kStages < w.tile[1].nk)
+          ok = mbar_wait(bar(L::kBarKEmpty + 2 * st + 1), par, abort_flag, a, 1);
         if (!ok) break;
         mbar_expect_tx(bar(L::kBarKFull + st), L::kKBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), &k_map, bar(L::kBarKFull + st),
                       c * L::kSub, key0, w.bh, w.slot);
         k_issued = j + 1;
-        if (j >= kStages) ok = mbar_wait(bar(L::kBarVEmpty + st), par, abort_flag, a, 2);
+        if (j >= kStages && j - kStages < w.tile[0].nk)
+          ok = mbar_wait(bar(L::kBarVEmpty + 2 * st), par, abort_flag, a, 2);
+        if (ok && j >= kStages && j - kStages < w.tile[1].nk)
+          ok = mbar_wait(bar(L::kBarVEmpty + 2 * st + 1), par, abort_flag, a, 2);
         if (!ok) break;
         if (a.debug_drop_v) continue;  // test hook: nothing ever completes v_full
         mbar_expect_tx(bar(L::kBarVFull + st), L::kVBytes);
@@ -632,20 +647,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
         mbar_drain_wait(bar(L::kBarVFull + j % kStages), (j / kStages) & 1, lim);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------ MMA issuers (A, B)
     // The whole warp runs this loop (every lane waits on the barriers);
     // one elected lane issues the MMAs and commits.
-    if (nk > 0) {
+    const int t = warp - 1;
+    const int nkt = t == 0 ? w.tile[0].nk : w.tile[1].nk;
+    if (nkt > 0) {
       constexpr uint32_t idesc_qk = instr_desc(kTileM, kTileN, false);
       constexpr uint32_t idesc_pv = instr_desc(kTileM, D, true);
-      auto issue_s = [&](int t, int j) {
-        const uint32_t q_s = sbase + L::kOffQ + t * L::kQBytes;
+      const uint32_t q_s = sbase + L::kOffQ + t * L::kQBytes;
+      auto issue_s = [&](int j) {
         const uint32_t k_s = sbase + L::kOffK + (j % kStages) * L::kKBytes;
         mma_qk<D>(tmem + L::tmem_s(t), smem_desc(q_s, 16, 1024), smem_desc(k_s, 16, 1024), idesc_qk);
         mma_commit_elect(bar(L::kBarSFull + t));
       };
-      auto issue_pv = [&](int t, int j) {
+      auto issue_pv = [&](int j) {
         const uint32_t v_s = sbase + L::kOffV + (j % kStages) * L::kVBytes;
         mma_pv(tmem + L::tmem_o(t), tmem + L::tmem_s(t), smem_desc(v_s, kTileN * 128, 1024), idesc_pv,
                (j > 0 || a.accumulate) ? 1u : 0u);
@@ -654,44 +671,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       // transaction count completes only after the bytes are in shared
       // memory.  Only the wait for P (written to TMEM by the softmax warps)
       // is followed by tcgen05.fence::after_thread_sync; a fence issued right
-      // after commits measured ~125 cycles of tensor-pipe bubble.
+      // after commits measured ~125 cycles of tensor-pipe bubble.  The data
+      // waits come first, so the wait for P alone gates the PV + S issue.
       bool ok = warp_wait(bar(L::kBarQFull), 0, abort_flag, a, 3) &&
                 warp_wait(bar(L::kBarKFull), 0, abort_flag, a, 4);
       if (ok) {
-        if (w.tile[0].nk > 0) issue_s(0, 0);
-        if (w.tile[1].nk > 0) issue_s(1, 0);
-        mma_commit_elect(bar(L::kBarKEmpty + 0));
+        issue_s(0);
+        mma_commit_elect(bar(L::kBarKEmpty + t));
       }
-      const int nk_t[2] = {w.tile[0].nk, w.tile[1].nk};
-      for (int j = 0; j < nk && ok; ++j) {
+      for (int j = 0; j < nkt && ok; ++j) {
         const int st = j % kStages;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok || j >= nk_t[t]) continue;
-          ok = warp_wait(bar(L::kBarVFull + st), (j / kStages) & 1, abort_flag, a, 6) &&
-               warp_wait(bar(L::kBarPFull + t), j & 1, abort_flag, a, 5);
-          if (!ok) continue;
-          tc_fence_after();
-          issue_pv(t, j);
-          if (j + 1 < nk_t[t]) {
-            ok = warp_wait(bar(L::kBarKFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag, a, 7);
-            if (!ok) continue;
-            issue_s(t, j + 1);
-          } else {
-            mma_commit_elect(bar(L::kBarOFull + t));
-          }
-        }
+        const bool more = j + 1 < nkt;
+        ok = warp_wait(bar(L::kBarVFull + st), (j / kStages) & 1, abort_flag, a, 6);
+        if (ok && more)
+          ok = warp_wait(bar(L::kBarKFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag, a, 7);
+        ok = ok && warp_wait(bar(L::kBarPFull + t), j & 1, abort_flag, a, 5);
         if (!ok) break;
-        mma_commit_elect(bar(L::kBarVEmpty + st));
-        if (j + 1 < nk) mma_commit_elect(bar(L::kBarKEmpty + (j + 1) % kStages));
+        tc_fence_after();
+        issue_pv(j);
+        if (more) {
+          issue_s(j + 1);
+        } else {
+          mma_commit_elect(bar(L::kBarOFull + t));
+        }
+        mma_commit_elect(bar(L::kBarVEmpty + 2 * st + t));
+        if (more) mma_commit_elect(bar(L::kBarKEmpty + 2 * ((j + 1) % kStages) + t));
       }
       // Drain: all MMAs this warp issued are complete before TMEM is freed.
-      mma_commit_elect(bar(L::kBarDrain));
-      mbar_drain_wait(bar(L::kBarDrain), 0, a.wait_limit_ns);
+      mma_commit_elect(bar(L::kBarDrain + t));
+      mbar_drain_wait(bar(L::kBarDrain + t), 0, a.wait_limit_ns);
     }
   } else {
     // -------------------------------------------- softmax and epilogue
-    const int t = (warp - 2) / 4;  // 0: tile A (warps 2-5), 1: tile B (warps 6-9)
+    const int t = (warp - 3) / 4;  // 0: tile A (warps 3-6), 1: tile B (warps 7-10)
     const Tile tw = t == 0 ? w.tile[0] : w.tile[1];
     // first loop index whose key tile may need the mask: in the rotated
     // order of a FULL block the ragged last tile comes at KT - 1 - rot (the
