@@ -90,8 +90,8 @@ struct Layout {
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKBytes;
   static constexpr int kOffBar = kOffV + kStages * kVBytes;
-  static constexpr int kBarQFull = 0;
-  static constexpr int kBarKFull = 1;
+  static constexpr int kBarQFull = 0;  // [2]: tile A, B
+  static constexpr int kBarKFull = 2;
   static constexpr int kBarKEmpty = kBarKFull + kStages;      // [stage][tile]
   static constexpr int kBarVFull = kBarKEmpty + 2 * kStages;
   static constexpr int kBarVEmpty = kBarVFull + kStages;      // [stage][tile]
@@ -355,10 +355,6 @@ __device__ __forceinline__ void tmem_load128(uint32_t taddr, uint32_t (&x)[128])
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&x)[32]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], " RA_ST_REGS32 ";" ::"r"(taddr), RA_IN32(x)
-               : "memory");
-}
 
 __device__ __forceinline__ void tmem_store64(uint32_t taddr, const uint32_t (&x)[64]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], " RA_ST_REGS64 ";" ::"r"(taddr), RA_IN64(x)
@@ -531,9 +527,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
   const WorkItem w = decode_item(a);
   const int nk = max(w.tile[0].nk, w.tile[1].nk);
+  // Loads for sending only (tiles the mask leaves unused) follow the
+  // computed ones; DIAG blocks end on the sent tiles, so np <= nk + 2 and
+  // the MMA warps have released every stage they reuse.
+  const int np = a.forward ? max(nk, w.fwd_hi) : nk;
+  const int nq = nk == 0 ? 0 : (w.tile[1].nk > 0 ? 2 : 1);  // Q tiles to load (tile A has keys if B has)
+
+  // Softmax threads (warps 3..10, tile (warp-3)/4, one query row each) start
+  // the loads of their incoming state now, so the latency overlaps the
+  // set-up; the values reach TMEM after the barrier below.
+  const int t_sm = warp >= 3 ? (warp - 3) / 4 : 0;
+  const Tile tw = t_sm == 0 ? w.tile[0] : w.tile[1];
+  const int quad = warp & 3;
+  const long long i_row = (long long)tw.t * kTileM + quad * 32 + lane;
+  const bool valid = i_row < a.n;
+  const bool in_range = tw.t < a.T;  // the tile exists (its rows may still be partly past n)
+  const long long g = (long long)w.bh * a.row_bh + (long long)w.r * a.row_r + i_row * a.row_i;
+  uint32_t o_in[D];
+  float m_in = -INFINITY, l_in = 0.0f;
+  const bool load_state = warp >= 3 && a.accumulate && in_range;
+  if (load_state) {
+    const float* src = a.o_state + g * D;
+#pragma unroll
+    for (int q8 = 0; q8 < D / 8; ++q8) {
+      if (valid) {
+        ld_global_v8(src + q8 * 8, o_in + q8 * 8);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o_in[q8 * 8 + e] = 0u;
+      }
+    }
+    if (valid) {
+      m_in = a.m_state[g] * kLog2e;
+      l_in = a.l_state[g];
+    }
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kBarQFull), 1);
+    mbar_init(bar(L::kBarQFull + 1), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kBarKFull + s), 1);
       mbar_init(bar(L::kBarVFull + s), 1);
@@ -551,6 +583,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
+    // First loads before the TMEM allocation and the barrier, in the order
+    // the first MMA needs them: Q_A and K(0) gate S_A(0).
+    if (np > 0) {
+      auto load_q = [&](int t) {
+        const int i0 = w.tile[t].t * kTileM;
+        mbar_expect_tx(bar(L::kBarQFull + t), L::kQBytes);
+        for (int c = 0; c < D / L::kSub; ++c) {
+          const uint32_t dst = sbase + L::kOffQ + t * L::kQBytes + c * (kTileM * 128);
+          if (a.q_mode == kQStriped)
+            tma_load_4d(dst, &q_map, bar(L::kBarQFull + t), c * L::kSub, w.r, i0, w.bh);
+          else if (a.q_mode == kQContiguous)
+            tma_load_4d(dst, &q_map, bar(L::kBarQFull + t), c * L::kSub, i0, w.r, w.bh);
+          else
+            tma_load_4d(dst, &q_map, bar(L::kBarQFull + t), c * L::kSub, i0, 0, w.bh);
+        }
+      };
+      const int key0 = key_tile(a, w, 0) * kTileN;
+      if (nq > 0) load_q(0);
+      mbar_expect_tx(bar(L::kBarKFull), L::kKBytes);
+      for (int c = 0; c < D / L::kSub; ++c)
+        tma_load_4d(sbase + L::kOffK + c * (kTileN * 128), &k_map, bar(L::kBarKFull), c * L::kSub, key0, w.bh,
+                    w.slot);
+      if (nq > 1) load_q(1);
+      if (!a.debug_drop_v) {  // test hook: nothing ever completes v_full
+        mbar_expect_tx(bar(L::kBarVFull), L::kVBytes);
+        for (int c = 0; c < D / L::kSub; ++c)
+          tma_load_4d(sbase + L::kOffV + c * (kTileN * 128), &v_map, bar(L::kBarVFull), c * L::kSub, key0, w.bh,
+                      w.slot);
+      }
+    }
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -566,28 +628,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    // Loads for sending only (tiles the mask leaves unused) follow the
-    // computed ones; DIAG blocks end on the sent tiles, so np <= nk + 2 and
-    // the MMA warp has released every stage they reuse.
-    const int np = a.forward ? max(nk, w.fwd_hi) : nk;
+    // (Q tiles and key tile 0 were issued before the set-up barrier.)
     if (lane == 0 && np > 0) {
-      const int ntiles = nk == 0 ? 0 : (w.tile[1].nk > 0 ? 2 : 1);
-      if (ntiles > 0) mbar_expect_tx(bar(L::kBarQFull), ntiles * L::kQBytes);
-      for (int t = 0; t < ntiles; ++t) {
-        const int i0 = w.tile[t].t * kTileM;
-        for (int c = 0; c < D / L::kSub; ++c) {
-          const uint32_t dst = sbase + L::kOffQ + t * L::kQBytes + c * (kTileM * 128);
-          if (a.q_mode == kQStriped)
-            tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, w.r, i0, w.bh);
-          else if (a.q_mode == kQContiguous)
-            tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, i0, w.r, w.bh);
-          else
-            tma_load_4d(dst, &q_map, bar(L::kBarQFull), c * L::kSub, i0, 0, w.bh);
-        }
-      }
-      int k_issued = 0, v_issued = 0;
+      int k_issued = 1, v_issued = a.debug_drop_v ? 0 : 1;
       bool ok = true;
-      for (int j = 0; j < np && ok; ++j) {
+      for (int j = 1; j < np && ok; ++j) {
         const int st = j % kStages;
         const uint32_t par = ((j / kStages) - 1) & 1;
         const int key0 = key_tile(a, w, j) * kTileN;
@@ -641,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Drain: every load this thread started has landed before the CTA
       // can exit (normally these waits return at once).
       const unsigned long long lim = a.wait_limit_ns;
-      if (ntiles > 0) mbar_drain_wait(bar(L::kBarQFull), 0, lim);
+      for (int t = 0; t < nq; ++t) mbar_drain_wait(bar(L::kBarQFull + t), 0, lim);
       for (int j = (k_issued > kStages ? k_issued - kStages : 0); j < k_issued; ++j)
         mbar_drain_wait(bar(L::kBarKFull + j % kStages), (j / kStages) & 1, lim);
       for (int j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
@@ -673,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // is followed by tcgen05.fence::after_thread_sync; a fence issued right
       // after commits measured ~125 cycles of tensor-pipe bubble.  The data
       // waits come first, so the wait for P alone gates the PV + S issue.
-      bool ok = warp_wait(bar(L::kBarQFull), 0, abort_flag, a, 3) &&
+      bool ok = warp_wait(bar(L::kBarQFull + t), 0, abort_flag, a, 3) &&
                 warp_wait(bar(L::kBarKFull), 0, abort_flag, a, 4);
       if (ok) {
         issue_s(0);
@@ -703,43 +748,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------- softmax and epilogue
-    const int t = (warp - 3) / 4;  // 0: tile A (warps 3-6), 1: tile B (warps 7-10)
-    const Tile tw = t == 0 ? w.tile[0] : w.tile[1];
+    const int t = t_sm;  // 0: tile A (warps 3-6), 1: tile B (warps 7-10)
     // first loop index whose key tile may need the mask: in the rotated
     // order of a FULL block the ragged last tile comes at KT - 1 - rot (the
     // tiles after it take the mask too, which leaves them unchanged)
     const int mask_from = w.rot == 0 ? tw.full_kt : (tw.full_kt < a.KT ? a.KT - 1 - w.rot : a.KT);
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const long long i = (long long)tw.t * kTileM + row;
-    const bool valid = i < a.n;
-    const bool in_range = tw.t < a.T;  // the tile exists (its rows may still be partly past n)
+    const long long i = i_row;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + L::tmem_s(t);
     const uint32_t o_addr = tmem + lane_off + L::tmem_o(t);
-    const long long g = (long long)w.bh * a.row_bh + (long long)w.r * a.row_r + i * a.row_i;
-    float m2 = -INFINITY;  // reference max, log2 domain
-    float l = 0.0f;
-    if (a.accumulate && in_range) {
-      if (valid) {
-        m2 = a.m_state[g] * kLog2e;
-        l = a.l_state[g];
-      }
-      const float* src = a.o_state + g * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t x[32];
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          if (valid) {
-            ld_global_v8(src + c * 32 + q8 * 8, x + q8 * 8);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[q8 * 8 + e] = 0u;
-          }
-        }
-        tmem_store32(o_addr + c * 32, x);
-      }
+    float m2 = m_in;  // reference max, log2 domain
+    float l = l_in;
+    if (load_state) {
+      if constexpr (D == 128) tmem_store128(o_addr, o_in);
+      else tmem_store64(o_addr, o_in);
       tmem_store_wait();
     }
     bool ok = true;
