@@ -350,7 +350,10 @@ def run_ours(args, w):
                          "launches_per_step": w.P, "avg_launch_ms": k_total_ms / w.P},
             "ring": {"step_kernel_ms": kernel_ms, "rotation_copy_ms": copy_ms, "exposed_wait_ms": wait_ms,
                      "pack_ms": pack_ms, "exposed_wait_total_ms": sum(wait_ms),
-                     "rotation_bytes_per_copy": 2 * w.B * w.H * w.N * w.d * 2},
+                     "rotation": "each step kernel sends its K/V blocks to the next shard's slot "
+                                 "(TMA stores from shared memory); side-stream copies only for shards "
+                                 "with no work in a step",
+                     "rotation_bytes_per_step": 2 * w.B * w.H * w.N * w.d * 2},
             "clocks": clocks.summary(),
             "gpu_launches": args.steps * (1 + w.P),
             "e2e": e2e,
