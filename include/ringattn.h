@@ -124,7 +124,9 @@ RINGATTN_API const char* ring_attn_last_error(void);
 /* Bytes of device workspace ring_attn_fwd needs: the two K/V rotation
  * buffers A and B, each [P][B][H][n][d] bf16 for K and for V ([RA-CN]
  * "双缓冲是重叠成立的基础": buffer A read by compute while B receives), plus
- * the running l state [B][H][N] fp32.  256-byte aligned by the caller. */
+ * the running state (m, l, O~) between steps, fp32, stored per 128-row tile
+ * of each shard (n rounded up to whole tiles).  256-byte aligned by the
+ * caller. */
 RINGATTN_API int ring_attn_workspace_size(ring_attn_t h, size_t* bytes);
 
 /* ---------------------------------------------------------------- planner
@@ -180,15 +182,15 @@ RINGATTN_API int ring_attn_finalize(ring_attn_t h, int r, ring_state_t s, float*
 /* Whole ring forward on one device ([RA-CN] "环是怎样工作的" forward loop;
  * "双缓冲是重叠成立的基础" double buffering):
  *   q, k, v   natural order [B][H][N][d] bf16
- *   out       natural order [B][H][N][d] fp32 (also holds O~ between steps)
- *   lse       natural order [B][H][N]   fp32 (also holds m between steps)
+ *   out       natural order [B][H][N][d] fp32
+ *   lse       natural order [B][H][N]   fp32
  *   workspace ring_attn_workspace_size() bytes, 256-byte aligned
  * K/V are packed shard-major into buffer A; step s runs one kernel over every
- * shard's block (r - s) mod P, reading slot r of the current buffer, while a
- * side stream copies the rotated blocks into the other buffer for step s+1
- * (slot r <- slot r-1), ordered with events.  The last step writes the
- * normalised output and lse.  Returns after enqueueing; `stream` orders it
- * with the caller's work. */
+ * shard's block (r - s) mod P, reading slot r of the current buffer, and
+ * moves every block to slot r+1 of the other buffer for step s+1 as set by
+ * RING_OPT_ROTATION.  The running state stays in the workspace; the last step
+ * writes the normalised output and lse.  Returns after enqueueing; `stream`
+ * orders it with the caller's work. */
 RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
                   void* workspace, void* stream);
 

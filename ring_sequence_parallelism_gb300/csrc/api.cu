@@ -180,6 +180,24 @@ int ensure_device(ring_attn* h) {
 
 bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
+// ring_attn_fwd's workspace: rotation buffers X and Y (K and V each, bf16
+// [P][B][H][n][d]), then the running state between steps in 128-row tile
+// blocks (O~ [BH][P][T][D/8][128][8] fp32, m and l [BH][P][T][128] fp32).
+struct FwdWorkspace {
+  size_t tensor_bytes, o_off, m_off, l_off, total;
+};
+FwdWorkspace fwd_workspace(const Plan& p) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  FwdWorkspace f;
+  f.tensor_bytes = (size_t)p.B * p.H * (size_t)p.N * p.d * 2;
+  const size_t rows = (size_t)p.B * p.H * p.P * (size_t)p.T * kTileM;  // padded to whole tiles
+  f.o_off = 4 * f.tensor_bytes;
+  f.m_off = f.o_off + up(rows * p.d * 4);
+  f.l_off = f.m_off + up(rows * 4);
+  f.total = f.l_off + up(rows * 4);
+  return f;
+}
+
 StepArgs base_args(const ring_attn* h) {
   StepArgs a;
   std::memset(&a, 0, sizeof a);
@@ -243,11 +261,7 @@ int ring_attn_destroy(ring_attn_t h) {
 
 int ring_attn_workspace_size(ring_attn_t h, size_t* bytes) {
   if (!h || !bytes) return fail(RING_ERR_INVALID_ARG, "NULL argument");
-  const Plan& p = h->plan;
-  const size_t elems = (size_t)p.B * p.H * (size_t)p.N * p.d;
-  const size_t rot = 4 * elems * 2;                      // X and Y, each K and V, bf16
-  const size_t lstate = (size_t)p.B * p.H * (size_t)p.N * 4;  // l rows
-  *bytes = rot + ((lstate + 255) / 256) * 256;
+  *bytes = fwd_workspace(h->plan).total;
   return RING_OK;
 }
 
@@ -398,12 +412,11 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
   const Plan& p = h->plan;
   const int P = p.P, BH = p.B * p.H;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const size_t elems = (size_t)BH * (size_t)p.N * p.d;
-  const size_t tensor_bytes = elems * 2;
+  const FwdWorkspace fw = fwd_workspace(p);
+  const size_t tensor_bytes = fw.tensor_bytes;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* kbuf[2] = {ws, ws + 2 * tensor_bytes};
   void* vbuf[2] = {ws + tensor_bytes, ws + 3 * tensor_bytes};
-  float* l_state = reinterpret_cast<float*>(ws + 4 * tensor_bytes);
   const int mode = P > 1 ? h->rotation : 0;
   const bool rotate = mode != 0;
 
@@ -434,10 +447,11 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
 
   const size_t slot_bytes = (size_t)BH * (size_t)p.n * p.d * 2;
   StepArgs a = base_args(h);
-  a.o_state = out;   // O~ lives in `out` between steps
-  a.m_state = lse;   // m lives in `lse` between steps
-  a.l_state = l_state;
-  a.out = out;
+  a.o_state = reinterpret_cast<float*>(ws + fw.o_off);  // the running state, tile blocks
+  a.m_state = reinterpret_cast<float*>(ws + fw.m_off);
+  a.l_state = reinterpret_cast<float*>(ws + fw.l_off);
+  a.state_tiled = 1;
+  a.out = out;  // natural order, written by the last step
   a.lse = lse;
   a.row_bh = p.N;
   a.row_r = p.layout == RING_LAYOUT_STRIPED ? 1 : p.n;

@@ -543,23 +543,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool valid = i_row < a.n;
   const bool in_range = tw.t < a.T;  // the tile exists (its rows may still be partly past n)
   const long long g = (long long)w.bh * a.row_bh + (long long)w.r * a.row_r + i_row * a.row_i;
+  // Running state: row-major [row][D] (the C ABI's states), or with
+  // state_tiled one block per (head, shard, 128-row tile) laid out
+  // [D/8][128 rows][8], so a warp's 32 rows of one 8-column chunk are 1 KB
+  // contiguous (row-major rows put each lane of a warp on its own line).
+  const long long tile_base = (long long)(w.bh * a.P + w.r) * a.T + tw.t;
+  const long long ml_idx = a.state_tiled ? tile_base * kTileM + quad * 32 + lane : g;
+  float* const o_row = a.state_tiled ? a.o_state + tile_base * (kTileM * D) + (quad * 32 + lane) * 8 : a.o_state + g * D;
+  const int o_stride = a.state_tiled ? kTileM * 8 : 8;  // floats from one 8-column chunk to the next
   uint32_t o_in[D];
   float m_in = -INFINITY, l_in = 0.0f;
   const bool load_state = warp >= 3 && a.accumulate && in_range;
   if (load_state) {
-    const float* src = a.o_state + g * D;
 #pragma unroll
     for (int q8 = 0; q8 < D / 8; ++q8) {
       if (valid) {
-        ld_global_v8(src + q8 * 8, o_in + q8 * 8);
+        ld_global_v8(o_row + q8 * o_stride, o_in + q8 * 8);
       } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) o_in[q8 * 8 + e] = 0u;
       }
     }
     if (valid) {
-      m_in = a.m_state[g] * kLog2e;
-      l_in = a.l_state[g];
+      m_in = a.m_state[ml_idx] * kLog2e;
+      l_in = a.l_state[ml_idx];
     }
   }
 
@@ -866,7 +873,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (valid) a.lse[g] = (l > 0.0f) ? (m2 + __log2f(l)) * kLn2 : -INFINITY;
       } else {
-        float* dst = a.o_state + g * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t x[32];
@@ -877,13 +883,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) v[e] = have_o ? __uint_as_float(x[q8 * 8 + e]) : 0.0f;
-              st_global_v8(dst + c * 32 + q8 * 8, v);
+              st_global_v8(o_row + (c * 4 + q8) * o_stride, v);
             }
           }
         }
         if (valid) {
-          a.m_state[g] = m2 * kLn2;
-          a.l_state[g] = l;
+          a.m_state[ml_idx] = m2 * kLn2;
+          a.l_state[ml_idx] = l;
         }
       }
     }

@@ -82,6 +82,7 @@ struct StepArgs {
   int fixed_r;     // >= 0: single shard (block partial); ignores `active`
   int debug_drop_v;  // test hook: issue no V loads (see RING_OPT_DEBUG_DROP_V_LOADS)
   int forward;       // send the CTA's key tiles 2u, 2u+1 to slot r+1 of the next maps
+  int state_tiled;   // state in [BH][P][T][D/8][128][8] (O~) and [BH][P][T][128] (m, l) blocks
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned short active[kMaxShards];
 };

@@ -86,9 +86,17 @@ def test_calls_reject_null_arguments_without_a_gpu(lib):
 
 
 def test_workspace_size(lib):
+    # rotation buffers (2 x K and V, bf16) + the running state in 128-row
+    # tiles per shard: O~ (d floats) and m, l per row
     att = ra.RingAttention(1, 16, 131072, 128, 16, causal=True, layout="striped")
     elems = 16 * 131072 * 128
-    assert att.workspace_size() == 4 * elems * 2 + 16 * 131072 * 4
+    assert att.workspace_size() == 4 * elems * 2 + 16 * 131072 * (128 + 2) * 4
+    att.close()
+    # ragged shards round up to whole tiles: n = 200 -> 2 tiles of 128 rows
+    att = ra.RingAttention(2, 2, 3 * 200, 64, 3, causal=True, layout="contiguous")
+    rows = 2 * 2 * 3 * 256
+    up = lambda x: (x + 255) // 256 * 256
+    assert att.workspace_size() == 4 * (2 * 2 * 600 * 64) * 2 + up(rows * 64 * 4) + 2 * up(rows * 4)
     att.close()
 
 
