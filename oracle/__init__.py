@@ -31,6 +31,7 @@ LIBRARY = os.path.join(_HERE, "liboracle.so")
 
 LAYOUT_CONTIGUOUS = 0
 LAYOUT_STRIPED = 1
+LAYOUT_ZIGZAG = 2
 
 
 def build(source: str = SOURCE, output: str = LIBRARY, force: bool = False) -> str:
@@ -81,6 +82,8 @@ class Oracle:
         L.oracle_max_threads.restype = _I
         L.oracle_position.argtypes = [_I, _L, _I, _I, _L]
         L.oracle_position.restype = _L
+        L.oracle_owner.argtypes = [_I, _L, _I, _L, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_long)]
+        L.oracle_owner.restype = None
         L.oracle_block_at.argtypes = [_I, _I, _I]
         L.oracle_block_at.restype = _I
         L.oracle_dense_rows.argtypes = [_I, _L, _I, _I, _P, _P, _P, _L, _P, _P, _P, _I]
@@ -104,6 +107,12 @@ class Oracle:
 
     def position(self, layout: int, n: int, P: int, r: int, i: int) -> int:
         return self.lib.oracle_position(layout, n, P, r, i)
+
+    def owner(self, layout: int, n: int, P: int, t: int):
+        """(shard, local row) holding global position t."""
+        r, i = ctypes.c_int(), ctypes.c_long()
+        self.lib.oracle_owner(layout, n, P, t, ctypes.byref(r), ctypes.byref(i))
+        return r.value, i.value
 
     def block_at(self, P: int, r: int, s: int) -> int:
         return self.lib.oracle_block_at(P, r, s)

@@ -28,6 +28,9 @@
  *   - finalize: out = O~ / l, lse = m + ln(l);
  *   - layouts: contiguous pos(r,i) = r*n + i ([RA-CN] "位置编码必须使用全局位置");
  *     striped pos(r,i) = i*P + r (token t goes to shard t mod P);
+ *     zigzag: the sequence cut into 2P chunks of c = n/2 tokens, shard r
+ *     holding chunk r then chunk 2P-1-r ([GRA] "Striping the sequence to
+ *     flatten the triangle"), local rows in that order;
  *   - causal: key position <= query position.
  *
  * All inputs Q, K, V are bf16 bit patterns (uint16) in natural token order,
@@ -43,6 +46,7 @@
 
 #define ORACLE_LAYOUT_CONTIGUOUS 0
 #define ORACLE_LAYOUT_STRIPED 1
+#define ORACLE_LAYOUT_ZIGZAG 2
 
 static double widen_bf16(uint16_t bits) {
   uint32_t u = ((uint32_t)bits) << 16;
@@ -73,7 +77,33 @@ int oracle_max_threads(int nthreads) {
  * for the contiguous map; the striped map sends token t to shard t mod P). */
 long oracle_position(int layout, long n, int P, int r, long i) {
   if (layout == ORACLE_LAYOUT_STRIPED) return i * (long)P + r;
+  if (layout == ORACLE_LAYOUT_ZIGZAG) {
+    const long c = n / 2;
+    return i < c ? (long)r * c + i : (long)(2 * P - 1 - r) * c + (i - c);
+  }
   return (long)r * n + i;
+}
+
+/* The inverse: the shard holding global position t and its local row. */
+void oracle_owner(int layout, long n, int P, long t, int* r, long* i) {
+  if (layout == ORACLE_LAYOUT_STRIPED) {
+    *r = (int)(t % P);
+    *i = t / P;
+  } else if (layout == ORACLE_LAYOUT_ZIGZAG) {
+    const long c = n / 2, chunk = t / c;
+    *r = chunk < P ? (int)chunk : (int)(2 * P - 1 - chunk);
+    *i = t % c + (chunk < P ? 0 : c);
+  } else {
+    *r = (int)(t / n);
+    *i = t % n;
+  }
+}
+
+/* Shapes a layout accepts: N divisible by P, and for zigzag by 2P. */
+static int layout_ok(int layout, long N, int P) {
+  if (P <= 0 || N % P != 0) return 0;
+  if (layout == ORACLE_LAYOUT_ZIGZAG) return (N / P) % 2 == 0;
+  return layout == ORACLE_LAYOUT_CONTIGUOUS || layout == ORACLE_LAYOUT_STRIPED;
 }
 
 /* The K/V block that rank r holds at ring step s: rank r sends to r+1 and
@@ -222,7 +252,7 @@ int oracle_ring_rows(int BH, long N, int d, int P, int causal, int layout,
                      const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      long nrows, const long* rows, double* out, double* lse,
                      long* visits, int nthreads) {
-  if (BH <= 0 || N <= 0 || d <= 0 || P <= 0 || N % P != 0 || nrows < 0)
+  if (BH <= 0 || N <= 0 || d <= 0 || !layout_ok(layout, N, P) || nrows < 0)
     return -1;
   set_threads(nthreads);
   const long n = N / P;
@@ -249,8 +279,9 @@ int oracle_ring_rows(int BH, long N, int d, int P, int causal, int layout,
       long bh = idx / nrows, ri = idx % nrows;
       long t = rows ? rows[ri] : ri;
       /* which rank owns query position t, and its local row */
-      int r = (layout == ORACLE_LAYOUT_STRIPED) ? (int)(t % P) : (int)(t / n);
-      long i = (layout == ORACLE_LAYOUT_STRIPED) ? t / P : t % n;
+      int r;
+      long i;
+      oracle_owner(layout, n, P, t, &r, &i);
       const uint16_t* qrow =
           q + ((size_t)bh * N + oracle_position(layout, n, P, r, i)) * d;
       long* visit_row = visits ? visits + ((size_t)bh * N + t) * N : NULL;
@@ -302,8 +333,8 @@ int oracle_block_partial(int BH, long n, int d, int P, int causal, int layout,
                          int r, int j, const uint16_t* q_shard,
                          const uint16_t* k_block, const uint16_t* v_block,
                          double* m, double* l, double* o, int nthreads) {
-  if (BH <= 0 || n <= 0 || d <= 0 || P <= 0 || r < 0 || r >= P || j < 0 ||
-      j >= P)
+  if (BH <= 0 || n <= 0 || d <= 0 || !layout_ok(layout, n * (long)P, P) ||
+      r < 0 || r >= P || j < 0 || j >= P)
     return -1;
   set_threads(nthreads);
   const double scale = 1.0 / sqrt((double)d);
@@ -412,7 +443,7 @@ int oracle_finalize(long rows, int d, const double* m, const double* l,
 int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, int layout,
                            const uint16_t* q, const uint16_t* k,
                            const uint16_t* v, double* out) {
-  if (BH <= 0 || N <= 0 || d <= 0 || P <= 0 || N % P != 0) return -1;
+  if (BH <= 0 || N <= 0 || d <= 0 || !layout_ok(layout, N, P)) return -1;
   const long n = N / P;
   const double scale = 1.0 / sqrt((double)d);
   double* s = (double*)malloc(sizeof(double) * (size_t)n);

@@ -18,11 +18,16 @@ import os
 import numpy as np
 import torch
 
-from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED, bits_to_f64, bf16_bits
+from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED, LAYOUT_ZIGZAG, bits_to_f64, bf16_bits
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
-LAYOUTS = (LAYOUT_CONTIGUOUS, LAYOUT_STRIPED)
+LAYOUTS = (LAYOUT_CONTIGUOUS, LAYOUT_STRIPED, LAYOUT_ZIGZAG)
+
+
+def layouts_for(N, P):
+    """The layouts a shape admits: zigzag needs N divisible by 2P."""
+    return [lay for lay in LAYOUTS if lay != LAYOUT_ZIGZAG or N % (2 * P) == 0]
 
 
 def rand_bits(shape, seed, scale=1.0):
@@ -151,7 +156,7 @@ def pin_ring_equals_dense(orc):
         for causal in (False, True):
             ref_out, ref_lse = orc.dense(q, k, v, causal)
             for P in [p for p in range(1, N + 1) if N % p == 0]:
-                for layout in LAYOUTS:
+                for layout in layouts_for(N, P):
                     out, lse = orc.ring(q, k, v, P, causal, layout)
                     tol = 1e-13 if P == 1 else 1e-12
                     _close(out, ref_out, tol, f"ring=dense out P={P} layout={layout} causal={causal}")
@@ -159,15 +164,17 @@ def pin_ring_equals_dense(orc):
 
 
 def pin_layouts_agree(orc):
-    """Contiguous and striped layouts give the same natural-order result."""
+    """Contiguous, striped and zigzag layouts give the same natural-order
+    result (a layout only changes which tokens each shard holds)."""
     BH, N, d = 2, 32, 8
     q, k, v = rand_bits((BH, N, d), 71), rand_bits((BH, N, d), 72), rand_bits((BH, N, d), 73)
     for causal in (False, True):
         for P in (2, 4, 8):
             a = orc.ring(q, k, v, P, causal, LAYOUT_CONTIGUOUS)
-            b = orc.ring(q, k, v, P, causal, LAYOUT_STRIPED)
-            _close(a[0], b[0], 1e-12, "layouts out")
-            _close(a[1], b[1], 1e-12, "layouts lse")
+            for layout in (LAYOUT_STRIPED, LAYOUT_ZIGZAG):
+                b = orc.ring(q, k, v, P, causal, layout)
+                _close(a[0], b[0], 1e-12, f"layouts out {layout}")
+                _close(a[1], b[1], 1e-12, f"layouts lse {layout}")
 
 
 def pin_visits_exactly_once(orc):
@@ -178,7 +185,7 @@ def pin_visits_exactly_once(orc):
     for causal in (False, True):
         want = allowed_matrix(N, causal).astype(np.int64)
         for P in (1, 2, 3, 4, 6, 8, 12, 24):
-            for layout in LAYOUTS:
+            for layout in layouts_for(N, P):
                 _, _, cnt = orc.ring(q, k, v, P, causal, layout, visits=True)
                 assert np.array_equal(cnt[0], want), f"visits P={P} layout={layout} causal={causal}"
 
@@ -186,13 +193,17 @@ def pin_visits_exactly_once(orc):
 def pin_shard_work_closed_forms(orc):
     """Allowed pairs per shard under the causal mask, from the visit counts:
     contiguous W_r = r n^2 + n(n+1)/2; striped W_r = (r+1) n(n+1)/2 +
-    (P-1-r) n(n-1)/2; both sum to N(N+1)/2 ([GRA] "The causal mask wrecks the
-    load balance": a linear ramp from one block of work to P)."""
+    (P-1-r) n(n-1)/2; all sum to N(N+1)/2 ([GRA] "The causal mask wrecks the
+    load balance": a linear ramp from one block of work to P).  Zigzag, with
+    chunks of c = N/2P: the rows of chunks r and 2P-1-r see r c^2 + c(c+1)/2
+    and (2P-1-r) c^2 + c(c+1)/2 pairs, W_r = 2P c^2 + c for every shard ([GRA]
+    "Striping the sequence to flatten the triangle": the work is shared
+    evenly)."""
     BH, N, d = 1, 24, 1
     q, k, v = rand_bits((BH, N, d), 91), rand_bits((BH, N, d), 92), rand_bits((BH, N, d), 93)
     for P in (2, 3, 4, 6):
         n = N // P
-        for layout in LAYOUTS:
+        for layout in layouts_for(N, P):
             _, _, cnt = orc.ring(q, k, v, P, True, layout, visits=True)
             per_row = cnt[0].sum(axis=1)
             for r in range(P):
@@ -200,8 +211,11 @@ def pin_shard_work_closed_forms(orc):
                 got = int(per_row[rows].sum())
                 if layout == LAYOUT_CONTIGUOUS:
                     want = r * n * n + n * (n + 1) // 2
-                else:
+                elif layout == LAYOUT_STRIPED:
                     want = (r + 1) * n * (n + 1) // 2 + (P - 1 - r) * n * (n - 1) // 2
+                else:
+                    c = n // 2
+                    want = 2 * P * c * c + c
                 assert got == want, f"W_{r} layout={layout} P={P}: {got} != {want}"
             assert int(per_row.sum()) == N * (N + 1) // 2
 
@@ -230,7 +244,7 @@ def pin_merge_order_independent(orc):
     n = N // P
     q, k, v = rand_bits((BH, N, d), 111), rand_bits((BH, N, d), 112), rand_bits((BH, N, d), 113)
     rng = np.random.default_rng(5)
-    for layout in LAYOUTS:
+    for layout in layouts_for(N, P):
         for causal in (False, True):
             ref_out, ref_lse = orc.dense(q, k, v, causal)
             for r in range(P):
@@ -307,14 +321,24 @@ def pin_golden_schedule(orc):
 
 def pin_positions(orc):
     """Global positions: contiguous device p local i -> p*n + i ([RA-CN]
-    "位置编码必须使用全局位置"); striped: token t on shard t mod P; both maps are
-    bijections onto 0..N-1."""
-    n, P = 5, 4
-    assert orc.position(LAYOUT_CONTIGUOUS, n, P, 2, 3) == 13
+    "位置编码必须使用全局位置"); striped: token t on shard t mod P; zigzag
+    ([GRA] "Striping the sequence to flatten the triangle"): shard 0 holds
+    the very first and the very last chunk, the last shard the two middle
+    chunks.  Every map is a bijection onto 0..N-1 and owner() inverts it."""
+    n, P = 6, 4
+    assert orc.position(LAYOUT_CONTIGUOUS, n, P, 2, 3) == 15
     assert orc.position(LAYOUT_STRIPED, n, P, 2, 3) == 14
+    N, c = n * P, n // 2
+    first, last = [orc.position(LAYOUT_ZIGZAG, n, P, 0, i) for i in range(n)], \
+        [orc.position(LAYOUT_ZIGZAG, n, P, P - 1, i) for i in range(n)]
+    assert first == list(range(c)) + list(range(N - c, N))
+    assert last == list(range((P - 1) * c, (P + 1) * c))
     for layout in LAYOUTS:
         seen = sorted(orc.position(layout, n, P, r, i) for r in range(P) for i in range(n))
         assert seen == list(range(n * P))
+        for r in range(P):
+            for i in range(n):
+                assert orc.owner(layout, n, P, orc.position(layout, n, P, r, i)) == (r, i)
 
 
 ALL_PINS = [

@@ -30,6 +30,12 @@ MUTATIONS = [
      "sum += exp(s[kk]);\n      double l = log(sum);", None),
     ("block weight scaled by a constant", "double w = exp(s[kk] - m);\n      l += w;",
      "double w = 0.5 * exp(s[kk] - m);\n      l += w;", None),
+    ("zigzag second chunk off by one",
+     "return i < c ? (long)r * c + i : (long)(2 * P - 1 - r) * c + (i - c);",
+     "return i < c ? (long)r * c + i : (long)(2 * P - 2 - r) * c + (i - c);", None),
+    ("zigzag halves in the wrong order",
+     "return i < c ? (long)r * c + i : (long)(2 * P - 1 - r) * c + (i - c);",
+     "return i < c ? (long)(2 * P - 1 - r) * c + i : (long)r * c + (i - c);", None),
     ("block partial ignores the mask in the sum",
      "      if (!allowed(causal, pos_q, kpos[kk])) continue;\n      double w",
      "      double w", None),
