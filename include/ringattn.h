@@ -60,12 +60,28 @@ typedef enum {
   RING_ERR_OOM = -5          /* host allocation failed */
 } ring_status_t;
 
-typedef enum { RING_LAYOUT_CONTIGUOUS = 0, RING_LAYOUT_STRIPED = 1 } ring_layout_t;
+/* Token t of the sequence goes to shard:
+ *   CONTIGUOUS  t / n, local row t mod n;
+ *   STRIPED     t mod P, local row t / P;
+ *   ZIGZAG      the sequence cut into 2P chunks of c = n/2 tokens, shard r
+ *               holding chunk r (local rows 0..c-1) and chunk 2P-1-r (rows
+ *               c..n-1), so every shard has one early and one late chunk
+ *               ([GRA] "Striping the sequence to flatten the triangle");
+ *               needs N divisible by 2P and c a multiple of 128. */
+typedef enum { RING_LAYOUT_CONTIGUOUS = 0, RING_LAYOUT_STRIPED = 1, RING_LAYOUT_ZIGZAG = 2 } ring_layout_t;
 
 /* Class of the (query shard r, K/V block j) pair under the mask
  * ([RA-CN] "Causal Attention 让环不再完全对称": skip a strictly-future block,
- * mask a block crossing the diagonal, run the rest unmasked). */
-typedef enum { RING_BLOCK_SKIP = 0, RING_BLOCK_FULL = 1, RING_BLOCK_DIAG = 2 } ring_block_class_t;
+ * mask a block crossing the diagonal, run the rest unmasked).  PARTIAL (the
+ * zigzag layout only): whole chunks of the block are allowed for whole
+ * chunks of the shard's rows, and the rest is skipped (no diagonal); see
+ * ring_attn_plan_mask. */
+typedef enum {
+  RING_BLOCK_SKIP = 0,
+  RING_BLOCK_FULL = 1,
+  RING_BLOCK_DIAG = 2,
+  RING_BLOCK_PARTIAL = 3
+} ring_block_class_t;
 
 /* Per-row online-softmax state of one shard ([RA-CN] "局部 Softmax 为什么不能直接相加":
  * running max m, exp-sum l scaled by exp(-m), unnormalised value sum O~).
@@ -138,6 +154,19 @@ RINGATTN_API int ring_attn_workspace_size(ring_attn_t h, size_t* bytes);
  * k - i <= delta (contiguous delta = (r - j) n; striped delta = 0 if j <= r
  * else -1; non-causal FULL).  Any output pointer may be NULL. */
 RINGATTN_API int ring_attn_plan_block(ring_attn_t h, int r, int step, int* j, int* cls, long long* delta);
+
+/* The mask of local query row `row` of shard r at ring step s, in the
+ * block's local key columns: key k is allowed iff k < key_limit and
+ * k - row <= delta.  For CONTIGUOUS and STRIPED every row of a block has
+ * key_limit = n (0 for a skipped block) and the block's delta.  ZIGZAG
+ * (chunks of c = n/2; the rule follows from comparing global positions):
+ *   j < r:  key_limit = c for every row (the block's early chunk), no diagonal;
+ *   j = r:  key_limit = n, delta = 0;
+ *   j > r:  rows of the early chunk none (key_limit 0), rows of the late
+ *           chunk every key.
+ * "No diagonal" is returned as delta = n.  Any output pointer may be NULL. */
+RINGATTN_API int ring_attn_plan_mask(ring_attn_t h, int r, int step, long long row, long long* key_limit,
+                                     long long* delta);
 
 /* Per-shard totals over all P steps: allowed (q, k) pairs[P] and the
  * 128x128 MMA tiles the kernel computes[P] (any pointer may be NULL). */

@@ -8,20 +8,21 @@ streams.
     ra = RingAttention(B, H, N, d, P, causal=True, layout="striped")
     out, lse = ra.fwd(q, k, v)          # q, k, v: cuda bf16 [B, H, N, d]
 
-Layouts: "contiguous" (shard r holds tokens r*n .. r*n+n-1) or "striped"
-(token t goes to shard t mod P).
+Layouts: "contiguous" (shard r holds tokens r*n .. r*n+n-1), "striped"
+(token t goes to shard t mod P) or "zigzag" (2P chunks; shard r holds chunk r
+and chunk 2P-1-r).
 """
 from __future__ import annotations
 
 import ctypes
 
 from . import _lib
-from ._lib import (RING_BLOCK_DIAG, RING_BLOCK_FULL, RING_BLOCK_SKIP, RING_LAYOUT_CONTIGUOUS,  # noqa: F401
-                   RING_LAYOUT_STRIPED, RING_OPT_DEBUG_DROP_V_LOADS, RING_OPT_ROTATION, RING_OPT_TIMING,
+from ._lib import (RING_BLOCK_DIAG, RING_BLOCK_FULL, RING_BLOCK_PARTIAL, RING_BLOCK_SKIP,  # noqa: F401
+                   RING_LAYOUT_CONTIGUOUS, RING_LAYOUT_STRIPED, RING_LAYOUT_ZIGZAG, RING_OPT_DEBUG_DROP_V_LOADS, RING_OPT_ROTATION, RING_OPT_TIMING,
                    RING_OPT_WAIT_LIMIT_NS,
                    RingAttnError, RingState)
 
-LAYOUTS = {"contiguous": RING_LAYOUT_CONTIGUOUS, "striped": RING_LAYOUT_STRIPED}
+LAYOUTS = {"contiguous": RING_LAYOUT_CONTIGUOUS, "striped": RING_LAYOUT_STRIPED, "zigzag": RING_LAYOUT_ZIGZAG}
 
 
 def _layout_id(layout) -> int:
@@ -113,6 +114,12 @@ class RingAttention:
         _lib.check(self._lib.ring_attn_plan_block(self.handle, r, step, ctypes.byref(j), ctypes.byref(cls),
                                                   ctypes.byref(delta)))
         return j.value, cls.value, delta.value
+
+    def plan_mask(self, r: int, step: int, row: int):
+        """(key_limit, delta) of local row `row`: key k allowed iff k < key_limit and k - row <= delta."""
+        klim, delta = ctypes.c_longlong(), ctypes.c_longlong()
+        _lib.check(self._lib.ring_attn_plan_mask(self.handle, r, step, row, ctypes.byref(klim), ctypes.byref(delta)))
+        return klim.value, delta.value
 
     def shard_work(self):
         pairs = (ctypes.c_longlong * self.P)()

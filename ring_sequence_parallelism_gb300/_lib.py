@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "RING_OK", -1: "RING_ERR_INVALID_ARG", -2: "RING_ERR_UNSUPPOR
 
 RING_LAYOUT_CONTIGUOUS = 0
 RING_LAYOUT_STRIPED = 1
-RING_BLOCK_SKIP, RING_BLOCK_FULL, RING_BLOCK_DIAG = 0, 1, 2
+RING_LAYOUT_ZIGZAG = 2
+RING_BLOCK_SKIP, RING_BLOCK_FULL, RING_BLOCK_DIAG, RING_BLOCK_PARTIAL = 0, 1, 2, 3
 RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_WAIT_LIMIT_NS, RING_OPT_DEBUG_DROP_V_LOADS = 0, 1, 2, 3
 
 # Every symbol include/ringattn.h declares, with (restype, argtypes).
@@ -45,6 +46,7 @@ SIGNATURES = {
     "ring_attn_last_error": (ctypes.c_char_p, []),
     "ring_attn_workspace_size": (_i, [_vp, ctypes.POINTER(ctypes.c_size_t)]),
     "ring_attn_plan_block": (_i, [_vp, _i, _i, _pi, _pi, _pll]),
+    "ring_attn_plan_mask": (_i, [_vp, _i, _i, ctypes.c_longlong, _pll, _pll]),
     "ring_attn_shard_work": (_i, [_vp, _pll, _pll]),
     "ring_attn_step_work": (_i, [_vp, _i, _pll, _pll]),
     "ring_attn_state_init": (_i, [_vp, RingState, _vp]),

@@ -276,6 +276,18 @@ int ring_attn_plan_block(ring_attn_t h, int r, int step, int* j, int* cls, long 
   return RING_OK;
 }
 
+int ring_attn_plan_mask(ring_attn_t h, int r, int step, long long row, long long* key_limit, long long* delta) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  const Plan& p = h->plan;
+  if (r < 0 || r >= p.P || step < 0 || step >= p.P) return fail(RING_ERR_INVALID_ARG, "r or step out of range");
+  if (row < 0 || row >= p.n) return fail(RING_ERR_INVALID_ARG, "row out of range");
+  const BlockPlan& b = p.at(step, r);
+  const int half = row_half(p.layout, p.n, row);
+  if (key_limit) *key_limit = b.klim[half];
+  if (delta) *delta = b.hdelta[half];
+  return RING_OK;
+}
+
 int ring_attn_shard_work(ring_attn_t h, long long* pairs, long long* tiles) {
   if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
   for (int r = 0; r < h->plan.P; ++r) {
@@ -427,6 +439,11 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     cuuint64_t dims[4] = {d, (cuuint64_t)P, n, (cuuint64_t)BH};
     cuuint64_t str[3] = {row_b, row_b * P, row_b * (cuuint64_t)p.N};
     if ((rc = encode_map(&qm, q, dims, str, 1, kTileM))) return rc;
+  } else if (p.layout == RING_LAYOUT_ZIGZAG) {
+    // chunks of c = n/2 tokens: dims (d, c, 2P chunks, BH)
+    cuuint64_t dims[4] = {d, n / 2, (cuuint64_t)(2 * P), (cuuint64_t)BH};
+    cuuint64_t str[3] = {row_b, row_b * (n / 2), row_b * (cuuint64_t)p.N};
+    if ((rc = encode_map(&qm, q, dims, str, kTileM, 1))) return rc;
   } else {
     cuuint64_t dims[4] = {d, n, (cuuint64_t)P, (cuuint64_t)BH};
     cuuint64_t str[3] = {row_b, row_b * n, row_b * (cuuint64_t)p.N};
@@ -456,7 +473,7 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
   a.row_bh = p.N;
   a.row_r = p.layout == RING_LAYOUT_STRIPED ? 1 : p.n;
   a.row_i = p.layout == RING_LAYOUT_STRIPED ? P : 1;
-  a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : kQContiguous;
+  a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : (p.layout == RING_LAYOUT_ZIGZAG ? kQZigzag : kQContiguous);
   a.kv_mode = rotate ? kKvSlotR : kKvSlotJ;
   h->copied.assign((size_t)P, 0);
 

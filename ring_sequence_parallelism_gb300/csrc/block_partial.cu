@@ -437,42 +437,67 @@ __device__ __forceinline__ void fence_async_smem() {
 
 // ------------------------------------------------------------- work items
 struct Tile {
-  int t;        // query tile index within the shard
-  int nk;       // key tiles to visit
-  int full_kt;  // key tiles [0, full_kt) need no mask
+  int t;         // query tile index within the shard
+  int nk;        // key tiles to visit: a prefix [0, nk) of the block
+  int full_kt;   // key tiles [0, full_kt) need no mask
+  int klim;      // mask: key k allowed iff k < klim and k - i <= delta
+  long long delta;
 };
 
 struct WorkItem {
-  int bh, r, j, slot, cls;
-  long long delta;
+  int bh, r, j, slot;
   Tile tile[2];
-  int rot;             // loop index j visits key tile (j + rot) mod KT
+  int nk;              // max of the two tiles' nk
+  int rot;             // loop index j < nk visits key tile (j + rot) mod nk
   int fwd_lo, fwd_hi;  // key tiles this CTA sends along the ring
 };
 
+// Loop index -> key tile.  The computed prefix [0, nk) comes first, rotated
+// so that the sent tiles [fwd_lo, fwd_hi) end it when they lie inside it;
+// sent tiles beyond the prefix follow it.
 __device__ __forceinline__ int key_tile(const StepArgs& a, const WorkItem& w, int j) {
+  if (j >= w.nk) return max(w.fwd_lo, w.nk) + (j - w.nk);
   const int kt = j + w.rot;
-  return kt >= a.KT ? kt - a.KT : kt;
+  return kt >= w.nk ? kt - w.nk : kt;
 }
 
-__device__ __forceinline__ Tile tile_work(const StepArgs& a, int cls, long long delta, int t) {
-  Tile w{t, 0, 0};
+// The mask rule of the block for the rows in half h of the shard (see the
+// planner: k < klim and k - i <= delta; delta = n means no diagonal).
+__device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int h, int* klim, long long* delta) {
   const long long n = a.n;
-  if (t >= a.T || cls == RING_BLOCK_SKIP) return w;
-  const bool ragged = (n % kTileN) != 0;
-  if (cls == RING_BLOCK_FULL) {
-    w.nk = a.KT;
-    w.full_kt = ragged ? a.KT - 1 : a.KT;
-    return w;
+  *klim = a.n;
+  *delta = n;
+  if (!a.causal) return;
+  if (a.layout == RING_LAYOUT_ZIGZAG) {
+    if (j < r) {
+      *klim = a.n / 2;
+    } else if (j == r) {
+      *delta = 0;
+    } else if (h == 0) {
+      *klim = 0;
+    }
+    return;
   }
+  const long long dl = (a.layout == RING_LAYOUT_STRIPED) ? (j <= r ? 0 : -1) : (long long)(r - j) * n;
+  if (dl <= -n) {
+    *klim = 0;
+  } else if (dl < n - 1) {
+    *delta = dl;
+  }
+}
+
+__device__ __forceinline__ Tile tile_work(const StepArgs& a, int r, int j, int t) {
+  Tile w{t, 0, 0, 0, 0};
+  if (t >= a.T) return w;
+  const long long n = a.n;
   const long long i_min = (long long)t * kTileM;
   const long long i_max = min(n - 1, i_min + kTileM - 1);
-  const long long last_key = i_max + delta;
+  const int h = (a.layout == RING_LAYOUT_ZIGZAG && i_min >= n / 2) ? 1 : 0;
+  block_rule(a, r, j, h, &w.klim, &w.delta);
+  const long long last_key = min((long long)w.klim - 1, i_max + w.delta);
   w.nk = last_key < 0 ? 0 : (int)min((long long)a.KT, last_key / kTileN + 1);
-  const long long first_keys = i_min + delta + 1;
-  int full = first_keys <= 0 ? 0 : (int)min((long long)w.nk, first_keys / kTileN);
-  if (ragged && full == a.KT) full = a.KT - 1;
-  w.full_kt = full;
+  const long long common = min((long long)w.klim, i_min + w.delta + 1);  // keys allowed for every row
+  w.full_kt = common <= 0 ? 0 : (int)min((long long)w.nk, common / kTileN);
   return w;
 }
 
@@ -491,19 +516,15 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   int j = (w.r - a.step) % a.P;
   if (j < 0) j += a.P;
   w.j = j;
-  const long long n = a.n;
-  if (!a.causal) {
-    w.cls = RING_BLOCK_FULL;
-    w.delta = n;
-  } else {
-    w.delta = (a.layout == RING_LAYOUT_STRIPED) ? (j <= w.r ? 0 : -1) : (long long)(w.r - j) * n;
-    w.cls = w.delta >= n - 1 ? RING_BLOCK_FULL : (w.delta <= -n ? RING_BLOCK_SKIP : RING_BLOCK_DIAG);
-  }
-  w.tile[0] = tile_work(a, w.cls, w.delta, 2 * u);
-  w.tile[1] = tile_work(a, w.cls, w.delta, 2 * u + 1);
+  w.tile[0] = tile_work(a, w.r, j, 2 * u);
+  w.tile[1] = tile_work(a, w.r, j, 2 * u + 1);
+  w.nk = max(w.tile[0].nk, w.tile[1].nk);
   w.fwd_lo = 2 * u;
   w.fwd_hi = min(2 * u + 2, a.KT);
-  w.rot = (w.cls == RING_BLOCK_FULL && w.fwd_hi < a.KT) ? w.fwd_hi : 0;
+  // Rotating is needed only when the sent tiles are inside the computed
+  // prefix but not at its end; then both tiles visit the whole prefix
+  // (blocks without a diagonal), so one order serves both.
+  w.rot = (w.fwd_hi < w.nk) ? w.fwd_hi : 0;
   w.slot = a.kv_mode == kKvSlotR ? w.r : (a.kv_mode == kKvSlotJ ? j : 0);
   return w;
 }
@@ -526,11 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const WorkItem w = decode_item(a);
-  const int nk = max(w.tile[0].nk, w.tile[1].nk);
+  const int nk = w.nk;
   // Loads for sending only (tiles the mask leaves unused) follow the
-  // computed ones; DIAG blocks end on the sent tiles, so np <= nk + 2 and
-  // the MMA warps have released every stage they reuse.
-  const int np = a.forward ? max(nk, w.fwd_hi) : nk;
+  // computed prefix (key_tile), at most two of them, so the MMA warps have
+  // released every stage they reuse.
+  const int np = a.forward ? nk + max(0, w.fwd_hi - max(w.fwd_lo, nk)) : nk;
   const int nq = nk == 0 ? 0 : (w.tile[1].nk > 0 ? 2 : 1);  // Q tiles to load (tile A has keys if B has)
 
   // Softmax threads (warps 3..10, tile (warp-3)/4, one query row each) start
@@ -542,7 +563,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long i_row = (long long)tw.t * kTileM + quad * 32 + lane;
   const bool valid = i_row < a.n;
   const bool in_range = tw.t < a.T;  // the tile exists (its rows may still be partly past n)
-  const long long g = (long long)w.bh * a.row_bh + (long long)w.r * a.row_r + i_row * a.row_i;
+  const long long half_n = a.n / 2;
+  const long long g =
+      (long long)w.bh * a.row_bh +
+      (a.q_mode == kQZigzag ? (i_row < half_n ? (long long)w.r * half_n + i_row
+                                              : (long long)(2 * a.P - 1 - w.r) * half_n + (i_row - half_n))
+                            : (long long)w.r * a.row_r + i_row * a.row_i);
   // Running state: row-major [row][D] (the C ABI's states), or with
   // state_tiled one block per (head, shard, 128-row tile) laid out
   // [D/8][128 rows][8], so a warp's 32 rows of one 8-column chunk are 1 KB
@@ -600,6 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dst = sbase + L::kOffQ + t * L::kQBytes + c * (kTileM * 128);
           if (a.q_mode == kQStriped)
             tma_load_4d(dst, &q_map, bar(L::kBarQFull + t), c * L::kSub, w.r, i0, w.bh);
+          else if (a.q_mode == kQZigzag)
+            tma_load_4d(dst, &q_map, bar(L::kBarQFull + t), c * L::kSub, i0 < a.n / 2 ? i0 : i0 - a.n / 2,
+                        i0 < a.n / 2 ? w.r : 2 * a.P - 1 - w.r, w.bh);
           else if (a.q_mode == kQContiguous)
             tma_load_4d(dst, &q_map, bar(L::kBarQFull + t), c * L::kSub, i0, w.r, w.bh);
           else
@@ -759,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first loop index whose key tile may need the mask: in the rotated
     // order of a FULL block the ragged last tile comes at KT - 1 - rot (the
     // tiles after it take the mask too, which leaves them unchanged)
-    const int mask_from = w.rot == 0 ? tw.full_kt : (tw.full_kt < a.KT ? a.KT - 1 - w.rot : a.KT);
+    const int mask_from = w.rot == 0 ? tw.full_kt : (tw.full_kt < w.nk ? w.nk - 1 - w.rot : w.nk);
     const long long i = i_row;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + L::tmem_s(t);
@@ -788,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < kTileN; ++e) {
           const long long key = kbase + e;
-          if (key >= a.n || key - i > w.delta) s[e] = -INFINITY;
+          if (key >= tw.klim || key - i > tw.delta) s[e] = -INFINITY;
         }
       }
       // row max: eight independent chains of 3-input max, then a tree

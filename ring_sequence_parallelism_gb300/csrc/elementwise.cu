@@ -89,6 +89,16 @@ __global__ void merge_kernel(float* __restrict__ ma, float* __restrict__ la, flo
   }
 }
 
+// Natural position of local row i of shard r (see ring_layout_t).
+__device__ __forceinline__ long long natural_pos(int layout, long long n, int P, long long r, long long i) {
+  if (layout == RING_LAYOUT_STRIPED) return i * P + r;
+  if (layout == RING_LAYOUT_ZIGZAG) {
+    const long long c = n / 2;
+    return i < c ? r * c + i : (2 * P - 1 - r) * c + (i - c);
+  }
+  return r * n + i;
+}
+
 // Finalize shard r ([RA-CN] "环是怎样工作的": local_output = finalize(state)):
 // out = O~ / l, lse = m + ln l at natural position pos(r, i).
 __global__ void finalize_kernel(const float* __restrict__ m, const float* __restrict__ l,
@@ -102,8 +112,7 @@ __global__ void finalize_kernel(const float* __restrict__ m, const float* __rest
     const long long row = x / d4;
     const int c = (int)(x % d4);
     const long long bh = row / n, i = row % n;
-    const long long pos = layout == RING_LAYOUT_STRIPED ? i * P + r : (long long)r * n + i;
-    const long long dst_row = bh * N + pos;
+    const long long dst_row = bh * N + natural_pos(layout, n, P, r, i);
     const float lv = l[row];
     const float inv = lv > 0.0f ? 1.0f / lv : 0.0f;
     float4 v = o[x];
@@ -131,8 +140,7 @@ __global__ void pack_kv_kernel(const uint4* __restrict__ k, const uint4* __restr
     const long long kk = row % n;
     const long long bh = (row / n) % BH;
     const long long r = row / (n * BH);
-    const long long pos = layout == RING_LAYOUT_STRIPED ? kk * P + r : r * n + kk;
-    dst[x] = src[(bh * N + pos) * u16 + c];
+    dst[x] = src[(bh * N + natural_pos(layout, n, P, r, kk)) * u16 + c];
   }
 }
 

@@ -143,6 +143,10 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
     unsigned long long dims[4] = {d, (unsigned long long)P, n, (unsigned long long)BH};
     unsigned long long str[3] = {row_b, row_b * P, row_b * (unsigned long long)p.N};
     if ((rc = tensor_map_4d(qm, q, dims, str, 1, kTileM))) return rc;
+  } else if (p.layout == RING_LAYOUT_ZIGZAG) {
+    unsigned long long dims[4] = {d, n / 2, 2ULL * P, (unsigned long long)BH};
+    unsigned long long str[3] = {row_b, row_b * (n / 2), row_b * (unsigned long long)p.N};
+    if ((rc = tensor_map_4d(qm, q, dims, str, kTileM, 1))) return rc;
   } else {
     unsigned long long dims[4] = {d, n, (unsigned long long)P, (unsigned long long)BH};
     unsigned long long str[3] = {row_b, row_b * n, row_b * (unsigned long long)p.N};
@@ -175,7 +179,7 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
   a.BH = BH;
   a.T = p.T;
   a.KT = p.KT;
-  a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : kQContiguous;
+  a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : (p.layout == RING_LAYOUT_ZIGZAG ? kQZigzag : kQContiguous);
   a.kv_mode = kKvSlotJ;
   a.causal = p.causal;
   a.layout = p.layout;

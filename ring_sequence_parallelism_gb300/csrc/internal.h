@@ -16,15 +16,21 @@ constexpr int kTileN = 128;       // keys per k-tile
 constexpr int kMaxShards = 1024;  // P limit (kernel parameter table size)
 
 // ---------------------------------------------------------------- planner
-// Unified diagonal-offset rule: inside block (query shard r, key block j) the
-// pair (local row i, local column k) is allowed iff k - i <= delta.
+// Unified mask rule: inside block (query shard r, key block j) the pair
+// (local row i, local column k) is allowed iff k < klim[h] and
+// k - i <= hdelta[h], h the half of the shard that row i is in (zigzag:
+// i >= n/2; the other layouts use half 0 only):
 //   contiguous: pos(j,k) <= pos(r,i)  <=>  k - i <= (r - j) n
 //   striped:    k P + j <= i P + r    <=>  k - i <= 0 if j <= r, else -1
-//   non-causal: every pair (delta = n, FULL).
+//   zigzag:     j < r: k < n/2; j = r: k - i <= 0; j > r: half 1 every key
+//   non-causal: every pair (FULL).
+// "No diagonal" is hdelta = n; a skipped row set has klim = 0.
 struct BlockPlan {
   int j;            // key block held by shard r at this step
   int cls;          // ring_block_class_t
-  long long delta;  // diagonal offset (see above)
+  long long delta;  // diagonal offset of the block (n when it has none)
+  long long klim[2];
+  long long hdelta[2];
 };
 
 struct Plan {
@@ -44,9 +50,14 @@ struct Plan {
 
 int block_of(int P, int r, int step);  // (r - step) mod P
 BlockPlan classify(int layout, int causal, long long n, int r, int j);
-long long block_pairs(long long n, const BlockPlan& b);
-// Key tiles a query tile t needs (count) and how many of them need no mask.
-void tile_range(long long n, int KT, const BlockPlan& b, int t, int* nk, int* full_kt);
+// Half of the shard that local row i is in (1 only for the zigzag layout's late chunk).
+inline int row_half(int layout, long long n, long long i) {
+  return (layout == RING_LAYOUT_ZIGZAG && i >= n / 2) ? 1 : 0;
+}
+long long block_pairs(int layout, long long n, const BlockPlan& b);
+// Key tiles a query tile t needs (a prefix of the block: count) and how many
+// of them need no mask.
+void tile_range(int layout, long long n, int KT, const BlockPlan& b, int t, int* nk, int* full_kt);
 int build_plan(Plan* plan, int B, int H, long long N, int d, int P, int causal, int layout,
                std::string* err);
 
@@ -55,7 +66,8 @@ int build_plan(Plan* plan, int B, int H, long long N, int d, int P, int causal, 
 enum QMode : int {
   kQShardMajor = 0,  // [BH][n][d], map dims (d, n, 1, BH), coords (c, i, 0, bh)
   kQContiguous = 1,  // natural [BH][N][d] with pos = r n + i, dims (d, n, P, BH)
-  kQStriped = 2      // natural with pos = i P + r, dims (d, P, n, BH)
+  kQStriped = 2,     // natural with pos = i P + r, dims (d, P, n, BH)
+  kQZigzag = 3       // natural, chunks of c = n/2: dims (d, c, 2P, BH), chunk r then 2P-1-r
 };
 // Which slot of the K/V map holds the block of shard r at step s.
 enum KvMode : int {

@@ -20,8 +20,31 @@ int block_of(int P, int r, int step) {
 }
 
 BlockPlan classify(int layout, int causal, long long n, int r, int j) {
-  BlockPlan b{j, RING_BLOCK_FULL, n};
+  BlockPlan b{j, RING_BLOCK_FULL, n, {n, n}, {n, n}};
   if (!causal) return b;
+  if (layout == RING_LAYOUT_ZIGZAG) {
+    // Shard r holds chunks r and 2P-1-r (c = n/2 tokens each), rows in that
+    // order; block j likewise.  Comparing chunk ids (all of r, j < P <= the
+    // late chunks): early rows see block j's early chunk entirely if j < r,
+    // up to the diagonal if j = r, never if j > r, and never its late chunk;
+    // late rows see the early chunk entirely, and the late chunk entirely
+    // if j > r, up to the diagonal if j = r, never if j < r.  In block
+    // columns that is k < c for both halves (j < r), k - i <= 0 (j = r; for
+    // a late row it also admits the whole early chunk), and for j > r
+    // nothing for early rows and everything for late ones.
+    const long long c = n / 2;
+    if (j < r) {
+      b.klim[0] = b.klim[1] = c;
+      b.cls = RING_BLOCK_PARTIAL;
+    } else if (j == r) {
+      b.hdelta[0] = b.hdelta[1] = b.delta = 0;
+      b.cls = RING_BLOCK_DIAG;
+    } else {
+      b.klim[0] = 0;
+      b.cls = RING_BLOCK_PARTIAL;
+    }
+    return b;
+  }
   if (layout == RING_LAYOUT_STRIPED) {
     // token positions i*P + r (queries) and k*P + j (keys): k*P + j <= i*P + r
     // <=> k - i <= 0 when j <= r, and k - i <= -1 when j > r.
@@ -30,48 +53,40 @@ BlockPlan classify(int layout, int causal, long long n, int r, int j) {
     b.delta = (long long)(r - j) * n;
   }
   if (b.delta >= n - 1) {
-    b.cls = RING_BLOCK_FULL;
+    b.cls = RING_BLOCK_FULL;  // the offset admits every pair: no diagonal
   } else if (b.delta <= -n) {
     b.cls = RING_BLOCK_SKIP;
+    b.klim[0] = b.klim[1] = 0;
   } else {
     b.cls = RING_BLOCK_DIAG;
   }
+  b.hdelta[0] = b.hdelta[1] = b.delta;
   return b;
 }
 
-long long block_pairs(long long n, const BlockPlan& b) {
-  if (b.cls == RING_BLOCK_SKIP) return 0;
-  if (b.cls == RING_BLOCK_FULL) return n * n;
-  // rows i = 0..n-1 allow columns 0..min(n-1, i+delta)
+long long block_pairs(int layout, long long n, const BlockPlan& b) {
+  // rows i = 0..n-1 allow columns 0..min(klim, i + hdelta + 1) - 1
   long long total = 0;
   for (long long i = 0; i < n; ++i) {
-    long long c = std::min(n, std::max(0LL, i + b.delta + 1));
-    total += c;
+    const int h = row_half(layout, n, i);
+    total += std::min(b.klim[h], std::max(0LL, i + b.hdelta[h] + 1));
   }
   return total;
 }
 
-void tile_range(long long n, int KT, const BlockPlan& b, int t, int* nk, int* full_kt) {
-  const bool ragged = (n % kTileN) != 0;
-  if (b.cls == RING_BLOCK_SKIP) {
-    *nk = 0;
-    *full_kt = 0;
-    return;
-  }
-  if (b.cls == RING_BLOCK_FULL) {
-    *nk = KT;
-    *full_kt = ragged ? KT - 1 : KT;
-    return;
-  }
+void tile_range(int layout, long long n, int KT, const BlockPlan& b, int t, int* nk, int* full_kt) {
+  // The rows of a tile are in one half (the zigzag layout needs n/2 to be a
+  // multiple of the tile), so one (klim, hdelta) rule covers the tile.
   const long long i_min = (long long)t * kTileM;
   const long long i_max = std::min(n - 1, i_min + kTileM - 1);
-  const long long last_key = i_max + b.delta;  // largest allowed key of the tile
+  const int h = row_half(layout, n, i_min);
+  const long long klim = b.klim[h], hd = b.hdelta[h];
+  const long long last_key = std::min(klim - 1, i_max + hd);  // largest allowed key of the tile
   int cnt = last_key < 0 ? 0 : (int)std::min<long long>(KT, last_key / kTileN + 1);
-  const long long first_row_keys = i_min + b.delta + 1;  // keys allowed for every row
-  int full = first_row_keys <= 0 ? 0 : (int)std::min<long long>(cnt, first_row_keys / kTileN);
-  if (ragged && full == KT) full = KT - 1;
+  // key tiles allowed for every row of the tile: below klim and i_min + hd
+  const long long common = std::min(klim, i_min + hd + 1);
   *nk = cnt;
-  *full_kt = full;
+  *full_kt = common <= 0 ? 0 : (int)std::min<long long>(cnt, common / kTileN);
 }
 
 int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int layout,
@@ -86,8 +101,8 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
     *err = "causal must be 0 or 1";
     return RING_ERR_INVALID_ARG;
   }
-  if (layout != RING_LAYOUT_CONTIGUOUS && layout != RING_LAYOUT_STRIPED) {
-    *err = "layout must be RING_LAYOUT_CONTIGUOUS or RING_LAYOUT_STRIPED";
+  if (layout != RING_LAYOUT_CONTIGUOUS && layout != RING_LAYOUT_STRIPED && layout != RING_LAYOUT_ZIGZAG) {
+    *err = "layout must be RING_LAYOUT_CONTIGUOUS, RING_LAYOUT_STRIPED or RING_LAYOUT_ZIGZAG";
     return RING_ERR_INVALID_ARG;
   }
   if ((long long)P > N) {
@@ -112,6 +127,12 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   }
   const long long n = N / P;
   const long long bh = (long long)B * H;
+  if (layout == RING_LAYOUT_ZIGZAG && (n % (2 * kTileM)) != 0) {
+    std::snprintf(buf, sizeof buf,
+                  "zigzag needs chunks N/2P that are multiples of %d tokens (N=%lld, P=%d)", kTileM, N, P);
+    *err = buf;
+    return RING_ERR_UNSUPPORTED;
+  }
   if (n > (1LL << 30) || bh > (1LL << 30)) {
     *err = "shard length or B*H too large";
     return RING_ERR_UNSUPPORTED;
@@ -132,20 +153,20 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   p->step_pairs.assign(P, 0);
   p->step_tiles.assign(P, 0);
   p->active.assign(P, {});
-  // Work per distinct (class, delta): the striped layout has two deltas, the
-  // contiguous one FULL/SKIP plus the diagonal, so a small cache suffices.
-  std::vector<std::pair<long long, std::pair<long long, long long>>> cache;
+  // Work per distinct mask rule: every layout has at most four rules, so a
+  // small cache suffices.
+  std::vector<std::pair<std::vector<long long>, std::pair<long long, long long>>> cache;
   auto work = [&](const BlockPlan& b) {
-    long long key = b.cls == RING_BLOCK_DIAG ? b.delta : (b.cls == RING_BLOCK_FULL ? (1LL << 62) : -(1LL << 62));
+    const std::vector<long long> key{b.klim[0], b.klim[1], b.hdelta[0], b.hdelta[1]};
     for (auto& e : cache)
       if (e.first == key) return e.second;
     long long tiles = 0;
     for (int t = 0; t < p->T; ++t) {
       int nk, full;
-      tile_range(n, p->KT, b, t, &nk, &full);
+      tile_range(layout, n, p->KT, b, t, &nk, &full);
       tiles += nk;
     }
-    std::pair<long long, long long> w{block_pairs(n, b), tiles};
+    std::pair<long long, long long> w{block_pairs(layout, n, b), tiles};
     cache.push_back({key, w});
     return w;
   };
@@ -159,7 +180,7 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
       p->step_pairs[s] += w.first * bh;
       p->step_tiles[s] += w.second * bh;
       // The last step finalizes every shard, so it lists them all.
-      if (b.cls != RING_BLOCK_SKIP || s == P - 1) p->active[s].push_back((unsigned short)r);
+      if (w.first > 0 || s == P - 1) p->active[s].push_back((unsigned short)r);
     }
   }
   return RING_OK;

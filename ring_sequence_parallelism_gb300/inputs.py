@@ -27,7 +27,7 @@ class Workload:
     d: int
     P: int
     causal: bool
-    layout: str  # "contiguous" | "striped"
+    layout: str  # "contiguous" | "striped" | "zigzag"
     seed: int
     key_boost_frac: float = 0.0  # fraction of key rows scaled by key_boost
     key_boost: float = 8.0
@@ -38,7 +38,7 @@ class Workload:
 
     @property
     def layout_id(self) -> int:
-        return 1 if self.layout == "striped" else 0
+        return {"contiguous": 0, "striped": 1, "zigzag": 2}[self.layout]
 
     def allowed_pairs_per_head(self) -> int:
         return self.N * (self.N + 1) // 2 if self.causal else self.N * self.N
@@ -54,8 +54,11 @@ WORKLOADS = {
         Workload("noncausal-512", 1, 2, 512, 64, 4, False, "contiguous", 1000),
         Workload("contiguous-8k", 1, 8, 8192, 128, 8, True, "contiguous", 1001),
         Workload("striped-8k", 1, 8, 8192, 128, 8, True, "striped", 1001),
+        Workload("zigzag-8k", 1, 8, 8192, 128, 8, True, "zigzag", 1001),
         Workload("striped-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01),
         Workload("striped-1m", 1, 8, 1048576, 128, 64, True, "striped", 1004),
+        # the 128K workload in the zigzag layout (2P chunks of 4096 tokens)
+        Workload("zigzag-128k", 1, 16, 131072, 128, 16, True, "zigzag", 1003, key_boost_frac=0.01),
         # profiling size: the 128K striped workload with 4 heads (inputs 3 x 134 MB)
         Workload("striped-128k-h4", 1, 4, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01),
     )

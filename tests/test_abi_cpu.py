@@ -176,6 +176,66 @@ def test_planner_agrees_with_oracle_visits(lib, orc, layout, causal, P):
     att.close()
 
 
+@pytest.mark.parametrize("P,n", [(1, 256), (2, 256), (4, 512), (16, 8192), (64, 16384)])
+def test_zigzag_shard_work_is_balanced(lib, P, n):
+    """Zigzag ("GPU Ring Attention", "Striping the sequence to flatten the
+    triangle"): every shard holds one early and one late chunk of c = n/2
+    tokens and does the same causal work, W_r = 2P c^2 + c."""
+    B, H, c = 1, 2, n // 2
+    att = ra.RingAttention(B, H, P * n, 64, P, causal=True, layout="zigzag")
+    pairs, tiles = att.shard_work()
+    assert pairs == [(2 * P * c * c + c) * B * H] * P
+    assert sum(pairs) == B * H * (P * n) * (P * n + 1) // 2
+    assert sum(att.step_work(s)[0] for s in range(P)) == sum(pairs)
+    assert sum(tiles) * 128 * 128 >= sum(pairs)
+    att.close()
+
+
+@pytest.mark.parametrize("P", [1, 2, 3])
+@pytest.mark.parametrize("causal", [False, True])
+def test_zigzag_plan_agrees_with_oracle(lib, orc, P, causal):
+    """The planner's per-row mask (ring_attn_plan_mask: k < key_limit and
+    k - row <= delta) admits exactly the keys the oracle's global positions
+    allow, for every shard, step and row; per-block counts equal the oracle
+    ring simulation's visits."""
+    from oracle import LAYOUT_ZIGZAG
+    import oracle_pins
+
+    n = 256
+    N, d = P * n, 2
+    q = oracle_pins.rand_bits((1, N, d), 3)
+    _, _, cnt = orc.ring(q, q, q, P, causal, LAYOUT_ZIGZAG, visits=True)
+    att = ra.RingAttention(1, 1, N, 64, P, causal=causal, layout="zigzag")
+    for r in range(P):
+        qpos = np.array([orc.position(LAYOUT_ZIGZAG, n, P, r, i) for i in range(n)])
+        for s in range(P):
+            j, cls, _ = att.plan_block(r, s)
+            assert j == orc.block_at(P, r, s)
+            kpos = np.array([orc.position(LAYOUT_ZIGZAG, n, P, j, k) for k in range(n)])
+            ks = np.arange(n)
+            total = 0
+            for i in range(n):
+                klim, delta = att.plan_mask(r, s, i)
+                rule = (ks < klim) & (ks - i <= delta)
+                want = (kpos <= qpos[i]) if causal else np.ones(n, bool)
+                assert np.array_equal(rule, want), (r, s, i)
+                total += int(rule.sum())
+            assert total == int(cnt[0][np.ix_(qpos, kpos)].sum())
+            assert cls == (ra.RING_BLOCK_FULL if total == n * n else
+                           ra.RING_BLOCK_DIAG if j == r else ra.RING_BLOCK_PARTIAL), (r, s, cls)
+    att.close()
+
+
+def test_zigzag_needs_whole_tile_chunks(lib):
+    """Chunks of N/2P tokens must be multiples of the 128-row tile."""
+    h = ctypes.c_void_p()
+    assert lib.ring_attn_create(ctypes.byref(h), 1, 1, 4 * 200, 64, 2, 1, ra.RING_LAYOUT_ZIGZAG) == \
+        _lib.RING_ERR_UNSUPPORTED
+    assert b"zigzag" in lib.ring_attn_last_error()
+    assert lib.ring_attn_create(ctypes.byref(h), 1, 1, 4 * 256, 64, 2, 1, ra.RING_LAYOUT_ZIGZAG) == 0
+    assert lib.ring_attn_destroy(h) == 0
+
+
 def test_step_time_model_golden():
     """Pipelined ring time P x max(T_compute, T_comm): the worked estimate in
     "Ring Attention：把超长序列沿设备环流动", section "一个容量与时间的估算示例"."""

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import ring_sequence_parallelism_gb300 as ra
-from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED
+from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED, LAYOUT_ZIGZAG
 from ring_sequence_parallelism_gb300.inputs import WORKLOADS, make_qkv, make_workload, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -30,7 +30,7 @@ def built():
 
 
 def lid(layout):
-    return LAYOUT_STRIPED if layout == "striped" else LAYOUT_CONTIGUOUS
+    return {"contiguous": LAYOUT_CONTIGUOUS, "striped": LAYOUT_STRIPED, "zigzag": LAYOUT_ZIGZAG}[layout]
 
 
 def flat(t, BH):
@@ -126,9 +126,9 @@ def test_state_init_and_finalize():
 
 
 # ------------------------------------------------------------ block partial
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout,n", [("contiguous", 128), ("contiguous", 328), ("striped", 128), ("striped", 328),
+                                      ("zigzag", 256), ("zigzag", 512)])
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("n", [128, 328])
 def test_block_partial_matches_oracle(layout, d, n):
     """Every (shard, step) block of a small ring, fresh (accumulate 0): the
     block state's unique parts, m + ln l and O~/l, against the oracle's block
@@ -171,7 +171,7 @@ def test_block_partial_matches_oracle(layout, d, n):
     att.close()
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 def test_block_partial_ring_with_accumulate(layout):
     """The pages' loop driven through the C ABI: empty state, then P block
     partials with accumulate 1 in ring order, then finalize; equals dense
@@ -225,6 +225,13 @@ SMALL_CASES = [
     # ragged tile first for the CTA of query tiles 0, 1
     (1, 2, 3 * 328, 128, 3, True, "contiguous"),
     (1, 2, 2 * 328, 64, 2, False, "striped"),
+    # zigzag: chunks of 128 tokens put tile 0 in the early chunk and tile 1
+    # in the late one (one tile pair spans both); chunks of 256 and 512
+    (1, 2, 4 * 256, 64, 4, True, "zigzag"),
+    (2, 2, 3 * 512, 128, 3, True, "zigzag"),
+    (1, 2, 8 * 1024, 128, 8, True, "zigzag"),
+    (1, 2, 2 * 256, 128, 2, False, "zigzag"),
+    (1, 3, 256, 128, 1, True, "zigzag"),
 ]
 
 
@@ -250,7 +257,10 @@ def test_fwd_rotation_matches_direct_indexing(shape):
     stream copies in mode 2) and for non-causal FULL blocks."""
     B, H, N, d, P = shape
     q, k, v = make_qkv(B, H, N, d, seed=5)
-    for layout, causal in (("contiguous", True), ("striped", True), ("contiguous", False)):
+    cases = [("contiguous", True), ("striped", True), ("contiguous", False)]
+    if (N // P) % 256 == 0:
+        cases.append(("zigzag", True))
+    for layout, causal in cases:
         ref = run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=0)
         for mode in (1, 2):
             got = run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=mode)
@@ -272,23 +282,25 @@ def test_fwd_noncausal_512_workload():
 
 
 def test_fwd_8k_contiguous_and_striped():
-    """Both 8K causal workloads, every row, against dense; then the striped
-    result against the contiguous one (same seeded inputs; outputs are in
-    natural order, so no un-permuting is left to do)."""
-    wc, ws = WORKLOADS["contiguous-8k"], WORKLOADS["striped-8k"]
+    """The 8K causal workloads in the three layouts, every row, against
+    dense; then the striped and zigzag results against the contiguous one
+    (same seeded inputs; outputs are in natural order, so no un-permuting is
+    left to do)."""
+    wc, ws, wz = WORKLOADS["contiguous-8k"], WORKLOADS["striped-8k"], WORKLOADS["zigzag-8k"]
     q, k, v = make_workload(wc)
     BH = wc.B * wc.H
     ref_out, ref_lse = oracle.default().dense(flat(q, BH), flat(k, BH), flat(v, BH), True)
     res = {}
-    for w in (wc, ws):
+    for w in (wc, ws, wz):
         out, lse = run_fwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v)
         res[w.name] = (out, lse)
         d_out, d_lse = report(w.name, out.double().numpy().reshape(BH, w.N, w.d),
                               lse.double().numpy().reshape(BH, w.N), ref_out, ref_lse)
         assert d_out <= TOL_OUT and d_lse <= TOL_LSE
-    a, b = res[wc.name], res[ws.name]
-    assert float((a[0] - b[0]).abs().max()) <= 2 * TOL_OUT
-    assert float((a[1] - b[1]).abs().max()) <= 2 * TOL_LSE
+    a = res[wc.name]
+    for b in (res[ws.name], res[wz.name]):
+        assert float((a[0] - b[0]).abs().max()) <= 2 * TOL_OUT
+        assert float((a[1] - b[1]).abs().max()) <= 2 * TOL_LSE
 
 
 def _sampled_check(w, rows_per_head, ring_rows=0):
@@ -296,7 +308,8 @@ def _sampled_check(w, rows_per_head, ring_rows=0):
     out, lse = run_fwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v)
     BH = w.B * w.H
     n = w.n
-    extra = (0, 1, w.N - 1, n - 1, n, w.P - 1, w.P, w.N // 2)
+    # shard and chunk edges (zigzag chunks are n/2 long) and the middle
+    extra = (0, 1, w.N - 1, n - 1, n, w.P - 1, w.P, w.N // 2, n // 2 - 1, n // 2, w.N - n // 2 - 1, w.N - n // 2)
     rows = sample_rows(w.N, rows_per_head, extra=extra).numpy()
     orc = oracle.default()
     qf, kf, vf = flat(q, BH), flat(k, BH), flat(v, BH)
@@ -319,6 +332,10 @@ def _sampled_check(w, rows_per_head, ring_rows=0):
 
 def test_fwd_128k_striped_sampled():
     _sampled_check(WORKLOADS["striped-128k"], 256, ring_rows=16)
+
+
+def test_fwd_128k_zigzag_sampled():
+    _sampled_check(WORKLOADS["zigzag-128k"], 256, ring_rows=16)
 
 
 @pytest.mark.slow

@@ -42,7 +42,7 @@ def test_noalloc_rejects_problems_above_its_fixed_scratch(lib):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("layout", ["striped", "contiguous"])
+@pytest.mark.parametrize("layout", ["striped", "contiguous", "zigzag"])
 def test_noalloc_matches_fwd_twice(lib, layout):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
