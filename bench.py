@@ -172,8 +172,11 @@ def oracle_sample(w, q, k, v, seconds: float, seed: int = 4242):
     import oracle
     from ring_sequence_parallelism_gb300.inputs import sample_rows
 
+    from ring_sequence_parallelism_gb300.inputs import expand_kv
+
     orc = oracle.default()
     BH = w.B * w.H
+    k, v = expand_kv(k, w.H), expand_kv(v, w.H)  # grouped K/V heads written out per query head
     qf, kf, vf = (oracle.bf16_bits(x.reshape(BH, w.N, w.d)) for x in (q, k, v))
     rows_per_head = 2
     t_used = 0.0
@@ -208,8 +211,11 @@ def run_reference(args, w):
     import oracle
     from ring_sequence_parallelism_gb300.inputs import sample_rows
 
+    from ring_sequence_parallelism_gb300.inputs import expand_kv
+
     orc = oracle.default()
     BH = w.B * w.H
+    k, v = expand_kv(k, w.H), expand_kv(v, w.H)
     qf, kf, vf = (oracle.bf16_bits(x.reshape(BH, w.N, w.d)) for x in (q, k, v))
     times, flops = [], 0
     for i in range(args.warmup + args.steps):
@@ -237,8 +243,8 @@ def run_reference(args, w):
 
 
 def config_of(w):
-    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "P": w.P, "layout": w.layout,
-            "causal": w.causal, "global_batch": w.B, "seq_len": w.N,
+    return {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N": w.N, "d": w.d, "P": w.P,
+            "layout": w.layout, "causal": w.causal, "global_batch": w.B, "seq_len": w.N,
             "inputs": "Q,K,V ~ N(0,1) rounded to bf16" + (", 1% of key rows x8" if w.key_boost_frac else ""),
             "l2": l2_note(w)}
 
@@ -266,7 +272,7 @@ def run_ours(args, w):
     q_h, k_h, v_h = make_workload(w, pin=True)
     q, k, v = (x.to("cuda", non_blocking=True) for x in (q_h, k_h, v_h))
     torch.cuda.synchronize()
-    att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout)
+    att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
     out = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device="cuda")
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
     att.set_option(ra.RING_OPT_TIMING, 1)

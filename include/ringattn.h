@@ -129,6 +129,18 @@ typedef enum {
  * RING_ERR_UNSUPPORTED for N % P != 0 or d not in {64, 128}. */
 RINGATTN_API int ring_attn_create(ring_attn_t* out, int B, int H, long long N, int d, int P, int causal, int layout);
 
+/* As ring_attn_create, with grouped-query (GQA) or multi-query (MQA, Hkv = 1)
+ * attention: H query heads share Hkv K/V heads, query head h reading K/V
+ * head h / (H / Hkv).  k and v (and the K/V blocks of ring_attn_block_partial)
+ * are then [B][Hkv][.][d]; q, out, lse and the states keep H heads.  Only
+ * the Hkv heads travel the ring, so the rotation buffers and the bytes sent
+ * per step shrink by H / Hkv ([GRA] "What memory actually does as the ring
+ * grows": KV per device; the shared K/V of grouped heads rotates once).
+ * Errors as ring_attn_create, plus RING_ERR_INVALID_ARG when Hkv <= 0 or H is
+ * not a multiple of Hkv.  ring_attn_create(..., H, ...) is Hkv = H. */
+RINGATTN_API int ring_attn_create_gqa(ring_attn_t* out, int B, int H, int Hkv, long long N, int d, int P, int causal,
+                                      int layout);
+
 /* Release a handle (its events, side stream and plan memory).  Waits for no
  * stream; the caller must not destroy a handle with launches in flight.
  * NULL is accepted. */

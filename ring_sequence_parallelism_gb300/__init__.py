@@ -54,6 +54,13 @@ def ring_attn_create(B: int, H: int, N: int, d: int, P: int, causal: bool, layou
     return h.value
 
 
+def ring_attn_create_gqa(B: int, H: int, Hkv: int, N: int, d: int, P: int, causal: bool, layout) -> int:
+    lib = _lib.load()
+    h = ctypes.c_void_p()
+    _lib.check(lib.ring_attn_create_gqa(ctypes.byref(h), B, H, Hkv, N, d, P, int(bool(causal)), _layout_id(layout)))
+    return h.value
+
+
 def ring_attn_destroy(h: int) -> None:
     _lib.check(_lib.load().ring_attn_destroy(h))
 
@@ -88,12 +95,18 @@ def ring_attn_check(h, stream=None):
 class RingAttention:
     """One problem shape: plan, workspace and the calls of the C ABI."""
 
-    def __init__(self, B: int, H: int, N: int, d: int, P: int, causal: bool = True, layout="striped"):
+    def __init__(self, B: int, H: int, N: int, d: int, P: int, causal: bool = True, layout="striped",
+                 kv_heads: int | None = None):
+        """kv_heads: K/V heads for grouped-query attention (H a multiple of it); None = H."""
         self.B, self.H, self.N, self.d, self.P = B, H, N, d, P
+        self.Hkv = H if kv_heads is None else int(kv_heads)
         self.causal = bool(causal)
         self.layout = _layout_id(layout)
         self.n = N // P
-        self.handle = ring_attn_create(B, H, N, d, P, causal, self.layout)
+        if self.Hkv == H:
+            self.handle = ring_attn_create(B, H, N, d, P, causal, self.layout)
+        else:
+            self.handle = ring_attn_create_gqa(B, H, self.Hkv, N, d, P, causal, self.layout)
         self._lib = _lib.load()
         self._workspace = None
 
@@ -172,11 +185,11 @@ class RingAttention:
     def fwd(self, q, k, v, out=None, lse=None, stream=None):
         import torch
 
-        for t in (q, k, v):
+        for t, heads in ((q, self.H), (k, self.Hkv), (v, self.Hkv)):
             if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-                raise ValueError("q, k, v must be contiguous CUDA bfloat16 tensors [B, H, N, d]")
-            if tuple(t.shape) != (self.B, self.H, self.N, self.d):
-                raise ValueError(f"expected shape {(self.B, self.H, self.N, self.d)}, got {tuple(t.shape)}")
+                raise ValueError("q, k, v must be contiguous CUDA bfloat16 tensors [B, H (K/V: Hkv), N, d]")
+            if tuple(t.shape) != (self.B, heads, self.N, self.d):
+                raise ValueError(f"expected shape {(self.B, heads, self.N, self.d)}, got {tuple(t.shape)}")
         if out is None:
             out = torch.empty((self.B, self.H, self.N, self.d), dtype=torch.float32, device=q.device)
         if lse is None:

@@ -189,7 +189,7 @@ struct FwdWorkspace {
 FwdWorkspace fwd_workspace(const Plan& p) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   FwdWorkspace f;
-  f.tensor_bytes = (size_t)p.B * p.H * (size_t)p.N * p.d * 2;
+  f.tensor_bytes = (size_t)p.B * p.Hkv * (size_t)p.N * p.d * 2;  // one K or V buffer (K/V heads)
   const size_t rows = (size_t)p.B * p.H * p.P * (size_t)p.T * kTileM;  // padded to whole tiles
   f.o_off = 4 * f.tensor_bytes;
   f.m_off = f.o_off + up(rows * p.d * 4);
@@ -207,6 +207,7 @@ StepArgs base_args(const ring_attn* h) {
   a.n = (int)p.n;
   a.P = p.P;
   a.BH = p.B * p.H;
+  a.G = p.H / p.Hkv;
   a.T = p.T;
   a.KT = p.KT;
   a.causal = p.causal;
@@ -224,8 +225,15 @@ extern "C" {
 const char* ring_attn_last_error(void) { return g_last_error.c_str(); }
 
 int ring_attn_create(ring_attn_t* out, int B, int H, long long N, int d, int P, int causal, int layout) {
+  return ring_attn_create_gqa(out, B, H, H, N, d, P, causal, layout);
+}
+
+int ring_attn_create_gqa(ring_attn_t* out, int B, int H, int Hkv, long long N, int d, int P, int causal,
+                         int layout) {
   if (!out) return fail(RING_ERR_INVALID_ARG, "out handle pointer is NULL");
   *out = nullptr;
+  if (Hkv <= 0 || H <= 0 || H % Hkv != 0)
+    return fail(RING_ERR_INVALID_ARG, "the query heads H must be a positive multiple of the K/V heads Hkv");
   ring_attn* h = new (std::nothrow) ring_attn();
   if (!h) return fail(RING_ERR_OOM, "out of host memory");
   std::string err;
@@ -234,6 +242,7 @@ int ring_attn_create(ring_attn_t* out, int B, int H, long long N, int d, int P, 
     delete h;
     return fail(rc, err);
   }
+  h->plan.Hkv = Hkv;
   *out = h;
   g_last_error.clear();
   return RING_OK;
@@ -386,8 +395,9 @@ int ring_attn_block_partial(ring_attn_t h, int r, int step, const void* q_shard,
     if ((rc = encode_map(&qm, q_shard, dims, str, kTileM, 1))) return rc;
   }
   {
-    cuuint64_t dims[4] = {d, n, (cuuint64_t)BH, 1};
-    cuuint64_t str[3] = {row_b, row_b * n, row_b * n * BH};
+    const cuuint64_t BHkv = (cuuint64_t)p.B * p.Hkv;  // K/V blocks carry the K/V heads
+    cuuint64_t dims[4] = {d, n, BHkv, 1};
+    cuuint64_t str[3] = {row_b, row_b * n, row_b * n * BHkv};
     if ((rc = encode_map(&km, k_block, dims, str, kTileN, 1))) return rc;
     if ((rc = encode_map(&vm, v_block, dims, str, kTileN, 1))) return rc;
   }
@@ -449,20 +459,21 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     cuuint64_t str[3] = {row_b, row_b * n, row_b * (cuuint64_t)p.N};
     if ((rc = encode_map(&qm, q, dims, str, kTileM, 1))) return rc;
   }
+  const int BHkv = p.B * p.Hkv;  // the rotation buffers hold the K/V heads only
   for (int x = 0; x < 2; ++x) {
-    cuuint64_t dims[4] = {d, n, (cuuint64_t)BH, (cuuint64_t)P};
-    cuuint64_t str[3] = {row_b, row_b * n, row_b * n * BH};
+    cuuint64_t dims[4] = {d, n, (cuuint64_t)BHkv, (cuuint64_t)P};
+    cuuint64_t str[3] = {row_b, row_b * n, row_b * n * BHkv};
     if ((rc = encode_map(&km[x], kbuf[x], dims, str, kTileN, 1))) return rc;
     if ((rc = encode_map(&vm[x], vbuf[x], dims, str, kTileN, 1))) return rc;
   }
 
   const bool timing = h->timing != 0;
   if (timing) RA_CUDA(cudaEventRecord(h->tp0, cs), "cudaEventRecord");
-  RA_CUDA((cudaError_t)launch_pack_kv(k, v, kbuf[0], vbuf[0], BH, p.n, p.d, P, p.layout, cs), "pack launch");
+  RA_CUDA((cudaError_t)launch_pack_kv(k, v, kbuf[0], vbuf[0], BHkv, p.n, p.d, P, p.layout, cs), "pack launch");
   if (timing) RA_CUDA(cudaEventRecord(h->tp1, cs), "cudaEventRecord");
   if (rotate) RA_CUDA(cudaEventRecord(h->packed, cs), "cudaEventRecord");
 
-  const size_t slot_bytes = (size_t)BH * (size_t)p.n * p.d * 2;
+  const size_t slot_bytes = (size_t)BHkv * (size_t)p.n * p.d * 2;
   StepArgs a = base_args(h);
   a.o_state = reinterpret_cast<float*>(ws + fw.o_off);  // the running state, tile blocks
   a.m_state = reinterpret_cast<float*>(ws + fw.m_off);

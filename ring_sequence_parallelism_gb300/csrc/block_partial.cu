@@ -445,7 +445,7 @@ struct Tile {
 };
 
 struct WorkItem {
-  int bh, r, j, slot;
+  int bh, kvh, r, j, slot;  // kvh: the K/V head that query head bh reads
   Tile tile[2];
   int nk;              // max of the two tiles' nk
   int rot;             // loop index j < nk visits key tile (j + rot) mod nk
@@ -511,6 +511,7 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   const int u = U - 1 - item % U;
   const int g = item / U;
   w.bh = g % a.BH;
+  w.kvh = w.bh / a.G;
   const int slot_in_list = a.fixed_r >= 0 ? 0 : g / a.BH;
   w.r = a.fixed_r >= 0 ? a.fixed_r : (int)a.active[slot_in_list];
   int j = (w.r - a.step) % a.P;
@@ -551,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Loads for sending only (tiles the mask leaves unused) follow the
   // computed prefix (key_tile), at most two of them, so the MMA warps have
   // released every stage they reuse.
-  const int np = a.forward ? nk + max(0, w.fwd_hi - max(w.fwd_lo, nk)) : nk;
+  // With grouped heads, the first query head of each group sends the shared block.
+  const bool sends = a.forward && (w.bh % a.G) == 0;
+  const int np = sends ? nk + max(0, w.fwd_hi - max(w.fwd_lo, nk)) : nk;
   const int nq = nk == 0 ? 0 : (w.tile[1].nk > 0 ? 2 : 1);  // Q tiles to load (tile A has keys if B has)
 
   // Softmax threads (warps 3..10, tile (warp-3)/4, one query row each) start
@@ -639,13 +642,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nq > 0) load_q(0);
       mbar_expect_tx(bar(L::kBarKFull), L::kKBytes);
       for (int c = 0; c < D / L::kSub; ++c)
-        tma_load_4d(sbase + L::kOffK + c * (kTileN * 128), &k_map, bar(L::kBarKFull), c * L::kSub, key0, w.bh,
+        tma_load_4d(sbase + L::kOffK + c * (kTileN * 128), &k_map, bar(L::kBarKFull), c * L::kSub, key0, w.kvh,
                     w.slot);
       if (nq > 1) load_q(1);
       if (!a.debug_drop_v) {  // test hook: nothing ever completes v_full
         mbar_expect_tx(bar(L::kBarVFull), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
-          tma_load_4d(sbase + L::kOffV + c * (kTileN * 128), &v_map, bar(L::kBarVFull), c * L::kSub, key0, w.bh,
+          tma_load_4d(sbase + L::kOffV + c * (kTileN * 128), &v_map, bar(L::kBarVFull), c * L::kSub, key0, w.kvh,
                       w.slot);
       }
     }
@@ -681,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar(L::kBarKFull + st), L::kKBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), &k_map, bar(L::kBarKFull + st),
-                      c * L::kSub, key0, w.bh, w.slot);
+                      c * L::kSub, key0, w.kvh, w.slot);
         k_issued = j + 1;
         if (j >= kStages && j - kStages < w.tile[0].nk)
           ok = mbar_wait(bar(L::kBarVEmpty + 2 * st), par, abort_flag, a, 2);
@@ -692,10 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar(L::kBarVFull + st), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), &v_map, bar(L::kBarVFull + st),
-                      c * L::kSub, key0, w.bh, w.slot);
+                      c * L::kSub, key0, w.kvh, w.slot);
         v_issued = j + 1;
       }
-      if (a.forward && ok) {
+      if (sends && ok) {
         // Send the last fwd_hi - fwd_lo tiles (still resident in their
         // stages: nothing loads after them) to slot r+1 of the next buffer.
         const int dst = w.r + 1 == a.P ? 0 : w.r + 1;
@@ -707,13 +710,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(bar(L::kBarKFull + st), par, abort_flag, a, 10);
           if (!ok) break;
           for (int c = 0; c < D / L::kSub; ++c)
-            tma_store_4d(&k_next, sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), c * L::kSub, key0, w.bh,
+            tma_store_4d(&k_next, sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), c * L::kSub, key0, w.kvh,
                          dst);
           if (a.debug_drop_v) continue;
           ok = mbar_wait(bar(L::kBarVFull + st), par, abort_flag, a, 11);
           if (!ok) break;
           for (int c = 0; c < D / L::kSub; ++c)
-            tma_store_4d(&v_next, sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), c * L::kSub, key0, w.bh,
+            tma_store_4d(&v_next, sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), c * L::kSub, key0, w.kvh,
                          dst);
         }
         // the stores have read shared memory and written HBM before exit

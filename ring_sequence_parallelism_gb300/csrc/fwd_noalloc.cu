@@ -106,8 +106,8 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
       (status && reinterpret_cast<uintptr_t>(status) % 4 != 0))
     return report_error(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
   const Plan& p = handle_plan(h);
-  const int P = p.P, BH = p.B * p.H;
-  const size_t elems = (size_t)BH * (size_t)p.N * p.d;
+  const int P = p.P, BH = p.B * p.H, BHkv = p.B * p.Hkv;
+  const size_t elems = (size_t)BHkv * (size_t)p.N * p.d;  // one of K, V (K/V heads)
   const size_t kv_bytes = round256(elems * 2);
   const size_t l_bytes = round256((size_t)BH * (size_t)p.N * 4);
   const size_t need = kErrBytes + 2 * kv_bytes + l_bytes;
@@ -153,13 +153,13 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
     if ((rc = tensor_map_4d(qm, q, dims, str, kTileM, 1))) return rc;
   }
   {
-    unsigned long long dims[4] = {d, n, (unsigned long long)BH, (unsigned long long)P};
-    unsigned long long str[3] = {row_b, row_b * n, row_b * n * BH};
+    unsigned long long dims[4] = {d, n, (unsigned long long)BHkv, (unsigned long long)P};
+    unsigned long long str[3] = {row_b, row_b * n, row_b * n * BHkv};
     if ((rc = tensor_map_4d(km, kbuf, dims, str, kTileN, 1))) return rc;
     if ((rc = tensor_map_4d(vm, vbuf, dims, str, kTileN, 1))) return rc;
   }
 
-  e = (cudaError_t)launch_pack_kv(k, v, kbuf, vbuf, BH, p.n, p.d, P, p.layout, cs);
+  e = (cudaError_t)launch_pack_kv(k, v, kbuf, vbuf, BHkv, p.n, p.d, P, p.layout, cs);
   if (e != cudaSuccess) return cuda_error(e, "pack launch");
 
   StepArgs a;
@@ -177,6 +177,7 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
   a.n = (int)p.n;
   a.P = P;
   a.BH = BH;
+  a.G = p.H / p.Hkv;
   a.T = p.T;
   a.KT = p.KT;
   a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : (p.layout == RING_LAYOUT_ZIGZAG ? kQZigzag : kQContiguous);

@@ -35,6 +35,7 @@ struct BlockPlan {
 
 struct Plan {
   int B = 0, H = 0, d = 0, P = 0, causal = 0, layout = 0;
+  int Hkv = 0;  // K/V heads (H for plain multi-head attention)
   long long N = 0, n = 0;
   int T = 0;   // query tiles per shard, ceil(n / kTileM)
   int KT = 0;  // key tiles per block,  ceil(n / kTileN)
@@ -95,6 +96,7 @@ struct StepArgs {
   int debug_drop_v;  // test hook: issue no V loads (see RING_OPT_DEBUG_DROP_V_LOADS)
   int forward;       // send the CTA's key tiles 2u, 2u+1 to slot r+1 of the next maps
   int state_tiled;   // state in [BH][P][T][D/8][128][8] (O~) and [BH][P][T][128] (m, l) blocks
+  int G;             // query heads per K/V head: query head bh reads K/V head bh / G
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned short active[kMaxShards];
 };

@@ -144,6 +144,7 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   p->P = P;
   p->causal = causal;
   p->layout = layout;
+  p->Hkv = H;
   p->n = n;
   p->T = (int)((n + kTileM - 1) / kTileM);
   p->KT = (int)((n + kTileN - 1) / kTileN);

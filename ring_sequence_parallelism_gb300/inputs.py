@@ -31,6 +31,11 @@ class Workload:
     seed: int
     key_boost_frac: float = 0.0  # fraction of key rows scaled by key_boost
     key_boost: float = 8.0
+    Hkv: int = 0  # K/V heads for grouped-query attention (0: H)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv or self.H
 
     @property
     def n(self) -> int:
@@ -59,6 +64,8 @@ WORKLOADS = {
         Workload("striped-1m", 1, 8, 1048576, 128, 64, True, "striped", 1004),
         # the 128K workload in the zigzag layout (2P chunks of 4096 tokens)
         Workload("zigzag-128k", 1, 16, 131072, 128, 16, True, "zigzag", 1003, key_boost_frac=0.01),
+        # grouped-query attention: 16 query heads sharing 4 K/V heads
+        Workload("gqa-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01, Hkv=4),
         # profiling size: the 128K striped workload with 4 heads (inputs 3 x 134 MB)
         Workload("striped-128k-h4", 1, 4, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01),
     )
@@ -68,15 +75,17 @@ ROW_SAMPLE_SEED = 2004
 
 
 def make_qkv(B: int, H: int, N: int, d: int, seed: int, key_boost_frac: float = 0.0,
-             key_boost: float = 8.0, device="cpu", pin: bool = False):
-    """Return (q, k, v) bf16 tensors [B, H, N, d] drawn as the module docstring says."""
+             key_boost: float = 8.0, device="cpu", pin: bool = False, Hkv: int = 0):
+    """Return (q, k, v) bf16 tensors drawn as the module docstring says: q
+    [B, H, N, d], k and v [B, Hkv, N, d] (Hkv = H unless given)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     out = []
-    for _ in range(3):
-        t = torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=pin)
+    for x in range(3):
+        heads = H if x == 0 else (Hkv or H)
+        t = torch.empty((B, heads, N, d), dtype=torch.bfloat16, pin_memory=pin)
         for b in range(B):
-            for h in range(H):
+            for h in range(heads):
                 t[b, h].copy_(torch.randn((N, d), generator=g, dtype=torch.float32))
         out.append(t)
     q, k, v = out
@@ -96,7 +105,14 @@ def boosted_key_rows(N: int, seed: int, frac: float) -> torch.Tensor:
 
 
 def make_workload(w: Workload, device="cpu", pin: bool = False):
-    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.key_boost_frac, w.key_boost, device=device, pin=pin)
+    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.key_boost_frac, w.key_boost, device=device, pin=pin, Hkv=w.Hkv)
+
+
+def expand_kv(t: torch.Tensor, H: int) -> torch.Tensor:
+    """K or V with Hkv heads, repeated so that query head h sees K/V head
+    h / (H / Hkv): the grouped-query sharing written out as plain multi-head
+    attention (for the oracle)."""
+    return t if t.shape[1] == H else t.repeat_interleave(H // t.shape[1], dim=1)
 
 
 def sample_rows(N: int, count: int, seed: int = ROW_SAMPLE_SEED, extra=()) -> torch.Tensor:

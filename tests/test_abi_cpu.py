@@ -226,6 +226,20 @@ def test_zigzag_plan_agrees_with_oracle(lib, orc, P, causal):
     att.close()
 
 
+def test_grouped_query_handles(lib):
+    """ring_attn_create_gqa: H must be a positive multiple of Hkv; the
+    workspace holds the rotation buffers of the Hkv heads only."""
+    h = ctypes.c_void_p()
+    assert lib.ring_attn_create_gqa(ctypes.byref(h), 1, 6, 4, 1024, 64, 4, 1, 1) == _lib.RING_ERR_INVALID_ARG
+    assert lib.ring_attn_create_gqa(ctypes.byref(h), 1, 6, 0, 1024, 64, 4, 1, 1) == _lib.RING_ERR_INVALID_ARG
+    full = ra.RingAttention(1, 16, 131072, 128, 16, causal=True, layout="striped")
+    gqa = ra.RingAttention(1, 16, 131072, 128, 16, causal=True, layout="striped", kv_heads=4)
+    per_head = 131072 * 128 * 2  # one K or V buffer of one head, bf16
+    assert full.workspace_size() - gqa.workspace_size() == 4 * (16 - 4) * per_head  # X and Y, K and V
+    full.close()
+    gqa.close()
+
+
 def test_zigzag_needs_whole_tile_chunks(lib):
     """Chunks of N/2P tokens must be multiples of the 128-row tile."""
     h = ctypes.c_void_p()

@@ -10,7 +10,7 @@ import torch
 import oracle
 import ring_sequence_parallelism_gb300 as ra
 from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED, LAYOUT_ZIGZAG
-from ring_sequence_parallelism_gb300.inputs import WORKLOADS, make_qkv, make_workload, sample_rows
+from ring_sequence_parallelism_gb300.inputs import WORKLOADS, expand_kv, make_qkv, make_workload, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ def report(name, out, lse, ref_out, ref_lse):
 
 
 def run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=None):
-    att = ra.RingAttention(B, H, N, d, P, causal=causal, layout=layout)
+    att = ra.RingAttention(B, H, N, d, P, causal=causal, layout=layout, kv_heads=k.shape[1])
     if rotation is not None:
         att.set_option(ra.RING_OPT_ROTATION, rotation)
     out, lse = att.fwd(q.cuda(), k.cuda(), v.cuda())
@@ -306,6 +306,7 @@ def test_fwd_8k_contiguous_and_striped():
 def _sampled_check(w, rows_per_head, ring_rows=0):
     q, k, v = make_workload(w)
     out, lse = run_fwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v)
+    k, v = expand_kv(k, w.H), expand_kv(v, w.H)  # the oracle sees each query head's K/V
     BH = w.B * w.H
     n = w.n
     # shard and chunk edges (zigzag chunks are n/2 long) and the middle
@@ -336,6 +337,71 @@ def test_fwd_128k_striped_sampled():
 
 def test_fwd_128k_zigzag_sampled():
     _sampled_check(WORKLOADS["zigzag-128k"], 256, ring_rows=16)
+
+
+def test_fwd_128k_gqa_sampled():
+    _sampled_check(WORKLOADS["gqa-128k"], 256, ring_rows=16)
+
+
+GQA_CASES = [
+    # (B, H, Hkv, N, d, P, causal, layout)
+    (1, 4, 2, 4 * 256, 64, 4, True, "striped"),
+    (2, 6, 1, 3 * 200, 128, 3, True, "contiguous"),  # multi-query, ragged shards
+    (1, 8, 2, 8 * 256, 128, 8, True, "zigzag"),
+    (1, 4, 1, 2 * 256, 128, 2, False, "striped"),
+]
+
+
+@pytest.mark.parametrize("case", GQA_CASES, ids=lambda c: "B{}H{}kv{}N{}d{}P{}{}{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], "c" if c[6] else "n", c[7][0]))
+def test_fwd_grouped_query(case):
+    """Grouped-query / multi-query attention: H query heads over Hkv K/V
+    heads (query head h reads K/V head h / (H/Hkv)).  Against the oracle on
+    the K/V heads repeated per query head, and the three rotation modes bit
+    for bit (one query head of each group sends the shared block)."""
+    B, H, Hkv, N, d, P, causal, layout = case
+    q, k, v = make_qkv(B, H, N, d, seed=N + H + Hkv, Hkv=Hkv)
+    assert k.shape[1] == Hkv
+    out, lse = run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=2)
+    BH = B * H
+    ref_out, ref_lse = oracle.default().dense(flat(q, BH), flat(expand_kv(k, H), BH), flat(expand_kv(v, H), BH),
+                                              causal)
+    d_out, d_lse = report(f"gqa {case}", out.double().numpy().reshape(BH, N, d), lse.double().numpy().reshape(BH, N),
+                          ref_out, ref_lse)
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE
+    for mode in (0, 1):
+        got = run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=mode)
+        assert torch.equal(got[0], out) and torch.equal(got[1], lse), mode
+
+
+def test_block_partial_grouped_query():
+    """ring_attn_block_partial with K/V blocks of Hkv heads, accumulated over
+    the ring and finalized, equals dense attention on the repeated heads."""
+    B, H, Hkv, n, d, P = 2, 4, 2, 256, 128, 3
+    N = n * P
+    q, k, v = make_qkv(B, H, N, d, seed=91, Hkv=Hkv)
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped", kv_heads=Hkv)
+    orc = oracle.default()
+    L = LAYOUT_STRIPED
+    out = torch.empty((B, H, N, d), device="cuda")
+    lse = torch.empty((B, H, N), device="cuda")
+    for r in range(P):
+        pos_r = [orc.position(L, n, P, r, i) for i in range(n)]
+        st = att.new_state()
+        att.state_init(st)
+        for s in range(P):
+            j = orc.block_at(P, r, s)
+            pos_j = [orc.position(L, n, P, j, i) for i in range(n)]
+            att.block_partial(r, s, q[:, :, pos_r].contiguous().cuda(), k[:, :, pos_j].contiguous().cuda(),
+                              v[:, :, pos_j].contiguous().cuda(), st, 1)
+        att.finalize(r, st, out, lse)
+    att.check()
+    BH = B * H
+    ref_out, ref_lse = orc.dense(flat(q, BH), flat(expand_kv(k, H), BH), flat(expand_kv(v, H), BH), True)
+    d_out, d_lse = report("block ring gqa", out.cpu().double().numpy().reshape(BH, N, d),
+                          lse.cpu().double().numpy().reshape(BH, N), ref_out, ref_lse)
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE
+    att.close()
 
 
 @pytest.mark.slow
