@@ -235,6 +235,26 @@ RINGATTN_API int ring_attn_finalize(ring_attn_t h, int r, ring_state_t s, float*
 RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
                   void* workspace, void* stream);
 
+/* Split-K/V decode and short-query prefill ([RA-CN]: the query is sent to
+ * every K/V shard, each shard computes a local online-softmax state, and the
+ * states are merged exactly; [GRA] "Why partial results are allowed to
+ * merge").  Lq new queries sit at global positions N-Lq .. N-1 of the
+ * sequence the handle describes, and their K/V are already part of the
+ * cache, so under the causal mask query i sees the cached keys at positions
+ * <= N-Lq+i (all N keys for Lq = 1).  One launch computes the P shard states
+ * (shard r: its K/V block read in place from the cache, laid out as the
+ * handle's layout says); a second merges the P states of each row and
+ * finalizes.
+ *   q         [B][H][Lq][d] bf16
+ *   k, v      the cache, natural order [B][Hkv][N][d] bf16
+ *   out       [B][H][Lq][d] fp32,  lse [B][H][Lq] fp32
+ *   workspace ring_attn_decode_workspace_size(h, Lq) bytes, 256-byte aligned
+ * Layouts CONTIGUOUS and STRIPED (ZIGZAG returns RING_ERR_UNSUPPORTED);
+ * 1 <= Lq <= N.  Asynchronous on `stream`. */
+RINGATTN_API int ring_attn_decode_workspace_size(ring_attn_t h, long long Lq, size_t* bytes);
+RINGATTN_API int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v, long long Lq, float* out,
+                                  float* lse, void* workspace, void* stream);
+
 /* Set an option (see ring_option_t). */
 RINGATTN_API int ring_attn_set_option(ring_attn_t h, int option, long long value);
 

@@ -214,6 +214,31 @@ class RingAttention:
         lse_host.copy_(lse, non_blocking=True)
         return out_host, lse_host
 
+    def decode(self, q, k, v, out=None, lse=None, stream=None):
+        """Split-K/V decode / short-query prefill: q [B, H, Lq, d] bf16 at
+        global positions N-Lq .. N-1 over the cache k, v [B, Hkv, N, d]
+        (natural order); returns out [B, H, Lq, d] fp32 and lse [B, H, Lq]."""
+        import torch
+
+        Lq = int(q.shape[2])
+        if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous() or \
+                tuple(q.shape) != (self.B, self.H, Lq, self.d):
+            raise ValueError(f"q must be a contiguous CUDA bfloat16 tensor {(self.B, self.H, 'Lq', self.d)}")
+        for t in (k, v):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or \
+                    tuple(t.shape) != (self.B, self.Hkv, self.N, self.d):
+                raise ValueError(f"k, v must be contiguous CUDA bfloat16 tensors {(self.B, self.Hkv, self.N, self.d)}")
+        if out is None:
+            out = torch.empty((self.B, self.H, Lq, self.d), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((self.B, self.H, Lq), dtype=torch.float32, device=q.device)
+        need = ctypes.c_size_t()
+        _lib.check(self._lib.ring_attn_decode_workspace_size(self.handle, Lq, ctypes.byref(need)))
+        ws = torch.empty(max(need.value, 256), dtype=torch.uint8, device=q.device)
+        _lib.check(self._lib.ring_attn_decode(self.handle, _ptr(q), _ptr(k), _ptr(v), Lq, _ptr(out), _ptr(lse),
+                                              _ptr(ws), _stream(stream)))
+        return out, lse
+
     def timing(self):
         P = self.P
         k, c, w = (ctypes.c_float * P)(), (ctypes.c_float * P)(), (ctypes.c_float * P)()

@@ -43,6 +43,8 @@ class RingState(ctypes.Structure):
 SIGNATURES = {
     "ring_attn_create": (_i, [ctypes.POINTER(_vp), _i, _i, _ll, _i, _i, _i, _i]),
     "ring_attn_create_gqa": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _ll, _i, _i, _i, _i]),
+    "ring_attn_decode_workspace_size": (_i, [_vp, _ll, ctypes.POINTER(ctypes.c_size_t)]),
+    "ring_attn_decode": (_i, [_vp, _vp, _vp, _vp, _ll, _vp, _vp, _vp, _vp]),
     "ring_attn_destroy": (_i, [_vp]),
     "ring_attn_last_error": (ctypes.c_char_p, []),
     "ring_attn_workspace_size": (_i, [_vp, ctypes.POINTER(ctypes.c_size_t)]),

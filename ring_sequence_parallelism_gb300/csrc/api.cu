@@ -208,6 +208,8 @@ StepArgs base_args(const ring_attn* h) {
   a.P = p.P;
   a.BH = p.B * p.H;
   a.G = p.H / p.Hkv;
+  a.nq = (int)p.n;
+  a.decode_pos0 = -1;
   a.T = p.T;
   a.KT = p.KT;
   a.causal = p.causal;
@@ -550,6 +552,87 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     h->copied[s + 1] = 1;
   }
   h->timed_valid = timing;
+  return RING_OK;
+}
+
+// ---------------------------------------------------------------- decode
+// Workspace of ring_attn_decode: the P shard states of the Lq query rows,
+// m and l [P][B][H][Lq] and O~ [P][B][H][Lq][d] fp32.
+static size_t decode_ws(const Plan& p, long long Lq) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = (size_t)p.P * p.B * p.H * (size_t)Lq;
+  return up(rows * p.d * 4) + 2 * up(rows * 4);
+}
+
+int ring_attn_decode_workspace_size(ring_attn_t h, long long Lq, size_t* bytes) {
+  if (!h || !bytes) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  if (Lq < 1 || Lq > h->plan.N) return fail(RING_ERR_INVALID_ARG, "Lq must be in [1, N]");
+  *bytes = decode_ws(h->plan, Lq);
+  return RING_OK;
+}
+
+int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v, long long Lq, float* out,
+                     float* lse, void* workspace, void* stream) {
+  if (!h || !q || !k || !v || !out || !lse || !workspace) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  const Plan& p = h->plan;
+  if (Lq < 1 || Lq > p.N) return fail(RING_ERR_INVALID_ARG, "Lq must be in [1, N]");
+  if (Lq > (1LL << 30)) return fail(RING_ERR_UNSUPPORTED, "Lq too large");
+  if (p.layout == RING_LAYOUT_ZIGZAG) return fail(RING_ERR_UNSUPPORTED, "decode supports the contiguous and striped layouts");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(RING_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  int rc = ensure_device(h);
+  if (rc) return rc;
+  const int P = p.P, BH = p.B * p.H, BHkv = p.B * p.Hkv;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cuuint64_t d = (cuuint64_t)p.d, n = (cuuint64_t)p.n, row_b = d * 2, lq = (cuuint64_t)Lq;
+  CUtensorMap qm, km, vm;
+  {
+    cuuint64_t dims[4] = {d, lq, 1, (cuuint64_t)BH};
+    cuuint64_t str[3] = {row_b, row_b * lq, row_b * lq};
+    if ((rc = encode_map(&qm, q, dims, str, kTileM, 1))) return rc;
+  }
+  {
+    // block j of the cache in place: key row k of block j is token j n + k
+    // (contiguous) or k P + j (striped); dims (d, n, BHkv, P)
+    const cuuint64_t Nn = (cuuint64_t)p.N;
+    const bool striped = p.layout == RING_LAYOUT_STRIPED;
+    cuuint64_t dims[4] = {d, n, (cuuint64_t)BHkv, (cuuint64_t)P};
+    cuuint64_t str[3] = {striped ? row_b * P : row_b, row_b * Nn, striped ? row_b : row_b * n};
+    if ((rc = encode_map(&km, k, dims, str, kTileN, 1))) return rc;
+    if ((rc = encode_map(&vm, v, dims, str, kTileN, 1))) return rc;
+  }
+  const size_t rows = (size_t)P * BH * (size_t)Lq;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  float* o_st = reinterpret_cast<float*>(ws);
+  float* m_st = reinterpret_cast<float*>(ws + up(rows * p.d * 4));
+  float* l_st = reinterpret_cast<float*>(ws + up(rows * p.d * 4) + up(rows * 4));
+
+  StepArgs a = base_args(h);
+  a.o_state = o_st;  // shard r's states: rows [r][bh][i]
+  a.m_state = m_st;
+  a.l_state = l_st;
+  a.out = nullptr;
+  a.lse = nullptr;
+  a.row_bh = Lq;
+  a.row_r = (long long)BH * Lq;
+  a.row_i = 1;
+  a.nq = (int)Lq;
+  a.T = (int)((Lq + kTileM - 1) / kTileM);
+  a.decode_pos0 = p.N - Lq;
+  a.q_mode = kQShardMajor;
+  a.kv_mode = kKvSlotJ;  // at step 0 shard r reads block r
+  a.step = 0;
+  a.accumulate = 0;
+  a.finalize = 0;
+  a.n_active = P;
+  for (int r = 0; r < P; ++r) a.active[r] = (unsigned short)r;
+  const int grid = block_partial_grid(a.T, P, BH);
+  RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km, &vm, p.d, grid, cs), "decode block launch");
+  RA_CUDA((cudaError_t)launch_merge_shards(m_st, l_st, o_st, out, lse, (long long)BH * Lq, p.d, P, cs),
+          "decode merge launch");
   return RING_OK;
 }
 

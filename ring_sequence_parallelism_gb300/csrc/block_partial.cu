@@ -437,12 +437,20 @@ __device__ __forceinline__ void fence_async_smem() {
 
 // ------------------------------------------------------------- work items
 struct Tile {
-  int t;         // query tile index within the shard
-  int nk;        // key tiles to visit: a prefix [0, nk) of the block
-  int full_kt;   // key tiles [0, full_kt) need no mask
-  int klim;      // mask: key k allowed iff k < klim and k - i <= delta
-  long long delta;
+  int t;        // query tile index within the shard
+  int nk;       // key tiles to visit: a prefix [0, nk) of the block
+  int full_kt;  // key tiles [0, full_kt) need no mask
+  int klim;     // mask: key k allowed iff k < klim and k <= kmax(i) = floor((i + b) / q)
+  int q;        // 1 for ring blocks (kmax = i + delta); P for striped keys against consecutive queries
+  long long b;
 };
+
+__device__ __forceinline__ long long floor_div(long long x, int q) {
+  return x >= 0 ? x / q : -((-x + q - 1) / q);
+}
+__device__ __forceinline__ long long tile_kmax(const Tile& w, long long i) {
+  return w.q == 1 ? i + w.b : floor_div(i + w.b, w.q);
+}
 
 struct WorkItem {
   int bh, kvh, r, j, slot;  // kvh: the K/V head that query head bh reads
@@ -463,11 +471,25 @@ __device__ __forceinline__ int key_tile(const StepArgs& a, const WorkItem& w, in
 
 // The mask rule of the block for the rows in half h of the shard (see the
 // planner: k < klim and k - i <= delta; delta = n means no diagonal).
-__device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int h, int* klim, long long* delta) {
+__device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int h, int* klim, long long* delta,
+                                           int* q) {
   const long long n = a.n;
   *klim = a.n;
   *delta = n;
+  *q = 1;
   if (!a.causal) return;
+  if (a.decode_pos0 >= 0) {
+    // Short queries at global positions pos0 + i against the keys of block
+    // j: key k is at j n + k (contiguous) or k P + j (striped), so k is
+    // allowed iff k <= (pos0 + i) - j n, or k <= floor((pos0 + i - j) / P).
+    if (a.layout == RING_LAYOUT_STRIPED) {
+      *delta = a.decode_pos0 - j;
+      *q = a.P;
+    } else {
+      *delta = a.decode_pos0 - (long long)j * n;
+    }
+    return;
+  }
   if (a.layout == RING_LAYOUT_ZIGZAG) {
     if (j < r) {
       *klim = a.n / 2;
@@ -487,16 +509,18 @@ __device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int 
 }
 
 __device__ __forceinline__ Tile tile_work(const StepArgs& a, int r, int j, int t) {
-  Tile w{t, 0, 0, 0, 0};
+  Tile w{t, 0, 0, 0, 1, 0};
   if (t >= a.T) return w;
   const long long n = a.n;
   const long long i_min = (long long)t * kTileM;
-  const long long i_max = min(n - 1, i_min + kTileM - 1);
+  const long long i_max = min((long long)a.nq - 1, i_min + kTileM - 1);
   const int h = (a.layout == RING_LAYOUT_ZIGZAG && i_min >= n / 2) ? 1 : 0;
-  block_rule(a, r, j, h, &w.klim, &w.delta);
-  const long long last_key = min((long long)w.klim - 1, i_max + w.delta);
+  block_rule(a, r, j, h, &w.klim, &w.b, &w.q);
+  // kmax is non-decreasing in i: the last row bounds the tiles, the first
+  // row the tiles every row may use in full
+  const long long last_key = min((long long)w.klim - 1, tile_kmax(w, i_max));
   w.nk = last_key < 0 ? 0 : (int)min((long long)a.KT, last_key / kTileN + 1);
-  const long long common = min((long long)w.klim, i_min + w.delta + 1);  // keys allowed for every row
+  const long long common = min((long long)w.klim, tile_kmax(w, i_min) + 1);  // keys allowed for every row
   w.full_kt = common <= 0 ? 0 : (int)min((long long)w.nk, common / kTileN);
   return w;
 }
@@ -523,9 +547,10 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   w.fwd_lo = 2 * u;
   w.fwd_hi = min(2 * u + 2, a.KT);
   // Rotating is needed only when the sent tiles are inside the computed
-  // prefix but not at its end; then both tiles visit the whole prefix
-  // (blocks without a diagonal), so one order serves both.
-  w.rot = (w.fwd_hi < w.nk) ? w.fwd_hi : 0;
+  // prefix but not at its end; then both tiles of a ring block visit the
+  // whole prefix (blocks without a diagonal), so one order serves both.
+  // Short queries (decode) send nothing and keep the natural order.
+  w.rot = (a.decode_pos0 < 0 && w.fwd_hi < w.nk) ? w.fwd_hi : 0;
   w.slot = a.kv_mode == kKvSlotR ? w.r : (a.kv_mode == kKvSlotJ ? j : 0);
   return w;
 }
@@ -564,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Tile tw = t_sm == 0 ? w.tile[0] : w.tile[1];
   const int quad = warp & 3;
   const long long i_row = (long long)tw.t * kTileM + quad * 32 + lane;
-  const bool valid = i_row < a.n;
+  const bool valid = i_row < a.nq;
   const bool in_range = tw.t < a.T;  // the tile exists (its rows may still be partly past n)
   const long long half_n = a.n / 2;
   const long long g =
@@ -792,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // order of a FULL block the ragged last tile comes at KT - 1 - rot (the
     // tiles after it take the mask too, which leaves them unchanged)
     const int mask_from = w.rot == 0 ? tw.full_kt : (tw.full_kt < w.nk ? w.nk - 1 - w.rot : w.nk);
-    const long long i = i_row;
+    const long long kmax_row = tile_kmax(tw, i_row);  // this row's last allowed key
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + L::tmem_s(t);
     const uint32_t o_addr = tmem + lane_off + L::tmem_o(t);
@@ -820,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < kTileN; ++e) {
           const long long key = kbase + e;
-          if (key >= tw.klim || key - i > tw.delta) s[e] = -INFINITY;
+          if (key >= tw.klim || key > kmax_row) s[e] = -INFINITY;
         }
       }
       // row max: eight independent chains of 3-input max, then a tree

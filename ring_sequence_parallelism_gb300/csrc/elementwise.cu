@@ -144,7 +144,50 @@ __global__ void pack_kv_kernel(const uint4* __restrict__ k, const uint4* __restr
   }
 }
 
+// Split-K/V decode: merge the P shard states of every row and finalize
+// ([RA-CN] the query is sent to every K/V shard, each returns a local
+// state, and the states are merged exactly; [GRA] "Why partial results are
+// allowed to merge"): m = max_s m_s, each side scaled by e^{m_s - m} (0 for
+// an empty side), out = O~/l, lse = m + ln l.  One warp per row: lanes hold
+// d/32 columns; states are [P][rows] and [P][rows][d].
+__global__ void merge_shards_kernel(const float* __restrict__ m, const float* __restrict__ l,
+                                    const float* __restrict__ o, float* __restrict__ out,
+                                    float* __restrict__ lse, long long rows, int d, int P) {
+  const int lane = threadIdx.x % 32;
+  const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+  for (long long row = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; row < rows; row += warps) {
+    float mx = -INFINITY;
+    for (int s = 0; s < P; ++s) mx = fmaxf(mx, m[(long long)s * rows + row]);
+    float lsum = 0.0f;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int per = d / 32;  // 2 or 4 columns per lane
+    if (mx != -INFINITY) {
+      for (int s = 0; s < P; ++s) {
+        const float ms = m[(long long)s * rows + row];
+        if (ms == -INFINITY) continue;
+        const float w = expf(ms - mx);
+        lsum += w * l[(long long)s * rows + row];
+        const float* src = o + ((long long)s * rows + row) * d + lane * per;
+        for (int c = 0; c < per; ++c) acc[c] += w * src[c];
+      }
+    }
+    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+    float* dst = out + row * d + lane * per;
+    for (int c = 0; c < per; ++c) dst[c] = acc[c] * inv;
+    if (lane == 0) lse[row] = lsum > 0.0f ? mx + logf(lsum) : -INFINITY;
+  }
+}
+
 }  // namespace
+
+int launch_merge_shards(const float* m, const float* l, const float* o, float* out, float* lse, long long rows,
+                        int d, int P, void* stream) {
+  if (rows <= 0) return 0;
+  const long long blocks = (rows + 7) / 8;  // 8 warps a block
+  merge_shards_kernel<<<(int)(blocks < 65535 * 32 ? blocks : 65535 * 32), 256, 0,
+                        static_cast<cudaStream_t>(stream)>>>(m, l, o, out, lse, rows, d, P);
+  return (int)cudaGetLastError();
+}
 
 int launch_state_init(float* m, float* l, float* o, long long rows, int d, void* stream) {
   const int d4 = d / 4;

@@ -178,6 +178,8 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
   a.P = P;
   a.BH = BH;
   a.G = p.H / p.Hkv;
+  a.nq = (int)p.n;
+  a.decode_pos0 = -1;
   a.T = p.T;
   a.KT = p.KT;
   a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : (p.layout == RING_LAYOUT_ZIGZAG ? kQZigzag : kQContiguous);

@@ -97,6 +97,9 @@ struct StepArgs {
   int forward;       // send the CTA's key tiles 2u, 2u+1 to slot r+1 of the next maps
   int state_tiled;   // state in [BH][P][T][D/8][128][8] (O~) and [BH][P][T][128] (m, l) blocks
   int G;             // query heads per K/V head: query head bh reads K/V head bh / G
+  int nq;            // query rows per shard (n for the ring; the short query length otherwise)
+  long long decode_pos0;  // >= 0: queries at global positions pos0 + i against block j's keys
+                          //       (the causal rule from global positions; see ring_attn_decode)
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned short active[kMaxShards];
 };
@@ -115,6 +118,8 @@ int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map
 int launch_state_init(float* m, float* l, float* o, long long rows, int d, void* stream);
 int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* lb, const float* ob,
                  long long rows, int d, void* stream);
+int launch_merge_shards(const float* m, const float* l, const float* o, float* out, float* lse, long long rows,
+                        int d, int P, void* stream);
 int launch_finalize(const float* m, const float* l, const float* o, float* out, float* lse, int BH,
                     long long n, int d, int P, int r, int layout, long long N, void* stream);
 int launch_pack_kv(const void* k, const void* v, void* kbuf, void* vbuf, int BH, long long n, int d,
