@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--decode", type=int, default=0, metavar="LQ",
+                    help="measure split-K/V decode of LQ new queries over the workload's K/V cache instead")
     return ap.parse_args()
 
 
@@ -371,12 +373,69 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_decode(args, w):
+    """Split-K/V decode / short-query prefill (ring_attn_decode): LQ queries
+    at the end of the workload's sequence over its K/V cache, inputs resident,
+    K calls timed with CUDA events.  The roofline is HBM for short queries:
+    algorithmic bytes per call = the K/V cache read once + q read + the P
+    shard states written and read back + out and lse written."""
+    import torch
+
+    import ring_sequence_parallelism_gb300 as ra
+    from ring_sequence_parallelism_gb300.inputs import make_workload
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    Lq = args.decode
+    q_all, k, v = (x.to("cuda") for x in make_workload(w))
+    q = q_all[:, :, :Lq].contiguous()
+    att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
+    for _ in range(args.warmup):
+        out, lse = att.decode(q, k, v)
+    att.check()
+    stream = torch.cuda.current_stream()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            att.decode(q, k, v, out, lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    att.check()
+    ms = e0.elapsed_time(e1) / args.steps
+    BH = w.B * w.H
+    pairs = sum(min(w.N, w.N - Lq + i + 1) for i in range(Lq)) if w.causal else Lq * w.N
+    flops = 4 * w.d * BH * pairs
+    state_bytes = 2 * w.P * BH * Lq * (w.d + 2) * 4
+    bytes_ = 2 * w.B * w.kv_heads * w.N * w.d * 2 + BH * Lq * w.d * 2 + state_bytes + BH * Lq * (w.d + 1) * 4
+    pk, pk_kind = peaks()
+    hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    gbs = bytes_ / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"split-K/V decode of {Lq} queries over the {w.N}-token cache, causal-adjusted TFLOP/s",
+        "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": dict(config_of(w), Lq=Lq),
+        "tokens_per_s": w.B * Lq / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "peak_kind": f"hbm_gbs ({pk_kind})", "algorithmic_bytes": bytes_,
+                     "kernels": "block_partial_kernel (P shard states) + merge_shards_kernel"},
+        "clocks": clocks.summary(),
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    att.close()
+
+
 def main():
     args = parse()
     from ring_sequence_parallelism_gb300.inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.decode > 0:
+        run_decode(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)
