@@ -86,11 +86,11 @@ class Oracle:
         L.oracle_owner.restype = None
         L.oracle_block_at.argtypes = [_I, _I, _I]
         L.oracle_block_at.restype = _I
-        L.oracle_dense_rows.argtypes = [_I, _L, _I, _I, _P, _P, _P, _L, _P, _P, _P, _I]
+        L.oracle_dense_rows.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _L, _P, _P, _P, _I]
         L.oracle_dense_rows.restype = _I
-        L.oracle_ring_rows.argtypes = [_I, _L, _I, _I, _I, _I, _P, _P, _P, _L, _P, _P, _P, _P, _I]
+        L.oracle_ring_rows.argtypes = [_I, _L, _I, _I, _I, _L, _I, _P, _P, _P, _L, _P, _P, _P, _P, _I]
         L.oracle_ring_rows.restype = _I
-        L.oracle_block_partial.argtypes = [_I, _L, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I]
+        L.oracle_block_partial.argtypes = [_I, _L, _I, _I, _I, _L, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I]
         L.oracle_block_partial.restype = _I
         L.oracle_merge_states.argtypes = [_L, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]
         L.oracle_merge_states.restype = _I
@@ -98,7 +98,7 @@ class Oracle:
         L.oracle_merge_inplace.restype = _I
         L.oracle_finalize.argtypes = [_L, _I, _P, _P, _P, _P, _P]
         L.oracle_finalize.restype = _I
-        L.oracle_naive_block_sum.argtypes = [_I, _L, _I, _I, _I, _I, _P, _P, _P, _P]
+        L.oracle_naive_block_sum.argtypes = [_I, _L, _I, _I, _I, _L, _I, _P, _P, _P, _P]
         L.oracle_naive_block_sum.restype = _I
 
     # -- small helpers -------------------------------------------------
@@ -132,38 +132,39 @@ class Oracle:
         return r, r.size
 
     # -- the method ------------------------------------------------------
-    def dense(self, q, k, v, causal: bool, rows=None):
+    def dense(self, q, k, v, causal: bool, rows=None, window: int = 0):
         q, k, v = self._qkv(q, k, v)
         BH, N, d = q.shape
         r, R = self._rows(rows, N)
         out = np.empty((BH, R, d), np.float64)
         lse = np.empty((BH, R), np.float64)
-        rc = self.lib.oracle_dense_rows(BH, N, d, int(causal), _ptr(q), _ptr(k), _ptr(v), R, _ptr(r),
+        rc = self.lib.oracle_dense_rows(BH, N, d, int(causal), int(window), _ptr(q), _ptr(k), _ptr(v), R, _ptr(r),
                                         _ptr(out), _ptr(lse), self.nthreads)
         if rc != 0:
             raise RuntimeError(f"oracle_dense_rows failed: {rc}")
         return out, lse
 
-    def ring(self, q, k, v, P: int, causal: bool, layout: int, rows=None, visits: bool = False):
+    def ring(self, q, k, v, P: int, causal: bool, layout: int, rows=None, visits: bool = False, window: int = 0):
         q, k, v = self._qkv(q, k, v)
         BH, N, d = q.shape
         r, R = self._rows(rows, N)
         out = np.empty((BH, R, d), np.float64)
         lse = np.empty((BH, R), np.float64)
         cnt = np.zeros((BH, N, N), np.int64) if visits else None
-        rc = self.lib.oracle_ring_rows(BH, N, d, P, int(causal), layout, _ptr(q), _ptr(k), _ptr(v), R,
+        rc = self.lib.oracle_ring_rows(BH, N, d, P, int(causal), int(window), layout, _ptr(q), _ptr(k), _ptr(v), R,
                                        _ptr(r), _ptr(out), _ptr(lse), _ptr(cnt), self.nthreads)
         if rc != 0:
             raise RuntimeError(f"oracle_ring_rows failed: {rc}")
         return (out, lse, cnt) if visits else (out, lse)
 
-    def block_partial(self, q_shard, k_block, v_block, P: int, causal: bool, layout: int, r: int, j: int):
+    def block_partial(self, q_shard, k_block, v_block, P: int, causal: bool, layout: int, r: int, j: int,
+                      window: int = 0):
         q, k, v = self._qkv(q_shard, k_block, v_block)
         BH, n, d = q.shape
         m = np.empty((BH, n), np.float64)
         l = np.empty((BH, n), np.float64)
         o = np.empty((BH, n, d), np.float64)
-        rc = self.lib.oracle_block_partial(BH, n, d, P, int(causal), layout, r, j, _ptr(q), _ptr(k), _ptr(v),
+        rc = self.lib.oracle_block_partial(BH, n, d, P, int(causal), int(window), layout, r, j, _ptr(q), _ptr(k), _ptr(v),
                                            _ptr(m), _ptr(l), _ptr(o), self.nthreads)
         if rc != 0:
             raise RuntimeError(f"oracle_block_partial failed: {rc}")
@@ -209,11 +210,11 @@ class Oracle:
             raise RuntimeError(f"oracle_finalize failed: {rc}")
         return out, lse
 
-    def naive_block_sum(self, q, k, v, P: int, causal: bool, layout: int):
+    def naive_block_sum(self, q, k, v, P: int, causal: bool, layout: int, window: int = 0):
         q, k, v = self._qkv(q, k, v)
         BH, N, d = q.shape
         out = np.empty((BH, N, d), np.float64)
-        rc = self.lib.oracle_naive_block_sum(BH, N, d, P, int(causal), layout, _ptr(q), _ptr(k), _ptr(v),
+        rc = self.lib.oracle_naive_block_sum(BH, N, d, P, int(causal), int(window), layout, _ptr(q), _ptr(k), _ptr(v),
                                              _ptr(out))
         if rc != 0:
             raise RuntimeError(f"oracle_naive_block_sum failed: {rc}")

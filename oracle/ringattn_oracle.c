@@ -31,7 +31,12 @@
  *     zigzag: the sequence cut into 2P chunks of c = n/2 tokens, shard r
  *     holding chunk r then chunk 2P-1-r ([GRA] "Striping the sequence to
  *     flatten the triangle"), local rows in that order;
- *   - causal: key position <= query position.
+ *   - causal: key position <= query position;
+ *   - sliding window W > 0 (with the causal mask): a query also drops the
+ *     keys W or more positions behind it, i.e. it sees itself and the W-1
+ *     tokens before it ([RA-CN] "正确性测试应覆盖哪些边界" lists
+ *     sliding-window masks among the cases to cover; the window is the
+ *     usual causal local-attention window).
  *
  * All inputs Q, K, V are bf16 bit patterns (uint16) in natural token order,
  * laid out [BH][N][d]; they are widened exactly to double.
@@ -115,7 +120,8 @@ int oracle_block_at(int P, int r, int s) {
   return j;
 }
 
-static int allowed(int causal, long pos_q, long pos_k) {
+static int allowed(int causal, long window, long pos_q, long pos_k) {
+  if (window > 0 && pos_q - pos_k >= window) return 0;
   return !causal || pos_k <= pos_q;
 }
 
@@ -133,7 +139,7 @@ static double dot_q_k(const uint16_t* q, const uint16_t* k, int d) {
  * rows == NULL means every position 0..N-1 (nrows must equal N then).
  * out is [BH][nrows][d], lse is [BH][nrows].
  */
-int oracle_dense_rows(int BH, long N, int d, int causal, const uint16_t* q,
+int oracle_dense_rows(int BH, long N, int d, int causal, long window, const uint16_t* q,
                       const uint16_t* k, const uint16_t* v, long nrows,
                       const long* rows, double* out, double* lse,
                       int nthreads) {
@@ -159,18 +165,18 @@ int oracle_dense_rows(int BH, long N, int d, int causal, const uint16_t* q,
       const uint16_t* vb = v + (size_t)bh * N * d;
       double m = -INFINITY;
       for (long kk = 0; kk < N; ++kk) {
-        if (!allowed(causal, t, kk)) continue;
+        if (!allowed(causal, window, t, kk)) continue;
         s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
         if (s[kk] > m) m = s[kk];
       }
       double sum = 0.0;
       for (long kk = 0; kk < N; ++kk)
-        if (allowed(causal, t, kk)) sum += exp(s[kk] - m);
+        if (allowed(causal, window, t, kk)) sum += exp(s[kk] - m);
       double l = m + log(sum);
       double* o = out + (size_t)idx * d;
       for (int c = 0; c < d; ++c) o[c] = 0.0;
       for (long kk = 0; kk < N; ++kk) {
-        if (!allowed(causal, t, kk)) continue;
+        if (!allowed(causal, window, t, kk)) continue;
         double w = exp(s[kk] - l);
         const uint16_t* vr = vb + (size_t)kk * d;
         for (int c = 0; c < d; ++c) o[c] += w * widen_bf16(vr[c]);
@@ -193,11 +199,11 @@ int oracle_dense_rows(int BH, long N, int d, int causal, const uint16_t* q,
  */
 static void row_block_state(const uint16_t* qrow, long pos_q, const uint16_t* kb,
                             const uint16_t* vb, const long* kpos, long nk, int d,
-                            int causal, double scale, double* s, double* m_out,
+                            int causal, long window, double scale, double* s, double* m_out,
                             double* l_out, double* o_out, long* visit_row) {
   double m = -INFINITY;
   for (long kk = 0; kk < nk; ++kk) {
-    if (!allowed(causal, pos_q, kpos[kk])) continue;
+    if (!allowed(causal, window, pos_q, kpos[kk])) continue;
     s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
     if (s[kk] > m) m = s[kk];
   }
@@ -205,7 +211,7 @@ static void row_block_state(const uint16_t* qrow, long pos_q, const uint16_t* kb
   for (int c = 0; c < d; ++c) o_out[c] = 0.0;
   if (m != -INFINITY) {
     for (long kk = 0; kk < nk; ++kk) {
-      if (!allowed(causal, pos_q, kpos[kk])) continue;
+      if (!allowed(causal, window, pos_q, kpos[kk])) continue;
       double w = exp(s[kk] - m);
       l += w;
       const uint16_t* vr = vb + (size_t)kk * d;
@@ -248,7 +254,7 @@ static void merge_pair(double ma, double la, const double* oa, double mb,
  * indexed like oracle_dense_rows.  visits (NULL or [BH][N][N] counters)
  * receives +1 for every (query, key) pair the simulation used.
  */
-int oracle_ring_rows(int BH, long N, int d, int P, int causal, int layout,
+int oracle_ring_rows(int BH, long N, int d, int P, int causal, long window, int layout,
                      const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      long nrows, const long* rows, double* out, double* lse,
                      long* visits, int nthreads) {
@@ -299,7 +305,7 @@ int oracle_ring_rows(int BH, long N, int d, int P, int causal, int layout,
                  sizeof(uint16_t) * d);
         }
         double mb, lb;
-        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, scale, s, &mb,
+        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, window, scale, s, &mb,
                         &lb, ob, visit_row);
         double mn, ln;
         merge_pair(m, l, ost, mb, lb, ob, d, &mn, &ln, otmp);
@@ -329,7 +335,7 @@ int oracle_ring_rows(int BH, long N, int d, int P, int causal, int layout,
  * q_shard, k_block, v_block are shard-major [BH][n][d] bf16 bit patterns.
  * Outputs m, l [BH][n] and o [BH][n][d] as defined in row_block_state.
  */
-int oracle_block_partial(int BH, long n, int d, int P, int causal, int layout,
+int oracle_block_partial(int BH, long n, int d, int P, int causal, long window, int layout,
                          int r, int j, const uint16_t* q_shard,
                          const uint16_t* k_block, const uint16_t* v_block,
                          double* m, double* l, double* o, int nthreads) {
@@ -359,7 +365,7 @@ int oracle_block_partial(int BH, long n, int d, int P, int causal, int layout,
       row_block_state(q_shard + (size_t)idx * d,
                       oracle_position(layout, n, P, r, i),
                       k_block + (size_t)bh * n * d, v_block + (size_t)bh * n * d,
-                      kpos, n, d, causal, scale, s, &m[idx], &l[idx],
+                      kpos, n, d, causal, window, scale, s, &m[idx], &l[idx],
                       o + (size_t)idx * d, NULL);
     }
     free(s);
@@ -440,7 +446,7 @@ int oracle_finalize(long rows, int d, const double* m, const double* l,
  *   out_naive = sum over blocks j with an allowed key of softmax(S^(j)) V_j.
  * Natural order in and out, out is [BH][N][d].
  */
-int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, int layout,
+int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, long window, int layout,
                            const uint16_t* q, const uint16_t* k,
                            const uint16_t* v, double* out) {
   if (BH <= 0 || N <= 0 || d <= 0 || !layout_ok(layout, N, P)) return -1;
@@ -470,7 +476,7 @@ int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, int layout,
                  sizeof(uint16_t) * d);
         }
         double mb, lb;
-        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, scale, s, &mb,
+        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, window, scale, s, &mb,
                         &lb, ob, NULL);
         if (lb > 0.0)
           for (int c = 0; c < d; ++c) o[c] += ob[c] / lb;

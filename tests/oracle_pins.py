@@ -146,6 +146,45 @@ def pin_sdpa(orc):
             _close(lse, ref_lse.numpy(), 1e-12, "sdpa lse")
 
 
+def band_matrix(N, window):
+    """Causal sliding window: query t sees keys t-window+1 .. t."""
+    t = np.arange(N)
+    dist = t[:, None] - t[None, :]
+    return (dist >= 0) & (dist < window)
+
+
+def pin_window_closed_forms(orc):
+    """Sliding window ([RA-CN] "正确性测试应覆盖哪些边界": sliding-window masks):
+    window 1 leaves each query its own key only, so out_t = v_t and
+    lse_t = s_tt exactly; a window of N or more is the plain causal mask."""
+    BH, N, d = 2, 19, 8
+    q, k, v = rand_bits((BH, N, d), 131), rand_bits((BH, N, d), 132), rand_bits((BH, N, d), 133)
+    out, lse = orc.dense(q, k, v, True, window=1)
+    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    _close(out, vf, 0.0, "window 1 out = v")
+    _close(lse, np.einsum("btd,btd->bt", qf, kf) / math.sqrt(d), 1e-13, "window 1 lse = own score")
+    ref = orc.dense(q, k, v, True)
+    for w in (N, N + 5):
+        got = orc.dense(q, k, v, True, window=w)
+        _close(got[0], ref[0], 0.0, f"window {w} = causal out")
+        _close(got[1], ref[1], 0.0, f"window {w} = causal lse")
+
+
+def pin_window_sdpa(orc):
+    """Sliding window against torch's scaled_dot_product_attention in float64
+    with the explicit band mask."""
+    BH, N, d = 2, 37, 16
+    q, k, v = rand_bits((BH, N, d), 141), rand_bits((BH, N, d), 142), rand_bits((BH, N, d), 143)
+    qt, kt, vt = (torch.from_numpy(bits_to_f64(x)) for x in (q, k, v))
+    for w in (2, 3, 8, 20):
+        band = torch.from_numpy(band_matrix(N, w))
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=band)
+        sc = (torch.einsum("bqd,bkd->bqk", qt, kt) / math.sqrt(d)).masked_fill(~band, float("-inf"))
+        out, lse = orc.dense(q, k, v, True, window=w)
+        _close(out, ref.numpy(), 1e-12, f"window {w} sdpa out")
+        _close(lse, torch.logsumexp(sc, dim=-1).numpy(), 1e-12, f"window {w} sdpa lse")
+
+
 # ------------------------------------------------------------------ the ring
 def pin_ring_equals_dense(orc):
     """The ring reaches the dense result ([GRA] "Why partial results are
@@ -161,6 +200,21 @@ def pin_ring_equals_dense(orc):
                     tol = 1e-13 if P == 1 else 1e-12
                     _close(out, ref_out, tol, f"ring=dense out P={P} layout={layout} causal={causal}")
                     _close(lse, ref_lse, tol, f"ring=dense lse P={P} layout={layout} causal={causal}")
+
+
+def pin_window_ring(orc):
+    """With a sliding window the ring still reaches the dense result, in
+    every layout, and visits exactly the pairs inside the band once."""
+    BH, N, d = 1, 24, 4
+    q, k, v = rand_bits((BH, N, d), 151), rand_bits((BH, N, d), 152), rand_bits((BH, N, d), 153)
+    for w in (1, 2, 5, 13):
+        ref_out, ref_lse = orc.dense(q, k, v, True, window=w)
+        for P in (1, 2, 3, 4, 6):
+            for layout in layouts_for(N, P):
+                out, lse, cnt = orc.ring(q, k, v, P, True, layout, visits=True, window=w)
+                _close(out, ref_out, 1e-12, f"window ring out w={w} P={P} layout={layout}")
+                _close(lse, ref_lse, 1e-12, f"window ring lse w={w} P={P} layout={layout}")
+                assert np.array_equal(cnt[0], band_matrix(N, w).astype(np.int64)), (w, P, layout)
 
 
 def pin_layouts_agree(orc):
@@ -347,7 +401,10 @@ ALL_PINS = [
     pin_causal_first_row,
     pin_dominant_key,
     pin_sdpa,
+    pin_window_closed_forms,
+    pin_window_sdpa,
     pin_ring_equals_dense,
+    pin_window_ring,
     pin_layouts_agree,
     pin_visits_exactly_once,
     pin_shard_work_closed_forms,

@@ -36,8 +36,11 @@ MUTATIONS = [
     ("zigzag halves in the wrong order",
      "return i < c ? (long)r * c + i : (long)(2 * P - 1 - r) * c + (i - c);",
      "return i < c ? (long)(2 * P - 1 - r) * c + i : (long)r * c + (i - c);", None),
+    ("sliding window off by one", "if (window > 0 && pos_q - pos_k >= window) return 0;",
+     "if (window > 0 && pos_q - pos_k > window) return 0;", None),
+    ("sliding window ignored", "if (window > 0 && pos_q - pos_k >= window) return 0;", "", None),
     ("block partial ignores the mask in the sum",
-     "      if (!allowed(causal, pos_q, kpos[kk])) continue;\n      double w",
+     "      if (!allowed(causal, window, pos_q, kpos[kk])) continue;\n      double w",
      "      double w", None),
 ]
 
