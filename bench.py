@@ -186,9 +186,9 @@ def oracle_sample(w, q, k, v, seconds: float, seed: int = 4242):
     while True:
         rows = sample_rows(w.N, rows_per_head, seed=seed).numpy()
         t0 = time.perf_counter()
-        orc.dense(qf, kf, vf, w.causal, rows=rows)
+        orc.dense(qf, kf, vf, w.causal, rows=rows, window=w.window)
         t_used = time.perf_counter() - t0
-        keys = (rows + 1).sum() if w.causal else rows.size * w.N
+        keys = (rows + 1).clip(max=w.window or None).sum() if w.causal else rows.size * w.N
         flops = 4 * w.d * BH * int(keys)
         if t_used >= seconds / 4 or rows_per_head >= w.N:
             break
@@ -222,9 +222,9 @@ def run_reference(args, w):
     times, flops = [], 0
     for i in range(args.warmup + args.steps):
         rows = sample_rows(w.N, rph, seed=5000 + i).numpy()
-        keys = (rows + 1).sum() if w.causal else rows.size * w.N
+        keys = (rows + 1).clip(max=w.window or None).sum() if w.causal else rows.size * w.N
         t0 = time.perf_counter()
-        orc.dense(qf, kf, vf, w.causal, rows=rows)
+        orc.dense(qf, kf, vf, w.causal, rows=rows, window=w.window)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -246,7 +246,7 @@ def run_reference(args, w):
 
 def config_of(w):
     return {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N": w.N, "d": w.d, "P": w.P,
-            "layout": w.layout, "causal": w.causal, "global_batch": w.B, "seq_len": w.N,
+            "layout": w.layout, "causal": w.causal, "window": w.window, "global_batch": w.B, "seq_len": w.N,
             "inputs": "Q,K,V ~ N(0,1) rounded to bf16" + (", 1% of key rows x8" if w.key_boost_frac else ""),
             "l2": l2_note(w)}
 
@@ -275,6 +275,8 @@ def run_ours(args, w):
     q, k, v = (x.to("cuda", non_blocking=True) for x in (q_h, k_h, v_h))
     torch.cuda.synchronize()
     att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
+    if w.window:
+        att.set_option(ra.RING_OPT_WINDOW, w.window)
     out = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device="cuda")
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
     att.set_option(ra.RING_OPT_TIMING, 1)

@@ -118,7 +118,14 @@ typedef enum {
    * the kernel then drains what it started, frees its tensor memory and
    * returns, and ring_attn_check reports RING_ERR_TIMEOUT.  The outputs of
    * such a call are undefined.  Exists to test the bounded-wait error path. */
-  RING_OPT_DEBUG_DROP_V_LOADS = 3
+  RING_OPT_DEBUG_DROP_V_LOADS = 3,
+  /* Causal sliding window W (tokens; 0 = none, the default): a query sees
+   * itself and the W-1 tokens before it ([RA-CN] "正确性测试应覆盖哪些边界"
+   * lists sliding-window masks).  Applies to ring_attn_fwd, block_partial,
+   * the planner queries and ring_attn_decode.  Rebuilds the plan; needs the
+   * causal mask and the CONTIGUOUS or STRIPED layout (RING_ERR_UNSUPPORTED
+   * otherwise, the handle keeping its previous window). */
+  RING_OPT_WINDOW = 4
 } ring_option_t;
 
 /* Create a handle for one problem shape.  Validates the shape and builds the
@@ -179,6 +186,13 @@ RINGATTN_API int ring_attn_plan_block(ring_attn_t h, int r, int step, int* j, in
  * "No diagonal" is returned as delta = n.  Any output pointer may be NULL. */
 RINGATTN_API int ring_attn_plan_mask(ring_attn_t h, int r, int step, long long row, long long* key_limit,
                                      long long* delta);
+
+/* The keys local row `row` of shard r sees at ring step s, in the block's
+ * local columns: first .. last inclusive (first > last: none).  Covers every
+ * mask the handle applies (causal, layout, sliding window).  Any output
+ * pointer may be NULL. */
+RINGATTN_API int ring_attn_plan_key_range(ring_attn_t h, int r, int step, long long row, long long* first,
+                                          long long* last);
 
 /* Per-shard totals over all P steps: allowed (q, k) pairs[P] and the
  * 128x128 MMA tiles the kernel computes[P] (any pointer may be NULL). */

@@ -18,7 +18,8 @@ import ctypes
 
 from . import _lib
 from ._lib import (RING_BLOCK_DIAG, RING_BLOCK_FULL, RING_BLOCK_PARTIAL, RING_BLOCK_SKIP,  # noqa: F401
-                   RING_LAYOUT_CONTIGUOUS, RING_LAYOUT_STRIPED, RING_LAYOUT_ZIGZAG, RING_OPT_DEBUG_DROP_V_LOADS, RING_OPT_ROTATION, RING_OPT_TIMING,
+                   RING_LAYOUT_CONTIGUOUS, RING_LAYOUT_STRIPED, RING_LAYOUT_ZIGZAG, RING_OPT_DEBUG_DROP_V_LOADS,
+                   RING_OPT_WINDOW, RING_OPT_ROTATION, RING_OPT_TIMING,
                    RING_OPT_WAIT_LIMIT_NS,
                    RingAttnError, RingState)
 
@@ -133,6 +134,13 @@ class RingAttention:
         klim, delta = ctypes.c_longlong(), ctypes.c_longlong()
         _lib.check(self._lib.ring_attn_plan_mask(self.handle, r, step, row, ctypes.byref(klim), ctypes.byref(delta)))
         return klim.value, delta.value
+
+    def plan_key_range(self, r: int, step: int, row: int):
+        """(first, last): the block-local keys row `row` of shard r sees at step s (first > last: none)."""
+        first, last = ctypes.c_longlong(), ctypes.c_longlong()
+        _lib.check(self._lib.ring_attn_plan_key_range(self.handle, r, step, row, ctypes.byref(first),
+                                                      ctypes.byref(last)))
+        return first.value, last.value
 
     def shard_work(self):
         pairs = (ctypes.c_longlong * self.P)()

@@ -25,7 +25,7 @@ RING_LAYOUT_CONTIGUOUS = 0
 RING_LAYOUT_STRIPED = 1
 RING_LAYOUT_ZIGZAG = 2
 RING_BLOCK_SKIP, RING_BLOCK_FULL, RING_BLOCK_DIAG, RING_BLOCK_PARTIAL = 0, 1, 2, 3
-RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_WAIT_LIMIT_NS, RING_OPT_DEBUG_DROP_V_LOADS = 0, 1, 2, 3
+RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_WAIT_LIMIT_NS, RING_OPT_DEBUG_DROP_V_LOADS, RING_OPT_WINDOW = 0, 1, 2, 3, 4
 
 # Every symbol include/ringattn.h declares, with (restype, argtypes).
 _vp = ctypes.c_void_p
@@ -50,6 +50,7 @@ SIGNATURES = {
     "ring_attn_workspace_size": (_i, [_vp, ctypes.POINTER(ctypes.c_size_t)]),
     "ring_attn_plan_block": (_i, [_vp, _i, _i, _pi, _pi, _pll]),
     "ring_attn_plan_mask": (_i, [_vp, _i, _i, ctypes.c_longlong, _pll, _pll]),
+    "ring_attn_plan_key_range": (_i, [_vp, _i, _i, ctypes.c_longlong, _pll, _pll]),
     "ring_attn_shard_work": (_i, [_vp, _pll, _pll]),
     "ring_attn_step_work": (_i, [_vp, _i, _pll, _pll]),
     "ring_attn_state_init": (_i, [_vp, RingState, _vp]),

@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -210,6 +211,7 @@ StepArgs base_args(const ring_attn* h) {
   a.G = p.H / p.Hkv;
   a.nq = (int)p.n;
   a.decode_pos0 = -1;
+  a.window = p.window;
   a.T = p.T;
   a.KT = p.KT;
   a.causal = p.causal;
@@ -299,6 +301,18 @@ int ring_attn_plan_mask(ring_attn_t h, int r, int step, long long row, long long
   return RING_OK;
 }
 
+int ring_attn_plan_key_range(ring_attn_t h, int r, int step, long long row, long long* first, long long* last) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  const Plan& p = h->plan;
+  if (r < 0 || r >= p.P || step < 0 || step >= p.P) return fail(RING_ERR_INVALID_ARG, "r or step out of range");
+  if (row < 0 || row >= p.n) return fail(RING_ERR_INVALID_ARG, "row out of range");
+  const BlockPlan& b = p.at(step, r);
+  const int half = row_half(p.layout, p.n, row);
+  if (first) *first = std::max(0LL, row + b.lodelta);
+  if (last) *last = std::min(b.klim[half], std::max(0LL, row + b.hdelta[half] + 1)) - 1;
+  return RING_OK;
+}
+
 int ring_attn_shard_work(ring_attn_t h, long long* pairs, long long* tiles) {
   if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
   for (int r = 0; r < h->plan.P; ++r) {
@@ -331,6 +345,17 @@ int ring_attn_set_option(ring_attn_t h, int option, long long value) {
       if (value <= 0) return fail(RING_ERR_INVALID_ARG, "wait limit must be positive");
       h->wait_limit_ns = (unsigned long long)value;
       return RING_OK;
+    case RING_OPT_WINDOW: {
+      if (value < 0) return fail(RING_ERR_INVALID_ARG, "window must be >= 0");
+      Plan np;
+      std::string err;
+      const Plan& p = h->plan;
+      int rc = build_plan(&np, p.B, p.H, p.N, p.d, p.P, p.causal, p.layout, &err, value);
+      if (rc != RING_OK) return fail(rc, err);
+      np.Hkv = p.Hkv;
+      h->plan = std::move(np);
+      return RING_OK;
+    }
     case RING_OPT_DEBUG_DROP_V_LOADS:
       if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "debug option must be 0 or 1");
       h->debug_drop_v = (int)value;

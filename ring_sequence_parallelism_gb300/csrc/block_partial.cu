@@ -437,13 +437,17 @@ __device__ __forceinline__ void fence_async_smem() {
 
 // ------------------------------------------------------------- work items
 struct Tile {
-  int t;        // query tile index within the shard
-  int nk;       // key tiles to visit: a prefix [0, nk) of the block
-  int full_kt;  // key tiles [0, full_kt) need no mask
-  int klim;     // mask: key k allowed iff k < klim and k <= kmax(i) = floor((i + b) / q)
-  int q;        // 1 for ring blocks (kmax = i + delta); P for striped keys against consecutive queries
-  long long b;
+  int t;                  // query tile index within the shard
+  int jb, je;             // loop indices [jb, je) this tile computes
+  int mask_lo, mask_from;  // loop indices below mask_lo or from mask_from take the mask
+  int klim;               // mask: key k allowed iff kmin(i) <= k, k < klim and k <= kmax(i)
+  int q;                  // kmax(i) = floor((i + b) / q); kmin(i) = floor((i + bl) / q) + 1
+  long long b, bl;        // (bl very negative: no lower bound)
+  // key-tile space, before decode_item makes them loop indices
+  int kt_lo, kt_hi, full_lo, full_hi;
 };
+
+constexpr long long kNoLowerBound = -(1LL << 50);
 
 __device__ __forceinline__ long long floor_div(long long x, int q) {
   return x >= 0 ? x / q : -((-x + q - 1) / q);
@@ -451,77 +455,93 @@ __device__ __forceinline__ long long floor_div(long long x, int q) {
 __device__ __forceinline__ long long tile_kmax(const Tile& w, long long i) {
   return w.q == 1 ? i + w.b : floor_div(i + w.b, w.q);
 }
+__device__ __forceinline__ long long tile_kmin(const Tile& w, long long i) {
+  return (w.q == 1 ? i + w.bl : floor_div(i + w.bl, w.q)) + 1;
+}
 
 struct WorkItem {
   int bh, kvh, r, j, slot;  // kvh: the K/V head that query head bh reads
   Tile tile[2];
-  int nk;              // max of the two tiles' nk
-  int rot;             // loop index j < nk visits key tile (j + rot) mod nk
+  int lo, nk;          // loop index j < nk visits key tile lo + ((j + rot) mod nk)
+  int rot;
+  int ext0;            // loop indices from nk on load key tiles ext0, ext0 + 1, .. (sending only)
+  int np_send;         // loop indices in all when the CTA sends
   int fwd_lo, fwd_hi;  // key tiles this CTA sends along the ring
 };
 
-// Loop index -> key tile.  The computed prefix [0, nk) comes first, rotated
-// so that the sent tiles [fwd_lo, fwd_hi) end it when they lie inside it;
-// sent tiles beyond the prefix follow it.
 __device__ __forceinline__ int key_tile(const StepArgs& a, const WorkItem& w, int j) {
-  if (j >= w.nk) return max(w.fwd_lo, w.nk) + (j - w.nk);
+  if (j >= w.nk) return w.ext0 + (j - w.nk);
   const int kt = j + w.rot;
-  return kt >= w.nk ? kt - w.nk : kt;
+  return w.lo + (kt >= w.nk ? kt - w.nk : kt);
 }
 
 // The mask rule of the block for the rows in half h of the shard (see the
-// planner: k < klim and k - i <= delta; delta = n means no diagonal).
-__device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int h, int* klim, long long* delta,
-                                           int* q) {
+// planner): kmax(i) = floor((i + b) / q) and, with a sliding window W,
+// kmin(i) = floor((i + bl) / q) + 1; key limit klim.
+__device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int h, Tile* w) {
   const long long n = a.n;
-  *klim = a.n;
-  *delta = n;
-  *q = 1;
+  w->klim = a.n;
+  w->b = n;
+  w->bl = kNoLowerBound;
+  w->q = 1;
   if (!a.causal) return;
+  const long long W = a.window;
   if (a.decode_pos0 >= 0) {
     // Short queries at global positions pos0 + i against the keys of block
     // j: key k is at j n + k (contiguous) or k P + j (striped), so k is
-    // allowed iff k <= (pos0 + i) - j n, or k <= floor((pos0 + i - j) / P).
+    // allowed iff k <= (pos0 + i) - j n, or k <= floor((pos0 + i - j) / P);
+    // a window drops positions W or more behind the query.
     if (a.layout == RING_LAYOUT_STRIPED) {
-      *delta = a.decode_pos0 - j;
-      *q = a.P;
+      w->b = a.decode_pos0 - j;
+      w->q = a.P;
     } else {
-      *delta = a.decode_pos0 - (long long)j * n;
+      w->b = a.decode_pos0 - (long long)j * n;
     }
+    if (W > 0) w->bl = w->b - W;
     return;
   }
   if (a.layout == RING_LAYOUT_ZIGZAG) {
     if (j < r) {
-      *klim = a.n / 2;
+      w->klim = a.n / 2;
     } else if (j == r) {
-      *delta = 0;
+      w->b = 0;
     } else if (h == 0) {
-      *klim = 0;
+      w->klim = 0;
     }
     return;
   }
-  const long long dl = (a.layout == RING_LAYOUT_STRIPED) ? (j <= r ? 0 : -1) : (long long)(r - j) * n;
+  // contiguous: pos_q - pos_k = (r - j) n + i - k; striped: (i - k) P + (r - j)
+  const bool striped = a.layout == RING_LAYOUT_STRIPED;
+  const long long dl = striped ? (j <= r ? 0 : -1) : (long long)(r - j) * n;
   if (dl <= -n) {
-    *klim = 0;
+    w->klim = 0;
   } else if (dl < n - 1) {
-    *delta = dl;
+    w->b = dl;
   }
+  if (W > 0) w->bl = striped ? floor_div((long long)(r - j) - W, a.P) : (long long)(r - j) * n - W;
 }
 
 __device__ __forceinline__ Tile tile_work(const StepArgs& a, int r, int j, int t) {
-  Tile w{t, 0, 0, 0, 1, 0};
+  Tile w{};
+  w.t = t;
+  w.q = 1;
   if (t >= a.T) return w;
   const long long n = a.n;
   const long long i_min = (long long)t * kTileM;
   const long long i_max = min((long long)a.nq - 1, i_min + kTileM - 1);
   const int h = (a.layout == RING_LAYOUT_ZIGZAG && i_min >= n / 2) ? 1 : 0;
-  block_rule(a, r, j, h, &w.klim, &w.b, &w.q);
-  // kmax is non-decreasing in i: the last row bounds the tiles, the first
-  // row the tiles every row may use in full
+  block_rule(a, r, j, h, &w);
+  // kmin and kmax are non-decreasing in i: the last row bounds the tiles
+  // from above, the first row from below, and the tiles every row may use
+  // in full lie between the first row's kmax and the last row's kmin.
   const long long last_key = min((long long)w.klim - 1, tile_kmax(w, i_max));
-  w.nk = last_key < 0 ? 0 : (int)min((long long)a.KT, last_key / kTileN + 1);
-  const long long common = min((long long)w.klim, tile_kmax(w, i_min) + 1);  // keys allowed for every row
-  w.full_kt = common <= 0 ? 0 : (int)min((long long)w.nk, common / kTileN);
+  const long long first_key = max(0LL, tile_kmin(w, i_min));
+  w.kt_hi = last_key < 0 ? 0 : (int)min((long long)a.KT, last_key / kTileN + 1);
+  w.kt_lo = (int)min((long long)w.kt_hi, first_key / kTileN);
+  const long long common_hi = min((long long)w.klim, tile_kmax(w, i_min) + 1);  // keys < this for every row
+  const long long common_lo = max(0LL, tile_kmin(w, i_max));                       // keys >= this for every row
+  w.full_hi = common_hi <= 0 ? 0 : (int)min((long long)w.kt_hi, common_hi / kTileN);
+  w.full_lo = (int)min((long long)w.kt_hi, (common_lo + kTileN - 1) / kTileN);
   return w;
 }
 
@@ -543,14 +563,50 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   w.j = j;
   w.tile[0] = tile_work(a, w.r, j, 2 * u);
   w.tile[1] = tile_work(a, w.r, j, 2 * u + 1);
-  w.nk = max(w.tile[0].nk, w.tile[1].nk);
+  // The CTA loads the union of the two tiles' key-tile ranges (the second
+  // tile's range starts and ends no earlier than the first's).
+  int lo = a.KT, hi = 0;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    if (w.tile[x].kt_hi > w.tile[x].kt_lo) {
+      lo = min(lo, w.tile[x].kt_lo);
+      hi = max(hi, w.tile[x].kt_hi);
+    }
+  }
+  if (hi == 0) lo = 0;
+  w.lo = lo;
+  w.nk = hi - lo;
   w.fwd_lo = 2 * u;
   w.fwd_hi = min(2 * u + 2, a.KT);
-  // Rotating is needed only when the sent tiles are inside the computed
-  // prefix but not at its end; then both tiles of a ring block visit the
-  // whole prefix (blocks without a diagonal), so one order serves both.
+  // Rotating is needed only when the sent tiles are inside a computed prefix
+  // but not at its end; then both tiles of a ring block visit the whole
+  // prefix (blocks without a diagonal or window), so one order serves both.
   // Short queries (decode) send nothing and keep the natural order.
-  w.rot = (a.decode_pos0 < 0 && w.fwd_hi < w.nk) ? w.fwd_hi : 0;
+  w.rot = (a.decode_pos0 < 0 && a.window == 0 && lo == 0 && w.fwd_hi < hi) ? w.fwd_hi : 0;
+  // Tiles sent along the ring come last: either they end the computed range
+  // (after the rotation), possibly followed by the ones beyond it, or they
+  // are loaded again after it (a window can leave them inside or below it).
+  if (w.fwd_lo >= lo && (w.fwd_hi >= hi || w.rot != 0)) {
+    w.ext0 = max(w.fwd_lo, hi);
+  } else {
+    w.ext0 = w.fwd_lo;
+  }
+  w.np_send = w.nk + max(0, w.fwd_hi - w.ext0);
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    Tile& tt = w.tile[x];
+    if (tt.kt_hi > tt.kt_lo) {
+      tt.jb = tt.kt_lo - lo;
+      tt.je = tt.kt_hi - lo;
+    } else {
+      tt.jb = tt.je = 0;
+    }
+    // with a rotation (lo = 0, no window) only the ragged last key tile can
+    // need the mask; it comes at loop index nk - 1 - rot, and the tiles after
+    // it take the mask too, which leaves them unchanged
+    tt.mask_lo = tt.full_lo >= tt.full_hi ? tt.je : tt.full_lo - lo;
+    tt.mask_from = w.rot == 0 ? tt.full_hi - lo : (tt.full_hi < tt.kt_hi ? w.nk - 1 - w.rot : w.nk);
+  }
   w.slot = a.kv_mode == kKvSlotR ? w.r : (a.kv_mode == kKvSlotJ ? j : 0);
   return w;
 }
@@ -573,14 +629,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const WorkItem w = decode_item(a);
-  const int nk = w.nk;
+  const int nk = w.nk;  // loop indices of computed key tiles
   // Loads for sending only (tiles the mask leaves unused) follow the
   // computed prefix (key_tile), at most two of them, so the MMA warps have
   // released every stage they reuse.
   // With grouped heads, the first query head of each group sends the shared block.
   const bool sends = a.forward && (w.bh % a.G) == 0;
-  const int np = sends ? nk + max(0, w.fwd_hi - max(w.fwd_lo, nk)) : nk;
-  const int nq = nk == 0 ? 0 : (w.tile[1].nk > 0 ? 2 : 1);  // Q tiles to load (tile A has keys if B has)
+  const int np = sends ? w.np_send : nk;
+  const int nq = nk == 0 ? 0 : (w.tile[1].je > w.tile[1].jb ? 2 : 1);  // Q tiles to load (tile A has keys if B has)
 
   // Softmax threads (warps 3..10, tile (warp-3)/4, one query row each) start
   // the loads of their incoming state now, so the latency overlaps the
@@ -701,20 +757,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = ((j / kStages) - 1) & 1;
         const int key0 = key_tile(a, w, j) * kTileN;
         // stage st last held tile j - 2; wait for each tile that used it
-        if (j >= kStages && j - kStages < w.tile[0].nk)
-          ok = mbar_wait(bar(L::kBarKEmpty + 2 * st), par, abort_flag, a, 1);
-        if (ok && j >= kStages && j - kStages < w.tile[1].nk)
-          ok = mbar_wait(bar(L::kBarKEmpty + 2 * st + 1), par, abort_flag, a, 1);
+        const int jp = j - kStages;  // the loop index that last used stage st
+        const bool used0 = jp >= w.tile[0].jb && jp < w.tile[0].je;
+        const bool used1 = jp >= w.tile[1].jb && jp < w.tile[1].je;
+        if (used0) ok = mbar_wait(bar(L::kBarKEmpty + 2 * st), par, abort_flag, a, 1);
+        if (ok && used1) ok = mbar_wait(bar(L::kBarKEmpty + 2 * st + 1), par, abort_flag, a, 1);
         if (!ok) break;
         mbar_expect_tx(bar(L::kBarKFull + st), L::kKBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), &k_map, bar(L::kBarKFull + st),
                       c * L::kSub, key0, w.kvh, w.slot);
         k_issued = j + 1;
-        if (j >= kStages && j - kStages < w.tile[0].nk)
-          ok = mbar_wait(bar(L::kBarVEmpty + 2 * st), par, abort_flag, a, 2);
-        if (ok && j >= kStages && j - kStages < w.tile[1].nk)
-          ok = mbar_wait(bar(L::kBarVEmpty + 2 * st + 1), par, abort_flag, a, 2);
+        if (used0) ok = mbar_wait(bar(L::kBarVEmpty + 2 * st), par, abort_flag, a, 2);
+        if (ok && used1) ok = mbar_wait(bar(L::kBarVEmpty + 2 * st + 1), par, abort_flag, a, 2);
         if (!ok) break;
         if (a.debug_drop_v) continue;  // test hook: nothing ever completes v_full
         mbar_expect_tx(bar(L::kBarVFull + st), L::kVBytes);
@@ -761,8 +816,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs this loop (every lane waits on the barriers);
     // one elected lane issues the MMAs and commits.
     const int t = warp - 1;
-    const int nkt = t == 0 ? w.tile[0].nk : w.tile[1].nk;
-    if (nkt > 0) {
+    const int jb = t == 0 ? w.tile[0].jb : w.tile[1].jb;  // this tile's loop indices [jb, je)
+    const int je = t == 0 ? w.tile[0].je : w.tile[1].je;
+    if (je > jb) {
       constexpr uint32_t idesc_qk = instr_desc(kTileM, kTileN, false);
       constexpr uint32_t idesc_pv = instr_desc(kTileM, D, true);
       const uint32_t q_s = sbase + L::kOffQ + t * L::kQBytes;
@@ -774,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int j) {
         const uint32_t v_s = sbase + L::kOffV + (j % kStages) * L::kVBytes;
         mma_pv(tmem + L::tmem_o(t), tmem + L::tmem_s(t), smem_desc(v_s, kTileN * 128, 1024), idesc_pv,
-               (j > 0 || a.accumulate) ? 1u : 0u);
+               (j > jb || a.accumulate) ? 1u : 0u);
       };
       // Waits on TMA data (Q, K, V) need no tcgen05 fence: the mbarrier's
       // transaction count completes only after the bytes are in shared
@@ -783,18 +839,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // after commits measured ~125 cycles of tensor-pipe bubble.  The data
       // waits come first, so the wait for P alone gates the PV + S issue.
       bool ok = warp_wait(bar(L::kBarQFull + t), 0, abort_flag, a, 3) &&
-                warp_wait(bar(L::kBarKFull), 0, abort_flag, a, 4);
+                warp_wait(bar(L::kBarKFull + jb % kStages), (jb / kStages) & 1, abort_flag, a, 4);
       if (ok) {
-        issue_s(0);
-        mma_commit_elect(bar(L::kBarKEmpty + t));
+        issue_s(jb);
+        mma_commit_elect(bar(L::kBarKEmpty + 2 * (jb % kStages) + t));
       }
-      for (int j = 0; j < nkt && ok; ++j) {
+      for (int j = jb; j < je && ok; ++j) {
         const int st = j % kStages;
-        const bool more = j + 1 < nkt;
+        const bool more = j + 1 < je;
         ok = warp_wait(bar(L::kBarVFull + st), (j / kStages) & 1, abort_flag, a, 6);
         if (ok && more)
           ok = warp_wait(bar(L::kBarKFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, abort_flag, a, 7);
-        ok = ok && warp_wait(bar(L::kBarPFull + t), j & 1, abort_flag, a, 5);
+        ok = ok && warp_wait(bar(L::kBarPFull + t), (j - jb) & 1, abort_flag, a, 5);
         if (!ok) break;
         tc_fence_after();
         issue_pv(j);
@@ -813,11 +869,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------- softmax and epilogue
     const int t = t_sm;  // 0: tile A (warps 3-6), 1: tile B (warps 7-10)
-    // first loop index whose key tile may need the mask: in the rotated
-    // order of a FULL block the ragged last tile comes at KT - 1 - rot (the
-    // tiles after it take the mask too, which leaves them unchanged)
-    const int mask_from = w.rot == 0 ? tw.full_kt : (tw.full_kt < w.nk ? w.nk - 1 - w.rot : w.nk);
-    const long long kmax_row = tile_kmax(tw, i_row);  // this row's last allowed key
+    // this row's allowed keys [kmin_row, kmax_row] (keys fit in int; the
+    // bounds are clamped to it)
+    const int kmax_row = (int)max(-1LL, min((long long)tw.klim - 1, tile_kmax(tw, i_row)));
+    const int kmin_row = (int)max(0LL, min((long long)a.n, tile_kmin(tw, i_row)));
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + L::tmem_s(t);
     const uint32_t o_addr = tmem + lane_off + L::tmem_o(t);
@@ -829,8 +884,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_store_wait();
     }
     bool ok = true;
-    for (int j = 0; j < tw.nk; ++j) {
-      ok = warp_wait(bar(L::kBarSFull + t), j & 1, abort_flag, a, 8);
+    for (int j = tw.jb; j < tw.je; ++j) {
+      ok = warp_wait(bar(L::kBarSFull + t), (j - tw.jb) & 1, abort_flag, a, 8);
       if (!ok) break;
       tc_fence_after();
       float s[kTileN];
@@ -840,12 +895,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < kTileN; ++e) s[e] = __uint_as_float(x[e]);
       }
-      if (j >= mask_from) {
-        const long long kbase = (long long)key_tile(a, w, j) * kTileN;
+      if (j < tw.mask_lo || j >= tw.mask_from) {
+        const int kbase = key_tile(a, w, j) * kTileN;
 #pragma unroll
         for (int e = 0; e < kTileN; ++e) {
-          const long long key = kbase + e;
-          if (key >= tw.klim || key > kmax_row) s[e] = -INFINITY;
+          const int key = kbase + e;
+          if (key > kmax_row || key < kmin_row) s[e] = -INFINITY;
         }
       }
       // row max: eight independent chains of 3-input max, then a tree
@@ -885,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       l = l * alpha + ((r0 + r1) + (r2 + r3));
       m2 = m_new;
       tmem_store64(s_addr, pb);  // P_t over the first 64 columns of S_t
-      if ((j > 0 || a.accumulate) && __any_sync(0xffffffffu, need)) {
+      if ((j > tw.jb || a.accumulate) && __any_sync(0xffffffffu, need)) {
         const uint64_t al2 = f2(alpha, alpha);
         uint32_t x[D];
         if constexpr (D == 128) tmem_load128(o_addr, x);
@@ -904,13 +959,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + t));
     }
-    if (ok && tw.nk > 0) {
+    if (ok && tw.je > tw.jb) {
       ok = warp_wait(bar(L::kBarOFull + t), 0, abort_flag, a, 9);
       tc_fence_after();
     }
     if (ok && in_range) {
       // ------------------------------------------------------ epilogue
-      const bool have_o = tw.nk > 0 || a.accumulate;
+      const bool have_o = tw.je > tw.jb || a.accumulate;
       if (a.finalize) {
         const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
         float* dst = a.out + g * D;

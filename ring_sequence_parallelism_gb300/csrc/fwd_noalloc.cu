@@ -180,6 +180,7 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
   a.G = p.H / p.Hkv;
   a.nq = (int)p.n;
   a.decode_pos0 = -1;
+  a.window = p.window;
   a.T = p.T;
   a.KT = p.KT;
   a.q_mode = p.layout == RING_LAYOUT_STRIPED ? kQStriped : (p.layout == RING_LAYOUT_ZIGZAG ? kQZigzag : kQContiguous);

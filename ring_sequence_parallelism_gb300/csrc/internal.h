@@ -31,11 +31,14 @@ struct BlockPlan {
   long long delta;  // diagonal offset of the block (n when it has none)
   long long klim[2];
   long long hdelta[2];
+  long long lodelta;  // sliding window: also k - i >= lodelta (kNoLowerOffset without one)
 };
+constexpr long long kNoLowerOffset = -(1LL << 50);
 
 struct Plan {
   int B = 0, H = 0, d = 0, P = 0, causal = 0, layout = 0;
   int Hkv = 0;  // K/V heads (H for plain multi-head attention)
+  long long window = 0;  // causal sliding window (0: none)
   long long N = 0, n = 0;
   int T = 0;   // query tiles per shard, ceil(n / kTileM)
   int KT = 0;  // key tiles per block,  ceil(n / kTileN)
@@ -50,7 +53,7 @@ struct Plan {
 };
 
 int block_of(int P, int r, int step);  // (r - step) mod P
-BlockPlan classify(int layout, int causal, long long n, int r, int j);
+BlockPlan classify(int layout, int causal, long long n, int r, int j, int P = 1, long long window = 0);
 // Half of the shard that local row i is in (1 only for the zigzag layout's late chunk).
 inline int row_half(int layout, long long n, long long i) {
   return (layout == RING_LAYOUT_ZIGZAG && i >= n / 2) ? 1 : 0;
@@ -60,7 +63,7 @@ long long block_pairs(int layout, long long n, const BlockPlan& b);
 // of them need no mask.
 void tile_range(int layout, long long n, int KT, const BlockPlan& b, int t, int* nk, int* full_kt);
 int build_plan(Plan* plan, int B, int H, long long N, int d, int P, int causal, int layout,
-               std::string* err);
+               std::string* err, long long window = 0);
 
 // ---------------------------------------------------------------- kernels
 // Query tensor addressing modes for the TMA map of Q.
@@ -98,6 +101,7 @@ struct StepArgs {
   int state_tiled;   // state in [BH][P][T][D/8][128][8] (O~) and [BH][P][T][128] (m, l) blocks
   int G;             // query heads per K/V head: query head bh reads K/V head bh / G
   int nq;            // query rows per shard (n for the ring; the short query length otherwise)
+  long long window;  // > 0: causal sliding window, a query sees itself and the window-1 tokens before it
   long long decode_pos0;  // >= 0: queries at global positions pos0 + i against block j's keys
                           //       (the causal rule from global positions; see ring_attn_decode)
   float scale_log2;  // log2(e) / sqrt(d)

@@ -19,9 +19,18 @@ int block_of(int P, int r, int step) {
   return j < 0 ? j + P : j;
 }
 
-BlockPlan classify(int layout, int causal, long long n, int r, int j) {
-  BlockPlan b{j, RING_BLOCK_FULL, n, {n, n}, {n, n}};
+static long long floor_div(long long x, long long q) { return x >= 0 ? x / q : -((-x + q - 1) / q); }
+
+BlockPlan classify(int layout, int causal, long long n, int r, int j, int P, long long window) {
+  BlockPlan b{j, RING_BLOCK_FULL, n, {n, n}, {n, n}, kNoLowerOffset};
   if (!causal) return b;
+  if (window > 0 && layout != RING_LAYOUT_ZIGZAG) {
+    // a key W or more positions behind the query is dropped: contiguous
+    // (r-j) n + i - k < W  <=>  k - i >= (r-j) n - W + 1; striped
+    // (i-k) P + (r-j) < W  <=>  k - i >= floor((r-j-W)/P) + 1
+    b.lodelta = layout == RING_LAYOUT_STRIPED ? floor_div((long long)(r - j) - window, P) + 1
+                                              : (long long)(r - j) * n - window + 1;
+  }
   if (layout == RING_LAYOUT_ZIGZAG) {
     // Shard r holds chunks r and 2P-1-r (c = n/2 tokens each), rows in that
     // order; block j likewise.  Comparing chunk ids (all of r, j < P <= the
@@ -65,11 +74,13 @@ BlockPlan classify(int layout, int causal, long long n, int r, int j) {
 }
 
 long long block_pairs(int layout, long long n, const BlockPlan& b) {
-  // rows i = 0..n-1 allow columns 0..min(klim, i + hdelta + 1) - 1
+  // row i allows columns max(0, i + lodelta) .. min(klim, i + hdelta + 1) - 1
   long long total = 0;
   for (long long i = 0; i < n; ++i) {
     const int h = row_half(layout, n, i);
-    total += std::min(b.klim[h], std::max(0LL, i + b.hdelta[h] + 1));
+    const long long hi = std::min(b.klim[h], std::max(0LL, i + b.hdelta[h] + 1));
+    const long long lo = std::max(0LL, i + b.lodelta);
+    total += std::max(0LL, hi - lo);
   }
   return total;
 }
@@ -85,12 +96,14 @@ void tile_range(int layout, long long n, int KT, const BlockPlan& b, int t, int*
   int cnt = last_key < 0 ? 0 : (int)std::min<long long>(KT, last_key / kTileN + 1);
   // key tiles allowed for every row of the tile: below klim and i_min + hd
   const long long common = std::min(klim, i_min + hd + 1);
-  *nk = cnt;
+  // a sliding window starts the tile's keys at i_min + lodelta
+  const int first = (int)std::min<long long>(cnt, std::max(0LL, i_min + b.lodelta) / kTileN);
+  *nk = cnt - first;  // key tiles visited
   *full_kt = common <= 0 ? 0 : (int)std::min<long long>(cnt, common / kTileN);
 }
 
 int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int layout,
-               std::string* err) {
+               std::string* err, long long window) {
   char buf[256];
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0 || P <= 0) {
     std::snprintf(buf, sizeof buf, "sizes must be positive (B=%d H=%d N=%lld d=%d P=%d)", B, H, N, d, P);
@@ -127,6 +140,10 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   }
   const long long n = N / P;
   const long long bh = (long long)B * H;
+  if (window < 0 || (window > 0 && (!causal || layout == RING_LAYOUT_ZIGZAG))) {
+    *err = "a sliding window needs the causal mask and the contiguous or striped layout";
+    return window < 0 ? RING_ERR_INVALID_ARG : RING_ERR_UNSUPPORTED;
+  }
   if (layout == RING_LAYOUT_ZIGZAG && (n % (2 * kTileM)) != 0) {
     std::snprintf(buf, sizeof buf,
                   "zigzag needs chunks N/2P that are multiples of %d tokens (N=%lld, P=%d)", kTileM, N, P);
@@ -145,6 +162,7 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   p->causal = causal;
   p->layout = layout;
   p->Hkv = H;
+  p->window = window;
   p->n = n;
   p->T = (int)((n + kTileM - 1) / kTileM);
   p->KT = (int)((n + kTileN - 1) / kTileN);
@@ -158,7 +176,7 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   // small cache suffices.
   std::vector<std::pair<std::vector<long long>, std::pair<long long, long long>>> cache;
   auto work = [&](const BlockPlan& b) {
-    const std::vector<long long> key{b.klim[0], b.klim[1], b.hdelta[0], b.hdelta[1]};
+    const std::vector<long long> key{b.klim[0], b.klim[1], b.hdelta[0], b.hdelta[1], b.lodelta};
     for (auto& e : cache)
       if (e.first == key) return e.second;
     long long tiles = 0;
@@ -173,7 +191,7 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   };
   for (int s = 0; s < P; ++s) {
     for (int r = 0; r < P; ++r) {
-      BlockPlan b = classify(layout, causal, n, r, block_of(P, r, s));
+      BlockPlan b = classify(layout, causal, n, r, block_of(P, r, s), P, window);
       p->blocks[(size_t)s * P + r] = b;
       auto w = work(b);
       p->shard_pairs[r] += w.first * bh;

@@ -32,6 +32,7 @@ class Workload:
     key_boost_frac: float = 0.0  # fraction of key rows scaled by key_boost
     key_boost: float = 8.0
     Hkv: int = 0  # K/V heads for grouped-query attention (0: H)
+    window: int = 0  # causal sliding window (0: none)
 
     @property
     def kv_heads(self) -> int:
@@ -46,6 +47,9 @@ class Workload:
         return {"contiguous": 0, "striped": 1, "zigzag": 2}[self.layout]
 
     def allowed_pairs_per_head(self) -> int:
+        if self.causal and self.window > 0:
+            W, N = min(self.window, self.N), self.N
+            return W * (W + 1) // 2 + (N - W) * W  # row t sees min(t + 1, W) keys
         return self.N * (self.N + 1) // 2 if self.causal else self.N * self.N
 
     def flops(self) -> int:
@@ -64,6 +68,8 @@ WORKLOADS = {
         Workload("striped-1m", 1, 8, 1048576, 128, 64, True, "striped", 1004),
         # the 128K workload in the zigzag layout (2P chunks of 4096 tokens)
         Workload("zigzag-128k", 1, 16, 131072, 128, 16, True, "zigzag", 1003, key_boost_frac=0.01),
+        # causal sliding window of 4096 tokens over the 128K striped sequence
+        Workload("swa-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01, window=4096),
         # grouped-query attention: 16 query heads sharing 4 K/V heads
         Workload("gqa-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01, Hkv=4),
         # profiling size: the 128K striped workload with 4 heads (inputs 3 x 134 MB)

@@ -30,7 +30,7 @@ def built():
     ra._lib.load()
 
 
-def decode_reference(q, k, v, causal):
+def decode_reference(q, k, v, causal, window=0):
     """Dense rows N-Lq .. N-1 of the oracle for queries q [B, H, Lq, d]."""
     B, H, Lq, d = q.shape
     N = k.shape[2]
@@ -40,17 +40,19 @@ def decode_reference(q, k, v, causal):
     k, v = expand_kv(k, H), expand_kv(v, H)
     rows = np.arange(N - Lq, N)
     return oracle.default().dense(q_full.reshape(BH, N, d), k.reshape(BH, N, d), v.reshape(BH, N, d), causal,
-                                  rows=rows)
+                                  rows=rows, window=window)
 
 
-def check(B, H, Hkv, N, d, P, causal, layout, Lq, seed):
+def check(B, H, Hkv, N, d, P, causal, layout, Lq, seed, window=0):
     q_all, k, v = make_qkv(B, H, N, d, seed=seed, Hkv=Hkv)
     q = q_all[:, :, :Lq].contiguous()  # any Lq rows serve as the new queries
     att = ra.RingAttention(B, H, N, d, P, causal=causal, layout=layout, kv_heads=Hkv)
+    if window:
+        att.set_option(ra.RING_OPT_WINDOW, window)
     out, lse = att.decode(q.cuda(), k.cuda(), v.cuda())
     att.check()
     torch.cuda.synchronize()
-    ref_out, ref_lse = decode_reference(q, k, v, causal)
+    ref_out, ref_lse = decode_reference(q, k, v, causal, window)
     BH = B * H
     d_out = float(np.max(np.abs(out.cpu().double().numpy().reshape(BH, Lq, d) - ref_out)))
     d_lse = float(np.max(np.abs(lse.cpu().double().numpy().reshape(BH, Lq) - ref_lse)))
@@ -80,6 +82,14 @@ CASES = [
 def test_decode_matches_oracle(case):
     B, H, Hkv, N, d, P, causal, layout, Lq = case
     check(B, H, Hkv, N, d, P, causal, layout, Lq, seed=N + Lq + H)
+
+
+@pytest.mark.parametrize("layout,window,Lq", [("contiguous", 100, 1), ("striped", 300, 64), ("striped", 129, 200),
+                                              ("contiguous", 1000, 300)])
+def test_decode_sliding_window(layout, window, Lq):
+    """Decode with a causal sliding window: each new query sees the last
+    `window` positions up to its own."""
+    check(1, 2, 2, 4 * 256, 128, 4, True, layout, Lq, seed=Lq + window, window=window)
 
 
 @pytest.mark.parametrize("Lq", [1, 128])

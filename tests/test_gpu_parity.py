@@ -44,8 +44,10 @@ def report(name, out, lse, ref_out, ref_lse):
     return d_out, d_lse
 
 
-def run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=None):
+def run_fwd(B, H, N, d, P, causal, layout, q, k, v, rotation=None, window=0):
     att = ra.RingAttention(B, H, N, d, P, causal=causal, layout=layout, kv_heads=k.shape[1])
+    if window:
+        att.set_option(ra.RING_OPT_WINDOW, window)
     if rotation is not None:
         att.set_option(ra.RING_OPT_ROTATION, rotation)
     out, lse = att.fwd(q.cuda(), k.cuda(), v.cuda())
@@ -305,7 +307,7 @@ def test_fwd_8k_contiguous_and_striped():
 
 def _sampled_check(w, rows_per_head, ring_rows=0):
     q, k, v = make_workload(w)
-    out, lse = run_fwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v)
+    out, lse = run_fwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v, window=w.window)
     k, v = expand_kv(k, w.H), expand_kv(v, w.H)  # the oracle sees each query head's K/V
     BH = w.B * w.H
     n = w.n
@@ -314,14 +316,14 @@ def _sampled_check(w, rows_per_head, ring_rows=0):
     rows = sample_rows(w.N, rows_per_head, extra=extra).numpy()
     orc = oracle.default()
     qf, kf, vf = flat(q, BH), flat(k, BH), flat(v, BH)
-    ref_out, ref_lse = orc.dense(qf, kf, vf, w.causal, rows=rows)
+    ref_out, ref_lse = orc.dense(qf, kf, vf, w.causal, rows=rows, window=w.window)
     got_out = out.reshape(BH, w.N, w.d)[:, rows].double().numpy()
     got_lse = lse.reshape(BH, w.N)[:, rows].double().numpy()
     d_out, d_lse = report(f"{w.name} ({rows.size} rows/head)", got_out, got_lse, ref_out, ref_lse)
     assert d_out <= TOL_OUT and d_lse <= TOL_LSE
     if ring_rows:
         rr = rows[:ring_rows]
-        r_out, r_lse = orc.ring(qf, kf, vf, w.P, w.causal, w.layout_id, rows=rr)
+        r_out, r_lse = orc.ring(qf, kf, vf, w.P, w.causal, w.layout_id, rows=rr, window=w.window)
         assert np.max(np.abs(r_out - ref_out[:, :ring_rows])) <= 1e-10
         assert np.max(np.abs(r_lse - ref_lse[:, :ring_rows])) <= 1e-10
     # properties that hold at any size: finite everywhere, lse above the
@@ -337,6 +339,84 @@ def test_fwd_128k_striped_sampled():
 
 def test_fwd_128k_zigzag_sampled():
     _sampled_check(WORKLOADS["zigzag-128k"], 256, ring_rows=16)
+
+
+def test_fwd_128k_window_sampled():
+    _sampled_check(WORKLOADS["swa-128k"], 256, ring_rows=16)
+
+
+WINDOW_CASES = [
+    # (B, H, N, d, P, layout, window)
+    (1, 2, 4 * 256, 64, 4, "contiguous", 1),
+    (1, 2, 4 * 256, 128, 4, "striped", 100),
+    (2, 2, 3 * 200, 128, 3, "contiguous", 129),  # ragged shards
+    (1, 2, 3 * 200, 64, 3, "striped", 300),
+    (1, 2, 8 * 256, 128, 8, "striped", 700),
+    (1, 2, 8 * 256, 128, 8, "contiguous", 700),
+    (1, 2, 4 * 256, 128, 4, "contiguous", 4 * 256),  # a window of N: plain causal
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=lambda c: "B{}H{}N{}d{}P{}{}W{}".format(*c[:5], c[5][0], c[6]))
+def test_fwd_sliding_window(case):
+    """Causal sliding window (RING_OPT_WINDOW): every row against the
+    oracle's windowed dense attention, and the three rotation modes bit for
+    bit (with a window the sent tiles can sit inside or below a tile pair's
+    key range; they are loaded again at the end)."""
+    B, H, N, d, P, layout, W = case
+    q, k, v = make_qkv(B, H, N, d, seed=N + W)
+    out, lse = run_fwd(B, H, N, d, P, True, layout, q, k, v, rotation=2, window=W)
+    BH = B * H
+    ref_out, ref_lse = oracle.default().dense(flat(q, BH), flat(k, BH), flat(v, BH), True, window=W)
+    d_out, d_lse = report(f"window {case}", out.double().numpy().reshape(BH, N, d),
+                          lse.double().numpy().reshape(BH, N), ref_out, ref_lse)
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE
+    for mode in (0, 1):
+        got = run_fwd(B, H, N, d, P, True, layout, q, k, v, rotation=mode, window=W)
+        assert torch.equal(got[0], out) and torch.equal(got[1], lse), mode
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_block_partial_window(layout):
+    """Block partials with a window against the oracle's windowed block
+    partials, every block of a small ring."""
+    B, H, n, d, P, W = 1, 2, 328, 128, 3, 200
+    N = n * P
+    q, k, v = make_qkv(B, H, N, d, seed=123)
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout=layout)
+    att.set_option(ra.RING_OPT_WINDOW, W)
+    orc = oracle.default()
+    L = lid(layout)
+    BH = B * H
+    qf, kf, vf = flat(q, BH), flat(k, BH), flat(v, BH)
+    worst_o = worst_l = 0.0
+    for r in range(P):
+        pos_r = [orc.position(L, n, P, r, i) for i in range(n)]
+        q_sh = qf[:, pos_r].contiguous()
+        for s in range(P):
+            j = orc.block_at(P, r, s)
+            pos_j = [orc.position(L, n, P, j, i) for i in range(n)]
+            k_bl, v_bl = kf[:, pos_j].contiguous(), vf[:, pos_j].contiguous()
+            st = att.new_state()
+            for x in st:
+                x.fill_(float("nan"))
+            att.block_partial(r, s, q_sh.reshape(B, H, n, d).cuda(), k_bl.reshape(B, H, n, d).cuda(),
+                              v_bl.reshape(B, H, n, d).cuda(), st, 0)
+            att.check()
+            m, l, o = (x.cpu().double().numpy().reshape(BH * n, -1) for x in st)
+            m, l = m[:, 0], l[:, 0]
+            rm, rl, ro = orc.block_partial(q_sh, k_bl, v_bl, P, True, L, r, j, window=W)
+            rm, rl, ro = rm.reshape(-1), rl.reshape(-1), ro.reshape(BH * n, d)
+            empty = np.isneginf(rm)
+            assert np.all(np.isneginf(m[empty])) and np.all(l[empty] == 0) and np.all(o[empty] == 0), (r, s)
+            ne = ~empty
+            if ne.any():
+                dl = np.abs((m[ne] + np.log(l[ne])) - (rm[ne] + np.log(rl[ne])))
+                do = np.abs(o[ne] / l[ne][:, None] - ro[ne] / rl[ne][:, None])
+                worst_l, worst_o = max(worst_l, float(dl.max())), max(worst_o, float(do.max()))
+    print(f"block partial window {layout}: max|dout|={worst_o:.3e} max|dlse|={worst_l:.3e}")
+    assert worst_o <= TOL_OUT and worst_l <= TOL_LSE
+    att.close()
 
 
 def test_fwd_128k_gqa_sampled():
