@@ -478,6 +478,7 @@ __device__ __forceinline__ int key_tile(const StepArgs& a, const WorkItem& w, in
 // The mask rule of the block for the rows in half h of the shard (see the
 // planner): kmax(i) = floor((i + b) / q) and, with a sliding window W,
 // kmin(i) = floor((i + bl) / q) + 1; key limit klim.
+template <bool kWin>
 __device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int h, Tile* w) {
   const long long n = a.n;
   w->klim = a.n;
@@ -485,7 +486,7 @@ __device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int 
   w->bl = kNoLowerBound;
   w->q = 1;
   if (!a.causal) return;
-  const long long W = a.window;
+  const long long W = kWin ? a.window : 0;
   if (a.decode_pos0 >= 0) {
     // Short queries at global positions pos0 + i against the keys of block
     // j: key k is at j n + k (contiguous) or k P + j (striped), so k is
@@ -521,6 +522,7 @@ __device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int 
   if (W > 0) w->bl = striped ? floor_div((long long)(r - j) - W, a.P) : (long long)(r - j) * n - W;
 }
 
+template <bool kWin>
 __device__ __forceinline__ Tile tile_work(const StepArgs& a, int r, int j, int t) {
   Tile w{};
   w.t = t;
@@ -530,16 +532,16 @@ __device__ __forceinline__ Tile tile_work(const StepArgs& a, int r, int j, int t
   const long long i_min = (long long)t * kTileM;
   const long long i_max = min((long long)a.nq - 1, i_min + kTileM - 1);
   const int h = (a.layout == RING_LAYOUT_ZIGZAG && i_min >= n / 2) ? 1 : 0;
-  block_rule(a, r, j, h, &w);
+  block_rule<kWin>(a, r, j, h, &w);
   // kmin and kmax are non-decreasing in i: the last row bounds the tiles
   // from above, the first row from below, and the tiles every row may use
   // in full lie between the first row's kmax and the last row's kmin.
   const long long last_key = min((long long)w.klim - 1, tile_kmax(w, i_max));
-  const long long first_key = max(0LL, tile_kmin(w, i_min));
+  const long long first_key = kWin ? max(0LL, tile_kmin(w, i_min)) : 0;
   w.kt_hi = last_key < 0 ? 0 : (int)min((long long)a.KT, last_key / kTileN + 1);
   w.kt_lo = (int)min((long long)w.kt_hi, first_key / kTileN);
   const long long common_hi = min((long long)w.klim, tile_kmax(w, i_min) + 1);  // keys < this for every row
-  const long long common_lo = max(0LL, tile_kmin(w, i_max));                       // keys >= this for every row
+  const long long common_lo = kWin ? max(0LL, tile_kmin(w, i_max)) : 0;                       // keys >= this for every row
   w.full_hi = common_hi <= 0 ? 0 : (int)min((long long)w.kt_hi, common_hi / kTileN);
   w.full_lo = (int)min((long long)w.kt_hi, (common_lo + kTileN - 1) / kTileN);
   return w;
@@ -548,6 +550,7 @@ __device__ __forceinline__ Tile tile_work(const StepArgs& a, int r, int j, int t
 // blockIdx.x -> (shard, head, tile pair).  CTAs of one (shard, head) group
 // are consecutive so the K/V block they share stays in L2; within a group
 // the heaviest pairs (largest u under the causal mask) start first.
+template <bool kWin>
 __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   WorkItem w;
   const int U = (a.T + 1) / 2;
@@ -561,8 +564,8 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   int j = (w.r - a.step) % a.P;
   if (j < 0) j += a.P;
   w.j = j;
-  w.tile[0] = tile_work(a, w.r, j, 2 * u);
-  w.tile[1] = tile_work(a, w.r, j, 2 * u + 1);
+  w.tile[0] = tile_work<kWin>(a, w.r, j, 2 * u);
+  w.tile[1] = tile_work<kWin>(a, w.r, j, 2 * u + 1);
   // The CTA loads the union of the two tiles' key-tile ranges (the second
   // tile's range starts and ends no earlier than the first's).
   int lo = a.KT, hi = 0;
@@ -582,7 +585,7 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   // but not at its end; then both tiles of a ring block visit the whole
   // prefix (blocks without a diagonal or window), so one order serves both.
   // Short queries (decode) send nothing and keep the natural order.
-  w.rot = (a.decode_pos0 < 0 && a.window == 0 && lo == 0 && w.fwd_hi < hi) ? w.fwd_hi : 0;
+  w.rot = (a.decode_pos0 < 0 && !(kWin && a.window > 0) && lo == 0 && w.fwd_hi < hi) ? w.fwd_hi : 0;
   // Tiles sent along the ring come last: either they end the computed range
   // (after the rotation), possibly followed by the ones beyond it, or they
   // are loaded again after it (a window can leave them inside or below it).
@@ -612,7 +615,9 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
 }
 
 // ------------------------------------------------------------- the kernel
-template <int D>
+// kWin: the sliding-window lower bound is in force (instantiated apart so the
+// unwindowed kernel carries none of its bookkeeping).
+template <int D, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
     block_partial_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ CUtensorMap q_map,
                          const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
@@ -628,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const WorkItem w = decode_item(a);
+  const WorkItem w = decode_item<kWin>(a);
   const int nk = w.nk;  // loop indices of computed key tiles
   // Loads for sending only (tiles the mask leaves unused) follow the
   // computed prefix (key_tile), at most two of them, so the MMA warps have
@@ -872,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this row's allowed keys [kmin_row, kmax_row] (keys fit in int; the
     // bounds are clamped to it)
     const int kmax_row = (int)max(-1LL, min((long long)tw.klim - 1, tile_kmax(tw, i_row)));
-    const int kmin_row = (int)max(0LL, min((long long)a.n, tile_kmin(tw, i_row)));
+    const int kmin_row = kWin ? (int)max(0LL, min((long long)a.n, tile_kmin(tw, i_row))) : 0;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + L::tmem_s(t);
     const uint32_t o_addr = tmem + lane_off + L::tmem_o(t);
@@ -900,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < kTileN; ++e) {
           const int key = kbase + e;
-          if (key > kmax_row || key < kmin_row) s[e] = -INFINITY;
+          if (key > kmax_row || (kWin && key < kmin_row)) s[e] = -INFINITY;
         }
       }
       // row max: eight independent chains of 3-input max, then a tree
@@ -1019,8 +1024,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 int prepare_one() {
-  return (int)cudaFuncSetAttribute(block_partial_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  int e = (int)cudaFuncSetAttribute(block_partial_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Layout<D>::kAlloc);
+  if (e) return e;
+  return (int)cudaFuncSetAttribute(block_partial_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   Layout<D>::kAlloc);
 }
 
 }  // namespace
@@ -1046,10 +1054,13 @@ int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map
   // without `forward` the kernel never touches the send maps
   const CUtensorMap& kn = *static_cast<const CUtensorMap*>(k_next_map ? k_next_map : k_map);
   const CUtensorMap& vn = *static_cast<const CUtensorMap*>(v_next_map ? v_next_map : v_map);
+  const bool win = a.causal && a.window > 0;
   if (d == 64) {
-    block_partial_kernel<64><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
+    if (win) block_partial_kernel<64, true><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
+    else block_partial_kernel<64, false><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
   } else {
-    block_partial_kernel<128><<<grid, kThreads, Layout<128>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
+    if (win) block_partial_kernel<128, true><<<grid, kThreads, Layout<128>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
+    else block_partial_kernel<128, false><<<grid, kThreads, Layout<128>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
   }
   return (int)cudaGetLastError();
 }
