@@ -14,6 +14,9 @@ Functions mirror the C entry points; every array is numpy:
   merge_inplace(a, b) (float64)
   finalize(m, l, o)
   naive_block_sum(q, k, v, P, causal, layout)
+  dense_bwd(q, k, v, dout, causal)          -> dq, dk, dv [BH,N,d]
+  dense_bwd_rows(q, k, v, dout, causal, qrows, krows)
+  ring_bwd(q, k, v, dout, out, lse, P, causal, layout, visits=False)
 q, k, v are bf16 bit patterns (uint16) shaped [BH, N, d] in natural order,
 or torch bf16 tensors (converted with ``bf16_bits``).
 """
@@ -100,6 +103,12 @@ class Oracle:
         L.oracle_finalize.restype = _I
         L.oracle_naive_block_sum.argtypes = [_I, _L, _I, _I, _I, _L, _I, _P, _P, _P, _P]
         L.oracle_naive_block_sum.restype = _I
+        L.oracle_dense_bwd.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _I]
+        L.oracle_dense_bwd.restype = _I
+        L.oracle_dense_bwd_rows.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _L, _P, _L, _P, _P, _P, _P, _I]
+        L.oracle_dense_bwd_rows.restype = _I
+        L.oracle_ring_bwd.argtypes = [_I, _L, _I, _I, _I, _L, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I]
+        L.oracle_ring_bwd.restype = _I
 
     # -- small helpers -------------------------------------------------
     def threads(self) -> int:
@@ -219,6 +228,55 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"oracle_naive_block_sum failed: {rc}")
         return out
+
+    # -- the backward ------------------------------------------------------
+    def dense_bwd(self, q, k, v, dout, causal: bool, window: int = 0):
+        """dq, dk, dv (float64, [BH][N][d]) by the plain definition."""
+        q, k, v = self._qkv(q, k, v)
+        do = bf16_bits(dout)
+        assert do.shape == q.shape
+        BH, N, d = q.shape
+        dq, dk, dv = (np.empty((BH, N, d), np.float64) for _ in range(3))
+        rc = self.lib.oracle_dense_bwd(BH, N, d, int(causal), int(window), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), self.nthreads)
+        if rc != 0:
+            raise RuntimeError(f"oracle_dense_bwd failed: {rc}")
+        return dq, dk, dv
+
+    def dense_bwd_rows(self, q, k, v, dout, causal: bool, qrows, krows, window: int = 0):
+        """dq at query positions qrows ([BH][len(qrows)][d]) and dk, dv at key
+        positions krows ([BH][len(krows)][d])."""
+        q, k, v = self._qkv(q, k, v)
+        do = bf16_bits(dout)
+        BH, N, d = q.shape
+        qr, nq = self._rows(qrows, N)
+        kr, nk = self._rows(krows, N)
+        dq = np.empty((BH, nq, d), np.float64)
+        dk = np.empty((BH, nk, d), np.float64)
+        dv = np.empty((BH, nk, d), np.float64)
+        rc = self.lib.oracle_dense_bwd_rows(BH, N, d, int(causal), int(window), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
+                                            nq, _ptr(qr), nk, _ptr(kr), _ptr(dq), _ptr(dk), _ptr(dv), self.nthreads)
+        if rc != 0:
+            raise RuntimeError(f"oracle_dense_bwd_rows failed: {rc}")
+        return dq, dk, dv
+
+    def ring_bwd(self, q, k, v, dout, out, lse, P: int, causal: bool, layout: int, visits: bool = False,
+                 window: int = 0):
+        """The ring backward simulation from the forward's out and lse
+        (float64, natural order).  Returns dq, dk, dv (and the visit counts)."""
+        q, k, v = self._qkv(q, k, v)
+        do = bf16_bits(dout)
+        BH, N, d = q.shape
+        out = np.ascontiguousarray(out, np.float64).reshape(BH, N, d)
+        lse = np.ascontiguousarray(lse, np.float64).reshape(BH, N)
+        dq, dk, dv = (np.empty((BH, N, d), np.float64) for _ in range(3))
+        cnt = np.zeros((BH, N, N), np.int64) if visits else None
+        rc = self.lib.oracle_ring_bwd(BH, N, d, P, int(causal), int(window), layout, _ptr(q), _ptr(k), _ptr(v),
+                                      _ptr(do), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cnt),
+                                      self.nthreads)
+        if rc != 0:
+            raise RuntimeError(f"oracle_ring_bwd failed: {rc}")
+        return (dq, dk, dv, cnt) if visits else (dq, dk, dv)
 
 
 _DEFAULT: Oracle | None = None

@@ -486,3 +486,314 @@ int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, long window
   free(s); free(kpos); free(kblk); free(vblk); free(ob);
   return 0;
 }
+
+/* ------------------------------------------------------------------ backward
+ *
+ * The gradients of attention for an upstream gradient dO ([RA-CN] "Backward
+ * 需要让梯度也沿环传播": every Q-K/V block interaction contributes a gradient;
+ * the softmax statistics are restored from the saved per-row logsumexp and
+ * the probabilities recomputed block by block, as in FlashAttention's
+ * backward).  With P_tk = exp(s_tk - lse_t) over the allowed keys of query t:
+ *   dV_k = sum_t P_tk dO_t
+ *   dP_tk = dO_t . v_k
+ *   D_t  = sum_k P_tk dP_tk = dO_t . O_t
+ *   dS_tk = P_tk (dP_tk - D_t)
+ *   dQ_t = scale sum_k dS_tk k_k
+ *   dK_k = scale sum_t dS_tk q_t
+ * (the chain rule through O = softmax(scale Q K^T) V; the derivative of a
+ * softmax row p is diag(p) - p p^T, which gives the D_t term).
+ */
+
+/*
+ * Dense backward by the definition above, from scratch (the forward's O and
+ * lse are recomputed here in float64).  q, k, v, dout are bf16 bit patterns
+ * [BH][N][d] in natural order; dq, dk, dv are [BH][N][d] doubles.
+ * Two passes so that every output row has a single writer:
+ *   pass 1, per query t: lse_t, O_t, D_t and dQ_t;
+ *   pass 2, per key k:   dK_k and dV_k over the queries that see k.
+ */
+int oracle_dense_bwd(int BH, long N, int d, int causal, long window, const uint16_t* q,
+                     const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                     double* dq, double* dk, double* dv, int nthreads) {
+  if (BH <= 0 || N <= 0 || d <= 0) return -1;
+  set_threads(nthreads);
+  const double scale = 1.0 / sqrt((double)d);
+  double* lse = (double*)malloc(sizeof(double) * (size_t)BH * N);
+  double* D = (double*)malloc(sizeof(double) * (size_t)BH * N);
+  if (!lse || !D) {
+    free(lse);
+    free(D);
+    return -2;
+  }
+  int failed = 0;
+  const long total = (long)BH * N;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    double* o = (double*)malloc(sizeof(double) * (size_t)d);
+    const int ok = s && o;
+    if (!ok) {
+#pragma omp atomic write
+      failed = 1;
+    }
+    /* pass 1: per query row */
+#pragma omp for schedule(dynamic, 4)
+    for (long idx = 0; idx < total; ++idx) {
+      if (!ok) continue;
+      const long bh = idx / N, t = idx % N;
+      const uint16_t* qrow = q + (size_t)idx * d;
+      const uint16_t* dorow = dout + (size_t)idx * d;
+      const uint16_t* kb = k + (size_t)bh * N * d;
+      const uint16_t* vb = v + (size_t)bh * N * d;
+      double m = -INFINITY;
+      for (long kk = 0; kk < N; ++kk) {
+        if (!allowed(causal, window, t, kk)) continue;
+        s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
+        if (s[kk] > m) m = s[kk];
+      }
+      double sum = 0.0;
+      for (long kk = 0; kk < N; ++kk)
+        if (allowed(causal, window, t, kk)) sum += exp(s[kk] - m);
+      const double l = m + log(sum);
+      lse[idx] = l;
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      for (long kk = 0; kk < N; ++kk) {
+        if (!allowed(causal, window, t, kk)) continue;
+        const double p = exp(s[kk] - l);
+        for (int c = 0; c < d; ++c) o[c] += p * widen_bf16(vb[(size_t)kk * d + c]);
+      }
+      double Dt = 0.0;
+      for (int c = 0; c < d; ++c) Dt += widen_bf16(dorow[c]) * o[c];
+      D[idx] = Dt;
+      double* g = dq + (size_t)idx * d;
+      for (int c = 0; c < d; ++c) g[c] = 0.0;
+      for (long kk = 0; kk < N; ++kk) {
+        if (!allowed(causal, window, t, kk)) continue;
+        const double p = exp(s[kk] - l);
+        const double ds = p * (dot_q_k(dorow, vb + (size_t)kk * d, d) - Dt);
+        for (int c = 0; c < d; ++c) g[c] += scale * ds * widen_bf16(kb[(size_t)kk * d + c]);
+      }
+    }
+    /* pass 2: per key row (the implicit barrier above makes lse and D ready) */
+#pragma omp for schedule(dynamic, 4)
+    for (long idx = 0; idx < total; ++idx) {
+      if (!ok) continue;
+      const long bh = idx / N, kk = idx % N;
+      const uint16_t* krow = k + (size_t)idx * d;
+      const uint16_t* vrow = v + (size_t)idx * d;
+      double* gk = dk + (size_t)idx * d;
+      double* gv = dv + (size_t)idx * d;
+      for (int c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
+      for (long t = 0; t < N; ++t) {
+        if (!allowed(causal, window, t, kk)) continue;
+        const size_t row = (size_t)bh * N + t;
+        const uint16_t* qrow = q + row * d;
+        const uint16_t* dorow = dout + row * d;
+        const double p = exp(scale * dot_q_k(qrow, krow, d) - lse[row]);
+        const double ds = p * (dot_q_k(dorow, vrow, d) - D[row]);
+        for (int c = 0; c < d; ++c) {
+          gk[c] += scale * ds * widen_bf16(qrow[c]);
+          gv[c] += p * widen_bf16(dorow[c]);
+        }
+      }
+    }
+    free(s);
+    free(o);
+  }
+  free(lse);
+  free(D);
+  return failed ? -2 : 0;
+}
+
+/* lse_t and D_t = dO_t . O_t of one query row, by definition. */
+static void row_lse_and_D(const uint16_t* qrow, const uint16_t* dorow, long t, const uint16_t* kb,
+                          const uint16_t* vb, long N, int d, int causal, long window, double scale,
+                          double* s, double* o, double* lse_out, double* D_out) {
+  double m = -INFINITY;
+  for (long kk = 0; kk < N; ++kk) {
+    if (!allowed(causal, window, t, kk)) continue;
+    s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
+    if (s[kk] > m) m = s[kk];
+  }
+  double sum = 0.0;
+  for (long kk = 0; kk < N; ++kk)
+    if (allowed(causal, window, t, kk)) sum += exp(s[kk] - m);
+  const double l = m + log(sum);
+  for (int c = 0; c < d; ++c) o[c] = 0.0;
+  for (long kk = 0; kk < N; ++kk) {
+    if (!allowed(causal, window, t, kk)) continue;
+    const double p = exp(s[kk] - l);
+    for (int c = 0; c < d; ++c) o[c] += p * widen_bf16(vb[(size_t)kk * d + c]);
+  }
+  double Dt = 0.0;
+  for (int c = 0; c < d; ++c) Dt += widen_bf16(dorow[c]) * o[c];
+  *lse_out = l;
+  *D_out = Dt;
+}
+
+/*
+ * The dense backward for sampled rows only: dQ at the query positions qrows
+ * (dq is [BH][nq][d]) and dK, dV at the key positions krows (dk, dv are
+ * [BH][nk][d]).  Same definition as oracle_dense_bwd; the statistics of each
+ * query that a sampled key meets are recomputed on demand, so a key late in
+ * a causal sequence (or any key under a sliding window) is cheap.
+ */
+int oracle_dense_bwd_rows(int BH, long N, int d, int causal, long window, const uint16_t* q,
+                          const uint16_t* k, const uint16_t* v, const uint16_t* dout, long nq,
+                          const long* qrows, long nk, const long* krows, double* dq, double* dk,
+                          double* dv, int nthreads) {
+  if (BH <= 0 || N <= 0 || d <= 0 || nq < 0 || nk < 0) return -1;
+  set_threads(nthreads);
+  const double scale = 1.0 / sqrt((double)d);
+  int failed = 0;
+  const long total = (long)BH * (nq + nk);
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    double* o = (double*)malloc(sizeof(double) * (size_t)d);
+    const int ok = s && o;
+    if (!ok) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (long idx = 0; idx < total; ++idx) {
+      if (!ok) continue;
+      const long bh = idx / (nq + nk), x = idx % (nq + nk);
+      const uint16_t* qb = q + (size_t)bh * N * d;
+      const uint16_t* kb = k + (size_t)bh * N * d;
+      const uint16_t* vb = v + (size_t)bh * N * d;
+      const uint16_t* ob = dout + (size_t)bh * N * d;
+      if (x < nq) {
+        const long t = qrows[x];
+        double l, Dt;
+        row_lse_and_D(qb + (size_t)t * d, ob + (size_t)t * d, t, kb, vb, N, d, causal, window, scale, s, o,
+                      &l, &Dt);
+        double* g = dq + ((size_t)bh * nq + x) * d;
+        for (int c = 0; c < d; ++c) g[c] = 0.0;
+        for (long kk = 0; kk < N; ++kk) {
+          if (!allowed(causal, window, t, kk)) continue;
+          const double p = exp(s[kk] - l);
+          const double ds = p * (dot_q_k(ob + (size_t)t * d, vb + (size_t)kk * d, d) - Dt);
+          for (int c = 0; c < d; ++c) g[c] += scale * ds * widen_bf16(kb[(size_t)kk * d + c]);
+        }
+      } else {
+        const long kk = krows[x - nq];
+        double* gk = dk + ((size_t)bh * nk + (x - nq)) * d;
+        double* gv = dv + ((size_t)bh * nk + (x - nq)) * d;
+        for (int c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
+        for (long t = 0; t < N; ++t) {
+          if (!allowed(causal, window, t, kk)) continue;
+          double l, Dt;
+          row_lse_and_D(qb + (size_t)t * d, ob + (size_t)t * d, t, kb, vb, N, d, causal, window, scale, s, o,
+                        &l, &Dt);
+          const double p = exp(scale * dot_q_k(qb + (size_t)t * d, kb + (size_t)kk * d, d) - l);
+          const double ds = p * (dot_q_k(ob + (size_t)t * d, vb + (size_t)kk * d, d) - Dt);
+          for (int c = 0; c < d; ++c) {
+            gk[c] += scale * ds * widen_bf16(qb[(size_t)t * d + c]);
+            gv[c] += p * widen_bf16(ob[(size_t)t * d + c]);
+          }
+        }
+      }
+    }
+    free(s);
+    free(o);
+  }
+  return failed ? -2 : 0;
+}
+
+/*
+ * Ring simulation of the backward ([RA-CN] "Backward 需要让梯度也沿环传播": the
+ * owner of a query shard accumulates its dQ from every K/V block; the dK and
+ * dV of a travelling block accumulate the contributions of each query owner
+ * it passes and return to the block's owner at the end; the probabilities
+ * are recomputed from the forward's saved logsumexp).
+ * Inputs: q, k, v, dout (bf16 bit patterns) and the forward's out and lse
+ * (doubles), all in natural order.  First D_t = dO_t . out_t for every row.
+ * P virtual ranks; at step s rank r holds block j = (r - s) mod P together
+ * with that block's accumulators (dK~, dV~); for its allowed pairs (i, k):
+ *   P_ik = exp(scale q_i . k_k - lse_i),  dS_ik = P_ik (dO_i . v_k - D_i)
+ *   dQ_i += scale dS_ik k_k   (kept by rank r)
+ *   dK~_k += scale dS_ik q_i,  dV~_k += P_ik dO_i   (travel with block j)
+ * then every rank passes block j and its accumulators to rank r + 1.  After
+ * P steps each block's accumulators are back at its owner, which writes
+ * them as dK, dV.  Outputs dq, dk, dv are [BH][N][d] doubles in natural
+ * order; visits (NULL or [BH][N][N]) counts every (query, key) pair used.
+ */
+int oracle_ring_bwd(int BH, long N, int d, int P, int causal, long window, int layout,
+                    const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                    const double* out, const double* lse, double* dq, double* dk, double* dv,
+                    long* visits, int nthreads) {
+  if (BH <= 0 || N <= 0 || d <= 0 || !layout_ok(layout, N, P)) return -1;
+  set_threads(nthreads);
+  const long n = N / P;
+  const double scale = 1.0 / sqrt((double)d);
+  int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int bh = 0; bh < BH; ++bh) {
+    const size_t base = (size_t)bh * N;
+    double* D = (double*)malloc(sizeof(double) * (size_t)N);
+    /* accumulators by the rank holding them: acc[holder][local key][c] */
+    double* accK = (double*)calloc((size_t)P * n * d, sizeof(double));
+    double* accV = (double*)calloc((size_t)P * n * d, sizeof(double));
+    double* nextK = (double*)malloc(sizeof(double) * (size_t)P * n * d);
+    double* nextV = (double*)malloc(sizeof(double) * (size_t)P * n * d);
+    if (!D || !accK || !accV || !nextK || !nextV) {
+#pragma omp atomic write
+      failed = 1;
+      free(D); free(accK); free(accV); free(nextK); free(nextV);
+      continue;
+    }
+    for (long t = 0; t < N; ++t) {
+      double acc = 0.0;
+      for (int c = 0; c < d; ++c) acc += widen_bf16(dout[(base + t) * d + c]) * out[(base + t) * d + c];
+      D[t] = acc;
+    }
+    for (long t = 0; t < N; ++t)
+      for (int c = 0; c < d; ++c) dq[(base + t) * d + c] = 0.0;
+    for (int step = 0; step < P; ++step) {
+      for (int r = 0; r < P; ++r) {
+        const int j = oracle_block_at(P, r, step);
+        double* aK = accK + (size_t)r * n * d;
+        double* aV = accV + (size_t)r * n * d;
+        for (long i = 0; i < n; ++i) {
+          const long tq = oracle_position(layout, n, P, r, i);
+          const uint16_t* qrow = q + (base + tq) * d;
+          const uint16_t* dorow = dout + (base + tq) * d;
+          double* g = dq + (base + tq) * d;
+          for (long kk = 0; kk < n; ++kk) {
+            const long tk = oracle_position(layout, n, P, j, kk);
+            if (!allowed(causal, window, tq, tk)) continue;
+            const uint16_t* krow = k + (base + tk) * d;
+            const uint16_t* vrow = v + (base + tk) * d;
+            const double p = exp(scale * dot_q_k(qrow, krow, d) - lse[base + tq]);
+            const double ds = p * (dot_q_k(dorow, vrow, d) - D[tq]);
+            for (int c = 0; c < d; ++c) {
+              g[c] += scale * ds * widen_bf16(krow[c]);
+              aK[(size_t)kk * d + c] += scale * ds * widen_bf16(qrow[c]);
+              aV[(size_t)kk * d + c] += p * widen_bf16(dorow[c]);
+            }
+            if (visits) visits[(base + tq) * N + tk] += 1;
+          }
+        }
+      }
+      /* rank r passes its block's accumulators to rank r + 1 */
+      for (int r = 0; r < P; ++r) {
+        const int to = (r + 1) % P;
+        memcpy(nextK + (size_t)to * n * d, accK + (size_t)r * n * d, sizeof(double) * (size_t)n * d);
+        memcpy(nextV + (size_t)to * n * d, accV + (size_t)r * n * d, sizeof(double) * (size_t)n * d);
+      }
+      double* tK = accK; accK = nextK; nextK = tK;
+      double* tV = accV; accV = nextV; nextV = tV;
+    }
+    /* back at the owner: rank j holds block j's accumulators */
+    for (int j = 0; j < P; ++j)
+      for (long kk = 0; kk < n; ++kk) {
+        const long tk = oracle_position(layout, n, P, j, kk);
+        memcpy(dk + (base + tk) * d, accK + ((size_t)j * n + kk) * d, sizeof(double) * d);
+        memcpy(dv + (base + tk) * d, accV + ((size_t)j * n + kk) * d, sizeof(double) * d);
+      }
+    free(D); free(accK); free(accV); free(nextK); free(nextV);
+  }
+  return failed ? -2 : 0;
+}

@@ -395,6 +395,137 @@ def pin_positions(orc):
                 assert orc.owner(layout, n, P, orc.position(layout, n, P, r, i)) == (r, i)
 
 
+# -------------------------------------------------------------- the backward
+def _torch_grads(q, k, v, dout, mask):
+    """float64 autograd of torch's scaled_dot_product_attention (a library
+    routine) for the bf16 inputs widened exactly; mask is a boolean [N, N]
+    (True = allowed) or None."""
+    qt, kt, vt = (torch.from_numpy(bits_to_f64(x)).requires_grad_(True) for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, attn_mask=None if mask is None else torch.from_numpy(mask))
+    out.backward(torch.from_numpy(bits_to_f64(dout)))
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+def _mask(N, causal, window=0):
+    if window:
+        return band_matrix(N, window)
+    return allowed_matrix(N, True) if causal else None
+
+
+def pin_bwd_autograd(orc):
+    """Reduction to a library routine: the dense backward equals float64
+    autograd through torch's scaled_dot_product_attention ([RA-CN] "Backward
+    需要让梯度也沿环传播": every Q-K/V interaction contributes a gradient)."""
+    for (BH, N, d, causal, w) in ((2, 19, 8, False, 0), (2, 24, 16, True, 0), (1, 33, 64, True, 0),
+                                  (1, 21, 4, True, 5), (3, 5, 1, True, 0)):
+        q, k, v, do = (rand_bits((BH, N, d), 300 + N + x) for x in range(4))
+        ref = _torch_grads(q, k, v, do, _mask(N, causal, w))
+        got = orc.dense_bwd(q, k, v, do, causal, window=w)
+        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+            _close(a, b, 1e-12, f"bwd autograd {name} N={N} d={d} causal={causal} w={w}")
+
+
+def pin_bwd_finite_differences(orc):
+    """Central differences of L = sum(dO * O), O from torch's float64
+    scaled_dot_product_attention, at a few coordinates of q, k and v: an
+    independent check of the chain rule (including the D = rowsum(dO * O)
+    term of the softmax derivative)."""
+    BH, N, d = 1, 10, 4
+    q, k, v, do = (rand_bits((BH, N, d), 320 + x) for x in range(4))
+    base = [torch.from_numpy(bits_to_f64(x)) for x in (q, k, v)]
+    dof = torch.from_numpy(bits_to_f64(do))
+    rng = np.random.default_rng(5)
+    for causal in (False, True):
+        grads = orc.dense_bwd(q, k, v, do, causal)
+        for which in range(3):
+            for _ in range(4):
+                t, c = int(rng.integers(N)), int(rng.integers(d))
+                h = 1e-5
+                vals = []
+                for sign in (1.0, -1.0):
+                    xs = [b.clone() for b in base]
+                    xs[which][0, t, c] += sign * h
+                    o = torch.nn.functional.scaled_dot_product_attention(*xs, is_causal=causal)
+                    vals.append(float((o * dof).sum()))
+                fd = (vals[0] - vals[1]) / (2 * h)
+                got = grads[which][0, t, c]
+                assert abs(fd - got) <= 1e-7 * max(1.0, abs(got)), \
+                    f"finite difference {'qkv'[which]}[{t},{c}] causal={causal}: {fd} vs {got}"
+
+
+def pin_bwd_closed_forms(orc):
+    """Closed forms: (a) every v row equal: O does not depend on q or k, so
+    dq = dk = 0; (b) window 1 (each query sees only itself): P = 1, so dv = dO
+    and dq = dk = 0; (c) N = 1: the same."""
+    BH, N, d = 2, 12, 4
+    q, k, do = rand_bits((BH, N, d), 331), rand_bits((BH, N, d), 332), rand_bits((BH, N, d), 333)
+    c = np.array([0.75, -2.0, 0.125, 1.5], np.float32)
+    v = to_bits(np.broadcast_to(c, (BH, N, d)))
+    for causal in (False, True):
+        dq, dk, _ = orc.dense_bwd(q, k, v, do, causal)
+        _close(dq, 0.0, 1e-13, "constant v: dq")
+        _close(dk, 0.0, 1e-13, "constant v: dk")
+    v = rand_bits((BH, N, d), 334)
+    dq, dk, dv = orc.dense_bwd(q, k, v, do, True, window=1)
+    _close(dv, bits_to_f64(do), 0.0, "window 1: dv = dO")
+    _close(dq, 0.0, 0.0, "window 1: dq")
+    _close(dk, 0.0, 0.0, "window 1: dk")
+    dq, dk, dv = orc.dense_bwd(q[:, :1], k[:, :1], v[:, :1], do[:, :1], False)
+    _close(dv, bits_to_f64(do[:, :1]), 0.0, "N = 1: dv = dO")
+    _close(dq, 0.0, 0.0, "N = 1: dq")
+
+
+def pin_bwd_invariants(orc):
+    """Identities of the gradients: each softmax row's dS sums to zero, so
+    sum_k dK_k = 0; each probability row sums to one, so sum_k dV_k =
+    sum_t dO_t; and sum_t q_t . dQ_t = sum_k k_k . dK_k (both are
+    scale * sum dS_tk q_t . k_k), which a transposed dS would break."""
+    BH, N, d = 2, 26, 8
+    q, k, v, do = (rand_bits((BH, N, d), 340 + x) for x in range(4))
+    qf, kf, dof = bits_to_f64(q), bits_to_f64(k), bits_to_f64(do)
+    for causal, w in ((False, 0), (True, 0), (True, 7)):
+        dq, dk, dv = orc.dense_bwd(q, k, v, do, causal, window=w)
+        _close(dk.sum(1), 0.0, 1e-12, f"sum dK = 0 (causal={causal}, w={w})")
+        _close(dv.sum(1), dof.sum(1), 1e-12, f"sum dV = sum dO (causal={causal}, w={w})")
+        _close(np.einsum("btd,btd->b", qf, dq), np.einsum("btd,btd->b", kf, dk), 1e-12,
+               f"q.dQ = k.dK (causal={causal}, w={w})")
+
+
+def pin_bwd_rows_match(orc):
+    """The sampled-row backward gives the same rows as the full one."""
+    BH, N, d = 2, 30, 8
+    q, k, v, do = (rand_bits((BH, N, d), 350 + x) for x in range(4))
+    qrows, krows = [0, 7, 29, 13], [29, 0, 15, 28]
+    for causal, w in ((False, 0), (True, 0), (True, 6)):
+        full = orc.dense_bwd(q, k, v, do, causal, window=w)
+        dq, dk, dv = orc.dense_bwd_rows(q, k, v, do, causal, qrows, krows, window=w)
+        _close(dq, full[0][:, qrows], 1e-13, "rows dq")
+        _close(dk, full[1][:, krows], 1e-13, "rows dk")
+        _close(dv, full[2][:, krows], 1e-13, "rows dv")
+
+
+def pin_ring_bwd_equals_dense(orc):
+    """The ring backward (dQ kept by the query owner, dK and dV travelling
+    with their block and returning to its owner; [RA-CN] "Backward
+    需要让梯度也沿环传播") reaches the dense gradients for every divisor P of
+    N, every layout, causal or not, with and without a window, and uses
+    every allowed (query, key) pair exactly once."""
+    for (BH, N, d) in ((2, 24, 4), (1, 12, 16)):
+        q, k, v, do = (rand_bits((BH, N, d), 360 + d + x) for x in range(4))
+        for causal, w in ((False, 0), (True, 0), (True, 5)):
+            ref = orc.dense_bwd(q, k, v, do, causal, window=w)
+            out, lse = orc.dense(q, k, v, causal, window=w)
+            allowed = _mask(N, causal, w)
+            allowed = np.ones((N, N), bool) if allowed is None else allowed
+            for P in [p for p in range(1, N + 1) if N % p == 0]:
+                for layout in layouts_for(N, P):
+                    got = orc.ring_bwd(q, k, v, do, out, lse, P, causal, layout, visits=True, window=w)
+                    for name, a, b in zip(("dq", "dk", "dv"), got[:3], ref):
+                        _close(a, b, 1e-12, f"ring bwd {name} P={P} layout={layout} causal={causal} w={w}")
+                    assert np.array_equal(got[3][0], allowed.astype(np.int64)), (P, layout, causal, w)
+
+
 ALL_PINS = [
     pin_equal_keys_closed_form,
     pin_constant_values,
@@ -414,4 +545,10 @@ ALL_PINS = [
     pin_merge_two_point_example,
     pin_golden_schedule,
     pin_positions,
+    pin_bwd_autograd,
+    pin_bwd_finite_differences,
+    pin_bwd_closed_forms,
+    pin_bwd_invariants,
+    pin_bwd_rows_match,
+    pin_ring_bwd_equals_dense,
 ]

@@ -42,6 +42,28 @@ MUTATIONS = [
     ("block partial ignores the mask in the sum",
      "      if (!allowed(causal, window, pos_q, kpos[kk])) continue;\n      double w",
      "      double w", None),
+    ("backward dS drops the D term (dense)",
+     "const double ds = p * (dot_q_k(dorow, vb + (size_t)kk * d, d) - Dt);",
+     "const double ds = p * dot_q_k(dorow, vb + (size_t)kk * d, d);", 0),
+    ("backward dK without the scale (dense)", "gk[c] += scale * ds * widen_bf16(qrow[c]);",
+     "gk[c] += ds * widen_bf16(qrow[c]);", None),
+    ("backward dV weighted by dS instead of P (dense)", "gv[c] += p * widen_bf16(dorow[c]);",
+     "gv[c] += ds * widen_bf16(dorow[c]);", None),
+    ("backward D taken as zero (dense)", "      D[idx] = Dt;", "      D[idx] = 0.0;", None),
+    ("backward dQ against V instead of K (dense)",
+     "for (int c = 0; c < d; ++c) g[c] += scale * ds * widen_bf16(kb[(size_t)kk * d + c]);",
+     "for (int c = 0; c < d; ++c) g[c] += scale * ds * widen_bf16(vb[(size_t)kk * d + c]);", 0),
+    ("ring backward passes accumulators the wrong way", "const int to = (r + 1) % P;",
+     "const int to = (r + P - 1) % P;", None),
+    ("ring backward drops D", "const double ds = p * (dot_q_k(dorow, vrow, d) - D[tq]);",
+     "const double ds = p * dot_q_k(dorow, vrow, d);", None),
+    ("ring backward dQ uses q instead of k", "g[c] += scale * ds * widen_bf16(krow[c]);",
+     "g[c] += scale * ds * widen_bf16(qrow[c]);", None),
+    ("ring backward ignores the saved lse",
+     "const double p = exp(scale * dot_q_k(qrow, krow, d) - lse[base + tq]);",
+     "const double p = exp(scale * dot_q_k(qrow, krow, d));", None),
+    ("sampled backward dV uses the query's q",
+     "gv[c] += p * widen_bf16(ob[(size_t)t * d + c]);", "gv[c] += p * widen_bf16(qb[(size_t)t * d + c]);", None),
 ]
 
 
