@@ -249,6 +249,34 @@ RINGATTN_API int ring_attn_finalize(ring_attn_t h, int r, ring_state_t s, float*
 RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
                   void* workspace, void* stream);
 
+/* Ring backward on one device ([RA-CN] "Backward 需要让梯度也沿环传播": every
+ * Q-K/V block interaction contributes a gradient; the owner of a query shard
+ * accumulates its dQ from every K/V block, while the dK and dV of a
+ * travelling block accumulate the contributions of each query owner it
+ * passes and return to the block's owner; the probabilities are recomputed
+ * from the forward's saved per-row logsumexp).  With P = exp(scale QK^T -
+ * lse) over the allowed pairs, D = rowsum(dO * out), dS = P (dO V^T - D):
+ *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+ *   q, k, v   natural order [B][H][N][d] bf16 (the forward's inputs)
+ *   out, lse  the forward's outputs: [B][H][N][d] and [B][H][N] fp32
+ *   dout      the gradient of the loss with respect to out, [B][H][N][d] bf16
+ *   dq, dk, dv  outputs, natural order [B][H][N][d] fp32
+ *   workspace ring_attn_bwd_workspace_size() bytes, 256-byte aligned: the
+ *             per-row lse and D, shard-major, and two buffers of the
+ *             travelling dK/dV accumulators, fp32 [P][B][H][n][d] each
+ * P steps; step s runs two kernels over every shard r and block
+ * j = (r - s) mod P: one per 128-key tile of j (dK and dV, the accumulators
+ * entering from slot r of one buffer and leaving to slot r + 1 of the other)
+ * and one per 128-row query tile of shard r (dQ, kept in dq between steps).
+ * K/V blocks are read in place through strided views of k and v.  Layouts
+ * CONTIGUOUS and STRIPED, causal or not, with or without RING_OPT_WINDOW;
+ * RING_ERR_UNSUPPORTED for ZIGZAG and for grouped K/V heads (Hkv < H).
+ * Pointers 16-byte aligned.  Asynchronous on `stream`. */
+RINGATTN_API int ring_attn_bwd_workspace_size(ring_attn_t h, size_t* bytes);
+RINGATTN_API int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, const float* out,
+                               const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                               void* workspace, void* stream);
+
 /* Split-K/V decode and short-query prefill ([RA-CN]: the query is sent to
  * every K/V shard, each shard computes a local online-softmax state, and the
  * states are merged exactly; [GRA] "Why partial results are allowed to

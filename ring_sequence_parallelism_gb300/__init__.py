@@ -88,6 +88,11 @@ def ring_attn_fwd(h, q, k, v, out, lse, workspace, stream=None):
                                          _stream(stream)))
 
 
+def ring_attn_bwd(h, q, k, v, out, lse, dout, dq, dk, dv, workspace, stream=None):
+    _lib.check(_lib.load().ring_attn_bwd(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), _ptr(workspace), _stream(stream)))
+
+
 def ring_attn_check(h, stream=None):
     _lib.check(_lib.load().ring_attn_check(h, _stream(stream)))
 
@@ -169,6 +174,34 @@ class RingAttention:
         if self._workspace is None or self._workspace.numel() < need:
             self._workspace = torch.empty(need, dtype=torch.uint8, device=device or "cuda")
         return self._workspace
+
+    def bwd_workspace_size(self) -> int:
+        n = ctypes.c_size_t()
+        _lib.check(self._lib.ring_attn_bwd_workspace_size(self.handle, ctypes.byref(n)))
+        return n.value
+
+    def bwd(self, q, k, v, out, lse, dout, dq=None, dk=None, dv=None, stream=None):
+        """Gradients of the forward's loss with respect to q, k, v given dout
+        (the gradient at out), from the forward's out and lse.  Returns fp32
+        dq, dk, dv [B, H, N, d] in natural order."""
+        import torch
+
+        shape = (self.B, self.H, self.N, self.d)
+        for t in (q, k, v, dout):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
+                raise ValueError(f"q, k, v, dout must be contiguous CUDA bfloat16 tensors {shape}")
+        if out.dtype != torch.float32 or tuple(out.shape) != shape or not out.is_contiguous():
+            raise ValueError(f"out must be a contiguous float32 tensor {shape}")
+        if lse.dtype != torch.float32 or tuple(lse.shape) != shape[:3] or not lse.is_contiguous():
+            raise ValueError(f"lse must be a contiguous float32 tensor {shape[:3]}")
+        dq = torch.empty(shape, dtype=torch.float32, device=q.device) if dq is None else dq
+        dk = torch.empty(shape, dtype=torch.float32, device=q.device) if dk is None else dk
+        dv = torch.empty(shape, dtype=torch.float32, device=q.device) if dv is None else dv
+        need = self.bwd_workspace_size()
+        if getattr(self, "_bwd_ws", None) is None or self._bwd_ws.numel() < need:
+            self._bwd_ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ring_attn_bwd(self.handle, q, k, v, out, lse, dout, dq, dk, dv, self._bwd_ws, stream)
+        return dq, dk, dv
 
     def new_state(self, device=None):
         import torch

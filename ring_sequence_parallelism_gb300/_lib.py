@@ -62,6 +62,8 @@ SIGNATURES = {
     "ring_attn_get_timing": (_i, [_vp, _pf, _pf, _pf, _pf]),
     "ring_attn_check": (_i, [_vp, _vp]),
     "ring_attn_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_bwd_workspace_size": (_i, [_vp, ctypes.POINTER(ctypes.c_size_t)]),
+    "ring_attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
 _LIB = None

@@ -163,6 +163,7 @@ int ensure_device(ring_attn* h) {
   int rc = get_encoder();
   if (rc) return rc;
   RA_CUDA((cudaError_t)prepare_block_partial_kernels(), "cudaFuncSetAttribute");
+  RA_CUDA((cudaError_t)prepare_backward_kernels(), "cudaFuncSetAttribute (backward)");
   RA_CUDA(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking), "cudaStreamCreate");
   const int P = h->plan.P;
   RA_CUDA(cudaEventCreateWithFlags(&h->packed, cudaEventDisableTiming), "cudaEventCreate");
@@ -577,6 +578,115 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     h->copied[s + 1] = 1;
   }
   h->timed_valid = timing;
+  return RING_OK;
+}
+
+// ---------------------------------------------------------------- backward
+// Workspace of ring_attn_bwd: lse2 and D shard-major [BH][P][n_pad] fp32,
+// then the dK~ and dV~ accumulator buffers X and Y, [P][BH][n][d] fp32 each.
+struct BwdWorkspace {
+  size_t lse_off, d_off, acc_bytes, acc_off, total;
+  int n_pad;
+};
+static BwdWorkspace bwd_workspace(const Plan& p) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  BwdWorkspace w;
+  w.n_pad = p.T * kTileM;
+  const size_t vec = up((size_t)p.B * p.H * p.P * (size_t)w.n_pad * 4);
+  w.lse_off = 0;
+  w.d_off = vec;
+  w.acc_bytes = up((size_t)p.B * p.H * (size_t)p.N * p.d * 4);
+  w.acc_off = 2 * vec;
+  w.total = w.acc_off + 4 * w.acc_bytes;
+  return w;
+}
+
+int ring_attn_bwd_workspace_size(ring_attn_t h, size_t* bytes) {
+  if (!h || !bytes) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  *bytes = bwd_workspace(h->plan).total;
+  return RING_OK;
+}
+
+int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, const float* out, const float* lse,
+                  const void* dout, float* dq, float* dk, float* dv, void* workspace, void* stream) {
+  if (!h || !q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  const Plan& p = h->plan;
+  if (p.layout == RING_LAYOUT_ZIGZAG)
+    return fail(RING_ERR_UNSUPPORTED, "the backward supports the contiguous and striped layouts");
+  if (p.Hkv != p.H) return fail(RING_ERR_UNSUPPORTED, "the backward needs one K/V head per query head");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(RING_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  int rc = ensure_device(h);
+  if (rc) return rc;
+  const int P = p.P, BH = p.B * p.H;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const BwdWorkspace w = bwd_workspace(p);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse_off);
+  float* Dv = reinterpret_cast<float*>(ws + w.d_off);
+  float* acc_k[2] = {reinterpret_cast<float*>(ws + w.acc_off), reinterpret_cast<float*>(ws + w.acc_off + 2 * w.acc_bytes)};
+  float* acc_v[2] = {reinterpret_cast<float*>(ws + w.acc_off + w.acc_bytes),
+                     reinterpret_cast<float*>(ws + w.acc_off + 3 * w.acc_bytes)};
+
+  // shard views of the natural-order bf16 tensors (box 64 columns x 128 rows)
+  const bool striped = p.layout == RING_LAYOUT_STRIPED;
+  const cuuint64_t d = (cuuint64_t)p.d, n = (cuuint64_t)p.n, row_b = d * 2;
+  CUtensorMap maps[4];
+  const void* src[4] = {q, dout, k, v};
+  for (int x = 0; x < 4; ++x) {
+    if (striped) {
+      cuuint64_t dims[4] = {d, (cuuint64_t)P, n, (cuuint64_t)BH};
+      cuuint64_t str[3] = {row_b, row_b * P, row_b * (cuuint64_t)p.N};
+      if ((rc = encode_map(&maps[x], src[x], dims, str, 1, kTileM))) return rc;
+    } else {
+      cuuint64_t dims[4] = {d, n, (cuuint64_t)P, (cuuint64_t)BH};
+      cuuint64_t str[3] = {row_b, row_b * n, row_b * (cuuint64_t)p.N};
+      if ((rc = encode_map(&maps[x], src[x], dims, str, kTileM, 1))) return rc;
+    }
+  }
+  const long long row_r = striped ? 1 : p.n, row_i = striped ? P : 1;
+  RA_CUDA((cudaError_t)launch_bwd_prep(out, lse, dout, lse2, Dv, BH, p.n, w.n_pad, p.d, P, row_r, row_i, p.N, cs),
+          "backward prep launch");
+  BwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.lse2 = lse2;
+  a.Dv = Dv;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.N = p.N;
+  a.row_r = row_r;
+  a.row_i = row_i;
+  a.err = h->d_err;
+  a.wait_limit_ns = h->wait_limit_ns;
+  a.n = (int)p.n;
+  a.n_pad = w.n_pad;
+  a.P = P;
+  a.BH = BH;
+  a.T = p.T;
+  a.KT = p.KT;
+  a.q_mode = striped ? kQStriped : kQContiguous;
+  a.causal = p.causal;
+  a.layout = p.layout;
+  a.window = p.window;
+  a.scale = (float)(1.0 / std::sqrt((double)p.d));
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
+  for (int s = 0; s < P; ++s) {
+    const int cur = s & 1;
+    a.step = s;
+    a.accumulate = s > 0 ? 1 : 0;
+    a.last = s == P - 1 ? 1 : 0;
+    a.acc_in_k = acc_k[cur];
+    a.acc_in_v = acc_v[cur];
+    a.acc_out_k = acc_k[cur ^ 1];
+    a.acc_out_v = acc_v[cur ^ 1];
+    RA_CUDA((cudaError_t)launch_bwd_dkdv(a, &maps[0], &maps[1], &maps[2], &maps[3], p.d, cs), "backward dK/dV launch");
+    RA_CUDA((cudaError_t)launch_bwd_dq(a, &maps[0], &maps[1], &maps[2], &maps[3], p.d, cs), "backward dQ launch");
+  }
   return RING_OK;
 }
 

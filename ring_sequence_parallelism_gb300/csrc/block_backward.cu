@@ -1,0 +1,818 @@
+// block_backward.cu -- the ring backward of blockwise attention (sm_103a).
+//
+// What it computes ([RA-CN] "Backward 需要让梯度也沿环传播": every Q-K/V block
+// interaction contributes a gradient; the owner of a query shard accumulates
+// its dQ from every K/V block; the dK and dV of a travelling K/V block
+// accumulate the contributions of the query owners it passes and return to
+// the block's owner; the probabilities are recomputed from the forward's
+// saved per-row logsumexp, block by block, as in FlashAttention's backward).
+// For the allowed pairs (i, k) of query shard r against block j:
+//   P_ik  = exp(scale q_i . k_k - lse_i)
+//   dP_ik = dO_i . v_k
+//   dS_ik = P_ik (dP_ik - D_i),   D_i = dO_i . out_i
+//   dV~_k += P_ik dO_i,  dK~_k += dS_ik q_i,  dQ~_i += dS_ik k_k
+// and at the end dK = scale dK~, dV = dV~, dQ = scale dQ~.
+//
+// Kernels of one ring step (every shard r against block j = (r - s) mod P):
+//   bwd_dkdv_kernel  one 128-key tile of block j per CTA (keys stationary),
+//                    looping over the query tiles of shard r that see it:
+//                      S^T  = K Q^T            (tcgen05, K-major operands)
+//                      dP^T = V dO^T
+//                      P^T, dS^T by the key-row threads, bf16 into TMEM
+//                      dV~ += P^T dO,  dK~ += dS^T Q   (A operand in TMEM)
+//                    The accumulators enter from slot r of one buffer and
+//                    leave to slot r + 1 of the other: they travel with the
+//                    block; the last step writes dK and dV in natural order.
+//   bwd_dq_kernel    one 128-row query tile of shard r per CTA (queries
+//                    stationary), looping over the key tiles of block j:
+//                      S = Q K^T,  dP = dO V^T,  dS by the query-row threads,
+//                      dQ~ += dS K              (A operand in TMEM)
+//                    dQ~ stays with its owner: the running value lives in dq.
+// Every MMA shape is one the forward kernel uses (S = Q K^T with both
+// operands K-major; O += P V with P in TMEM and V MN-major): each operand
+// here is a 128-row tile of a natural-order tensor loaded by TMA with the
+// 128-byte swizzle.  S and dP are computed in both kernels (7 MMAs per tile
+// pair, 5 of them distinct) so that no gradient needs atomics.
+//
+// CTA: 192 threads.  warp 0 allocates TMEM and its lane 0 issues the TMA
+// loads; warp 1 issues the MMAs (elected lane); warps 2-5 own one TMEM lane
+// quadrant each (warp % 4), one row per thread.  Every mbarrier wait is
+// bounded; on expiry the CTA drains what it started and frees TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "tc_ptx.h"
+#include "tmem_regs.h"
+
+namespace ringattn {
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdTmemCols = 512;
+constexpr long long kFar = 1LL << 40;  // "no bound" for the diagonal offsets
+
+// Shared memory of both kernels: two stationary tiles (K, V or Q, dO), two
+// stages of two streamed tiles, two stages of 128 lse2 and D values (dK/dV
+// kernel only), the barriers.  Every tile starts on a 1024-byte boundary.
+template <int D>
+struct BwdLayout {
+  static constexpr int kTile = kTileM * D * 2;      // one 128-row tile
+  static constexpr int kOffA = 0;                   // stationary tile 1 (K or Q)
+  static constexpr int kOffB = kTile;               // stationary tile 2 (V or dO)
+  static constexpr int kOffX = 2 * kTile;           // streamed tile 1, 2 stages (Q or K)
+  static constexpr int kOffY = 4 * kTile;           // streamed tile 2, 2 stages (dO or V)
+  static constexpr int kOffLse = 6 * kTile;         // [2][128] floats
+  static constexpr int kOffD = kOffLse + 1024;      // [2][128] floats
+  static constexpr int kOffBar = kOffD + 1024;
+  static constexpr int kBarAB = 0;       // stationary tiles landed
+  static constexpr int kBarFull = 1;     // [2] stage landed
+  static constexpr int kBarEmpty = 3;    // [2] stage released by the MMAs
+  static constexpr int kBarS = 5;        // S (or S^T) in TMEM
+  static constexpr int kBarDP = 6;       // dP (or dP^T) in TMEM
+  static constexpr int kBarP = 7;        // P^T in TMEM (dK/dV) / S read (dQ), 128 arrivals
+  static constexpr int kBarDS = 8;       // dS in TMEM, 128 arrivals
+  static constexpr int kBarAcc = 9;      // every MMA done: accumulators final
+  static constexpr int kBarDrain = 10;
+  static constexpr int kNumBars = 11;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kBytes = kOffAbort + 4;
+  // room to align the base to 1024; at least 120 KB so that only one CTA
+  // (the owner of all 512 TMEM columns) is resident per SM
+  static constexpr int kAlloc = (kBytes + 1024) > 122880 ? (kBytes + 1024) : 122880;
+  // TMEM columns: S/P [0,128), dP/dS [128,256), accumulators from 256
+  static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc1 = 256, kTmAcc2 = 256 + D;
+};
+
+// Mask of block (shard r, block j) for the contiguous and striped layouts:
+// local query i and local key k form an allowed pair iff
+//   dlo <= k - i <= dhi  and  k < klim.
+// Contiguous: pos_q - pos_k = (r - j) n + i - k; striped: (i - k) P + r - j.
+// Causal: pos_k <= pos_q.  Window W: pos_q - pos_k < W.
+struct BwdRule {
+  long long dhi, dlo, kmax;  // kmax: last key that can be allowed (n - 1, or -1 for none)
+};
+
+__device__ __forceinline__ long long floor_div_ll(long long x, long long q) {
+  return x >= 0 ? x / q : -((-x + q - 1) / q);
+}
+
+__device__ __forceinline__ BwdRule bwd_rule(const BwdArgs& a, int r, int j) {
+  BwdRule w;
+  w.kmax = a.n - 1;
+  w.dhi = kFar;
+  w.dlo = -kFar;
+  if (!a.causal) return w;
+  if (a.layout == RING_LAYOUT_STRIPED) {
+    w.dhi = j <= r ? 0 : -1;
+    if (a.window > 0) w.dlo = floor_div_ll((long long)(r - j) - a.window, a.P) + 1;
+  } else {
+    w.dhi = (long long)(r - j) * a.n;
+    if (a.window > 0) w.dlo = (long long)(r - j) * a.n - a.window + 1;
+  }
+  return w;
+}
+
+// Row of (shard r, local i) of head bh in a natural-order tensor.
+__device__ __forceinline__ long long nat_row(const BwdArgs& a, int bh, int r, long long i) {
+  return (long long)bh * a.N + (long long)r * a.row_r + i * a.row_i;
+}
+
+// TMA load of a 128-row tile (rows i0.. of shard `sh`, head bh) of a
+// natural-order tensor through its shard view, D/64 sub-tiles of 64 columns.
+template <int D>
+__device__ __forceinline__ void load_rows(const BwdArgs& a, uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                          int sh, int i0, int bh) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint32_t to = dst + c * (kTileM * 128);
+    if (a.q_mode == kQStriped)
+      tma_load_4d(to, map, bar, c * 64, sh, i0, bh);
+    else
+      tma_load_4d(to, map, bar, c * 64, i0, sh, bh);
+  }
+}
+
+// ------------------------------------------------------------ preprocessing
+// lse2 = lse * log2(e) and D = dO . out for every query row, written
+// shard-major [BH][P][n_pad] (rows n..n_pad-1 of a shard get 0).  Eight
+// threads per row, 16 columns each (d = 128) or 8 (d = 64).
+__global__ void bwd_prep_kernel(const float* __restrict__ out, const float* __restrict__ lse,
+                                const __nv_bfloat16* __restrict__ dout, float* __restrict__ lse2,
+                                float* __restrict__ Dv, int BH, long long n, int n_pad, int d, int P,
+                                long long row_r, long long row_i, long long N) {
+  const long long rows = (long long)BH * P * n_pad;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = gid / 8;
+  const int part = (int)(gid % 8);
+  if (row >= rows) return;  // whole groups of 8 leave together (rows are a multiple of 128)
+  const long long i = row % n_pad;
+  const long long rb = row / n_pad;
+  const int r = (int)(rb % P);
+  const int bh = (int)(rb / P);
+  float acc = 0.0f;
+  float l2 = 0.0f;
+  if (i < n) {
+    const long long g = (long long)bh * N + (long long)r * row_r + i * row_i;
+    const int cols = d / 8;
+    const float* o = out + g * d + part * cols;
+    const __nv_bfloat16* x = dout + g * d + part * cols;
+    for (int c = 0; c < cols; c += 8) {
+      const float4 o0 = *reinterpret_cast<const float4*>(o + c);
+      const float4 o1 = *reinterpret_cast<const float4*>(o + c + 4);
+      const uint4 xb = *reinterpret_cast<const uint4*>(x + c);
+      const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xb);
+      const float2 a0 = __bfloat1622float2(x2[0]), a1 = __bfloat1622float2(x2[1]);
+      const float2 a2 = __bfloat1622float2(x2[2]), a3 = __bfloat1622float2(x2[3]);
+      acc += a0.x * o0.x + a0.y * o0.y + a1.x * o0.z + a1.y * o0.w;
+      acc += a2.x * o1.x + a2.y * o1.y + a3.x * o1.z + a3.y * o1.w;
+    }
+    l2 = lse[g] * 1.4426950408889634f;
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  if (part == 0) {
+    Dv[row] = i < n ? acc : 0.0f;
+    lse2[row] = l2;
+  }
+}
+
+// ------------------------------------------------------------ dK/dV kernel
+// blockIdx.x -> (shard r, head bh, key tile kt); the CTAs of one (shard,
+// head) are consecutive so its Q and dO tiles stay in L2, and within it the
+// key tiles run in ascending order (under the causal mask the early keys of
+// a block meet the most queries).
+template <int D, bool kWin>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ CUtensorMap q_map,
+                    const __grid_constant__ CUtensorMap do_map, const __grid_constant__ CUtensorMap k_map,
+                    const __grid_constant__ CUtensorMap v_map) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar0 = sbase + L::kOffBar;
+  auto bar = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  const int kt = blockIdx.x % a.KT;
+  const int g = blockIdx.x / a.KT;
+  const int bh = g % a.BH;
+  const int r = g / a.BH;
+  int j = (r - a.step) % a.P;
+  if (j < 0) j += a.P;
+  BwdRule rule = bwd_rule(a, r, j);
+  if (!kWin) rule.dlo = -kFar;
+  // query tiles that see a key of this tile
+  const long long k0 = (long long)kt * kTileN;
+  const long long k1 = min(k0 + kTileN - 1, rule.kmax);
+  int it_lo = 0, n_it = 0;
+  if (k0 <= k1) {
+    const long long i_lo = max(0LL, k0 - rule.dhi);
+    const long long i_hi = min((long long)a.n - 1, k1 - rule.dlo);
+    if (i_lo <= i_hi) {
+      it_lo = (int)(i_lo / kTileM);
+      n_it = (int)(i_hi / kTileM) + 1 - it_lo;
+    }
+  }
+
+  // key-row threads (warps 2..5): start loading the incoming accumulators
+  const int quad = warp & 3;
+  const long long k_row = k0 + quad * 32 + lane;  // this thread's key
+  const bool k_valid = k_row < a.n;
+  const size_t slot_rows = (size_t)a.BH * a.n;
+  const float* in_k = a.acc_in_k + ((size_t)r * slot_rows + (size_t)bh * a.n + (size_t)k_row) * D;
+  const float* in_v = a.acc_in_v + ((size_t)r * slot_rows + (size_t)bh * a.n + (size_t)k_row) * D;
+  const bool load_acc = warp >= 2 && a.accumulate && k_valid;
+
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < L::kNumBars; ++x)
+      mbar_init(bar(x), (x == L::kBarP || x == L::kBarDS) ? 128 : 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_async_smem();
+    if (n_it > 0) {
+      // K and V tiles of block j, then the first query stage
+      mbar_expect_tx(bar(L::kBarAB), 2 * L::kTile);
+      load_rows<D>(a, sbase + L::kOffA, &k_map, bar(L::kBarAB), j, (int)k0, bh);
+      load_rows<D>(a, sbase + L::kOffB, &v_map, bar(L::kBarAB), j, (int)k0, bh);
+    }
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(kBwdTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0 && n_it > 0) {
+      const float* lse_base = a.lse2 + ((size_t)bh * a.P + r) * a.n_pad;
+      const float* d_base = a.Dv + ((size_t)bh * a.P + r) * a.n_pad;
+      int issued = 0;
+      bool ok = true;
+      for (int x = 0; x < n_it && ok; ++x) {
+        const int st = x & 1;
+        if (x >= 2) ok = mbar_wait(bar(L::kBarEmpty + st), ((x >> 1) - 1) & 1, abort_flag, a, 21);
+        if (!ok) break;
+        const int i0 = (it_lo + x) * kTileM;
+        mbar_expect_tx(bar(L::kBarFull + st), 2 * L::kTile + 1024);
+        load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &q_map, bar(L::kBarFull + st), r, i0, bh);
+        load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &do_map, bar(L::kBarFull + st), r, i0, bh);
+        bulk_load(sbase + L::kOffLse + st * 512, lse_base + i0, 512, bar(L::kBarFull + st));
+        bulk_load(sbase + L::kOffD + st * 512, d_base + i0, 512, bar(L::kBarFull + st));
+        issued = x + 1;
+      }
+      // drain: every load started has landed before the CTA can exit
+      const unsigned long long lim = a.wait_limit_ns;
+      mbar_drain_wait(bar(L::kBarAB), 0, lim);
+      for (int x = issued > 2 ? issued - 2 : 0; x < issued; ++x)
+        mbar_drain_wait(bar(L::kBarFull + (x & 1)), (x >> 1) & 1, lim);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (n_it > 0) {
+      constexpr uint32_t idesc_s = instr_desc(kTileM, kTileN, false);
+      constexpr uint32_t idesc_acc = instr_desc(kTileM, D, true);
+      const uint64_t k_desc = smem_desc(sbase + L::kOffA, 16, 1024);
+      const uint64_t v_desc = smem_desc(sbase + L::kOffB, 16, 1024);
+      auto q_s = [&](int x) { return sbase + L::kOffX + (x & 1) * L::kTile; };
+      auto do_s = [&](int x) { return sbase + L::kOffY + (x & 1) * L::kTile; };
+      bool ok = warp_wait(bar(L::kBarAB), 0, abort_flag, a, 22) &&
+                warp_wait(bar(L::kBarFull), 0, abort_flag, a, 23);
+      if (ok) {
+        mma_qk<D>(tmem + L::kTmS, k_desc, smem_desc(q_s(0), 16, 1024), idesc_s);  // S^T(0) = K Q^T
+        mma_commit_elect(bar(L::kBarS));
+        mma_qk<D>(tmem + L::kTmDP, v_desc, smem_desc(do_s(0), 16, 1024), idesc_s);  // dP^T(0) = V dO^T
+        mma_commit_elect(bar(L::kBarDP));
+      }
+      for (int x = 0; x < n_it && ok; ++x) {
+        const uint32_t acc = (x > 0 || a.accumulate) ? 1u : 0u;
+        const bool more = x + 1 < n_it;
+        // dV~ += P^T dO once P^T(x) is in TMEM
+        ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 24);
+        if (!ok) break;
+        tc_fence_after();
+        mma_pv(tmem + L::kTmAcc1, tmem + L::kTmS, smem_desc(do_s(x), kTileM * 128, 1024), idesc_acc, acc);
+        // S^T(x+1) overwrites S/P(x) after that MMA (one thread's MMAs run in order)
+        if (more) {
+          ok = warp_wait(bar(L::kBarFull + ((x + 1) & 1)), ((x + 1) >> 1) & 1, abort_flag, a, 25);
+          if (!ok) break;
+          mma_qk<D>(tmem + L::kTmS, k_desc, smem_desc(q_s(x + 1), 16, 1024), idesc_s);
+          mma_commit_elect(bar(L::kBarS));
+        }
+        // dK~ += dS^T Q once dS^T(x) is in TMEM
+        ok = warp_wait(bar(L::kBarDS), x & 1, abort_flag, a, 26);
+        if (!ok) break;
+        tc_fence_after();
+        mma_pv(tmem + L::kTmAcc2, tmem + L::kTmDP, smem_desc(q_s(x), kTileM * 128, 1024), idesc_acc, acc);
+        mma_commit_elect(bar(L::kBarEmpty + (x & 1)));
+        if (more) {
+          mma_qk<D>(tmem + L::kTmDP, v_desc, smem_desc(do_s(x + 1), 16, 1024), idesc_s);
+          mma_commit_elect(bar(L::kBarDP));
+        }
+      }
+      if (ok) mma_commit_elect(bar(L::kBarAcc));
+      mma_commit_elect(bar(L::kBarDrain));
+      mbar_drain_wait(bar(L::kBarDrain), 0, a.wait_limit_ns);
+    }
+  } else {
+    // ------------------------------------- key-row threads and epilogue
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    uint32_t buf[D];
+    if (load_acc) {
+#pragma unroll
+      for (int q8 = 0; q8 < D / 8; ++q8) ld_global_v8(in_v + q8 * 8, buf + q8 * 8);
+    }
+    // keep both accumulators in TMEM before the first MMA (dV first, then dK)
+    if (a.accumulate) {
+      if (!load_acc) {
+#pragma unroll
+        for (int e = 0; e < D; ++e) buf[e] = 0u;
+      }
+      if constexpr (D == 128) tmem_store128(tmem + lane_off + L::kTmAcc1, buf);
+      else tmem_store64(tmem + lane_off + L::kTmAcc1, buf);
+      tmem_store_wait();
+      if (load_acc) {
+#pragma unroll
+        for (int q8 = 0; q8 < D / 8; ++q8) ld_global_v8(in_k + q8 * 8, buf + q8 * 8);
+      }
+      if constexpr (D == 128) tmem_store128(tmem + lane_off + L::kTmAcc2, buf);
+      else tmem_store64(tmem + lane_off + L::kTmAcc2, buf);
+      tmem_store_wait();
+    }
+    // this key's allowed queries: i_lo_k <= i <= i_hi_k
+    const long long i_lo_k = k_row <= rule.kmax ? max(0LL, k_row - rule.dhi) : (long long)a.n;
+    const long long i_hi_k = min((long long)a.n - 1, k_row - rule.dlo);
+    bool ok = true;
+    for (int x = 0; x < n_it; ++x) {
+      const int st = x & 1;
+      const long long i0 = (long long)(it_lo + x) * kTileM;
+      const float* lse_s = reinterpret_cast<const float*>(smem + L::kOffLse + st * 512);
+      const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512);
+      // the stage's lse2 and D landed (TMA writes are visible to the threads
+      // that observe this barrier), then S^T(x) is in TMEM
+      ok = warp_wait(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30) &&
+           warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 27);
+      if (!ok) break;
+      tc_fence_after();
+      float p[kTileM];
+      {
+        uint32_t t[kTileM];
+        tmem_load128(tmem + lane_off + L::kTmS, t);
+#pragma unroll
+        for (int e = 0; e < kTileM; ++e) p[e] = __uint_as_float(t[e]);
+      }
+      const bool masked = !(i0 >= i_lo_k && i0 + kTileM - 1 <= i_hi_k);
+      // P^T = exp2(S^T scale log2(e) - lse2), 0 outside the mask; bf16 pairs
+      // over the first 64 columns, in two halves
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pb[32];
+#pragma unroll
+        for (int e = h * 64; e < h * 64 + 64; e += 2) {
+          float v0 = fast_exp2(fmaf(p[e], a.scale_log2, -lse_s[e]));
+          float v1 = fast_exp2(fmaf(p[e + 1], a.scale_log2, -lse_s[e + 1]));
+          if (masked) {
+            const long long i = i0 + e;
+            if (i < i_lo_k || i > i_hi_k) v0 = 0.0f;
+            if (i + 1 < i_lo_k || i + 1 > i_hi_k) v1 = 0.0f;
+          }
+          p[e] = v0;
+          p[e + 1] = v1;
+          pb[(e - h * 64) / 2] = pack_bf16(v0, v1);
+        }
+        tmem_store32(tmem + lane_off + L::kTmS + h * 32, pb);
+      }
+      tmem_store_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarP));
+      // dS^T = P^T (dP^T - D), 32 columns at a time, bf16 over the read columns
+      ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 28);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kTileM / 32; ++c) {
+        uint32_t t[32];
+        tmem_load32(tmem + lane_off + L::kTmDP + c * 32, t);
+        uint32_t sb[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float s0 = p[c * 32 + e] * (__uint_as_float(t[e]) - d_s[c * 32 + e]);
+          const float s1 = p[c * 32 + e + 1] * (__uint_as_float(t[e + 1]) - d_s[c * 32 + e + 1]);
+          sb[e / 2] = pack_bf16(s0, s1);
+        }
+        tmem_store16(tmem + lane_off + L::kTmDP + c * 16, sb);
+      }
+      tmem_store_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDS));
+    }
+    if (ok && n_it > 0) {
+      ok = warp_wait(bar(L::kBarAcc), 0, abort_flag, a, 29);
+      tc_fence_after();
+    }
+    if (ok) {
+      // ------------------------------------------------------ epilogue
+      // (tcgen05.ld is warp-collective: every lane loads, valid keys store)
+      const bool have = n_it > 0 || a.accumulate;
+      float* dst_v;
+      float* dst_k;
+      if (a.last) {
+        const long long gk = nat_row(a, bh, j, k_row);
+        dst_v = a.dv + gk * D;
+        dst_k = a.dk + gk * D;
+      } else {
+        const int to = r + 1 == a.P ? 0 : r + 1;
+        const size_t off = ((size_t)to * slot_rows + (size_t)bh * a.n + (size_t)k_row) * D;
+        dst_v = a.acc_out_v + off;
+        dst_k = a.acc_out_k + off;
+      }
+      const float ks = a.last ? a.scale : 1.0f;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        float* dst = which == 0 ? dst_v : dst_k;
+        const float mul = which == 0 ? 1.0f : ks;
+        const uint32_t col = which == 0 ? L::kTmAcc1 : L::kTmAcc2;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t t[32];
+          if (have) tmem_load32(tmem + lane_off + col + c * 32, t);
+          if (k_valid) {
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = have ? __uint_as_float(t[q8 * 8 + e]) * mul : 0.0f;
+              st_global_v8(dst + c * 32 + q8 * 8, v);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBwdTmemCols)
+                 : "memory");
+  }
+}
+
+// --------------------------------------------------------------- dQ kernel
+// blockIdx.x -> (shard r, head bh, query tile t); consecutive CTAs share a
+// (shard, head) so the key block stays in L2, and the query tiles with the
+// most keys (the last ones under the causal mask) start first.
+template <int D, bool kWin>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ CUtensorMap q_map,
+                  const __grid_constant__ CUtensorMap do_map, const __grid_constant__ CUtensorMap k_map,
+                  const __grid_constant__ CUtensorMap v_map) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar0 = sbase + L::kOffBar;
+  auto bar = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  const int t = a.T - 1 - (int)(blockIdx.x % a.T);
+  const int g = blockIdx.x / a.T;
+  const int bh = g % a.BH;
+  const int r = g / a.BH;
+  int j = (r - a.step) % a.P;
+  if (j < 0) j += a.P;
+  BwdRule rule = bwd_rule(a, r, j);
+  if (!kWin) rule.dlo = -kFar;
+  // key tiles with an allowed key for a row of this tile
+  const long long i0 = (long long)t * kTileM;
+  const long long i1 = min(i0 + kTileM - 1, (long long)a.n - 1);
+  int kt_lo = 0, n_kt = 0;
+  {
+    const long long k_lo = max(0LL, i0 + rule.dlo);
+    const long long k_hi = min(rule.kmax, i1 + rule.dhi);
+    if (k_lo <= k_hi) {
+      kt_lo = (int)(k_lo / kTileN);
+      n_kt = (int)(k_hi / kTileN) + 1 - kt_lo;
+    }
+  }
+
+  // query-row threads (warps 2..5): this row's statistics and incoming dQ~
+  const int quad = warp & 3;
+  const long long i_row = i0 + quad * 32 + lane;
+  const bool i_valid = i_row < a.n;
+  const long long g_row = nat_row(a, bh, r, i_valid ? i_row : 0);
+  float* dq_row = a.dq + g_row * D;
+  uint32_t buf[D];
+  float lse2_i = 0.0f, D_i = 0.0f;
+  const bool rows = warp >= 2;
+  if (rows) {
+    const size_t v = ((size_t)bh * a.P + r) * a.n_pad + (size_t)i_row;
+    if (i_valid && n_kt > 0) {
+      lse2_i = a.lse2[v];
+      D_i = a.Dv[v];
+    }
+    if (a.accumulate && n_kt > 0) {
+#pragma unroll
+      for (int q8 = 0; q8 < D / 8; ++q8) {
+        if (i_valid) {
+          ld_global_v8(dq_row + q8 * 8, buf + q8 * 8);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) buf[q8 * 8 + e] = 0u;
+        }
+      }
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    for (int x = 0; x < L::kNumBars; ++x)
+      mbar_init(bar(x), (x == L::kBarP || x == L::kBarDS) ? 128 : 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_async_smem();
+    if (n_kt > 0) {
+      mbar_expect_tx(bar(L::kBarAB), 2 * L::kTile);
+      load_rows<D>(a, sbase + L::kOffA, &q_map, bar(L::kBarAB), r, (int)i0, bh);
+      load_rows<D>(a, sbase + L::kOffB, &do_map, bar(L::kBarAB), r, (int)i0, bh);
+    }
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(kBwdTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0 && n_kt > 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int x = 0; x < n_kt && ok; ++x) {
+        const int st = x & 1;
+        if (x >= 2) ok = mbar_wait(bar(L::kBarEmpty + st), ((x >> 1) - 1) & 1, abort_flag, a, 31);
+        if (!ok) break;
+        const int k0 = (kt_lo + x) * kTileN;
+        mbar_expect_tx(bar(L::kBarFull + st), 2 * L::kTile);
+        load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &k_map, bar(L::kBarFull + st), j, k0, bh);
+        load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &v_map, bar(L::kBarFull + st), j, k0, bh);
+        issued = x + 1;
+      }
+      const unsigned long long lim = a.wait_limit_ns;
+      mbar_drain_wait(bar(L::kBarAB), 0, lim);
+      for (int x = issued > 2 ? issued - 2 : 0; x < issued; ++x)
+        mbar_drain_wait(bar(L::kBarFull + (x & 1)), (x >> 1) & 1, lim);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (n_kt > 0) {
+      constexpr uint32_t idesc_s = instr_desc(kTileM, kTileN, false);
+      constexpr uint32_t idesc_acc = instr_desc(kTileM, D, true);
+      const uint64_t q_desc = smem_desc(sbase + L::kOffA, 16, 1024);
+      const uint64_t do_desc = smem_desc(sbase + L::kOffB, 16, 1024);
+      auto k_s = [&](int x) { return sbase + L::kOffX + (x & 1) * L::kTile; };
+      auto v_s = [&](int x) { return sbase + L::kOffY + (x & 1) * L::kTile; };
+      bool ok = warp_wait(bar(L::kBarAB), 0, abort_flag, a, 32) &&
+                warp_wait(bar(L::kBarFull), 0, abort_flag, a, 33);
+      if (ok) {
+        mma_qk<D>(tmem + L::kTmS, q_desc, smem_desc(k_s(0), 16, 1024), idesc_s);  // S(0) = Q K^T
+        mma_commit_elect(bar(L::kBarS));
+        mma_qk<D>(tmem + L::kTmDP, do_desc, smem_desc(v_s(0), 16, 1024), idesc_s);  // dP(0) = dO V^T
+        mma_commit_elect(bar(L::kBarDP));
+      }
+      for (int x = 0; x < n_kt && ok; ++x) {
+        const bool more = x + 1 < n_kt;
+        // S(x+1) may overwrite S(x) once the row threads have read it
+        if (more) {
+          ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 34) &&
+               warp_wait(bar(L::kBarFull + ((x + 1) & 1)), ((x + 1) >> 1) & 1, abort_flag, a, 35);
+          if (!ok) break;
+          tc_fence_after();
+          mma_qk<D>(tmem + L::kTmS, q_desc, smem_desc(k_s(x + 1), 16, 1024), idesc_s);
+          mma_commit_elect(bar(L::kBarS));
+        }
+        // dQ~ += dS K once dS(x) is in TMEM (over the dP columns)
+        ok = warp_wait(bar(L::kBarDS), x & 1, abort_flag, a, 36);
+        if (!ok) break;
+        tc_fence_after();
+        mma_pv(tmem + L::kTmAcc1, tmem + L::kTmDP, smem_desc(k_s(x), kTileN * 128, 1024), idesc_acc,
+               (x > 0 || a.accumulate) ? 1u : 0u);
+        mma_commit_elect(bar(L::kBarEmpty + (x & 1)));
+        if (more) {
+          mma_qk<D>(tmem + L::kTmDP, do_desc, smem_desc(v_s(x + 1), 16, 1024), idesc_s);
+          mma_commit_elect(bar(L::kBarDP));
+        }
+      }
+      if (ok) mma_commit_elect(bar(L::kBarAcc));
+      mma_commit_elect(bar(L::kBarDrain));
+      mbar_drain_wait(bar(L::kBarDrain), 0, a.wait_limit_ns);
+    }
+  } else {
+    // ------------------------------------- query-row threads and epilogue
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    if (a.accumulate && n_kt > 0) {
+      if constexpr (D == 128) tmem_store128(tmem + lane_off + L::kTmAcc1, buf);
+      else tmem_store64(tmem + lane_off + L::kTmAcc1, buf);
+      tmem_store_wait();
+    }
+    // this row's allowed keys: k_lo_i <= k <= k_hi_i
+    const long long k_lo_i = max(0LL, i_row + rule.dlo);
+    const long long k_hi_i = i_valid ? min(rule.kmax, i_row + rule.dhi) : -1;
+    bool ok = true;
+    for (int x = 0; x < n_kt; ++x) {
+      const long long kbase = (long long)(kt_lo + x) * kTileN;
+      ok = warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 37);
+      if (!ok) break;
+      tc_fence_after();
+      float p[kTileN];
+      {
+        uint32_t tt[kTileN];
+        tmem_load128(tmem + lane_off + L::kTmS, tt);
+#pragma unroll
+        for (int e = 0; e < kTileN; ++e) p[e] = __uint_as_float(tt[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarP));  // S(x) read: the S columns are free
+      const bool masked = !(kbase >= k_lo_i && kbase + kTileN - 1 <= k_hi_i);
+#pragma unroll
+      for (int e = 0; e < kTileN; ++e) {
+        float v = fast_exp2(fmaf(p[e], a.scale_log2, -lse2_i));
+        if (masked && (kbase + e < k_lo_i || kbase + e > k_hi_i)) v = 0.0f;
+        p[e] = v;
+      }
+      ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 38);
+      if (!ok) break;
+      tc_fence_after();
+      // dS = P (dP - D), 32 columns at a time, bf16 over the read dP columns
+#pragma unroll
+      for (int c = 0; c < kTileN / 32; ++c) {
+        uint32_t tt[32];
+        tmem_load32(tmem + lane_off + L::kTmDP + c * 32, tt);
+        uint32_t sb[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float s0 = p[c * 32 + e] * (__uint_as_float(tt[e]) - D_i);
+          const float s1 = p[c * 32 + e + 1] * (__uint_as_float(tt[e + 1]) - D_i);
+          sb[e / 2] = pack_bf16(s0, s1);
+        }
+        tmem_store16(tmem + lane_off + L::kTmDP + c * 16, sb);
+      }
+      tmem_store_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDS));
+    }
+    if (ok && n_kt > 0) {
+      ok = warp_wait(bar(L::kBarAcc), 0, abort_flag, a, 39);
+      tc_fence_after();
+    }
+    if (ok) {
+      // ------------------------------------------------------ epilogue
+      // (tcgen05.ld is warp-collective: every lane loads, valid rows store)
+      const float mul = a.last ? a.scale : 1.0f;
+      if (n_kt > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t tt[32];
+          tmem_load32(tmem + lane_off + L::kTmAcc1 + c * 32, tt);
+          if (i_valid) {
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(tt[q8 * 8 + e]) * mul;
+              st_global_v8(dq_row + c * 32 + q8 * 8, v);
+            }
+          }
+        }
+      } else if (i_valid && (!a.accumulate || a.last)) {
+        // no key of this block for the tile: dQ~ stays as it is (zero at
+        // step 0), scaled at the last step
+#pragma unroll
+        for (int q8 = 0; q8 < D / 8; ++q8) {
+          uint32_t x8[8];
+          float v[8];
+          if (a.accumulate) {
+            ld_global_v8(dq_row + q8 * 8, x8);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x8[e] = 0u;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(x8[e]) * mul;
+          st_global_v8(dq_row + q8 * 8, v);
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBwdTmemCols)
+                 : "memory");
+  }
+}
+
+template <int D>
+int prepare_bwd_one() {
+  int e;
+  if ((e = (int)cudaFuncSetAttribute(bwd_dkdv_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     BwdLayout<D>::kAlloc)))
+    return e;
+  if ((e = (int)cudaFuncSetAttribute(bwd_dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     BwdLayout<D>::kAlloc)))
+    return e;
+  if ((e = (int)cudaFuncSetAttribute(bwd_dq_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     BwdLayout<D>::kAlloc)))
+    return e;
+  return (int)cudaFuncSetAttribute(bwd_dq_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   BwdLayout<D>::kAlloc);
+}
+
+}  // namespace
+
+int prepare_backward_kernels() {
+  int e = prepare_bwd_one<64>();
+  if (e) return e;
+  return prepare_bwd_one<128>();
+}
+
+int launch_bwd_prep(const float* out, const float* lse, const void* dout, float* lse2, float* Dv, int BH,
+                    long long n, int n_pad, int d, int P, long long row_r, long long row_i, long long N,
+                    void* stream) {
+  const long long threads = (long long)BH * P * n_pad * 8;
+  const int block = 256;
+  const long long grid = (threads + block - 1) / block;
+  if (grid <= 0) return 0;
+  bwd_prep_kernel<<<(unsigned)grid, block, 0, static_cast<cudaStream_t>(stream)>>>(
+      out, lse, static_cast<const __nv_bfloat16*>(dout), lse2, Dv, BH, n, n_pad, d, P, row_r, row_i, N);
+  return (int)cudaGetLastError();
+}
+
+int launch_bwd_dkdv(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
+                    int d, void* stream) {
+  const int grid = a.KT * a.P * a.BH;
+  if (grid <= 0) return 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
+  const CUtensorMap& om = *static_cast<const CUtensorMap*>(do_map);
+  const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
+  const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
+  const bool win = a.causal && a.window > 0;
+  if (d == 64) {
+    if (win) bwd_dkdv_kernel<64, true><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
+    else bwd_dkdv_kernel<64, false><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
+  } else {
+    if (win) bwd_dkdv_kernel<128, true><<<grid, kBwdThreads, BwdLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
+    else bwd_dkdv_kernel<128, false><<<grid, kBwdThreads, BwdLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
+  }
+  return (int)cudaGetLastError();
+}
+
+int launch_bwd_dq(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
+                  int d, void* stream) {
+  const int grid = a.T * a.P * a.BH;
+  if (grid <= 0) return 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
+  const CUtensorMap& om = *static_cast<const CUtensorMap*>(do_map);
+  const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
+  const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
+  const bool win = a.causal && a.window > 0;
+  if (d == 64) {
+    if (win) bwd_dq_kernel<64, true><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
+    else bwd_dq_kernel<64, false><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
+  } else {
+    if (win) bwd_dq_kernel<128, true><<<grid, kBwdThreads, BwdLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
+    else bwd_dq_kernel<128, false><<<grid, kBwdThreads, BwdLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
+  }
+  return (int)cudaGetLastError();
+}
+
+}  // namespace ringattn

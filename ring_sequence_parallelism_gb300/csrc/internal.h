@@ -108,6 +108,31 @@ struct StepArgs {
   unsigned short active[kMaxShards];
 };
 
+// Arguments of the backward step kernels (one ring step, every shard).
+// Natural-order tensors are [BH][N][d]; the row of (shard r, local i) within
+// a head is r * row_r + i * row_i.  Shard-major vectors are [BH][P][n_pad].
+struct BwdArgs {
+  const float* lse2;  // lse * log2(e) of every query row, shard-major
+  const float* Dv;    // D = rowsum(dO * out) of every query row, shard-major
+  float* dq;          // natural: the running dQ (unscaled) between steps, scale * dQ after the last
+  const float* acc_in_k;  // [P][BH][n][d]: the dK~ and dV~ accumulators held by shard r (slot r)
+  const float* acc_in_v;
+  float* acc_out_k;  // the other buffer: shard r passes its block's accumulators to slot r + 1
+  float* acc_out_v;
+  float* dk;  // natural, written at the last step (dK scaled, dV as is)
+  float* dv;
+  long long N, row_r, row_i;
+  int* err;  // device error words [0] flags, [1] site
+  unsigned long long wait_limit_ns;
+  int n, n_pad, P, BH, T, KT;
+  int q_mode;  // kQContiguous or kQStriped: Q, dO, K and V through the same shard view
+  int causal, layout, step;
+  int accumulate;  // step > 0: continue the accumulators
+  int last;        // step P - 1: write the gradients
+  long long window;
+  float scale, scale_log2;
+};
+
 // Device error flags.
 constexpr int kErrTimeout = 1;
 
@@ -142,5 +167,15 @@ int block_partial_smem_bytes(int d);
 // CTAs of one block-partial launch: one per (pair of query tiles, shard, head).
 int block_partial_grid(int T, int n_active, int BH);
 int prepare_block_partial_kernels();
+// Backward (block_backward.cu).  The maps are shard views of natural-order
+// bf16 tensors (box 64 x 128 rows), coordinates as for kQContiguous/kQStriped.
+int launch_bwd_prep(const float* out, const float* lse, const void* dout, float* lse2, float* Dv, int BH,
+                    long long n, int n_pad, int d, int P, long long row_r, long long row_i, long long N,
+                    void* stream);
+int launch_bwd_dkdv(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
+                    int d, void* stream);
+int launch_bwd_dq(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
+                  int d, void* stream);
+int prepare_backward_kernels();
 
 }  // namespace ringattn

@@ -9,7 +9,9 @@ Recipe: Q, K, V are i.i.d. N(0, 1) float32 drawn on the CPU from a seeded
 rounded to bfloat16 with round-to-nearest-even.  The long-context workload
 additionally multiplies 1% of the key rows (floor(N/100) token positions, the
 same for every head, chosen by ``randperm`` of a second generator seeded
-``seed + 1``) by 8 after rounding; the multiplication is exact in bf16.
+``seed + 1``) by 8 after rounding; the multiplication is exact in bf16.  The
+backward's upstream gradient dO is drawn the same way from a generator
+seeded ``seed + 7``.
 """
 from __future__ import annotations
 
@@ -101,6 +103,19 @@ def make_qkv(B: int, H: int, N: int, d: int, seed: int, key_boost_frac: float = 
     if device != "cpu":
         q, k, v = (x.to(device) for x in (q, k, v))
     return q, k, v
+
+
+def make_dout(B: int, H: int, N: int, d: int, seed: int, device="cpu", pin: bool = False):
+    """The upstream gradient dO for the backward: [B, H, N, d] i.i.d. N(0, 1)
+    float32 from a CPU generator seeded ``seed + 7`` (one head at a time),
+    rounded to bf16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 7)
+    t = torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=pin)
+    for b in range(B):
+        for h in range(H):
+            t[b, h].copy_(torch.randn((N, d), generator=g, dtype=torch.float32))
+    return t.to(device) if device != "cpu" else t
 
 
 def boosted_key_rows(N: int, seed: int, frac: float) -> torch.Tensor:

@@ -354,6 +354,11 @@ WINDOW_CASES = [
     (1, 2, 8 * 256, 128, 8, "striped", 700),
     (1, 2, 8 * 256, 128, 8, "contiguous", 700),
     (1, 2, 4 * 256, 128, 4, "contiguous", 4 * 256),  # a window of N: plain causal
+    # tile ranges that start well inside the block (first loop index 1 to 3):
+    # the producer's stage-release waits count each tile's own uses
+    (1, 2, 4 * 512, 128, 4, "contiguous", 300),
+    (1, 2, 4 * 1024, 128, 4, "striped", 1500),
+    (1, 2, 2 * 1024, 64, 2, "contiguous", 333),
 ]
 
 
