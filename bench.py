@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--bwd", action="store_true", help="time the ring backward (ring_attn_bwd) instead")
     ap.add_argument("--decode", type=int, default=0, metavar="LQ",
                     help="measure split-K/V decode of LQ new queries over the workload's K/V cache instead")
     return ap.parse_args()
@@ -430,6 +431,73 @@ def run_decode(args, w):
     att.close()
 
 
+def run_bwd(args, w):
+    """The ring backward (ring_attn_bwd) on the workload: q, k, v, the
+    forward's out and lse and a seeded dO resident in HBM; K backward calls
+    timed with CUDA events.  The metric counts 10*d FLOPs per allowed pair
+    (the five distinct matmuls S, dP, dV, dK, dQ; 2.5x the forward); the
+    kernels execute seven (S and dP in both kernels).  The roofline is the
+    dK/dV kernel's: 8*d FLOPs per allowed pair of a step (S^T, dP^T, dV, dK)."""
+    import torch
+
+    import ring_sequence_parallelism_gb300 as ra
+    from ring_sequence_parallelism_gb300.inputs import make_dout, make_workload
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    q, k, v = (x.to("cuda") for x in make_workload(w))
+    do = make_dout(w.B, w.H, w.N, w.d, w.seed, device="cuda")
+    att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
+    if w.window:
+        att.set_option(ra.RING_OPT_WINDOW, w.window)
+    out, lse = att.fwd(q, k, v)
+    shape = (w.B, w.H, w.N, w.d)
+    dq, dk, dv = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(3))
+    att.set_option(ra.RING_OPT_TIMING, 1)
+    for _ in range(args.warmup):
+        att.bwd(q, k, v, out, lse, do, dq, dk, dv)
+    att.check()
+    stream = torch.cuda.current_stream()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            att.bwd(q, k, v, out, lse, do, dq, dk, dv)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    t = att.bwd_timing()
+    att.check()
+    ms = e0.elapsed_time(e1) / args.steps
+    pairs = [att.step_work(s)[0] for s in range(w.P)]
+    BH = w.B * w.H
+    flops = 10 * w.d * sum(pairs)
+    pk, pk_kind = peaks()
+    peak_sus = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    dkdv_ms, dq_ms = sum(t["dkdv_ms"]), sum(t["dq_ms"])
+    ach_dkdv = 8 * w.d * sum(pairs) / (dkdv_ms * 1e-3) / 1e12
+    ach_dq = 6 * w.d * sum(pairs) / (dq_ms * 1e-3) / 1e12
+    line = {
+        "metric": "causal-adjusted attention backward TFLOP/s (10*d FLOPs per allowed pair)",
+        "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": dict(config_of(w), dout="N(0,1) bf16, seed + 7"),
+        "tokens_per_s": w.B * w.N / (ms * 1e-3),
+        "roofline": {"bound": "tensor", "kernel": "bwd_dkdv_kernel<128> (one launch per ring step)",
+                     "achieved": ach_dkdv, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach_dkdv / peak_sus,
+                     "peak_kind": f"bf16_tflops_sustained ({pk_kind})", "traffic": None,
+                     "algorithmic": "8*d FLOPs per allowed pair (S^T, dP^T, dV, dK)"},
+        "dq_kernel": {"achieved": ach_dq, "frac": ach_dq / peak_sus,
+                      "algorithmic": "6*d FLOPs per allowed pair (S, dP, dQ)"},
+        "bwd": {"dkdv_ms": t["dkdv_ms"], "dq_ms": t["dq_ms"], "prep_ms": t["prep_ms"],
+                "kernel_ms_total": dkdv_ms + dq_ms + t["prep_ms"]},
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps * (1 + 2 * w.P),
+    }
+    print(json.dumps(line), flush=True)
+    att.close()
+
+
 def main():
     args = parse()
     from ring_sequence_parallelism_gb300.inputs import WORKLOADS
@@ -437,6 +505,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.decode > 0:
         run_decode(args, w)
+    elif args.bwd:
+        run_bwd(args, w)
     elif args.impl == "reference":
         run_reference(args, w)
     else:

@@ -277,6 +277,12 @@ RINGATTN_API int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, cons
                                const float* lse, const void* dout, float* dq, float* dk, float* dv,
                                void* workspace, void* stream);
 
+/* Timings of the last ring_attn_bwd with RING_OPT_TIMING on, in ms: the
+ * dK/dV kernel and the dQ kernel of every step (arrays of P entries, NULL to
+ * skip) and the preprocessing kernel (lse * log2(e) and D).  Synchronises
+ * on the recorded events. */
+RINGATTN_API int ring_attn_get_bwd_timing(ring_attn_t h, float* dkdv_ms, float* dq_ms, float* prep_ms);
+
 /* Split-K/V decode and short-query prefill ([RA-CN]: the query is sent to
  * every K/V shard, each shard computes a local online-softmax state, and the
  * states are merged exactly; [GRA] "Why partial results are allowed to

@@ -203,6 +203,14 @@ class RingAttention:
         ring_attn_bwd(self.handle, q, k, v, out, lse, dout, dq, dk, dv, self._bwd_ws, stream)
         return dq, dk, dv
 
+    def bwd_timing(self):
+        """Per-step dK/dV and dQ kernel times (ms) of the last timed backward."""
+        dkdv = (ctypes.c_float * self.P)()
+        dq = (ctypes.c_float * self.P)()
+        prep = ctypes.c_float()
+        _lib.check(self._lib.ring_attn_get_bwd_timing(self.handle, dkdv, dq, ctypes.byref(prep)))
+        return {"dkdv_ms": list(dkdv), "dq_ms": list(dq), "prep_ms": prep.value}
+
     def new_state(self, device=None):
         import torch
 

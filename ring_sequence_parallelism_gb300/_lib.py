@@ -64,6 +64,7 @@ SIGNATURES = {
     "ring_attn_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ring_attn_bwd_workspace_size": (_i, [_vp, ctypes.POINTER(ctypes.c_size_t)]),
     "ring_attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_get_bwd_timing": (_i, [_vp, _pf, _pf, _pf]),
 }
 
 _LIB = None

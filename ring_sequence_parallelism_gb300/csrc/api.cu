@@ -126,6 +126,9 @@ struct ring_attn {
   cudaEvent_t packed = nullptr;
   std::vector<cudaEvent_t> landed, released;
   std::vector<cudaEvent_t> tk0, tk1, tc0, tc1, tw0, tw1;
+  std::vector<cudaEvent_t> tbk0, tbk1, tbq0, tbq1;  // backward: dK/dV and dQ kernels per step
+  cudaEvent_t tbp0 = nullptr, tbp1 = nullptr;          // backward preprocessing
+  bool bwd_timed_valid = false;
   std::vector<char> copied;  // [s]: the side stream filled slots for step s (timing)
   cudaEvent_t tp0 = nullptr, tp1 = nullptr;
   bool timed_valid = false;
@@ -169,10 +172,12 @@ int ensure_device(ring_attn* h) {
   RA_CUDA(cudaEventCreateWithFlags(&h->packed, cudaEventDisableTiming), "cudaEventCreate");
   if ((rc = make_events(h->landed, P, cudaEventDisableTiming))) return rc;
   if ((rc = make_events(h->released, P, cudaEventDisableTiming))) return rc;
-  for (auto* v : {&h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1})
+  for (auto* v : {&h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1, &h->tbk0, &h->tbk1, &h->tbq0, &h->tbq1})
     if ((rc = make_events(*v, P, cudaEventDefault))) return rc;
   RA_CUDA(cudaEventCreate(&h->tp0), "cudaEventCreate");
   RA_CUDA(cudaEventCreate(&h->tp1), "cudaEventCreate");
+  RA_CUDA(cudaEventCreate(&h->tbp0), "cudaEventCreate");
+  RA_CUDA(cudaEventCreate(&h->tbp1), "cudaEventCreate");
   RA_CUDA(cudaMalloc(&h->d_err, 2 * sizeof(int)), "cudaMalloc(error word)");
   RA_CUDA(cudaMemset(h->d_err, 0, 2 * sizeof(int)), "cudaMemset");
   h->device = dev;
@@ -259,9 +264,12 @@ int ring_attn_destroy(ring_attn_t h) {
     int prev = -1;
     cudaGetDevice(&prev);
     if (prev != h->device) cudaSetDevice(h->device);
-    for (auto* v : {&h->landed, &h->released, &h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1})
+    for (auto* v : {&h->landed, &h->released, &h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1, &h->tbk0,
+                    &h->tbk1, &h->tbq0, &h->tbq1})
       for (auto e : *v)
         if (e) cudaEventDestroy(e);
+    if (h->tbp0) cudaEventDestroy(h->tbp0);
+    if (h->tbp1) cudaEventDestroy(h->tbp1);
     if (h->packed) cudaEventDestroy(h->packed);
     if (h->tp0) cudaEventDestroy(h->tp0);
     if (h->tp1) cudaEventDestroy(h->tp1);
@@ -649,8 +657,11 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
     }
   }
   const long long row_r = striped ? 1 : p.n, row_i = striped ? P : 1;
+  const bool timing = h->timing != 0;
+  if (timing) RA_CUDA(cudaEventRecord(h->tbp0, cs), "cudaEventRecord");
   RA_CUDA((cudaError_t)launch_bwd_prep(out, lse, dout, lse2, Dv, BH, p.n, w.n_pad, p.d, P, row_r, row_i, p.N, cs),
           "backward prep launch");
+  if (timing) RA_CUDA(cudaEventRecord(h->tbp1, cs), "cudaEventRecord");
   BwdArgs a;
   std::memset(&a, 0, sizeof a);
   a.lse2 = lse2;
@@ -684,9 +695,27 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
     a.acc_in_v = acc_v[cur];
     a.acc_out_k = acc_k[cur ^ 1];
     a.acc_out_v = acc_v[cur ^ 1];
+    if (timing) RA_CUDA(cudaEventRecord(h->tbk0[s], cs), "cudaEventRecord");
     RA_CUDA((cudaError_t)launch_bwd_dkdv(a, &maps[0], &maps[1], &maps[2], &maps[3], p.d, cs), "backward dK/dV launch");
+    if (timing) RA_CUDA(cudaEventRecord(h->tbk1[s], cs), "cudaEventRecord");
+    if (timing) RA_CUDA(cudaEventRecord(h->tbq0[s], cs), "cudaEventRecord");
     RA_CUDA((cudaError_t)launch_bwd_dq(a, &maps[0], &maps[1], &maps[2], &maps[3], p.d, cs), "backward dQ launch");
+    if (timing) RA_CUDA(cudaEventRecord(h->tbq1[s], cs), "cudaEventRecord");
   }
+  h->bwd_timed_valid = timing;
+  return RING_OK;
+}
+
+int ring_attn_get_bwd_timing(ring_attn_t h, float* dkdv_ms, float* dq_ms, float* prep_ms) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  if (!h->ready || !h->bwd_timed_valid)
+    return fail(RING_ERR_INVALID_ARG, "no timed backward (set RING_OPT_TIMING before ring_attn_bwd)");
+  const int P = h->plan.P;
+  for (int s = 0; s < P; ++s) {
+    if (dkdv_ms) RA_CUDA(cudaEventElapsedTime(&dkdv_ms[s], h->tbk0[s], h->tbk1[s]), "cudaEventElapsedTime");
+    if (dq_ms) RA_CUDA(cudaEventElapsedTime(&dq_ms[s], h->tbq0[s], h->tbq1[s]), "cudaEventElapsedTime");
+  }
+  if (prep_ms) RA_CUDA(cudaEventElapsedTime(prep_ms, h->tbp0, h->tbp1), "cudaEventElapsedTime");
   return RING_OK;
 }
 

@@ -34,9 +34,11 @@
 // 128-byte swizzle.  S and dP are computed in both kernels (7 MMAs per tile
 // pair, 5 of them distinct) so that no gradient needs atomics.
 //
-// CTA: 192 threads.  warp 0 allocates TMEM and its lane 0 issues the TMA
-// loads; warp 1 issues the MMAs (elected lane); warps 2-5 own one TMEM lane
-// quadrant each (warp % 4), one row per thread.  Every mbarrier wait is
+// CTA: 320 threads.  warp 0 allocates TMEM and its lane 0 issues the TMA
+// loads; warp 1 issues the MMAs (elected lane); warps 2-9 own the rows, two
+// warps per TMEM lane quadrant (warp % 4), each thread one row and one half
+// of its 128 columns (two warps per SM sub-partition hide each other's TMEM
+// and MUFU latency).  Every mbarrier wait is
 // bounded; on expiry the CTA drains what it started and frees TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -51,7 +53,7 @@
 namespace ringattn {
 namespace {
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;
 constexpr int kBwdTmemCols = 512;
 constexpr long long kFar = 1LL << 40;  // "no bound" for the diagonal offsets
 
@@ -87,6 +89,39 @@ struct BwdLayout {
   // TMEM columns: S/P [0,128), dP/dS [128,256), accumulators from 256
   static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc1 = 256, kTmAcc2 = 256 + D;
 };
+
+// D (+)= A B with A (128 x 128 bf16) in TMEM as two halves of 32 packed
+// columns: K steps 0-3 (columns 0-63 of A) at a_tmem + 0..31 and K steps 4-7
+// (columns 64-127) at a_tmem + 64..95, each half written by its own warps
+// over the TMEM columns they read; B MN-major with the 128-byte swizzle
+// (+2 KB = 16 rows per K step).
+__device__ __forceinline__ void mma_pv_split(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 at, bl;\n\t.reg .b64 bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t"
+      "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, 128;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, 1;\n\t"
+      "add.u32 at, %1, 16;\n\tadd.u32 bl, %2, 256;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, 1;\n\t"
+      "add.u32 at, %1, 24;\n\tadd.u32 bl, %2, 384;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, 1;\n\t"
+      "add.u32 at, %1, 64;\n\tadd.u32 bl, %2, 512;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, 1;\n\t"
+      "add.u32 at, %1, 72;\n\tadd.u32 bl, %2, 640;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, 1;\n\t"
+      "add.u32 at, %1, 80;\n\tadd.u32 bl, %2, 768;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, 1;\n\t"
+      "add.u32 at, %1, 88;\n\tadd.u32 bl, %2, 896;\n\tmov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, 1;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_tmem), "r"((uint32_t)b_desc), "r"((uint32_t)(b_desc >> 32)), "r"(idesc),
+      "r"(accumulate)
+      : "memory");
+}
 
 // Mask of block (shard r, block j) for the contiguous and striped layouts:
 // local query i and local key k form an allowed pair iff
@@ -224,8 +259,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   }
 
-  // key-row threads (warps 2..5): start loading the incoming accumulators
+  // key-row threads (warps 2..9): lane quadrant warp % 4, column half
   const int quad = warp & 3;
+  const int half = warp >= 2 ? (warp - 2) >> 2 : 0;
   const long long k_row = k0 + quad * 32 + lane;  // this thread's key
   const bool k_valid = k_row < a.n;
   const size_t slot_rows = (size_t)a.BH * a.n;
@@ -235,7 +271,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < L::kNumBars; ++x)
-      mbar_init(bar(x), (x == L::kBarP || x == L::kBarDS) ? 128 : 1);
+      mbar_init(bar(x), (x == L::kBarP || x == L::kBarDS) ? 256 : 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
@@ -306,7 +342,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 24);
         if (!ok) break;
         tc_fence_after();
-        mma_pv(tmem + L::kTmAcc1, tmem + L::kTmS, smem_desc(do_s(x), kTileM * 128, 1024), idesc_acc, acc);
+        mma_pv_split(tmem + L::kTmAcc1, tmem + L::kTmS, smem_desc(do_s(x), kTileM * 128, 1024), idesc_acc, acc);
         // S^T(x+1) overwrites S/P(x) after that MMA (one thread's MMAs run in order)
         if (more) {
           ok = warp_wait(bar(L::kBarFull + ((x + 1) & 1)), ((x + 1) >> 1) & 1, abort_flag, a, 25);
@@ -318,7 +354,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = warp_wait(bar(L::kBarDS), x & 1, abort_flag, a, 26);
         if (!ok) break;
         tc_fence_after();
-        mma_pv(tmem + L::kTmAcc2, tmem + L::kTmDP, smem_desc(q_s(x), kTileM * 128, 1024), idesc_acc, acc);
+        mma_pv_split(tmem + L::kTmAcc2, tmem + L::kTmDP, smem_desc(q_s(x), kTileM * 128, 1024), idesc_acc, acc);
         mma_commit_elect(bar(L::kBarEmpty + (x & 1)));
         if (more) {
           mma_qk<D>(tmem + L::kTmDP, v_desc, smem_desc(do_s(x + 1), 16, 1024), idesc_s);
@@ -331,27 +367,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------- key-row threads and epilogue
+    // Two warps per TMEM lane quadrant: half h owns query columns
+    // [64h, 64h + 64) of S^T and dP^T and writes its bf16 P^T and dS^T into
+    // the first 32 columns of its own range, so the halves never touch each
+    // other's columns (the MMAs read the A operand with a jump at the middle).
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    uint32_t buf[D];
-    if (load_acc) {
-#pragma unroll
-      for (int q8 = 0; q8 < D / 8; ++q8) ld_global_v8(in_v + q8 * 8, buf + q8 * 8);
-    }
-    // keep both accumulators in TMEM before the first MMA (dV first, then dK)
+    const int c0 = half * 64;
+    constexpr int kHalfD = D / 2;  // accumulator columns this thread loads and stores
+    // keep both accumulators in TMEM before the first MMA (dV, then dK)
     if (a.accumulate) {
-      if (!load_acc) {
 #pragma unroll
-        for (int e = 0; e < D; ++e) buf[e] = 0u;
-      }
-      if constexpr (D == 128) tmem_store128(tmem + lane_off + L::kTmAcc1, buf);
-      else tmem_store64(tmem + lane_off + L::kTmAcc1, buf);
-      tmem_store_wait();
-      if (load_acc) {
+      for (int which = 0; which < 2; ++which) {
+        const float* src = (which == 0 ? in_v : in_k) + half * kHalfD;
+        const uint32_t col = (which == 0 ? L::kTmAcc1 : L::kTmAcc2) + half * kHalfD;
 #pragma unroll
-        for (int q8 = 0; q8 < D / 8; ++q8) ld_global_v8(in_k + q8 * 8, buf + q8 * 8);
+        for (int c = 0; c < kHalfD / 32; ++c) {
+          uint32_t buf[32];
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            if (load_acc) {
+              ld_global_v8(src + c * 32 + q8 * 8, buf + q8 * 8);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) buf[q8 * 8 + e] = 0u;
+            }
+          }
+          tmem_store32(tmem + lane_off + col + c * 32, buf);
+        }
       }
-      if constexpr (D == 128) tmem_store128(tmem + lane_off + L::kTmAcc2, buf);
-      else tmem_store64(tmem + lane_off + L::kTmAcc2, buf);
       tmem_store_wait();
     }
     // this key's allowed queries: i_lo_k <= i <= i_hi_k
@@ -360,30 +403,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int x = 0; x < n_it; ++x) {
       const int st = x & 1;
-      const long long i0 = (long long)(it_lo + x) * kTileM;
-      const float* lse_s = reinterpret_cast<const float*>(smem + L::kOffLse + st * 512);
-      const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512);
+      const long long i0 = (long long)(it_lo + x) * kTileM + c0;  // first query of this half
+      const float* lse_s = reinterpret_cast<const float*>(smem + L::kOffLse + st * 512) + c0;
+      const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512) + c0;
       // the stage's lse2 and D landed (TMA writes are visible to the threads
       // that observe this barrier), then S^T(x) is in TMEM
       ok = warp_wait(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30) &&
            warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 27);
       if (!ok) break;
       tc_fence_after();
-      float p[kTileM];
+      float p[64];
       {
-        uint32_t t[kTileM];
-        tmem_load128(tmem + lane_off + L::kTmS, t);
+        uint32_t t[64];
+        tmem_load64(tmem + lane_off + L::kTmS + c0, t);
 #pragma unroll
-        for (int e = 0; e < kTileM; ++e) p[e] = __uint_as_float(t[e]);
+        for (int e = 0; e < 64; ++e) p[e] = __uint_as_float(t[e]);
       }
-      const bool masked = !(i0 >= i_lo_k && i0 + kTileM - 1 <= i_hi_k);
-      // P^T = exp2(S^T scale log2(e) - lse2), 0 outside the mask; bf16 pairs
-      // over the first 64 columns, in two halves
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      const bool masked = !(i0 >= i_lo_k && i0 + 63 <= i_hi_k);
+      // P^T = exp2(S^T scale log2(e) - lse2), 0 outside the mask
+      {
         uint32_t pb[32];
 #pragma unroll
-        for (int e = h * 64; e < h * 64 + 64; e += 2) {
+        for (int e = 0; e < 64; e += 2) {
           float v0 = fast_exp2(fmaf(p[e], a.scale_log2, -lse_s[e]));
           float v1 = fast_exp2(fmaf(p[e + 1], a.scale_log2, -lse_s[e + 1]));
           if (masked) {
@@ -393,9 +434,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           p[e] = v0;
           p[e + 1] = v1;
-          pb[(e - h * 64) / 2] = pack_bf16(v0, v1);
+          pb[e / 2] = pack_bf16(v0, v1);
         }
-        tmem_store32(tmem + lane_off + L::kTmS + h * 32, pb);
+        tmem_store32(tmem + lane_off + L::kTmS + c0, pb);
       }
       tmem_store_wait();
       tc_fence_before();
@@ -405,9 +446,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kTileM / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t t[32];
-        tmem_load32(tmem + lane_off + L::kTmDP + c * 32, t);
+        tmem_load32(tmem + lane_off + L::kTmDP + c0 + c * 32, t);
         uint32_t sb[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -415,7 +456,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float s1 = p[c * 32 + e + 1] * (__uint_as_float(t[e + 1]) - d_s[c * 32 + e + 1]);
           sb[e / 2] = pack_bf16(s0, s1);
         }
-        tmem_store16(tmem + lane_off + L::kTmDP + c * 16, sb);
+        tmem_store16(tmem + lane_off + L::kTmDP + c0 + c * 16, sb);
       }
       tmem_store_wait();
       tc_fence_before();
@@ -427,7 +468,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {
       // ------------------------------------------------------ epilogue
-      // (tcgen05.ld is warp-collective: every lane loads, valid keys store)
+      // (tcgen05.ld is warp-collective: every lane loads, valid keys store;
+      // half h stores accumulator columns [h D/2, (h + 1) D/2))
       const bool have = n_it > 0 || a.accumulate;
       float* dst_v;
       float* dst_k;
@@ -444,11 +486,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float ks = a.last ? a.scale : 1.0f;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        float* dst = which == 0 ? dst_v : dst_k;
+        float* dst = (which == 0 ? dst_v : dst_k) + half * kHalfD;
         const float mul = which == 0 ? 1.0f : ks;
-        const uint32_t col = which == 0 ? L::kTmAcc1 : L::kTmAcc2;
+        const uint32_t col = (which == 0 ? L::kTmAcc1 : L::kTmAcc2) + half * kHalfD;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t t[32];
           if (have) tmem_load32(tmem + lane_off + col + c * 32, t);
           if (k_valid) {
@@ -516,13 +558,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   }
 
-  // query-row threads (warps 2..5): this row's statistics and incoming dQ~
+  // query-row threads (warps 2..9): lane quadrant warp % 4, column half
   const int quad = warp & 3;
+  const int half = warp >= 2 ? (warp - 2) >> 2 : 0;
+  constexpr int kHalfD = D / 2;  // dQ~ columns this thread loads and stores
   const long long i_row = i0 + quad * 32 + lane;
   const bool i_valid = i_row < a.n;
   const long long g_row = nat_row(a, bh, r, i_valid ? i_row : 0);
-  float* dq_row = a.dq + g_row * D;
-  uint32_t buf[D];
+  float* dq_row = a.dq + g_row * D + half * kHalfD;  // this thread's half of the row
+  uint32_t buf[kHalfD];
   float lse2_i = 0.0f, D_i = 0.0f;
   const bool rows = warp >= 2;
   if (rows) {
@@ -533,7 +577,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (a.accumulate && n_kt > 0) {
 #pragma unroll
-      for (int q8 = 0; q8 < D / 8; ++q8) {
+      for (int q8 = 0; q8 < kHalfD / 8; ++q8) {
         if (i_valid) {
           ld_global_v8(dq_row + q8 * 8, buf + q8 * 8);
         } else {
@@ -546,7 +590,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < L::kNumBars; ++x)
-      mbar_init(bar(x), (x == L::kBarP || x == L::kBarDS) ? 128 : 1);
+      mbar_init(bar(x), (x == L::kBarP || x == L::kBarDS) ? 256 : 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
@@ -619,8 +663,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = warp_wait(bar(L::kBarDS), x & 1, abort_flag, a, 36);
         if (!ok) break;
         tc_fence_after();
-        mma_pv(tmem + L::kTmAcc1, tmem + L::kTmDP, smem_desc(k_s(x), kTileN * 128, 1024), idesc_acc,
-               (x > 0 || a.accumulate) ? 1u : 0u);
+        mma_pv_split(tmem + L::kTmAcc1, tmem + L::kTmDP, smem_desc(k_s(x), kTileN * 128, 1024), idesc_acc,
+                     (x > 0 || a.accumulate) ? 1u : 0u);
         mma_commit_elect(bar(L::kBarEmpty + (x & 1)));
         if (more) {
           mma_qk<D>(tmem + L::kTmDP, do_desc, smem_desc(v_s(x + 1), 16, 1024), idesc_s);
@@ -633,10 +677,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------- query-row threads and epilogue
+    // Two warps per TMEM lane quadrant: half h owns key columns [64h, 64h+64)
+    // of S and dP and writes its bf16 dS into the first 32 columns of its own
+    // dP range (the dQ MMA reads the A operand with a jump at the middle).
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int c0 = half * 64;
     if (a.accumulate && n_kt > 0) {
-      if constexpr (D == 128) tmem_store128(tmem + lane_off + L::kTmAcc1, buf);
-      else tmem_store64(tmem + lane_off + L::kTmAcc1, buf);
+#pragma unroll
+      for (int c = 0; c < kHalfD / 32; ++c) {
+        uint32_t x32[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x32[e] = buf[c * 32 + e];
+        tmem_store32(tmem + lane_off + L::kTmAcc1 + half * kHalfD + c * 32, x32);
+      }
       tmem_store_wait();
     }
     // this row's allowed keys: k_lo_i <= k <= k_hi_i
@@ -644,22 +697,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const long long k_hi_i = i_valid ? min(rule.kmax, i_row + rule.dhi) : -1;
     bool ok = true;
     for (int x = 0; x < n_kt; ++x) {
-      const long long kbase = (long long)(kt_lo + x) * kTileN;
+      const long long kbase = (long long)(kt_lo + x) * kTileN + c0;  // first key of this half
       ok = warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 37);
       if (!ok) break;
       tc_fence_after();
-      float p[kTileN];
+      float p[64];
       {
-        uint32_t tt[kTileN];
-        tmem_load128(tmem + lane_off + L::kTmS, tt);
+        uint32_t tt[64];
+        tmem_load64(tmem + lane_off + L::kTmS + c0, tt);
 #pragma unroll
-        for (int e = 0; e < kTileN; ++e) p[e] = __uint_as_float(tt[e]);
+        for (int e = 0; e < 64; ++e) p[e] = __uint_as_float(tt[e]);
       }
       tc_fence_before();
       mbar_arrive(bar(L::kBarP));  // S(x) read: the S columns are free
-      const bool masked = !(kbase >= k_lo_i && kbase + kTileN - 1 <= k_hi_i);
+      const bool masked = !(kbase >= k_lo_i && kbase + 63 <= k_hi_i);
 #pragma unroll
-      for (int e = 0; e < kTileN; ++e) {
+      for (int e = 0; e < 64; ++e) {
         float v = fast_exp2(fmaf(p[e], a.scale_log2, -lse2_i));
         if (masked && (kbase + e < k_lo_i || kbase + e > k_hi_i)) v = 0.0f;
         p[e] = v;
@@ -669,9 +722,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       // dS = P (dP - D), 32 columns at a time, bf16 over the read dP columns
 #pragma unroll
-      for (int c = 0; c < kTileN / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t tt[32];
-        tmem_load32(tmem + lane_off + L::kTmDP + c * 32, tt);
+        tmem_load32(tmem + lane_off + L::kTmDP + c0 + c * 32, tt);
         uint32_t sb[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -679,7 +732,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float s1 = p[c * 32 + e + 1] * (__uint_as_float(tt[e + 1]) - D_i);
           sb[e / 2] = pack_bf16(s0, s1);
         }
-        tmem_store16(tmem + lane_off + L::kTmDP + c * 16, sb);
+        tmem_store16(tmem + lane_off + L::kTmDP + c0 + c * 16, sb);
       }
       tmem_store_wait();
       tc_fence_before();
@@ -691,13 +744,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {
       // ------------------------------------------------------ epilogue
-      // (tcgen05.ld is warp-collective: every lane loads, valid rows store)
+      // (tcgen05.ld is warp-collective: every lane loads, valid rows store;
+      // half h stores dQ columns [h D/2, (h + 1) D/2))
       const float mul = a.last ? a.scale : 1.0f;
       if (n_kt > 0) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t tt[32];
-          tmem_load32(tmem + lane_off + L::kTmAcc1 + c * 32, tt);
+          tmem_load32(tmem + lane_off + L::kTmAcc1 + half * kHalfD + c * 32, tt);
           if (i_valid) {
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8) {
@@ -712,7 +766,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // no key of this block for the tile: dQ~ stays as it is (zero at
         // step 0), scaled at the last step
 #pragma unroll
-        for (int q8 = 0; q8 < D / 8; ++q8) {
+        for (int q8 = 0; q8 < kHalfD / 8; ++q8) {
           uint32_t x8[8];
           float v[8];
           if (a.accumulate) {
