@@ -590,7 +590,7 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
 }
 
 // ---------------------------------------------------------------- backward
-// Workspace of ring_attn_bwd: lse2 and D shard-major [BH][P][n_pad] fp32,
+// Workspace of ring_attn_bwd: -lse*log2(e) and -D shard-major [BH][P][n_pad] fp32,
 // then the dK~ and dV~ accumulator buffers X and Y, [P][BH][n][d] fp32 each.
 struct BwdWorkspace {
   size_t lse_off, d_off, acc_bytes, acc_off, total;
@@ -634,8 +634,8 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const BwdWorkspace w = bwd_workspace(p);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* lse2 = reinterpret_cast<float*>(ws + w.lse_off);
-  float* Dv = reinterpret_cast<float*>(ws + w.d_off);
+  float* nlse2 = reinterpret_cast<float*>(ws + w.lse_off);
+  float* nD = reinterpret_cast<float*>(ws + w.d_off);
   float* acc_k[2] = {reinterpret_cast<float*>(ws + w.acc_off), reinterpret_cast<float*>(ws + w.acc_off + 2 * w.acc_bytes)};
   float* acc_v[2] = {reinterpret_cast<float*>(ws + w.acc_off + w.acc_bytes),
                      reinterpret_cast<float*>(ws + w.acc_off + 3 * w.acc_bytes)};
@@ -659,13 +659,13 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   const long long row_r = striped ? 1 : p.n, row_i = striped ? P : 1;
   const bool timing = h->timing != 0;
   if (timing) RA_CUDA(cudaEventRecord(h->tbp0, cs), "cudaEventRecord");
-  RA_CUDA((cudaError_t)launch_bwd_prep(out, lse, dout, lse2, Dv, BH, p.n, w.n_pad, p.d, P, row_r, row_i, p.N, cs),
+  RA_CUDA((cudaError_t)launch_bwd_prep(out, lse, dout, nlse2, nD, BH, p.n, w.n_pad, p.d, P, row_r, row_i, p.N, cs),
           "backward prep launch");
   if (timing) RA_CUDA(cudaEventRecord(h->tbp1, cs), "cudaEventRecord");
   BwdArgs a;
   std::memset(&a, 0, sizeof a);
-  a.lse2 = lse2;
-  a.Dv = Dv;
+  a.nlse2 = nlse2;
+  a.nD = nD;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;

@@ -58,7 +58,7 @@ constexpr int kBwdTmemCols = 512;
 constexpr long long kFar = 1LL << 40;  // "no bound" for the diagonal offsets
 
 // Shared memory of both kernels: two stationary tiles (K, V or Q, dO), two
-// stages of two streamed tiles, two stages of 128 lse2 and D values (dK/dV
+// stages of two streamed tiles, two stages of 128 nlse2 and nD values (dK/dV
 // kernel only), the barriers.  Every tile starts on a 1024-byte boundary.
 template <int D>
 struct BwdLayout {
@@ -173,12 +173,14 @@ __device__ __forceinline__ void load_rows(const BwdArgs& a, uint32_t dst, const 
 }
 
 // ------------------------------------------------------------ preprocessing
-// lse2 = lse * log2(e) and D = dO . out for every query row, written
-// shard-major [BH][P][n_pad] (rows n..n_pad-1 of a shard get 0).  Eight
+// nlse2 = -lse * log2(e) and nD = -(dO . out) for every query row, written
+// shard-major [BH][P][n_pad] (rows n..n_pad-1 of a shard get 0); negated so
+// that P = exp2(S scale log2(e) + nlse2) and dP - D = dP + nD take one packed
+// FMA or add per column pair in the step kernels.  Eight
 // threads per row, 16 columns each (d = 128) or 8 (d = 64).
 __global__ void bwd_prep_kernel(const float* __restrict__ out, const float* __restrict__ lse,
-                                const __nv_bfloat16* __restrict__ dout, float* __restrict__ lse2,
-                                float* __restrict__ Dv, int BH, long long n, int n_pad, int d, int P,
+                                const __nv_bfloat16* __restrict__ dout, float* __restrict__ nlse2,
+                                float* __restrict__ nD, int BH, long long n, int n_pad, int d, int P,
                                 long long row_r, long long row_i, long long N) {
   const long long rows = (long long)BH * P * n_pad;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -212,8 +214,8 @@ __global__ void bwd_prep_kernel(const float* __restrict__ out, const float* __re
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
   if (part == 0) {
-    Dv[row] = i < n ? acc : 0.0f;
-    lse2[row] = l2;
+    nD[row] = i < n ? -acc : 0.0f;
+    nlse2[row] = -l2;
   }
 }
 
@@ -296,8 +298,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0 && n_it > 0) {
-      const float* lse_base = a.lse2 + ((size_t)bh * a.P + r) * a.n_pad;
-      const float* d_base = a.Dv + ((size_t)bh * a.P + r) * a.n_pad;
+      const float* lse_base = a.nlse2 + ((size_t)bh * a.P + r) * a.n_pad;
+      const float* d_base = a.nD + ((size_t)bh * a.P + r) * a.n_pad;
       int issued = 0;
       bool ok = true;
       for (int x = 0; x < n_it && ok; ++x) {
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const long long i0 = (long long)(it_lo + x) * kTileM + c0;  // first query of this half
       const float* lse_s = reinterpret_cast<const float*>(smem + L::kOffLse + st * 512) + c0;
       const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512) + c0;
-      // the stage's lse2 and D landed (TMA writes are visible to the threads
+      // the stage's nlse2 and D landed (TMA writes are visible to the threads
       // that observe this barrier), then S^T(x) is in TMEM
       ok = warp_wait(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30) &&
            warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 27);
@@ -420,22 +422,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int e = 0; e < 64; ++e) p[e] = __uint_as_float(t[e]);
       }
       const bool masked = !(i0 >= i_lo_k && i0 + 63 <= i_hi_k);
-      // P^T = exp2(S^T scale log2(e) - lse2), 0 outside the mask
+      // P^T = exp2(S^T scale log2(e) + nlse2): one packed FMA and two MUFU
+      // ex2 per column pair; bf16 pairs over the first 32 columns of the half
       {
+        const float4* nl4 = reinterpret_cast<const float4*>(lse_s);
+        const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
         uint32_t pb[32];
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          float v0 = fast_exp2(fmaf(p[e], a.scale_log2, -lse_s[e]));
-          float v1 = fast_exp2(fmaf(p[e + 1], a.scale_log2, -lse_s[e + 1]));
-          if (masked) {
-            const long long i = i0 + e;
-            if (i < i_lo_k || i > i_hi_k) v0 = 0.0f;
-            if (i + 1 < i_lo_k || i + 1 > i_hi_k) v1 = 0.0f;
-          }
-          p[e] = v0;
-          p[e + 1] = v1;
-          pb[e / 2] = pack_bf16(v0, v1);
+        for (int e4 = 0; e4 < 16; ++e4) {
+          const float4 nl = nl4[e4];
+          float v0, v1, v2, v3;
+          unf2(ffma2(f2(p[4 * e4], p[4 * e4 + 1]), sc2, f2(nl.x, nl.y)), v0, v1);
+          unf2(ffma2(f2(p[4 * e4 + 2], p[4 * e4 + 3]), sc2, f2(nl.z, nl.w)), v2, v3);
+          p[4 * e4] = fast_exp2(v0);
+          p[4 * e4 + 1] = fast_exp2(v1);
+          p[4 * e4 + 2] = fast_exp2(v2);
+          p[4 * e4 + 3] = fast_exp2(v3);
         }
+        if (masked) {
+          // queries of this half outside [i_lo_k, i_hi_k] get 0 (relative
+          // bounds clamped to [-1, 64] fit in 32 bits)
+          const int lo = (int)max(-1LL, min(64LL, i_lo_k - i0));
+          const int hi = (int)max(-1LL, min(64LL, i_hi_k - i0));
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e < lo || e > hi) p[e] = 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) pb[e / 2] = pack_bf16(p[e], p[e + 1]);
         tmem_store32(tmem + lane_off + L::kTmS + c0, pb);
       }
       tmem_store_wait();
@@ -445,16 +459,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 28);
       if (!ok) break;
       tc_fence_after();
+      const float4* nd4 = reinterpret_cast<const float4*>(d_s);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t t[32];
         tmem_load32(tmem + lane_off + L::kTmDP + c0 + c * 32, t);
         uint32_t sb[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float s0 = p[c * 32 + e] * (__uint_as_float(t[e]) - d_s[c * 32 + e]);
-          const float s1 = p[c * 32 + e + 1] * (__uint_as_float(t[e + 1]) - d_s[c * 32 + e + 1]);
-          sb[e / 2] = pack_bf16(s0, s1);
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 nd = nd4[c * 8 + e4];
+          const int e = c * 32 + e4 * 4;
+          float s0, s1, s2, s3;
+          unf2(fmul2(f2(p[e], p[e + 1]),
+                     fadd2(f2(__uint_as_float(t[e4 * 4]), __uint_as_float(t[e4 * 4 + 1])), f2(nd.x, nd.y))),
+               s0, s1);
+          unf2(fmul2(f2(p[e + 2], p[e + 3]),
+                     fadd2(f2(__uint_as_float(t[e4 * 4 + 2]), __uint_as_float(t[e4 * 4 + 3])), f2(nd.z, nd.w))),
+               s2, s3);
+          sb[e4 * 2] = pack_bf16(s0, s1);
+          sb[e4 * 2 + 1] = pack_bf16(s2, s3);
         }
         tmem_store16(tmem + lane_off + L::kTmDP + c0 + c * 16, sb);
       }
@@ -567,13 +590,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const long long g_row = nat_row(a, bh, r, i_valid ? i_row : 0);
   float* dq_row = a.dq + g_row * D + half * kHalfD;  // this thread's half of the row
   uint32_t buf[kHalfD];
-  float lse2_i = 0.0f, D_i = 0.0f;
+  float nlse2_i = 0.0f, nD_i = 0.0f;
   const bool rows = warp >= 2;
   if (rows) {
     const size_t v = ((size_t)bh * a.P + r) * a.n_pad + (size_t)i_row;
     if (i_valid && n_kt > 0) {
-      lse2_i = a.lse2[v];
-      D_i = a.Dv[v];
+      nlse2_i = a.nlse2[v];
+      nD_i = a.nD[v];
     }
     if (a.accumulate && n_kt > 0) {
 #pragma unroll
@@ -711,16 +734,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(L::kBarP));  // S(x) read: the S columns are free
       const bool masked = !(kbase >= k_lo_i && kbase + 63 <= k_hi_i);
+      // P = exp2(S scale log2(e) + nlse2): one packed FMA, two MUFU ex2 per pair
+      {
+        const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
+        const uint64_t nl2 = f2(nlse2_i, nlse2_i);
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        float v = fast_exp2(fmaf(p[e], a.scale_log2, -lse2_i));
-        if (masked && (kbase + e < k_lo_i || kbase + e > k_hi_i)) v = 0.0f;
-        p[e] = v;
+        for (int e = 0; e < 64; e += 2) {
+          float v0, v1;
+          unf2(ffma2(f2(p[e], p[e + 1]), sc2, nl2), v0, v1);
+          p[e] = fast_exp2(v0);
+          p[e + 1] = fast_exp2(v1);
+        }
+        if (masked) {
+          // keys of this half outside [k_lo_i, k_hi_i] get 0 (relative
+          // bounds clamped to [-1, 64] fit in 32 bits)
+          const int lo = (int)max(-1LL, min(64LL, k_lo_i - kbase));
+          const int hi = (int)max(-1LL, min(64LL, k_hi_i - kbase));
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e < lo || e > hi) p[e] = 0.0f;
+        }
       }
       ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 38);
       if (!ok) break;
       tc_fence_after();
       // dS = P (dP - D), 32 columns at a time, bf16 over the read dP columns
+      const uint64_t nd2 = f2(nD_i, nD_i);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t tt[32];
@@ -728,8 +767,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t sb[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float s0 = p[c * 32 + e] * (__uint_as_float(tt[e]) - D_i);
-          const float s1 = p[c * 32 + e + 1] * (__uint_as_float(tt[e + 1]) - D_i);
+          float s0, s1;
+          unf2(fmul2(f2(p[c * 32 + e], p[c * 32 + e + 1]),
+                     fadd2(f2(__uint_as_float(tt[e]), __uint_as_float(tt[e + 1])), nd2)),
+               s0, s1);
           sb[e / 2] = pack_bf16(s0, s1);
         }
         tmem_store16(tmem + lane_off + L::kTmDP + c0 + c * 16, sb);
@@ -817,7 +858,7 @@ int prepare_backward_kernels() {
   return prepare_bwd_one<128>();
 }
 
-int launch_bwd_prep(const float* out, const float* lse, const void* dout, float* lse2, float* Dv, int BH,
+int launch_bwd_prep(const float* out, const float* lse, const void* dout, float* nlse2, float* nD, int BH,
                     long long n, int n_pad, int d, int P, long long row_r, long long row_i, long long N,
                     void* stream) {
   const long long threads = (long long)BH * P * n_pad * 8;
@@ -825,7 +866,7 @@ int launch_bwd_prep(const float* out, const float* lse, const void* dout, float*
   const long long grid = (threads + block - 1) / block;
   if (grid <= 0) return 0;
   bwd_prep_kernel<<<(unsigned)grid, block, 0, static_cast<cudaStream_t>(stream)>>>(
-      out, lse, static_cast<const __nv_bfloat16*>(dout), lse2, Dv, BH, n, n_pad, d, P, row_r, row_i, N);
+      out, lse, static_cast<const __nv_bfloat16*>(dout), nlse2, nD, BH, n, n_pad, d, P, row_r, row_i, N);
   return (int)cudaGetLastError();
 }
 

@@ -112,8 +112,8 @@ struct StepArgs {
 // Natural-order tensors are [BH][N][d]; the row of (shard r, local i) within
 // a head is r * row_r + i * row_i.  Shard-major vectors are [BH][P][n_pad].
 struct BwdArgs {
-  const float* lse2;  // lse * log2(e) of every query row, shard-major
-  const float* Dv;    // D = rowsum(dO * out) of every query row, shard-major
+  const float* nlse2;  // -lse * log2(e) of every query row, shard-major
+  const float* nD;     // -D = -rowsum(dO * out) of every query row, shard-major
   float* dq;          // natural: the running dQ (unscaled) between steps, scale * dQ after the last
   const float* acc_in_k;  // [P][BH][n][d]: the dK~ and dV~ accumulators held by shard r (slot r)
   const float* acc_in_v;
@@ -169,7 +169,7 @@ int block_partial_grid(int T, int n_active, int BH);
 int prepare_block_partial_kernels();
 // Backward (block_backward.cu).  The maps are shard views of natural-order
 // bf16 tensors (box 64 x 128 rows), coordinates as for kQContiguous/kQStriped.
-int launch_bwd_prep(const float* out, const float* lse, const void* dout, float* lse2, float* Dv, int BH,
+int launch_bwd_prep(const float* out, const float* lse, const void* dout, float* nlse2, float* nD, int BH,
                     long long n, int n_pad, int d, int P, long long row_r, long long row_i, long long N,
                     void* stream);
 int launch_bwd_dkdv(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
