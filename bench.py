@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 METRIC = "causal-adjusted attention TFLOP/s and % of GB300 bf16 peak; tokens/s (1 GPU)"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCE = os.path.join(ROOT, "ring_sequence_parallelism_gb300", "csrc", "block_partial.cu")
+BWD_SOURCE = os.path.join(ROOT, "ring_sequence_parallelism_gb300", "csrc", "block_backward.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -91,21 +92,21 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_hash():
-    with open(KERNEL_SOURCE, "rb") as f:
+def source_hash(path=KERNEL_SOURCE):
+    with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def traffic_for(workload: str):
-    """ncu DRAM bytes per launch of the step kernel, if taken on this exact
-    kernel source (else None)."""
+def traffic_for(key: str, source=KERNEL_SOURCE):
+    """ncu DRAM bytes per launch of a kernel (entry `key` of the traffic
+    record), if taken on this exact kernel source (else None)."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    e = t.get(workload)
-    if not e or e.get("kernel_sha256_16") != source_hash():
+    e = t.get(key)
+    if not e or e.get("kernel_sha256_16") != source_hash(source):
         return None
     return e.get("bytes_per_launch")
 
@@ -485,7 +486,8 @@ def run_bwd(args, w):
         "tokens_per_s": w.B * w.N / (ms * 1e-3),
         "roofline": {"bound": "tensor", "kernel": "bwd_dkdv_kernel<128> (one launch per ring step)",
                      "achieved": ach_dkdv, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach_dkdv / peak_sus,
-                     "peak_kind": f"bf16_tflops_sustained ({pk_kind})", "traffic": None,
+                     "peak_kind": f"bf16_tflops_sustained ({pk_kind})",
+                     "traffic": traffic_for(f"{w.name}:bwd_dkdv", BWD_SOURCE),
                      "algorithmic": "8*d FLOPs per allowed pair (S^T, dP^T, dV, dK)"},
         "dq_kernel": {"achieved": ach_dq, "frac": ach_dq / peak_sus,
                       "algorithmic": "6*d FLOPs per allowed pair (S, dP, dQ)"},
