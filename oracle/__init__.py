@@ -48,6 +48,16 @@ def build(source: str = SOURCE, output: str = LIBRARY, force: bool = False) -> s
     return output
 
 
+def _segment_ids(segments, N: int):
+    """Document boundaries [0, b1, .., N] (sequence packing) -> the document
+    of every position as int64 [N]; None -> None (one document)."""
+    if segments is None:
+        return None
+    b = np.asarray(segments, dtype=np.int64)
+    assert b.ndim == 1 and b.size >= 2 and b[0] == 0 and b[-1] == N and np.all(np.diff(b) > 0), "bad boundaries"
+    return np.ascontiguousarray(np.repeat(np.arange(b.size - 1, dtype=np.int64), np.diff(b)))
+
+
 def bf16_bits(t) -> np.ndarray:
     """torch bf16 tensor (any device) or uint16 array -> contiguous uint16 numpy."""
     if isinstance(t, np.ndarray):
@@ -89,11 +99,11 @@ class Oracle:
         L.oracle_owner.restype = None
         L.oracle_block_at.argtypes = [_I, _I, _I]
         L.oracle_block_at.restype = _I
-        L.oracle_dense_rows.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _L, _P, _P, _P, _I]
+        L.oracle_dense_rows.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _L, _P, _P, _P, _I]
         L.oracle_dense_rows.restype = _I
-        L.oracle_ring_rows.argtypes = [_I, _L, _I, _I, _I, _L, _I, _P, _P, _P, _L, _P, _P, _P, _P, _I]
+        L.oracle_ring_rows.argtypes = [_I, _L, _I, _I, _I, _L, _P, _I, _P, _P, _P, _L, _P, _P, _P, _P, _I]
         L.oracle_ring_rows.restype = _I
-        L.oracle_block_partial.argtypes = [_I, _L, _I, _I, _I, _L, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I]
+        L.oracle_block_partial.argtypes = [_I, _L, _I, _I, _I, _L, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I]
         L.oracle_block_partial.restype = _I
         L.oracle_merge_states.argtypes = [_L, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]
         L.oracle_merge_states.restype = _I
@@ -101,13 +111,13 @@ class Oracle:
         L.oracle_merge_inplace.restype = _I
         L.oracle_finalize.argtypes = [_L, _I, _P, _P, _P, _P, _P]
         L.oracle_finalize.restype = _I
-        L.oracle_naive_block_sum.argtypes = [_I, _L, _I, _I, _I, _L, _I, _P, _P, _P, _P]
+        L.oracle_naive_block_sum.argtypes = [_I, _L, _I, _I, _I, _L, _P, _I, _P, _P, _P, _P]
         L.oracle_naive_block_sum.restype = _I
-        L.oracle_dense_bwd.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _I]
+        L.oracle_dense_bwd.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _P, _I]
         L.oracle_dense_bwd.restype = _I
-        L.oracle_dense_bwd_rows.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _L, _P, _L, _P, _P, _P, _P, _I]
+        L.oracle_dense_bwd_rows.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _P, _L, _P, _L, _P, _P, _P, _P, _I]
         L.oracle_dense_bwd_rows.restype = _I
-        L.oracle_ring_bwd.argtypes = [_I, _L, _I, _I, _I, _L, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I]
+        L.oracle_ring_bwd.argtypes = [_I, _L, _I, _I, _I, _L, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I]
         L.oracle_ring_bwd.restype = _I
 
     # -- small helpers -------------------------------------------------
@@ -141,39 +151,42 @@ class Oracle:
         return r, r.size
 
     # -- the method ------------------------------------------------------
-    def dense(self, q, k, v, causal: bool, rows=None, window: int = 0):
+    def dense(self, q, k, v, causal: bool, rows=None, window: int = 0, segments=None):
         q, k, v = self._qkv(q, k, v)
         BH, N, d = q.shape
         r, R = self._rows(rows, N)
         out = np.empty((BH, R, d), np.float64)
         lse = np.empty((BH, R), np.float64)
-        rc = self.lib.oracle_dense_rows(BH, N, d, int(causal), int(window), _ptr(q), _ptr(k), _ptr(v), R, _ptr(r),
+        seg = _segment_ids(segments, N)
+        rc = self.lib.oracle_dense_rows(BH, N, d, int(causal), int(window), _ptr(seg), _ptr(q), _ptr(k), _ptr(v), R, _ptr(r),
                                         _ptr(out), _ptr(lse), self.nthreads)
         if rc != 0:
             raise RuntimeError(f"oracle_dense_rows failed: {rc}")
         return out, lse
 
-    def ring(self, q, k, v, P: int, causal: bool, layout: int, rows=None, visits: bool = False, window: int = 0):
+    def ring(self, q, k, v, P: int, causal: bool, layout: int, rows=None, visits: bool = False, window: int = 0, segments=None):
         q, k, v = self._qkv(q, k, v)
         BH, N, d = q.shape
         r, R = self._rows(rows, N)
         out = np.empty((BH, R, d), np.float64)
         lse = np.empty((BH, R), np.float64)
         cnt = np.zeros((BH, N, N), np.int64) if visits else None
-        rc = self.lib.oracle_ring_rows(BH, N, d, P, int(causal), int(window), layout, _ptr(q), _ptr(k), _ptr(v), R,
+        seg = _segment_ids(segments, N)
+        rc = self.lib.oracle_ring_rows(BH, N, d, P, int(causal), int(window), _ptr(seg), layout, _ptr(q), _ptr(k), _ptr(v), R,
                                        _ptr(r), _ptr(out), _ptr(lse), _ptr(cnt), self.nthreads)
         if rc != 0:
             raise RuntimeError(f"oracle_ring_rows failed: {rc}")
         return (out, lse, cnt) if visits else (out, lse)
 
     def block_partial(self, q_shard, k_block, v_block, P: int, causal: bool, layout: int, r: int, j: int,
-                      window: int = 0):
+                      window: int = 0, segments=None):
         q, k, v = self._qkv(q_shard, k_block, v_block)
         BH, n, d = q.shape
         m = np.empty((BH, n), np.float64)
         l = np.empty((BH, n), np.float64)
         o = np.empty((BH, n, d), np.float64)
-        rc = self.lib.oracle_block_partial(BH, n, d, P, int(causal), int(window), layout, r, j, _ptr(q), _ptr(k), _ptr(v),
+        seg = _segment_ids(segments, n * P)
+        rc = self.lib.oracle_block_partial(BH, n, d, P, int(causal), int(window), _ptr(seg), layout, r, j, _ptr(q), _ptr(k), _ptr(v),
                                            _ptr(m), _ptr(l), _ptr(o), self.nthreads)
         if rc != 0:
             raise RuntimeError(f"oracle_block_partial failed: {rc}")
@@ -219,31 +232,33 @@ class Oracle:
             raise RuntimeError(f"oracle_finalize failed: {rc}")
         return out, lse
 
-    def naive_block_sum(self, q, k, v, P: int, causal: bool, layout: int, window: int = 0):
+    def naive_block_sum(self, q, k, v, P: int, causal: bool, layout: int, window: int = 0, segments=None):
         q, k, v = self._qkv(q, k, v)
         BH, N, d = q.shape
         out = np.empty((BH, N, d), np.float64)
-        rc = self.lib.oracle_naive_block_sum(BH, N, d, P, int(causal), int(window), layout, _ptr(q), _ptr(k), _ptr(v),
+        seg = _segment_ids(segments, N)
+        rc = self.lib.oracle_naive_block_sum(BH, N, d, P, int(causal), int(window), _ptr(seg), layout, _ptr(q), _ptr(k), _ptr(v),
                                              _ptr(out))
         if rc != 0:
             raise RuntimeError(f"oracle_naive_block_sum failed: {rc}")
         return out
 
     # -- the backward ------------------------------------------------------
-    def dense_bwd(self, q, k, v, dout, causal: bool, window: int = 0):
+    def dense_bwd(self, q, k, v, dout, causal: bool, window: int = 0, segments=None):
         """dq, dk, dv (float64, [BH][N][d]) by the plain definition."""
         q, k, v = self._qkv(q, k, v)
         do = bf16_bits(dout)
         assert do.shape == q.shape
         BH, N, d = q.shape
         dq, dk, dv = (np.empty((BH, N, d), np.float64) for _ in range(3))
-        rc = self.lib.oracle_dense_bwd(BH, N, d, int(causal), int(window), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
+        seg = _segment_ids(segments, N)
+        rc = self.lib.oracle_dense_bwd(BH, N, d, int(causal), int(window), _ptr(seg), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
                                        _ptr(dq), _ptr(dk), _ptr(dv), self.nthreads)
         if rc != 0:
             raise RuntimeError(f"oracle_dense_bwd failed: {rc}")
         return dq, dk, dv
 
-    def dense_bwd_rows(self, q, k, v, dout, causal: bool, qrows, krows, window: int = 0):
+    def dense_bwd_rows(self, q, k, v, dout, causal: bool, qrows, krows, window: int = 0, segments=None):
         """dq at query positions qrows ([BH][len(qrows)][d]) and dk, dv at key
         positions krows ([BH][len(krows)][d])."""
         q, k, v = self._qkv(q, k, v)
@@ -254,14 +269,15 @@ class Oracle:
         dq = np.empty((BH, nq, d), np.float64)
         dk = np.empty((BH, nk, d), np.float64)
         dv = np.empty((BH, nk, d), np.float64)
-        rc = self.lib.oracle_dense_bwd_rows(BH, N, d, int(causal), int(window), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
+        seg = _segment_ids(segments, N)
+        rc = self.lib.oracle_dense_bwd_rows(BH, N, d, int(causal), int(window), _ptr(seg), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
                                             nq, _ptr(qr), nk, _ptr(kr), _ptr(dq), _ptr(dk), _ptr(dv), self.nthreads)
         if rc != 0:
             raise RuntimeError(f"oracle_dense_bwd_rows failed: {rc}")
         return dq, dk, dv
 
     def ring_bwd(self, q, k, v, dout, out, lse, P: int, causal: bool, layout: int, visits: bool = False,
-                 window: int = 0):
+                 window: int = 0, segments=None):
         """The ring backward simulation from the forward's out and lse
         (float64, natural order).  Returns dq, dk, dv (and the visit counts)."""
         q, k, v = self._qkv(q, k, v)
@@ -271,7 +287,8 @@ class Oracle:
         lse = np.ascontiguousarray(lse, np.float64).reshape(BH, N)
         dq, dk, dv = (np.empty((BH, N, d), np.float64) for _ in range(3))
         cnt = np.zeros((BH, N, N), np.int64) if visits else None
-        rc = self.lib.oracle_ring_bwd(BH, N, d, P, int(causal), int(window), layout, _ptr(q), _ptr(k), _ptr(v),
+        seg = _segment_ids(segments, N)
+        rc = self.lib.oracle_ring_bwd(BH, N, d, P, int(causal), int(window), _ptr(seg), layout, _ptr(q), _ptr(k), _ptr(v),
                                       _ptr(do), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cnt),
                                       self.nthreads)
         if rc != 0:

@@ -37,6 +37,12 @@
  *     tokens before it ([RA-CN] "正确性测试应覆盖哪些边界" lists
  *     sliding-window masks among the cases to cover; the window is the
  *     usual causal local-attention window).
+ *   - segments (sequence packing, [RA-CN] "正确性测试应覆盖哪些边界": several
+ *     documents packed into one sequence must not attend to each other):
+ *     seg[t] is the document of position t (NULL: one document); a pair is
+ *     allowed only inside one document, on top of the causal rule and the
+ *     window.  A valid-length mask (padding at the tail) is the case where
+ *     the padding forms a document of its own.
  *
  * All inputs Q, K, V are bf16 bit patterns (uint16) in natural token order,
  * laid out [BH][N][d]; they are widened exactly to double.
@@ -120,7 +126,8 @@ int oracle_block_at(int P, int r, int s) {
   return j;
 }
 
-static int allowed(int causal, long window, long pos_q, long pos_k) {
+static int allowed(int causal, long window, const long* seg, long pos_q, long pos_k) {
+  if (seg && seg[pos_q] != seg[pos_k]) return 0;
   if (window > 0 && pos_q - pos_k >= window) return 0;
   return !causal || pos_k <= pos_q;
 }
@@ -139,7 +146,7 @@ static double dot_q_k(const uint16_t* q, const uint16_t* k, int d) {
  * rows == NULL means every position 0..N-1 (nrows must equal N then).
  * out is [BH][nrows][d], lse is [BH][nrows].
  */
-int oracle_dense_rows(int BH, long N, int d, int causal, long window, const uint16_t* q,
+int oracle_dense_rows(int BH, long N, int d, int causal, long window, const long* seg, const uint16_t* q,
                       const uint16_t* k, const uint16_t* v, long nrows,
                       const long* rows, double* out, double* lse,
                       int nthreads) {
@@ -165,18 +172,18 @@ int oracle_dense_rows(int BH, long N, int d, int causal, long window, const uint
       const uint16_t* vb = v + (size_t)bh * N * d;
       double m = -INFINITY;
       for (long kk = 0; kk < N; ++kk) {
-        if (!allowed(causal, window, t, kk)) continue;
+        if (!allowed(causal, window, seg, t, kk)) continue;
         s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
         if (s[kk] > m) m = s[kk];
       }
       double sum = 0.0;
       for (long kk = 0; kk < N; ++kk)
-        if (allowed(causal, window, t, kk)) sum += exp(s[kk] - m);
+        if (allowed(causal, window, seg, t, kk)) sum += exp(s[kk] - m);
       double l = m + log(sum);
       double* o = out + (size_t)idx * d;
       for (int c = 0; c < d; ++c) o[c] = 0.0;
       for (long kk = 0; kk < N; ++kk) {
-        if (!allowed(causal, window, t, kk)) continue;
+        if (!allowed(causal, window, seg, t, kk)) continue;
         double w = exp(s[kk] - l);
         const uint16_t* vr = vb + (size_t)kk * d;
         for (int c = 0; c < d; ++c) o[c] += w * widen_bf16(vr[c]);
@@ -199,11 +206,11 @@ int oracle_dense_rows(int BH, long N, int d, int causal, long window, const uint
  */
 static void row_block_state(const uint16_t* qrow, long pos_q, const uint16_t* kb,
                             const uint16_t* vb, const long* kpos, long nk, int d,
-                            int causal, long window, double scale, double* s, double* m_out,
+                            int causal, long window, const long* seg, double scale, double* s, double* m_out,
                             double* l_out, double* o_out, long* visit_row) {
   double m = -INFINITY;
   for (long kk = 0; kk < nk; ++kk) {
-    if (!allowed(causal, window, pos_q, kpos[kk])) continue;
+    if (!allowed(causal, window, seg, pos_q, kpos[kk])) continue;
     s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
     if (s[kk] > m) m = s[kk];
   }
@@ -211,7 +218,7 @@ static void row_block_state(const uint16_t* qrow, long pos_q, const uint16_t* kb
   for (int c = 0; c < d; ++c) o_out[c] = 0.0;
   if (m != -INFINITY) {
     for (long kk = 0; kk < nk; ++kk) {
-      if (!allowed(causal, window, pos_q, kpos[kk])) continue;
+      if (!allowed(causal, window, seg, pos_q, kpos[kk])) continue;
       double w = exp(s[kk] - m);
       l += w;
       const uint16_t* vr = vb + (size_t)kk * d;
@@ -254,7 +261,7 @@ static void merge_pair(double ma, double la, const double* oa, double mb,
  * indexed like oracle_dense_rows.  visits (NULL or [BH][N][N] counters)
  * receives +1 for every (query, key) pair the simulation used.
  */
-int oracle_ring_rows(int BH, long N, int d, int P, int causal, long window, int layout,
+int oracle_ring_rows(int BH, long N, int d, int P, int causal, long window, const long* seg, int layout,
                      const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      long nrows, const long* rows, double* out, double* lse,
                      long* visits, int nthreads) {
@@ -305,7 +312,7 @@ int oracle_ring_rows(int BH, long N, int d, int P, int causal, long window, int 
                  sizeof(uint16_t) * d);
         }
         double mb, lb;
-        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, window, scale, s, &mb,
+        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, window, seg, scale, s, &mb,
                         &lb, ob, visit_row);
         double mn, ln;
         merge_pair(m, l, ost, mb, lb, ob, d, &mn, &ln, otmp);
@@ -335,7 +342,7 @@ int oracle_ring_rows(int BH, long N, int d, int P, int causal, long window, int 
  * q_shard, k_block, v_block are shard-major [BH][n][d] bf16 bit patterns.
  * Outputs m, l [BH][n] and o [BH][n][d] as defined in row_block_state.
  */
-int oracle_block_partial(int BH, long n, int d, int P, int causal, long window, int layout,
+int oracle_block_partial(int BH, long n, int d, int P, int causal, long window, const long* seg, int layout,
                          int r, int j, const uint16_t* q_shard,
                          const uint16_t* k_block, const uint16_t* v_block,
                          double* m, double* l, double* o, int nthreads) {
@@ -365,7 +372,7 @@ int oracle_block_partial(int BH, long n, int d, int P, int causal, long window, 
       row_block_state(q_shard + (size_t)idx * d,
                       oracle_position(layout, n, P, r, i),
                       k_block + (size_t)bh * n * d, v_block + (size_t)bh * n * d,
-                      kpos, n, d, causal, window, scale, s, &m[idx], &l[idx],
+                      kpos, n, d, causal, window, seg, scale, s, &m[idx], &l[idx],
                       o + (size_t)idx * d, NULL);
     }
     free(s);
@@ -446,7 +453,7 @@ int oracle_finalize(long rows, int d, const double* m, const double* l,
  *   out_naive = sum over blocks j with an allowed key of softmax(S^(j)) V_j.
  * Natural order in and out, out is [BH][N][d].
  */
-int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, long window, int layout,
+int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, long window, const long* seg, int layout,
                            const uint16_t* q, const uint16_t* k,
                            const uint16_t* v, double* out) {
   if (BH <= 0 || N <= 0 || d <= 0 || !layout_ok(layout, N, P)) return -1;
@@ -476,7 +483,7 @@ int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, long window
                  sizeof(uint16_t) * d);
         }
         double mb, lb;
-        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, window, scale, s, &mb,
+        row_block_state(qrow, t, kblk, vblk, kpos, n, d, causal, window, seg, scale, s, &mb,
                         &lb, ob, NULL);
         if (lb > 0.0)
           for (int c = 0; c < d; ++c) o[c] += ob[c] / lb;
@@ -512,7 +519,7 @@ int oracle_naive_block_sum(int BH, long N, int d, int P, int causal, long window
  *   pass 1, per query t: lse_t, O_t, D_t and dQ_t;
  *   pass 2, per key k:   dK_k and dV_k over the queries that see k.
  */
-int oracle_dense_bwd(int BH, long N, int d, int causal, long window, const uint16_t* q,
+int oracle_dense_bwd(int BH, long N, int d, int causal, long window, const long* seg, const uint16_t* q,
                      const uint16_t* k, const uint16_t* v, const uint16_t* dout,
                      double* dq, double* dk, double* dv, int nthreads) {
   if (BH <= 0 || N <= 0 || d <= 0) return -1;
@@ -547,18 +554,18 @@ int oracle_dense_bwd(int BH, long N, int d, int causal, long window, const uint1
       const uint16_t* vb = v + (size_t)bh * N * d;
       double m = -INFINITY;
       for (long kk = 0; kk < N; ++kk) {
-        if (!allowed(causal, window, t, kk)) continue;
+        if (!allowed(causal, window, seg, t, kk)) continue;
         s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
         if (s[kk] > m) m = s[kk];
       }
       double sum = 0.0;
       for (long kk = 0; kk < N; ++kk)
-        if (allowed(causal, window, t, kk)) sum += exp(s[kk] - m);
+        if (allowed(causal, window, seg, t, kk)) sum += exp(s[kk] - m);
       const double l = m + log(sum);
       lse[idx] = l;
       for (int c = 0; c < d; ++c) o[c] = 0.0;
       for (long kk = 0; kk < N; ++kk) {
-        if (!allowed(causal, window, t, kk)) continue;
+        if (!allowed(causal, window, seg, t, kk)) continue;
         const double p = exp(s[kk] - l);
         for (int c = 0; c < d; ++c) o[c] += p * widen_bf16(vb[(size_t)kk * d + c]);
       }
@@ -568,7 +575,7 @@ int oracle_dense_bwd(int BH, long N, int d, int causal, long window, const uint1
       double* g = dq + (size_t)idx * d;
       for (int c = 0; c < d; ++c) g[c] = 0.0;
       for (long kk = 0; kk < N; ++kk) {
-        if (!allowed(causal, window, t, kk)) continue;
+        if (!allowed(causal, window, seg, t, kk)) continue;
         const double p = exp(s[kk] - l);
         const double ds = p * (dot_q_k(dorow, vb + (size_t)kk * d, d) - Dt);
         for (int c = 0; c < d; ++c) g[c] += scale * ds * widen_bf16(kb[(size_t)kk * d + c]);
@@ -585,7 +592,7 @@ int oracle_dense_bwd(int BH, long N, int d, int causal, long window, const uint1
       double* gv = dv + (size_t)idx * d;
       for (int c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
       for (long t = 0; t < N; ++t) {
-        if (!allowed(causal, window, t, kk)) continue;
+        if (!allowed(causal, window, seg, t, kk)) continue;
         const size_t row = (size_t)bh * N + t;
         const uint16_t* qrow = q + row * d;
         const uint16_t* dorow = dout + row * d;
@@ -607,21 +614,21 @@ int oracle_dense_bwd(int BH, long N, int d, int causal, long window, const uint1
 
 /* lse_t and D_t = dO_t . O_t of one query row, by definition. */
 static void row_lse_and_D(const uint16_t* qrow, const uint16_t* dorow, long t, const uint16_t* kb,
-                          const uint16_t* vb, long N, int d, int causal, long window, double scale,
+                          const uint16_t* vb, long N, int d, int causal, long window, const long* seg, double scale,
                           double* s, double* o, double* lse_out, double* D_out) {
   double m = -INFINITY;
   for (long kk = 0; kk < N; ++kk) {
-    if (!allowed(causal, window, t, kk)) continue;
+    if (!allowed(causal, window, seg, t, kk)) continue;
     s[kk] = scale * dot_q_k(qrow, kb + (size_t)kk * d, d);
     if (s[kk] > m) m = s[kk];
   }
   double sum = 0.0;
   for (long kk = 0; kk < N; ++kk)
-    if (allowed(causal, window, t, kk)) sum += exp(s[kk] - m);
+    if (allowed(causal, window, seg, t, kk)) sum += exp(s[kk] - m);
   const double l = m + log(sum);
   for (int c = 0; c < d; ++c) o[c] = 0.0;
   for (long kk = 0; kk < N; ++kk) {
-    if (!allowed(causal, window, t, kk)) continue;
+    if (!allowed(causal, window, seg, t, kk)) continue;
     const double p = exp(s[kk] - l);
     for (int c = 0; c < d; ++c) o[c] += p * widen_bf16(vb[(size_t)kk * d + c]);
   }
@@ -638,7 +645,7 @@ static void row_lse_and_D(const uint16_t* qrow, const uint16_t* dorow, long t, c
  * query that a sampled key meets are recomputed on demand, so a key late in
  * a causal sequence (or any key under a sliding window) is cheap.
  */
-int oracle_dense_bwd_rows(int BH, long N, int d, int causal, long window, const uint16_t* q,
+int oracle_dense_bwd_rows(int BH, long N, int d, int causal, long window, const long* seg, const uint16_t* q,
                           const uint16_t* k, const uint16_t* v, const uint16_t* dout, long nq,
                           const long* qrows, long nk, const long* krows, double* dq, double* dk,
                           double* dv, int nthreads) {
@@ -667,12 +674,12 @@ int oracle_dense_bwd_rows(int BH, long N, int d, int causal, long window, const 
       if (x < nq) {
         const long t = qrows[x];
         double l, Dt;
-        row_lse_and_D(qb + (size_t)t * d, ob + (size_t)t * d, t, kb, vb, N, d, causal, window, scale, s, o,
+        row_lse_and_D(qb + (size_t)t * d, ob + (size_t)t * d, t, kb, vb, N, d, causal, window, seg, scale, s, o,
                       &l, &Dt);
         double* g = dq + ((size_t)bh * nq + x) * d;
         for (int c = 0; c < d; ++c) g[c] = 0.0;
         for (long kk = 0; kk < N; ++kk) {
-          if (!allowed(causal, window, t, kk)) continue;
+          if (!allowed(causal, window, seg, t, kk)) continue;
           const double p = exp(s[kk] - l);
           const double ds = p * (dot_q_k(ob + (size_t)t * d, vb + (size_t)kk * d, d) - Dt);
           for (int c = 0; c < d; ++c) g[c] += scale * ds * widen_bf16(kb[(size_t)kk * d + c]);
@@ -683,9 +690,9 @@ int oracle_dense_bwd_rows(int BH, long N, int d, int causal, long window, const 
         double* gv = dv + ((size_t)bh * nk + (x - nq)) * d;
         for (int c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
         for (long t = 0; t < N; ++t) {
-          if (!allowed(causal, window, t, kk)) continue;
+          if (!allowed(causal, window, seg, t, kk)) continue;
           double l, Dt;
-          row_lse_and_D(qb + (size_t)t * d, ob + (size_t)t * d, t, kb, vb, N, d, causal, window, scale, s, o,
+          row_lse_and_D(qb + (size_t)t * d, ob + (size_t)t * d, t, kb, vb, N, d, causal, window, seg, scale, s, o,
                         &l, &Dt);
           const double p = exp(scale * dot_q_k(qb + (size_t)t * d, kb + (size_t)kk * d, d) - l);
           const double ds = p * (dot_q_k(ob + (size_t)t * d, vb + (size_t)kk * d, d) - Dt);
@@ -720,7 +727,7 @@ int oracle_dense_bwd_rows(int BH, long N, int d, int causal, long window, const 
  * them as dK, dV.  Outputs dq, dk, dv are [BH][N][d] doubles in natural
  * order; visits (NULL or [BH][N][N]) counts every (query, key) pair used.
  */
-int oracle_ring_bwd(int BH, long N, int d, int P, int causal, long window, int layout,
+int oracle_ring_bwd(int BH, long N, int d, int P, int causal, long window, const long* seg, int layout,
                     const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
                     const double* out, const double* lse, double* dq, double* dk, double* dv,
                     long* visits, int nthreads) {
@@ -763,7 +770,7 @@ int oracle_ring_bwd(int BH, long N, int d, int P, int causal, long window, int l
           double* g = dq + (base + tq) * d;
           for (long kk = 0; kk < n; ++kk) {
             const long tk = oracle_position(layout, n, P, j, kk);
-            if (!allowed(causal, window, tq, tk)) continue;
+            if (!allowed(causal, window, seg, tq, tk)) continue;
             const uint16_t* krow = k + (base + tk) * d;
             const uint16_t* vrow = v + (base + tk) * d;
             const double p = exp(scale * dot_q_k(qrow, krow, d) - lse[base + tq]);

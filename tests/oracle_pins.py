@@ -526,6 +526,85 @@ def pin_ring_bwd_equals_dense(orc):
                     assert np.array_equal(got[3][0], allowed.astype(np.int64)), (P, layout, causal, w)
 
 
+# ---------------------------------------------------------------- segments
+def segment_matrix(bounds, N, causal, window=0):
+    """Allowed (query, key) pairs of a packed sequence: same document, and
+    the causal rule and window on top."""
+    seg = np.repeat(np.arange(len(bounds) - 1), np.diff(bounds))
+    m = seg[:, None] == seg[None, :]
+    if causal or window:
+        m &= _mask(N, True, window) if window else allowed_matrix(N, True)
+    return m
+
+
+def pin_segments_independent(orc):
+    """Sequence packing ([RA-CN] "正确性测试应覆盖哪些边界": documents packed into
+    one sequence must not attend to each other): the result on the packed
+    sequence equals attention over each document on its own, and a valid
+    length L (the tail padding as a document of its own) leaves the first L
+    rows as attention over those L tokens alone."""
+    BH, N, d = 2, 40, 8
+    q, k, v = rand_bits((BH, N, d), 401), rand_bits((BH, N, d), 402), rand_bits((BH, N, d), 403)
+    bounds = [0, 7, 20, 33, 40]
+    for causal in (False, True):
+        out, lse = orc.dense(q, k, v, causal, segments=bounds)
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            sl = lambda x: np.ascontiguousarray(x[:, a:b])
+            ref_o, ref_l = orc.dense(sl(q), sl(k), sl(v), causal)
+            _close(out[:, a:b], ref_o, 1e-13, f"segment [{a},{b}) out causal={causal}")
+            _close(lse[:, a:b], ref_l, 1e-13, f"segment [{a},{b}) lse causal={causal}")
+        L = 29
+        out, lse = orc.dense(q, k, v, causal, segments=[0, L, N])
+        sl = lambda x: np.ascontiguousarray(x[:, :L])
+        ref_o, ref_l = orc.dense(sl(q), sl(k), sl(v), causal)
+        _close(out[:, :L], ref_o, 1e-13, f"valid length {L} out causal={causal}")
+        _close(lse[:, :L], ref_l, 1e-13, f"valid length {L} lse causal={causal}")
+    out1 = orc.dense(q, k, v, True, segments=[0, N])
+    out0 = orc.dense(q, k, v, True)
+    _close(out1[0], out0[0], 0.0, "one segment = no segments")
+
+
+def pin_segments_sdpa(orc):
+    """Segments against torch's float64 scaled_dot_product_attention with the
+    explicit mask (same document, and causal / window)."""
+    BH, N, d = 2, 37, 16
+    q, k, v = rand_bits((BH, N, d), 411), rand_bits((BH, N, d), 412), rand_bits((BH, N, d), 413)
+    qt, kt, vt = (torch.from_numpy(bits_to_f64(x)) for x in (q, k, v))
+    bounds = [0, 5, 6, 19, 37]
+    for causal, w in ((False, 0), (True, 0), (True, 6)):
+        m = torch.from_numpy(segment_matrix(bounds, N, causal, w))
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m)
+        sc = (torch.einsum("bqd,bkd->bqk", qt, kt) / math.sqrt(d)).masked_fill(~m, float("-inf"))
+        out, lse = orc.dense(q, k, v, causal, segments=bounds, window=w)
+        _close(out, ref.numpy(), 1e-12, f"segments sdpa out causal={causal} w={w}")
+        _close(lse, torch.logsumexp(sc, dim=-1).numpy(), 1e-12, f"segments sdpa lse causal={causal} w={w}")
+
+
+def pin_segments_ring(orc):
+    """With segments the ring reaches the dense result in every layout and
+    uses exactly the allowed pairs once; the ring backward reaches the dense
+    gradients, and those match float64 autograd through SDPA with the mask."""
+    BH, N, d = 1, 24, 4
+    q, k, v, do = (rand_bits((BH, N, d), 420 + x) for x in range(4))
+    bounds = [0, 5, 13, 14, 24]
+    for causal, w in ((False, 0), (True, 0), (True, 4)):
+        ref_out, ref_lse = orc.dense(q, k, v, causal, segments=bounds, window=w)
+        ref_g = orc.dense_bwd(q, k, v, do, causal, segments=bounds, window=w)
+        auto = _torch_grads(q, k, v, do, segment_matrix(bounds, N, causal, w))
+        for name, a, b in zip(("dq", "dk", "dv"), ref_g, auto):
+            _close(a, b, 1e-12, f"segments bwd autograd {name} causal={causal} w={w}")
+        allowed = segment_matrix(bounds, N, causal, w).astype(np.int64)
+        for P in (1, 2, 3, 4, 6):
+            for layout in layouts_for(N, P):
+                out, lse, cnt = orc.ring(q, k, v, P, causal, layout, visits=True, segments=bounds, window=w)
+                _close(out, ref_out, 1e-12, f"segments ring out P={P} layout={layout} causal={causal}")
+                _close(lse, ref_lse, 1e-12, f"segments ring lse P={P} layout={layout} causal={causal}")
+                assert np.array_equal(cnt[0], allowed), (P, layout, causal, w)
+                g = orc.ring_bwd(q, k, v, do, ref_out, ref_lse, P, causal, layout, segments=bounds, window=w)
+                for name, a, b in zip(("dq", "dk", "dv"), g, ref_g):
+                    _close(a, b, 1e-12, f"segments ring bwd {name} P={P} layout={layout} causal={causal}")
+
+
 ALL_PINS = [
     pin_equal_keys_closed_form,
     pin_constant_values,
@@ -551,4 +630,7 @@ ALL_PINS = [
     pin_bwd_invariants,
     pin_bwd_rows_match,
     pin_ring_bwd_equals_dense,
+    pin_segments_independent,
+    pin_segments_sdpa,
+    pin_segments_ring,
 ]

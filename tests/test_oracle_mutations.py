@@ -64,6 +64,10 @@ MUTATIONS = [
      "const double p = exp(scale * dot_q_k(qrow, krow, d));", None),
     ("sampled backward dV uses the query's q",
      "gv[c] += p * widen_bf16(ob[(size_t)t * d + c]);", "gv[c] += p * widen_bf16(qb[(size_t)t * d + c]);", None),
+    ("segment rule ignored", "  if (seg && seg[pos_q] != seg[pos_k]) return 0;\n", "", None),
+    ("segment rule compares the query with a neighbour",
+     "  if (seg && seg[pos_q] != seg[pos_k]) return 0;",
+     "  if (seg && pos_k > 0 && seg[pos_q] != seg[pos_k - 1]) return 0;", None),
 ]
 
 
