@@ -40,7 +40,7 @@ MUTATIONS = [
      "if (window > 0 && pos_q - pos_k > window) return 0;", None),
     ("sliding window ignored", "if (window > 0 && pos_q - pos_k >= window) return 0;", "", None),
     ("block partial ignores the mask in the sum",
-     "      if (!allowed(causal, window, pos_q, kpos[kk])) continue;\n      double w",
+     "      if (!allowed(causal, window, seg, pos_q, kpos[kk])) continue;\n      double w",
      "      double w", None),
     ("backward dS drops the D term (dense)",
      "const double ds = p * (dot_q_k(dorow, vb + (size_t)kk * d, d) - Dt);",
