@@ -303,6 +303,24 @@ RINGATTN_API int ring_attn_decode_workspace_size(ring_attn_t h, long long Lq, si
 RINGATTN_API int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v, long long Lq, float* out,
                                   float* lse, void* workspace, void* stream);
 
+/* Sequence packing ([RA-CN] "正确性测试应覆盖哪些边界": several documents packed
+ * into one sequence must not attend to each other; the same list names
+ * sliding-window/segment masks and the tail padding with a valid-length
+ * mask).  bounds: host array of num_segments + 1 natural positions,
+ * 0 = b_0 < b_1 < .. < b_num_segments = N; document s is [b_s, b_{s+1}).
+ * A pair (query, key) is then allowed only inside one document, on top of
+ * the causal mask and the window.  A valid length L < N is the list
+ * {0, L, N}: the padding forms its own document, so no real token sees it.
+ * num_segments = 0 (bounds may be NULL) removes the segments.  Rebuilds the
+ * plan (the work counts follow the segments); the device copy of the table
+ * (two ints per position, owned by the handle) is made by the next compute
+ * call.  Applies to ring_attn_fwd, block_partial, decode and bwd.
+ * RING_ERR_INVALID_ARG for a list that does not rise strictly from 0 to N;
+ * RING_ERR_UNSUPPORTED for the ZIGZAG layout or N >= 2^31 (the handle keeps
+ * its previous segments).  ring_attn_fwd_noalloc returns
+ * RING_ERR_UNSUPPORTED while segments are set. */
+RINGATTN_API int ring_attn_set_segments(ring_attn_t h, const long long* bounds, int num_segments);
+
 /* Set an option (see ring_option_t). */
 RINGATTN_API int ring_attn_set_option(ring_attn_t h, int option, long long value);
 

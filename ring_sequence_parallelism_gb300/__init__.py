@@ -166,6 +166,13 @@ class RingAttention:
     def set_option(self, option: int, value: int):
         _lib.check(self._lib.ring_attn_set_option(self.handle, option, int(value)))
 
+    def set_segments(self, bounds):
+        """Sequence packing: document boundaries [0, b1, .., N] (None or []
+        removes them).  A valid length L is [0, L, N]."""
+        b = [] if bounds is None else [int(x) for x in bounds]
+        arr = (ctypes.c_longlong * max(len(b), 1))(*b)
+        _lib.check(self._lib.ring_attn_set_segments(self.handle, arr, max(len(b) - 1, 0)))
+
     # -- device calls ---------------------------------------------------
     def workspace(self, device=None):
         import torch

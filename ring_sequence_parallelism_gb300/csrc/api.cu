@@ -133,6 +133,9 @@ struct ring_attn {
   cudaEvent_t tp0 = nullptr, tp1 = nullptr;
   bool timed_valid = false;
   int* d_err = nullptr;  // [0] flags, [1] first failing site
+  int* d_seg = nullptr;  // segments: first / one-past-last position of each position's document, [2][N]
+  long long d_seg_n = 0;
+  bool seg_dirty = false;
 };
 
 namespace ringattn {
@@ -186,6 +189,32 @@ int ensure_device(ring_attn* h) {
 }
 
 bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+// Device copy of the segment table (after ensure_device): seg_lo at d_seg,
+// seg_hi at d_seg + N, or nullptr without segments.  Copied once per change.
+int device_segments(ring_attn* h, const int** lo, const int** hi) {
+  const Plan& p = h->plan;
+  *lo = *hi = nullptr;
+  if (p.seg_bounds.empty()) return RING_OK;
+  if (h->seg_dirty || !h->d_seg) {
+    if (h->d_seg && h->d_seg_n != p.N) {
+      RA_CUDA(cudaFree(h->d_seg), "cudaFree(segments)");
+      h->d_seg = nullptr;
+    }
+    if (!h->d_seg) {
+      RA_CUDA(cudaMalloc(&h->d_seg, (size_t)2 * p.N * sizeof(int)), "cudaMalloc(segments)");
+      h->d_seg_n = p.N;
+    }
+    RA_CUDA(cudaMemcpy(h->d_seg, p.seg_lo.data(), (size_t)p.N * sizeof(int), cudaMemcpyHostToDevice),
+            "cudaMemcpy(segments)");
+    RA_CUDA(cudaMemcpy(h->d_seg + p.N, p.seg_hi.data(), (size_t)p.N * sizeof(int), cudaMemcpyHostToDevice),
+            "cudaMemcpy(segments)");
+    h->seg_dirty = false;
+  }
+  *lo = h->d_seg;
+  *hi = h->d_seg + p.N;
+  return RING_OK;
+}
 
 // ring_attn_fwd's workspace: rotation buffers X and Y (K and V each, bf16
 // [P][B][H][n][d]), then the running state between steps in 128-row tile
@@ -275,6 +304,7 @@ int ring_attn_destroy(ring_attn_t h) {
     if (h->tp1) cudaEventDestroy(h->tp1);
     if (h->side) cudaStreamDestroy(h->side);
     if (h->d_err) cudaFree(h->d_err);
+    if (h->d_seg) cudaFree(h->d_seg);
     if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
   }
   delete h;
@@ -317,8 +347,16 @@ int ring_attn_plan_key_range(ring_attn_t h, int r, int step, long long row, long
   if (row < 0 || row >= p.n) return fail(RING_ERR_INVALID_ARG, "row out of range");
   const BlockPlan& b = p.at(step, r);
   const int half = row_half(p.layout, p.n, row);
-  if (first) *first = std::max(0LL, row + b.lodelta);
-  if (last) *last = std::min(b.klim[half], std::max(0LL, row + b.hdelta[half] + 1)) - 1;
+  long long lo = std::max(0LL, row + b.lodelta);
+  long long hi = std::min(b.klim[half], std::max(0LL, row + b.hdelta[half] + 1)) - 1;
+  if (!p.seg_bounds.empty()) {
+    long long slo, shi;
+    seg_key_bounds(p, r, b.j, row, &slo, &shi);
+    lo = std::max(lo, slo);
+    hi = std::min(hi, shi);
+  }
+  if (first) *first = lo;
+  if (last) *last = hi;
   return RING_OK;
 }
 
@@ -336,6 +374,22 @@ int ring_attn_step_work(ring_attn_t h, int step, long long* pairs, long long* ti
   if (step < 0 || step >= h->plan.P) return fail(RING_ERR_INVALID_ARG, "step out of range");
   if (pairs) *pairs = h->plan.step_pairs[step];
   if (tiles) *tiles = h->plan.step_tiles[step];
+  return RING_OK;
+}
+
+int ring_attn_set_segments(ring_attn_t h, const long long* bounds, int num_segments) {
+  if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
+  if (num_segments < 0 || (num_segments > 0 && !bounds)) return fail(RING_ERR_INVALID_ARG, "bad segment list");
+  std::vector<long long> sb;
+  if (num_segments > 0) sb.assign(bounds, bounds + num_segments + 1);
+  const Plan& p = h->plan;
+  Plan np;
+  std::string err;
+  int rc = build_plan(&np, p.B, p.H, p.N, p.d, p.P, p.causal, p.layout, &err, p.window, &sb);
+  if (rc != RING_OK) return fail(rc, err);
+  np.Hkv = p.Hkv;
+  h->plan = std::move(np);
+  h->seg_dirty = true;
   return RING_OK;
 }
 
@@ -359,7 +413,7 @@ int ring_attn_set_option(ring_attn_t h, int option, long long value) {
       Plan np;
       std::string err;
       const Plan& p = h->plan;
-      int rc = build_plan(&np, p.B, p.H, p.N, p.d, p.P, p.causal, p.layout, &err, value);
+      int rc = build_plan(&np, p.B, p.H, p.N, p.d, p.P, p.causal, p.layout, &err, value, &p.seg_bounds);
       if (rc != RING_OK) return fail(rc, err);
       np.Hkv = p.Hkv;
       h->plan = std::move(np);
@@ -438,6 +492,7 @@ int ring_attn_block_partial(ring_attn_t h, int r, int step, const void* q_shard,
     if ((rc = encode_map(&vm, v_block, dims, str, kTileN, 1))) return rc;
   }
   StepArgs a = base_args(h);
+  if ((rc = device_segments(h, &a.seg_lo, &a.seg_hi))) return rc;
   a.o_state = state.o;
   a.m_state = state.m;
   a.l_state = state.l;
@@ -511,6 +566,7 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
 
   const size_t slot_bytes = (size_t)BHkv * (size_t)p.n * p.d * 2;
   StepArgs a = base_args(h);
+  if ((rc = device_segments(h, &a.seg_lo, &a.seg_hi))) return rc;
   a.o_state = reinterpret_cast<float*>(ws + fw.o_off);  // the running state, tile blocks
   a.m_state = reinterpret_cast<float*>(ws + fw.m_off);
   a.l_state = reinterpret_cast<float*>(ws + fw.l_off);
@@ -664,6 +720,7 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   if (timing) RA_CUDA(cudaEventRecord(h->tbp1, cs), "cudaEventRecord");
   BwdArgs a;
   std::memset(&a, 0, sizeof a);
+  if ((rc = device_segments(h, &a.seg_lo, &a.seg_hi))) return rc;
   a.nlse2 = nlse2;
   a.nD = nD;
   a.dq = dq;
@@ -775,6 +832,7 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
   float* l_st = reinterpret_cast<float*>(ws + up(rows * p.d * 4) + up(rows * 4));
 
   StepArgs a = base_args(h);
+  if ((rc = device_segments(h, &a.seg_lo, &a.seg_hi))) return rc;
   a.o_state = o_st;  // shard r's states: rows [r][bh][i]
   a.m_state = m_st;
   a.l_state = l_st;

@@ -152,6 +152,24 @@ __device__ __forceinline__ BwdRule bwd_rule(const BwdArgs& a, int r, int j) {
   return w;
 }
 
+// Sequence packing: local row x of shard `sh` sits in a document [ds, de)
+// of natural positions; as local indices of shard `other` that document is
+// [lo, hi] (contiguous: positions sh n + x and o n + y; striped: x P + sh and
+// y P + o).  Non-decreasing in x.
+__device__ __forceinline__ void doc_range(const BwdArgs& a, int sh, int other, long long x, long long& lo,
+                                          long long& hi) {
+  const bool striped = a.layout == RING_LAYOUT_STRIPED;
+  const long long pos = striped ? x * a.P + sh : (long long)sh * a.n + x;
+  const long long ds = a.seg_lo[pos], de = a.seg_hi[pos];
+  if (striped) {
+    lo = floor_div_ll(ds - other + a.P - 1, a.P);
+    hi = floor_div_ll(de - 1 - other, a.P);
+  } else {
+    lo = ds - (long long)other * a.n;
+    hi = de - 1 - (long long)other * a.n;
+  }
+}
+
 // Row of (shard r, local i) of head bh in a natural-order tensor.
 __device__ __forceinline__ long long nat_row(const BwdArgs& a, int bh, int r, long long i) {
   return (long long)bh * a.N + (long long)r * a.row_r + i * a.row_i;
@@ -253,8 +271,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const long long k1 = min(k0 + kTileN - 1, rule.kmax);
   int it_lo = 0, n_it = 0;
   if (k0 <= k1) {
-    const long long i_lo = max(0LL, k0 - rule.dhi);
-    const long long i_hi = min((long long)a.n - 1, k1 - rule.dlo);
+    long long i_lo = max(0LL, k0 - rule.dhi);
+    long long i_hi = min((long long)a.n - 1, k1 - rule.dlo);
+    if (kWin && a.seg_lo) {
+      // queries in the documents of the tile's first and last keys
+      long long lo0, hi0, lo1, hi1;
+      doc_range(a, j, r, k0, lo0, hi0);
+      doc_range(a, j, r, k1, lo1, hi1);
+      i_lo = max(i_lo, lo0);
+      i_hi = min(i_hi, hi1);
+    }
     if (i_lo <= i_hi) {
       it_lo = (int)(i_lo / kTileM);
       n_it = (int)(i_hi / kTileM) + 1 - it_lo;
@@ -400,8 +426,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_store_wait();
     }
     // this key's allowed queries: i_lo_k <= i <= i_hi_k
-    const long long i_lo_k = k_row <= rule.kmax ? max(0LL, k_row - rule.dhi) : (long long)a.n;
-    const long long i_hi_k = min((long long)a.n - 1, k_row - rule.dlo);
+    long long i_lo_k = k_row <= rule.kmax ? max(0LL, k_row - rule.dhi) : (long long)a.n;
+    long long i_hi_k = min((long long)a.n - 1, k_row - rule.dlo);
+    if (kWin && a.seg_lo && k_row <= rule.kmax) {
+      long long qlo, qhi;
+      doc_range(a, j, r, k_row, qlo, qhi);
+      i_lo_k = max(i_lo_k, qlo);
+      i_hi_k = min(i_hi_k, qhi);
+    }
     bool ok = true;
     for (int x = 0; x < n_it; ++x) {
       const int st = x & 1;
@@ -573,8 +605,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const long long i1 = min(i0 + kTileM - 1, (long long)a.n - 1);
   int kt_lo = 0, n_kt = 0;
   {
-    const long long k_lo = max(0LL, i0 + rule.dlo);
-    const long long k_hi = min(rule.kmax, i1 + rule.dhi);
+    long long k_lo = max(0LL, i0 + rule.dlo);
+    long long k_hi = min(rule.kmax, i1 + rule.dhi);
+    if (kWin && a.seg_lo) {
+      // keys in the documents of the tile's first and last rows
+      long long lo0, hi0, lo1, hi1;
+      doc_range(a, r, j, i0, lo0, hi0);
+      doc_range(a, r, j, i1, lo1, hi1);
+      k_lo = max(k_lo, lo0);
+      k_hi = min(k_hi, hi1);
+    }
     if (k_lo <= k_hi) {
       kt_lo = (int)(k_lo / kTileN);
       n_kt = (int)(k_hi / kTileN) + 1 - kt_lo;
@@ -716,8 +756,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_store_wait();
     }
     // this row's allowed keys: k_lo_i <= k <= k_hi_i
-    const long long k_lo_i = max(0LL, i_row + rule.dlo);
-    const long long k_hi_i = i_valid ? min(rule.kmax, i_row + rule.dhi) : -1;
+    long long k_lo_i = max(0LL, i_row + rule.dlo);
+    long long k_hi_i = i_valid ? min(rule.kmax, i_row + rule.dhi) : -1;
+    if (kWin && a.seg_lo && i_valid) {
+      long long klo, khi;
+      doc_range(a, r, j, i_row, klo, khi);
+      k_lo_i = max(k_lo_i, klo);
+      k_hi_i = min(k_hi_i, khi);
+    }
     bool ok = true;
     for (int x = 0; x < n_kt; ++x) {
       const long long kbase = (long long)(kt_lo + x) * kTileN + c0;  // first key of this half
@@ -879,7 +925,7 @@ int launch_bwd_dkdv(const BwdArgs& a, const void* q_map, const void* do_map, con
   const CUtensorMap& om = *static_cast<const CUtensorMap*>(do_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
   const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
-  const bool win = a.causal && a.window > 0;
+  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
   if (d == 64) {
     if (win) bwd_dkdv_kernel<64, true><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
     else bwd_dkdv_kernel<64, false><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
@@ -899,7 +945,7 @@ int launch_bwd_dq(const BwdArgs& a, const void* q_map, const void* do_map, const
   const CUtensorMap& om = *static_cast<const CUtensorMap*>(do_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
   const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
-  const bool win = a.causal && a.window > 0;
+  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
   if (d == 64) {
     if (win) bwd_dq_kernel<64, true><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
     else bwd_dq_kernel<64, false><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);

@@ -199,6 +199,24 @@ __device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int 
   if (W > 0) w->bl = striped ? floor_div((long long)(r - j) - W, a.P) : (long long)(r - j) * n - W;
 }
 
+// Sequence packing: the keys of block j that local query row i of shard r
+// may see lie in its document [ds, de) of natural positions.  Keys of block
+// j sit at j n + k (contiguous) or k P + j (striped); queries at r n + i,
+// i P + r, or pos0 + i for short queries.  Inclusive local key bounds.
+__device__ __forceinline__ void seg_bounds(const StepArgs& a, int r, int j, long long i, long long& lo,
+                                           long long& hi) {
+  const long long pos = a.decode_pos0 >= 0 ? a.decode_pos0 + i
+                                           : (a.layout == RING_LAYOUT_STRIPED ? i * a.P + r : (long long)r * a.n + i);
+  const long long ds = a.seg_lo[pos], de = a.seg_hi[pos];
+  if (a.layout == RING_LAYOUT_STRIPED) {
+    lo = floor_div(ds - j + a.P - 1, a.P);
+    hi = floor_div(de - 1 - j, a.P);
+  } else {
+    lo = ds - (long long)j * a.n;
+    hi = de - 1 - (long long)j * a.n;
+  }
+}
+
 template <bool kWin>
 __device__ __forceinline__ Tile tile_work(const StepArgs& a, int r, int j, int t) {
   Tile w{};
@@ -213,12 +231,22 @@ __device__ __forceinline__ Tile tile_work(const StepArgs& a, int r, int j, int t
   // kmin and kmax are non-decreasing in i: the last row bounds the tiles
   // from above, the first row from below, and the tiles every row may use
   // in full lie between the first row's kmax and the last row's kmin.
-  const long long last_key = min((long long)w.klim - 1, tile_kmax(w, i_max));
-  const long long first_key = kWin ? max(0LL, tile_kmin(w, i_min)) : 0;
+  long long last_key = min((long long)w.klim - 1, tile_kmax(w, i_max));
+  long long first_key = kWin ? max(0LL, tile_kmin(w, i_min)) : 0;
+  long long common_hi = min((long long)w.klim, tile_kmax(w, i_min) + 1);  // keys < this for every row
+  long long common_lo = kWin ? max(0LL, tile_kmin(w, i_max)) : 0;          // keys >= this for every row
+  if (kWin && a.seg_lo) {
+    // the document bounds are non-decreasing in i too
+    long long lo0, hi0, lo1, hi1;
+    seg_bounds(a, r, j, i_min, lo0, hi0);
+    seg_bounds(a, r, j, i_max, lo1, hi1);
+    first_key = max(first_key, lo0);
+    last_key = min(last_key, hi1);
+    common_lo = max(common_lo, lo1);
+    common_hi = min(common_hi, hi0 + 1);
+  }
   w.kt_hi = last_key < 0 ? 0 : (int)min((long long)a.KT, last_key / kTileN + 1);
   w.kt_lo = (int)min((long long)w.kt_hi, first_key / kTileN);
-  const long long common_hi = min((long long)w.klim, tile_kmax(w, i_min) + 1);  // keys < this for every row
-  const long long common_lo = kWin ? max(0LL, tile_kmin(w, i_max)) : 0;                       // keys >= this for every row
   w.full_hi = common_hi <= 0 ? 0 : (int)min((long long)w.kt_hi, common_hi / kTileN);
   w.full_lo = (int)min((long long)w.kt_hi, (common_lo + kTileN - 1) / kTileN);
   return w;
@@ -262,7 +290,7 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   // but not at its end; then both tiles of a ring block visit the whole
   // prefix (blocks without a diagonal or window), so one order serves both.
   // Short queries (decode) send nothing and keep the natural order.
-  w.rot = (a.decode_pos0 < 0 && !(kWin && a.window > 0) && lo == 0 && w.fwd_hi < hi) ? w.fwd_hi : 0;
+  w.rot = (a.decode_pos0 < 0 && !(kWin && (a.window > 0 || a.seg_lo)) && lo == 0 && w.fwd_hi < hi) ? w.fwd_hi : 0;
   // Tiles sent along the ring come last: either they end the computed range
   // (after the rotation), possibly followed by the ones beyond it, or they
   // are loaded again after it (a window can leave them inside or below it).
@@ -278,6 +306,17 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
     if (tt.kt_hi > tt.kt_lo) {
       tt.jb = tt.kt_lo - lo;
       tt.je = tt.kt_hi - lo;
+      // With documents the two tiles' ranges can start far apart and leave
+      // loaded key tiles that neither uses between them.  A tile whose first
+      // loop index is 2 or more would then wait on a stage barrier two
+      // phases ahead of its current one (the wait would return at once), and
+      // a stage could be reloaded before its unused tile landed.  So each
+      // tile with keys runs the CTA's whole range; the masks zero the rest.
+      // (A window shifts the second tile's range by at most one tile.)
+      if (kWin && a.seg_lo) {
+        tt.jb = 0;
+        tt.je = w.nk;
+      }
     } else {
       tt.jb = tt.je = 0;
     }
@@ -292,8 +331,9 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
 }
 
 // ------------------------------------------------------------- the kernel
-// kWin: the sliding-window lower bound is in force (instantiated apart so the
-// unwindowed kernel carries none of its bookkeeping).
+// kWin: row-dependent bounds are in force, a sliding window's lower bound
+// and/or the document bounds of sequence packing (instantiated apart so the
+// plain kernel carries none of their bookkeeping).
 template <int D, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
     block_partial_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ CUtensorMap q_map,
@@ -560,8 +600,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = t_sm;  // 0: tile A (warps 3-6), 1: tile B (warps 7-10)
     // this row's allowed keys [kmin_row, kmax_row] (keys fit in int; the
     // bounds are clamped to it)
-    const int kmax_row = (int)max(-1LL, min((long long)tw.klim - 1, tile_kmax(tw, i_row)));
-    const int kmin_row = kWin ? (int)max(0LL, min((long long)a.n, tile_kmin(tw, i_row))) : 0;
+    int kmax_row = (int)max(-1LL, min((long long)tw.klim - 1, tile_kmax(tw, i_row)));
+    int kmin_row = kWin ? (int)max(0LL, min((long long)a.n, tile_kmin(tw, i_row))) : 0;
+    if (kWin && a.seg_lo && in_range) {
+      long long slo, shi;
+      seg_bounds(a, w.r, w.j, min(i_row, (long long)a.nq - 1), slo, shi);
+      kmin_row = max(kmin_row, (int)max(0LL, min((long long)a.n, slo)));
+      kmax_row = min(kmax_row, (int)max(-1LL, min((long long)a.n, shi)));
+    }
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + L::tmem_s(t);
     const uint32_t o_addr = tmem + lane_off + L::tmem_o(t);
@@ -738,7 +784,7 @@ int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map
   // without `forward` the kernel never touches the send maps
   const CUtensorMap& kn = *static_cast<const CUtensorMap*>(k_next_map ? k_next_map : k_map);
   const CUtensorMap& vn = *static_cast<const CUtensorMap*>(v_next_map ? v_next_map : v_map);
-  const bool win = a.causal && a.window > 0;
+  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
   if (d == 64) {
     if (win) block_partial_kernel<64, true><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
     else block_partial_kernel<64, false><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);

@@ -106,6 +106,9 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
       (status && reinterpret_cast<uintptr_t>(status) % 4 != 0))
     return report_error(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
   const Plan& p = handle_plan(h);
+  if (!p.seg_bounds.empty())
+    return report_error(RING_ERR_UNSUPPORTED,
+                        "segments need a device table of document bounds; use ring_attn_fwd");
   const int P = p.P, BH = p.B * p.H, BHkv = p.B * p.Hkv;
   const size_t elems = (size_t)BHkv * (size_t)p.N * p.d;  // one of K, V (K/V heads)
   const size_t kv_bytes = round256(elems * 2);

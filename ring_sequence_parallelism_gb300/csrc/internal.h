@@ -48,9 +48,18 @@ struct Plan {
   std::vector<long long> step_pairs;   // [P]
   std::vector<long long> step_tiles;   // [P]
   std::vector<std::vector<unsigned short>> active;  // [step] shards with work
+  // Sequence packing: document boundaries [0, .., N] (empty: one document)
+  // and, per natural position, the first and one-past-last position of its
+  // document.
+  std::vector<long long> seg_bounds;
+  std::vector<int> seg_lo, seg_hi;
 
   const BlockPlan& at(int step, int r) const { return blocks[(size_t)step * P + r]; }
 };
+
+// Local key bounds (inclusive) that the segments allow row i of shard r in
+// block j (contiguous or striped layout); lo > hi when none.
+void seg_key_bounds(const Plan& p, int r, int j, long long i, long long* lo, long long* hi);
 
 int block_of(int P, int r, int step);  // (r - step) mod P
 BlockPlan classify(int layout, int causal, long long n, int r, int j, int P = 1, long long window = 0);
@@ -63,7 +72,7 @@ long long block_pairs(int layout, long long n, const BlockPlan& b);
 // of them need no mask.
 void tile_range(int layout, long long n, int KT, const BlockPlan& b, int t, int* nk, int* full_kt);
 int build_plan(Plan* plan, int B, int H, long long N, int d, int P, int causal, int layout,
-               std::string* err, long long window = 0);
+               std::string* err, long long window = 0, const std::vector<long long>* segments = nullptr);
 
 // ---------------------------------------------------------------- kernels
 // Query tensor addressing modes for the TMA map of Q.
@@ -105,6 +114,11 @@ struct StepArgs {
   long long decode_pos0;  // >= 0: queries at global positions pos0 + i against block j's keys
                           //       (the causal rule from global positions; see ring_attn_decode)
   float scale_log2;  // log2(e) / sqrt(d)
+  // sequence packing (nullptr: one document): per natural position, the
+  // first and one-past-last position of its document; a pair is allowed
+  // only inside one document
+  const int* seg_lo;
+  const int* seg_hi;
   unsigned short active[kMaxShards];
 };
 
@@ -131,6 +145,8 @@ struct BwdArgs {
   int last;        // step P - 1: write the gradients
   long long window;
   float scale, scale_log2;
+  const int* seg_lo;  // sequence packing, as in StepArgs (nullptr: one document)
+  const int* seg_hi;
 };
 
 // Device error flags.

@@ -102,8 +102,51 @@ void tile_range(int layout, long long n, int KT, const BlockPlan& b, int t, int*
   *full_kt = common <= 0 ? 0 : (int)std::min<long long>(cnt, common / kTileN);
 }
 
+void seg_key_bounds(const Plan& p, int r, int j, long long i, long long* lo, long long* hi) {
+  // the query's document [ds, de); keys of block j at j n + k (contiguous)
+  // or k P + j (striped)
+  const long long pos = p.layout == RING_LAYOUT_STRIPED ? i * p.P + r : (long long)r * p.n + i;
+  const long long ds = p.seg_lo[(size_t)pos], de = p.seg_hi[(size_t)pos];
+  if (p.layout == RING_LAYOUT_STRIPED) {
+    *lo = floor_div(ds - j + p.P - 1, p.P);
+    *hi = floor_div(de - 1 - j, p.P);
+  } else {
+    *lo = ds - (long long)j * p.n;
+    *hi = de - 1 - (long long)j * p.n;
+  }
+}
+
+// Allowed pairs and computed 128x128 tiles of block (r, j) with segments:
+// row i allows columns max(0, i + lodelta, slo(i)) .. min(klim, i + hdelta
+// + 1, shi(i) + 1) - 1; the bounds are non-decreasing in i, so a tile's key
+// tiles run from its first row's lower bound to its last row's upper bound.
+static std::pair<long long, long long> segment_work(const Plan& p, const BlockPlan& b, int r) {
+  const long long n = p.n;
+  long long pairs = 0, tiles = 0;
+  auto lo_of = [&](long long i) {
+    long long slo, shi;
+    seg_key_bounds(p, r, b.j, i, &slo, &shi);
+    return std::max({0LL, i + b.lodelta, slo});
+  };
+  auto hi_of = [&](long long i) {  // exclusive
+    long long slo, shi;
+    seg_key_bounds(p, r, b.j, i, &slo, &shi);
+    return std::min({b.klim[0], std::max(0LL, i + b.hdelta[0] + 1), shi + 1});
+  };
+  for (long long i = 0; i < n; ++i) pairs += std::max(0LL, hi_of(i) - lo_of(i));
+  for (int t = 0; t < p.T; ++t) {
+    const long long i_min = (long long)t * kTileM, i_max = std::min(n - 1, i_min + kTileM - 1);
+    const long long last = std::min<long long>(hi_of(i_max), n) - 1;
+    if (last < 0) continue;
+    const long long first = std::min(lo_of(i_min), last + 1);
+    if (first > last) continue;
+    tiles += last / kTileN - first / kTileN + 1;
+  }
+  return {pairs, tiles};
+}
+
 int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int layout,
-               std::string* err, long long window) {
+               std::string* err, long long window, const std::vector<long long>* segments) {
   char buf[256];
   if (B <= 0 || H <= 0 || N <= 0 || d <= 0 || P <= 0) {
     std::snprintf(buf, sizeof buf, "sizes must be positive (B=%d H=%d N=%lld d=%d P=%d)", B, H, N, d, P);
@@ -154,6 +197,24 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
     *err = "shard length or B*H too large";
     return RING_ERR_UNSUPPORTED;
   }
+  const bool packed = segments && !segments->empty();
+  if (packed) {
+    const std::vector<long long>& sb = *segments;
+    bool ok = sb.size() >= 2 && sb.front() == 0 && sb.back() == N;
+    for (size_t x = 1; ok && x < sb.size(); ++x) ok = sb[x] > sb[x - 1];
+    if (!ok) {
+      *err = "segment boundaries must rise strictly from 0 to N";
+      return RING_ERR_INVALID_ARG;
+    }
+    if (layout == RING_LAYOUT_ZIGZAG) {
+      *err = "segments need the contiguous or striped layout";
+      return RING_ERR_UNSUPPORTED;
+    }
+    if (N > (1LL << 31) - 1) {
+      *err = "segments need N < 2^31";
+      return RING_ERR_UNSUPPORTED;
+    }
+  }
   p->B = B;
   p->H = H;
   p->N = N;
@@ -172,6 +233,19 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   p->step_pairs.assign(P, 0);
   p->step_tiles.assign(P, 0);
   p->active.assign(P, {});
+  p->seg_bounds.clear();
+  p->seg_lo.clear();
+  p->seg_hi.clear();
+  if (packed) {
+    p->seg_bounds = *segments;
+    p->seg_lo.resize((size_t)N);
+    p->seg_hi.resize((size_t)N);
+    for (size_t x = 0; x + 1 < segments->size(); ++x)
+      for (long long t = (*segments)[x]; t < (*segments)[x + 1]; ++t) {
+        p->seg_lo[(size_t)t] = (int)(*segments)[x];
+        p->seg_hi[(size_t)t] = (int)(*segments)[x + 1];
+      }
+  }
   // Work per distinct mask rule: every layout has at most four rules, so a
   // small cache suffices.
   std::vector<std::pair<std::vector<long long>, std::pair<long long, long long>>> cache;
@@ -193,7 +267,7 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
     for (int r = 0; r < P; ++r) {
       BlockPlan b = classify(layout, causal, n, r, block_of(P, r, s), P, window);
       p->blocks[(size_t)s * P + r] = b;
-      auto w = work(b);
+      auto w = packed ? segment_work(*p, b, r) : work(b);
       p->shard_pairs[r] += w.first * bh;
       p->shard_tiles[r] += w.second * bh;
       p->step_pairs[s] += w.first * bh;

@@ -35,6 +35,7 @@ class Workload:
     key_boost: float = 8.0
     Hkv: int = 0  # K/V heads for grouped-query attention (0: H)
     window: int = 0  # causal sliding window (0: none)
+    doc_len: tuple = ()  # sequence packing: (min, max) document length (empty: one document)
 
     @property
     def kv_heads(self) -> int:
@@ -48,7 +49,18 @@ class Workload:
     def layout_id(self) -> int:
         return {"contiguous": 0, "striped": 1, "zigzag": 2}[self.layout]
 
+    def segments(self):
+        """Document boundaries of the packed sequence, or None."""
+        return document_bounds(self.N, self.seed, *self.doc_len) if self.doc_len else None
+
     def allowed_pairs_per_head(self) -> int:
+        if self.doc_len:
+            b = self.segments()
+            lens = [y - x for x, y in zip(b[:-1], b[1:])]
+            if not self.causal:
+                return sum(L * L for L in lens)
+            W = self.window or self.N
+            return sum(min(W, L) * (min(W, L) + 1) // 2 + (L - min(W, L)) * W for L in lens)
         if self.causal and self.window > 0:
             W, N = min(self.window, self.N), self.N
             return W * (W + 1) // 2 + (N - W) * W  # row t sees min(t + 1, W) keys
@@ -72,6 +84,9 @@ WORKLOADS = {
         Workload("zigzag-128k", 1, 16, 131072, 128, 16, True, "zigzag", 1003, key_boost_frac=0.01),
         # causal sliding window of 4096 tokens over the 128K striped sequence
         Workload("swa-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01, window=4096),
+        # sequence packing: documents of 1K-16K tokens packed into the 128K striped sequence
+        Workload("packed-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01,
+                 doc_len=(1024, 16384)),
         # grouped-query attention: 16 query heads sharing 4 K/V heads
         Workload("gqa-128k", 1, 16, 131072, 128, 16, True, "striped", 1003, key_boost_frac=0.01, Hkv=4),
         # profiling size: the 128K striped workload with 4 heads (inputs 3 x 134 MB)
@@ -116,6 +131,20 @@ def make_dout(B: int, H: int, N: int, d: int, seed: int, device="cpu", pin: bool
         for h in range(H):
             t[b, h].copy_(torch.randn((N, d), generator=g, dtype=torch.float32))
     return t.to(device) if device != "cpu" else t
+
+
+def document_bounds(N: int, seed: int, min_len: int, max_len: int) -> list:
+    """Sequence packing: documents of lengths drawn uniformly from
+    [min_len, max_len] by a CPU generator seeded ``seed + 11``, packed until
+    they cover N tokens (the last one cut at N).  Returns the boundaries
+    [0, b1, .., N]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 11)
+    bounds = [0]
+    while bounds[-1] < N:
+        length = int(torch.randint(min_len, max_len + 1, (1,), generator=g))
+        bounds.append(min(N, bounds[-1] + length))
+    return bounds
 
 
 def boosted_key_rows(N: int, seed: int, frac: float) -> torch.Tensor:

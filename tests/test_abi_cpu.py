@@ -260,3 +260,55 @@ def test_step_time_model_golden():
         if line.strip() and not line.startswith("#"):
             steps, tc, tm, total = map(float, line.split())
             assert pipelined_ring_ms(int(steps), tc, tm) == pytest.approx(total)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 5)])
+@pytest.mark.parametrize("P", [1, 2, 3, 4])
+def test_segment_plan_agrees_with_oracle(lib, orc, layout, causal, window, P):
+    """With sequence packing the planner's key range of every (shard, step,
+    row) and its per-step pair counts equal the pairs the oracle's ring
+    simulation visits (same documents, causal rule and window)."""
+    from oracle import LAYOUT_CONTIGUOUS, LAYOUT_STRIPED
+    import oracle_pins
+
+    N, d = 24, 2
+    n = N // P
+    bounds = [0, 5, 13, 14, 24]
+    lid = LAYOUT_STRIPED if layout == "striped" else LAYOUT_CONTIGUOUS
+    q = oracle_pins.rand_bits((1, N, d), 3)
+    _, _, cnt = orc.ring(q, q, q, P, causal, lid, visits=True, window=window, segments=bounds)
+    att = ra.RingAttention(1, 1, N, 64, P, causal=causal, layout=layout)
+    if window:
+        att.set_option(ra.RING_OPT_WINDOW, window)
+    att.set_segments(bounds)
+    for s in range(P):
+        step_pairs = 0
+        for r in range(P):
+            j = orc.block_at(P, r, s)
+            for i in range(n):
+                tq = orc.position(lid, n, P, r, i)
+                first, last = att.plan_key_range(r, s, i)
+                want = [kk for kk in range(n) if cnt[0][tq, orc.position(lid, n, P, j, kk)]]
+                got = list(range(max(first, 0), min(last, n - 1) + 1))
+                assert got == want, (r, s, i, first, last, want)
+                step_pairs += len(want)
+        assert att.step_work(s)[0] == step_pairs, (s, att.step_work(s), step_pairs)
+    att.set_segments(None)
+    att.close()
+
+
+def test_segments_rejected(lib):
+    """Boundaries must rise strictly from 0 to N; the zigzag layout has no
+    segment support; the handle keeps its previous segments on an error."""
+    att = ra.RingAttention(1, 1, 64, 64, 4, causal=True, layout="striped")
+    for bad in ([0, 10, 10, 64], [1, 64], [0, 63], [0, 70, 64]):
+        with pytest.raises(_lib.RingAttnError) as e:
+            att.set_segments(bad)
+        assert e.value.status == _lib.RING_ERR_INVALID_ARG
+    att.close()
+    z = ra.RingAttention(1, 1, 1024, 64, 2, causal=True, layout="zigzag")
+    with pytest.raises(_lib.RingAttnError) as e:
+        z.set_segments([0, 100, 1024])
+    assert e.value.status == _lib.RING_ERR_UNSUPPORTED
+    z.close()
