@@ -170,6 +170,26 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- oracle leg
+def allowed_keys(w, rows) -> int:
+    """Allowed keys summed over the sampled query rows (causal mask, window
+    and documents of the workload)."""
+    import numpy as np
+
+    rows = np.asarray(rows, dtype=np.int64)
+    lo = np.zeros_like(rows)
+    hi = np.full_like(rows, w.N - 1)
+    if w.causal:
+        hi = rows.copy()
+        if w.window:
+            lo = np.maximum(lo, rows - w.window + 1)
+    if w.doc_len:
+        b = np.asarray(w.segments(), dtype=np.int64)
+        x = np.searchsorted(b, rows, side="right") - 1
+        lo = np.maximum(lo, b[x])
+        hi = np.minimum(hi, b[x + 1] - 1)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
 def oracle_sample(w, q, k, v, seconds: float, seed: int = 4242):
     """Time the float64 oracle on a bounded sample of query rows.  Returns
     (TFLOP/s, rows per second, threads, description, wall seconds)."""
@@ -188,9 +208,9 @@ def oracle_sample(w, q, k, v, seconds: float, seed: int = 4242):
     while True:
         rows = sample_rows(w.N, rows_per_head, seed=seed).numpy()
         t0 = time.perf_counter()
-        orc.dense(qf, kf, vf, w.causal, rows=rows, window=w.window)
+        orc.dense(qf, kf, vf, w.causal, rows=rows, window=w.window, segments=w.segments())
         t_used = time.perf_counter() - t0
-        keys = (rows + 1).clip(max=w.window or None).sum() if w.causal else rows.size * w.N
+        keys = allowed_keys(w, rows)
         flops = 4 * w.d * BH * int(keys)
         if t_used >= seconds / 4 or rows_per_head >= w.N:
             break
@@ -224,9 +244,9 @@ def run_reference(args, w):
     times, flops = [], 0
     for i in range(args.warmup + args.steps):
         rows = sample_rows(w.N, rph, seed=5000 + i).numpy()
-        keys = (rows + 1).clip(max=w.window or None).sum() if w.causal else rows.size * w.N
+        keys = allowed_keys(w, rows)
         t0 = time.perf_counter()
-        orc.dense(qf, kf, vf, w.causal, rows=rows, window=w.window)
+        orc.dense(qf, kf, vf, w.causal, rows=rows, window=w.window, segments=w.segments())
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -248,7 +268,8 @@ def run_reference(args, w):
 
 def config_of(w):
     return {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N": w.N, "d": w.d, "P": w.P,
-            "layout": w.layout, "causal": w.causal, "window": w.window, "global_batch": w.B, "seq_len": w.N,
+            "layout": w.layout, "causal": w.causal, "window": w.window,
+            "documents": len(w.segments()) - 1 if w.doc_len else 1, "global_batch": w.B, "seq_len": w.N,
             "inputs": "Q,K,V ~ N(0,1) rounded to bf16" + (", 1% of key rows x8" if w.key_boost_frac else ""),
             "l2": l2_note(w)}
 
@@ -279,6 +300,8 @@ def run_ours(args, w):
     att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
     if w.window:
         att.set_option(ra.RING_OPT_WINDOW, w.window)
+    if w.doc_len:
+        att.set_segments(w.segments())
     out = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device="cuda")
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
     att.set_option(ra.RING_OPT_TIMING, 1)
@@ -451,6 +474,8 @@ def run_bwd(args, w):
     att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
     if w.window:
         att.set_option(ra.RING_OPT_WINDOW, w.window)
+    if w.doc_len:
+        att.set_segments(w.segments())
     out, lse = att.fwd(q, k, v)
     shape = (w.B, w.H, w.N, w.d)
     dq, dk, dv = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(3))
