@@ -257,20 +257,25 @@ RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, cons
  * from the forward's saved per-row logsumexp).  With P = exp(scale QK^T -
  * lse) over the allowed pairs, D = rowsum(dO * out), dS = P (dO V^T - D):
  *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
- *   q, k, v   natural order [B][H][N][d] bf16 (the forward's inputs)
+ *   q         natural order [B][H][N][d] bf16 (the forward's input)
+ *   k, v      natural order [B][Hkv][N][d] bf16 (Hkv = H unless the handle
+ *             was made by ring_attn_create_gqa)
  *   out, lse  the forward's outputs: [B][H][N][d] and [B][H][N] fp32
  *   dout      the gradient of the loss with respect to out, [B][H][N][d] bf16
- *   dq, dk, dv  outputs, natural order [B][H][N][d] fp32
+ *   dq        output, natural order [B][H][N][d] fp32
+ *   dk, dv    outputs, natural order [B][Hkv][N][d] fp32; with grouped K/V
+ *             heads a shared head's gradient sums the contributions of the
+ *             H/Hkv query heads that read it
  *   workspace ring_attn_bwd_workspace_size() bytes, 256-byte aligned: the
  *             per-row lse and D, shard-major, and two buffers of the
- *             travelling dK/dV accumulators, fp32 [P][B][H][n][d] each
+ *             travelling dK/dV accumulators, fp32 [P][B][Hkv][n][d] each
  * P steps; step s runs two kernels over every shard r and block
  * j = (r - s) mod P: one per 128-key tile of j (dK and dV, the accumulators
  * entering from slot r of one buffer and leaving to slot r + 1 of the other)
  * and one per 128-row query tile of shard r (dQ, kept in dq between steps).
  * K/V blocks are read in place through strided views of k and v.  Layouts
- * CONTIGUOUS and STRIPED, causal or not, with or without RING_OPT_WINDOW;
- * RING_ERR_UNSUPPORTED for ZIGZAG and for grouped K/V heads (Hkv < H).
+ * CONTIGUOUS and STRIPED, causal or not, with or without RING_OPT_WINDOW
+ * and segments; RING_ERR_UNSUPPORTED for ZIGZAG.
  * Pointers 16-byte aligned.  Asynchronous on `stream`. */
 RINGATTN_API int ring_attn_bwd_workspace_size(ring_attn_t h, size_t* bytes);
 RINGATTN_API int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, const float* out,

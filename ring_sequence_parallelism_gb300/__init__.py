@@ -190,20 +190,21 @@ class RingAttention:
     def bwd(self, q, k, v, out, lse, dout, dq=None, dk=None, dv=None, stream=None):
         """Gradients of the forward's loss with respect to q, k, v given dout
         (the gradient at out), from the forward's out and lse.  Returns fp32
-        dq, dk, dv [B, H, N, d] in natural order."""
+        dq [B, H, N, d] and dk, dv [B, Hkv, N, d] in natural order."""
         import torch
 
         shape = (self.B, self.H, self.N, self.d)
-        for t in (q, k, v, dout):
-            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
-                raise ValueError(f"q, k, v, dout must be contiguous CUDA bfloat16 tensors {shape}")
+        kv_shape = (self.B, self.Hkv, self.N, self.d)
+        for t, want in ((q, shape), (k, kv_shape), (v, kv_shape), (dout, shape)):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != want:
+                raise ValueError(f"q, dout must be contiguous CUDA bfloat16 tensors {shape}, k, v {kv_shape}")
         if out.dtype != torch.float32 or tuple(out.shape) != shape or not out.is_contiguous():
             raise ValueError(f"out must be a contiguous float32 tensor {shape}")
         if lse.dtype != torch.float32 or tuple(lse.shape) != shape[:3] or not lse.is_contiguous():
             raise ValueError(f"lse must be a contiguous float32 tensor {shape[:3]}")
         dq = torch.empty(shape, dtype=torch.float32, device=q.device) if dq is None else dq
-        dk = torch.empty(shape, dtype=torch.float32, device=q.device) if dk is None else dk
-        dv = torch.empty(shape, dtype=torch.float32, device=q.device) if dv is None else dv
+        dk = torch.empty(kv_shape, dtype=torch.float32, device=q.device) if dk is None else dk
+        dv = torch.empty(kv_shape, dtype=torch.float32, device=q.device) if dv is None else dv
         need = self.bwd_workspace_size()
         if getattr(self, "_bwd_ws", None) is None or self._bwd_ws.numel() < need:
             self._bwd_ws = torch.empty(need, dtype=torch.uint8, device=q.device)

@@ -659,7 +659,7 @@ static BwdWorkspace bwd_workspace(const Plan& p) {
   const size_t vec = up((size_t)p.B * p.H * p.P * (size_t)w.n_pad * 4);
   w.lse_off = 0;
   w.d_off = vec;
-  w.acc_bytes = up((size_t)p.B * p.H * (size_t)p.N * p.d * 4);
+  w.acc_bytes = up((size_t)p.B * p.Hkv * (size_t)p.N * p.d * 4);  // dK~ or dV~ of the K/V heads
   w.acc_off = 2 * vec;
   w.total = w.acc_off + 4 * w.acc_bytes;
   return w;
@@ -678,7 +678,6 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   const Plan& p = h->plan;
   if (p.layout == RING_LAYOUT_ZIGZAG)
     return fail(RING_ERR_UNSUPPORTED, "the backward supports the contiguous and striped layouts");
-  if (p.Hkv != p.H) return fail(RING_ERR_UNSUPPORTED, "the backward needs one K/V head per query head");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
@@ -701,13 +700,15 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   const cuuint64_t d = (cuuint64_t)p.d, n = (cuuint64_t)p.n, row_b = d * 2;
   CUtensorMap maps[4];
   const void* src[4] = {q, dout, k, v};
+  const int BHkv = p.B * p.Hkv;
   for (int x = 0; x < 4; ++x) {
+    const cuuint64_t heads = (cuuint64_t)(x < 2 ? BH : BHkv);  // q, dout: query heads; k, v: K/V heads
     if (striped) {
-      cuuint64_t dims[4] = {d, (cuuint64_t)P, n, (cuuint64_t)BH};
+      cuuint64_t dims[4] = {d, (cuuint64_t)P, n, heads};
       cuuint64_t str[3] = {row_b, row_b * P, row_b * (cuuint64_t)p.N};
       if ((rc = encode_map(&maps[x], src[x], dims, str, 1, kTileM))) return rc;
     } else {
-      cuuint64_t dims[4] = {d, n, (cuuint64_t)P, (cuuint64_t)BH};
+      cuuint64_t dims[4] = {d, n, (cuuint64_t)P, heads};
       cuuint64_t str[3] = {row_b, row_b * n, row_b * (cuuint64_t)p.N};
       if ((rc = encode_map(&maps[x], src[x], dims, str, kTileM, 1))) return rc;
     }
@@ -735,6 +736,8 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   a.n_pad = w.n_pad;
   a.P = P;
   a.BH = BH;
+  a.BHkv = BHkv;
+  a.G = p.H / p.Hkv;
   a.T = p.T;
   a.KT = p.KT;
   a.q_mode = striped ? kQStriped : kQContiguous;

@@ -260,8 +260,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int kt = blockIdx.x % a.KT;
   const int g = blockIdx.x / a.KT;
-  const int bh = g % a.BH;
-  const int r = g / a.BH;
+  const int kvh = g % a.BHkv;  // the K/V head; its G query heads share the block
+  const int r = g / a.BHkv;
   int j = (r - a.step) % a.P;
   if (j < 0) j += a.P;
   BwdRule rule = bwd_rule(a, r, j);
@@ -292,9 +292,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int half = warp >= 2 ? (warp - 2) >> 2 : 0;
   const long long k_row = k0 + quad * 32 + lane;  // this thread's key
   const bool k_valid = k_row < a.n;
-  const size_t slot_rows = (size_t)a.BH * a.n;
-  const float* in_k = a.acc_in_k + ((size_t)r * slot_rows + (size_t)bh * a.n + (size_t)k_row) * D;
-  const float* in_v = a.acc_in_v + ((size_t)r * slot_rows + (size_t)bh * a.n + (size_t)k_row) * D;
+  const size_t slot_rows = (size_t)a.BHkv * a.n;
+  const float* in_k = a.acc_in_k + ((size_t)r * slot_rows + (size_t)kvh * a.n + (size_t)k_row) * D;
+  const float* in_v = a.acc_in_v + ((size_t)r * slot_rows + (size_t)kvh * a.n + (size_t)k_row) * D;
+  // every query head of the group visits the same query tiles: loop index x
+  // is query head kvh G + x / n_it, query tile it_lo + x % n_it
+  const int n_tot = n_it * a.G;
   const bool load_acc = warp >= 2 && a.accumulate && k_valid;
 
   if (threadIdx.x == 0) {
@@ -306,8 +309,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (n_it > 0) {
       // K and V tiles of block j, then the first query stage
       mbar_expect_tx(bar(L::kBarAB), 2 * L::kTile);
-      load_rows<D>(a, sbase + L::kOffA, &k_map, bar(L::kBarAB), j, (int)k0, bh);
-      load_rows<D>(a, sbase + L::kOffB, &v_map, bar(L::kBarAB), j, (int)k0, bh);
+      load_rows<D>(a, sbase + L::kOffA, &k_map, bar(L::kBarAB), j, (int)k0, kvh);
+      load_rows<D>(a, sbase + L::kOffB, &v_map, bar(L::kBarAB), j, (int)k0, kvh);
     }
   }
   if (warp == 0) {
@@ -324,18 +327,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0 && n_it > 0) {
-      const float* lse_base = a.nlse2 + ((size_t)bh * a.P + r) * a.n_pad;
-      const float* d_base = a.nD + ((size_t)bh * a.P + r) * a.n_pad;
       int issued = 0;
       bool ok = true;
-      for (int x = 0; x < n_it && ok; ++x) {
+      for (int x = 0; x < n_tot && ok; ++x) {
+        const int qh = kvh * a.G + x / n_it;  // query head of this loop index
+        const float* lse_base = a.nlse2 + ((size_t)qh * a.P + r) * a.n_pad;
+        const float* d_base = a.nD + ((size_t)qh * a.P + r) * a.n_pad;
         const int st = x & 1;
         if (x >= 2) ok = mbar_wait(bar(L::kBarEmpty + st), ((x >> 1) - 1) & 1, abort_flag, a, 21);
         if (!ok) break;
-        const int i0 = (it_lo + x) * kTileM;
+        const int i0 = (it_lo + x % n_it) * kTileM;
         mbar_expect_tx(bar(L::kBarFull + st), 2 * L::kTile + 1024);
-        load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &q_map, bar(L::kBarFull + st), r, i0, bh);
-        load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &do_map, bar(L::kBarFull + st), r, i0, bh);
+        load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &q_map, bar(L::kBarFull + st), r, i0, qh);
+        load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &do_map, bar(L::kBarFull + st), r, i0, qh);
         bulk_load(sbase + L::kOffLse + st * 512, lse_base + i0, 512, bar(L::kBarFull + st));
         bulk_load(sbase + L::kOffD + st * 512, d_base + i0, 512, bar(L::kBarFull + st));
         issued = x + 1;
@@ -363,9 +367,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_qk<D>(tmem + L::kTmDP, v_desc, smem_desc(do_s(0), 16, 1024), idesc_s);  // dP^T(0) = V dO^T
         mma_commit_elect(bar(L::kBarDP));
       }
-      for (int x = 0; x < n_it && ok; ++x) {
+      for (int x = 0; x < n_tot && ok; ++x) {
         const uint32_t acc = (x > 0 || a.accumulate) ? 1u : 0u;
-        const bool more = x + 1 < n_it;
+        const bool more = x + 1 < n_tot;
         // dV~ += P^T dO once P^T(x) is in TMEM
         ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 24);
         if (!ok) break;
@@ -435,9 +439,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       i_hi_k = min(i_hi_k, qhi);
     }
     bool ok = true;
-    for (int x = 0; x < n_it; ++x) {
+    for (int x = 0; x < n_tot; ++x) {
       const int st = x & 1;
-      const long long i0 = (long long)(it_lo + x) * kTileM + c0;  // first query of this half
+      const long long i0 = (long long)(it_lo + x % n_it) * kTileM + c0;  // first query of this half
       const float* lse_s = reinterpret_cast<const float*>(smem + L::kOffLse + st * 512) + c0;
       const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512) + c0;
       // the stage's nlse2 and D landed (TMA writes are visible to the threads
@@ -529,12 +533,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       float* dst_v;
       float* dst_k;
       if (a.last) {
-        const long long gk = nat_row(a, bh, j, k_row);
+        const long long gk = nat_row(a, kvh, j, k_row);
         dst_v = a.dv + gk * D;
         dst_k = a.dk + gk * D;
       } else {
         const int to = r + 1 == a.P ? 0 : r + 1;
-        const size_t off = ((size_t)to * slot_rows + (size_t)bh * a.n + (size_t)k_row) * D;
+        const size_t off = ((size_t)to * slot_rows + (size_t)kvh * a.n + (size_t)k_row) * D;
         dst_v = a.acc_out_v + off;
         dst_k = a.acc_out_k + off;
       }
@@ -685,8 +689,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) break;
         const int k0 = (kt_lo + x) * kTileN;
         mbar_expect_tx(bar(L::kBarFull + st), 2 * L::kTile);
-        load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &k_map, bar(L::kBarFull + st), j, k0, bh);
-        load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &v_map, bar(L::kBarFull + st), j, k0, bh);
+        load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &k_map, bar(L::kBarFull + st), j, k0, bh / a.G);
+        load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &v_map, bar(L::kBarFull + st), j, k0, bh / a.G);
         issued = x + 1;
       }
       const unsigned long long lim = a.wait_limit_ns;
@@ -918,7 +922,7 @@ int launch_bwd_prep(const float* out, const float* lse, const void* dout, float*
 
 int launch_bwd_dkdv(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
                     int d, void* stream) {
-  const int grid = a.KT * a.P * a.BH;
+  const int grid = a.KT * a.P * a.BHkv;
   if (grid <= 0) return 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);

@@ -139,6 +139,7 @@ struct BwdArgs {
   int* err;  // device error words [0] flags, [1] site
   unsigned long long wait_limit_ns;
   int n, n_pad, P, BH, T, KT;
+  int BHkv, G;  // K/V heads, and query heads per K/V head (query head bh reads K/V head bh / G)
   int q_mode;  // kQContiguous or kQStriped: Q, dO, K and V through the same shard view
   int causal, layout, step;
   int accumulate;  // step > 0: continue the accumulators

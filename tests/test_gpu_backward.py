@@ -155,3 +155,30 @@ def test_bwd_128k_sampled(orc):
     rq, rk, rv = orc.dense_bwd_rows(sel(q), sel(k), sel(v), sel(do), True, qrows, krows)
     got = (dq[heads][:, qrows].numpy(), dk[heads][:, krows].numpy(), dv[heads][:, krows].numpy())
     check_grads("bwd striped-128k sampled", got, (rq, rk, rv))
+
+
+@pytest.mark.parametrize("layout,window", [("striped", 0), ("contiguous", 0), ("striped", 300)])
+def test_bwd_grouped_query(orc, layout, window):
+    """Grouped-query attention (8 query heads over 2 K/V heads): dQ per
+    query head, and dK, dV per K/V head, which reads as G = 4 query heads'
+    copies of one tensor, so its gradient is the sum of the copies'
+    gradients (the oracle runs on K/V repeated per query head)."""
+    from ring_sequence_parallelism_gb300.inputs import expand_kv
+
+    B, H, Hkv, N, d, P = 1, 8, 2, 2048, 128, 4
+    G = H // Hkv
+    q, k, v = make_qkv(B, H, N, d, seed=660, Hkv=Hkv)
+    do = make_dout(B, H, N, d, seed=660)
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout=layout, kv_heads=Hkv)
+    if window:
+        att.set_option(ra.RING_OPT_WINDOW, window)
+    qc, kc, vc, doc = (x.cuda() for x in (q, k, v, do))
+    out, lse = att.fwd(qc, kc, vc)
+    dq, dk, dv = att.bwd(qc, kc, vc, out, lse, doc)
+    att.check()
+    att.close()
+    flat = lambda t: t.reshape(-1, N, d)
+    rq, rk, rv = orc.dense_bwd(flat(q), flat(expand_kv(k, H)), flat(expand_kv(v, H)), flat(do), True, window=window)
+    rk = rk.reshape(B * Hkv, G, N, d).sum(1)
+    rv = rv.reshape(B * Hkv, G, N, d).sum(1)
+    check_grads(f"bwd gqa {layout} w={window}", [flat(g).cpu().numpy() for g in (dq, dk, dv)], (rq, rk, rv))
