@@ -289,7 +289,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // key-row threads (warps 2..9): lane quadrant warp % 4, column half
   const int quad = warp & 3;
-  const int half = warp >= 2 ? (warp - 2) >> 2 : 0;
   const long long k_row = k0 + quad * 32 + lane;  // this thread's key
   const bool k_valid = k_row < a.n;
   const size_t slot_rows = (size_t)a.BHkv * a.n;
@@ -298,7 +297,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // every query head of the group visits the same query tiles: loop index x
   // is query head kvh G + x / n_it, query tile it_lo + x % n_it
   const int n_tot = n_it * a.G;
+  // Row threads issue the loads of their half of both incoming accumulator
+  // rows now, so the latency overlaps the set-up; the values reach TMEM
+  // after the barrier.
+  constexpr int kHalfD = D / 2;  // accumulator columns this thread loads and stores
+  const int half = warp >= 2 ? (warp - 2) >> 2 : 0;
   const bool load_acc = warp >= 2 && a.accumulate && k_valid;
+  uint32_t acc_in[2 * kHalfD];
+  if (warp >= 2 && a.accumulate) {
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const float* src = (which == 0 ? in_v : in_k) + half * kHalfD;
+#pragma unroll
+      for (int q8 = 0; q8 < kHalfD / 8; ++q8) {
+        if (load_acc) {
+          ld_global_v8(src + q8 * 8, acc_in + which * kHalfD + q8 * 8);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc_in[which * kHalfD + q8 * 8 + e] = 0u;
+        }
+      }
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < L::kNumBars; ++x)
@@ -405,25 +425,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // other's columns (the MMAs read the A operand with a jump at the middle).
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int c0 = half * 64;
-    constexpr int kHalfD = D / 2;  // accumulator columns this thread loads and stores
     // keep both accumulators in TMEM before the first MMA (dV, then dK)
     if (a.accumulate) {
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const float* src = (which == 0 ? in_v : in_k) + half * kHalfD;
         const uint32_t col = (which == 0 ? L::kTmAcc1 : L::kTmAcc2) + half * kHalfD;
 #pragma unroll
         for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t buf[32];
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            if (load_acc) {
-              ld_global_v8(src + c * 32 + q8 * 8, buf + q8 * 8);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) buf[q8 * 8 + e] = 0u;
-            }
-          }
+          for (int e = 0; e < 32; ++e) buf[e] = acc_in[which * kHalfD + c * 32 + e];
           tmem_store32(tmem + lane_off + col + c * 32, buf);
         }
       }
