@@ -274,8 +274,8 @@ RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, cons
  * entering from slot r of one buffer and leaving to slot r + 1 of the other)
  * and one per 128-row query tile of shard r (dQ, kept in dq between steps).
  * K/V blocks are read in place through strided views of k and v.  Layouts
- * CONTIGUOUS and STRIPED, causal or not, with or without RING_OPT_WINDOW
- * and segments; RING_ERR_UNSUPPORTED for ZIGZAG.
+ * CONTIGUOUS, STRIPED and ZIGZAG, causal or not, with or without
+ * RING_OPT_WINDOW and segments (which the zigzag layout does not take).
  * Pointers 16-byte aligned.  Asynchronous on `stream`. */
 RINGATTN_API int ring_attn_bwd_workspace_size(ring_attn_t h, size_t* bytes);
 RINGATTN_API int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, const float* out,

@@ -676,8 +676,6 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   if (!h || !q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
     return fail(RING_ERR_INVALID_ARG, "NULL argument");
   const Plan& p = h->plan;
-  if (p.layout == RING_LAYOUT_ZIGZAG)
-    return fail(RING_ERR_UNSUPPORTED, "the backward supports the contiguous and striped layouts");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
@@ -697,6 +695,7 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
 
   // shard views of the natural-order bf16 tensors (box 64 columns x 128 rows)
   const bool striped = p.layout == RING_LAYOUT_STRIPED;
+  const bool zigzag = p.layout == RING_LAYOUT_ZIGZAG;
   const cuuint64_t d = (cuuint64_t)p.d, n = (cuuint64_t)p.n, row_b = d * 2;
   CUtensorMap maps[4];
   const void* src[4] = {q, dout, k, v};
@@ -707,6 +706,11 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
       cuuint64_t dims[4] = {d, (cuuint64_t)P, n, heads};
       cuuint64_t str[3] = {row_b, row_b * P, row_b * (cuuint64_t)p.N};
       if ((rc = encode_map(&maps[x], src[x], dims, str, 1, kTileM))) return rc;
+    } else if (zigzag) {
+      // chunks of n/2 tokens: dims (d, n/2, 2P, heads)
+      cuuint64_t dims[4] = {d, n / 2, (cuuint64_t)(2 * P), heads};
+      cuuint64_t str[3] = {row_b, row_b * (n / 2), row_b * (cuuint64_t)p.N};
+      if ((rc = encode_map(&maps[x], src[x], dims, str, kTileM, 1))) return rc;
     } else {
       cuuint64_t dims[4] = {d, n, (cuuint64_t)P, heads};
       cuuint64_t str[3] = {row_b, row_b * n, row_b * (cuuint64_t)p.N};
@@ -716,7 +720,8 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   const long long row_r = striped ? 1 : p.n, row_i = striped ? P : 1;
   const bool timing = h->timing != 0;
   if (timing) RA_CUDA(cudaEventRecord(h->tbp0, cs), "cudaEventRecord");
-  RA_CUDA((cudaError_t)launch_bwd_prep(out, lse, dout, nlse2, nD, BH, p.n, w.n_pad, p.d, P, row_r, row_i, p.N, cs),
+  RA_CUDA((cudaError_t)launch_bwd_prep(out, lse, dout, nlse2, nD, BH, p.n, w.n_pad, p.d, P, row_r, row_i, p.N,
+                                       zigzag ? 1 : 0, cs),
           "backward prep launch");
   if (timing) RA_CUDA(cudaEventRecord(h->tbp1, cs), "cudaEventRecord");
   BwdArgs a;
@@ -740,7 +745,7 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   a.G = p.H / p.Hkv;
   a.T = p.T;
   a.KT = p.KT;
-  a.q_mode = striped ? kQStriped : kQContiguous;
+  a.q_mode = striped ? kQStriped : (zigzag ? kQZigzag : kQContiguous);
   a.causal = p.causal;
   a.layout = p.layout;
   a.window = p.window;

@@ -130,6 +130,7 @@ __device__ __forceinline__ void mma_pv_split(uint32_t d_tmem, uint32_t a_tmem, u
 // Causal: pos_k <= pos_q.  Window W: pos_q - pos_k < W.
 struct BwdRule {
   long long dhi, dlo, kmax;  // kmax: last key that can be allowed (n - 1, or -1 for none)
+  long long dhi1, kmax1;     // zigzag: the rule of the shard's late chunk (rows i >= n/2)
 };
 
 __device__ __forceinline__ long long floor_div_ll(long long x, long long q) {
@@ -138,10 +139,24 @@ __device__ __forceinline__ long long floor_div_ll(long long x, long long q) {
 
 __device__ __forceinline__ BwdRule bwd_rule(const BwdArgs& a, int r, int j) {
   BwdRule w;
-  w.kmax = a.n - 1;
-  w.dhi = kFar;
+  w.kmax = w.kmax1 = a.n - 1;
+  w.dhi = w.dhi1 = kFar;
   w.dlo = -kFar;
   if (!a.causal) return w;
+  if (a.layout == RING_LAYOUT_ZIGZAG) {
+    // chunks of c = n/2: shard r holds chunk r, then chunk 2P-1-r.  j < r:
+    // both halves see block j's early chunk entirely; j = r: k - i <= 0;
+    // j > r: the early rows see nothing, the late rows every key.
+    const long long c = a.n / 2;
+    if (j < r) {
+      w.kmax = w.kmax1 = c - 1;
+    } else if (j == r) {
+      w.dhi = w.dhi1 = 0;
+    } else {
+      w.kmax = -1;
+    }
+    return w;
+  }
   if (a.layout == RING_LAYOUT_STRIPED) {
     w.dhi = j <= r ? 0 : -1;
     if (a.window > 0) w.dlo = floor_div_ll((long long)(r - j) - a.window, a.P) + 1;
@@ -170,8 +185,39 @@ __device__ __forceinline__ void doc_range(const BwdArgs& a, int sh, int other, l
   }
 }
 
+// Zigzag: the query rows of shard r that key k of block j meets, as one
+// range [lo, hi] (lo > hi: none).  Half h of the shard (rows [h c, (h+1) c),
+// c = n/2) follows (kmax_h, dhi_h): row i allowed iff k <= kmax_h and
+// i >= k - dhi_h.  Under the zigzag rules the two halves' ranges join
+// without a gap (j < r: every row; j = r: rows >= k; j > r: the late half).
+__device__ __forceinline__ void zig_query_range(const BwdArgs& a, const BwdRule& w, long long k, long long& lo,
+                                                long long& hi) {
+  const long long c = a.n / 2;
+  lo = a.n;
+  hi = -1;
+  if (k <= w.kmax) {
+    const long long s0 = max(0LL, k - w.dhi);
+    if (s0 <= c - 1) {
+      lo = s0;
+      hi = c - 1;
+    }
+  }
+  if (k <= w.kmax1) {
+    const long long s1 = max(c, k - w.dhi1);
+    if (s1 <= (long long)a.n - 1) {
+      lo = min(lo, s1);
+      hi = (long long)a.n - 1;
+    }
+  }
+}
+
 // Row of (shard r, local i) of head bh in a natural-order tensor.
 __device__ __forceinline__ long long nat_row(const BwdArgs& a, int bh, int r, long long i) {
+  if (a.layout == RING_LAYOUT_ZIGZAG) {
+    const long long c = a.n / 2;
+    const long long pos = i < c ? (long long)r * c + i : (long long)(2 * a.P - 1 - r) * c + (i - c);
+    return (long long)bh * a.N + pos;
+  }
   return (long long)bh * a.N + (long long)r * a.row_r + i * a.row_i;
 }
 
@@ -183,10 +229,15 @@ __device__ __forceinline__ void load_rows(const BwdArgs& a, uint32_t dst, const 
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
     const uint32_t to = dst + c * (kTileM * 128);
-    if (a.q_mode == kQStriped)
+    if (a.q_mode == kQStriped) {
       tma_load_4d(to, map, bar, c * 64, sh, i0, bh);
-    else
+    } else if (a.q_mode == kQZigzag) {
+      // map dims (d, n/2, 2P chunks, heads): rows of chunk sh, then 2P-1-sh
+      const int half_n = a.n / 2;
+      tma_load_4d(to, map, bar, c * 64, i0 < half_n ? i0 : i0 - half_n, i0 < half_n ? sh : 2 * a.P - 1 - sh, bh);
+    } else {
       tma_load_4d(to, map, bar, c * 64, i0, sh, bh);
+    }
   }
 }
 
@@ -199,7 +250,7 @@ __device__ __forceinline__ void load_rows(const BwdArgs& a, uint32_t dst, const 
 __global__ void bwd_prep_kernel(const float* __restrict__ out, const float* __restrict__ lse,
                                 const __nv_bfloat16* __restrict__ dout, float* __restrict__ nlse2,
                                 float* __restrict__ nD, int BH, long long n, int n_pad, int d, int P,
-                                long long row_r, long long row_i, long long N) {
+                                long long row_r, long long row_i, long long N, int zigzag) {
   const long long rows = (long long)BH * P * n_pad;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gid / 8;
@@ -212,7 +263,10 @@ __global__ void bwd_prep_kernel(const float* __restrict__ out, const float* __re
   float acc = 0.0f;
   float l2 = 0.0f;
   if (i < n) {
-    const long long g = (long long)bh * N + (long long)r * row_r + i * row_i;
+    const long long c = n / 2;
+    const long long pos = !zigzag ? (long long)r * row_r + i * row_i
+                                  : (i < c ? (long long)r * c + i : (long long)(2 * P - 1 - r) * c + (i - c));
+    const long long g = (long long)bh * N + pos;
     const int cols = d / 8;
     const float* o = out + g * d + part * cols;
     const __nv_bfloat16* x = dout + g * d + part * cols;
@@ -268,11 +322,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (!kWin) rule.dlo = -kFar;
   // query tiles that see a key of this tile
   const long long k0 = (long long)kt * kTileN;
-  const long long k1 = min(k0 + kTileN - 1, rule.kmax);
+  // last key of the tile that any row can see (zigzag: either half's rule)
+  const long long k1 = min(k0 + kTileN - 1, a.layout == RING_LAYOUT_ZIGZAG ? max(rule.kmax, rule.kmax1) : rule.kmax);
   int it_lo = 0, n_it = 0;
   if (k0 <= k1) {
     long long i_lo = max(0LL, k0 - rule.dhi);
     long long i_hi = min((long long)a.n - 1, k1 - rule.dlo);
+    if (a.layout == RING_LAYOUT_ZIGZAG) {
+      // (the chunk size is a multiple of the tile: a key tile is in one chunk)
+      long long lo1, hi1;
+      zig_query_range(a, rule, k0, i_lo, i_hi);
+      zig_query_range(a, rule, k1, lo1, hi1);
+      i_hi = max(i_hi, hi1);
+    }
     if (kWin && a.seg_lo) {
       // queries in the documents of the tile's first and last keys
       long long lo0, hi0, lo1, hi1;
@@ -443,6 +505,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // this key's allowed queries: i_lo_k <= i <= i_hi_k
     long long i_lo_k = k_row <= rule.kmax ? max(0LL, k_row - rule.dhi) : (long long)a.n;
     long long i_hi_k = min((long long)a.n - 1, k_row - rule.dlo);
+    if (a.layout == RING_LAYOUT_ZIGZAG) zig_query_range(a, rule, k_row, i_lo_k, i_hi_k);
     if (kWin && a.seg_lo && k_row <= rule.kmax) {
       long long qlo, qhi;
       doc_range(a, j, r, k_row, qlo, qhi);
@@ -615,6 +678,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (j < 0) j += a.P;
   BwdRule rule = bwd_rule(a, r, j);
   if (!kWin) rule.dlo = -kFar;
+  if (a.layout == RING_LAYOUT_ZIGZAG && (long long)t * kTileM >= a.n / 2) {
+    // a zigzag tile lies in one chunk; the late chunk has its own rule
+    rule.kmax = rule.kmax1;
+    rule.dhi = rule.dhi1;
+  }
   // key tiles with an allowed key for a row of this tile
   const long long i0 = (long long)t * kTileM;
   const long long i1 = min(i0 + kTileM - 1, (long long)a.n - 1);
@@ -921,13 +989,13 @@ int prepare_backward_kernels() {
 
 int launch_bwd_prep(const float* out, const float* lse, const void* dout, float* nlse2, float* nD, int BH,
                     long long n, int n_pad, int d, int P, long long row_r, long long row_i, long long N,
-                    void* stream) {
+                    int zigzag, void* stream) {
   const long long threads = (long long)BH * P * n_pad * 8;
   const int block = 256;
   const long long grid = (threads + block - 1) / block;
   if (grid <= 0) return 0;
   bwd_prep_kernel<<<(unsigned)grid, block, 0, static_cast<cudaStream_t>(stream)>>>(
-      out, lse, static_cast<const __nv_bfloat16*>(dout), nlse2, nD, BH, n, n_pad, d, P, row_r, row_i, N);
+      out, lse, static_cast<const __nv_bfloat16*>(dout), nlse2, nD, BH, n, n_pad, d, P, row_r, row_i, N, zigzag);
   return (int)cudaGetLastError();
 }
 

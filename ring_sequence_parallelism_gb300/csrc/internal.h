@@ -140,7 +140,7 @@ struct BwdArgs {
   unsigned long long wait_limit_ns;
   int n, n_pad, P, BH, T, KT;
   int BHkv, G;  // K/V heads, and query heads per K/V head (query head bh reads K/V head bh / G)
-  int q_mode;  // kQContiguous or kQStriped: Q, dO, K and V through the same shard view
+  int q_mode;  // kQContiguous, kQStriped or kQZigzag: Q, dO, K and V through the same shard view
   int causal, layout, step;
   int accumulate;  // step > 0: continue the accumulators
   int last;        // step P - 1: write the gradients
@@ -188,7 +188,7 @@ int prepare_block_partial_kernels();
 // bf16 tensors (box 64 x 128 rows), coordinates as for kQContiguous/kQStriped.
 int launch_bwd_prep(const float* out, const float* lse, const void* dout, float* nlse2, float* nD, int BH,
                     long long n, int n_pad, int d, int P, long long row_r, long long row_i, long long N,
-                    void* stream);
+                    int zigzag, void* stream);
 int launch_bwd_dkdv(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
                     int d, void* stream);
 int launch_bwd_dq(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,

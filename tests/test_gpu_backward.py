@@ -182,3 +182,28 @@ def test_bwd_grouped_query(orc, layout, window):
     rk = rk.reshape(B * Hkv, G, N, d).sum(1)
     rv = rv.reshape(B * Hkv, G, N, d).sum(1)
     check_grads(f"bwd gqa {layout} w={window}", [flat(g).cpu().numpy() for g in (dq, dk, dv)], (rq, rk, rv))
+
+
+@pytest.mark.parametrize("P,causal", [(4, True), (2, True), (4, False), (1, True)])
+def test_bwd_zigzag(orc, P, causal):
+    """The zigzag layout (2P chunks, shard r holding chunks r and 2P-1-r):
+    every gradient element against the oracle."""
+    B, H, d = 1, 2, 128
+    N = 2 * P * 256  # chunks of 256 tokens
+    q, k, v = make_qkv(B, H, N, d, seed=670 + P)
+    do = make_dout(B, H, N, d, seed=670 + P)
+    got = gpu_fwd_bwd(B, H, N, d, P, causal, "zigzag", q, k, v, do)
+    flat = lambda t: t.reshape(B * H, N, d)
+    ref = orc.dense_bwd(flat(q), flat(k), flat(v), flat(do), causal)
+    check_grads(f"bwd zigzag P={P} causal={causal}", [flat(g).numpy() for g in got], ref)
+
+
+def test_bwd_zigzag_8k(orc):
+    """The 8K workload in the zigzag layout, in full."""
+    w = WORKLOADS["zigzag-8k"]
+    q, k, v = make_workload(w)
+    do = make_dout(w.B, w.H, w.N, w.d, w.seed)
+    got = gpu_fwd_bwd(w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v, do)
+    flat = lambda t: t.reshape(w.B * w.H, w.N, w.d)
+    ref = orc.dense_bwd(flat(q), flat(k), flat(v), flat(do), w.causal)
+    check_grads("bwd zigzag-8k", [flat(g).numpy() for g in got], ref)
