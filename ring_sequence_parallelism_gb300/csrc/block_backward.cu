@@ -520,8 +520,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512) + c0;
       // the stage's nlse2 and D landed (TMA writes are visible to the threads
       // that observe this barrier), then S^T(x) is in TMEM
-      ok = warp_wait(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30) &&
-           warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 27);
+      ok = warp_wait(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30);
+      if (!ok) break;
+      // the first 32 of this half's 64 values of -lse log2(e), read while
+      // S^T(x) is computed (all 64 would not fit the register budget)
+      float4 nl[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) nl[e4] = reinterpret_cast<const float4*>(lse_s)[e4];
+      ok = warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 27);
       if (!ok) break;
       tc_fence_after();
       float p[64];
@@ -535,15 +541,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P^T = exp2(S^T scale log2(e) + nlse2): one packed FMA and two MUFU
       // ex2 per column pair; bf16 pairs over the first 32 columns of the half
       {
-        const float4* nl4 = reinterpret_cast<const float4*>(lse_s);
         const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
         uint32_t pb[32];
 #pragma unroll
+        for (int e4 = 8; e4 < 16; ++e4) nl[e4] = reinterpret_cast<const float4*>(lse_s)[e4];
+#pragma unroll
         for (int e4 = 0; e4 < 16; ++e4) {
-          const float4 nl = nl4[e4];
           float v0, v1, v2, v3;
-          unf2(ffma2(f2(p[4 * e4], p[4 * e4 + 1]), sc2, f2(nl.x, nl.y)), v0, v1);
-          unf2(ffma2(f2(p[4 * e4 + 2], p[4 * e4 + 3]), sc2, f2(nl.z, nl.w)), v2, v3);
+          unf2(ffma2(f2(p[4 * e4], p[4 * e4 + 1]), sc2, f2(nl[e4].x, nl[e4].y)), v0, v1);
+          unf2(ffma2(f2(p[4 * e4 + 2], p[4 * e4 + 3]), sc2, f2(nl[e4].z, nl[e4].w)), v2, v3);
           p[4 * e4] = fast_exp2(v0);
           p[4 * e4 + 1] = fast_exp2(v1);
           p[4 * e4 + 2] = fast_exp2(v2);
@@ -565,15 +571,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_store_wait();
       tc_fence_before();
       mbar_arrive(bar(L::kBarP));
-      // dS^T = P^T (dP^T - D), 32 columns at a time, bf16 over the read columns
+      // dS^T = P^T (dP^T - D), 32 columns at a time, bf16 over the read
+      // columns; the first 32 values of -D are read while dP^T(x) finishes
+      float4 nd4[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) nd4[e4] = reinterpret_cast<const float4*>(d_s)[e4];
       ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 28);
       if (!ok) break;
       tc_fence_after();
-      const float4* nd4 = reinterpret_cast<const float4*>(d_s);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t t[32];
         tmem_load32(tmem + lane_off + L::kTmDP + c0 + c * 32, t);
+        if (c == 0) {
+#pragma unroll
+          for (int e4 = 8; e4 < 16; ++e4) nd4[e4] = reinterpret_cast<const float4*>(d_s)[e4];
+        }
         uint32_t sb[16];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
