@@ -123,6 +123,39 @@ __device__ __forceinline__ void mma_pv_split(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Shared memory of the dQ kernel: Q and dO stationary, then separate rings
+// for K (3 stages: a K tile serves S(x) and, at the end of the tile, dQ(x))
+// and V (2 stages: a V tile serves dP(x) only), so the load of a K tile has
+// about two tile periods to land; 224 KB at d = 128.
+template <int D>
+struct DqLayout {
+  static constexpr int kTile = kTileM * D * 2;
+  static constexpr int kKStages = 3, kVStages = 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kTile;
+  static constexpr int kOffK = 2 * kTile;
+  static constexpr int kOffV = kOffK + kKStages * kTile;
+  static constexpr int kOffBar = kOffV + kVStages * kTile;
+  static constexpr int kBarAB = 0;                         // Q and dO landed
+  static constexpr int kBarKFull = 1;                      // [3]
+  static constexpr int kBarKEmpty = kBarKFull + kKStages;  // [3]
+  static constexpr int kBarVFull = kBarKEmpty + kKStages;  // [2]
+  static constexpr int kBarVEmpty = kBarVFull + kVStages;  // [2]
+  static constexpr int kBarS = kBarVEmpty + kVStages;
+  static constexpr int kBarDP = kBarS + 1;
+  static constexpr int kBarP = kBarDP + 1;   // S read, 256 arrivals
+  static constexpr int kBarDS = kBarP + 1;   // dS in TMEM, 256 arrivals
+  static constexpr int kBarAcc = kBarDS + 1;
+  static constexpr int kBarDrain = kBarAcc + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr bool row_barrier(int x) { return x == kBarP || x == kBarDS; }
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kBytes = kOffAbort + 4;
+  static constexpr int kAlloc = (kBytes + 1024) > 122880 ? (kBytes + 1024) : 122880;
+  static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc1 = 256;
+};
+
 // Mask of block (shard r, block j) for the contiguous and striped layouts:
 // local query i and local key k form an allowed pair iff
 //   dlo <= k - i <= dhi  and  k < klim.
@@ -672,7 +705,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap do_map, const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map) {
-  using L = BwdLayout<D>;
+  using L = DqLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -749,14 +782,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < L::kNumBars; ++x)
-      mbar_init(bar(x), (x == L::kBarP || x == L::kBarDS) ? 256 : 1);
+      mbar_init(bar(x), L::row_barrier(x) ? 256 : 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
     if (n_kt > 0) {
       mbar_expect_tx(bar(L::kBarAB), 2 * L::kTile);
-      load_rows<D>(a, sbase + L::kOffA, &q_map, bar(L::kBarAB), r, (int)i0, bh);
-      load_rows<D>(a, sbase + L::kOffB, &do_map, bar(L::kBarAB), r, (int)i0, bh);
+      load_rows<D>(a, sbase + L::kOffQ, &q_map, bar(L::kBarAB), r, (int)i0, bh);
+      load_rows<D>(a, sbase + L::kOffDO, &do_map, bar(L::kBarAB), r, (int)i0, bh);
     }
   }
   if (warp == 0) {
@@ -773,46 +806,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0 && n_kt > 0) {
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int x = 0; x < n_kt && ok; ++x) {
-        const int st = x & 1;
-        if (x >= 2) ok = mbar_wait(bar(L::kBarEmpty + st), ((x >> 1) - 1) & 1, abort_flag, a, 31);
-        if (!ok) break;
         const int k0 = (kt_lo + x) * kTileN;
-        mbar_expect_tx(bar(L::kBarFull + st), 2 * L::kTile);
-        load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &k_map, bar(L::kBarFull + st), j, k0, bh / a.G);
-        load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &v_map, bar(L::kBarFull + st), j, k0, bh / a.G);
-        issued = x + 1;
+        const int ks = x % L::kKStages, vs = x % L::kVStages;
+        // K(x) into its stage once dQ(x - 3) has released it
+        if (x >= L::kKStages)
+          ok = mbar_wait(bar(L::kBarKEmpty + ks), ((x / L::kKStages) - 1) & 1, abort_flag, a, 31);
+        if (!ok) break;
+        mbar_expect_tx(bar(L::kBarKFull + ks), L::kTile);
+        load_rows<D>(a, sbase + L::kOffK + ks * L::kTile, &k_map, bar(L::kBarKFull + ks), j, k0, bh / a.G);
+        k_issued = x + 1;
+        // V(x) once dP(x - 2) has released its stage
+        if (x >= L::kVStages)
+          ok = mbar_wait(bar(L::kBarVEmpty + vs), ((x / L::kVStages) - 1) & 1, abort_flag, a, 41);
+        if (!ok) break;
+        mbar_expect_tx(bar(L::kBarVFull + vs), L::kTile);
+        load_rows<D>(a, sbase + L::kOffV + vs * L::kTile, &v_map, bar(L::kBarVFull + vs), j, k0, bh / a.G);
+        v_issued = x + 1;
       }
       const unsigned long long lim = a.wait_limit_ns;
       mbar_drain_wait(bar(L::kBarAB), 0, lim);
-      for (int x = issued > 2 ? issued - 2 : 0; x < issued; ++x)
-        mbar_drain_wait(bar(L::kBarFull + (x & 1)), (x >> 1) & 1, lim);
+      for (int x = k_issued > L::kKStages ? k_issued - L::kKStages : 0; x < k_issued; ++x)
+        mbar_drain_wait(bar(L::kBarKFull + x % L::kKStages), (x / L::kKStages) & 1, lim);
+      for (int x = v_issued > L::kVStages ? v_issued - L::kVStages : 0; x < v_issued; ++x)
+        mbar_drain_wait(bar(L::kBarVFull + x % L::kVStages), (x / L::kVStages) & 1, lim);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (n_kt > 0) {
       constexpr uint32_t idesc_s = instr_desc(kTileM, kTileN, false);
       constexpr uint32_t idesc_acc = instr_desc(kTileM, D, true);
-      const uint64_t q_desc = smem_desc(sbase + L::kOffA, 16, 1024);
-      const uint64_t do_desc = smem_desc(sbase + L::kOffB, 16, 1024);
-      auto k_s = [&](int x) { return sbase + L::kOffX + (x & 1) * L::kTile; };
-      auto v_s = [&](int x) { return sbase + L::kOffY + (x & 1) * L::kTile; };
-      bool ok = warp_wait(bar(L::kBarAB), 0, abort_flag, a, 32) &&
-                warp_wait(bar(L::kBarFull), 0, abort_flag, a, 33);
+      const uint64_t q_desc = smem_desc(sbase + L::kOffQ, 16, 1024);
+      const uint64_t do_desc = smem_desc(sbase + L::kOffDO, 16, 1024);
+      auto k_s = [&](int x) { return sbase + L::kOffK + (x % L::kKStages) * L::kTile; };
+      auto v_s = [&](int x) { return sbase + L::kOffV + (x % L::kVStages) * L::kTile; };
+      auto k_full = [&](int x, int site) {
+        return warp_wait(bar(L::kBarKFull + x % L::kKStages), (x / L::kKStages) & 1, abort_flag, a, site);
+      };
+      auto v_full = [&](int x, int site) {
+        return warp_wait(bar(L::kBarVFull + x % L::kVStages), (x / L::kVStages) & 1, abort_flag, a, site);
+      };
+      bool ok = warp_wait(bar(L::kBarAB), 0, abort_flag, a, 32) && k_full(0, 33);
       if (ok) {
         mma_qk<D>(tmem + L::kTmS, q_desc, smem_desc(k_s(0), 16, 1024), idesc_s);  // S(0) = Q K^T
         mma_commit_elect(bar(L::kBarS));
+        ok = v_full(0, 42);
+      }
+      if (ok) {
         mma_qk<D>(tmem + L::kTmDP, do_desc, smem_desc(v_s(0), 16, 1024), idesc_s);  // dP(0) = dO V^T
         mma_commit_elect(bar(L::kBarDP));
+        mma_commit_elect(bar(L::kBarVEmpty));  // V(0) served its only MMA
       }
       for (int x = 0; x < n_kt && ok; ++x) {
         const bool more = x + 1 < n_kt;
         // S(x+1) may overwrite S(x) once the row threads have read it
         if (more) {
-          ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 34) &&
-               warp_wait(bar(L::kBarFull + ((x + 1) & 1)), ((x + 1) >> 1) & 1, abort_flag, a, 35);
+          ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 34) && k_full(x + 1, 35);
           if (!ok) break;
           tc_fence_after();
           mma_qk<D>(tmem + L::kTmS, q_desc, smem_desc(k_s(x + 1), 16, 1024), idesc_s);
@@ -824,10 +875,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         mma_pv_split(tmem + L::kTmAcc1, tmem + L::kTmDP, smem_desc(k_s(x), kTileN * 128, 1024), idesc_acc,
                      (x > 0 || a.accumulate) ? 1u : 0u);
-        mma_commit_elect(bar(L::kBarEmpty + (x & 1)));
+        mma_commit_elect(bar(L::kBarKEmpty + x % L::kKStages));  // K(x) served S(x) and dQ(x)
         if (more) {
+          ok = v_full(x + 1, 43);
+          if (!ok) break;
           mma_qk<D>(tmem + L::kTmDP, do_desc, smem_desc(v_s(x + 1), 16, 1024), idesc_s);
           mma_commit_elect(bar(L::kBarDP));
+          mma_commit_elect(bar(L::kBarVEmpty + (x + 1) % L::kVStages));
         }
       }
       if (ok) mma_commit_elect(bar(L::kBarAcc));
@@ -986,10 +1040,10 @@ int prepare_bwd_one() {
                                      BwdLayout<D>::kAlloc)))
     return e;
   if ((e = (int)cudaFuncSetAttribute(bwd_dq_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     BwdLayout<D>::kAlloc)))
+                                     DqLayout<D>::kAlloc)))
     return e;
   return (int)cudaFuncSetAttribute(bwd_dq_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   BwdLayout<D>::kAlloc);
+                                   DqLayout<D>::kAlloc);
 }
 
 }  // namespace
@@ -1043,11 +1097,11 @@ int launch_bwd_dq(const BwdArgs& a, const void* q_map, const void* do_map, const
   const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
   const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
   if (d == 64) {
-    if (win) bwd_dq_kernel<64, true><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
-    else bwd_dq_kernel<64, false><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
+    if (win) bwd_dq_kernel<64, true><<<grid, kBwdThreads, DqLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
+    else bwd_dq_kernel<64, false><<<grid, kBwdThreads, DqLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
   } else {
-    if (win) bwd_dq_kernel<128, true><<<grid, kBwdThreads, BwdLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
-    else bwd_dq_kernel<128, false><<<grid, kBwdThreads, BwdLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
+    if (win) bwd_dq_kernel<128, true><<<grid, kBwdThreads, DqLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
+    else bwd_dq_kernel<128, false><<<grid, kBwdThreads, DqLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
   }
   return (int)cudaGetLastError();
 }
