@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--bwd", action="store_true", help="time the ring backward (ring_attn_bwd) instead")
+    ap.add_argument("--bwd-per-step", action="store_true",
+                    help="with --bwd: one dK/dV and one dQ launch per ring step (RING_OPT_BWD_LAP 0) instead "
+                         "of one launch per kernel for the whole ring")
     ap.add_argument("--decode", type=int, default=0, metavar="LQ",
                     help="measure split-K/V decode of LQ new queries over the workload's K/V cache instead")
     return ap.parse_args()
@@ -477,8 +480,11 @@ def run_bwd(args, w):
     if w.doc_len:
         att.set_segments(w.segments())
     out, lse = att.fwd(q, k, v)
+    lap = not args.bwd_per_step and w.P > 1
+    att.set_option(ra.RING_OPT_BWD_LAP, 0 if args.bwd_per_step else 1)
     shape = (w.B, w.H, w.N, w.d)
-    dq, dk, dv = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(3))
+    dq = torch.empty(shape, dtype=torch.float32, device="cuda")
+    dk, dv = (torch.empty((w.B, att.Hkv, w.N, w.d), dtype=torch.float32, device="cuda") for _ in range(2))
     att.set_option(ra.RING_OPT_TIMING, 1)
     for _ in range(args.warmup):
         att.bwd(q, k, v, out, lse, do, dq, dk, dv)
@@ -509,17 +515,20 @@ def run_bwd(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
         "data": "synthetic", "config": dict(config_of(w), dout="N(0,1) bf16, seed + 7"),
         "tokens_per_s": w.B * w.N / (ms * 1e-3),
-        "roofline": {"bound": "tensor", "kernel": "bwd_dkdv_kernel<128> (one launch per ring step)",
+        "schedule": "lap (one launch per kernel)" if lap else "per step",
+        "roofline": {"bound": "tensor",
+                     "kernel": "bwd_dkdv_kernel<128> " + ("(one launch for the ring)" if lap else
+                                                          "(one launch per ring step)"),
                      "achieved": ach_dkdv, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach_dkdv / peak_sus,
                      "peak_kind": f"bf16_tflops_sustained ({pk_kind})",
-                     "traffic": traffic_for(f"{w.name}:bwd_dkdv", BWD_SOURCE),
+                     "traffic": traffic_for(f"{w.name}:bwd_dkdv" + (":lap" if lap else ""), BWD_SOURCE),
                      "algorithmic": "8*d FLOPs per allowed pair (S^T, dP^T, dV, dK)"},
         "dq_kernel": {"achieved": ach_dq, "frac": ach_dq / peak_sus,
                       "algorithmic": "6*d FLOPs per allowed pair (S, dP, dQ)"},
         "bwd": {"dkdv_ms": t["dkdv_ms"], "dq_ms": t["dq_ms"], "prep_ms": t["prep_ms"],
                 "kernel_ms_total": dkdv_ms + dq_ms + t["prep_ms"]},
         "clocks": clocks.summary(),
-        "gpu_launches": args.steps * (1 + 2 * w.P),
+        "gpu_launches": args.steps * (1 + (2 if lap else 2 * w.P)),
     }
     print(json.dumps(line), flush=True)
     att.close()

@@ -125,7 +125,20 @@ typedef enum {
    * the planner queries and ring_attn_decode.  Rebuilds the plan; needs the
    * causal mask and the CONTIGUOUS or STRIPED layout (RING_ERR_UNSUPPORTED
    * otherwise, the handle keeping its previous window). */
-  RING_OPT_WINDOW = 4
+  RING_OPT_WINDOW = 4,
+  /* How ring_attn_bwd schedules the ring ([RA-CN] "Backward 需要让梯度也沿环传播"
+   * has each block's dK/dV accumulators travel with it around the ring).
+   * 0: one dK/dV and one dQ launch per ring step; the travelling
+   *   accumulators pass between steps through the workspace buffers.
+   * 1 (default): one launch of each kernel for the whole ring: a CTA owning a key
+   *   tile of block j visits shards j, j+1, .. in step order, and a CTA
+   *   owning a query tile of shard r visits blocks r, r-1, .., with the
+   *   accumulators held in tensor memory from the first visit to the last
+   *   (the accumulator buffers are not used).  The MMAs run in the same
+   *   order on the same fp32 values as in mode 0, so the results are
+   *   identical.  ring_attn_get_bwd_timing then reports both kernels' times
+   *   in entry 0 and zeros in the others. */
+  RING_OPT_BWD_LAP = 5
 } ring_option_t;
 
 /* Create a handle for one problem shape.  Validates the shape and builds the
@@ -267,12 +280,17 @@ RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, cons
  *             heads a shared head's gradient sums the contributions of the
  *             H/Hkv query heads that read it
  *   workspace ring_attn_bwd_workspace_size() bytes, 256-byte aligned: the
- *             per-row lse and D, shard-major, and two buffers of the
- *             travelling dK/dV accumulators, fp32 [P][B][Hkv][n][d] each
- * P steps; step s runs two kernels over every shard r and block
- * j = (r - s) mod P: one per 128-key tile of j (dK and dV, the accumulators
- * entering from slot r of one buffer and leaving to slot r + 1 of the other)
- * and one per 128-row query tile of shard r (dQ, kept in dq between steps).
+ *             per-row lse and D, shard-major; with RING_OPT_BWD_LAP 0 and
+ *             P > 1 also two buffers of the travelling dK/dV accumulators,
+ *             fp32 [P][B][Hkv][n][d] each.  The size depends on that option:
+ *             query it after setting the option.
+ * The ring: at step s every shard r meets block j = (r - s) mod P.  Two
+ * kernels cover it: one per 128-key tile of a block (dK and dV) and one per
+ * 128-row query tile of a shard (dQ).  RING_OPT_BWD_LAP 1 (default): one
+ * launch of each, every CTA making its tile's visits in step order with the
+ * accumulators in tensor memory.  RING_OPT_BWD_LAP 0: two launches per step,
+ * the dK/dV accumulators entering from slot r of one buffer and leaving to
+ * slot r + 1 of the other, dQ kept in dq between steps.
  * K/V blocks are read in place through strided views of k and v.  Layouts
  * CONTIGUOUS, STRIPED and ZIGZAG, causal or not, with or without
  * RING_OPT_WINDOW and segments (which the zigzag layout does not take).

@@ -117,6 +117,7 @@ struct ring_attn {
   Plan plan;
   int rotation = 2;
   int timing = 0;
+  int bwd_lap = 1;       // RING_OPT_BWD_LAP
   int debug_drop_v = 0;
   unsigned long long wait_limit_ns = 2000000000ULL;
   // device resources, made on first use
@@ -129,6 +130,7 @@ struct ring_attn {
   std::vector<cudaEvent_t> tbk0, tbk1, tbq0, tbq1;  // backward: dK/dV and dQ kernels per step
   cudaEvent_t tbp0 = nullptr, tbp1 = nullptr;          // backward preprocessing
   bool bwd_timed_valid = false;
+  bool bwd_timed_lap = false;  // the timed backward ran in lap mode (one launch each)
   std::vector<char> copied;  // [s]: the side stream filled slots for step s (timing)
   cudaEvent_t tp0 = nullptr, tp1 = nullptr;
   bool timed_valid = false;
@@ -419,6 +421,10 @@ int ring_attn_set_option(ring_attn_t h, int option, long long value) {
       h->plan = std::move(np);
       return RING_OK;
     }
+    case RING_OPT_BWD_LAP:
+      if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "backward lap must be 0 or 1");
+      h->bwd_lap = (int)value;
+      return RING_OK;
     case RING_OPT_DEBUG_DROP_V_LOADS:
       if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "debug option must be 0 or 1");
       h->debug_drop_v = (int)value;
@@ -647,12 +653,16 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
 
 // ---------------------------------------------------------------- backward
 // Workspace of ring_attn_bwd: -lse*log2(e) and -D shard-major [BH][P][n_pad] fp32,
-// then the dK~ and dV~ accumulator buffers X and Y, [P][BH][n][d] fp32 each.
+// then (one launch per ring step only) the dK~ and dV~ accumulator buffers X
+// and Y, [P][BHkv][n][d] fp32 each.
 struct BwdWorkspace {
   size_t lse_off, d_off, acc_bytes, acc_off, total;
   int n_pad;
 };
-static BwdWorkspace bwd_workspace(const Plan& p) {
+// whether ring_attn_bwd runs one launch per ring step (and so needs the
+// accumulator buffers): RING_OPT_BWD_LAP 0 with more than one shard
+static bool bwd_per_step(const ring_attn* h) { return h->bwd_lap == 0 && h->plan.P > 1; }
+static BwdWorkspace bwd_workspace(const Plan& p, bool per_step) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   BwdWorkspace w;
   w.n_pad = p.T * kTileM;
@@ -661,13 +671,13 @@ static BwdWorkspace bwd_workspace(const Plan& p) {
   w.d_off = vec;
   w.acc_bytes = up((size_t)p.B * p.Hkv * (size_t)p.N * p.d * 4);  // dK~ or dV~ of the K/V heads
   w.acc_off = 2 * vec;
-  w.total = w.acc_off + 4 * w.acc_bytes;
+  w.total = w.acc_off + (per_step ? 4 * w.acc_bytes : 0);
   return w;
 }
 
 int ring_attn_bwd_workspace_size(ring_attn_t h, size_t* bytes) {
   if (!h || !bytes) return fail(RING_ERR_INVALID_ARG, "NULL argument");
-  *bytes = bwd_workspace(h->plan).total;
+  *bytes = bwd_workspace(h->plan, bwd_per_step(h)).total;
   return RING_OK;
 }
 
@@ -685,7 +695,8 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   if (rc) return rc;
   const int P = p.P, BH = p.B * p.H;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const BwdWorkspace w = bwd_workspace(p);
+  const bool lap = !bwd_per_step(h);
+  const BwdWorkspace w = bwd_workspace(p, !lap);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* nlse2 = reinterpret_cast<float*>(ws + w.lse_off);
   float* nD = reinterpret_cast<float*>(ws + w.d_off);
@@ -751,7 +762,20 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   a.window = p.window;
   a.scale = (float)(1.0 / std::sqrt((double)p.d));
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
-  for (int s = 0; s < P; ++s) {
+  if (lap) {
+    // one launch per kernel: each CTA makes its tile's whole lap
+    a.lap = 1;
+    a.step = 0;
+    a.accumulate = 0;
+    a.last = 1;
+    if (timing) RA_CUDA(cudaEventRecord(h->tbk0[0], cs), "cudaEventRecord");
+    RA_CUDA((cudaError_t)launch_bwd_dkdv(a, &maps[0], &maps[1], &maps[2], &maps[3], p.d, cs), "backward dK/dV launch");
+    if (timing) RA_CUDA(cudaEventRecord(h->tbk1[0], cs), "cudaEventRecord");
+    if (timing) RA_CUDA(cudaEventRecord(h->tbq0[0], cs), "cudaEventRecord");
+    RA_CUDA((cudaError_t)launch_bwd_dq(a, &maps[0], &maps[1], &maps[2], &maps[3], p.d, cs), "backward dQ launch");
+    if (timing) RA_CUDA(cudaEventRecord(h->tbq1[0], cs), "cudaEventRecord");
+  }
+  for (int s = 0; s < P && !lap; ++s) {
     const int cur = s & 1;
     a.step = s;
     a.accumulate = s > 0 ? 1 : 0;
@@ -768,6 +792,7 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
     if (timing) RA_CUDA(cudaEventRecord(h->tbq1[s], cs), "cudaEventRecord");
   }
   h->bwd_timed_valid = timing;
+  h->bwd_timed_lap = lap;
   return RING_OK;
 }
 
@@ -776,7 +801,13 @@ int ring_attn_get_bwd_timing(ring_attn_t h, float* dkdv_ms, float* dq_ms, float*
   if (!h->ready || !h->bwd_timed_valid)
     return fail(RING_ERR_INVALID_ARG, "no timed backward (set RING_OPT_TIMING before ring_attn_bwd)");
   const int P = h->plan.P;
+  const int timed = h->bwd_timed_lap ? 1 : P;  // lap mode: one launch each, in entry 0
   for (int s = 0; s < P; ++s) {
+    if (s >= timed) {
+      if (dkdv_ms) dkdv_ms[s] = 0.0f;
+      if (dq_ms) dq_ms[s] = 0.0f;
+      continue;
+    }
     if (dkdv_ms) RA_CUDA(cudaEventElapsedTime(&dkdv_ms[s], h->tbk0[s], h->tbk1[s]), "cudaEventElapsedTime");
     if (dq_ms) RA_CUDA(cudaEventElapsedTime(&dq_ms[s], h->tbq0[s], h->tbq1[s]), "cudaEventElapsedTime");
   }

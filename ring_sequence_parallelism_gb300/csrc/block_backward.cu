@@ -329,7 +329,7 @@ __global__ void bwd_prep_kernel(const float* __restrict__ out, const float* __re
 // head) are consecutive so its Q and dO tiles stay in L2, and within it the
 // key tiles run in ascending order (under the causal mask the early keys of
 // a block meet the most queries).
-template <int D, bool kWin>
+template <int D, bool kWin, bool kLap>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap do_map, const __grid_constant__ CUtensorMap k_map,
@@ -347,39 +347,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int kt = blockIdx.x % a.KT;
   const int g = blockIdx.x / a.KT;
-  const int kvh = g % a.BHkv;  // the K/V head; its G query heads share the block
-  const int r = g / a.BHkv;
-  int j = (r - a.step) % a.P;
+  // the K/V head (its G query heads share the block) and the block.  Lap
+  // launches go head-major: the CTAs resident at one time then share one
+  // head's Q and dO (64 MB at 128K tokens, d = 128), which L2 holds.
+  const int kvh = kLap ? g / a.P : g % a.BHkv;
+  const int gq = kLap ? g % a.P : g / a.BHkv;
+  // Per-step launch: this CTA is shard gq's visit to block (gq - step) mod P.
+  // Lap (kLap): the CTA owns block gq and makes the block's whole lap
+  // itself, visiting shards gq, gq + 1, .. in step order (shard r holds
+  // block j at step (r - j) mod P), with dK~ and dV~ kept in TMEM.
+  const int nvis = kLap ? a.P : 1;
+  int j = kLap ? gq : (gq - a.step) % a.P;
   if (j < 0) j += a.P;
-  BwdRule rule = bwd_rule(a, r, j);
-  if (!kWin) rule.dlo = -kFar;
-  // query tiles that see a key of this tile
+  const int r = gq;  // the shard of visit 0
+  auto visit_r = [&](int s) { return r + s >= a.P ? r + s - a.P : r + s; };
   const long long k0 = (long long)kt * kTileN;
-  // last key of the tile that any row can see (zigzag: either half's rule)
-  const long long k1 = min(k0 + kTileN - 1, a.layout == RING_LAYOUT_ZIGZAG ? max(rule.kmax, rule.kmax1) : rule.kmax);
-  int it_lo = 0, n_it = 0;
-  if (k0 <= k1) {
-    long long i_lo = max(0LL, k0 - rule.dhi);
-    long long i_hi = min((long long)a.n - 1, k1 - rule.dlo);
-    if (a.layout == RING_LAYOUT_ZIGZAG) {
-      // (the chunk size is a multiple of the tile: a key tile is in one chunk)
-      long long lo1, hi1;
-      zig_query_range(a, rule, k0, i_lo, i_hi);
-      zig_query_range(a, rule, k1, lo1, hi1);
-      i_hi = max(i_hi, hi1);
+  // the rule of (shard rv, block j) and the query tiles of shard rv that see
+  // a key of this tile
+  auto range_of = [&](int rv, BwdRule& rule, int& it_lo, int& n_it) {
+    const int r = rv;
+    rule = bwd_rule(a, r, j);
+    if (!kWin) rule.dlo = -kFar;
+    // last key of the tile that any row can see (zigzag: either half's rule)
+    const long long k1 = min(k0 + kTileN - 1, a.layout == RING_LAYOUT_ZIGZAG ? max(rule.kmax, rule.kmax1) : rule.kmax);
+    it_lo = 0;
+    n_it = 0;
+    if (k0 <= k1) {
+      long long i_lo = max(0LL, k0 - rule.dhi);
+      long long i_hi = min((long long)a.n - 1, k1 - rule.dlo);
+      if (a.layout == RING_LAYOUT_ZIGZAG) {
+        // (the chunk size is a multiple of the tile: a key tile is in one chunk)
+        long long lo1, hi1;
+        zig_query_range(a, rule, k0, i_lo, i_hi);
+        zig_query_range(a, rule, k1, lo1, hi1);
+        i_hi = max(i_hi, hi1);
+      }
+      if (kWin && a.seg_lo) {
+        // queries in the documents of the tile's first and last keys
+        long long lo0, hi0, lo1, hi1;
+        doc_range(a, j, r, k0, lo0, hi0);
+        doc_range(a, j, r, k1, lo1, hi1);
+        i_lo = max(i_lo, lo0);
+        i_hi = min(i_hi, hi1);
+      }
+      if (i_lo <= i_hi) {
+        it_lo = (int)(i_lo / kTileM);
+        n_it = (int)(i_hi / kTileM) + 1 - it_lo;
+      }
     }
-    if (kWin && a.seg_lo) {
-      // queries in the documents of the tile's first and last keys
-      long long lo0, hi0, lo1, hi1;
-      doc_range(a, j, r, k0, lo0, hi0);
-      doc_range(a, j, r, k1, lo1, hi1);
-      i_lo = max(i_lo, lo0);
-      i_hi = min(i_hi, hi1);
-    }
-    if (i_lo <= i_hi) {
-      it_lo = (int)(i_lo / kTileM);
-      n_it = (int)(i_hi / kTileM) + 1 - it_lo;
-    }
+  };
+  // visit 0's rule and query tiles (the only visit of a per-step launch)
+  BwdRule rule0;
+  int it_lo0, n_it0;
+  range_of(r, rule0, it_lo0, n_it0);
+  int total = n_it0 * a.G;  // loop indices of all visits (visit s: its query tiles x the G query heads)
+  for (int s = 1; s < nvis; ++s) {
+    BwdRule rl;
+    int lo, cnt;
+    range_of(visit_r(s), rl, lo, cnt);
+    total += cnt * a.G;
   }
 
   // key-row threads (warps 2..9): lane quadrant warp % 4, column half
@@ -389,9 +415,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const size_t slot_rows = (size_t)a.BHkv * a.n;
   const float* in_k = a.acc_in_k + ((size_t)r * slot_rows + (size_t)kvh * a.n + (size_t)k_row) * D;
   const float* in_v = a.acc_in_v + ((size_t)r * slot_rows + (size_t)kvh * a.n + (size_t)k_row) * D;
-  // every query head of the group visits the same query tiles: loop index x
-  // is query head kvh G + x / n_it, query tile it_lo + x % n_it
-  const int n_tot = n_it * a.G;
   // Row threads issue the loads of their half of both incoming accumulator
   // rows now, so the latency overlaps the set-up; the values reach TMEM
   // after the barrier.
@@ -421,7 +444,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
-    if (n_it > 0) {
+    if (total > 0) {
       // K and V tiles of block j, then the first query stage
       mbar_expect_tx(bar(L::kBarAB), 2 * L::kTile);
       load_rows<D>(a, sbase + L::kOffA, &k_map, bar(L::kBarAB), j, (int)k0, kvh);
@@ -441,23 +464,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0 && n_it > 0) {
+    if (lane == 0 && total > 0) {
       int issued = 0;
       bool ok = true;
-      for (int x = 0; x < n_tot && ok; ++x) {
-        const int qh = kvh * a.G + x / n_it;  // query head of this loop index
-        const float* lse_base = a.nlse2 + ((size_t)qh * a.P + r) * a.n_pad;
-        const float* d_base = a.nD + ((size_t)qh * a.P + r) * a.n_pad;
-        const int st = x & 1;
-        if (x >= 2) ok = mbar_wait(bar(L::kBarEmpty + st), ((x >> 1) - 1) & 1, abort_flag, a, 21);
-        if (!ok) break;
-        const int i0 = (it_lo + x % n_it) * kTileM;
-        mbar_expect_tx(bar(L::kBarFull + st), 2 * L::kTile + 1024);
-        load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &q_map, bar(L::kBarFull + st), r, i0, qh);
-        load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &do_map, bar(L::kBarFull + st), r, i0, qh);
-        bulk_load(sbase + L::kOffLse + st * 512, lse_base + i0, 512, bar(L::kBarFull + st));
-        bulk_load(sbase + L::kOffD + st * 512, d_base + i0, 512, bar(L::kBarFull + st));
-        issued = x + 1;
+      int x = 0;  // loop index over all visits
+      for (int s = 0; s < nvis && ok; ++s) {
+        const int rv = visit_r(s);
+        BwdRule rl;
+        int it_lo, n_it;
+        range_of(rv, rl, it_lo, n_it);
+        // every query head of the group visits the same query tiles: local
+        // index xl is query head kvh G + xl / n_it, query tile it_lo + xl % n_it
+        for (int xl = 0; xl < n_it * a.G && ok; ++xl, ++x) {
+          const int qh = kvh * a.G + xl / n_it;
+          const float* lse_base = a.nlse2 + ((size_t)qh * a.P + rv) * a.n_pad;
+          const float* d_base = a.nD + ((size_t)qh * a.P + rv) * a.n_pad;
+          const int st = x & 1;
+          if (x >= 2) ok = mbar_wait(bar(L::kBarEmpty + st), ((x >> 1) - 1) & 1, abort_flag, a, 21);
+          if (!ok) break;
+          const int i0 = (it_lo + xl % n_it) * kTileM;
+          mbar_expect_tx(bar(L::kBarFull + st), 2 * L::kTile + 1024);
+          load_rows<D>(a, sbase + L::kOffX + st * L::kTile, &q_map, bar(L::kBarFull + st), rv, i0, qh);
+          load_rows<D>(a, sbase + L::kOffY + st * L::kTile, &do_map, bar(L::kBarFull + st), rv, i0, qh);
+          bulk_load(sbase + L::kOffLse + st * 512, lse_base + i0, 512, bar(L::kBarFull + st));
+          bulk_load(sbase + L::kOffD + st * 512, d_base + i0, 512, bar(L::kBarFull + st));
+          issued = x + 1;
+        }
       }
       // drain: every load started has landed before the CTA can exit
       const unsigned long long lim = a.wait_limit_ns;
@@ -467,7 +499,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (n_it > 0) {
+    if (total > 0) {
       constexpr uint32_t idesc_s = instr_desc(kTileM, kTileN, false);
       constexpr uint32_t idesc_acc = instr_desc(kTileM, D, true);
       const uint64_t k_desc = smem_desc(sbase + L::kOffA, 16, 1024);
@@ -482,9 +514,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_qk<D>(tmem + L::kTmDP, v_desc, smem_desc(do_s(0), 16, 1024), idesc_s);  // dP^T(0) = V dO^T
         mma_commit_elect(bar(L::kBarDP));
       }
-      for (int x = 0; x < n_tot && ok; ++x) {
+      for (int x = 0; x < total && ok; ++x) {
         const uint32_t acc = (x > 0 || a.accumulate) ? 1u : 0u;
-        const bool more = x + 1 < n_tot;
+        const bool more = x + 1 < total;
         // dV~ += P^T dO once P^T(x) is in TMEM
         ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 24);
         if (!ok) break;
@@ -535,113 +567,122 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_store_wait();
     }
-    // this key's allowed queries: i_lo_k <= i <= i_hi_k
-    long long i_lo_k = k_row <= rule.kmax ? max(0LL, k_row - rule.dhi) : (long long)a.n;
-    long long i_hi_k = min((long long)a.n - 1, k_row - rule.dlo);
-    if (a.layout == RING_LAYOUT_ZIGZAG) zig_query_range(a, rule, k_row, i_lo_k, i_hi_k);
-    if (kWin && a.seg_lo && k_row <= rule.kmax) {
-      long long qlo, qhi;
-      doc_range(a, j, r, k_row, qlo, qhi);
-      i_lo_k = max(i_lo_k, qlo);
-      i_hi_k = min(i_hi_k, qhi);
-    }
     bool ok = true;
-    for (int x = 0; x < n_tot; ++x) {
-      const int st = x & 1;
-      const long long i0 = (long long)(it_lo + x % n_it) * kTileM + c0;  // first query of this half
-      const float* lse_s = reinterpret_cast<const float*>(smem + L::kOffLse + st * 512) + c0;
-      const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512) + c0;
-      // the stage's nlse2 and D landed (TMA writes are visible to the threads
-      // that observe this barrier), then S^T(x) is in TMEM
-      ok = warp_wait(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30);
-      if (!ok) break;
-      // the first 32 of this half's 64 values of -lse log2(e), read while
-      // S^T(x) is computed (all 64 would not fit the register budget)
-      float4 nl[16];
-#pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) nl[e4] = reinterpret_cast<const float4*>(lse_s)[e4];
-      ok = warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 27);
-      if (!ok) break;
-      tc_fence_after();
-      float p[64];
-      {
-        uint32_t t[64];
-        tmem_load64(tmem + lane_off + L::kTmS + c0, t);
-#pragma unroll
-        for (int e = 0; e < 64; ++e) p[e] = __uint_as_float(t[e]);
+    int x = 0;  // loop index over all visits
+    for (int s = 0; s < nvis && ok; ++s) {
+      const int rv = visit_r(s);
+      BwdRule rule = rule0;
+      int it_lo = it_lo0, n_it = n_it0;
+      if (s > 0) range_of(rv, rule, it_lo, n_it);
+      // this key's allowed queries: i_lo_k <= i <= i_hi_k
+      long long i_lo_k = k_row <= rule.kmax ? max(0LL, k_row - rule.dhi) : (long long)a.n;
+      long long i_hi_k = min((long long)a.n - 1, k_row - rule.dlo);
+      if (a.layout == RING_LAYOUT_ZIGZAG) zig_query_range(a, rule, k_row, i_lo_k, i_hi_k);
+      if (kWin && a.seg_lo && k_row <= rule.kmax) {
+        long long qlo, qhi;
+        doc_range(a, j, rv, k_row, qlo, qhi);
+        i_lo_k = max(i_lo_k, qlo);
+        i_hi_k = min(i_hi_k, qhi);
       }
-      const bool masked = !(i0 >= i_lo_k && i0 + 63 <= i_hi_k);
-      // P^T = exp2(S^T scale log2(e) + nlse2): one packed FMA and two MUFU
-      // ex2 per column pair; bf16 pairs over the first 32 columns of the half
-      {
-        const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
-        uint32_t pb[32];
+      // (per-step kernels: x_begin is 0, and the loop is the single visit's)
+      const int x_begin = x, x_end = x + n_it * a.G;
+      for (; x < x_end; ++x) {
+        const int st = x & 1;
+        const long long i0 = (long long)(it_lo + (x - x_begin) % n_it) * kTileM + c0;  // first query of this half
+        const float* lse_s = reinterpret_cast<const float*>(smem + L::kOffLse + st * 512) + c0;
+        const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512) + c0;
+        // the stage's nlse2 and D landed (TMA writes are visible to the threads
+        // that observe this barrier), then S^T(x) is in TMEM
+        ok = warp_wait(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30);
+        if (!ok) break;
+        // the first 32 of this half's 64 values of -lse log2(e), read while
+        // S^T(x) is computed (all 64 would not fit the register budget)
+        float4 nl[16];
 #pragma unroll
-        for (int e4 = 8; e4 < 16; ++e4) nl[e4] = reinterpret_cast<const float4*>(lse_s)[e4];
+        for (int e4 = 0; e4 < 8; ++e4) nl[e4] = reinterpret_cast<const float4*>(lse_s)[e4];
+        ok = warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 27);
+        if (!ok) break;
+        tc_fence_after();
+        float p[64];
+        {
+          uint32_t t[64];
+          tmem_load64(tmem + lane_off + L::kTmS + c0, t);
 #pragma unroll
-        for (int e4 = 0; e4 < 16; ++e4) {
-          float v0, v1, v2, v3;
-          unf2(ffma2(f2(p[4 * e4], p[4 * e4 + 1]), sc2, f2(nl[e4].x, nl[e4].y)), v0, v1);
-          unf2(ffma2(f2(p[4 * e4 + 2], p[4 * e4 + 3]), sc2, f2(nl[e4].z, nl[e4].w)), v2, v3);
-          p[4 * e4] = fast_exp2(v0);
-          p[4 * e4 + 1] = fast_exp2(v1);
-          p[4 * e4 + 2] = fast_exp2(v2);
-          p[4 * e4 + 3] = fast_exp2(v3);
+          for (int e = 0; e < 64; ++e) p[e] = __uint_as_float(t[e]);
         }
-        if (masked) {
-          // queries of this half outside [i_lo_k, i_hi_k] get 0 (relative
-          // bounds clamped to [-1, 64] fit in 32 bits)
-          const int lo = (int)max(-1LL, min(64LL, i_lo_k - i0));
-          const int hi = (int)max(-1LL, min(64LL, i_hi_k - i0));
+        const bool masked = !(i0 >= i_lo_k && i0 + 63 <= i_hi_k);
+        // P^T = exp2(S^T scale log2(e) + nlse2): one packed FMA and two MUFU
+        // ex2 per column pair; bf16 pairs over the first 32 columns of the half
+        {
+          const uint64_t sc2 = f2(a.scale_log2, a.scale_log2);
+          uint32_t pb[32];
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (e < lo || e > hi) p[e] = 0.0f;
+          for (int e4 = 8; e4 < 16; ++e4) nl[e4] = reinterpret_cast<const float4*>(lse_s)[e4];
+#pragma unroll
+          for (int e4 = 0; e4 < 16; ++e4) {
+            float v0, v1, v2, v3;
+            unf2(ffma2(f2(p[4 * e4], p[4 * e4 + 1]), sc2, f2(nl[e4].x, nl[e4].y)), v0, v1);
+            unf2(ffma2(f2(p[4 * e4 + 2], p[4 * e4 + 3]), sc2, f2(nl[e4].z, nl[e4].w)), v2, v3);
+            p[4 * e4] = fast_exp2(v0);
+            p[4 * e4 + 1] = fast_exp2(v1);
+            p[4 * e4 + 2] = fast_exp2(v2);
+            p[4 * e4 + 3] = fast_exp2(v3);
+          }
+          if (masked) {
+            // queries of this half outside [i_lo_k, i_hi_k] get 0 (relative
+            // bounds clamped to [-1, 64] fit in 32 bits)
+            const int lo = (int)max(-1LL, min(64LL, i_lo_k - i0));
+            const int hi = (int)max(-1LL, min(64LL, i_hi_k - i0));
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (e < lo || e > hi) p[e] = 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) pb[e / 2] = pack_bf16(p[e], p[e + 1]);
+          tmem_store32(tmem + lane_off + L::kTmS + c0, pb);
         }
+        tmem_store_wait();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarP));
+        // dS^T = P^T (dP^T - D), 32 columns at a time, bf16 over the read
+        // columns; the first 32 values of -D are read while dP^T(x) finishes
+        float4 nd4[16];
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) pb[e / 2] = pack_bf16(p[e], p[e + 1]);
-        tmem_store32(tmem + lane_off + L::kTmS + c0, pb);
+        for (int e4 = 0; e4 < 8; ++e4) nd4[e4] = reinterpret_cast<const float4*>(d_s)[e4];
+        ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 28);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t t[32];
+          tmem_load32(tmem + lane_off + L::kTmDP + c0 + c * 32, t);
+          if (c == 0) {
+#pragma unroll
+            for (int e4 = 8; e4 < 16; ++e4) nd4[e4] = reinterpret_cast<const float4*>(d_s)[e4];
+          }
+          uint32_t sb[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 nd = nd4[c * 8 + e4];
+            const int e = c * 32 + e4 * 4;
+            float s0, s1, s2, s3;
+            unf2(fmul2(f2(p[e], p[e + 1]),
+                       fadd2(f2(__uint_as_float(t[e4 * 4]), __uint_as_float(t[e4 * 4 + 1])), f2(nd.x, nd.y))),
+                 s0, s1);
+            unf2(fmul2(f2(p[e + 2], p[e + 3]),
+                       fadd2(f2(__uint_as_float(t[e4 * 4 + 2]), __uint_as_float(t[e4 * 4 + 3])), f2(nd.z, nd.w))),
+                 s2, s3);
+            sb[e4 * 2] = pack_bf16(s0, s1);
+            sb[e4 * 2 + 1] = pack_bf16(s2, s3);
+          }
+          tmem_store16(tmem + lane_off + L::kTmDP + c0 + c * 16, sb);
+        }
+        tmem_store_wait();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDS));
       }
-      tmem_store_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarP));
-      // dS^T = P^T (dP^T - D), 32 columns at a time, bf16 over the read
-      // columns; the first 32 values of -D are read while dP^T(x) finishes
-      float4 nd4[16];
-#pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) nd4[e4] = reinterpret_cast<const float4*>(d_s)[e4];
-      ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 28);
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t t[32];
-        tmem_load32(tmem + lane_off + L::kTmDP + c0 + c * 32, t);
-        if (c == 0) {
-#pragma unroll
-          for (int e4 = 8; e4 < 16; ++e4) nd4[e4] = reinterpret_cast<const float4*>(d_s)[e4];
-        }
-        uint32_t sb[16];
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 nd = nd4[c * 8 + e4];
-          const int e = c * 32 + e4 * 4;
-          float s0, s1, s2, s3;
-          unf2(fmul2(f2(p[e], p[e + 1]),
-                     fadd2(f2(__uint_as_float(t[e4 * 4]), __uint_as_float(t[e4 * 4 + 1])), f2(nd.x, nd.y))),
-               s0, s1);
-          unf2(fmul2(f2(p[e + 2], p[e + 3]),
-                     fadd2(f2(__uint_as_float(t[e4 * 4 + 2]), __uint_as_float(t[e4 * 4 + 3])), f2(nd.z, nd.w))),
-               s2, s3);
-          sb[e4 * 2] = pack_bf16(s0, s1);
-          sb[e4 * 2 + 1] = pack_bf16(s2, s3);
-        }
-        tmem_store16(tmem + lane_off + L::kTmDP + c0 + c * 16, sb);
-      }
-      tmem_store_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarDS));
     }
-    if (ok && n_it > 0) {
+    if (ok && total > 0) {
       ok = warp_wait(bar(L::kBarAcc), 0, abort_flag, a, 29);
       tc_fence_after();
     }
@@ -649,7 +690,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ------------------------------------------------------ epilogue
       // (tcgen05.ld is warp-collective: every lane loads, valid keys store;
       // half h stores accumulator columns [h D/2, (h + 1) D/2))
-      const bool have = n_it > 0 || a.accumulate;
+      const bool have = total > 0 || a.accumulate;
       float* dst_v;
       float* dst_k;
       if (a.last) {
@@ -700,7 +741,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // blockIdx.x -> (shard r, head bh, query tile t); consecutive CTAs share a
 // (shard, head) so the key block stays in L2, and the query tiles with the
 // most keys (the last ones under the causal mask) start first.
-template <int D, bool kWin>
+template <int D, bool kWin, bool kLap>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap do_map, const __grid_constant__ CUtensorMap k_map,
@@ -718,22 +759,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int t = a.T - 1 - (int)(blockIdx.x % a.T);
   const int g = blockIdx.x / a.T;
-  const int bh = g % a.BH;
-  const int r = g / a.BH;
-  int j = (r - a.step) % a.P;
-  if (j < 0) j += a.P;
-  BwdRule rule = bwd_rule(a, r, j);
-  if (!kWin) rule.dlo = -kFar;
-  if (a.layout == RING_LAYOUT_ZIGZAG && (long long)t * kTileM >= a.n / 2) {
-    // a zigzag tile lies in one chunk; the late chunk has its own rule
-    rule.kmax = rule.kmax1;
-    rule.dhi = rule.dhi1;
-  }
-  // key tiles with an allowed key for a row of this tile
+  // head and shard; lap launches go head-major so that the resident CTAs
+  // share one head's K and V in L2
+  const int bh = kLap ? g / a.P : g % a.BH;
+  const int r = kLap ? g % a.P : g / a.BH;
+  // Per-step launch: the tile's visit to block (r - step) mod P.  Lap
+  // (kLap): the tile visits every block in step order, j = r, r - 1, ..,
+  // with dQ~ kept in TMEM.
+  const int nvis = kLap ? a.P : 1;
+  auto visit_j = [&](int s) {
+    int jv = (r - (kLap ? s : a.step)) % a.P;
+    return jv < 0 ? jv + a.P : jv;
+  };
   const long long i0 = (long long)t * kTileM;
   const long long i1 = min(i0 + kTileM - 1, (long long)a.n - 1);
-  int kt_lo = 0, n_kt = 0;
-  {
+  // the rule of (shard r, block jv) for this tile's rows and the key tiles
+  // with an allowed key for one of them
+  auto range_of = [&](int jv, BwdRule& rule, int& kt_lo, int& n_kt) {
+    const int j = jv;
+    rule = bwd_rule(a, r, j);
+    if (!kWin) rule.dlo = -kFar;
+    if (a.layout == RING_LAYOUT_ZIGZAG && i0 >= a.n / 2) {
+      // a zigzag tile lies in one chunk; the late chunk has its own rule
+      rule.kmax = rule.kmax1;
+      rule.dhi = rule.dhi1;
+    }
+    kt_lo = 0;
+    n_kt = 0;
     long long k_lo = max(0LL, i0 + rule.dlo);
     long long k_hi = min(rule.kmax, i1 + rule.dhi);
     if (kWin && a.seg_lo) {
@@ -748,7 +800,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       kt_lo = (int)(k_lo / kTileN);
       n_kt = (int)(k_hi / kTileN) + 1 - kt_lo;
     }
+  };
+  int total = 0;  // key tiles of all visits
+  for (int s = 0; s < nvis; ++s) {
+    BwdRule rl;
+    int lo, cnt;
+    range_of(visit_j(s), rl, lo, cnt);
+    total += cnt;
   }
+  const int n_kt = total;
 
   // query-row threads (warps 2..9): lane quadrant warp % 4, column half
   const int quad = warp & 3;
@@ -808,8 +868,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && n_kt > 0) {
       int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int x = 0; x < n_kt && ok; ++x) {
-        const int k0 = (kt_lo + x) * kTileN;
+      int x = 0;  // key tile index over all visits
+      for (int s = 0; s < nvis && ok; ++s) {
+      const int j = visit_j(s);
+      BwdRule rl;
+      int kt_lo, n_vis;
+      range_of(j, rl, kt_lo, n_vis);
+      for (int xl = 0; xl < n_vis && ok; ++xl, ++x) {
+        const int k0 = (kt_lo + xl) * kTileN;
         const int ks = x % L::kKStages, vs = x % L::kVStages;
         // K(x) into its stage once dQ(x - 3) has released it
         if (x >= L::kKStages)
@@ -825,6 +891,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_expect_tx(bar(L::kBarVFull + vs), L::kTile);
         load_rows<D>(a, sbase + L::kOffV + vs * L::kTile, &v_map, bar(L::kBarVFull + vs), j, k0, bh / a.G);
         v_issued = x + 1;
+      }
       }
       const unsigned long long lim = a.wait_limit_ns;
       mbar_drain_wait(bar(L::kBarAB), 0, lim);
@@ -905,18 +972,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_store_wait();
     }
-    // this row's allowed keys: k_lo_i <= k <= k_hi_i
-    long long k_lo_i = max(0LL, i_row + rule.dlo);
-    long long k_hi_i = i_valid ? min(rule.kmax, i_row + rule.dhi) : -1;
-    if (kWin && a.seg_lo && i_valid) {
-      long long klo, khi;
-      doc_range(a, r, j, i_row, klo, khi);
-      k_lo_i = max(k_lo_i, klo);
-      k_hi_i = min(k_hi_i, khi);
-    }
     bool ok = true;
-    for (int x = 0; x < n_kt; ++x) {
-      const long long kbase = (long long)(kt_lo + x) * kTileN + c0;  // first key of this half
+    int x = 0;  // key tile index over all visits
+    for (int s = 0; s < nvis && ok; ++s) {
+      const int j = visit_j(s);
+      BwdRule rule;
+      int kt_lo, n_vis;
+      range_of(j, rule, kt_lo, n_vis);
+      // this row's allowed keys: k_lo_i <= k <= k_hi_i
+      long long k_lo_i = max(0LL, i_row + rule.dlo);
+      long long k_hi_i = i_valid ? min(rule.kmax, i_row + rule.dhi) : -1;
+      if (kWin && a.seg_lo && i_valid) {
+        long long klo, khi;
+        doc_range(a, r, j, i_row, klo, khi);
+        k_lo_i = max(k_lo_i, klo);
+        k_hi_i = min(k_hi_i, khi);
+      }
+    for (int xl = 0; xl < n_vis; ++xl, ++x) {
+      const long long kbase = (long long)(kt_lo + xl) * kTileN + c0;  // first key of this half
       ok = warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 37);
       if (!ok) break;
       tc_fence_after();
@@ -975,6 +1048,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(L::kBarDS));
     }
+    }
     if (ok && n_kt > 0) {
       ok = warp_wait(bar(L::kBarAcc), 0, abort_flag, a, 39);
       tc_fence_after();
@@ -1030,20 +1104,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+template <int D, bool kWin, bool kLap>
+int prepare_bwd_variant() {
+  int e;
+  if ((e = (int)cudaFuncSetAttribute(bwd_dkdv_kernel<D, kWin, kLap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     BwdLayout<D>::kAlloc)))
+    return e;
+  return (int)cudaFuncSetAttribute(bwd_dq_kernel<D, kWin, kLap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   DqLayout<D>::kAlloc);
+}
+
 template <int D>
 int prepare_bwd_one() {
   int e;
-  if ((e = (int)cudaFuncSetAttribute(bwd_dkdv_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     BwdLayout<D>::kAlloc)))
-    return e;
-  if ((e = (int)cudaFuncSetAttribute(bwd_dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     BwdLayout<D>::kAlloc)))
-    return e;
-  if ((e = (int)cudaFuncSetAttribute(bwd_dq_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     DqLayout<D>::kAlloc)))
-    return e;
-  return (int)cudaFuncSetAttribute(bwd_dq_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   DqLayout<D>::kAlloc);
+  if ((e = prepare_bwd_variant<D, false, false>())) return e;
+  if ((e = prepare_bwd_variant<D, true, false>())) return e;
+  if ((e = prepare_bwd_variant<D, false, true>())) return e;
+  return prepare_bwd_variant<D, true, true>();
+}
+
+// one launch of a dK/dV or dQ kernel variant (kDq picks the kernel)
+template <bool kDq, int D, bool kWin, bool kLap>
+void launch_variant(int grid, cudaStream_t s, const BwdArgs& a, const CUtensorMap& qm, const CUtensorMap& om,
+                    const CUtensorMap& km, const CUtensorMap& vm) {
+  if (kDq)
+    bwd_dq_kernel<D, kWin, kLap><<<grid, kBwdThreads, DqLayout<D>::kAlloc, s>>>(a, qm, om, km, vm);
+  else
+    bwd_dkdv_kernel<D, kWin, kLap><<<grid, kBwdThreads, BwdLayout<D>::kAlloc, s>>>(a, qm, om, km, vm);
+}
+
+template <bool kDq>
+int launch_kernel(const BwdArgs& a, int grid, const void* q_map, const void* do_map, const void* k_map,
+                  const void* v_map, int d, void* stream) {
+  if (grid <= 0) return 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
+  const CUtensorMap& om = *static_cast<const CUtensorMap*>(do_map);
+  const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
+  const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
+  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
+  const bool lap = a.lap != 0;
+  const int sel = (d == 64 ? 0 : 4) + (win ? 2 : 0) + (lap ? 1 : 0);
+  switch (sel) {
+    case 0: launch_variant<kDq, 64, false, false>(grid, s, a, qm, om, km, vm); break;
+    case 1: launch_variant<kDq, 64, false, true>(grid, s, a, qm, om, km, vm); break;
+    case 2: launch_variant<kDq, 64, true, false>(grid, s, a, qm, om, km, vm); break;
+    case 3: launch_variant<kDq, 64, true, true>(grid, s, a, qm, om, km, vm); break;
+    case 4: launch_variant<kDq, 128, false, false>(grid, s, a, qm, om, km, vm); break;
+    case 5: launch_variant<kDq, 128, false, true>(grid, s, a, qm, om, km, vm); break;
+    case 6: launch_variant<kDq, 128, true, false>(grid, s, a, qm, om, km, vm); break;
+    default: launch_variant<kDq, 128, true, true>(grid, s, a, qm, om, km, vm); break;
+  }
+  return (int)cudaGetLastError();
 }
 
 }  // namespace
@@ -1068,42 +1180,12 @@ int launch_bwd_prep(const float* out, const float* lse, const void* dout, float*
 
 int launch_bwd_dkdv(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
                     int d, void* stream) {
-  const int grid = a.KT * a.P * a.BHkv;
-  if (grid <= 0) return 0;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
-  const CUtensorMap& om = *static_cast<const CUtensorMap*>(do_map);
-  const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
-  const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
-  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
-  if (d == 64) {
-    if (win) bwd_dkdv_kernel<64, true><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
-    else bwd_dkdv_kernel<64, false><<<grid, kBwdThreads, BwdLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
-  } else {
-    if (win) bwd_dkdv_kernel<128, true><<<grid, kBwdThreads, BwdLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
-    else bwd_dkdv_kernel<128, false><<<grid, kBwdThreads, BwdLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
-  }
-  return (int)cudaGetLastError();
+  return launch_kernel<false>(a, a.KT * a.P * a.BHkv, q_map, do_map, k_map, v_map, d, stream);
 }
 
 int launch_bwd_dq(const BwdArgs& a, const void* q_map, const void* do_map, const void* k_map, const void* v_map,
                   int d, void* stream) {
-  const int grid = a.T * a.P * a.BH;
-  if (grid <= 0) return 0;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
-  const CUtensorMap& om = *static_cast<const CUtensorMap*>(do_map);
-  const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
-  const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
-  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
-  if (d == 64) {
-    if (win) bwd_dq_kernel<64, true><<<grid, kBwdThreads, DqLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
-    else bwd_dq_kernel<64, false><<<grid, kBwdThreads, DqLayout<64>::kAlloc, s>>>(a, qm, om, km, vm);
-  } else {
-    if (win) bwd_dq_kernel<128, true><<<grid, kBwdThreads, DqLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
-    else bwd_dq_kernel<128, false><<<grid, kBwdThreads, DqLayout<128>::kAlloc, s>>>(a, qm, om, km, vm);
-  }
-  return (int)cudaGetLastError();
+  return launch_kernel<true>(a, a.T * a.P * a.BH, q_map, do_map, k_map, v_map, d, stream);
 }
 
 }  // namespace ringattn

@@ -144,6 +144,8 @@ struct BwdArgs {
   int causal, layout, step;
   int accumulate;  // step > 0: continue the accumulators
   int last;        // step P - 1: write the gradients
+  int lap;         // one launch for the whole ring: each CTA visits every shard in step order,
+                   // its accumulators staying on chip (then step 0, accumulate 0, last 1)
   long long window;
   float scale, scale_log2;
   const int* seg_lo;  // sequence packing, as in StepArgs (nullptr: one document)

@@ -60,10 +60,16 @@ def check_grads(name, got, ref):
     print(f"{name}: " + "; ".join(worst))
 
 
-def gpu_fwd_bwd(B, H, N, d, P, causal, layout, q, k, v, do, window=0):
-    att = ra.RingAttention(B, H, N, d, P, causal=causal, layout=layout)
+def gpu_fwd_bwd(B, H, N, d, P, causal, layout, q, k, v, do, window=0, lap=None, kv_heads=None, segments=None):
+    """Forward then backward through the C ABI; lap None keeps the library's
+    default schedule (RING_OPT_BWD_LAP), True/False sets it."""
+    att = ra.RingAttention(B, H, N, d, P, causal=causal, layout=layout, kv_heads=kv_heads)
     if window:
         att.set_option(ra.RING_OPT_WINDOW, window)
+    if segments is not None:
+        att.set_segments(segments)
+    if lap is not None:
+        att.set_option(ra.RING_OPT_BWD_LAP, 1 if lap else 0)
     qc, kc, vc, doc = (x.cuda() for x in (q, k, v, do))
     out, lse = att.fwd(qc, kc, vc)
     dq, dk, dv = att.bwd(qc, kc, vc, out, lse, doc)
@@ -207,3 +213,59 @@ def test_bwd_zigzag_8k(orc):
     flat = lambda t: t.reshape(w.B * w.H, w.N, w.d)
     ref = orc.dense_bwd(flat(q), flat(k), flat(v), flat(do), w.causal)
     check_grads("bwd zigzag-8k", [flat(g).numpy() for g in got], ref)
+
+
+LAP_CASES = [
+    # (B, H, Hkv, N, d, P, causal, layout, window, segments)
+    (1, 2, 2, 1024, 128, 8, True, "striped", 0, None),
+    (1, 2, 2, 1024, 64, 4, False, "contiguous", 0, None),
+    (1, 2, 2, 2624, 128, 8, True, "contiguous", 0, None),  # n = 328: ragged last tile
+    (1, 2, 2, 2048, 128, 4, True, "zigzag", 0, None),
+    (1, 2, 2, 2048, 128, 4, True, "striped", 300, None),  # sliding window
+    (1, 8, 2, 2048, 128, 4, True, "contiguous", 0, None),  # grouped-query: G = 4
+    (1, 2, 2, 1024, 128, 4, True, "striped", 0, [0, 100, 101, 613, 1024]),  # packed documents
+    (2, 1, 1, 768, 64, 3, True, "contiguous", 0, None),  # B = 2, odd P
+]
+
+
+@pytest.mark.parametrize("case", LAP_CASES,
+                         ids=[f"{c[7]}-N{c[3]}-d{c[4]}-P{c[5]}-H{c[1]}/{c[2]}-{'c' if c[6] else 'nc'}-w{c[8]}"
+                              f"-s{0 if c[9] is None else len(c[9]) - 1}" for c in LAP_CASES])
+def test_bwd_lap(orc, case):
+    """RING_OPT_BWD_LAP = 1 (one launch per kernel, every CTA making its
+    tile's whole lap with the accumulators in tensor memory) gives exactly
+    the gradients of RING_OPT_BWD_LAP = 0 (one launch per ring step; same
+    MMAs on the same fp32 values in the same order), and both pass the
+    oracle check."""
+    from ring_sequence_parallelism_gb300.inputs import expand_kv
+
+    B, H, Hkv, N, d, P, causal, layout, window, segments = case
+    q, k, v = make_qkv(B, H, N, d, seed=680 + N + P, Hkv=Hkv)
+    do = make_dout(B, H, N, d, seed=680 + N + P)
+    args = (B, H, N, d, P, causal, layout, q, k, v, do)
+    step = gpu_fwd_bwd(*args, window=window, kv_heads=Hkv, segments=segments, lap=False)
+    lap = gpu_fwd_bwd(*args, window=window, kv_heads=Hkv, segments=segments, lap=True)
+    for name, a, b in zip(("dq", "dk", "dv"), lap, step):
+        assert torch.equal(a, b), f"lap and per-step {name} differ (max {float((a - b).abs().max()):.3e})"
+    G = H // Hkv
+    flat = lambda t: t.reshape(-1, N, d)
+    rq, rk, rv = orc.dense_bwd(flat(q), flat(expand_kv(k, H)), flat(expand_kv(v, H)), flat(do), causal,
+                               window=window, segments=segments)
+    rk = rk.reshape(B * Hkv, G, N, d).sum(1)
+    rv = rv.reshape(B * Hkv, G, N, d).sum(1)
+    check_grads(f"bwd lap {case}", [flat(g).numpy() for g in lap], (rq, rk, rv))
+    check_grads(f"bwd per-step {case}", [flat(g).numpy() for g in step], (rq, rk, rv))
+
+
+def test_bwd_lap_128k_sampled(orc):
+    """The two schedules on the 128K striped workload give identical
+    gradients (every element); the sampled oracle test above checks the
+    default one."""
+    w = WORKLOADS["striped-128k"]
+    q, k, v = make_workload(w)
+    do = make_dout(w.B, w.H, w.N, w.d, w.seed)
+    args = (w.B, w.H, w.N, w.d, w.P, w.causal, w.layout, q, k, v, do)
+    step = gpu_fwd_bwd(*args, lap=False)
+    lap = gpu_fwd_bwd(*args, lap=True)
+    for name, a, b in zip(("dq", "dk", "dv"), lap, step):
+        assert torch.equal(a, b), f"lap and per-step {name} differ (max {float((a - b).abs().max()):.3e})"
