@@ -345,13 +345,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  const int kt = blockIdx.x % a.KT;
-  const int g = blockIdx.x / a.KT;
-  // the K/V head (its G query heads share the block) and the block.  Lap
-  // launches go head-major: the CTAs resident at one time then share one
-  // head's Q and dO (64 MB at 128K tokens, d = 128), which L2 holds.
-  const int kvh = kLap ? g / a.P : g % a.BHkv;
-  const int gq = kLap ? g % a.P : g / a.BHkv;
+  // the key tile, the K/V head (its G query heads share the block) and the
+  // block.  Lap launches go head-major, so the CTAs resident at one time
+  // share one head's Q and dO (64 MB at 128K tokens, d = 128), which L2
+  // holds; within a head the key tiles go in ascending order across all
+  // blocks (the early key tiles meet the most queries), so the last wave
+  // holds the lightest tiles.
+  const int per_head = a.P * a.KT;
+  const int kt = kLap ? (int)(blockIdx.x % per_head) / a.P : (int)(blockIdx.x % a.KT);
+  const int kvh = kLap ? (int)(blockIdx.x / per_head) : (int)(blockIdx.x / a.KT) % a.BHkv;
+  const int gq = kLap ? (int)(blockIdx.x % a.P) : (int)(blockIdx.x / a.KT) / a.BHkv;
   // Per-step launch: this CTA is shard gq's visit to block (gq - step) mod P.
   // Lap (kLap): the CTA owns block gq and makes the block's whole lap
   // itself, visiting shards gq, gq + 1, .. in step order (shard r holds
@@ -757,12 +760,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  const int t = a.T - 1 - (int)(blockIdx.x % a.T);
-  const int g = blockIdx.x / a.T;
-  // head and shard; lap launches go head-major so that the resident CTAs
-  // share one head's K and V in L2
-  const int bh = kLap ? g / a.P : g % a.BH;
-  const int r = kLap ? g % a.P : g / a.BH;
+  // query tile, head and shard.  Lap launches go head-major so that the
+  // resident CTAs share one head's K and V in L2; within a head the query
+  // tiles go in descending order across all shards (the last ones see the
+  // most keys), so the last wave holds the lightest tiles.
+  const int per_head = a.P * a.T;
+  const int t = a.T - 1 - (kLap ? (int)(blockIdx.x % per_head) / a.P : (int)(blockIdx.x % a.T));
+  const int bh = kLap ? (int)(blockIdx.x / per_head) : (int)(blockIdx.x / a.T) % a.BH;
+  const int r = kLap ? (int)(blockIdx.x % a.P) : (int)(blockIdx.x / a.T) / a.BH;
   // Per-step launch: the tile's visit to block (r - step) mod P.  Lap
   // (kLap): the tile visits every block in step order, j = r, r - 1, ..,
   // with dQ~ kept in TMEM.
