@@ -142,18 +142,20 @@ struct DqLayout {
   static constexpr int kBarVFull = kBarKEmpty + kKStages;  // [2]
   static constexpr int kBarVEmpty = kBarVFull + kVStages;  // [2]
   static constexpr int kBarS = kBarVEmpty + kVStages;
-  static constexpr int kBarDP = kBarS + 1;
-  static constexpr int kBarP = kBarDP + 1;   // S read, 256 arrivals
-  static constexpr int kBarDS = kBarP + 1;   // dS in TMEM, 256 arrivals
-  static constexpr int kBarAcc = kBarDS + 1;
+  static constexpr int kBarDP = kBarS + 1;   // [2]: dP buffer b computed
+  static constexpr int kBarP = kBarDP + 2;   // S read, 256 arrivals
+  static constexpr int kBarDS = kBarP + 1;   // [2]: dS in dP buffer b, 256 arrivals each
+  static constexpr int kBarAcc = kBarDS + 2;
   static constexpr int kBarDrain = kBarAcc + 1;
   static constexpr int kNumBars = kBarDrain + 1;
-  static constexpr bool row_barrier(int x) { return x == kBarP || x == kBarDS; }
+  static constexpr bool row_barrier(int x) { return x == kBarP || x == kBarDS || x == kBarDS + 1; }
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
   static constexpr int kAlloc = (kBytes + 1024) > 122880 ? (kBytes + 1024) : 122880;
-  static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc1 = 256;
+  // TMEM columns: S [0,128), dP/dS buffers [128,256) and [384,512), dQ~ from 256
+  static constexpr uint32_t kTmS = 0, kTmAcc1 = 256;
+  __device__ static constexpr uint32_t tm_dp(int b) { return b ? 384u : 128u; }
 };
 
 // Mask of block (shard r, block j) for the contiguous and striped layouts:
@@ -927,34 +929,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = v_full(0, 42);
       }
       if (ok) {
-        mma_qk<D>(tmem + L::kTmDP, do_desc, smem_desc(v_s(0), 16, 1024), idesc_s);  // dP(0) = dO V^T
+        mma_qk<D>(tmem + L::tm_dp(0), do_desc, smem_desc(v_s(0), 16, 1024), idesc_s);  // dP(0) = dO V^T
         mma_commit_elect(bar(L::kBarDP));
         mma_commit_elect(bar(L::kBarVEmpty));  // V(0) served its only MMA
       }
+      // Per key tile x: S(x+1) and dP(x+1) go ahead of dQ(x), so the row
+      // threads find both ready when they finish dS(x).  dP alternates
+      // between two TMEM buffers: dP(x+1) overwrites dS(x-1), whose reader
+      // dQ(x-1) was issued before it (one thread's MMAs run in order).
       for (int x = 0; x < n_kt && ok; ++x) {
         const bool more = x + 1 < n_kt;
-        // S(x+1) may overwrite S(x) once the row threads have read it
         if (more) {
+          // S(x+1) may overwrite S(x) once the row threads have read it
           ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 34) && k_full(x + 1, 35);
           if (!ok) break;
           tc_fence_after();
           mma_qk<D>(tmem + L::kTmS, q_desc, smem_desc(k_s(x + 1), 16, 1024), idesc_s);
           mma_commit_elect(bar(L::kBarS));
-        }
-        // dQ~ += dS K once dS(x) is in TMEM (over the dP columns)
-        ok = warp_wait(bar(L::kBarDS), x & 1, abort_flag, a, 36);
-        if (!ok) break;
-        tc_fence_after();
-        mma_pv_split(tmem + L::kTmAcc1, tmem + L::kTmDP, smem_desc(k_s(x), kTileN * 128, 1024), idesc_acc,
-                     (x > 0 || a.accumulate) ? 1u : 0u);
-        mma_commit_elect(bar(L::kBarKEmpty + x % L::kKStages));  // K(x) served S(x) and dQ(x)
-        if (more) {
           ok = v_full(x + 1, 43);
           if (!ok) break;
-          mma_qk<D>(tmem + L::kTmDP, do_desc, smem_desc(v_s(x + 1), 16, 1024), idesc_s);
-          mma_commit_elect(bar(L::kBarDP));
+          const int b1 = (x + 1) & 1;
+          mma_qk<D>(tmem + L::tm_dp(b1), do_desc, smem_desc(v_s(x + 1), 16, 1024), idesc_s);
+          mma_commit_elect(bar(L::kBarDP + b1));
           mma_commit_elect(bar(L::kBarVEmpty + (x + 1) % L::kVStages));
         }
+        // dQ~ += dS K once dS(x) is in TMEM (over dP buffer x mod 2)
+        ok = warp_wait(bar(L::kBarDS + (x & 1)), (x >> 1) & 1, abort_flag, a, 36);
+        if (!ok) break;
+        tc_fence_after();
+        mma_pv_split(tmem + L::kTmAcc1, tmem + L::tm_dp(x & 1), smem_desc(k_s(x), kTileN * 128, 1024), idesc_acc,
+                     (x > 0 || a.accumulate) ? 1u : 0u);
+        mma_commit_elect(bar(L::kBarKEmpty + x % L::kKStages));  // K(x) served S(x) and dQ(x)
       }
       if (ok) mma_commit_elect(bar(L::kBarAcc));
       mma_commit_elect(bar(L::kBarDrain));
@@ -1029,7 +1034,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (e < lo || e > hi) p[e] = 0.0f;
         }
       }
-      ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 38);
+      const int b = x & 1;  // dP buffer of this tile
+      ok = warp_wait(bar(L::kBarDP + b), (x >> 1) & 1, abort_flag, a, 38);
       if (!ok) break;
       tc_fence_after();
       // dS = P (dP - D), 32 columns at a time, bf16 over the read dP columns
@@ -1037,7 +1043,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t tt[32];
-        tmem_load32(tmem + lane_off + L::kTmDP + c0 + c * 32, tt);
+        tmem_load32(tmem + lane_off + L::tm_dp(b) + c0 + c * 32, tt);
         uint32_t sb[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -1047,11 +1053,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                s0, s1);
           sb[e / 2] = pack_bf16(s0, s1);
         }
-        tmem_store16(tmem + lane_off + L::kTmDP + c0 + c * 16, sb);
+        tmem_store16(tmem + lane_off + L::tm_dp(b) + c0 + c * 16, sb);
       }
       tmem_store_wait();
       tc_fence_before();
-      mbar_arrive(bar(L::kBarDS));
+      mbar_arrive(bar(L::kBarDS + b));
     }
     }
     if (ok && n_kt > 0) {
