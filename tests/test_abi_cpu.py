@@ -100,6 +100,30 @@ def test_workspace_size(lib):
     att.close()
 
 
+def test_bwd_workspace_size_follows_the_schedule(lib):
+    """The backward's workspace: -lse log2(e) and -D per row (shard-major,
+    rows padded to whole tiles), plus, for one launch per ring step only,
+    two buffers each of the travelling dK~ and dV~ (fp32, K/V heads)."""
+    up = lambda x: (x + 255) // 256 * 256
+    B, H, Hkv, N, d, P = 1, 8, 2, 4096, 128, 4
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped", kv_heads=Hkv)
+    vec = up(B * H * P * 1024 * 4)  # n = 1024: 8 tiles of 128 rows
+    acc = up(B * Hkv * N * d * 4)
+    assert att.bwd_workspace_size() == 2 * vec  # lap schedule (the default)
+    att.set_option(ra.RING_OPT_BWD_LAP, 0)
+    assert att.bwd_workspace_size() == 2 * vec + 4 * acc
+    att.set_option(ra.RING_OPT_BWD_LAP, 1)
+    assert att.bwd_workspace_size() == 2 * vec
+    for bad in (2, -1):
+        assert lib.ring_attn_set_option(att.handle, _lib.RING_OPT_BWD_LAP, bad) == _lib.RING_ERR_INVALID_ARG
+    att.close()
+    # one shard: a single step, which needs no accumulator buffers either way
+    att = ra.RingAttention(1, 2, 512, 64, 1, causal=True, layout="contiguous")
+    att.set_option(ra.RING_OPT_BWD_LAP, 0)
+    assert att.bwd_workspace_size() == 2 * up(2 * 1 * 512 * 4)
+    att.close()
+
+
 # -------------------------------------------------------------- planner
 def test_plan_matches_golden_schedule(lib):
     """The 4-device walk-through in "Ring Attention：把超长序列沿设备环流动",
