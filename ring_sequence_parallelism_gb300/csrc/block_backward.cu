@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float* lse_base = a.nlse2 + ((size_t)qh * a.P + rv) * a.n_pad;
           const float* d_base = a.nD + ((size_t)qh * a.P + rv) * a.n_pad;
           const int st = x & 1;
-          if (x >= 2) ok = mbar_wait(bar(L::kBarEmpty + st), ((x >> 1) - 1) & 1, abort_flag, a, 21);
+          if (x >= 2) ok = mbar_poll(bar(L::kBarEmpty + st), ((x >> 1) - 1) & 1, abort_flag, a, 21);
           if (!ok) break;
           const int i0 = (it_lo + xl % n_it) * kTileM;
           mbar_expect_tx(bar(L::kBarFull + st), 2 * L::kTile + 1024);
@@ -511,8 +511,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t v_desc = smem_desc(sbase + L::kOffB, 16, 1024);
       auto q_s = [&](int x) { return sbase + L::kOffX + (x & 1) * L::kTile; };
       auto do_s = [&](int x) { return sbase + L::kOffY + (x & 1) * L::kTile; };
-      bool ok = warp_wait(bar(L::kBarAB), 0, abort_flag, a, 22) &&
-                warp_wait(bar(L::kBarFull), 0, abort_flag, a, 23);
+      bool ok = warp_poll(bar(L::kBarAB), 0, abort_flag, a, 22) &&
+                warp_poll(bar(L::kBarFull), 0, abort_flag, a, 23);
       if (ok) {
         mma_qk<D>(tmem + L::kTmS, k_desc, smem_desc(q_s(0), 16, 1024), idesc_s);  // S^T(0) = K Q^T
         mma_commit_elect(bar(L::kBarS));
@@ -523,19 +523,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t acc = (x > 0 || a.accumulate) ? 1u : 0u;
         const bool more = x + 1 < total;
         // dV~ += P^T dO once P^T(x) is in TMEM
-        ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 24);
+        ok = warp_poll(bar(L::kBarP), x & 1, abort_flag, a, 24);
         if (!ok) break;
         tc_fence_after();
         mma_pv_split(tmem + L::kTmAcc1, tmem + L::kTmS, smem_desc(do_s(x), kTileM * 128, 1024), idesc_acc, acc);
         // S^T(x+1) overwrites S/P(x) after that MMA (one thread's MMAs run in order)
         if (more) {
-          ok = warp_wait(bar(L::kBarFull + ((x + 1) & 1)), ((x + 1) >> 1) & 1, abort_flag, a, 25);
+          ok = warp_poll(bar(L::kBarFull + ((x + 1) & 1)), ((x + 1) >> 1) & 1, abort_flag, a, 25);
           if (!ok) break;
           mma_qk<D>(tmem + L::kTmS, k_desc, smem_desc(q_s(x + 1), 16, 1024), idesc_s);
           mma_commit_elect(bar(L::kBarS));
         }
         // dK~ += dS^T Q once dS^T(x) is in TMEM
-        ok = warp_wait(bar(L::kBarDS), x & 1, abort_flag, a, 26);
+        ok = warp_poll(bar(L::kBarDS), x & 1, abort_flag, a, 26);
         if (!ok) break;
         tc_fence_after();
         mma_pv_split(tmem + L::kTmAcc2, tmem + L::kTmDP, smem_desc(q_s(x), kTileM * 128, 1024), idesc_acc, acc);
@@ -598,14 +598,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float* d_s = reinterpret_cast<const float*>(smem + L::kOffD + st * 512) + c0;
         // the stage's nlse2 and D landed (TMA writes are visible to the threads
         // that observe this barrier), then S^T(x) is in TMEM
-        ok = warp_wait(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30);
+        ok = warp_poll(bar(L::kBarFull + st), (x >> 1) & 1, abort_flag, a, 30);
         if (!ok) break;
         // the first 32 of this half's 64 values of -lse log2(e), read while
         // S^T(x) is computed (all 64 would not fit the register budget)
         float4 nl[16];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) nl[e4] = reinterpret_cast<const float4*>(lse_s)[e4];
-        ok = warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 27);
+        ok = warp_poll(bar(L::kBarS), x & 1, abort_flag, a, 27);
         if (!ok) break;
         tc_fence_after();
         float p[64];
@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float4 nd4[16];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) nd4[e4] = reinterpret_cast<const float4*>(d_s)[e4];
-        ok = warp_wait(bar(L::kBarDP), x & 1, abort_flag, a, 28);
+        ok = warp_poll(bar(L::kBarDP), x & 1, abort_flag, a, 28);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     if (ok && total > 0) {
-      ok = warp_wait(bar(L::kBarAcc), 0, abort_flag, a, 29);
+      ok = warp_poll(bar(L::kBarAcc), 0, abort_flag, a, 29);
       tc_fence_after();
     }
     if (ok) {
@@ -886,14 +886,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int ks = x % L::kKStages, vs = x % L::kVStages;
         // K(x) into its stage once dQ(x - 3) has released it
         if (x >= L::kKStages)
-          ok = mbar_wait(bar(L::kBarKEmpty + ks), ((x / L::kKStages) - 1) & 1, abort_flag, a, 31);
+          ok = mbar_poll(bar(L::kBarKEmpty + ks), ((x / L::kKStages) - 1) & 1, abort_flag, a, 31);
         if (!ok) break;
         mbar_expect_tx(bar(L::kBarKFull + ks), L::kTile);
         load_rows<D>(a, sbase + L::kOffK + ks * L::kTile, &k_map, bar(L::kBarKFull + ks), j, k0, bh / a.G);
         k_issued = x + 1;
         // V(x) once dP(x - 2) has released its stage
         if (x >= L::kVStages)
-          ok = mbar_wait(bar(L::kBarVEmpty + vs), ((x / L::kVStages) - 1) & 1, abort_flag, a, 41);
+          ok = mbar_poll(bar(L::kBarVEmpty + vs), ((x / L::kVStages) - 1) & 1, abort_flag, a, 41);
         if (!ok) break;
         mbar_expect_tx(bar(L::kBarVFull + vs), L::kTile);
         load_rows<D>(a, sbase + L::kOffV + vs * L::kTile, &v_map, bar(L::kBarVFull + vs), j, k0, bh / a.G);
@@ -917,12 +917,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto k_s = [&](int x) { return sbase + L::kOffK + (x % L::kKStages) * L::kTile; };
       auto v_s = [&](int x) { return sbase + L::kOffV + (x % L::kVStages) * L::kTile; };
       auto k_full = [&](int x, int site) {
-        return warp_wait(bar(L::kBarKFull + x % L::kKStages), (x / L::kKStages) & 1, abort_flag, a, site);
+        return warp_poll(bar(L::kBarKFull + x % L::kKStages), (x / L::kKStages) & 1, abort_flag, a, site);
       };
       auto v_full = [&](int x, int site) {
-        return warp_wait(bar(L::kBarVFull + x % L::kVStages), (x / L::kVStages) & 1, abort_flag, a, site);
+        return warp_poll(bar(L::kBarVFull + x % L::kVStages), (x / L::kVStages) & 1, abort_flag, a, site);
       };
-      bool ok = warp_wait(bar(L::kBarAB), 0, abort_flag, a, 32) && k_full(0, 33);
+      bool ok = warp_poll(bar(L::kBarAB), 0, abort_flag, a, 32) && k_full(0, 33);
       if (ok) {
         mma_qk<D>(tmem + L::kTmS, q_desc, smem_desc(k_s(0), 16, 1024), idesc_s);  // S(0) = Q K^T
         mma_commit_elect(bar(L::kBarS));
@@ -941,7 +941,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool more = x + 1 < n_kt;
         if (more) {
           // S(x+1) may overwrite S(x) once the row threads have read it
-          ok = warp_wait(bar(L::kBarP), x & 1, abort_flag, a, 34) && k_full(x + 1, 35);
+          ok = warp_poll(bar(L::kBarP), x & 1, abort_flag, a, 34) && k_full(x + 1, 35);
           if (!ok) break;
           tc_fence_after();
           mma_qk<D>(tmem + L::kTmS, q_desc, smem_desc(k_s(x + 1), 16, 1024), idesc_s);
@@ -954,7 +954,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit_elect(bar(L::kBarVEmpty + (x + 1) % L::kVStages));
         }
         // dQ~ += dS K once dS(x) is in TMEM (over dP buffer x mod 2)
-        ok = warp_wait(bar(L::kBarDS + (x & 1)), (x >> 1) & 1, abort_flag, a, 36);
+        ok = warp_poll(bar(L::kBarDS + (x & 1)), (x >> 1) & 1, abort_flag, a, 36);
         if (!ok) break;
         tc_fence_after();
         mma_pv_split(tmem + L::kTmAcc1, tmem + L::tm_dp(x & 1), smem_desc(k_s(x), kTileN * 128, 1024), idesc_acc,
@@ -1000,7 +1000,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     for (int xl = 0; xl < n_vis; ++xl, ++x) {
       const long long kbase = (long long)(kt_lo + xl) * kTileN + c0;  // first key of this half
-      ok = warp_wait(bar(L::kBarS), x & 1, abort_flag, a, 37);
+      ok = warp_poll(bar(L::kBarS), x & 1, abort_flag, a, 37);
       if (!ok) break;
       tc_fence_after();
       float p[64];
@@ -1035,7 +1035,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       const int b = x & 1;  // dP buffer of this tile
-      ok = warp_wait(bar(L::kBarDP + b), (x >> 1) & 1, abort_flag, a, 38);
+      ok = warp_poll(bar(L::kBarDP + b), (x >> 1) & 1, abort_flag, a, 38);
       if (!ok) break;
       tc_fence_after();
       // dS = P (dP - D), 32 columns at a time, bf16 over the read dP columns
@@ -1061,7 +1061,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     }
     if (ok && n_kt > 0) {
-      ok = warp_wait(bar(L::kBarAcc), 0, abort_flag, a, 39);
+      ok = warp_poll(bar(L::kBarAcc), 0, abort_flag, a, 39);
       tc_fence_after();
     }
     if (ok) {
