@@ -262,6 +262,27 @@ RINGATTN_API int ring_attn_finalize(ring_attn_t h, int r, ring_state_t s, float*
 RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
                   void* workspace, void* stream);
 
+/* ring_attn_fwd from HOST memory and back, with the copies overlapped with
+ * the computation.  The heads are independent problems, so they run in
+ * groups of whole K/V heads (4, 2 or 1 groups: the most that divides
+ * B * Hkv), each group a ring_attn_fwd over its heads: the inputs of group
+ * g+1 are copied in and the outputs of group g-1 copied out while group g
+ * computes.  The results equal ring_attn_fwd's over all heads.
+ *   q, k, v   HOST pointers, natural order as in ring_attn_fwd (bf16);
+ *             page-locked (cudaHostAlloc, or a pinned torch tensor) for the
+ *             copies to be asynchronous and overlapped
+ *   out, lse  HOST pointers, as in ring_attn_fwd (fp32)
+ * The handle owns the device buffers (inputs, outputs and one group's
+ * workspace), made on the first call and kept until ring_attn_destroy, and
+ * two copy streams.  Asynchronous on `stream`: the copies start after the
+ * caller's earlier work on it, and `stream` completes after the last output
+ * copy, so the host may read out and lse after synchronising it.  The host
+ * buffers must stay valid, and the inputs unchanged, until then.
+ * ring_attn_check covers the copy streams and the group handle.  Errors:
+ * RING_ERR_INVALID_ARG for NULL pointers; RING_ERR_CUDA, RING_ERR_OOM. */
+RINGATTN_API int ring_attn_fwd_host(ring_attn_t h, const void* q, const void* k, const void* v, float* out,
+                                    float* lse, void* stream);
+
 /* Ring backward on one device ([RA-CN] "Backward 需要让梯度也沿环传播": every
  * Q-K/V block interaction contributes a gradient; the owner of a query shard
  * accumulates its dQ from every K/V block, while the dK and dV of a

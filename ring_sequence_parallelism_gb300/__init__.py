@@ -255,20 +255,28 @@ class RingAttention:
         return out, lse
 
     def fwd_host(self, q_host, k_host, v_host, out_host=None, lse_host=None, stream=None):
-        """End-to-end call from host memory: copy pinned q, k, v to the device,
-        run the ring forward, copy out and lse back (the step's result)."""
+        """End-to-end call from host memory (ring_attn_fwd_host): pinned CPU
+        q, k, v in, pinned CPU out and lse back, the copies overlapped with
+        the computation over head groups.  The results are ready once the
+        stream (default: the current one) is synchronised."""
         import torch
 
-        q = q_host.to("cuda", non_blocking=True)
-        k = k_host.to("cuda", non_blocking=True)
-        v = v_host.to("cuda", non_blocking=True)
-        out, lse = self.fwd(q, k, v, stream=stream)
+        shape = (self.B, self.H, self.N, self.d)
+        kv_shape = (self.B, self.Hkv, self.N, self.d)
+        for t, want in ((q_host, shape), (k_host, kv_shape), (v_host, kv_shape)):
+            if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or tuple(t.shape) != want:
+                raise ValueError(f"q must be a contiguous CPU bfloat16 tensor {shape}, k, v {kv_shape}")
         if out_host is None:
-            out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+            out_host = torch.empty(shape, dtype=torch.float32, pin_memory=True)
         if lse_host is None:
-            lse_host = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        out_host.copy_(out, non_blocking=True)
-        lse_host.copy_(lse, non_blocking=True)
+            lse_host = torch.empty(shape[:3], dtype=torch.float32, pin_memory=True)
+        for t, want in ((out_host, shape), (lse_host, shape[:3])):
+            if t.dtype != torch.float32 or t.is_cuda or not t.is_contiguous() or tuple(t.shape) != want:
+                raise ValueError(f"out, lse must be contiguous CPU float32 tensors {shape}, {shape[:3]}")
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        _lib.check(self._lib.ring_attn_fwd_host(self.handle, _ptr(q_host), _ptr(k_host), _ptr(v_host),
+                                                _ptr(out_host), _ptr(lse_host), _stream(stream)))
         return out_host, lse_host
 
     def decode(self, q, k, v, out=None, lse=None, stream=None):

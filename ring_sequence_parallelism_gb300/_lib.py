@@ -59,6 +59,7 @@ SIGNATURES = {
     "ring_attn_merge": (_i, [_vp, RingState, RingState, _vp]),
     "ring_attn_finalize": (_i, [_vp, _i, RingState, _vp, _vp, _vp]),
     "ring_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ring_attn_set_option": (_i, [_vp, _i, _ll]),
     "ring_attn_set_segments": (_i, [_vp, _pll, _i]),
     "ring_attn_get_timing": (_i, [_vp, _pf, _pf, _pf, _pf]),

@@ -113,6 +113,23 @@ int tensor_map_4d(void* map, const void* base, const unsigned long long dims[4],
 }
 }  // namespace ringattn
 
+struct ring_attn;
+
+// ring_attn_fwd_host's pipeline over head groups (made on first use): a
+// handle for one group, device copies of the inputs and outputs of all
+// heads, the group handle's workspace, and a stream each for the copies in
+// and out.
+struct HostPipe {
+  ring_attn* sub = nullptr;
+  int groups = 0;
+  uint8_t* dev = nullptr;
+  size_t q_off = 0, k_off = 0, v_off = 0, o_off = 0, l_off = 0, ws_off = 0;
+  cudaStream_t in = nullptr, out = nullptr;
+  std::vector<cudaEvent_t> ev_in, ev_comp;
+  cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+  bool have_done = false;  // ev_done recorded by an earlier call
+};
+
 struct ring_attn {
   Plan plan;
   int rotation = 2;
@@ -138,6 +155,7 @@ struct ring_attn {
   int* d_seg = nullptr;  // segments: first / one-past-last position of each position's document, [2][N]
   long long d_seg_n = 0;
   bool seg_dirty = false;
+  HostPipe* pipe = nullptr;  // ring_attn_fwd_host
 };
 
 namespace ringattn {
@@ -146,6 +164,22 @@ unsigned long long handle_wait_limit(const ring_attn* h) { return h->wait_limit_
 }  // namespace ringattn
 
 namespace {
+
+void destroy_pipe(HostPipe* hp) {
+  if (!hp) return;
+  if (hp->in) cudaStreamSynchronize(hp->in);
+  if (hp->out) cudaStreamSynchronize(hp->out);
+  for (auto* v : {&hp->ev_in, &hp->ev_comp})
+    for (auto e : *v)
+      if (e) cudaEventDestroy(e);
+  if (hp->ev_start) cudaEventDestroy(hp->ev_start);
+  if (hp->ev_done) cudaEventDestroy(hp->ev_done);
+  if (hp->in) cudaStreamDestroy(hp->in);
+  if (hp->out) cudaStreamDestroy(hp->out);
+  if (hp->dev) cudaFree(hp->dev);
+  ring_attn_destroy(hp->sub);
+  delete hp;
+}
 
 int make_events(std::vector<cudaEvent_t>& v, int n, unsigned flags) {
   v.assign(n, nullptr);
@@ -291,6 +325,8 @@ int ring_attn_create_gqa(ring_attn_t* out, int B, int H, int Hkv, long long N, i
 
 int ring_attn_destroy(ring_attn_t h) {
   if (!h) return RING_OK;
+  destroy_pipe(h->pipe);
+  h->pipe = nullptr;
   if (h->ready) {
     int prev = -1;
     cudaGetDevice(&prev);
@@ -651,6 +687,154 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
   return RING_OK;
 }
 
+// ------------------------------------------------------- from host memory
+// ring_attn_fwd_host: the heads are independent problems, so they run in
+// groups of whole K/V heads with their query heads: the inputs of group g+1
+// are copied in (stream `in`) while group g computes on the caller's stream
+// and the outputs of group g-1 are copied out (stream `out`).  Each group is
+// one ring_attn_fwd of a handle for the group's heads, so the results are
+// those of one ring_attn_fwd over all heads.
+
+}  // extern "C"
+
+namespace {
+
+// groups: the most of 4, 2, 1 that divides the K/V heads of all batches
+int host_groups(const Plan& p) {
+  const int units = p.B * p.Hkv;
+  for (int g : {4, 2})
+    if (units % g == 0) return g;
+  return 1;
+}
+
+// The group handle follows the parent's options (window, documents,
+// rotation, wait limit); its plan is rebuilt when they changed.
+int sync_group_handle(ring_attn* h) {
+  HostPipe* hp = h->pipe;
+  ring_attn* sub = hp->sub;
+  const Plan& p = h->plan;
+  if (sub->plan.window != p.window || sub->plan.seg_bounds != p.seg_bounds) {
+    const int units = p.B * p.Hkv / hp->groups;
+    const int G = p.H / p.Hkv;
+    Plan np;
+    std::string err;
+    int rc = build_plan(&np, 1, units * G, p.N, p.d, p.P, p.causal, p.layout, &err, p.window, &p.seg_bounds);
+    if (rc != RING_OK) return fail(rc, err);
+    np.Hkv = units;
+    sub->plan = std::move(np);
+    sub->seg_dirty = true;
+  }
+  sub->rotation = h->rotation;
+  sub->wait_limit_ns = h->wait_limit_ns;
+  return RING_OK;
+}
+
+int build_pipe(ring_attn* h, HostPipe* hp);
+
+// The pipeline is attached to the handle only once every part of it exists.
+int ensure_pipe(ring_attn* h) {
+  if (h->pipe) return sync_group_handle(h);
+  HostPipe* hp = new (std::nothrow) HostPipe();
+  if (!hp) return fail(RING_ERR_OOM, "out of host memory");
+  h->pipe = hp;  // sync_group_handle reads it
+  const int rc = build_pipe(h, hp);
+  if (rc) {
+    h->pipe = nullptr;
+    destroy_pipe(hp);
+  }
+  return rc;
+}
+
+int build_pipe(ring_attn* h, HostPipe* hp) {
+  const Plan& p = h->plan;
+  hp->groups = host_groups(p);
+  const int units = p.B * p.Hkv / hp->groups;
+  const int G = p.H / p.Hkv;
+  int rc = ring_attn_create_gqa(&hp->sub, 1, units * G, units, p.N, p.d, p.P, p.causal, p.layout);
+  if (rc) return rc;
+  hp->sub->plan.window = -1;  // forces the first sync to build the plan with the options
+  if ((rc = sync_group_handle(h))) return rc;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t q_bytes = (size_t)p.B * p.H * (size_t)p.N * p.d * 2;
+  const size_t kv_bytes = (size_t)p.B * p.Hkv * (size_t)p.N * p.d * 2;
+  const size_t o_bytes = (size_t)p.B * p.H * (size_t)p.N * p.d * 4;
+  const size_t l_bytes = (size_t)p.B * p.H * (size_t)p.N * 4;
+  hp->q_off = 0;
+  hp->k_off = up(q_bytes);
+  hp->v_off = hp->k_off + up(kv_bytes);
+  hp->o_off = hp->v_off + up(kv_bytes);
+  hp->l_off = hp->o_off + up(o_bytes);
+  hp->ws_off = hp->l_off + up(l_bytes);
+  const size_t total = hp->ws_off + fwd_workspace(hp->sub->plan).total;
+  RA_CUDA(cudaMalloc(&hp->dev, total), "cudaMalloc(host-call buffers)");
+  RA_CUDA(cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking), "cudaStreamCreate");
+  RA_CUDA(cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking), "cudaStreamCreate");
+  if ((rc = make_events(hp->ev_in, hp->groups, cudaEventDisableTiming))) return rc;
+  if ((rc = make_events(hp->ev_comp, hp->groups, cudaEventDisableTiming))) return rc;
+  RA_CUDA(cudaEventCreateWithFlags(&hp->ev_start, cudaEventDisableTiming), "cudaEventCreate");
+  RA_CUDA(cudaEventCreateWithFlags(&hp->ev_done, cudaEventDisableTiming), "cudaEventCreate");
+  return RING_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ring_attn_fwd_host(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
+                       void* stream) {
+  if (!h || !q || !k || !v || !out || !lse) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  int rc = ensure_device(h);
+  if (rc) return rc;
+  if ((rc = ensure_pipe(h))) return rc;
+  HostPipe* hp = h->pipe;
+  const Plan& p = h->plan;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int groups = hp->groups;
+  const size_t units = (size_t)p.B * p.Hkv / groups;  // K/V heads per group
+  const size_t hq = units * (p.H / p.Hkv);             // query heads per group
+  const size_t rows = (size_t)p.N;
+  const size_t q_b = hq * rows * p.d * 2, kv_b = units * rows * p.d * 2;
+  const size_t o_b = hq * rows * p.d * 4, l_b = hq * rows * 4;
+  uint8_t* dev = hp->dev;
+  // the copies start after the caller's earlier work on its stream, and
+  // after the previous call's outputs have left the device buffers
+  RA_CUDA(cudaEventRecord(hp->ev_start, cs), "cudaEventRecord");
+  RA_CUDA(cudaStreamWaitEvent(hp->in, hp->ev_start, 0), "cudaStreamWaitEvent");
+  if (hp->have_done) RA_CUDA(cudaStreamWaitEvent(hp->in, hp->ev_done, 0), "cudaStreamWaitEvent");
+  for (int g = 0; g < groups; ++g) {
+    // K and V first: the forward's first kernel packs them
+    RA_CUDA(cudaMemcpyAsync(dev + hp->k_off + g * kv_b, static_cast<const uint8_t*>(k) + g * kv_b, kv_b,
+                            cudaMemcpyHostToDevice, hp->in),
+            "cudaMemcpyAsync(k)");
+    RA_CUDA(cudaMemcpyAsync(dev + hp->v_off + g * kv_b, static_cast<const uint8_t*>(v) + g * kv_b, kv_b,
+                            cudaMemcpyHostToDevice, hp->in),
+            "cudaMemcpyAsync(v)");
+    RA_CUDA(cudaMemcpyAsync(dev + hp->q_off + g * q_b, static_cast<const uint8_t*>(q) + g * q_b, q_b,
+                            cudaMemcpyHostToDevice, hp->in),
+            "cudaMemcpyAsync(q)");
+    RA_CUDA(cudaEventRecord(hp->ev_in[g], hp->in), "cudaEventRecord");
+  }
+  for (int g = 0; g < groups; ++g) {
+    RA_CUDA(cudaStreamWaitEvent(cs, hp->ev_in[g], 0), "cudaStreamWaitEvent");
+    float* o_dev = reinterpret_cast<float*>(dev + hp->o_off + g * o_b);
+    float* l_dev = reinterpret_cast<float*>(dev + hp->l_off + g * l_b);
+    if ((rc = ring_attn_fwd(hp->sub, dev + hp->q_off + g * q_b, dev + hp->k_off + g * kv_b,
+                            dev + hp->v_off + g * kv_b, o_dev, l_dev, dev + hp->ws_off, stream)))
+      return rc;
+    RA_CUDA(cudaEventRecord(hp->ev_comp[g], cs), "cudaEventRecord");
+    RA_CUDA(cudaStreamWaitEvent(hp->out, hp->ev_comp[g], 0), "cudaStreamWaitEvent");
+    RA_CUDA(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out) + g * o_b, o_dev, o_b, cudaMemcpyDeviceToHost, hp->out),
+            "cudaMemcpyAsync(out)");
+    RA_CUDA(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + g * l_b, l_dev, l_b, cudaMemcpyDeviceToHost, hp->out),
+            "cudaMemcpyAsync(lse)");
+  }
+  // the caller's stream completes after the last output copy
+  RA_CUDA(cudaEventRecord(hp->ev_done, hp->out), "cudaEventRecord");
+  hp->have_done = true;
+  RA_CUDA(cudaStreamWaitEvent(cs, hp->ev_done, 0), "cudaStreamWaitEvent");
+  return RING_OK;
+}
+
 // ---------------------------------------------------------------- backward
 // Workspace of ring_attn_bwd: -lse*log2(e) and -D shard-major [BH][P][n_pad] fp32,
 // then (one launch per ring step only) the dK~ and dV~ accumulator buffers X
@@ -940,6 +1124,13 @@ int ring_attn_check(ring_attn_t h, void* stream) {
   if (!h->ready) return RING_OK;
   RA_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
   RA_CUDA(cudaStreamSynchronize(h->side), "cudaStreamSynchronize");
+  if (h->pipe) {
+    // ring_attn_fwd_host: its copy streams, and the group handle's kernels
+    RA_CUDA(cudaStreamSynchronize(h->pipe->in), "cudaStreamSynchronize");
+    RA_CUDA(cudaStreamSynchronize(h->pipe->out), "cudaStreamSynchronize");
+    int rc = ring_attn_check(h->pipe->sub, stream);
+    if (rc) return rc;
+  }
   int words[2] = {0, 0};
   RA_CUDA(cudaMemcpy(words, h->d_err, sizeof words, cudaMemcpyDeviceToHost), "cudaMemcpy(error word)");
   if (words[0] != 0) {

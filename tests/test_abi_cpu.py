@@ -75,6 +75,7 @@ def test_calls_reject_null_arguments_without_a_gpu(lib):
     assert lib.ring_attn_merge(h, st, st, None) == _lib.RING_ERR_INVALID_ARG
     assert lib.ring_attn_fwd(h, None, None, None, None, None, None, None) == _lib.RING_ERR_INVALID_ARG
     assert lib.ring_attn_block_partial(h, 0, 0, None, None, None, st, 0, None) == _lib.RING_ERR_INVALID_ARG
+    assert lib.ring_attn_fwd_host(h, None, None, None, None, None, None) == _lib.RING_ERR_INVALID_ARG
     assert lib.ring_attn_set_option(h, 99, 1) == _lib.RING_ERR_INVALID_ARG
     for mode in (0, 1, 2):
         assert lib.ring_attn_set_option(h, _lib.RING_OPT_ROTATION, mode) == 0
