@@ -884,9 +884,15 @@ int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, co
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* nlse2 = reinterpret_cast<float*>(ws + w.lse_off);
   float* nD = reinterpret_cast<float*>(ws + w.d_off);
-  float* acc_k[2] = {reinterpret_cast<float*>(ws + w.acc_off), reinterpret_cast<float*>(ws + w.acc_off + 2 * w.acc_bytes)};
-  float* acc_v[2] = {reinterpret_cast<float*>(ws + w.acc_off + w.acc_bytes),
-                     reinterpret_cast<float*>(ws + w.acc_off + 3 * w.acc_bytes)};
+  // the accumulator buffers exist in the per-step schedule's workspace only
+  float* acc_k[2] = {nullptr, nullptr};
+  float* acc_v[2] = {nullptr, nullptr};
+  if (!lap) {
+    acc_k[0] = reinterpret_cast<float*>(ws + w.acc_off);
+    acc_k[1] = reinterpret_cast<float*>(ws + w.acc_off + 2 * w.acc_bytes);
+    acc_v[0] = reinterpret_cast<float*>(ws + w.acc_off + w.acc_bytes);
+    acc_v[1] = reinterpret_cast<float*>(ws + w.acc_off + 3 * w.acc_bytes);
+  }
 
   // shard views of the natural-order bf16 tensors (box 64 columns x 128 rows)
   const bool striped = p.layout == RING_LAYOUT_STRIPED;

@@ -28,6 +28,12 @@
 //                      S = Q K^T,  dP = dO V^T,  dS by the query-row threads,
 //                      dQ~ += dS K              (A operand in TMEM)
 //                    dQ~ stays with its owner: the running value lives in dq.
+// Lap schedule (kLap; one launch of each kernel for the whole ring): a
+// dK/dV CTA owns one key tile of block j and makes the block's lap itself,
+// visiting the shards j, j + 1, .. in step order, and a dQ CTA owns one
+// query tile of shard r and visits the blocks r, r - 1, ..; the
+// accumulators stay in TMEM from the first visit to the last.  Same MMAs
+// on the same values in the same order as the per-step launches.
 // Every MMA shape is one the forward kernel uses (S = Q K^T with both
 // operands K-major; O += P V with P in TMEM and V MN-major): each operand
 // here is a 128-row tile of a natural-order tensor loaded by TMA with the
