@@ -266,13 +266,14 @@ class RingAttention:
         for t, want in ((q_host, shape), (k_host, kv_shape), (v_host, kv_shape)):
             if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or tuple(t.shape) != want:
                 raise ValueError(f"q must be a contiguous CPU bfloat16 tensor {shape}, k, v {kv_shape}")
+        for t, want in ((out_host, shape), (lse_host, shape[:3])):
+            if t is not None and (t.dtype != torch.float32 or t.is_cuda or not t.is_contiguous() or
+                                  tuple(t.shape) != want):
+                raise ValueError(f"out, lse must be contiguous CPU float32 tensors {shape}, {shape[:3]}")
         if out_host is None:
             out_host = torch.empty(shape, dtype=torch.float32, pin_memory=True)
         if lse_host is None:
             lse_host = torch.empty(shape[:3], dtype=torch.float32, pin_memory=True)
-        for t, want in ((out_host, shape), (lse_host, shape[:3])):
-            if t.dtype != torch.float32 or t.is_cuda or not t.is_contiguous() or tuple(t.shape) != want:
-                raise ValueError(f"out, lse must be contiguous CPU float32 tensors {shape}, {shape[:3]}")
         if stream is None:
             stream = torch.cuda.current_stream()
         _lib.check(self._lib.ring_attn_fwd_host(self.handle, _ptr(q_host), _ptr(k_host), _ptr(v_host),

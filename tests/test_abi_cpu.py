@@ -101,6 +101,26 @@ def test_workspace_size(lib):
     att.close()
 
 
+def test_fwd_host_checks_its_arguments(lib):
+    """RingAttention.fwd_host rejects tensors of the wrong place, dtype or
+    shape before any device work (host bf16 q, k, v; host fp32 out, lse)."""
+    import torch
+
+    att = ra.RingAttention(1, 2, 256, 64, 2, causal=True, layout="striped")
+    q = torch.zeros(1, 2, 256, 64, dtype=torch.bfloat16)
+    bad = [
+        (q.float(), q, q, None, None),  # q not bf16
+        (q, q[:, :1].contiguous(), q, None, None),  # k of the wrong shape
+        (q, q, q.transpose(2, 3), None, None),  # v not contiguous
+        (q, q, q, torch.zeros(1, 2, 256, 64, dtype=torch.bfloat16), None),  # out not fp32
+        (q, q, q, None, torch.zeros(1, 2, 255)),  # lse of the wrong shape
+    ]
+    for args in bad:
+        with pytest.raises(ValueError):
+            att.fwd_host(*args)
+    att.close()
+
+
 def test_bwd_workspace_size_follows_the_schedule(lib):
     """The backward's workspace: -lse log2(e) and -D per row (shard-major,
     rows padded to whole tiles), plus, for one launch per ring step only,
