@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--bwd-per-step", action="store_true",
                     help="with --bwd: one dK/dV and one dQ launch per ring step (RING_OPT_BWD_LAP 0) instead "
                          "of one launch per kernel for the whole ring")
+    ap.add_argument("--merge", action="store_true",
+                    help="time the standalone merge of two fp32 states (ring_attn_merge) of one shard instead")
     ap.add_argument("--decode", type=int, default=0, metavar="LQ",
                     help="measure split-K/V decode of LQ new queries over the workload's K/V cache instead")
     return ap.parse_args()
@@ -534,12 +536,74 @@ def run_bwd(args, w):
     att.close()
 
 
+def run_merge(args, w):
+    """ring_attn_merge of two fp32 states of one shard of the workload
+    (B*H*n rows; 3*(d+2)*4 algorithmic bytes a row: a and b read, a
+    written), in place into a, K times.  Each merge is timed alone with
+    CUDA events after a 256 MB write that flushes L2 (the two states, 68 MB
+    each at the 128K workload, would otherwise partly stay in L2)."""
+    import torch
+
+    import ring_sequence_parallelism_gb300 as ra
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    rows = (w.B, w.H, w.n)
+
+    def state():
+        m = torch.randn(rows, device="cuda", generator=g)
+        l = torch.rand(rows, device="cuda", generator=g) + 0.5
+        o = torch.randn(rows + (w.d,), device="cuda", generator=g)
+        return m, l, o
+
+    a, b = state(), state()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        att.merge(a, b)
+    att.check()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            flush.fill_(1)
+            e0.record(stream)
+            att.merge(a, b)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    att.check()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / args.steps
+    n_rows = w.B * w.H * w.n
+    bytes_ = n_rows * 3 * (w.d + 2) * 4
+    gbs = bytes_ / (ms * 1e-3) / 1e9
+    pk, pk_kind = peaks()
+    hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    line = {
+        "metric": "merge of two fp32 online-softmax states (ring_attn_merge), algorithmic HBM GB/s",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+        "config": dict(config_of(w), rows=n_rows, l2="L2 flushed (256 MB write) before each timed merge"),
+        "roofline": {"bound": "hbm", "kernel": "merge_kernel", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "peak_kind": f"hbm_gbs ({pk_kind})", "traffic": None,
+                     "algorithmic": "3*(d+2)*4 bytes per row"},
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    att.close()
+
+
 def main():
     args = parse()
     from ring_sequence_parallelism_gb300.inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]
-    if args.decode > 0:
+    if args.merge:
+        run_merge(args, w)
+    elif args.decode > 0:
         run_decode(args, w)
     elif args.bwd:
         run_bwd(args, w)
