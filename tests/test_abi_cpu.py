@@ -36,6 +36,20 @@ def test_header_declares_the_abi():
     assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
 
 
+def test_header_compiles_as_plain_c():
+    """include/ringattn.h is a C header: plain C99 with warnings on, no C++
+    or CUDA types in the signatures."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    r = subprocess.run([cc, "-x", "c", "-std=c99", "-fsyntax-only", "-Wall", "-Wextra", "-Werror", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_symbol(lib):
     for name in declared_symbols():
         assert hasattr(lib, name), name
