@@ -50,6 +50,27 @@ def test_header_compiles_as_plain_c():
     assert r.returncode == 0, r.stderr
 
 
+def test_c_program_against_the_library(lib, tmp_path):
+    """tests/c_abi_host.c, a plain C program, built against the header and
+    linked with libringattn.so, runs the host-side calls (no GPU needed)."""
+    import shutil
+    import subprocess
+
+    from ring_sequence_parallelism_gb300 import build
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(build.LIBRARY)
+    exe = str(tmp_path / "c_abi_host")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c_abi_host.c"), "-o", exe, "-L", libdir, "-lringattn",
+                        "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
 def test_library_exports_every_symbol(lib):
     for name in declared_symbols():
         assert hasattr(lib, name), name
