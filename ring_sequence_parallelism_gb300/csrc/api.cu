@@ -814,25 +814,38 @@ int ring_attn_fwd_host(ring_attn_t h, const void* q, const void* k, const void* 
             "cudaMemcpyAsync(q)");
     RA_CUDA(cudaEventRecord(hp->ev_in[g], hp->in), "cudaEventRecord");
   }
-  for (int g = 0; g < groups; ++g) {
-    RA_CUDA(cudaStreamWaitEvent(cs, hp->ev_in[g], 0), "cudaStreamWaitEvent");
+  // Every group's forward and output copies.  Whatever happens, the copy
+  // streams are closed out below, so the caller's stream and the next call
+  // order after everything this call queued.
+  rc = RING_OK;
+  for (int g = 0; g < groups && rc == RING_OK; ++g) {
     float* o_dev = reinterpret_cast<float*>(dev + hp->o_off + g * o_b);
     float* l_dev = reinterpret_cast<float*>(dev + hp->l_off + g * l_b);
+    cudaError_t e = cudaStreamWaitEvent(cs, hp->ev_in[g], 0);
+    if (e != cudaSuccess) {
+      rc = fail(RING_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(e));
+      break;
+    }
     if ((rc = ring_attn_fwd(hp->sub, dev + hp->q_off + g * q_b, dev + hp->k_off + g * kv_b,
                             dev + hp->v_off + g * kv_b, o_dev, l_dev, dev + hp->ws_off, stream)))
-      return rc;
-    RA_CUDA(cudaEventRecord(hp->ev_comp[g], cs), "cudaEventRecord");
-    RA_CUDA(cudaStreamWaitEvent(hp->out, hp->ev_comp[g], 0), "cudaStreamWaitEvent");
-    RA_CUDA(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out) + g * o_b, o_dev, o_b, cudaMemcpyDeviceToHost, hp->out),
-            "cudaMemcpyAsync(out)");
-    RA_CUDA(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + g * l_b, l_dev, l_b, cudaMemcpyDeviceToHost, hp->out),
-            "cudaMemcpyAsync(lse)");
+      break;
+    if ((e = cudaEventRecord(hp->ev_comp[g], cs)) == cudaSuccess &&
+        (e = cudaStreamWaitEvent(hp->out, hp->ev_comp[g], 0)) == cudaSuccess &&
+        (e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out) + g * o_b, o_dev, o_b, cudaMemcpyDeviceToHost,
+                             hp->out)) == cudaSuccess)
+      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + g * l_b, l_dev, l_b, cudaMemcpyDeviceToHost, hp->out);
+    if (e != cudaSuccess) rc = fail(RING_ERR_CUDA, std::string("output copy: ") + cudaGetErrorString(e));
   }
-  // the caller's stream completes after the last output copy
+  // the caller's stream completes after the last output copy (and after
+  // the copy-in stream, in case a failure left copies there unwaited)
   RA_CUDA(cudaEventRecord(hp->ev_done, hp->out), "cudaEventRecord");
   hp->have_done = true;
   RA_CUDA(cudaStreamWaitEvent(cs, hp->ev_done, 0), "cudaStreamWaitEvent");
-  return RING_OK;
+  if (rc != RING_OK) {
+    RA_CUDA(cudaEventRecord(hp->ev_start, hp->in), "cudaEventRecord");
+    RA_CUDA(cudaStreamWaitEvent(cs, hp->ev_start, 0), "cudaStreamWaitEvent");
+  }
+  return rc;
 }
 
 // ---------------------------------------------------------------- backward
