@@ -375,6 +375,15 @@ RINGATTN_API int ring_attn_set_option(ring_attn_t h, int option, long long value
  * kernel.  Synchronises on the recorded events. */
 RINGATTN_API int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float* wait_ms, float* pack_ms);
 
+/* The other side of the overlap check of the last timed ring_attn_fwd
+ * ([RA-CN] "如何判断通信是否真的被覆盖": besides compute waiting for the
+ * communication, record how long the communication waits for the buffer to
+ * be released): release_wait_ms[s] (P entries, ms) is the time the side
+ * stream spent, before the copy that feeds step s, waiting for step s - 2 to
+ * release the buffer it fills (0 where no copy fed step s).  Needs
+ * RING_OPT_TIMING; synchronises on the recorded events. */
+RINGATTN_API int ring_attn_get_release_wait(ring_attn_t h, float* release_wait_ms);
+
 /* Synchronise `stream` and report any device-side error recorded by this
  * handle's kernels since the last check (RING_ERR_TIMEOUT for a wait that
  * ran out), clearing it. */
@@ -394,7 +403,8 @@ RINGATTN_API int ring_attn_check(ring_attn_t h, void* stream);
  *           error flags of this call (0 = ok, nonzero = a bounded wait ran
  *           out), written on `stream` at the end of the call
  * Errors: RING_ERR_UNSUPPORTED when the problem's scratch
- * (4*B*H*N*d + 4*B*H*N bytes, plus alignment) exceeds the array; otherwise
+ * (4*B*Hkv*N*d bytes of packed K and V, Hkv the K/V heads, plus
+ * 4*B*H*N bytes of l and alignment) exceeds the array; otherwise
  * as ring_attn_fwd.  Every step reads its block straight from the packed
  * buffer (no rotation copies); the result equals ring_attn_fwd's.
  * The call allocates nothing.  Its first call on a device, with that device

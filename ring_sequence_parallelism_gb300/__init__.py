@@ -310,7 +310,10 @@ class RingAttention:
         k, c, w = (ctypes.c_float * P)(), (ctypes.c_float * P)(), (ctypes.c_float * P)()
         pk = ctypes.c_float()
         _lib.check(self._lib.ring_attn_get_timing(self.handle, k, c, w, ctypes.byref(pk)))
-        return {"kernel_ms": list(k), "copy_ms": list(c), "wait_ms": list(w), "pack_ms": pk.value}
+        rw = (ctypes.c_float * P)()
+        _lib.check(self._lib.ring_attn_get_release_wait(self.handle, rw))
+        return {"kernel_ms": list(k), "copy_ms": list(c), "wait_ms": list(w), "pack_ms": pk.value,
+                "release_wait_ms": list(rw)}
 
     def check(self, stream=None):
         ring_attn_check(self.handle, stream)

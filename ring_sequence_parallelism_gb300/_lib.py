@@ -63,6 +63,7 @@ SIGNATURES = {
     "ring_attn_set_option": (_i, [_vp, _i, _ll]),
     "ring_attn_set_segments": (_i, [_vp, _pll, _i]),
     "ring_attn_get_timing": (_i, [_vp, _pf, _pf, _pf, _pf]),
+    "ring_attn_get_release_wait": (_i, [_vp, _pf]),
     "ring_attn_check": (_i, [_vp, _vp]),
     "ring_attn_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ring_attn_bwd_workspace_size": (_i, [_vp, ctypes.POINTER(ctypes.c_size_t)]),

@@ -144,6 +144,7 @@ struct ring_attn {
   cudaEvent_t packed = nullptr;
   std::vector<cudaEvent_t> landed, released;
   std::vector<cudaEvent_t> tk0, tk1, tc0, tc1, tw0, tw1;
+  std::vector<cudaEvent_t> tr0;  // side stream, before its wait for released[s-1] (then tc0)
   std::vector<cudaEvent_t> tbk0, tbk1, tbq0, tbq1;  // backward: dK/dV and dQ kernels per step
   cudaEvent_t tbp0 = nullptr, tbp1 = nullptr;          // backward preprocessing
   bool bwd_timed_valid = false;
@@ -161,6 +162,7 @@ struct ring_attn {
 namespace ringattn {
 const Plan& handle_plan(const ring_attn* h) { return h->plan; }
 unsigned long long handle_wait_limit(const ring_attn* h) { return h->wait_limit_ns; }
+int handle_debug_drop_v(const ring_attn* h) { return h->debug_drop_v; }
 }  // namespace ringattn
 
 namespace {
@@ -211,7 +213,8 @@ int ensure_device(ring_attn* h) {
   RA_CUDA(cudaEventCreateWithFlags(&h->packed, cudaEventDisableTiming), "cudaEventCreate");
   if ((rc = make_events(h->landed, P, cudaEventDisableTiming))) return rc;
   if ((rc = make_events(h->released, P, cudaEventDisableTiming))) return rc;
-  for (auto* v : {&h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1, &h->tbk0, &h->tbk1, &h->tbq0, &h->tbq1})
+  for (auto* v : {&h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1, &h->tr0, &h->tbk0, &h->tbk1, &h->tbq0,
+                  &h->tbq1})
     if ((rc = make_events(*v, P, cudaEventDefault))) return rc;
   RA_CUDA(cudaEventCreate(&h->tp0), "cudaEventCreate");
   RA_CUDA(cudaEventCreate(&h->tp1), "cudaEventCreate");
@@ -668,6 +671,7 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     for (int r = 0; r < P; ++r) any = any || send[r];
     if (!any) continue;
     // fill the other buffer once step s-1 has released it (and written it)
+    if (timing) RA_CUDA(cudaEventRecord(h->tr0[s + 1], h->side), "cudaEventRecord");
     RA_CUDA(cudaStreamWaitEvent(h->side, s == 0 ? h->packed : h->released[s - 1], 0), "cudaStreamWaitEvent");
     if (timing) RA_CUDA(cudaEventRecord(h->tc0[s + 1], h->side), "cudaEventRecord");
     // runs of consecutive slots r0..r1 (r1 < P-1) go to r0+1..r1+1; slot P-1 goes to 0
@@ -1134,6 +1138,20 @@ int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float*
     RA_CUDA(cudaEventSynchronize(h->tp1), "cudaEventSynchronize");
     RA_CUDA(cudaEventElapsedTime(&ms, h->tp0, h->tp1), "cudaEventElapsedTime");
     *pack_ms = ms;
+  }
+  return RING_OK;
+}
+
+int ring_attn_get_release_wait(ring_attn_t h, float* release_wait_ms) {
+  if (!h || !release_wait_ms) return fail(RING_ERR_INVALID_ARG, "NULL argument");
+  if (!h->timed_valid) return fail(RING_ERR_INVALID_ARG, "no timed ring_attn_fwd recorded (set RING_OPT_TIMING)");
+  for (int s = 0; s < h->plan.P; ++s) {
+    float ms = 0.f;
+    if (s < (int)h->copied.size() && h->copied[s]) {
+      RA_CUDA(cudaEventSynchronize(h->tc0[s]), "cudaEventSynchronize");
+      RA_CUDA(cudaEventElapsedTime(&ms, h->tr0[s], h->tc0[s]), "cudaEventElapsedTime");
+    }
+    release_wait_ms[s] = ms;
   }
   return RING_OK;
 }

@@ -116,11 +116,15 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
   const size_t need = kErrBytes + 2 * kv_bytes + l_bytes;
   if (need > kScratchBytes) {
     char buf[240];
-    const size_t max_rows = (kScratchBytes - kErrBytes - 3 * 256) / ((size_t)p.d * 4 + 4);
+    // per query row (B*H*N of them): its l (4 bytes) and 1/G of a K/V head
+    // row of K and V (2 tensors x d bf16 values), G query heads per K/V head
+    const size_t G = (size_t)(p.H / p.Hkv);
+    const size_t max_rows = (kScratchBytes - kErrBytes - 3 * 256) * G / (4 * G + (size_t)p.d * 4);
     std::snprintf(buf, sizeof buf,
                   "ring_attn_fwd_noalloc: this problem needs %zu bytes of scratch, more than the fixed %zu-byte "
-                  "array (B*H*N up to about %zu at d=%d); use ring_attn_fwd with a workspace",
-                  need, kScratchBytes, max_rows, p.d);
+                  "array (B*H*N up to about %zu at d=%d with %zu query heads per K/V head); use ring_attn_fwd "
+                  "with a workspace",
+                  need, kScratchBytes, max_rows, p.d, G);
     return report_error(RING_ERR_UNSUPPORTED, buf);
   }
   int dev = -1;
@@ -177,6 +181,7 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
   a.row_i = p.layout == RING_LAYOUT_STRIPED ? P : 1;
   a.err = err;
   a.wait_limit_ns = handle_wait_limit(h);
+  a.debug_drop_v = handle_debug_drop_v(h);  // the bounded-wait test hook, as in ring_attn_fwd
   a.n = (int)p.n;
   a.P = P;
   a.BH = BH;

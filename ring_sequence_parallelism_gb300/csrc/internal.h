@@ -182,6 +182,7 @@ int tensor_map_4d(void* map, const void* base, const unsigned long long dims[4],
 // The handle's plan and wait limit, for translation units outside api.cu.
 const Plan& handle_plan(const ring_attn* h);
 unsigned long long handle_wait_limit(const ring_attn* h);
+int handle_debug_drop_v(const ring_attn* h);  // RING_OPT_DEBUG_DROP_V_LOADS
 int block_partial_smem_bytes(int d);
 // CTAs of one block-partial launch: one per (pair of query tiles, shard, head).
 int block_partial_grid(int T, int n_active, int BH);
