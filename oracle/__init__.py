@@ -16,6 +16,7 @@ Functions mirror the C entry points; every array is numpy:
   naive_block_sum(q, k, v, P, causal, layout)
   dense_bwd(q, k, v, dout, causal)          -> dq, dk, dv [BH,N,d]
   dense_bwd_rows(q, k, v, dout, causal, qrows, krows)
+  dense_bwd_keys(q, k, v, dout, out, lse, causal, krows) (from the forward's statistics)
   ring_bwd(q, k, v, dout, out, lse, P, causal, layout, visits=False)
 q, k, v are bf16 bit patterns (uint16) shaped [BH, N, d] in natural order,
 or torch bf16 tensors (converted with ``bf16_bits``).
@@ -117,6 +118,8 @@ class Oracle:
         L.oracle_dense_bwd.restype = _I
         L.oracle_dense_bwd_rows.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _P, _L, _P, _L, _P, _P, _P, _P, _I]
         L.oracle_dense_bwd_rows.restype = _I
+        L.oracle_dense_bwd_keys.argtypes = [_I, _L, _I, _I, _L, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P, _I]
+        L.oracle_dense_bwd_keys.restype = _I
         L.oracle_ring_bwd.argtypes = [_I, _L, _I, _I, _I, _L, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I]
         L.oracle_ring_bwd.restype = _I
 
@@ -275,6 +278,25 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"oracle_dense_bwd_rows failed: {rc}")
         return dq, dk, dv
+
+    def dense_bwd_keys(self, q, k, v, dout, out, lse, causal: bool, krows, window: int = 0, segments=None):
+        """dk, dv at key positions krows ([BH][len(krows)][d]) from the
+        forward's out and lse (float64, natural order, e.g. from ``dense``)."""
+        q, k, v = self._qkv(q, k, v)
+        do = bf16_bits(dout)
+        BH, N, d = q.shape
+        out = np.ascontiguousarray(out, np.float64).reshape(BH, N, d)
+        lse = np.ascontiguousarray(lse, np.float64).reshape(BH, N)
+        kr, nk = self._rows(krows, N)
+        dk = np.empty((BH, nk, d), np.float64)
+        dv = np.empty((BH, nk, d), np.float64)
+        seg = _segment_ids(segments, N)
+        rc = self.lib.oracle_dense_bwd_keys(BH, N, d, int(causal), int(window), _ptr(seg), _ptr(q), _ptr(k), _ptr(v),
+                                            _ptr(do), _ptr(out), _ptr(lse), nk, _ptr(kr), _ptr(dk), _ptr(dv),
+                                            self.nthreads)
+        if rc != 0:
+            raise RuntimeError(f"oracle_dense_bwd_keys failed: {rc}")
+        return dk, dv
 
     def ring_bwd(self, q, k, v, dout, out, lse, P: int, causal: bool, layout: int, visits: bool = False,
                  window: int = 0, segments=None):

@@ -710,6 +710,55 @@ int oracle_dense_bwd_rows(int BH, long N, int d, int causal, long window, const 
 }
 
 /*
+ * dK and dV at sampled key positions from the forward's saved statistics
+ * (the data the ring's backward also starts from: [RA-CN] "Backward
+ * 需要让梯度也沿环传播" recomputes the probabilities from the saved logsumexp).
+ * For key kk and every query t allowed to see it:
+ *   D_t    = dO_t . out_t
+ *   P_tk   = exp(scale q_t . k_kk - lse_t)
+ *   dK_kk += scale P_tk (dO_t . v_kk - D_t) q_t
+ *   dV_kk += P_tk dO_t
+ * out [BH][N][d] and lse [BH][N] are doubles in natural order (the dense
+ * forward's); dk, dv are [BH][nk][d].  With the exact out and lse this is
+ * the plain definition of the two gradients; the cost per key is one pass
+ * over its queries, so keys that every query sees stay cheap at any N.
+ */
+int oracle_dense_bwd_keys(int BH, long N, int d, int causal, long window, const long* seg, const uint16_t* q,
+                          const uint16_t* k, const uint16_t* v, const uint16_t* dout, const double* out,
+                          const double* lse, long nk, const long* krows, double* dk, double* dv, int nthreads) {
+  if (BH <= 0 || N <= 0 || d <= 0 || nk < 0) return -1;
+  set_threads(nthreads);
+  const double scale = 1.0 / sqrt((double)d);
+  const long total = (long)BH * nk;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long idx = 0; idx < total; ++idx) {
+    const long bh = idx / nk, kk = krows[idx % nk];
+    const uint16_t* qb = q + (size_t)bh * N * d;
+    const uint16_t* ob = dout + (size_t)bh * N * d;
+    const uint16_t* krow = k + ((size_t)bh * N + kk) * d;
+    const uint16_t* vrow = v + ((size_t)bh * N + kk) * d;
+    double* gk = dk + (size_t)idx * d;
+    double* gv = dv + (size_t)idx * d;
+    for (int c = 0; c < d; ++c) gk[c] = gv[c] = 0.0;
+    for (long t = 0; t < N; ++t) {
+      if (!allowed(causal, window, seg, t, kk)) continue;
+      const uint16_t* qrow = qb + (size_t)t * d;
+      const uint16_t* dorow = ob + (size_t)t * d;
+      const double* orow = out + ((size_t)bh * N + t) * d;
+      double Dt = 0.0;
+      for (int c = 0; c < d; ++c) Dt += widen_bf16(dorow[c]) * orow[c];
+      const double p = exp(scale * dot_q_k(qrow, krow, d) - lse[(size_t)bh * N + t]);
+      const double ds = p * (dot_q_k(dorow, vrow, d) - Dt);
+      for (int c = 0; c < d; ++c) {
+        gk[c] += scale * ds * widen_bf16(qrow[c]);
+        gv[c] += p * widen_bf16(dorow[c]);
+      }
+    }
+  }
+  return 0;
+}
+
+/*
  * Ring simulation of the backward ([RA-CN] "Backward 需要让梯度也沿环传播": the
  * owner of a query shard accumulates its dQ from every K/V block; the dK and
  * dV of a travelling block accumulate the contributions of each query owner

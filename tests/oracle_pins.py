@@ -505,6 +505,21 @@ def pin_bwd_rows_match(orc):
         _close(dv, full[2][:, krows], 1e-13, "rows dv")
 
 
+def pin_bwd_keys_from_forward(orc):
+    """dK and dV from the forward's saved out and lse (the oracle's dense
+    forward) equal the full backward's at every key, causal or not, with a
+    window and with packed documents."""
+    BH, N, d = 2, 28, 8
+    q, k, v, do = (rand_bits((BH, N, d), 370 + x) for x in range(4))
+    keys = list(range(N))
+    for causal, w, seg in ((False, 0, None), (True, 0, None), (True, 6, None), (True, 0, [0, 9, 10, 28])):
+        full = orc.dense_bwd(q, k, v, do, causal, window=w, segments=seg)
+        out, lse = orc.dense(q, k, v, causal, window=w, segments=seg)
+        dk, dv = orc.dense_bwd_keys(q, k, v, do, out, lse, causal, keys, window=w, segments=seg)
+        _close(dk, full[1], 1e-12, f"keys dk causal={causal} w={w} seg={seg}")
+        _close(dv, full[2], 1e-12, f"keys dv causal={causal} w={w} seg={seg}")
+
+
 def pin_ring_bwd_equals_dense(orc):
     """The ring backward (dQ kept by the query owner, dK and dV travelling
     with their block and returning to its owner; [RA-CN] "Backward
@@ -629,6 +644,7 @@ ALL_PINS = [
     pin_bwd_closed_forms,
     pin_bwd_invariants,
     pin_bwd_rows_match,
+    pin_bwd_keys_from_forward,
     pin_ring_bwd_equals_dense,
     pin_segments_independent,
     pin_segments_sdpa,

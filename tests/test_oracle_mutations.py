@@ -64,6 +64,11 @@ MUTATIONS = [
      "const double p = exp(scale * dot_q_k(qrow, krow, d));", None),
     ("sampled backward dV uses the query's q",
      "gv[c] += p * widen_bf16(ob[(size_t)t * d + c]);", "gv[c] += p * widen_bf16(qb[(size_t)t * d + c]);", None),
+    ("backward from saved statistics drops D",
+     "const double ds = p * (dot_q_k(dorow, vrow, d) - Dt);", "const double ds = p * dot_q_k(dorow, vrow, d);", None),
+    ("backward from saved statistics takes D from the wrong row",
+     "const double* orow = out + ((size_t)bh * N + t) * d;", "const double* orow = out + ((size_t)bh * N + kk) * d;",
+     None),
     ("segment rule ignored", "  if (seg && seg[pos_q] != seg[pos_k]) return 0;\n", "", None),
     ("segment rule compares the query with a neighbour",
      "  if (seg && seg[pos_q] != seg[pos_k]) return 0;",
