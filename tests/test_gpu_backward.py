@@ -7,8 +7,9 @@ dQ operand) to bf16 (unit roundoff u = 2^-9), accumulating in fp32.  A
 float64 model of exactly that rounding on N(0, 1) inputs (N = 512..4096,
 d = 64 and 128, causal and not) gives a relative L2 error of 1.5-2.2e-3 and
 a largest element error of 1.2e-3 to 8.1e-3 times the tensor's largest
-magnitude.  The bounds, for each of dq, dk and dv:
-    ||got - ref||_2 <= 1e-2 ||ref||_2   and   max|got - ref| <= 2e-2 max|ref|.
+magnitude; the GPU measures 0.9e-3 to 3.2e-3 on the cases below.  The
+bounds, for each of dq, dk and dv (the second 1.2 times the model's worst):
+    ||got - ref||_2 <= 1e-2 ||ref||_2   and   max|got - ref| <= 1e-2 max|ref|.
 Where the reference is exactly zero (a window of one token: P = 1, so dQ
 and dK vanish), what remains is dS = P (dP - D) with dP = dO . v from the
 tensor cores and D = dO . out from the preprocessing, two fp32 evaluations
@@ -28,7 +29,7 @@ from ring_sequence_parallelism_gb300.inputs import WORKLOADS, make_dout, make_qk
 pytestmark = pytest.mark.gpu
 
 TOL_REL_L2 = 1e-2
-TOL_MAX = 2e-2
+TOL_MAX = 1e-2
 TOL_ZERO_REF = 1e-3
 
 
