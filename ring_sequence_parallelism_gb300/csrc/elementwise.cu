@@ -2,10 +2,8 @@
 // merge of two states, finalize into natural order, and the shard-major
 // packing of K/V into the rotation buffer.
 //
-// All of them move 16-byte vectors with consecutive threads on consecutive
-// addresses; the per-row scalars (m, l) are read by the threads of one row
-// at the same address, which the memory system broadcasts.  Grids are a
-// multiple of the SM count with grid-stride loops.
+// They move 16- or 32-byte vectors with consecutive threads on consecutive
+// addresses.  Grids are a multiple of the SM count with grid-stride loops.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -48,43 +46,97 @@ __global__ void state_init_kernel(float* __restrict__ m, float* __restrict__ l, 
   }
 }
 
+// Vector global accesses of V fp32 values: V = 8 (256 bits, one full
+// 32-byte sector per lane; needs 32-byte alignment) or V = 4 (128 bits).
+template <int V>
+__device__ __forceinline__ void ldv(const float* p, float (&x)[V]);
+template <>
+__device__ __forceinline__ void ldv<8>(const float* p, float (&x)[8]) {
+  asm volatile("ld.global.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7])
+               : "l"(p));
+}
+template <>
+__device__ __forceinline__ void ldv<4>(const float* p, float (&x)[4]) {
+  const float4 t = *reinterpret_cast<const float4*>(p);
+  x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
+}
+template <int V>
+__device__ __forceinline__ void stv(float* p, const float (&x)[V]);
+template <>
+__device__ __forceinline__ void stv<8>(float* p, const float (&x)[8]) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(x[0]), "f"(x[1]),
+               "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void stv<4>(float* p, const float (&x)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+}
+
 // a <- merge(a, b) ([GRA] "Why partial results are allowed to merge";
 // [ZQ]: rescale by exp(old_max - new_max)):
 //   m = max(ma, mb); alpha = e^{ma-m}, beta = e^{mb-m} (0 for an -inf side)
 //   l = alpha la + beta lb;  O~ = alpha O~a + beta O~b
-__global__ void merge_kernel(float* __restrict__ ma, float* __restrict__ la, float4* __restrict__ oa,
-                             const float* __restrict__ mb, const float* __restrict__ lb,
-                             const float4* __restrict__ ob, long long rows, int d4) {
-  // The loop runs per warp (all lanes share `base`, so every lane makes the
-  // same number of trips): the row's scalars are read by all its lanes before
-  // the __syncwarp, and only then overwritten.  d4 (16 or 32) divides 32, so
-  // a row never straddles two warps.
-  const long long total = rows * d4;
+// D / V lanes share a row, V columns each.  The first lane of the row reads
+// the four scalars once, computes alpha and beta and writes m and l; the
+// others get alpha and beta by a shuffle.  Each lane issues the O~ loads of
+// kUnroll rows before any arithmetic, so enough bytes are in flight to keep
+// HBM busy.  The loop is warp-uniform (the shuffles need every lane), with
+// rows past the end masked.
+template <int D, int V>
+__global__ void __launch_bounds__(256) merge_kernel(float* __restrict__ ma, float* __restrict__ la,
+                                                    float* __restrict__ oa, const float* __restrict__ mb,
+                                                    const float* __restrict__ lb, const float* __restrict__ ob,
+                                                    long long rows) {
+  constexpr int TPR = D / V;
+  constexpr int kRowsPerWarp = 32 / TPR;
+  constexpr int kUnroll = 2;
   const int lane = threadIdx.x & 31;
-  for (long long base = blockIdx.x * (long long)blockDim.x + (threadIdx.x & ~31); base < total;
-       base += (long long)gridDim.x * blockDim.x) {
-    const long long x = base + lane;
-    const bool act = x < total;
-    const long long row = act ? x / d4 : 0;
-    float m = 0.f, alpha = 0.f, beta = 0.f, l = 0.f;
-    if (act) {
-      const float m_a = ma[row], m_b = mb[row];
-      m = fmaxf(m_a, m_b);
-      alpha = (m_a == -INFINITY) ? 0.0f : expf(m_a - m);
-      beta = (m_b == -INFINITY) ? 0.0f : expf(m_b - m);
-      l = alpha * la[row] + beta * lb[row];
-      const float4 va = oa[x], vb = ob[x];
-      float4 r;
-      r.x = alpha * va.x + beta * vb.x;
-      r.y = alpha * va.y + beta * vb.y;
-      r.z = alpha * va.z + beta * vb.z;
-      r.w = alpha * va.w + beta * vb.w;
-      oa[x] = r;
+  const int sub = lane % TPR;
+  const int leader = lane - sub;
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const long long nwarps = (long long)gridDim.x * blockDim.x / 32;
+  const long long step = nwarps * kRowsPerWarp;
+  for (long long base = warp * kRowsPerWarp; base < rows; base += step * kUnroll) {
+    float xa[kUnroll][V], xb[kUnroll][V];
+    float sa[kUnroll], sb[kUnroll], sm[kUnroll], sl[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long row = base + u * step + lane / TPR;
+      if (row < rows) {
+        ldv<V>(oa + row * D + sub * V, xa[u]);
+        ldv<V>(ob + row * D + sub * V, xb[u]);
+      }
     }
-    __syncwarp();
-    if (act && x % d4 == 0) {
-      ma[row] = m;
-      la[row] = l;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long row = base + u * step + lane / TPR;
+      sa[u] = sb[u] = sm[u] = sl[u] = 0.0f;
+      if (row < rows && sub == 0) {
+        const float m_a = ma[row], m_b = mb[row];
+        const float m = fmaxf(m_a, m_b);
+        sa[u] = (m_a == -INFINITY) ? 0.0f : expf(m_a - m);
+        sb[u] = (m_b == -INFINITY) ? 0.0f : expf(m_b - m);
+        sm[u] = m;
+        sl[u] = sa[u] * la[row] + sb[u] * lb[row];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const float alpha = __shfl_sync(0xffffffffu, sa[u], leader);
+      const float beta = __shfl_sync(0xffffffffu, sb[u], leader);
+      const long long row = base + u * step + lane / TPR;
+      if (row < rows) {
+        float r[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) r[e] = alpha * xa[u][e] + beta * xb[u][e];
+        stv<V>(oa + row * D + sub * V, r);
+        if (sub == 0) {
+          ma[row] = sm[u];
+          la[row] = sl[u];
+        }
+      }
     }
   }
 }
@@ -199,10 +251,21 @@ int launch_state_init(float* m, float* l, float* o, long long rows, int d, void*
 
 int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* lb, const float* ob,
                  long long rows, int d, void* stream) {
-  const int d4 = d / 4;
   if (rows <= 0) return 0;
-  merge_kernel<<<grid_for(rows * d4, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      ma, la, reinterpret_cast<float4*>(oa), mb, lb, reinterpret_cast<const float4*>(ob), rows, d4);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // 256-bit accesses when both O~ arrays are 32-byte aligned (rows are d
+  // floats, a multiple of 8), else 128-bit ones; each lane takes two rows'
+  // worth of vectors per trip
+  const bool wide = reinterpret_cast<uintptr_t>(oa) % 32 == 0 && reinterpret_cast<uintptr_t>(ob) % 32 == 0;
+  const long long lanes = rows * (d / (wide ? 8 : 4)) / 2;
+  const int grid = grid_for(lanes, 256);
+  if (d == 64) {
+    if (wide) merge_kernel<64, 8><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);
+    else merge_kernel<64, 4><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);
+  } else {
+    if (wide) merge_kernel<128, 8><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);
+    else merge_kernel<128, 4><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);
+  }
   return (int)cudaGetLastError();
 }
 

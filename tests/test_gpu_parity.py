@@ -71,8 +71,12 @@ def random_state(rows, d, seed, empty_frac=0.1):
     return m, l, o
 
 
-@pytest.mark.parametrize("B,H,n,d", [(1, 2, 128, 64), (2, 3, 200, 128), (1, 8, 1024, 128)])
-def test_merge_matches_oracle(B, H, n, d):
+@pytest.mark.parametrize("B,H,n,d,offset", [(1, 2, 128, 64, 0), (2, 3, 200, 128, 0), (1, 8, 1024, 128, 0),
+                                             (2, 3, 200, 128, 4), (1, 2, 131, 64, 4)])
+def test_merge_matches_oracle(B, H, n, d, offset):
+    """The fp32 merge of two fp32 states against the oracle's float64 merge
+    of the same states (<= 1e-5).  offset 4 places both O~ arrays 16 bytes
+    past a 32-byte boundary, so the kernel takes its 128-bit path."""
     P = 2
     att = ra.RingAttention(B, H, n * P, d, P, causal=True, layout="striped")
     rows = B * H * n
@@ -82,8 +86,18 @@ def test_merge_matches_oracle(B, H, n, d):
     a[0][:3] = -np.inf; a[1][:3] = 0; a[2][:3] = 0
     b[0][:2] = -np.inf; b[1][:2] = 0; b[2][:2] = 0
     b[0][5] = a[0][5]
-    ga = tuple(torch.from_numpy(x.reshape((B, H, n) + x.shape[1:])).cuda().contiguous() for x in a)
-    gb = tuple(torch.from_numpy(x.reshape((B, H, n) + x.shape[1:])).cuda().contiguous() for x in b)
+    def to_gpu(x):
+        t = torch.from_numpy(x.reshape((B, H, n) + x.shape[1:]))
+        if x.ndim == 1 or not offset:
+            return t.cuda().contiguous()
+        buf = torch.empty(t.numel() + offset, dtype=t.dtype, device="cuda")
+        g = buf[offset:].view(t.shape)
+        g.copy_(t)
+        assert g.data_ptr() % 32 == 16
+        return g
+
+    ga = tuple(to_gpu(x) for x in a)
+    gb = tuple(to_gpu(x) for x in b)
     att.merge(ga, gb)
     torch.cuda.synchronize()
     m, l, o = (x.cpu().numpy().reshape(rows, -1).squeeze() for x in ga)
