@@ -60,6 +60,12 @@ def parse():
                     help="time the standalone merge of two fp32 states (ring_attn_merge) of one shard instead")
     ap.add_argument("--decode", type=int, default=0, metavar="LQ",
                     help="measure split-K/V decode of LQ new queries over the workload's K/V cache instead")
+    ap.add_argument("--imbalance", action="store_true",
+                    help="print only the per-shard work and time of the 8K causal workloads (contiguous, "
+                         "striped, zigzag)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="leave out the sub-records of the default line (side-stream rotation, per-shard "
+                         "imbalance, the other workloads)")
     return ap.parse_args()
 
 
@@ -286,6 +292,164 @@ def l2_note(w):
     return "inputs (3 x %.1f MB bf16) fit in L2: small case, not a timed workload" % (gb * 1e3)
 
 
+# ------------------------------------------------------------- sub-records
+def measure_imbalance(names=("contiguous-8k", "striped-8k", "zigzag-8k"), reps=5):
+    """Per-shard causal work and time ([GRA] "The causal mask wrecks the load
+    balance"; [RA-CN] "Causal Attention 让环不再完全对称" and
+    "如何判断通信是否真的被覆盖", which lists the spread of step times across
+    ranks).  Every (shard r, step s) block partial is one
+    ring_attn_block_partial launch on shard-major copies of the inputs,
+    timed alone with CUDA events after an L2 flush, the stream backed up so
+    the host's launch cost stays outside the events; the median over `reps`
+    rounds.  A shard's time is the sum of its P launches (skipped blocks
+    launch nothing); a synchronous ring step lasts as long as its slowest
+    shard."""
+    import statistics as st
+
+    import torch
+
+    import ring_sequence_parallelism_gb300 as ra
+    from ring_sequence_parallelism_gb300 import report
+    from ring_sequence_parallelism_gb300.inputs import WORKLOADS, make_workload
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    res = []
+    for name in names:
+        w = WORKLOADS[name]
+        q, k, v = make_workload(w)
+        att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
+        pos = [torch.tensor(report.shard_positions(w.layout, w.n, w.P, r)) for r in range(w.P)]
+        Qs = [q[:, :, p].contiguous().cuda() for p in pos]
+        Ks = [k[:, :, p].contiguous().cuda() for p in pos]
+        Vs = [v[:, :, p].contiguous().cuda() for p in pos]
+        states = [att.new_state() for _ in range(w.P)]
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(w.P)]
+              for _ in range(w.P)]
+        samples = [[[] for _ in range(w.P)] for _ in range(w.P)]  # [s][r]
+        for rep in range(reps + 1):  # round 0 warms up
+            for s in range(w.P):
+                for r in range(w.P):
+                    j = (r - s) % w.P
+                    flush.fill_(rep & 0xFF)
+                    torch.cuda._sleep(100000)
+                    e0, e1 = ev[s][r]
+                    e0.record(stream)
+                    att.block_partial(r, s, Qs[r], Ks[j], Vs[j], states[r], 1 if s > 0 else 0)
+                    e1.record(stream)
+            torch.cuda.synchronize()
+            if rep:
+                for s in range(w.P):
+                    for r in range(w.P):
+                        samples[s][r].append(ev[s][r][0].elapsed_time(ev[s][r][1]))
+        att.check()
+        t = [[st.median(samples[s][r]) for r in range(w.P)] for s in range(w.P)]
+        shard_ms = [sum(t[s][r] for s in range(w.P)) for r in range(w.P)]
+        pairs, tiles = att.shard_work()
+        ring_ms = report.synchronous_ring_ms(t)
+        balanced = sum(shard_ms) / w.P
+        res.append({
+            "workload": name, "layout": w.layout, "P": w.P, "n": w.n, "heads": w.B * w.H,
+            "shard_pairs": pairs,
+            "shard_pairs_closed_form": [w.B * w.H * x for x in report.shard_pairs_closed_form(w.layout, w.n, w.P)],
+            "shard_tiles": tiles, "shard_ms": shard_ms,
+            "pairs_max_over_min": report.imbalance(pairs), "ms_max_over_min": report.imbalance(shard_ms),
+            "step_max_ms": [max(row) for row in t], "synchronous_ring_ms": ring_ms, "balanced_ms": balanced,
+            "ring_over_balanced": ring_ms / balanced,
+        })
+        att.close()
+        del Qs, Ks, Vs, states
+    return {"method": "one ring_attn_block_partial launch per (shard, step), CUDA events, L2 flushed before "
+                      f"each, median of {reps} rounds; shard time = sum of its launches; synchronous ring = sum "
+                      "over steps of the slowest shard",
+            "workloads": res}
+
+
+def measure_side_stream_rotation(att, q, k, v, out, lse, w, warmup=3, steps=3):
+    """RING_OPT_ROTATION = 1, the pages' double-buffered rotation as written
+    ([RA-CN] "双缓冲是重叠成立的基础"; "如何判断通信是否真的被覆盖": compute
+    waiting for the communication, communication waiting for the buffer's
+    release): every step's K/V move is two cudaMemcpyAsync device-to-device
+    copies per tensor on the side stream, ordered by events.  Reports the
+    copy time and rate, the compute stream's exposed wait for each copy, and
+    the side stream's wait for the buffer it fills."""
+    import torch
+
+    import ring_sequence_parallelism_gb300 as ra
+
+    att.set_option(ra.RING_OPT_ROTATION, 1)
+    try:
+        for _ in range(warmup):
+            att.fwd(q, k, v, out, lse)
+        stream = torch.cuda.current_stream()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            att.fwd(q, k, v, out, lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = att.timing()
+        att.check()
+    finally:
+        att.set_option(ra.RING_OPT_ROTATION, 2)
+    ms = e0.elapsed_time(e1) / steps
+    copy_bytes = 2 * 2 * w.B * w.kv_heads * w.N * w.d * 2  # K and V, every slot, read + written
+    copies = [c for c in t["copy_ms"] if c > 0]
+    return {
+        "rotation": "side-stream cudaMemcpyAsync D2D, 2 per tensor per step, events landed/released",
+        "ms_per_step": ms, "tflops": w.flops() / (ms * 1e-3) / 1e12,
+        "step_kernel_ms": t["kernel_ms"], "copy_ms": t["copy_ms"], "copy_total_ms": sum(t["copy_ms"]),
+        "copy_gbs_mean": (copy_bytes / (sum(copies) / len(copies) * 1e-3) / 1e9) if copies else None,
+        "copy_bytes_each": copy_bytes,
+        "exposed_wait_ms": t["wait_ms"], "exposed_wait_total_ms": sum(t["wait_ms"]),
+        "release_wait_ms": t["release_wait_ms"], "release_wait_total_ms": sum(t["release_wait_ms"]),
+    }
+
+
+def measure_workloads(names, peak_burst, warmup=3):
+    """Whole forwards of other workloads, inputs resident; inputs that fit in
+    L2 are flushed (256 MB write) before each timed forward."""
+    import torch
+
+    import ring_sequence_parallelism_gb300 as ra
+    from ring_sequence_parallelism_gb300.inputs import WORKLOADS, make_workload
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    res = []
+    for name in names:
+        w = WORKLOADS[name]
+        q, k, v = (x.to("cuda") for x in make_workload(w))
+        att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
+        out = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+        for _ in range(warmup):
+            att.fwd(q, k, v, out, lse)
+        att.check()
+        small = 3 * w.B * w.H * w.N * w.d * 2 < (129 << 20)
+        steps = 3 if w.N >= (1 << 20) else 10
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            if small:
+                flush.fill_(1)
+            e0.record(stream)
+            att.fwd(q, k, v, out, lse)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        att.check()
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+        tf = w.flops() / (ms * 1e-3) / 1e12
+        res.append({"workload": name, "config": config_of(w), "ms_per_step": ms, "steps": steps, "warmup": warmup,
+                    "tflops": tf, "tokens_per_s": w.B * w.N / (ms * 1e-3), "frac_of_burst": tf / peak_burst,
+                    "l2": "flushed before each forward" if small else "inputs larger than L2"})
+        att.close()
+        del q, k, v, out, lse
+        torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------- our arm
 def run_ours(args, w):
     import torch
@@ -369,6 +533,14 @@ def run_ours(args, w):
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h)),
                "d2h_bytes_per_step": out_h.numel() * 4 + lse_h.numel() * 4}
 
+    extra = {}
+    if world == 1 and not args.no_extra:
+        extra["ring_mode1"] = measure_side_stream_rotation(att, q, k, v, out, lse, w)
+        extra["imbalance"] = measure_imbalance()
+        extra["workloads"] = measure_workloads(
+            [x for x in ("noncausal-512", "contiguous-8k", "striped-8k", "zigzag-8k", "striped-1m") if x != w.name],
+            peak_burst)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, rows_s, threads, desc, secs, _ = oracle_sample(w, q_h, k_h, v_h, args.cpu_seconds)
@@ -384,9 +556,9 @@ def run_ours(args, w):
             "pct_of_bf16_peak": {"sustained": 100 * value / world / peak_sus, "burst": 100 * value / world / peak_burst,
                                  "nominal_2250": 100 * value / world / 2250.0, "source": pk_kind},
             "roofline": {"bound": "tensor", "kernel": "block_partial_kernel<128> (one launch per ring step)",
-                         "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                         "frac": achieved / peak_sus, "peak_kind": f"bf16_tflops_sustained ({pk_kind})",
-                         "frac_of_burst": achieved / peak_burst, "traffic": traffic,
+                         "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                         "frac": achieved / peak_burst, "peak_kind": f"bf16_tflops burst ({pk_kind})",
+                         "frac_of_sustained": achieved / peak_sus, "traffic": traffic,
                          "launches_per_step": w.P, "avg_launch_ms": k_total_ms / w.P},
             "ring": {"step_kernel_ms": kernel_ms, "rotation_copy_ms": copy_ms, "exposed_wait_ms": wait_ms,
                      "pack_ms": pack_ms, "exposed_wait_total_ms": sum(wait_ms),
@@ -399,6 +571,7 @@ def run_ours(args, w):
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        line.update(extra)
         print(json.dumps(line), flush=True)
     att.close()
     if world > 1:
@@ -601,7 +774,12 @@ def main():
     from ring_sequence_parallelism_gb300.inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]
-    if args.merge:
+    if args.imbalance:
+        import torch
+
+        torch.cuda.set_device(dist_env()[2])
+        print(json.dumps({"metric": "per-shard causal work and time", "imbalance": measure_imbalance()}), flush=True)
+    elif args.merge:
         run_merge(args, w)
     elif args.decode > 0:
         run_decode(args, w)
