@@ -138,7 +138,23 @@ typedef enum {
    *   order on the same fp32 values as in mode 0, so the results are
    *   identical.  ring_attn_get_bwd_timing then reports both kernels' times
    *   in entry 0 and zeros in the others. */
-  RING_OPT_BWD_LAP = 5
+  RING_OPT_BWD_LAP = 5,
+  /* How ring_attn_fwd schedules the ring's steps.
+   * 0 (default): one step kernel per ring step, the running state (m, l, O~)
+   *   passing from step to step through the workspace, and the K/V blocks
+   *   moved as RING_OPT_ROTATION says.
+   * 1: one launch for the whole ring ("lap"): a CTA owning a pair of query
+   *   tiles of shard r meets blocks r, r-1, .. in step order, the state held
+   *   on chip from the first step to the last, and the blocks read in place
+   *   from the packed buffer (no rotation; RING_OPT_ROTATION is ignored).
+   *   Same arithmetic per key tile; the result matches mode 0 within the
+   *   parity tolerances, not bit for bit (mode 0 visits the key tiles of a
+   *   block without a diagonal in a rotated order, and stores m between
+   *   steps in natural-log units, so P is rounded against other running
+   *   maxima).  Worth it where a step has little work per query tile
+   *   (sliding windows, packed documents).
+   *   ring_attn_get_timing then reports the launch in kernel_ms[0]. */
+  RING_OPT_FWD_LAP = 6
 } ring_option_t;
 
 /* Create a handle for one problem shape.  Validates the shape and builds the

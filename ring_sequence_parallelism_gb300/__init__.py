@@ -19,7 +19,7 @@ import ctypes
 from . import _lib
 from ._lib import (RING_BLOCK_DIAG, RING_BLOCK_FULL, RING_BLOCK_PARTIAL, RING_BLOCK_SKIP,  # noqa: F401
                    RING_LAYOUT_CONTIGUOUS, RING_LAYOUT_STRIPED, RING_LAYOUT_ZIGZAG, RING_OPT_DEBUG_DROP_V_LOADS,
-                   RING_OPT_WINDOW, RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_BWD_LAP,
+                   RING_OPT_WINDOW, RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_BWD_LAP, RING_OPT_FWD_LAP,
                    RING_OPT_WAIT_LIMIT_NS,
                    RingAttnError, RingState)
 

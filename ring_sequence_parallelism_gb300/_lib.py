@@ -26,7 +26,7 @@ RING_LAYOUT_STRIPED = 1
 RING_LAYOUT_ZIGZAG = 2
 RING_BLOCK_SKIP, RING_BLOCK_FULL, RING_BLOCK_DIAG, RING_BLOCK_PARTIAL = 0, 1, 2, 3
 (RING_OPT_ROTATION, RING_OPT_TIMING, RING_OPT_WAIT_LIMIT_NS, RING_OPT_DEBUG_DROP_V_LOADS, RING_OPT_WINDOW,
- RING_OPT_BWD_LAP) = 0, 1, 2, 3, 4, 5
+ RING_OPT_BWD_LAP, RING_OPT_FWD_LAP) = 0, 1, 2, 3, 4, 5, 6
 
 # Every symbol include/ringattn.h declares, with (restype, argtypes).
 _vp = ctypes.c_void_p

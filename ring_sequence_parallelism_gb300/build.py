@@ -24,7 +24,8 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE]
-SOURCES = ["planner.cpp", "api.cu", "elementwise.cu", "block_partial.cu", "block_backward.cu", "fwd_noalloc.cu"]
+SOURCES = ["planner.cpp", "api.cu", "elementwise.cu", "block_partial.cu", "block_lap.cu", "block_backward.cu",
+           "fwd_noalloc.cu"]
 
 
 def nvcc() -> str:

@@ -135,6 +135,7 @@ struct ring_attn {
   int rotation = 2;
   int timing = 0;
   int bwd_lap = 1;       // RING_OPT_BWD_LAP
+  int fwd_lap = 0;       // RING_OPT_FWD_LAP
   int debug_drop_v = 0;
   unsigned long long wait_limit_ns = 2000000000ULL;
   // device resources, made on first use
@@ -208,6 +209,7 @@ int ensure_device(ring_attn* h) {
   if (rc) return rc;
   RA_CUDA((cudaError_t)prepare_block_partial_kernels(), "cudaFuncSetAttribute");
   RA_CUDA((cudaError_t)prepare_backward_kernels(), "cudaFuncSetAttribute (backward)");
+  RA_CUDA((cudaError_t)prepare_fwd_lap_kernels(), "cudaFuncSetAttribute (lap)");
   RA_CUDA(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking), "cudaStreamCreate");
   const int P = h->plan.P;
   RA_CUDA(cudaEventCreateWithFlags(&h->packed, cudaEventDisableTiming), "cudaEventCreate");
@@ -464,6 +466,10 @@ int ring_attn_set_option(ring_attn_t h, int option, long long value) {
       if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "backward lap must be 0 or 1");
       h->bwd_lap = (int)value;
       return RING_OK;
+    case RING_OPT_FWD_LAP:
+      if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "forward lap must be 0 or 1");
+      h->fwd_lap = (int)value;
+      return RING_OK;
     case RING_OPT_DEBUG_DROP_V_LOADS:
       if (value != 0 && value != 1) return fail(RING_ERR_INVALID_ARG, "debug option must be 0 or 1");
       h->debug_drop_v = (int)value;
@@ -625,6 +631,23 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
   a.kv_mode = rotate ? kKvSlotR : kKvSlotJ;
   h->copied.assign((size_t)P, 0);
 
+  if (h->fwd_lap) {
+    // the whole ring in one launch, blocks read in place (slot j = block j)
+    a.kv_mode = kKvSlotJ;
+    a.finalize = 1;
+    a.n_active = P;
+    if (timing) RA_CUDA(cudaEventRecord(h->tk0[0], cs), "cudaEventRecord");
+    RA_CUDA((cudaError_t)launch_fwd_lap(a, &qm, &km[0], &vm[0], p.d, cs), "lap kernel launch");
+    if (timing) {
+      for (int s = 0; s < P; ++s) {
+        if (s > 0) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
+        RA_CUDA(cudaEventRecord(h->tk1[s], cs), "cudaEventRecord");
+      }
+    }
+    h->timed_valid = timing;
+    return RING_OK;
+  }
+
   // side-stream copy of slots [r0, r0 + cnt) of buffer `cur` to [dst0, dst0 + cnt) of the other
   auto copy_slots = [&](int cur, int r0, int dst0, int cnt) -> int {
     for (int t = 0; t < 2; ++t) {
@@ -729,6 +752,7 @@ int sync_group_handle(ring_attn* h) {
     sub->seg_dirty = true;
   }
   sub->rotation = h->rotation;
+  sub->fwd_lap = h->fwd_lap;
   sub->wait_limit_ns = h->wait_limit_ns;
   return RING_OK;
 }

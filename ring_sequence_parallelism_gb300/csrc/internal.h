@@ -184,6 +184,10 @@ const Plan& handle_plan(const ring_attn* h);
 unsigned long long handle_wait_limit(const ring_attn* h);
 int handle_debug_drop_v(const ring_attn* h);  // RING_OPT_DEBUG_DROP_V_LOADS
 int block_partial_smem_bytes(int d);
+// The ring forward in one launch (block_lap.cu): a.out / a.lse receive the
+// result; K/V maps as for kKvSlotJ.
+int launch_fwd_lap(const StepArgs& a, const void* q_map, const void* k_map, const void* v_map, int d, void* stream);
+int prepare_fwd_lap_kernels();
 // CTAs of one block-partial launch: one per (pair of query tiles, shard, head).
 int block_partial_grid(int T, int n_active, int BH);
 int prepare_block_partial_kernels();
