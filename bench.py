@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--imbalance", action="store_true",
                     help="print only the per-shard work and time of the 8K causal workloads (contiguous, "
                          "striped, zigzag)")
+    ap.add_argument("--fwd-lap", action="store_true",
+                    help="run the forward as one launch for the whole ring (RING_OPT_FWD_LAP 1) instead of one "
+                         "step kernel per ring step")
     ap.add_argument("--no-extra", action="store_true",
                     help="leave out the sub-records of the default line (side-stream rotation, per-shard "
                          "imbalance, the other workloads)")
@@ -378,6 +381,7 @@ def measure_side_stream_rotation(att, q, k, v, out, lse, w, warmup=3, steps=3):
     import ring_sequence_parallelism_gb300 as ra
 
     att.set_option(ra.RING_OPT_ROTATION, 1)
+    att.set_option(ra.RING_OPT_TIMING, 1)
     try:
         for _ in range(warmup):
             att.fwd(q, k, v, out, lse)
@@ -405,6 +409,52 @@ def measure_side_stream_rotation(att, q, k, v, out, lse, w, warmup=3, steps=3):
         "exposed_wait_ms": t["wait_ms"], "exposed_wait_total_ms": sum(t["wait_ms"]),
         "release_wait_ms": t["release_wait_ms"], "release_wait_total_ms": sum(t["release_wait_ms"]),
     }
+
+
+def measure_schedules(q, k, v, base, names=("striped-128k", "swa-128k", "packed-128k"), warmup=3, steps=5):
+    """The step schedule (one kernel per ring step, state through HBM) and the
+    lap (RING_OPT_FWD_LAP 1: one launch, state on chip) on workloads whose
+    inputs are the given ones (the 128K workloads share their seed and
+    recipe; they differ in the mask).  Inputs are larger than L2."""
+    import torch
+
+    import ring_sequence_parallelism_gb300 as ra
+    from ring_sequence_parallelism_gb300.inputs import WORKLOADS
+
+    stream = torch.cuda.current_stream()
+    res = []
+    for name in names:
+        w = WORKLOADS[name]
+        if (w.B, w.H, w.kv_heads, w.N, w.d, w.seed, w.key_boost_frac) != \
+                (base.B, base.H, base.kv_heads, base.N, base.d, base.seed, base.key_boost_frac):
+            continue
+        att = ra.RingAttention(w.B, w.H, w.N, w.d, w.P, causal=w.causal, layout=w.layout, kv_heads=w.kv_heads)
+        if w.window:
+            att.set_option(ra.RING_OPT_WINDOW, w.window)
+        if w.doc_len:
+            att.set_segments(w.segments())
+        out = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+        rec = {"workload": name}
+        for lap in (0, 1):
+            att.set_option(ra.RING_OPT_FWD_LAP, lap)
+            for _ in range(warmup):
+                att.fwd(q, k, v, out, lse)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                att.fwd(q, k, v, out, lse)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            att.check()
+            ms = e0.elapsed_time(e1) / steps
+            rec["lap" if lap else "step"] = {"ms_per_step": ms, "tflops": w.flops() / (ms * 1e-3) / 1e12}
+        rec["lap_speedup"] = rec["step"]["ms_per_step"] / rec["lap"]["ms_per_step"]
+        res.append(rec)
+        att.close()
+        del out, lse
+    return res
 
 
 def measure_workloads(names, peak_burst, warmup=3):
@@ -471,6 +521,8 @@ def run_ours(args, w):
         att.set_option(ra.RING_OPT_WINDOW, w.window)
     if w.doc_len:
         att.set_segments(w.segments())
+    if args.fwd_lap:
+        att.set_option(ra.RING_OPT_FWD_LAP, 1)
     out = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device="cuda")
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
     att.set_option(ra.RING_OPT_TIMING, 1)
@@ -507,7 +559,7 @@ def run_ours(args, w):
 
     # ---- roofline of the dominant kernel (the block-partial step kernel)
     step_flops = [4 * w.d * att.step_work(s)[0] for s in range(w.P)]
-    k_total_ms = sum(kernel_ms)
+    k_total_ms = sum(kernel_ms)  # (lap: the one launch, in entry 0)
     achieved = sum(step_flops) / (k_total_ms * 1e-3) / 1e12
     peak_sus = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     peak_burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
@@ -535,7 +587,9 @@ def run_ours(args, w):
 
     extra = {}
     if world == 1 and not args.no_extra:
-        extra["ring_mode1"] = measure_side_stream_rotation(att, q, k, v, out, lse, w)
+        if not args.fwd_lap:
+            extra["ring_mode1"] = measure_side_stream_rotation(att, q, k, v, out, lse, w)
+        extra["schedules"] = measure_schedules(q, k, v, w)
         extra["imbalance"] = measure_imbalance()
         extra["workloads"] = measure_workloads(
             [x for x in ("noncausal-512", "contiguous-8k", "striped-8k", "zigzag-8k", "striped-1m") if x != w.name],
@@ -555,11 +609,15 @@ def run_ours(args, w):
             "tokens_per_s": tokens_s,
             "pct_of_bf16_peak": {"sustained": 100 * value / world / peak_sus, "burst": 100 * value / world / peak_burst,
                                  "nominal_2250": 100 * value / world / 2250.0, "source": pk_kind},
-            "roofline": {"bound": "tensor", "kernel": "block_partial_kernel<128> (one launch per ring step)",
+            "schedule": "lap (one launch for the ring, state on chip, blocks read in place)" if args.fwd_lap else
+                        "step (one kernel per ring step, blocks sent along the ring)",
+            "roofline": {"bound": "tensor", "kernel": ("fwd_lap_kernel<128> (one launch for the ring)" if args.fwd_lap
+                                                       else "block_partial_kernel<128> (one launch per ring step)"),
                          "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                          "frac": achieved / peak_burst, "peak_kind": f"bf16_tflops burst ({pk_kind})",
                          "frac_of_sustained": achieved / peak_sus, "traffic": traffic,
-                         "launches_per_step": w.P, "avg_launch_ms": k_total_ms / w.P},
+                         "launches_per_step": 1 if args.fwd_lap else w.P,
+                         "avg_launch_ms": k_total_ms / (1 if args.fwd_lap else w.P)},
             "ring": {"step_kernel_ms": kernel_ms, "rotation_copy_ms": copy_ms, "exposed_wait_ms": wait_ms,
                      "pack_ms": pack_ms, "exposed_wait_total_ms": sum(wait_ms),
                      "rotation": "each step kernel sends its K/V blocks to the next shard's slot "
@@ -567,7 +625,7 @@ def run_ours(args, w):
                                  "with no work in a step",
                      "rotation_bytes_per_step": 2 * w.B * w.H * w.N * w.d * 2},
             "clocks": clocks.summary(),
-            "gpu_launches": args.steps * (1 + w.P),
+            "gpu_launches": args.steps * (2 if args.fwd_lap else 1 + w.P),
             "e2e": e2e,
             "cpu_baseline": cpu,
         }

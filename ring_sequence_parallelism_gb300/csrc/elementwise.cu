@@ -80,18 +80,19 @@ __device__ __forceinline__ void stv<4>(float* p, const float (&x)[4]) {
 //   l = alpha la + beta lb;  O~ = alpha O~a + beta O~b
 // D / V lanes share a row, V columns each.  The first lane of the row reads
 // the four scalars once, computes alpha and beta and writes m and l; the
-// others get alpha and beta by a shuffle.  Each lane issues the O~ loads of
-// kUnroll rows before any arithmetic, so enough bytes are in flight to keep
-// HBM busy.  The loop is warp-uniform (the shuffles need every lane), with
-// rows past the end masked.
+// others get alpha and beta by a shuffle.  Each lane issues both O~ loads
+// before the scalar loads and the arithmetic; at 40 registers a lane, 6
+// blocks of 256 stay resident per SM, which keeps enough bytes in flight.
+// The loop is warp-uniform (the shuffles need every lane), with rows past the
+// end masked.
 template <int D, int V>
-__global__ void __launch_bounds__(256) merge_kernel(float* __restrict__ ma, float* __restrict__ la,
+__global__ void __launch_bounds__(256, 6) merge_kernel(float* __restrict__ ma, float* __restrict__ la,
                                                     float* __restrict__ oa, const float* __restrict__ mb,
                                                     const float* __restrict__ lb, const float* __restrict__ ob,
                                                     long long rows) {
   constexpr int TPR = D / V;
   constexpr int kRowsPerWarp = 32 / TPR;
-  constexpr int kUnroll = 2;
+  constexpr int kUnroll = 1;
   const int lane = threadIdx.x & 31;
   const int sub = lane % TPR;
   const int leader = lane - sub;
@@ -254,10 +255,9 @@ int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* 
   if (rows <= 0) return 0;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // 256-bit accesses when both O~ arrays are 32-byte aligned (rows are d
-  // floats, a multiple of 8), else 128-bit ones; each lane takes two rows'
-  // worth of vectors per trip
+  // floats, a multiple of 8), else 128-bit ones
   const bool wide = reinterpret_cast<uintptr_t>(oa) % 32 == 0 && reinterpret_cast<uintptr_t>(ob) % 32 == 0;
-  const long long lanes = rows * (d / (wide ? 8 : 4)) / 2;
+  const long long lanes = rows * (d / (wide ? 8 : 4));
   const int grid = grid_for(lanes, 256);
   if (d == 64) {
     if (wide) merge_kernel<64, 8><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);
