@@ -122,8 +122,8 @@ typedef enum {
   /* Causal sliding window W (tokens; 0 = none, the default): a query sees
    * itself and the W-1 tokens before it ([RA-CN] "正确性测试应覆盖哪些边界"
    * lists sliding-window masks).  Applies to ring_attn_fwd, block_partial,
-   * the planner queries and ring_attn_decode.  Rebuilds the plan; needs the
-   * causal mask and the CONTIGUOUS or STRIPED layout (RING_ERR_UNSUPPORTED
+   * the planner queries, ring_attn_decode and ring_attn_bwd, in all three
+   * layouts.  Rebuilds the plan; needs the causal mask (RING_ERR_UNSUPPORTED
    * otherwise, the handle keeping its previous window). */
   RING_OPT_WINDOW = 4,
   /* How ring_attn_bwd schedules the ring ([RA-CN] "Backward 需要让梯度也沿环传播"
@@ -212,14 +212,16 @@ RINGATTN_API int ring_attn_plan_block(ring_attn_t h, int r, int step, int* j, in
  *   j = r:  key_limit = n, delta = 0;
  *   j > r:  rows of the early chunk none (key_limit 0), rows of the late
  *           chunk every key.
- * "No diagonal" is returned as delta = n.  Any output pointer may be NULL. */
+ * "No diagonal" is returned as delta = n.  The causal rule only: with a
+ * window or segments ring_attn_plan_key_range gives a row's keys.  Any
+ * output pointer may be NULL. */
 RINGATTN_API int ring_attn_plan_mask(ring_attn_t h, int r, int step, long long row, long long* key_limit,
                                      long long* delta);
 
 /* The keys local row `row` of shard r sees at ring step s, in the block's
  * local columns: first .. last inclusive (first > last: none).  Covers every
- * mask the handle applies (causal, layout, sliding window).  Any output
- * pointer may be NULL. */
+ * mask the handle applies (causal, layout, sliding window, segments).  Any
+ * output pointer may be NULL. */
 RINGATTN_API int ring_attn_plan_key_range(ring_attn_t h, int r, int step, long long row, long long* first,
                                           long long* last);
 
@@ -330,7 +332,7 @@ RINGATTN_API int ring_attn_fwd_host(ring_attn_t h, const void* q, const void* k,
  * slot r + 1 of the other, dQ kept in dq between steps.
  * K/V blocks are read in place through strided views of k and v.  Layouts
  * CONTIGUOUS, STRIPED and ZIGZAG, causal or not, with or without
- * RING_OPT_WINDOW and segments (which the zigzag layout does not take).
+ * RING_OPT_WINDOW and segments.
  * Pointers 16-byte aligned.  Asynchronous on `stream`. */
 RINGATTN_API int ring_attn_bwd_workspace_size(ring_attn_t h, size_t* bytes);
 RINGATTN_API int ring_attn_bwd(ring_attn_t h, const void* q, const void* k, const void* v, const float* out,
@@ -352,13 +354,17 @@ RINGATTN_API int ring_attn_get_bwd_timing(ring_attn_t h, float* dkdv_ms, float* 
  * <= N-Lq+i (all N keys for Lq = 1).  One launch computes the P shard states
  * (shard r: its K/V block read in place from the cache, laid out as the
  * handle's layout says); a second merges the P states of each row and
- * finalizes.
+ * finalizes.  When the shards x heads x query tiles would leave the SMs
+ * mostly idle (short queries), each shard's keys are cut into up to
+ * ksplit pieces (a power of two, enough for about 1024 CTAs, at least 4
+ * key tiles a piece), each with its own state; the merge folds all
+ * P * ksplit states the same way.
  *   q         [B][H][Lq][d] bf16
  *   k, v      the cache, natural order [B][Hkv][N][d] bf16
  *   out       [B][H][Lq][d] fp32,  lse [B][H][Lq] fp32
  *   workspace ring_attn_decode_workspace_size(h, Lq) bytes, 256-byte aligned
- * Layouts CONTIGUOUS and STRIPED (ZIGZAG returns RING_ERR_UNSUPPORTED);
- * 1 <= Lq <= N.  Asynchronous on `stream`. */
+ * All three layouts (zigzag: shard r's block is chunk r then chunk 2P-1-r of
+ * the cache); 1 <= Lq <= N.  Asynchronous on `stream`. */
 RINGATTN_API int ring_attn_decode_workspace_size(ring_attn_t h, long long Lq, size_t* bytes);
 RINGATTN_API int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v, long long Lq, float* out,
                                   float* lse, void* workspace, void* stream);
@@ -376,8 +382,8 @@ RINGATTN_API int ring_attn_decode(ring_attn_t h, const void* q, const void* k, c
  * (two ints per position, owned by the handle) is made by the next compute
  * call.  Applies to ring_attn_fwd, block_partial, decode and bwd.
  * RING_ERR_INVALID_ARG for a list that does not rise strictly from 0 to N;
- * RING_ERR_UNSUPPORTED for the ZIGZAG layout or N >= 2^31 (the handle keeps
- * its previous segments).  ring_attn_fwd_noalloc returns
+ * RING_ERR_UNSUPPORTED for N >= 2^31 (the handle keeps its previous
+ * segments).  ring_attn_fwd_noalloc returns
  * RING_ERR_UNSUPPORTED while segments are set. */
 RINGATTN_API int ring_attn_set_segments(ring_attn_t h, const long long* bounds, int num_segments);
 

@@ -295,6 +295,7 @@ StepArgs base_args(const ring_attn* h) {
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
   a.fixed_r = -1;
   a.debug_drop_v = h->debug_drop_v;
+  a.ksplit = 1;
   return a;
 }
 
@@ -389,6 +390,13 @@ int ring_attn_plan_key_range(ring_attn_t h, int r, int step, long long row, long
   if (r < 0 || r >= p.P || step < 0 || step >= p.P) return fail(RING_ERR_INVALID_ARG, "r or step out of range");
   if (row < 0 || row >= p.n) return fail(RING_ERR_INVALID_ARG, "row out of range");
   const BlockPlan& b = p.at(step, r);
+  if (p.layout == RING_LAYOUT_ZIGZAG && (p.window > 0 || !p.seg_bounds.empty())) {
+    long long lo, hi;
+    zz_key_bounds(p, b.j, zz_position(p, r, row), &lo, &hi);
+    if (first) *first = lo;
+    if (last) *last = hi;
+    return RING_OK;
+  }
   const int half = row_half(p.layout, p.n, row);
   long long lo = std::max(0LL, row + b.lodelta);
   long long hi = std::min(b.klim[half], std::max(0LL, row + b.hdelta[half] + 1)) - 1;
@@ -1049,9 +1057,23 @@ int ring_attn_get_bwd_timing(ring_attn_t h, float* dkdv_ms, float* dq_ms, float*
 // ---------------------------------------------------------------- decode
 // Workspace of ring_attn_decode: the P shard states of the Lq query rows,
 // m and l [P][B][H][Lq] and O~ [P][B][H][Lq][d] fp32.
+// Short queries leave few CTAs (P shards x heads x query tile pairs): when
+// they would fill fewer than about 1024 CTAs, each block's key tiles are cut
+// into ksplit pieces, each with a state of its own, merged with the others
+// exactly like the shards' states (the smallest power of two reaching 1024
+// CTAs, with at least 4 key tiles a piece).
+static int decode_ksplit(const Plan& p, long long Lq) {
+  const long long T = (Lq + kTileM - 1) / kTileM;
+  const long long units = (long long)p.P * p.B * p.H * ((T + 1) / 2);
+  const int cap = std::max(1, p.KT / 4);
+  int ks = 1;
+  while (units * ks < 1024 && ks * 2 <= cap) ks *= 2;
+  return ks;
+}
+
 static size_t decode_ws(const Plan& p, long long Lq) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t rows = (size_t)p.P * p.B * p.H * (size_t)Lq;
+  const size_t rows = (size_t)p.P * decode_ksplit(p, Lq) * p.B * p.H * (size_t)Lq;
   return up(rows * p.d * 4) + 2 * up(rows * 4);
 }
 
@@ -1068,7 +1090,6 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
   const Plan& p = h->plan;
   if (Lq < 1 || Lq > p.N) return fail(RING_ERR_INVALID_ARG, "Lq must be in [1, N]");
   if (Lq > (1LL << 30)) return fail(RING_ERR_UNSUPPORTED, "Lq too large");
-  if (p.layout == RING_LAYOUT_ZIGZAG) return fail(RING_ERR_UNSUPPORTED, "decode supports the contiguous and striped layouts");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return fail(RING_ERR_INVALID_ARG, "tensor not 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
@@ -1084,7 +1105,16 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
     cuuint64_t str[3] = {row_b, row_b * lq, row_b * lq};
     if ((rc = encode_map(&qm, q, dims, str, kTileM, 1))) return rc;
   }
-  {
+  const bool zigzag = p.layout == RING_LAYOUT_ZIGZAG;
+  if (zigzag) {
+    // the cache as 2P chunks of c = n/2 tokens, dims (d, c, BHkv, 2P): block
+    // j is chunk j, then chunk 2P-1-j (kKvZigzag picks the chunk per tile)
+    const cuuint64_t c = n / 2;
+    cuuint64_t dims[4] = {d, c, (cuuint64_t)BHkv, (cuuint64_t)(2 * P)};
+    cuuint64_t str[3] = {row_b, row_b * (cuuint64_t)p.N, row_b * c};
+    if ((rc = encode_map(&km, k, dims, str, kTileN, 1))) return rc;
+    if ((rc = encode_map(&vm, v, dims, str, kTileN, 1))) return rc;
+  } else {
     // block j of the cache in place: key row k of block j is token j n + k
     // (contiguous) or k P + j (striped); dims (d, n, BHkv, P)
     const cuuint64_t Nn = (cuuint64_t)p.N;
@@ -1094,7 +1124,8 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
     if ((rc = encode_map(&km, k, dims, str, kTileN, 1))) return rc;
     if ((rc = encode_map(&vm, v, dims, str, kTileN, 1))) return rc;
   }
-  const size_t rows = (size_t)P * BH * (size_t)Lq;
+  const int ksplit = decode_ksplit(p, Lq);
+  const size_t rows = (size_t)P * ksplit * BH * (size_t)Lq;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   float* o_st = reinterpret_cast<float*>(ws);
@@ -1103,7 +1134,7 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
 
   StepArgs a = base_args(h);
   if ((rc = device_segments(h, &a.seg_lo, &a.seg_hi))) return rc;
-  a.o_state = o_st;  // shard r's states: rows [r][bh][i]
+  a.o_state = o_st;  // the states of shard r's key piece x: rows [r * ksplit + x][bh][i]
   a.m_state = m_st;
   a.l_state = l_st;
   a.out = nullptr;
@@ -1115,15 +1146,16 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
   a.T = (int)((Lq + kTileM - 1) / kTileM);
   a.decode_pos0 = p.N - Lq;
   a.q_mode = kQShardMajor;
-  a.kv_mode = kKvSlotJ;  // at step 0 shard r reads block r
+  a.kv_mode = zigzag ? kKvZigzag : kKvSlotJ;  // at step 0 shard r reads block r
+  a.ksplit = ksplit;
   a.step = 0;
   a.accumulate = 0;
   a.finalize = 0;
   a.n_active = P;
   for (int r = 0; r < P; ++r) a.active[r] = (unsigned short)r;
-  const int grid = block_partial_grid(a.T, P, BH);
+  const int grid = block_partial_grid(a.T, P, BH) * ksplit;
   RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km, &vm, p.d, grid, cs), "decode block launch");
-  RA_CUDA((cudaError_t)launch_merge_shards(m_st, l_st, o_st, out, lse, (long long)BH * Lq, p.d, P, cs),
+  RA_CUDA((cudaError_t)launch_merge_shards(m_st, l_st, o_st, out, lse, (long long)BH * Lq, p.d, P * ksplit, cs),
           "decode merge launch");
   return RING_OK;
 }

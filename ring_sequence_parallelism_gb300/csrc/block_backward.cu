@@ -53,6 +53,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "block_rules.h"
 #include "tc_ptx.h"
 #include "tmem_regs.h"
 
@@ -252,6 +253,48 @@ __device__ __forceinline__ void zig_query_range(const BwdArgs& a, const BwdRule&
   }
 }
 
+// Zigzag with a window or documents: a shard and a block each hold chunk x
+// then chunk 2P-1-x (c = n/2 tokens), positions increasing with the local
+// index, so the queries a key meets and the keys a query sees are one local
+// interval each (zz_local_interval of the forward's rules maps an interval
+// of allowed positions to it).
+__device__ __forceinline__ long long zz_pos_of(const BwdArgs& a, int sh, long long x) {
+  const long long c = a.n / 2;
+  return x < c ? (long long)sh * c + x : (long long)(2 * a.P - 1 - sh) * c + (x - c);
+}
+
+// Keys of block j (local, inclusive) that query row i of shard r sees.
+__device__ __forceinline__ void zz_keys_of_row(const BwdArgs& a, int r, int j, long long i, long long& lo,
+                                               long long& hi) {
+  const long long c = a.n / 2, t = zz_pos_of(a, r, i);
+  long long L = 0, U = a.N - 1;
+  if (a.causal) {
+    U = t;
+    if (a.window > 0) L = t - a.window + 1;
+  }
+  if (a.seg_lo) {
+    L = max(L, (long long)a.seg_lo[t]);
+    U = min(U, (long long)a.seg_hi[t] - 1);
+  }
+  zz_local_interval(c, (long long)j * c, (long long)(2 * a.P - 1 - j) * c, L, U, lo, hi);
+}
+
+// Query rows of shard r (local, inclusive) that see key k of block j.
+__device__ __forceinline__ void zz_rows_of_key(const BwdArgs& a, int r, int j, long long k, long long& lo,
+                                               long long& hi) {
+  const long long c = a.n / 2, p = zz_pos_of(a, j, k);
+  long long L = 0, U = a.N - 1;
+  if (a.causal) {
+    L = p;
+    if (a.window > 0) U = p + a.window - 1;
+  }
+  if (a.seg_lo) {
+    L = max(L, (long long)a.seg_lo[p]);
+    U = min(U, (long long)a.seg_hi[p] - 1);
+  }
+  zz_local_interval(c, (long long)r * c, (long long)(2 * a.P - 1 - r) * c, L, U, lo, hi);
+}
+
 // Row of (shard r, local i) of head bh in a natural-order tensor.
 __device__ __forceinline__ long long nat_row(const BwdArgs& a, int bh, int r, long long i) {
   if (a.layout == RING_LAYOUT_ZIGZAG) {
@@ -383,6 +426,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const long long k1 = min(k0 + kTileN - 1, a.layout == RING_LAYOUT_ZIGZAG ? max(rule.kmax, rule.kmax1) : rule.kmax);
     it_lo = 0;
     n_it = 0;
+    if (kWin && a.layout == RING_LAYOUT_ZIGZAG) {
+      // the key tile lies in one chunk, so its keys' query ranges are
+      // non-decreasing: the first key bounds them from below, the last from above
+      long long lo0, hi0, lo1, hi1;
+      zz_rows_of_key(a, r, j, k0, lo0, hi0);
+      zz_rows_of_key(a, r, j, min(k0 + kTileN - 1, (long long)a.n - 1), lo1, hi1);
+      const long long i_lo = max(0LL, lo0), i_hi = min((long long)a.n - 1, hi1);
+      if (i_lo <= i_hi) {
+        it_lo = (int)(i_lo / kTileM);
+        n_it = (int)(i_hi / kTileM) + 1 - it_lo;
+      }
+      return;
+    }
     if (k0 <= k1) {
       long long i_lo = max(0LL, k0 - rule.dhi);
       long long i_hi = min((long long)a.n - 1, k1 - rule.dlo);
@@ -589,7 +645,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       long long i_lo_k = k_row <= rule.kmax ? max(0LL, k_row - rule.dhi) : (long long)a.n;
       long long i_hi_k = min((long long)a.n - 1, k_row - rule.dlo);
       if (a.layout == RING_LAYOUT_ZIGZAG) zig_query_range(a, rule, k_row, i_lo_k, i_hi_k);
-      if (kWin && a.seg_lo && k_row <= rule.kmax) {
+      if (kWin && a.layout == RING_LAYOUT_ZIGZAG) {
+        zz_rows_of_key(a, rv, j, min(k_row, (long long)a.n - 1), i_lo_k, i_hi_k);
+        if (!k_valid) i_hi_k = -1;
+      } else if (kWin && a.seg_lo && k_row <= rule.kmax) {
         long long qlo, qhi;
         doc_range(a, j, rv, k_row, qlo, qhi);
         i_lo_k = max(i_lo_k, qlo);
@@ -801,7 +860,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     n_kt = 0;
     long long k_lo = max(0LL, i0 + rule.dlo);
     long long k_hi = min(rule.kmax, i1 + rule.dhi);
-    if (kWin && a.seg_lo) {
+    if (kWin && a.layout == RING_LAYOUT_ZIGZAG) {
+      // the tile's rows lie in one chunk: non-decreasing key ranges
+      long long lo0, hi0, lo1, hi1;
+      zz_keys_of_row(a, r, j, i0, lo0, hi0);
+      zz_keys_of_row(a, r, j, i1, lo1, hi1);
+      k_lo = max(0LL, lo0);
+      k_hi = min((long long)a.n - 1, hi1);
+    } else if (kWin && a.seg_lo) {
       // keys in the documents of the tile's first and last rows
       long long lo0, hi0, lo1, hi1;
       doc_range(a, r, j, i0, lo0, hi0);
@@ -998,7 +1064,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // this row's allowed keys: k_lo_i <= k <= k_hi_i
       long long k_lo_i = max(0LL, i_row + rule.dlo);
       long long k_hi_i = i_valid ? min(rule.kmax, i_row + rule.dhi) : -1;
-      if (kWin && a.seg_lo && i_valid) {
+      if (kWin && a.layout == RING_LAYOUT_ZIGZAG) {
+        zz_keys_of_row(a, r, j, min(i_row, (long long)a.n - 1), k_lo_i, k_hi_i);
+        if (!i_valid) k_hi_i = -1;
+      } else if (kWin && a.seg_lo && i_valid) {
         long long klo, khi;
         doc_range(a, r, j, i_row, klo, khi);
         k_lo_i = max(k_lo_i, klo);

@@ -336,16 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = cur.g;
         if (cur.s != cur_s) {
           // this row's allowed keys [kmin_row, kmax_row] in block cur.v.j
-          const Tile& tw = cur.v.tile;
           cur_s = cur.s;
-          kmax_row = (int)max(-1LL, min((long long)tw.klim - 1, tile_kmax(tw, i_row)));
-          kmin_row = kWin ? (int)max(0LL, min((long long)a.n, tile_kmin(tw, i_row))) : 0;
-          if (kWin && a.seg_lo) {
-            long long slo, shi;
-            seg_bounds(a, r, cur.v.j, min(i_row, (long long)a.nq - 1), slo, shi);
-            kmin_row = max(kmin_row, (int)max(0LL, min((long long)a.n, slo)));
-            kmax_row = min(kmax_row, (int)max(-1LL, min((long long)a.n, shi)));
-          }
+          row_key_bounds<kWin>(a, cur.v.tile, r, cur.v.j, i_row, kmin_row, kmax_row);
         }
         ok = warp_wait(bar(L::kBarSFull + t), c & 1, abort_flag, a, 8);
         if (!ok) break;
@@ -483,7 +475,7 @@ int launch_fwd_lap(const StepArgs& a, const void* q_map, const void* k_map, cons
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
   const CUtensorMap& vm = *static_cast<const CUtensorMap*>(v_map);
-  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
+  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;  // row-dependent bounds
   if (d == 64) {
     if (win) fwd_lap_kernel<64, true><<<(int)grid, kThreads, LapLayout<64>::kAlloc, s>>>(a, qm, km, vm);
     else fwd_lap_kernel<64, false><<<(int)grid, kThreads, LapLayout<64>::kAlloc, s>>>(a, qm, km, vm);

@@ -122,7 +122,8 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   const int U = (a.T + 1) / 2;
   const int item = blockIdx.x;
   const int u = U - 1 - item % U;
-  const int g = item / U;
+  const int piece = (item / U) % a.ksplit;
+  const int g = item / U / a.ksplit;
   w.bh = g % a.BH;
   w.kvh = w.bh / a.G;
   const int slot_in_list = a.fixed_r >= 0 ? 0 : g / a.BH;
@@ -132,6 +133,25 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   w.j = j;
   w.tile[0] = tile_work<kWin>(a, w.r, j, 2 * u);
   w.tile[1] = tile_work<kWin>(a, w.r, j, 2 * u + 1);
+  w.sr = w.r * a.ksplit + piece;
+  if (a.ksplit > 1) {
+    // this piece's key tiles only: [p0, p1) of the block's KT
+    const int span = (a.KT + a.ksplit - 1) / a.ksplit;
+    const int p0 = min(a.KT, piece * span), p1 = min(a.KT, p0 + span);
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      Tile& tt = w.tile[x];
+      const int lo_ = max(tt.kt_lo, p0), hi_ = min(tt.kt_hi, p1);
+      if (hi_ <= lo_) {
+        tt.kt_lo = tt.kt_hi = tt.full_lo = tt.full_hi = 0;
+      } else {
+        tt.full_lo = min(max(tt.full_lo, lo_), hi_);
+        tt.full_hi = min(max(tt.full_hi, lo_), hi_);
+        tt.kt_lo = lo_;
+        tt.kt_hi = hi_;
+      }
+    }
+  }
   // The CTA loads the union of the two tiles' key-tile ranges (the second
   // tile's range starts and ends no earlier than the first's).
   int lo = a.KT, hi = 0;
@@ -173,8 +193,10 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
       // phases ahead of its current one (the wait would return at once), and
       // a stage could be reloaded before its unused tile landed.  So each
       // tile with keys runs the CTA's whole range; the masks zero the rest.
-      // (A window shifts the second tile's range by at most one tile.)
-      if (kWin && a.seg_lo) {
+      // (A window shifts the second tile's range by at most one tile.  In the
+      // zigzag layout the two tiles can lie in different chunks, so a window
+      // or documents there take the whole range too.)
+      if (kWin && (a.seg_lo || a.layout == RING_LAYOUT_ZIGZAG)) {
         tt.jb = 0;
         tt.je = w.nk;
       }
@@ -189,6 +211,20 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   }
   w.slot = a.kv_mode == kKvSlotR ? w.r : (a.kv_mode == kKvSlotJ ? j : 0);
   return w;
+}
+
+// TMA coordinates (row, slot) of the key tile starting at key0 of the CTA's
+// block: the block's own slot, or for the zigzag cache (kKvZigzag) the chunk
+// holding the tile (chunks are whole tiles, so a tile lies in one chunk).
+__device__ __forceinline__ void kv_coords(const StepArgs& a, const WorkItem& w, int key0, int& row, int& slot) {
+  if (a.kv_mode == kKvZigzag) {
+    const int c = a.n / 2;
+    row = key0 < c ? key0 : key0 - c;
+    slot = key0 < c ? w.j : 2 * a.P - 1 - w.j;
+  } else {
+    row = key0;
+    slot = w.slot;
+  }
 }
 
 // ------------------------------------------------------------- the kernel
@@ -235,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (long long)w.bh * a.row_bh +
       (a.q_mode == kQZigzag ? (i_row < half_n ? (long long)w.r * half_n + i_row
                                               : (long long)(2 * a.P - 1 - w.r) * half_n + (i_row - half_n))
-                            : (long long)w.r * a.row_r + i_row * a.row_i);
+                            : (long long)w.sr * a.row_r + i_row * a.row_i);
   // Running state: row-major [row][D] (the C ABI's states), or with
   // state_tiled one block per (head, shard, 128-row tile) laid out
   // [D/8][128 rows][8], so a warp's 32 rows of one 8-column chunk are 1 KB
@@ -304,16 +340,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const int key0 = key_tile(a, w, 0) * kTileN;
       if (nq > 0) load_q(0);
+      int krow0, kslot0;
+      kv_coords(a, w, key0, krow0, kslot0);
       mbar_expect_tx(bar(L::kBarKFull), L::kKBytes);
       for (int c = 0; c < D / L::kSub; ++c)
-        tma_load_4d(sbase + L::kOffK + c * (kTileN * 128), &k_map, bar(L::kBarKFull), c * L::kSub, key0, w.kvh,
-                    w.slot);
+        tma_load_4d(sbase + L::kOffK + c * (kTileN * 128), &k_map, bar(L::kBarKFull), c * L::kSub, krow0, w.kvh,
+                    kslot0);
       if (nq > 1) load_q(1);
       if (!a.debug_drop_v) {  // test hook: nothing ever completes v_full
         mbar_expect_tx(bar(L::kBarVFull), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
-          tma_load_4d(sbase + L::kOffV + c * (kTileN * 128), &v_map, bar(L::kBarVFull), c * L::kSub, key0, w.kvh,
-                      w.slot);
+          tma_load_4d(sbase + L::kOffV + c * (kTileN * 128), &v_map, bar(L::kBarVFull), c * L::kSub, krow0, w.kvh,
+                      kslot0);
       }
     }
   }
@@ -353,10 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (used0) ok = mbar_wait(bar(L::kBarKEmpty + 2 * st), par0, abort_flag, a, 1);
         if (ok && used1) ok = mbar_wait(bar(L::kBarKEmpty + 2 * st + 1), par1, abort_flag, a, 1);
         if (!ok) break;
+        int krow, kslot;
+        kv_coords(a, w, key0, krow, kslot);
         mbar_expect_tx(bar(L::kBarKFull + st), L::kKBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), &k_map, bar(L::kBarKFull + st),
-                      c * L::kSub, key0, w.kvh, w.slot);
+                      c * L::kSub, krow, w.kvh, kslot);
         k_issued = j + 1;
         if (used0) ok = mbar_wait(bar(L::kBarVEmpty + 2 * st), par0, abort_flag, a, 2);
         if (ok && used1) ok = mbar_wait(bar(L::kBarVEmpty + 2 * st + 1), par1, abort_flag, a, 2);
@@ -365,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar(L::kBarVFull + st), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), &v_map, bar(L::kBarVFull + st),
-                      c * L::kSub, key0, w.kvh, w.slot);
+                      c * L::kSub, krow, w.kvh, kslot);
         v_issued = j + 1;
       }
       if (sends && ok) {
@@ -461,14 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = t_sm;  // 0: tile A (warps 3-6), 1: tile B (warps 7-10)
     // this row's allowed keys [kmin_row, kmax_row] (keys fit in int; the
     // bounds are clamped to it)
-    int kmax_row = (int)max(-1LL, min((long long)tw.klim - 1, tile_kmax(tw, i_row)));
-    int kmin_row = kWin ? (int)max(0LL, min((long long)a.n, tile_kmin(tw, i_row))) : 0;
-    if (kWin && a.seg_lo && in_range) {
-      long long slo, shi;
-      seg_bounds(a, w.r, w.j, min(i_row, (long long)a.nq - 1), slo, shi);
-      kmin_row = max(kmin_row, (int)max(0LL, min((long long)a.n, slo)));
-      kmax_row = min(kmax_row, (int)max(-1LL, min((long long)a.n, shi)));
-    }
+    int kmin_row, kmax_row;
+    row_key_bounds<kWin>(a, tw, w.r, w.j, i_row, kmin_row, kmax_row);
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + L::tmem_s(t);
     const uint32_t o_addr = tmem + lane_off + L::tmem_o(t);
@@ -645,7 +679,9 @@ int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map
   // without `forward` the kernel never touches the send maps
   const CUtensorMap& kn = *static_cast<const CUtensorMap*>(k_next_map ? k_next_map : k_map);
   const CUtensorMap& vn = *static_cast<const CUtensorMap*>(v_next_map ? v_next_map : v_map);
-  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
+  // row-dependent bounds: a window, documents, or short queries in the zigzag layout
+  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr ||
+                   (a.layout == RING_LAYOUT_ZIGZAG && a.decode_pos0 >= 0);
   if (d == 64) {
     if (win) block_partial_kernel<64, true><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
     else block_partial_kernel<64, false><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);

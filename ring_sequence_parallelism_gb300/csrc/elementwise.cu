@@ -6,6 +6,7 @@
 // addresses.  Grids are a multiple of the SM count with grid-stride loops.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -258,7 +259,12 @@ int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* 
   // floats, a multiple of 8), else 128-bit ones
   const bool wide = reinterpret_cast<uintptr_t>(oa) % 32 == 0 && reinterpret_cast<uintptr_t>(ob) % 32 == 0;
   const long long lanes = rows * (d / (wide ? 8 : 4));
-  const int grid = grid_for(lanes, 256);
+  // one wave: the 6 blocks of 256 per SM that fit at 40 registers a lane, the
+  // grid-stride loop covering the rest (more blocks would leave a partial
+  // last wave)
+  grid_for(1, 256);  // sets the SM count
+  const long long blocks = (lanes + 255) / 256;
+  const int grid = (int)std::max(1LL, std::min(blocks, (long long)g_sm_count * 6));
   if (d == 64) {
     if (wide) merge_kernel<64, 8><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);
     else merge_kernel<64, 4><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);

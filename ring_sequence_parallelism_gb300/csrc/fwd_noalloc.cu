@@ -196,6 +196,7 @@ extern "C" int ring_attn_fwd_noalloc(ring_attn_t h, const void* q, const void* k
   a.causal = p.causal;
   a.layout = p.layout;
   a.fixed_r = -1;
+  a.ksplit = 1;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p.d));
   for (int s = 0; s < P; ++s) {
     const auto& act = p.active[s];

@@ -60,6 +60,11 @@ struct Plan {
 // Local key bounds (inclusive) that the segments allow row i of shard r in
 // block j (contiguous or striped layout); lo > hi when none.
 void seg_key_bounds(const Plan& p, int r, int j, long long i, long long* lo, long long* hi);
+// Zigzag layout with a window or segments: local keys lo..hi of block j that
+// the query at global position t may see; zz_position: position of shard r's
+// local row i.
+void zz_key_bounds(const Plan& p, int j, long long t, long long* lo, long long* hi);
+long long zz_position(const Plan& p, int r, long long i);
 
 int block_of(int P, int r, int step);  // (r - step) mod P
 BlockPlan classify(int layout, int causal, long long n, int r, int j, int P = 1, long long window = 0);
@@ -86,7 +91,9 @@ enum QMode : int {
 enum KvMode : int {
   kKvSlotR = 0,  // rotation buffer: slot r holds block (r - s) mod P
   kKvSlotJ = 1,  // direct: slot j holds block j
-  kKvSingle = 2  // one block only (slot 0)
+  kKvSingle = 2,  // one block only (slot 0)
+  kKvZigzag = 3   // the natural-order cache in the zigzag layout: map dims (d, n/2, BHkv, 2P); block j's key
+                  // k < n/2 is row k of chunk j, k >= n/2 row k - n/2 of chunk 2P-1-j
 };
 
 struct StepArgs {
@@ -113,6 +120,8 @@ struct StepArgs {
   long long window;  // > 0: causal sliding window, a query sees itself and the window-1 tokens before it
   long long decode_pos0;  // >= 0: queries at global positions pos0 + i against block j's keys
                           //       (the causal rule from global positions; see ring_attn_decode)
+  int ksplit;             // >= 1: pieces each block's key tiles are cut into (short queries only); piece p
+                          //       of shard r keeps its state in slot r * ksplit + p
   float scale_log2;  // log2(e) / sqrt(d)
   // sequence packing (nullptr: one document): per natural position, the
   // first and one-past-last position of its document; a pair is allowed

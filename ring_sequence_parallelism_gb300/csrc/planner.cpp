@@ -25,7 +25,7 @@ BlockPlan classify(int layout, int causal, long long n, int r, int j, int P, lon
   BlockPlan b{j, RING_BLOCK_FULL, n, {n, n}, {n, n}, kNoLowerOffset};
   if (!causal) return b;
   if (window > 0 && layout != RING_LAYOUT_ZIGZAG) {
-    // a key W or more positions behind the query is dropped: contiguous
+    // (zigzag windows: zz_key_bounds) a key W or more positions behind the query is dropped: contiguous
     // (r-j) n + i - k < W  <=>  k - i >= (r-j) n - W + 1; striped
     // (i-k) P + (r-j) < W  <=>  k - i >= floor((r-j-W)/P) + 1
     b.lodelta = layout == RING_LAYOUT_STRIPED ? floor_div((long long)(r - j) - window, P) + 1
@@ -116,6 +116,52 @@ void seg_key_bounds(const Plan& p, int r, int j, long long i, long long* lo, lon
   }
 }
 
+// Zigzag with a window or documents.  Shard r and block j each hold chunk
+// x then chunk 2P-1-x (c = n/2 tokens), positions increasing with the local
+// index, so the positions a query may see ([t - W + 1, t] under the causal
+// mask and a window, cut to its document) are one interval of block keys.
+// Local keys lo..hi of block j that the query at position t may see.
+void zz_key_bounds(const Plan& p, int j, long long t, long long* lo, long long* hi) {
+  const long long c = p.n / 2;
+  long long L = 0, U = p.N - 1;
+  if (p.causal) {
+    U = t;
+    if (p.window > 0) L = t - p.window + 1;
+  }
+  if (!p.seg_lo.empty()) {
+    L = std::max(L, (long long)p.seg_lo[(size_t)t]);
+    U = std::min(U, (long long)p.seg_hi[(size_t)t] - 1);
+  }
+  const long long A0 = (long long)j * c, B0 = (long long)(2 * p.P - 1 - j) * c;
+  *hi = U >= B0 ? c + std::min(U - B0, c - 1) : (U >= A0 ? std::min(U - A0, c - 1) : -1);
+  *lo = L <= A0 ? 0 : (L < A0 + c ? L - A0 : (L <= B0 ? c : (L < B0 + c ? c + L - B0 : 2 * c)));
+}
+
+long long zz_position(const Plan& p, int r, long long i) {
+  const long long c = p.n / 2;
+  return i < c ? (long long)r * c + i : (long long)(2 * p.P - 1 - r) * c + (i - c);
+}
+
+// Allowed pairs and computed tiles of zigzag block (r, j) under those bounds.
+static std::pair<long long, long long> zigzag_work(const Plan& p, int r, int j) {
+  const long long n = p.n;
+  long long pairs = 0, tiles = 0;
+  for (long long i = 0; i < n; ++i) {
+    long long lo, hi;
+    zz_key_bounds(p, j, zz_position(p, r, i), &lo, &hi);
+    pairs += std::max(0LL, hi - lo + 1);
+  }
+  for (int t = 0; t < p.T; ++t) {
+    const long long i_min = (long long)t * kTileM, i_max = std::min(n - 1, i_min + kTileM - 1);
+    long long lo0, hi0, lo1, hi1;
+    zz_key_bounds(p, j, zz_position(p, r, i_min), &lo0, &hi0);
+    zz_key_bounds(p, j, zz_position(p, r, i_max), &lo1, &hi1);
+    const long long first = std::max(0LL, lo0), last = std::min(n - 1, hi1);
+    if (first <= last) tiles += last / kTileN - first / kTileN + 1;
+  }
+  return {pairs, tiles};
+}
+
 // Allowed pairs and computed 128x128 tiles of block (r, j) with segments:
 // row i allows columns max(0, i + lodelta, slo(i)) .. min(klim, i + hdelta
 // + 1, shi(i) + 1) - 1; the bounds are non-decreasing in i, so a tile's key
@@ -183,8 +229,8 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   }
   const long long n = N / P;
   const long long bh = (long long)B * H;
-  if (window < 0 || (window > 0 && (!causal || layout == RING_LAYOUT_ZIGZAG))) {
-    *err = "a sliding window needs the causal mask and the contiguous or striped layout";
+  if (window < 0 || (window > 0 && !causal)) {
+    *err = "a sliding window needs the causal mask";
     return window < 0 ? RING_ERR_INVALID_ARG : RING_ERR_UNSUPPORTED;
   }
   if (layout == RING_LAYOUT_ZIGZAG && (n % (2 * kTileM)) != 0) {
@@ -205,10 +251,6 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
     if (!ok) {
       *err = "segment boundaries must rise strictly from 0 to N";
       return RING_ERR_INVALID_ARG;
-    }
-    if (layout == RING_LAYOUT_ZIGZAG) {
-      *err = "segments need the contiguous or striped layout";
-      return RING_ERR_UNSUPPORTED;
     }
     if (N > (1LL << 31) - 1) {
       *err = "segments need N < 2^31";
@@ -266,8 +308,10 @@ int build_plan(Plan* p, int B, int H, long long N, int d, int P, int causal, int
   for (int s = 0; s < P; ++s) {
     for (int r = 0; r < P; ++r) {
       BlockPlan b = classify(layout, causal, n, r, block_of(P, r, s), P, window);
+      const bool zz_general = layout == RING_LAYOUT_ZIGZAG && (packed || window > 0);
+      auto w = zz_general ? zigzag_work(*p, r, b.j) : (packed ? segment_work(*p, b, r) : work(b));
+      if (zz_general && w.first == 0) b.cls = RING_BLOCK_SKIP;  // nothing left inside the window / documents
       p->blocks[(size_t)s * P + r] = b;
-      auto w = packed ? segment_work(*p, b, r) : work(b);
       p->shard_pairs[r] += w.first * bh;
       p->shard_tiles[r] += w.second * bh;
       p->step_pairs[s] += w.first * bh;

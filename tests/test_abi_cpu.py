@@ -306,6 +306,49 @@ def test_zigzag_plan_agrees_with_oracle(lib, orc, P, causal):
     att.close()
 
 
+@pytest.mark.parametrize("P,n,causal,window,bounds", [
+    (2, 256, True, 100, None), (3, 256, True, 300, None), (4, 512, True, 700, None), (2, 256, True, 1, None),
+    (3, 256, True, 0, [0, 100, 101, 500, 768]), (2, 256, False, 0, [0, 300, 512]),
+    (4, 256, True, 200, [0, 5, 600, 1024]),
+])
+def test_zigzag_window_and_segments_plan(lib, orc, P, n, causal, window, bounds):
+    """Zigzag with a sliding window or documents: every row's key range
+    (ring_attn_plan_key_range) is exactly the set of keys the oracle's ring
+    simulation visits for it (one interval in the block's local order), the
+    per-shard and per-step pair counts add up to the oracle's, and a block
+    with no allowed pair is SKIP."""
+    from oracle import LAYOUT_ZIGZAG
+    import oracle_pins
+
+    N, d = P * n, 2
+    q = oracle_pins.rand_bits((1, N, d), 5)
+    _, _, cnt = orc.ring(q, q, q, P, causal, LAYOUT_ZIGZAG, visits=True, window=window, segments=bounds)
+    att = ra.RingAttention(1, 1, N, 64, P, causal=causal, layout="zigzag")
+    if window:
+        att.set_option(ra.RING_OPT_WINDOW, window)
+    if bounds is not None:
+        att.set_segments(bounds)
+    pairs, _ = att.shard_work()
+    assert sum(pairs) == int(cnt[0].sum())
+    for r in range(P):
+        qpos = np.array([orc.position(LAYOUT_ZIGZAG, n, P, r, i) for i in range(n)])
+        shard_total = 0
+        for s in range(P):
+            j, cls, _ = att.plan_block(r, s)
+            kpos = np.array([orc.position(LAYOUT_ZIGZAG, n, P, j, k) for k in range(n)])
+            block_total = 0
+            for i in range(n):
+                first, last = att.plan_key_range(r, s, i)
+                visited = np.nonzero(cnt[0][qpos[i], kpos])[0]
+                want = np.arange(first, last + 1) if first <= last else np.array([], dtype=np.int64)
+                assert np.array_equal(visited, want), (r, s, i, first, last, visited[:5])
+                block_total += visited.size
+            assert (cls == ra.RING_BLOCK_SKIP) == (block_total == 0), (r, s, cls, block_total)
+            shard_total += block_total
+        assert shard_total == pairs[r], (r, shard_total, pairs[r])
+    att.close()
+
+
 def test_grouped_query_handles(lib):
     """ring_attn_create_gqa: H must be a positive multiple of Hkv; the
     workspace holds the rotation buffers of the Hkv heads only."""
@@ -379,16 +422,11 @@ def test_segment_plan_agrees_with_oracle(lib, orc, layout, causal, window, P):
 
 
 def test_segments_rejected(lib):
-    """Boundaries must rise strictly from 0 to N; the zigzag layout has no
-    segment support; the handle keeps its previous segments on an error."""
+    """Boundaries must rise strictly from 0 to N; the handle keeps its
+    previous segments on an error."""
     att = ra.RingAttention(1, 1, 64, 64, 4, causal=True, layout="striped")
     for bad in ([0, 10, 10, 64], [1, 64], [0, 63], [0, 70, 64]):
         with pytest.raises(_lib.RingAttnError) as e:
             att.set_segments(bad)
         assert e.value.status == _lib.RING_ERR_INVALID_ARG
     att.close()
-    z = ra.RingAttention(1, 1, 1024, 64, 2, causal=True, layout="zigzag")
-    with pytest.raises(_lib.RingAttnError) as e:
-        z.set_segments([0, 100, 1024])
-    assert e.value.status == _lib.RING_ERR_UNSUPPORTED
-    z.close()
