@@ -39,6 +39,7 @@ METRIC = "causal-adjusted attention TFLOP/s and % of GB300 bf16 peak; tokens/s (
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCE = os.path.join(ROOT, "ring_sequence_parallelism_gb300", "csrc", "block_partial.cu")
 BWD_SOURCE = os.path.join(ROOT, "ring_sequence_parallelism_gb300", "csrc", "block_backward.cu")
+LAP_SOURCE = os.path.join(ROOT, "ring_sequence_parallelism_gb300", "csrc", "block_lap.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -295,6 +296,23 @@ def l2_note(w):
     return "inputs (3 x %.1f MB bf16) fit in L2: small case, not a timed workload" % (gb * 1e3)
 
 
+class L2Flush:
+    """Evicts the inputs from the 129 MB L2 between timed calls: writes a
+    256 MB buffer, then reads another, so L2 ends up holding clean lines (a
+    write alone would leave 129 MB of dirty lines, written back to HBM
+    during the next timed kernel)."""
+
+    def __init__(self):
+        import torch
+
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.w.fill_(1)
+        return self.r.sum()
+
+
 # ------------------------------------------------------------- sub-records
 def measure_imbalance(names=("contiguous-8k", "striped-8k", "zigzag-8k"), reps=5):
     """Per-shard causal work and time ([GRA] "The causal mask wrecks the load
@@ -315,7 +333,7 @@ def measure_imbalance(names=("contiguous-8k", "striped-8k", "zigzag-8k"), reps=5
     from ring_sequence_parallelism_gb300 import report
     from ring_sequence_parallelism_gb300.inputs import WORKLOADS, make_workload
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
     res = []
     for name in names:
@@ -334,7 +352,7 @@ def measure_imbalance(names=("contiguous-8k", "striped-8k", "zigzag-8k"), reps=5
             for s in range(w.P):
                 for r in range(w.P):
                     j = (r - s) % w.P
-                    flush.fill_(rep & 0xFF)
+                    flush()
                     torch.cuda._sleep(100000)
                     e0, e1 = ev[s][r]
                     e0.record(stream)
@@ -459,13 +477,13 @@ def measure_schedules(q, k, v, base, names=("striped-128k", "swa-128k", "packed-
 
 def measure_workloads(names, peak_burst, warmup=3):
     """Whole forwards of other workloads, inputs resident; inputs that fit in
-    L2 are flushed (256 MB write) before each timed forward."""
+    L2 are flushed (L2Flush) before each timed forward."""
     import torch
 
     import ring_sequence_parallelism_gb300 as ra
     from ring_sequence_parallelism_gb300.inputs import WORKLOADS, make_workload
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
     res = []
     for name in names:
@@ -483,7 +501,7 @@ def measure_workloads(names, peak_burst, warmup=3):
         torch.cuda.synchronize()
         for e0, e1 in ev:
             if small:
-                flush.fill_(1)
+                flush()
             e0.record(stream)
             att.fwd(q, k, v, out, lse)
             e1.record(stream)
@@ -563,7 +581,7 @@ def run_ours(args, w):
     achieved = sum(step_flops) / (k_total_ms * 1e-3) / 1e12
     peak_sus = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     peak_burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    traffic = traffic_for(w.name)
+    traffic = traffic_for(f"{w.name}:fwd_lap", LAP_SOURCE) if args.fwd_lap else traffic_for(w.name)
 
     # ---- end to end through the public API, host buffers, copies in the timed region
     e2e = None
@@ -771,8 +789,8 @@ def run_merge(args, w):
     """ring_attn_merge of two fp32 states of one shard of the workload
     (B*H*n rows; 3*(d+2)*4 algorithmic bytes a row: a and b read, a
     written), in place into a, K times.  Each merge is timed alone with
-    CUDA events after a 256 MB write that flushes L2 (the two states, 68 MB
-    each at the 128K workload, would otherwise partly stay in L2)."""
+    CUDA events after an L2 flush (L2Flush; the two states, 68 MB each at
+    the 128K workload, would otherwise partly stay in L2)."""
     import torch
 
     import ring_sequence_parallelism_gb300 as ra
@@ -791,7 +809,7 @@ def run_merge(args, w):
         return m, l, o
 
     a, b = state(), state()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     for _ in range(args.warmup):
         att.merge(a, b)
     att.check()
@@ -800,7 +818,7 @@ def run_merge(args, w):
     with ClockSampler(torch.cuda.current_device()) as clocks:
         torch.cuda.synchronize()
         for e0, e1 in ev:
-            flush.fill_(1)
+            flush()
             e0.record(stream)
             att.merge(a, b)
             e1.record(stream)
@@ -816,7 +834,8 @@ def run_merge(args, w):
         "metric": "merge of two fp32 online-softmax states (ring_attn_merge), algorithmic HBM GB/s",
         "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "dtype": "f32", "data": "synthetic",
-        "config": dict(config_of(w), rows=n_rows, l2="L2 flushed (256 MB write) before each timed merge"),
+        "config": dict(config_of(w), rows=n_rows,
+                       l2="L2 flushed before each timed merge (256 MB written, then 256 MB read)"),
         "roofline": {"bound": "hbm", "kernel": "merge_kernel", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                      "frac": gbs / hbm, "peak_kind": f"hbm_gbs ({pk_kind})", "traffic": None,
                      "algorithmic": "3*(d+2)*4 bytes per row"},

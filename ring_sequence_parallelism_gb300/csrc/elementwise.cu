@@ -202,31 +202,60 @@ __global__ void pack_kv_kernel(const uint4* __restrict__ k, const uint4* __restr
 // ([RA-CN] the query is sent to every K/V shard, each returns a local
 // state, and the states are merged exactly; [GRA] "Why partial results are
 // allowed to merge"): m = max_s m_s, each side scaled by e^{m_s - m} (0 for
-// an empty side), out = O~/l, lse = m + ln l.  One warp per row: lanes hold
-// d/32 columns; states are [P][rows] and [P][rows][d].
+// an empty side), out = O~/l, lse = m + ln l.  One warp per row: the lanes
+// first find the row max over the states in parallel, then each lane holds
+// d/32 columns and folds the states in groups of kGroup, whose loads are
+// all issued before the arithmetic (the states of one row are independent
+// reads; one at a time they would cost a memory latency each).  States are
+// [P][rows] and [P][rows][d].
+template <int D>
 __global__ void merge_shards_kernel(const float* __restrict__ m, const float* __restrict__ l,
                                     const float* __restrict__ o, float* __restrict__ out,
-                                    float* __restrict__ lse, long long rows, int d, int P) {
+                                    float* __restrict__ lse, long long rows, int P) {
+  constexpr int kGroup = 16;
+  constexpr int per = D / 32;  // 2 or 4 columns per lane
+  constexpr int d = D;
   const int lane = threadIdx.x % 32;
   const long long warps = (long long)gridDim.x * (blockDim.x / 32);
   for (long long row = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; row < rows; row += warps) {
     float mx = -INFINITY;
-    for (int s = 0; s < P; ++s) mx = fmaxf(mx, m[(long long)s * rows + row]);
+    for (int s = lane; s < P; s += 32) mx = fmaxf(mx, m[(long long)s * rows + row]);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
     float lsum = 0.0f;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const int per = d / 32;  // 2 or 4 columns per lane
+    float acc[per];
+#pragma unroll
+    for (int c = 0; c < per; ++c) acc[c] = 0.0f;
     if (mx != -INFINITY) {
-      for (int s = 0; s < P; ++s) {
-        const float ms = m[(long long)s * rows + row];
-        if (ms == -INFINITY) continue;
-        const float w = expf(ms - mx);
-        lsum += w * l[(long long)s * rows + row];
-        const float* src = o + ((long long)s * rows + row) * d + lane * per;
-        for (int c = 0; c < per; ++c) acc[c] += w * src[c];
+      for (int s0 = 0; s0 < P; s0 += kGroup) {
+        float ms[kGroup], ls[kGroup], ov[kGroup][per];
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+          const int s = s0 + u;
+          ms[u] = -INFINITY;
+          ls[u] = 0.0f;
+#pragma unroll
+          for (int c = 0; c < per; ++c) ov[u][c] = 0.0f;
+          if (s < P) {
+            ms[u] = m[(long long)s * rows + row];
+            ls[u] = l[(long long)s * rows + row];
+            const float* src = o + ((long long)s * rows + row) * d + lane * per;
+#pragma unroll
+            for (int c = 0; c < per; ++c) ov[u][c] = src[c];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+          const float w = ms[u] == -INFINITY ? 0.0f : expf(ms[u] - mx);
+          lsum += w * ls[u];
+#pragma unroll
+          for (int c = 0; c < per; ++c) acc[c] += w * ov[u][c];
+        }
       }
     }
     const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
     float* dst = out + row * d + lane * per;
+#pragma unroll
     for (int c = 0; c < per; ++c) dst[c] = acc[c] * inv;
     if (lane == 0) lse[row] = lsum > 0.0f ? mx + logf(lsum) : -INFINITY;
   }
@@ -238,8 +267,11 @@ int launch_merge_shards(const float* m, const float* l, const float* o, float* o
                         int d, int P, void* stream) {
   if (rows <= 0) return 0;
   const long long blocks = (rows + 7) / 8;  // 8 warps a block
-  merge_shards_kernel<<<(int)(blocks < 65535 * 32 ? blocks : 65535 * 32), 256, 0,
-                        static_cast<cudaStream_t>(stream)>>>(m, l, o, out, lse, rows, d, P);
+  const int grid = (int)(blocks < 65535 * 32 ? blocks : 65535 * 32);
+  if (d == 64)
+    merge_shards_kernel<64><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(m, l, o, out, lse, rows, P);
+  else
+    merge_shards_kernel<128><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(m, l, o, out, lse, rows, P);
   return (int)cudaGetLastError();
 }
 
@@ -259,12 +291,7 @@ int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* 
   // floats, a multiple of 8), else 128-bit ones
   const bool wide = reinterpret_cast<uintptr_t>(oa) % 32 == 0 && reinterpret_cast<uintptr_t>(ob) % 32 == 0;
   const long long lanes = rows * (d / (wide ? 8 : 4));
-  // one wave: the 6 blocks of 256 per SM that fit at 40 registers a lane, the
-  // grid-stride loop covering the rest (more blocks would leave a partial
-  // last wave)
-  grid_for(1, 256);  // sets the SM count
-  const long long blocks = (lanes + 255) / 256;
-  const int grid = (int)std::max(1LL, std::min(blocks, (long long)g_sm_count * 6));
+  const int grid = grid_for(lanes, 256);
   if (d == 64) {
     if (wide) merge_kernel<64, 8><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);
     else merge_kernel<64, 4><<<grid, 256, 0, s>>>(ma, la, oa, mb, lb, ob, rows);
