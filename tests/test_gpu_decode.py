@@ -74,6 +74,12 @@ CASES = [
     (1, 4, 1, 2 * 256, 128, 2, False, "striped", 33),      # multi-query, no mask
     (1, 2, 2, 4 * 128, 128, 4, True, "striped", 4 * 128),  # Lq = N: the whole causal attention
     (1, 1, 1, 512, 64, 1, True, "contiguous", 5),          # one shard
+    # a few queries: every shard's keys cut into pieces (the key split)
+    (1, 4, 2, 8 * 256, 128, 8, True, "striped", 2),        # grouped-query
+    (2, 3, 3, 3 * 200, 64, 3, True, "contiguous", 3),      # ragged shards, B = 2
+    (1, 4, 1, 2 * 256, 128, 2, False, "striped", 4),       # multi-query, no mask
+    (1, 2, 2, 4 * 256, 128, 4, True, "zigzag", 2),
+    (1, 1, 1, 256, 128, 1, True, "contiguous", 1),         # one shard, one query
 ]
 
 
@@ -85,7 +91,7 @@ def test_decode_matches_oracle(case):
 
 
 @pytest.mark.parametrize("layout,window,Lq", [("contiguous", 100, 1), ("striped", 300, 64), ("striped", 129, 200),
-                                              ("contiguous", 1000, 300)])
+                                              ("contiguous", 1000, 300), ("striped", 300, 3)])
 def test_decode_sliding_window(layout, window, Lq):
     """Decode with a causal sliding window: each new query sees the last
     `window` positions up to its own."""
