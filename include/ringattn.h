@@ -282,22 +282,28 @@ RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, cons
 
 /* ring_attn_fwd from HOST memory and back, with the copies overlapped with
  * the computation.  The heads are independent problems, so they run in
- * groups of whole K/V heads (4, 2 or 1 groups: the most that divides
- * B * Hkv), each group a ring_attn_fwd over its heads: the inputs of group
- * g+1 are copied in and the outputs of group g-1 copied out while group g
- * computes.  The results equal ring_attn_fwd's over all heads.
+ * groups of whole K/V heads (with 8 or more K/V heads over all batches: one
+ * K/V head in each of the first two and the last two groups, the rest in an
+ * even number of near-equal groups; with fewer, one K/V head per group),
+ * each group a ring_attn_fwd over its heads.  The inputs are copied in
+ * group by group; each group computes as soon as its inputs are in, on one
+ * of two lanes in turn (`stream` and a stream the handle owns), so two
+ * groups share the SMs; each group's outputs are copied out as soon as it
+ * is done.  The results equal ring_attn_fwd's over all heads.
  *   q, k, v   HOST pointers, natural order as in ring_attn_fwd (bf16);
  *             page-locked (cudaHostAlloc, or a pinned torch tensor) for the
  *             copies to be asynchronous and overlapped
  *   out, lse  HOST pointers, as in ring_attn_fwd (fp32)
- * The handle owns the device buffers (inputs, outputs and one group's
- * workspace), made on the first call and kept until ring_attn_destroy, and
- * two copy streams.  Asynchronous on `stream`: the copies start after the
- * caller's earlier work on it, and `stream` completes after the last output
- * copy, so the host may read out and lse after synchronising it.  The host
- * buffers must stay valid, and the inputs unchanged, until then.
- * ring_attn_check covers the copy streams and the group handle.  Errors:
- * RING_ERR_INVALID_ARG for NULL pointers; RING_ERR_CUDA, RING_ERR_OOM. */
+ * The handle owns the device buffers (the inputs and outputs of all heads,
+ * and a workspace for each group size on each lane), made on the first call
+ * and kept until ring_attn_destroy, two copy streams and the second lane's
+ * stream.  Asynchronous on `stream`: the copies start after the caller's
+ * earlier work on it, and `stream` completes after the last output copy and
+ * the second lane's last kernel, so the host may read out and lse after
+ * synchronising it.  The host buffers must stay valid, and the inputs
+ * unchanged, until then.  ring_attn_check covers the copy streams, the
+ * second lane and the group handles.  Errors: RING_ERR_INVALID_ARG for NULL
+ * pointers; RING_ERR_CUDA, RING_ERR_OOM. */
 RINGATTN_API int ring_attn_fwd_host(ring_attn_t h, const void* q, const void* k, const void* v, float* out,
                                     float* lse, void* stream);
 

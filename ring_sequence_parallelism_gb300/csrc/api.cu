@@ -115,18 +115,23 @@ int tensor_map_4d(void* map, const void* base, const unsigned long long dims[4],
 
 struct ring_attn;
 
-// ring_attn_fwd_host's pipeline over head groups (made on first use): a
-// handle for one group, device copies of the inputs and outputs of all
-// heads, the group handle's workspace, and a stream each for the copies in
-// and out.
+// ring_attn_fwd_host's pipeline over head groups (made on first use):
+// device copies of the inputs and outputs of all heads, a handle with its
+// own workspace for each (lane, group size) in use, a stream each for the
+// copies in and out, and a stream for the second compute lane.
 struct HostPipe {
-  ring_attn* sub = nullptr;
-  int groups = 0;
+  std::vector<int> sizes;       // K/V heads of each group, in head order
+  std::vector<int> group_sub;   // the handle each group runs on
+  std::vector<ring_attn*> subs;  // one per (lane, group size)
+  std::vector<int> sub_units;   // K/V heads of each handle
+  std::vector<int> sub_lane;    // the lane each handle runs on
+  std::vector<size_t> sub_ws;   // workspace offset of each handle
+  int lanes = 1;
   uint8_t* dev = nullptr;
-  size_t q_off = 0, k_off = 0, v_off = 0, o_off = 0, l_off = 0, ws_off = 0;
-  cudaStream_t in = nullptr, out = nullptr;
+  size_t q_off = 0, k_off = 0, v_off = 0, o_off = 0, l_off = 0;
+  cudaStream_t in = nullptr, out = nullptr, lane1 = nullptr;
   std::vector<cudaEvent_t> ev_in, ev_comp;
-  cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_done = nullptr, ev_lane = nullptr;
   bool have_done = false;  // ev_done recorded by an earlier call
 };
 
@@ -170,20 +175,19 @@ namespace {
 
 void destroy_pipe(HostPipe* hp) {
   if (!hp) return;
-  if (hp->in) cudaStreamSynchronize(hp->in);
-  if (hp->out) cudaStreamSynchronize(hp->out);
+  for (cudaStream_t st : {hp->in, hp->out, hp->lane1})
+    if (st) cudaStreamSynchronize(st);
   for (auto* v : {&hp->ev_in, &hp->ev_comp})
     for (auto e : *v)
       if (e) cudaEventDestroy(e);
-  if (hp->ev_start) cudaEventDestroy(hp->ev_start);
-  if (hp->ev_done) cudaEventDestroy(hp->ev_done);
-  if (hp->in) cudaStreamDestroy(hp->in);
-  if (hp->out) cudaStreamDestroy(hp->out);
+  for (cudaEvent_t e : {hp->ev_start, hp->ev_done, hp->ev_lane})
+    if (e) cudaEventDestroy(e);
+  for (cudaStream_t st : {hp->in, hp->out, hp->lane1})
+    if (st) cudaStreamDestroy(st);
   if (hp->dev) cudaFree(hp->dev);
-  ring_attn_destroy(hp->sub);
+  for (ring_attn* sub : hp->subs) ring_attn_destroy(sub);
   delete hp;
 }
-
 int make_events(std::vector<cudaEvent_t>& v, int n, unsigned flags) {
   v.assign(n, nullptr);
   for (int i = 0; i < n; ++i) RA_CUDA(cudaEventCreateWithFlags(&v[i], flags), "cudaEventCreate");
@@ -724,44 +728,58 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
 
 // ------------------------------------------------------- from host memory
 // ring_attn_fwd_host: the heads are independent problems, so they run in
-// groups of whole K/V heads with their query heads: the inputs of group g+1
-// are copied in (stream `in`) while group g computes on the caller's stream
-// and the outputs of group g-1 are copied out (stream `out`).  Each group is
-// one ring_attn_fwd of a handle for the group's heads, so the results are
-// those of one ring_attn_fwd over all heads.
+// groups of whole K/V heads with their query heads.  The inputs of every
+// group are copied in on stream `in`, in group order; each group is one
+// ring_attn_fwd of a handle for the group's heads, on one of two compute
+// lanes (the caller's stream and `lane1`, alternately), as soon as its
+// inputs are in; its outputs are copied out on stream `out` as soon as it
+// is done.  The two lanes run at the same time, so the SMs one group's step
+// kernel leaves idle in its last wave take the other group's blocks.  The
+// first two and the last two groups hold one K/V head each, which shortens
+// the copy-in before the first kernel and the copy-out after the last.  The
+// results are those of one ring_attn_fwd over all heads.
 
 }  // extern "C"
 
 namespace {
 
-// groups: the most of 4, 2, 1 that divides the K/V heads of all batches
-int host_groups(const Plan& p) {
-  const int units = p.B * p.Hkv;
-  for (int g : {4, 2})
-    if (units % g == 0) return g;
-  return 1;
+// K/V heads of each group: with 8 or more K/V heads in all batches, one in
+// each of the first two and last two groups and the rest in an even number
+// of near-equal groups of at most a quarter of them; with fewer, one each.
+std::vector<int> host_group_sizes(int units) {
+  if (units < 8) return std::vector<int>(units, 1);
+  const int mid = units - 4, cap = (units + 3) / 4;
+  int m = (mid + cap - 1) / cap;
+  m += m & 1;
+  std::vector<int> sizes = {1, 1};
+  for (int i = 0; i < m; ++i) sizes.push_back(mid / m + (i < mid % m ? 1 : 0));
+  sizes.push_back(1);
+  sizes.push_back(1);
+  return sizes;
 }
 
-// The group handle follows the parent's options (window, documents,
-// rotation, wait limit); its plan is rebuilt when they changed.
-int sync_group_handle(ring_attn* h) {
+// The group handles follow the parent's options (window, documents,
+// rotation, wait limit); their plans are rebuilt when those changed.
+int sync_group_handles(ring_attn* h) {
   HostPipe* hp = h->pipe;
-  ring_attn* sub = hp->sub;
   const Plan& p = h->plan;
-  if (sub->plan.window != p.window || sub->plan.seg_bounds != p.seg_bounds) {
-    const int units = p.B * p.Hkv / hp->groups;
-    const int G = p.H / p.Hkv;
-    Plan np;
-    std::string err;
-    int rc = build_plan(&np, 1, units * G, p.N, p.d, p.P, p.causal, p.layout, &err, p.window, &p.seg_bounds);
-    if (rc != RING_OK) return fail(rc, err);
-    np.Hkv = units;
-    sub->plan = std::move(np);
-    sub->seg_dirty = true;
+  const int G = p.H / p.Hkv;
+  for (size_t i = 0; i < hp->subs.size(); ++i) {
+    ring_attn* sub = hp->subs[i];
+    if (sub->plan.window != p.window || sub->plan.seg_bounds != p.seg_bounds) {
+      const int units = hp->sub_units[i];
+      Plan np;
+      std::string err;
+      int rc = build_plan(&np, 1, units * G, p.N, p.d, p.P, p.causal, p.layout, &err, p.window, &p.seg_bounds);
+      if (rc != RING_OK) return fail(rc, err);
+      np.Hkv = units;
+      sub->plan = std::move(np);
+      sub->seg_dirty = true;
+    }
+    sub->rotation = h->rotation;
+    sub->fwd_lap = h->fwd_lap;
+    sub->wait_limit_ns = h->wait_limit_ns;
   }
-  sub->rotation = h->rotation;
-  sub->fwd_lap = h->fwd_lap;
-  sub->wait_limit_ns = h->wait_limit_ns;
   return RING_OK;
 }
 
@@ -769,10 +787,10 @@ int build_pipe(ring_attn* h, HostPipe* hp);
 
 // The pipeline is attached to the handle only once every part of it exists.
 int ensure_pipe(ring_attn* h) {
-  if (h->pipe) return sync_group_handle(h);
+  if (h->pipe) return sync_group_handles(h);
   HostPipe* hp = new (std::nothrow) HostPipe();
   if (!hp) return fail(RING_ERR_OOM, "out of host memory");
-  h->pipe = hp;  // sync_group_handle reads it
+  h->pipe = hp;  // sync_group_handles reads it
   const int rc = build_pipe(h, hp);
   if (rc) {
     h->pipe = nullptr;
@@ -783,13 +801,30 @@ int ensure_pipe(ring_attn* h) {
 
 int build_pipe(ring_attn* h, HostPipe* hp) {
   const Plan& p = h->plan;
-  hp->groups = host_groups(p);
-  const int units = p.B * p.Hkv / hp->groups;
   const int G = p.H / p.Hkv;
-  int rc = ring_attn_create_gqa(&hp->sub, 1, units * G, units, p.N, p.d, p.P, p.causal, p.layout);
+  hp->sizes = host_group_sizes(p.B * p.Hkv);
+  const int groups = (int)hp->sizes.size();
+  hp->lanes = groups > 1 ? 2 : 1;
+  // one handle per (lane, group size)
+  for (int g = 0; g < groups; ++g) {
+    const int lane = g % hp->lanes, units = hp->sizes[g];
+    int found = -1;
+    for (size_t i = 0; i < hp->subs.size(); ++i)
+      if (hp->sub_lane[i] == lane && hp->sub_units[i] == units) found = (int)i;
+    if (found < 0) {
+      ring_attn* sub = nullptr;
+      int rc = ring_attn_create_gqa(&sub, 1, units * G, units, p.N, p.d, p.P, p.causal, p.layout);
+      if (rc) return rc;
+      sub->plan.window = -1;  // forces the first sync to build the plan with the options
+      found = (int)hp->subs.size();
+      hp->subs.push_back(sub);
+      hp->sub_units.push_back(units);
+      hp->sub_lane.push_back(lane);
+    }
+    hp->group_sub.push_back(found);
+  }
+  int rc = sync_group_handles(h);
   if (rc) return rc;
-  hp->sub->plan.window = -1;  // forces the first sync to build the plan with the options
-  if ((rc = sync_group_handle(h))) return rc;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t q_bytes = (size_t)p.B * p.H * (size_t)p.N * p.d * 2;
   const size_t kv_bytes = (size_t)p.B * p.Hkv * (size_t)p.N * p.d * 2;
@@ -800,15 +835,19 @@ int build_pipe(ring_attn* h, HostPipe* hp) {
   hp->v_off = hp->k_off + up(kv_bytes);
   hp->o_off = hp->v_off + up(kv_bytes);
   hp->l_off = hp->o_off + up(o_bytes);
-  hp->ws_off = hp->l_off + up(l_bytes);
-  const size_t total = hp->ws_off + fwd_workspace(hp->sub->plan).total;
+  size_t total = hp->l_off + up(l_bytes);
+  for (ring_attn* sub : hp->subs) {
+    hp->sub_ws.push_back(total);
+    total += up(fwd_workspace(sub->plan).total);
+  }
   RA_CUDA(cudaMalloc(&hp->dev, total), "cudaMalloc(host-call buffers)");
   RA_CUDA(cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking), "cudaStreamCreate");
   RA_CUDA(cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking), "cudaStreamCreate");
-  if ((rc = make_events(hp->ev_in, hp->groups, cudaEventDisableTiming))) return rc;
-  if ((rc = make_events(hp->ev_comp, hp->groups, cudaEventDisableTiming))) return rc;
-  RA_CUDA(cudaEventCreateWithFlags(&hp->ev_start, cudaEventDisableTiming), "cudaEventCreate");
-  RA_CUDA(cudaEventCreateWithFlags(&hp->ev_done, cudaEventDisableTiming), "cudaEventCreate");
+  RA_CUDA(cudaStreamCreateWithFlags(&hp->lane1, cudaStreamNonBlocking), "cudaStreamCreate");
+  if ((rc = make_events(hp->ev_in, groups, cudaEventDisableTiming))) return rc;
+  if ((rc = make_events(hp->ev_comp, groups, cudaEventDisableTiming))) return rc;
+  for (cudaEvent_t* e : {&hp->ev_start, &hp->ev_done, &hp->ev_lane})
+    RA_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "cudaEventCreate");
   return RING_OK;
 }
 
@@ -825,58 +864,64 @@ int ring_attn_fwd_host(ring_attn_t h, const void* q, const void* k, const void* 
   HostPipe* hp = h->pipe;
   const Plan& p = h->plan;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const int groups = hp->groups;
-  const size_t units = (size_t)p.B * p.Hkv / groups;  // K/V heads per group
-  const size_t hq = units * (p.H / p.Hkv);             // query heads per group
-  const size_t rows = (size_t)p.N;
-  const size_t q_b = hq * rows * p.d * 2, kv_b = units * rows * p.d * 2;
-  const size_t o_b = hq * rows * p.d * 4, l_b = hq * rows * 4;
+  const int groups = (int)hp->sizes.size();
+  const size_t G = p.H / p.Hkv, rows = (size_t)p.N;
+  const size_t kv_head = rows * p.d * 2, q_head = G * rows * p.d * 2;  // bytes per K/V head
+  const size_t o_head = G * rows * p.d * 4, l_head = G * rows * 4;
   uint8_t* dev = hp->dev;
   // the copies start after the caller's earlier work on its stream, and
   // after the previous call's outputs have left the device buffers
   RA_CUDA(cudaEventRecord(hp->ev_start, cs), "cudaEventRecord");
   RA_CUDA(cudaStreamWaitEvent(hp->in, hp->ev_start, 0), "cudaStreamWaitEvent");
   if (hp->have_done) RA_CUDA(cudaStreamWaitEvent(hp->in, hp->ev_done, 0), "cudaStreamWaitEvent");
-  for (int g = 0; g < groups; ++g) {
+  for (int g = 0, u0 = 0; g < groups; u0 += hp->sizes[g++]) {
+    const size_t u = hp->sizes[g];
     // K and V first: the forward's first kernel packs them
-    RA_CUDA(cudaMemcpyAsync(dev + hp->k_off + g * kv_b, static_cast<const uint8_t*>(k) + g * kv_b, kv_b,
-                            cudaMemcpyHostToDevice, hp->in),
+    RA_CUDA(cudaMemcpyAsync(dev + hp->k_off + u0 * kv_head, static_cast<const uint8_t*>(k) + u0 * kv_head,
+                            u * kv_head, cudaMemcpyHostToDevice, hp->in),
             "cudaMemcpyAsync(k)");
-    RA_CUDA(cudaMemcpyAsync(dev + hp->v_off + g * kv_b, static_cast<const uint8_t*>(v) + g * kv_b, kv_b,
-                            cudaMemcpyHostToDevice, hp->in),
+    RA_CUDA(cudaMemcpyAsync(dev + hp->v_off + u0 * kv_head, static_cast<const uint8_t*>(v) + u0 * kv_head,
+                            u * kv_head, cudaMemcpyHostToDevice, hp->in),
             "cudaMemcpyAsync(v)");
-    RA_CUDA(cudaMemcpyAsync(dev + hp->q_off + g * q_b, static_cast<const uint8_t*>(q) + g * q_b, q_b,
-                            cudaMemcpyHostToDevice, hp->in),
+    RA_CUDA(cudaMemcpyAsync(dev + hp->q_off + u0 * q_head, static_cast<const uint8_t*>(q) + u0 * q_head,
+                            u * q_head, cudaMemcpyHostToDevice, hp->in),
             "cudaMemcpyAsync(q)");
     RA_CUDA(cudaEventRecord(hp->ev_in[g], hp->in), "cudaEventRecord");
   }
-  // Every group's forward and output copies.  Whatever happens, the copy
-  // streams are closed out below, so the caller's stream and the next call
-  // order after everything this call queued.
+  // Every group's forward on its lane, and its output copies.  Whatever
+  // happens, the other streams are closed out below, so the caller's stream
+  // and the next call order after everything this call queued.
   rc = RING_OK;
-  for (int g = 0; g < groups && rc == RING_OK; ++g) {
-    float* o_dev = reinterpret_cast<float*>(dev + hp->o_off + g * o_b);
-    float* l_dev = reinterpret_cast<float*>(dev + hp->l_off + g * l_b);
-    cudaError_t e = cudaStreamWaitEvent(cs, hp->ev_in[g], 0);
+  for (int g = 0, u0 = 0; g < groups && rc == RING_OK; u0 += hp->sizes[g++]) {
+    const size_t u = hp->sizes[g];
+    const int si = hp->group_sub[g];
+    const cudaStream_t ls = hp->sub_lane[si] == 0 ? cs : hp->lane1;
+    float* o_dev = reinterpret_cast<float*>(dev + hp->o_off + u0 * o_head);
+    float* l_dev = reinterpret_cast<float*>(dev + hp->l_off + u0 * l_head);
+    cudaError_t e = cudaStreamWaitEvent(ls, hp->ev_in[g], 0);
     if (e != cudaSuccess) {
       rc = fail(RING_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(e));
       break;
     }
-    if ((rc = ring_attn_fwd(hp->sub, dev + hp->q_off + g * q_b, dev + hp->k_off + g * kv_b,
-                            dev + hp->v_off + g * kv_b, o_dev, l_dev, dev + hp->ws_off, stream)))
+    if ((rc = ring_attn_fwd(hp->subs[si], dev + hp->q_off + u0 * q_head, dev + hp->k_off + u0 * kv_head,
+                            dev + hp->v_off + u0 * kv_head, o_dev, l_dev, dev + hp->sub_ws[si], ls)))
       break;
-    if ((e = cudaEventRecord(hp->ev_comp[g], cs)) == cudaSuccess &&
+    if ((e = cudaEventRecord(hp->ev_comp[g], ls)) == cudaSuccess &&
         (e = cudaStreamWaitEvent(hp->out, hp->ev_comp[g], 0)) == cudaSuccess &&
-        (e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out) + g * o_b, o_dev, o_b, cudaMemcpyDeviceToHost,
-                             hp->out)) == cudaSuccess)
-      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + g * l_b, l_dev, l_b, cudaMemcpyDeviceToHost, hp->out);
+        (e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out) + u0 * o_head, o_dev, u * o_head,
+                             cudaMemcpyDeviceToHost, hp->out)) == cudaSuccess)
+      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + u0 * l_head, l_dev, u * l_head,
+                          cudaMemcpyDeviceToHost, hp->out);
     if (e != cudaSuccess) rc = fail(RING_ERR_CUDA, std::string("output copy: ") + cudaGetErrorString(e));
   }
-  // the caller's stream completes after the last output copy (and after
-  // the copy-in stream, in case a failure left copies there unwaited)
+  // the caller's stream completes after the last output copy and after the
+  // second lane (and after the copy-in stream, in case a failure left
+  // copies there unwaited)
   RA_CUDA(cudaEventRecord(hp->ev_done, hp->out), "cudaEventRecord");
   hp->have_done = true;
   RA_CUDA(cudaStreamWaitEvent(cs, hp->ev_done, 0), "cudaStreamWaitEvent");
+  RA_CUDA(cudaEventRecord(hp->ev_lane, hp->lane1), "cudaEventRecord");
+  RA_CUDA(cudaStreamWaitEvent(cs, hp->ev_lane, 0), "cudaStreamWaitEvent");
   if (rc != RING_OK) {
     RA_CUDA(cudaEventRecord(hp->ev_start, hp->in), "cudaEventRecord");
     RA_CUDA(cudaStreamWaitEvent(cs, hp->ev_start, 0), "cudaStreamWaitEvent");
@@ -1218,11 +1263,14 @@ int ring_attn_check(ring_attn_t h, void* stream) {
   RA_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
   RA_CUDA(cudaStreamSynchronize(h->side), "cudaStreamSynchronize");
   if (h->pipe) {
-    // ring_attn_fwd_host: its copy streams, and the group handle's kernels
-    RA_CUDA(cudaStreamSynchronize(h->pipe->in), "cudaStreamSynchronize");
-    RA_CUDA(cudaStreamSynchronize(h->pipe->out), "cudaStreamSynchronize");
-    int rc = ring_attn_check(h->pipe->sub, stream);
-    if (rc) return rc;
+    // ring_attn_fwd_host: its copy streams, its second lane, and the group
+    // handles' kernels
+    for (cudaStream_t st : {h->pipe->in, h->pipe->out, h->pipe->lane1})
+      RA_CUDA(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+    for (ring_attn* sub : h->pipe->subs) {
+      int rc = ring_attn_check(sub, stream);
+      if (rc) return rc;
+    }
   }
   int words[2] = {0, 0};
   RA_CUDA(cudaMemcpy(words, h->d_err, sizeof words, cudaMemcpyDeviceToHost), "cudaMemcpy(error word)");

@@ -26,7 +26,9 @@ def built():
 
 CASES = [
     # (B, H, Hkv, N, d, P, causal, layout, window, segments)
-    (1, 8, 8, 4096, 128, 4, True, "striped", 0, None),  # 4 groups of 2 heads
+    (1, 8, 8, 4096, 128, 4, True, "striped", 0, None),  # groups of 1, 1, 2, 2, 1, 1 heads
+    (1, 16, 16, 1024, 64, 4, True, "striped", 0, None),  # 1, 1, 3, 3, 3, 3, 1, 1
+    (1, 9, 9, 1024, 128, 4, True, "contiguous", 0, None),  # 1, 1, 3, 2, 1, 1: a size on one lane only
     (1, 8, 2, 2048, 128, 4, True, "contiguous", 0, None),  # grouped K/V heads: 2 groups of 4 query heads
     (2, 1, 1, 1024, 64, 4, False, "contiguous", 0, None),  # groups across the batch
     (1, 3, 3, 1024, 128, 4, True, "striped", 0, None),  # 3 heads: one group
@@ -82,3 +84,27 @@ def test_fwd_host_new_inputs_and_oracle(orc):
         print(f"fwd_host seed {seed}: max|dout|={d_out:.3e} max|dlse|={d_lse:.3e}")
         assert d_out <= 1e-2 and d_lse <= 1e-3
     att.close()
+
+
+def test_fwd_host_options_change():
+    """Options set between calls reach every group handle: a window, then
+    documents, then neither, each call equal to ring_attn_fwd's result under
+    the same options (16 heads: groups of two sizes on both lanes)."""
+    B, H, N, d, P = 1, 16, 1024, 64, 4
+    q, k, v = make_qkv(B, H, N, d, seed=720)
+    qh, kh, vh = (x.pin_memory() for x in (q, k, v))
+    qc, kc, vc = (x.cuda() for x in (q, k, v))
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped")
+    ref = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped")
+    for window, segments in ((200, None), (0, [0, 300, 1024]), (0, None)):
+        for a in (att, ref):
+            a.set_option(ra.RING_OPT_WINDOW, window)
+            a.set_segments(segments)
+        out_d, lse_d = ref.fwd(qc, kc, vc)
+        out_h, lse_h = att.fwd_host(qh, kh, vh)
+        torch.cuda.current_stream().synchronize()
+        att.check()
+        ref.check()
+        assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu()), (window, segments)
+    att.close()
+    ref.close()
