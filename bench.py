@@ -658,8 +658,9 @@ def run_decode(args, w):
     """Split-K/V decode / short-query prefill (ring_attn_decode): LQ queries
     at the end of the workload's sequence over its K/V cache, inputs resident,
     K calls timed with CUDA events.  The roofline is HBM for short queries:
-    algorithmic bytes per call = the K/V cache read once + q read + the P
-    shard states written and read back + out and lse written."""
+    algorithmic bytes per call = the K/V cache read once + q read + out and
+    lse written (the key pieces' partial states, a few hundred KB, are the
+    implementation's and not counted)."""
     import torch
 
     import ring_sequence_parallelism_gb300 as ra
@@ -688,8 +689,7 @@ def run_decode(args, w):
     BH = w.B * w.H
     pairs = sum(min(w.N, w.N - Lq + i + 1) for i in range(Lq)) if w.causal else Lq * w.N
     flops = 4 * w.d * BH * pairs
-    state_bytes = 2 * w.P * BH * Lq * (w.d + 2) * 4
-    bytes_ = 2 * w.B * w.kv_heads * w.N * w.d * 2 + BH * Lq * w.d * 2 + state_bytes + BH * Lq * (w.d + 1) * 4
+    bytes_ = 2 * w.B * w.kv_heads * w.N * w.d * 2 + BH * Lq * w.d * 2 + BH * Lq * (w.d + 1) * 4
     pk, pk_kind = peaks()
     hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     gbs = bytes_ / (ms * 1e-3) / 1e9
@@ -701,7 +701,7 @@ def run_decode(args, w):
         "tokens_per_s": w.B * Lq / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "peak_kind": f"hbm_gbs ({pk_kind})", "algorithmic_bytes": bytes_,
-                     "kernels": "block_partial_kernel (P shard states) + merge_shards_kernel"},
+                     "kernels": "block_partial_kernel (one state per key piece) + merge_shards_kernel"},
         "clocks": clocks.summary(),
         "gpu_launches": 2 * args.steps,
     }

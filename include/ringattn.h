@@ -357,20 +357,22 @@ RINGATTN_API int ring_attn_get_bwd_timing(ring_attn_t h, float* dkdv_ms, float* 
  * merge").  Lq new queries sit at global positions N-Lq .. N-1 of the
  * sequence the handle describes, and their K/V are already part of the
  * cache, so under the causal mask query i sees the cached keys at positions
- * <= N-Lq+i (all N keys for Lq = 1).  One launch computes the P shard states
- * (shard r: its K/V block read in place from the cache, laid out as the
- * handle's layout says); a second merges the P states of each row and
- * finalizes.  When the shards x heads x query tiles would leave the SMs
- * mostly idle (short queries), each shard's keys are cut into up to
- * ksplit pieces (a power of two, enough for about 1024 CTAs, at least 4
- * key tiles a piece), each with its own state; the merge folds all
- * P * ksplit states the same way.
+ * <= N-Lq+i (all N keys for Lq = 1).  The cache is read in place in natural
+ * order; its keys are cut into ksplit contiguous pieces (the ring's shards
+ * are one partition of them; on one GPU the pieces are sized for the SMs),
+ * and one launch computes a local state per piece and query tile pair: the
+ * smallest ksplit that fills at least 90 % of the SMs in whole waves, at
+ * least 4 key tiles a piece (at Lq = 1 on 16 heads and 152 SMs: 9 pieces
+ * of about 114 key tiles, one wave).  A second launch merges the ksplit
+ * states of each row and finalizes.  The result does not depend on the
+ * handle's layout or P.
  *   q         [B][H][Lq][d] bf16
  *   k, v      the cache, natural order [B][Hkv][N][d] bf16
  *   out       [B][H][Lq][d] fp32,  lse [B][H][Lq] fp32
  *   workspace ring_attn_decode_workspace_size(h, Lq) bytes, 256-byte aligned
- * All three layouts (zigzag: shard r's block is chunk r then chunk 2P-1-r of
- * the cache); 1 <= Lq <= N.  Asynchronous on `stream`. */
+ *             (it depends on the current device's SM count)
+ * Windows and documents apply (RING_OPT_WINDOW, ring_attn_set_segments);
+ * 1 <= Lq <= N.  Asynchronous on `stream`. */
 RINGATTN_API int ring_attn_decode_workspace_size(ring_attn_t h, long long Lq, size_t* bytes);
 RINGATTN_API int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v, long long Lq, float* out,
                                   float* lse, void* workspace, void* stream);

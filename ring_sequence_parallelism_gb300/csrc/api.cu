@@ -1100,25 +1100,33 @@ int ring_attn_get_bwd_timing(ring_attn_t h, float* dkdv_ms, float* dq_ms, float*
 }
 
 // ---------------------------------------------------------------- decode
-// Workspace of ring_attn_decode: the P shard states of the Lq query rows,
-// m and l [P][B][H][Lq] and O~ [P][B][H][Lq][d] fp32.
-// Short queries leave few CTAs (P shards x heads x query tile pairs): when
-// they would fill fewer than about 1024 CTAs, each block's key tiles are cut
-// into ksplit pieces, each with a state of its own, merged with the others
-// exactly like the shards' states (the smallest power of two reaching 1024
-// CTAs, with at least 4 key tiles a piece).
+// ring_attn_decode reads the cache in place, in natural order, as one block
+// of N keys per K/V head (whatever the layout of the ring: its shards are a
+// partition of these keys, and any partition merges to the same result).
+// Short queries leave few CTAs, so the keys are cut into ksplit contiguous
+// pieces, each piece of each query tile pair one CTA with a state of its
+// own; merge_shards_kernel folds the ksplit states of each row exactly, by
+// the same rule that folds the shards' states.  ksplit is the smallest
+// count that fills at least 90 % of the SMs in whole waves (one wave of
+// long pieces when the queries are few, so each CTA's set-up is paid once
+// per SM), with at least 4 key tiles a piece.
+// Workspace: m and l [ksplit][B][H][Lq] and O~ [ksplit][B][H][Lq][d] fp32.
 static int decode_ksplit(const Plan& p, long long Lq) {
   const long long T = (Lq + kTileM - 1) / kTileM;
-  const long long units = (long long)p.P * p.B * p.H * ((T + 1) / 2);
-  const int cap = std::max(1, p.KT / 4);
-  int ks = 1;
-  while (units * ks < 1024 && ks * 2 <= cap) ks *= 2;
-  return ks;
+  const long long units = (long long)p.B * p.H * ((T + 1) / 2);
+  const long long KT = ((long long)p.N + kTileN - 1) / kTileN;
+  const long long cap = std::max(1LL, KT / 4);
+  const long long sms = sm_count();
+  for (long long ks = 1; ks <= cap; ++ks) {
+    const long long ctas = units * ks, waves = (ctas + sms - 1) / sms;
+    if (ctas * 10 >= sms * waves * 9) return (int)ks;
+  }
+  return (int)cap;
 }
 
 static size_t decode_ws(const Plan& p, long long Lq) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t rows = (size_t)p.P * decode_ksplit(p, Lq) * p.B * p.H * (size_t)Lq;
+  const size_t rows = (size_t)decode_ksplit(p, Lq) * p.B * p.H * (size_t)Lq;
   return up(rows * p.d * 4) + 2 * up(rows * 4);
 }
 
@@ -1141,36 +1149,24 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
     return fail(RING_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   int rc = ensure_device(h);
   if (rc) return rc;
-  const int P = p.P, BH = p.B * p.H, BHkv = p.B * p.Hkv;
+  const int BH = p.B * p.H, BHkv = p.B * p.Hkv;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const cuuint64_t d = (cuuint64_t)p.d, n = (cuuint64_t)p.n, row_b = d * 2, lq = (cuuint64_t)Lq;
+  const cuuint64_t d = (cuuint64_t)p.d, Nn = (cuuint64_t)p.N, row_b = d * 2, lq = (cuuint64_t)Lq;
   CUtensorMap qm, km, vm;
   {
     cuuint64_t dims[4] = {d, lq, 1, (cuuint64_t)BH};
     cuuint64_t str[3] = {row_b, row_b * lq, row_b * lq};
     if ((rc = encode_map(&qm, q, dims, str, kTileM, 1))) return rc;
   }
-  const bool zigzag = p.layout == RING_LAYOUT_ZIGZAG;
-  if (zigzag) {
-    // the cache as 2P chunks of c = n/2 tokens, dims (d, c, BHkv, 2P): block
-    // j is chunk j, then chunk 2P-1-j (kKvZigzag picks the chunk per tile)
-    const cuuint64_t c = n / 2;
-    cuuint64_t dims[4] = {d, c, (cuuint64_t)BHkv, (cuuint64_t)(2 * P)};
-    cuuint64_t str[3] = {row_b, row_b * (cuuint64_t)p.N, row_b * c};
-    if ((rc = encode_map(&km, k, dims, str, kTileN, 1))) return rc;
-    if ((rc = encode_map(&vm, v, dims, str, kTileN, 1))) return rc;
-  } else {
-    // block j of the cache in place: key row k of block j is token j n + k
-    // (contiguous) or k P + j (striped); dims (d, n, BHkv, P)
-    const cuuint64_t Nn = (cuuint64_t)p.N;
-    const bool striped = p.layout == RING_LAYOUT_STRIPED;
-    cuuint64_t dims[4] = {d, n, (cuuint64_t)BHkv, (cuuint64_t)P};
-    cuuint64_t str[3] = {striped ? row_b * P : row_b, row_b * Nn, striped ? row_b : row_b * n};
+  {
+    // the cache in natural order, one block of N keys per K/V head: dims (d, N, BHkv, 1)
+    cuuint64_t dims[4] = {d, Nn, (cuuint64_t)BHkv, 1};
+    cuuint64_t str[3] = {row_b, row_b * Nn, row_b * Nn * (cuuint64_t)BHkv};
     if ((rc = encode_map(&km, k, dims, str, kTileN, 1))) return rc;
     if ((rc = encode_map(&vm, v, dims, str, kTileN, 1))) return rc;
   }
   const int ksplit = decode_ksplit(p, Lq);
-  const size_t rows = (size_t)P * ksplit * BH * (size_t)Lq;
+  const size_t rows = (size_t)ksplit * BH * (size_t)Lq;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   float* o_st = reinterpret_cast<float*>(ws);
@@ -1179,7 +1175,12 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
 
   StepArgs a = base_args(h);
   if ((rc = device_segments(h, &a.seg_lo, &a.seg_hi))) return rc;
-  a.o_state = o_st;  // the states of shard r's key piece x: rows [r * ksplit + x][bh][i]
+  // one contiguous block (P = 1): key k is at position k
+  a.n = p.N;
+  a.P = 1;
+  a.KT = (int)((p.N + kTileN - 1) / kTileN);
+  a.layout = RING_LAYOUT_CONTIGUOUS;
+  a.o_state = o_st;  // the states of key piece x: rows [x][bh][i]
   a.m_state = m_st;
   a.l_state = l_st;
   a.out = nullptr;
@@ -1191,16 +1192,16 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
   a.T = (int)((Lq + kTileM - 1) / kTileM);
   a.decode_pos0 = p.N - Lq;
   a.q_mode = kQShardMajor;
-  a.kv_mode = zigzag ? kKvZigzag : kKvSlotJ;  // at step 0 shard r reads block r
+  a.kv_mode = kKvSlotJ;  // block 0 of the one-block map
   a.ksplit = ksplit;
   a.step = 0;
   a.accumulate = 0;
   a.finalize = 0;
-  a.n_active = P;
-  for (int r = 0; r < P; ++r) a.active[r] = (unsigned short)r;
-  const int grid = block_partial_grid(a.T, P, BH) * ksplit;
+  a.n_active = 1;
+  a.active[0] = 0;
+  const int grid = block_partial_grid(a.T, 1, BH) * ksplit;
   RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km, &vm, p.d, grid, cs), "decode block launch");
-  RA_CUDA((cudaError_t)launch_merge_shards(m_st, l_st, o_st, out, lse, (long long)BH * Lq, p.d, P * ksplit, cs),
+  RA_CUDA((cudaError_t)launch_merge_shards(m_st, l_st, o_st, out, lse, (long long)BH * Lq, p.d, ksplit, cs),
           "decode merge launch");
   return RING_OK;
 }

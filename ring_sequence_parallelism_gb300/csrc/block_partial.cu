@@ -213,20 +213,6 @@ __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   return w;
 }
 
-// TMA coordinates (row, slot) of the key tile starting at key0 of the CTA's
-// block: the block's own slot, or for the zigzag cache (kKvZigzag) the chunk
-// holding the tile (chunks are whole tiles, so a tile lies in one chunk).
-__device__ __forceinline__ void kv_coords(const StepArgs& a, const WorkItem& w, int key0, int& row, int& slot) {
-  if (a.kv_mode == kKvZigzag) {
-    const int c = a.n / 2;
-    row = key0 < c ? key0 : key0 - c;
-    slot = key0 < c ? w.j : 2 * a.P - 1 - w.j;
-  } else {
-    row = key0;
-    slot = w.slot;
-  }
-}
-
 // ------------------------------------------------------------- the kernel
 // kWin: row-dependent bounds are in force, a sliding window's lower bound
 // and/or the document bounds of sequence packing (instantiated apart so the
@@ -340,18 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const int key0 = key_tile(a, w, 0) * kTileN;
       if (nq > 0) load_q(0);
-      int krow0, kslot0;
-      kv_coords(a, w, key0, krow0, kslot0);
       mbar_expect_tx(bar(L::kBarKFull), L::kKBytes);
       for (int c = 0; c < D / L::kSub; ++c)
-        tma_load_4d(sbase + L::kOffK + c * (kTileN * 128), &k_map, bar(L::kBarKFull), c * L::kSub, krow0, w.kvh,
-                    kslot0);
+        tma_load_4d(sbase + L::kOffK + c * (kTileN * 128), &k_map, bar(L::kBarKFull), c * L::kSub, key0, w.kvh,
+                    w.slot);
       if (nq > 1) load_q(1);
       if (!a.debug_drop_v) {  // test hook: nothing ever completes v_full
         mbar_expect_tx(bar(L::kBarVFull), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
-          tma_load_4d(sbase + L::kOffV + c * (kTileN * 128), &v_map, bar(L::kBarVFull), c * L::kSub, krow0, w.kvh,
-                      kslot0);
+          tma_load_4d(sbase + L::kOffV + c * (kTileN * 128), &v_map, bar(L::kBarVFull), c * L::kSub, key0, w.kvh,
+                      w.slot);
       }
     }
   }
@@ -391,12 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (used0) ok = mbar_wait(bar(L::kBarKEmpty + 2 * st), par0, abort_flag, a, 1);
         if (ok && used1) ok = mbar_wait(bar(L::kBarKEmpty + 2 * st + 1), par1, abort_flag, a, 1);
         if (!ok) break;
-        int krow, kslot;
-        kv_coords(a, w, key0, krow, kslot);
         mbar_expect_tx(bar(L::kBarKFull + st), L::kKBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffK + st * L::kKBytes + c * (kTileN * 128), &k_map, bar(L::kBarKFull + st),
-                      c * L::kSub, krow, w.kvh, kslot);
+                      c * L::kSub, key0, w.kvh, w.slot);
         k_issued = j + 1;
         if (used0) ok = mbar_wait(bar(L::kBarVEmpty + 2 * st), par0, abort_flag, a, 2);
         if (ok && used1) ok = mbar_wait(bar(L::kBarVEmpty + 2 * st + 1), par1, abort_flag, a, 2);
@@ -405,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar(L::kBarVFull + st), L::kVBytes);
         for (int c = 0; c < D / L::kSub; ++c)
           tma_load_4d(sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), &v_map, bar(L::kBarVFull + st),
-                      c * L::kSub, krow, w.kvh, kslot);
+                      c * L::kSub, key0, w.kvh, w.slot);
         v_issued = j + 1;
       }
       if (sends && ok) {
@@ -679,9 +661,8 @@ int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map
   // without `forward` the kernel never touches the send maps
   const CUtensorMap& kn = *static_cast<const CUtensorMap*>(k_next_map ? k_next_map : k_map);
   const CUtensorMap& vn = *static_cast<const CUtensorMap*>(v_next_map ? v_next_map : v_map);
-  // row-dependent bounds: a window, documents, or short queries in the zigzag layout
-  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr ||
-                   (a.layout == RING_LAYOUT_ZIGZAG && a.decode_pos0 >= 0);
+  // row-dependent bounds: a window or documents
+  const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
   if (d == 64) {
     if (win) block_partial_kernel<64, true><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
     else block_partial_kernel<64, false><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);

@@ -67,16 +67,10 @@ __device__ __forceinline__ void block_rule(const StepArgs& a, int r, int j, int 
   if (!a.causal) return;
   const long long W = kWin ? a.window : 0;
   if (a.decode_pos0 >= 0) {
-    // Short queries at global positions pos0 + i against the keys of block
-    // j: key k is at j n + k (contiguous) or k P + j (striped), so k is
-    // allowed iff k <= (pos0 + i) - j n, or k <= floor((pos0 + i - j) / P);
-    // a window drops positions W or more behind the query.
-    if (a.layout == RING_LAYOUT_STRIPED) {
-      w->b = a.decode_pos0 - j;
-      w->q = a.P;
-    } else {
-      w->b = a.decode_pos0 - (long long)j * n;
-    }
+    // Short queries at global positions pos0 + i against the cache read as
+    // one contiguous block (key k at position k): key k is allowed iff
+    // k <= pos0 + i; a window drops positions W or more behind the query.
+    w->b = a.decode_pos0;
     if (W > 0) w->bl = w->b - W;
     return;
   }
@@ -119,7 +113,7 @@ __device__ __forceinline__ void seg_bounds(const StepArgs& a, int r, int j, long
   }
 }
 
-// Zigzag with a sliding window, documents or short queries.  A shard (or a
+// Zigzag with a sliding window or documents.  A shard (or a
 // block) holds chunk r then chunk 2P-1-r of c = n/2 tokens, so its positions
 // increase with the local index; the positions a query may see form one
 // interval [L, U] (causal: up to itself; a window: from W-1 tokens back; a
@@ -132,9 +126,8 @@ __device__ __forceinline__ void zz_local_interval(long long c, long long A0, lon
   lo = L <= A0 ? 0 : (L < A0 + c ? L - A0 : (L <= B0 ? c : (L < B0 + c ? c + L - B0 : 2 * c)));
 }
 
-// Global position of local query row i: zigzag shard r, or short queries at pos0 + i.
+// Global position of local query row i of zigzag shard r.
 __device__ __forceinline__ long long zz_query_pos(const StepArgs& a, int r, long long i) {
-  if (a.decode_pos0 >= 0) return a.decode_pos0 + i;
   const long long c = a.n / 2;
   return i < c ? (long long)r * c + i : (long long)(2 * a.P - 1 - r) * c + (i - c);
 }

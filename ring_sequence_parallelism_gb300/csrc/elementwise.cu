@@ -13,19 +13,25 @@
 #include "internal.h"
 
 namespace ringattn {
+
+int sm_count() {
+  static int count = 0;
+  if (count == 0) {
+    int dev = 0, c = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        c > 0)
+      count = c;
+    else
+      return 1;
+  }
+  return count;
+}
+
 namespace {
 
-int g_sm_count = 0;
-
 int grid_for(long long work, int threads) {
-  if (g_sm_count == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || g_sm_count <= 0)
-      g_sm_count = 1;
-  }
   long long blocks = (work + threads - 1) / threads;
-  long long cap = (long long)g_sm_count * 16;
+  long long cap = (long long)sm_count() * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return (int)blocks;

@@ -91,9 +91,7 @@ enum QMode : int {
 enum KvMode : int {
   kKvSlotR = 0,  // rotation buffer: slot r holds block (r - s) mod P
   kKvSlotJ = 1,  // direct: slot j holds block j
-  kKvSingle = 2,  // one block only (slot 0)
-  kKvZigzag = 3   // the natural-order cache in the zigzag layout: map dims (d, n/2, BHkv, 2P); block j's key
-                  // k < n/2 is row k of chunk j, k >= n/2 row k - n/2 of chunk 2P-1-j
+  kKvSingle = 2   // one block only (slot 0)
 };
 
 struct StepArgs {
@@ -118,10 +116,11 @@ struct StepArgs {
   int G;             // query heads per K/V head: query head bh reads K/V head bh / G
   int nq;            // query rows per shard (n for the ring; the short query length otherwise)
   long long window;  // > 0: causal sliding window, a query sees itself and the window-1 tokens before it
-  long long decode_pos0;  // >= 0: queries at global positions pos0 + i against block j's keys
-                          //       (the causal rule from global positions; see ring_attn_decode)
-  int ksplit;             // >= 1: pieces each block's key tiles are cut into (short queries only); piece p
-                          //       of shard r keeps its state in slot r * ksplit + p
+  long long decode_pos0;  // >= 0: short queries at global positions pos0 + i against the keys of
+                          //       the natural-order cache, read as one contiguous block (P = 1, key k
+                          //       at position k; see ring_attn_decode)
+  int ksplit;             // >= 1: pieces the block's key tiles are cut into (short queries only); piece p
+                          //       keeps its state in slot p
   float scale_log2;  // log2(e) / sqrt(d)
   // sequence packing (nullptr: one document): per natural position, the
   // first and one-past-last position of its document; a pair is allowed
@@ -173,6 +172,8 @@ int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map
                          int d, int grid, void* stream, const void* k_next_map = nullptr,
                          const void* v_next_map = nullptr);
 int launch_state_init(float* m, float* l, float* o, long long rows, int d, void* stream);
+// SMs of the current device (1 when there is none)
+int sm_count();
 int launch_merge(float* ma, float* la, float* oa, const float* mb, const float* lb, const float* ob,
                  long long rows, int d, void* stream);
 int launch_merge_shards(const float* m, const float* l, const float* o, float* out, float* lse, long long rows,

@@ -74,12 +74,14 @@ CASES = [
     (1, 4, 1, 2 * 256, 128, 2, False, "striped", 33),      # multi-query, no mask
     (1, 2, 2, 4 * 128, 128, 4, True, "striped", 4 * 128),  # Lq = N: the whole causal attention
     (1, 1, 1, 512, 64, 1, True, "contiguous", 5),          # one shard
-    # a few queries: every shard's keys cut into pieces (the key split)
+    # a few queries: the keys cut into several pieces (the key split)
     (1, 4, 2, 8 * 256, 128, 8, True, "striped", 2),        # grouped-query
     (2, 3, 3, 3 * 200, 64, 3, True, "contiguous", 3),      # ragged shards, B = 2
     (1, 4, 1, 2 * 256, 128, 2, False, "striped", 4),       # multi-query, no mask
     (1, 2, 2, 4 * 256, 128, 4, True, "zigzag", 2),
     (1, 1, 1, 256, 128, 1, True, "contiguous", 1),         # one shard, one query
+    (1, 2, 2, 2000, 128, 4, True, "striped", 1),           # 4 pieces, the last key tile ragged (80 keys)
+    (1, 2, 2, 2000, 64, 4, True, "contiguous", 130),       # two query tiles, ragged last key tile
 ]
 
 
@@ -116,6 +118,23 @@ def test_decode_128k_workload(Lq):
     print(f"decode striped-128k Lq={Lq}: max|dout|={d_out:.3e} max|dlse|={d_lse:.3e}")
     assert d_out <= TOL_OUT and d_lse <= TOL_LSE
     att.close()
+
+
+def test_decode_layout_independent():
+    """The cache is read in natural order and cut into the same key pieces
+    whatever the handle's layout and P: every layout gives the same bits."""
+    B, H, N, d, Lq = 1, 4, 4096, 128, 3
+    q_all, k, v = make_qkv(B, H, N, d, seed=733)
+    q, k, v = q_all[:, :, :Lq].contiguous().cuda(), k.cuda(), v.cuda()
+    got = []
+    for layout, P in (("contiguous", 4), ("striped", 4), ("zigzag", 4), ("striped", 8), ("contiguous", 1)):
+        att = ra.RingAttention(B, H, N, d, P, causal=True, layout=layout)
+        out, lse = att.decode(q, k, v)
+        att.check()
+        got.append((out.cpu(), lse.cpu()))
+        att.close()
+    for out, lse in got[1:]:
+        assert torch.equal(out, got[0][0]) and torch.equal(lse, got[0][1])
 
 
 def test_decode_rejects_bad_lengths():

@@ -6,8 +6,9 @@ A shard's (or block's) positions increase with its local index, so the keys
 a query may see in a block stay one local interval; the kernels take its
 bounds from global positions.  Forward: every row, the three rotation modes
 bit for bit, block partials, the one-launch lap.  Backward: every gradient
-element.  Decode: queries at the end of a zigzag-sharded cache (the key
-split included).  Tolerances as in the other GPU tests."""
+element.  Decode: queries at the end of the cache of a zigzag handle (the
+cache is read in natural order, so the layout does not enter).  Tolerances
+as in the other GPU tests."""
 import numpy as np
 import pytest
 import torch
@@ -166,9 +167,8 @@ def test_zigzag_bwd_masks(orc, case, lap):
 @pytest.mark.parametrize("Lq,window,bounds", [(1, 0, None), (5, 0, None), (130, 0, None), (300, 0, None),
                                                (64, 500, None), (200, 0, [0, 1000, 1900, 4096])])
 def test_zigzag_decode(orc, Lq, window, bounds):
-    """Short queries at positions N-Lq .. N-1 over a zigzag-sharded cache
-    (shard r's block is chunk r then chunk 2P-1-r), against the oracle's
-    dense rows; with Lq = 1 the keys are also cut into pieces."""
+    """Short queries at positions N-Lq .. N-1 over the cache of a zigzag
+    handle with a window or documents, against the oracle's dense rows."""
     B, H, N, d, P = 1, 4, 4096, 128, 4
     q_all, k, v = make_qkv(B, H, N, d, seed=980 + Lq)
     q = q_all[:, :, N - Lq:].contiguous()
