@@ -243,9 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int np = sends ? w.np_send : nk;
   const int nq = nk == 0 ? 0 : (w.tile[1].je > w.tile[1].jb ? 2 : 1);  // Q tiles to load (tile A has keys if B has)
 
-  // Softmax threads (warps 3..10, tile (warp-3)/4, one query row each) start
-  // the loads of their incoming state now, so the latency overlaps the
-  // set-up; the values reach TMEM after the barrier below.
+  // Softmax threads (warps 3..10, tile (warp-3)/4, one query row each) read
+  // their incoming m and l now; the incoming O~ (64 KB a tile) is read once
+  // the tile's Q has landed (below), so that the loads the first MMAs need
+  // (Q, K(0)) are not queued behind it.
   const int t_sm = warp >= 3 ? (warp - 3) / 4 : 0;
   const Tile tw = t_sm == 0 ? w.tile[0] : w.tile[1];
   const int quad = warp & 3;
@@ -266,23 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long ml_idx = a.state_tiled ? tile_base * kTileM + quad * 32 + lane : g;
   float* const o_row = a.state_tiled ? a.o_state + tile_base * (kTileM * D) + (quad * 32 + lane) * 8 : a.o_state + g * D;
   const int o_stride = a.state_tiled ? kTileM * 8 : 8;  // floats from one 8-column chunk to the next
-  uint32_t o_in[D];
   float m_in = -INFINITY, l_in = 0.0f;
   const bool load_state = warp >= 3 && a.accumulate && in_range;
-  if (load_state) {
-#pragma unroll
-    for (int q8 = 0; q8 < D / 8; ++q8) {
-      if (valid) {
-        ld_global_v8(o_row + q8 * o_stride, o_in + q8 * 8);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o_in[q8 * 8 + e] = 0u;
-      }
-    }
-    if (valid) {
-      m_in = a.m_state[ml_idx] * kLog2e;
-      l_in = a.l_state[ml_idx];
-    }
+  if (load_state && valid) {
+    m_in = a.m_state[ml_idx] * kLog2e;
+    l_in = a.l_state[ml_idx];
   }
 
   if (threadIdx.x == 0) {
@@ -490,12 +479,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_addr = tmem + lane_off + L::tmem_o(t);
     float m2 = m_in;  // reference max, log2 domain
     float l = l_in;
+    bool ok = true;
     if (load_state) {
+      // the incoming O~ into TMEM, after this tile's Q has landed (a tile
+      // with keys has its Q loaded; one without reads its state at once)
+      if (tw.je > tw.jb) ok = warp_wait(bar(L::kBarQFull + t), 0, abort_flag, a, 12);
+      uint32_t o_in[D];
+#pragma unroll
+      for (int q8 = 0; q8 < D / 8; ++q8) {
+        if (valid) {
+          ld_global_v8(o_row + q8 * o_stride, o_in + q8 * 8);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o_in[q8 * 8 + e] = 0u;
+        }
+      }
       if constexpr (D == 128) tmem_store128(o_addr, o_in);
       else tmem_store64(o_addr, o_in);
       tmem_store_wait();
     }
-    bool ok = true;
     for (int j = tw.jb; j < tw.je; ++j) {
       ok = warp_wait(bar(L::kBarSFull + t), (j - tw.jb) & 1, abort_flag, a, 8);
       if (!ok) break;
