@@ -592,16 +592,19 @@ def run_ours(args, w):
         att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
         barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(args.steps):
-            att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
-        f1.record(stream)
-        barrier()
+        with ClockSampler(torch.cuda.current_device()) as e2e_clocks:
+            f0.record(stream)
+            for _ in range(args.steps):
+                att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
+            f1.record(stream)
+            barrier()
+            torch.cuda.synchronize()
         e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, world)
         e2e = {"value": whole_job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s",
                "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h)),
-               "d2h_bytes_per_step": out_h.numel() * 4 + lse_h.numel() * 4}
+               "d2h_bytes_per_step": out_h.numel() * 4 + lse_h.numel() * 4,
+               "clocks": e2e_clocks.summary()}
 
     extra = {}
     if world == 1 and not args.no_extra:
