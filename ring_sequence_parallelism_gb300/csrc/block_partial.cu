@@ -233,6 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  // A kernel launched after this one as a programmatic dependent (the
+  // decode's merge) may be scheduled now; it waits for this grid's
+  // completion itself (griddepcontrol.wait) before reading what it wrote.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const WorkItem w = decode_item<kWin>(a);
   const int nk = w.nk;  // loop indices of computed key tiles
   // Loads for sending only (tiles the mask leaves unused) follow the

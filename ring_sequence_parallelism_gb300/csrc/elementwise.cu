@@ -221,6 +221,10 @@ __global__ void merge_shards_kernel(const float* __restrict__ m, const float* __
   constexpr int kGroup = 16;
   constexpr int per = D / 32;  // 2 or 4 columns per lane
   constexpr int d = D;
+  // Launched as a programmatic dependent of the kernel that wrote the
+  // states: wait until that grid has completed and its writes are visible
+  // (returns at once when launched without the dependency).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x % 32;
   const long long warps = (long long)gridDim.x * (blockDim.x / 32);
   for (long long row = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; row < rows; row += warps) {
@@ -274,10 +278,22 @@ int launch_merge_shards(const float* m, const float* l, const float* o, float* o
   if (rows <= 0) return 0;
   const long long blocks = (rows + 7) / 8;  // 8 warps a block
   const int grid = (int)(blocks < 65535 * 32 ? blocks : 65535 * 32);
-  if (d == 64)
-    merge_shards_kernel<64><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(m, l, o, out, lse, rows, P);
-  else
-    merge_shards_kernel<128><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(m, l, o, out, lse, rows, P);
+  // programmatic dependent launch: the merge's blocks are scheduled as the
+  // previous kernel's blocks exit and wait in griddepcontrol.wait, so the
+  // launch latency overlaps the previous kernel's last wave
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = d == 64 ? cudaLaunchKernelEx(&cfg, merge_shards_kernel<64>, m, l, o, out, lse, rows, P)
+                          : cudaLaunchKernelEx(&cfg, merge_shards_kernel<128>, m, l, o, out, lse, rows, P);
+  if (e != cudaSuccess) return (int)e;
   return (int)cudaGetLastError();
 }
 
