@@ -104,8 +104,9 @@ typedef enum {
    *   shared memory); only the slots of shards with no work at that step
    *   (skipped causal blocks) are copied on a side stream.
    * 1: device-to-device copies of the whole buffer on a side stream.
-   * 0: no movement; every step reads its block straight from the packed
-   *   buffer (for measuring the cost of the other two).
+   * 0: no movement; every step reads its block in place (from k and v for
+   *   the contiguous and striped layouts, from the packed buffer for
+   *   zigzag), for measuring the cost of the other two.
    * All three give bit-identical results. */
   RING_OPT_ROTATION = 0,
   /* 1: record CUDA events around every pack, copy and step kernel of
@@ -146,7 +147,8 @@ typedef enum {
    * 1: one launch for the whole ring ("lap"): a CTA owning a pair of query
    *   tiles of shard r meets blocks r, r-1, .. in step order, the state held
    *   on chip from the first step to the last, and the blocks read in place
-   *   from the packed buffer (no rotation; RING_OPT_ROTATION is ignored).
+   *   in place (from k and v, or the packed buffer for zigzag; no rotation;
+   *   RING_OPT_ROTATION is ignored).
    *   Same arithmetic per key tile; the result matches mode 0 within the
    *   parity tolerances, not bit for bit (mode 0 visits the key tiles of a
    *   block without a diagonal in a rotated order, and stores m between
@@ -271,10 +273,13 @@ RINGATTN_API int ring_attn_finalize(ring_attn_t h, int r, ring_state_t s, float*
  *   out       natural order [B][H][N][d] fp32
  *   lse       natural order [B][H][N]   fp32
  *   workspace ring_attn_workspace_size() bytes, 256-byte aligned
- * K/V are packed shard-major into buffer A; step s runs one kernel over every
- * shard's block (r - s) mod P, reading slot r of the current buffer, and
- * moves every block to slot r+1 of the other buffer for step s+1 as set by
- * RING_OPT_ROTATION.  The running state stays in the workspace; the last step
+ * Step s runs one kernel over every shard's block (r - s) mod P, reading
+ * slot r of the current buffer, and moves every block to slot r+1 of the
+ * other buffer for step s+1 as set by RING_OPT_ROTATION.  Step 0 reads the
+ * blocks in place from k and v (contiguous and striped layouts; key k of
+ * block j is token j n + k or k P + j); the zigzag layout, the side-stream
+ * rotation and a step 0 with an idle shard first pack K/V shard-major into
+ * buffer A instead.  The running state stays in the workspace; the last step
  * writes the normalised output and lse.  Returns after enqueueing; `stream`
  * orders it with the caller's work. */
 RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
@@ -402,7 +407,8 @@ RINGATTN_API int ring_attn_set_option(ring_attn_t h, int option, long long value
  * array has P entries (NULL to skip): step kernel time, rotation copy time
  * for the copy that feeds step s (0 for s = 0), and the time the compute
  * stream waited for that copy (exposed copy time).  pack_ms: the packing
- * kernel.  Synchronises on the recorded events. */
+ * kernel (0 when step 0 reads the blocks in place).  Synchronises on the
+ * recorded events. */
 RINGATTN_API int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float* wait_ms, float* pack_ms);
 
 /* The other side of the overlap check of the last timed ring_attn_fwd

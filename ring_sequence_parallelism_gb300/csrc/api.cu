@@ -620,10 +620,30 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     if ((rc = encode_map(&km[x], kbuf[x], dims, str, kTileN, 1))) return rc;
     if ((rc = encode_map(&vm[x], vbuf[x], dims, str, kTileN, 1))) return rc;
   }
+  // Blocks read in place from the caller's natural-order K/V, with the same
+  // coordinates as the packed buffer (d column, row k of block j, head, j):
+  // key k of block j is token j n + k (contiguous) or k P + j (striped).
+  // Step 0 reads block r there and its kernels send it on to buffer B, the
+  // direct schedule (rotation 0) and the lap read every block there, so the
+  // packing pass into buffer A is not needed.  Zigzag blocks are two chunks
+  // (not one strided map), and the side-stream rotation (mode 1) copies
+  // buffer A's slots, so those keep the packing; so does a step 0 with an
+  // idle shard (its slot would be copied from buffer A).
+  const bool in_place = p.layout != RING_LAYOUT_ZIGZAG && mode != 1 && (int)p.active[0].size() == P;
+  CUtensorMap kn_map, vn_map;
+  if (in_place) {
+    const bool striped = p.layout == RING_LAYOUT_STRIPED;
+    const cuuint64_t Nn = (cuuint64_t)p.N;
+    cuuint64_t dims[4] = {d, n, (cuuint64_t)BHkv, (cuuint64_t)P};
+    cuuint64_t str[3] = {striped ? row_b * P : row_b, row_b * Nn, striped ? row_b : row_b * n};
+    if ((rc = encode_map(&kn_map, k, dims, str, kTileN, 1))) return rc;
+    if ((rc = encode_map(&vn_map, v, dims, str, kTileN, 1))) return rc;
+  }
 
   const bool timing = h->timing != 0;
   if (timing) RA_CUDA(cudaEventRecord(h->tp0, cs), "cudaEventRecord");
-  RA_CUDA((cudaError_t)launch_pack_kv(k, v, kbuf[0], vbuf[0], BHkv, p.n, p.d, P, p.layout, cs), "pack launch");
+  if (!in_place)
+    RA_CUDA((cudaError_t)launch_pack_kv(k, v, kbuf[0], vbuf[0], BHkv, p.n, p.d, P, p.layout, cs), "pack launch");
   if (timing) RA_CUDA(cudaEventRecord(h->tp1, cs), "cudaEventRecord");
   if (rotate) RA_CUDA(cudaEventRecord(h->packed, cs), "cudaEventRecord");
 
@@ -649,7 +669,8 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     a.finalize = 1;
     a.n_active = P;
     if (timing) RA_CUDA(cudaEventRecord(h->tk0[0], cs), "cudaEventRecord");
-    RA_CUDA((cudaError_t)launch_fwd_lap(a, &qm, &km[0], &vm[0], p.d, cs), "lap kernel launch");
+    RA_CUDA((cudaError_t)launch_fwd_lap(a, &qm, in_place ? &kn_map : &km[0], in_place ? &vn_map : &vm[0], p.d, cs),
+            "lap kernel launch");
     if (timing) {
       for (int s = 0; s < P; ++s) {
         if (s > 0) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
@@ -688,8 +709,10 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     for (size_t x = 0; x < act.size(); ++x) a.active[x] = act[x];
     const int grid = block_partial_grid(p.T, a.n_active, BH);
     if (timing) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
-    RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km[cur], &vm[cur], p.d, grid, cs, &km[cur ^ 1],
-                                              &vm[cur ^ 1]),
+    // step 0 (and every step without rotation) reads the blocks in place
+    const bool nat = in_place && (s == 0 || !rotate);
+    RA_CUDA((cudaError_t)launch_block_partial(a, &qm, nat ? &kn_map : &km[cur], nat ? &vn_map : &vm[cur], p.d,
+                                              grid, cs, &km[cur ^ 1], &vm[cur ^ 1]),
             "step kernel launch");
     if (timing) RA_CUDA(cudaEventRecord(h->tk1[s], cs), "cudaEventRecord");
     if (rotate) RA_CUDA(cudaEventRecord(h->released[s], cs), "cudaEventRecord");
