@@ -646,8 +646,8 @@ def run_ours(args, w):
                                  "with no work in a step",
                      "rotation_bytes_per_step": 2 * w.B * w.H * w.N * w.d * 2},
             "clocks": clocks.summary(),
-            # the packing pass runs only for zigzag (the other layouts read step 0's blocks in place)
-            "gpu_launches": args.steps * ((1 if args.fwd_lap else w.P) + (1 if w.layout == "zigzag" else 0)),
+            # pack + P step kernels; the lap reads its blocks in place (packs only for zigzag)
+            "gpu_launches": args.steps * ((1 + (1 if w.layout == "zigzag" else 0)) if args.fwd_lap else 1 + w.P),
             "e2e": e2e,
             "cpu_baseline": cpu,
         }

@@ -104,9 +104,8 @@ typedef enum {
    *   shared memory); only the slots of shards with no work at that step
    *   (skipped causal blocks) are copied on a side stream.
    * 1: device-to-device copies of the whole buffer on a side stream.
-   * 0: no movement; every step reads its block in place (from k and v for
-   *   the contiguous and striped layouts, from the packed buffer for
-   *   zigzag), for measuring the cost of the other two.
+   * 0: no movement; every step reads its block straight from the packed
+   *   buffer (for measuring the cost of the other two).
    * All three give bit-identical results. */
   RING_OPT_ROTATION = 0,
   /* 1: record CUDA events around every pack, copy and step kernel of
@@ -273,13 +272,11 @@ RINGATTN_API int ring_attn_finalize(ring_attn_t h, int r, ring_state_t s, float*
  *   out       natural order [B][H][N][d] fp32
  *   lse       natural order [B][H][N]   fp32
  *   workspace ring_attn_workspace_size() bytes, 256-byte aligned
- * Step s runs one kernel over every shard's block (r - s) mod P, reading
- * slot r of the current buffer, and moves every block to slot r+1 of the
- * other buffer for step s+1 as set by RING_OPT_ROTATION.  Step 0 reads the
- * blocks in place from k and v (contiguous and striped layouts; key k of
- * block j is token j n + k or k P + j); the zigzag layout, the side-stream
- * rotation and a step 0 with an idle shard first pack K/V shard-major into
- * buffer A instead.  The running state stays in the workspace; the last step
+ * K/V are packed shard-major into buffer A; step s runs one kernel over every
+ * shard's block (r - s) mod P, reading slot r of the current buffer, and
+ * moves every block to slot r+1 of the other buffer for step s+1 as set by
+ * RING_OPT_ROTATION.  (The lap, RING_OPT_FWD_LAP, reads the blocks in place
+ * from k and v instead, except in the zigzag layout.)  The running state stays in the workspace; the last step
  * writes the normalised output and lse.  Returns after enqueueing; `stream`
  * orders it with the caller's work. */
 RINGATTN_API int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, float* out, float* lse,
@@ -407,7 +404,7 @@ RINGATTN_API int ring_attn_set_option(ring_attn_t h, int option, long long value
  * array has P entries (NULL to skip): step kernel time, rotation copy time
  * for the copy that feeds step s (0 for s = 0), and the time the compute
  * stream waited for that copy (exposed copy time).  pack_ms: the packing
- * kernel (0 when step 0 reads the blocks in place).  Synchronises on the
+ * kernel (0 for a lap that reads the blocks in place).  Synchronises on the
  * recorded events. */
 RINGATTN_API int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float* wait_ms, float* pack_ms);
 

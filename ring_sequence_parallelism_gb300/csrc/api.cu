@@ -620,16 +620,14 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     if ((rc = encode_map(&km[x], kbuf[x], dims, str, kTileN, 1))) return rc;
     if ((rc = encode_map(&vm[x], vbuf[x], dims, str, kTileN, 1))) return rc;
   }
-  // Blocks read in place from the caller's natural-order K/V, with the same
-  // coordinates as the packed buffer (d column, row k of block j, head, j):
-  // key k of block j is token j n + k (contiguous) or k P + j (striped).
-  // Step 0 reads block r there and its kernels send it on to buffer B, the
-  // direct schedule (rotation 0) and the lap read every block there, so the
-  // packing pass into buffer A is not needed.  Zigzag blocks are two chunks
-  // (not one strided map), and the side-stream rotation (mode 1) copies
-  // buffer A's slots, so those keep the packing; so does a step 0 with an
-  // idle shard (its slot would be copied from buffer A).
-  const bool in_place = p.layout != RING_LAYOUT_ZIGZAG && mode != 1 && (int)p.active[0].size() == P;
+  // The lap (no rotation) reads the blocks in place from the caller's
+  // natural-order K/V, with the same coordinates as the packed buffer
+  // (d column, row k of block j, head, j): key k of block j is token j n + k
+  // (contiguous) or k P + j (striped), so it needs no packing pass.  The
+  // step schedule packs the blocks into rotation buffer A, from which the
+  // ring moves them; zigzag blocks are two chunks (not one strided map), so
+  // the lap packs them too.
+  const bool in_place = h->fwd_lap && p.layout != RING_LAYOUT_ZIGZAG;
   CUtensorMap kn_map, vn_map;
   if (in_place) {
     const bool striped = p.layout == RING_LAYOUT_STRIPED;
@@ -709,10 +707,8 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     for (size_t x = 0; x < act.size(); ++x) a.active[x] = act[x];
     const int grid = block_partial_grid(p.T, a.n_active, BH);
     if (timing) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
-    // step 0 (and every step without rotation) reads the blocks in place
-    const bool nat = in_place && (s == 0 || !rotate);
-    RA_CUDA((cudaError_t)launch_block_partial(a, &qm, nat ? &kn_map : &km[cur], nat ? &vn_map : &vm[cur], p.d,
-                                              grid, cs, &km[cur ^ 1], &vm[cur ^ 1]),
+    RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km[cur], &vm[cur], p.d, grid, cs, &km[cur ^ 1],
+                                              &vm[cur ^ 1]),
             "step kernel launch");
     if (timing) RA_CUDA(cudaEventRecord(h->tk1[s], cs), "cudaEventRecord");
     if (rotate) RA_CUDA(cudaEventRecord(h->released[s], cs), "cudaEventRecord");
