@@ -127,6 +127,27 @@ def traffic_for(key: str, source=KERNEL_SOURCE):
 
 
 # ------------------------------------------------------------- clocks
+def host_link_rates(torch, mib=256, reps=3):
+    """Pinned host-to-device and device-to-host copy rates (GB/s, median of
+    `reps` copies of `mib` MiB), to read the end-to-end figure against."""
+    n = mib << 20
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(n, dtype=torch.uint8, device="cuda")
+    rates = {}
+    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)), ("d2h", lambda: h.copy_(d, non_blocking=True))):
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        rates[name] = round(n / sorted(ts)[len(ts) // 2] / 1e6, 1)
+    del h, d
+    return rates
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -588,6 +609,7 @@ def run_ours(args, w):
     if not args.no_e2e:
         out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        link = host_link_rates(torch)
         att.set_option(ra.RING_OPT_TIMING, 0)
         att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
         barrier()
@@ -604,7 +626,10 @@ def run_ours(args, w):
                "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h)),
                "d2h_bytes_per_step": out_h.numel() * 4 + lse_h.numel() * 4,
-               "clocks": e2e_clocks.summary()}
+               "clocks": e2e_clocks.summary(),
+               # pinned copy rates measured just before this leg (the host link is shared
+               # with the machine's other jobs and varies between runs)
+               "host_link_gbs": link}
 
     extra = {}
     if world == 1 and not args.no_extra:
