@@ -614,10 +614,13 @@ def run_ours(args, w):
         att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
         barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cpu_ms = []
         with ClockSampler(torch.cuda.current_device()) as e2e_clocks:
             f0.record(stream)
             for _ in range(args.steps):
+                c0 = time.perf_counter()
                 att.fwd_host(q_h, k_h, v_h, out_h, lse_h)
+                cpu_ms.append((time.perf_counter() - c0) * 1e3)
             f1.record(stream)
             barrier()
             torch.cuda.synchronize()
@@ -629,7 +632,10 @@ def run_ours(args, w):
                "clocks": e2e_clocks.summary(),
                # pinned copy rates measured just before this leg (the host link is shared
                # with the machine's other jobs and varies between runs)
-               "host_link_gbs": link}
+               "host_link_gbs": link,
+               # host time to enqueue one call (all its copies, events and launches): the first
+               # call of the loop (queues empty) and the median
+               "enqueue_ms": {"first": round(cpu_ms[0], 3), "median": round(sorted(cpu_ms)[len(cpu_ms) // 2], 3)}}
 
     extra = {}
     if world == 1 and not args.no_extra:
