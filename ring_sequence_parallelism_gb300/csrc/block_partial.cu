@@ -113,20 +113,26 @@ struct Layout {
   __device__ static constexpr uint32_t tmem_o(int t) { return t == 0 ? 256u : 256u + D; }
 };
 
-// blockIdx.x -> (shard, head, tile pair).  CTAs of one (shard, head) group
-// are consecutive so the K/V block they share stays in L2; within a group
-// the heaviest pairs (largest u under the causal mask) start first.
+// Grid (2^head_lg * U * ksplit, head groups, shards) -> (shard, head, tile
+// pair, key piece).  blockIdx.x runs over the 2^head_lg heads of a group
+// fastest, then the tile pairs from the heaviest (largest u under the causal
+// mask) down, then the key pieces; y is the head group, z the shard's slot
+// in the step's list.  The CTAs of one group of heads of one shard are
+// consecutive, so the K/V blocks they read stay in L2, and the launch order
+// puts the heaviest pairs of every group first: the last wave of the launch
+// holds light pairs, which shortens its tail.  No division on the way
+// without key pieces.
 template <bool kWin>
 __device__ __forceinline__ WorkItem decode_item(const StepArgs& a) {
   WorkItem w;
   const int U = (a.T + 1) / 2;
-  const int item = blockIdx.x;
-  const int u = U - 1 - item % U;
-  const int piece = (item / U) % a.ksplit;
-  const int g = item / U / a.ksplit;
-  w.bh = g % a.BH;
-  w.kvh = w.bh / a.G;
-  const int slot_in_list = a.fixed_r >= 0 ? 0 : g / a.BH;
+  const int x = blockIdx.x;
+  const int xi = x >> a.head_lg;
+  const int u = U - 1 - (a.ksplit == 1 ? xi : xi % U);
+  const int piece = a.ksplit == 1 ? 0 : xi / U;
+  w.bh = a.bh0 + ((int)blockIdx.y << a.head_lg) + (x & ((1 << a.head_lg) - 1));
+  w.kvh = a.G == 1 ? w.bh : w.bh / a.G;
+  const int slot_in_list = a.fixed_r >= 0 ? 0 : (int)blockIdx.z;
   w.r = a.fixed_r >= 0 ? a.fixed_r : (int)a.active[slot_in_list];
   int j = (w.r - a.step) % a.P;
   if (j < 0) j += a.P;
@@ -404,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_store_4d(&v_next, sbase + L::kOffV + st * L::kVBytes + c * (kTileN * 128), c * L::kSub, key0, w.kvh,
                          dst);
         }
-        // the stores have read shared memory and written HBM before exit
-        bulk_commit_and_wait_all();
+        // the stores have read shared memory before exit
+        bulk_commit_and_wait_read();
       }
       // Drain: every load this thread started has landed before the CTA
       // can exit (normally these waits return at once).
@@ -660,6 +666,15 @@ int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map
                          int grid, void* stream, const void* k_next_map, const void* v_next_map) {
   if (grid <= 0) return 0;
   if (a.forward && (!k_next_map || !v_next_map)) return (int)cudaErrorInvalidValue;
+  const int U = (a.T + 1) / 2;
+  const int per_slot = U * a.ksplit * a.BH;
+  if (grid % per_slot != 0) return (int)cudaErrorInvalidValue;
+  const int slots = grid / per_slot;
+  StepArgs b = a;
+  // four heads (two, one) interleave; with key pieces (short queries) one
+  b.head_lg = a.ksplit > 1 ? 0 : (a.BH % 4 == 0 ? 2 : (a.BH % 2 == 0 ? 1 : 0));
+  const int hg = 1 << b.head_lg;
+  const int max_groups = 65535;  // grid y limit
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const CUtensorMap& qm = *static_cast<const CUtensorMap*>(q_map);
   const CUtensorMap& km = *static_cast<const CUtensorMap*>(k_map);
@@ -669,14 +684,21 @@ int launch_block_partial(const StepArgs& a, const void* q_map, const void* k_map
   const CUtensorMap& vn = *static_cast<const CUtensorMap*>(v_next_map ? v_next_map : v_map);
   // row-dependent bounds: a window or documents
   const bool win = (a.causal && a.window > 0) || a.seg_lo != nullptr;
-  if (d == 64) {
-    if (win) block_partial_kernel<64, true><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
-    else block_partial_kernel<64, false><<<grid, kThreads, Layout<64>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
-  } else {
-    if (win) block_partial_kernel<128, true><<<grid, kThreads, Layout<128>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
-    else block_partial_kernel<128, false><<<grid, kThreads, Layout<128>::kAlloc, s>>>(a, qm, km, vm, kn, vn);
+  for (int h0 = 0; h0 < a.BH; h0 += max_groups * hg) {
+    b.bh0 = h0;
+    const int groups = (a.BH - h0) / hg < max_groups ? (a.BH - h0) / hg : max_groups;
+    const dim3 g3((unsigned)(hg * U * a.ksplit), (unsigned)groups, (unsigned)slots);
+    if (d == 64) {
+      if (win) block_partial_kernel<64, true><<<g3, kThreads, Layout<64>::kAlloc, s>>>(b, qm, km, vm, kn, vn);
+      else block_partial_kernel<64, false><<<g3, kThreads, Layout<64>::kAlloc, s>>>(b, qm, km, vm, kn, vn);
+    } else {
+      if (win) block_partial_kernel<128, true><<<g3, kThreads, Layout<128>::kAlloc, s>>>(b, qm, km, vm, kn, vn);
+      else block_partial_kernel<128, false><<<g3, kThreads, Layout<128>::kAlloc, s>>>(b, qm, km, vm, kn, vn);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
   }
-  return (int)cudaGetLastError();
+  return 0;
 }
 
 }  // namespace ringattn

@@ -119,6 +119,8 @@ struct StepArgs {
   long long decode_pos0;  // >= 0: short queries at global positions pos0 + i against the keys of
                           //       the natural-order cache, read as one contiguous block (P = 1, key k
                           //       at position k; see ring_attn_decode)
+  int bh0;                // first query head of this launch (launches cover at most 65535 head groups)
+  int head_lg;            // log2 of the heads whose CTAs interleave (set by the launch)
   int ksplit;             // >= 1: pieces the block's key tiles are cut into (short queries only); piece p
                           //       keeps its state in slot p
   float scale_log2;  // log2(e) / sqrt(d)

@@ -141,9 +141,11 @@ __device__ __forceinline__ void tma_store_4d(const void* map, uint32_t src, int 
       "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
-__device__ __forceinline__ void bulk_commit_and_wait_all() {
+// Waits until every bulk store this thread issued has read its shared-memory
+// source (the writes themselves are complete when the grid is).
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
