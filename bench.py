@@ -424,6 +424,8 @@ def measure_side_stream_rotation(att, q, k, v, out, lse, w, warmup=3, steps=3):
     try:
         for _ in range(warmup):
             att.fwd(q, k, v, out, lse)
+        if warmup:
+            att.timing()  # the timed calls below start a new record
         stream = torch.cuda.current_stream()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -569,6 +571,8 @@ def run_ours(args, w):
     for _ in range(args.warmup):
         att.fwd(q, k, v, out, lse)
     att.check()
+    if args.warmup:
+        att.timing()  # a read: the record of the timed region starts with its first forward
 
     def barrier():
         if world > 1:
@@ -585,7 +589,7 @@ def run_ours(args, w):
             att.fwd(q, k, v, out, lse)
         e1.record(stream)
         barrier()
-    t = att.timing()  # events of the last forward in the timed region (launch stream)
+    t = att.timing()  # per-launch means over every forward of the timed region (launch stream)
     kernel_ms, copy_ms, wait_ms, pack_ms = t["kernel_ms"], t["copy_ms"], t["wait_ms"], t["pack_ms"]
     att.check()
     ms = e0.elapsed_time(e1) / args.steps

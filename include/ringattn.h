@@ -109,7 +109,8 @@ typedef enum {
    * All three give bit-identical results. */
   RING_OPT_ROTATION = 0,
   /* 1: record CUDA events around every pack, copy and step kernel of
-   * ring_attn_fwd so ring_attn_get_timing can report them.  Default 0. */
+   * ring_attn_fwd so ring_attn_get_timing can report them, one set of
+   * events per call (the handle keeps up to 64).  Default 0. */
   RING_OPT_TIMING = 1,
   /* Upper bound, in nanoseconds, of every device-side wait.  Default 2e9. */
   RING_OPT_WAIT_LIMIT_NS = 2,
@@ -146,7 +147,7 @@ typedef enum {
    * 1: one launch for the whole ring ("lap"): a CTA owning a pair of query
    *   tiles of shard r meets blocks r, r-1, .. in step order, the state held
    *   on chip from the first step to the last, and the blocks read in place
-   *   in place (from k and v, or the packed buffer for zigzag; no rotation;
+   *   (from k and v, or the packed buffer for zigzag; no rotation;
    *   RING_OPT_ROTATION is ignored).
    *   Same arithmetic per key tile; the result matches mode 0 within the
    *   parity tolerances, not bit for bit (mode 0 visits the key tiles of a
@@ -400,21 +401,26 @@ RINGATTN_API int ring_attn_set_segments(ring_attn_t h, const long long* bounds, 
 /* Set an option (see ring_option_t). */
 RINGATTN_API int ring_attn_set_option(ring_attn_t h, int option, long long value);
 
-/* Timings of the last ring_attn_fwd with RING_OPT_TIMING on, in ms; each
- * array has P entries (NULL to skip): step kernel time, rotation copy time
- * for the copy that feeds step s (0 for s = 0), and the time the compute
- * stream waited for that copy (exposed copy time).  pack_ms: the packing
- * kernel (0 for a lap that reads the blocks in place).  Synchronises on the
- * recorded events. */
+/* Timings of the ring_attn_fwd calls made with RING_OPT_TIMING on, in ms,
+ * each the mean over the calls timed since the previous read of the timings
+ * (this function or ring_attn_get_release_wait; the latest 64 calls when
+ * there were more); each array has P entries (NULL to skip): step kernel
+ * time, rotation copy time for the copy that feeds step s (0 for s = 0, and
+ * 0 in calls where no copy fed step s), and the time the compute stream
+ * waited for that copy (exposed copy time).  pack_ms: the packing kernel
+ * (0 for a lap that reads the blocks in place).  Reading does not clear the
+ * record; the next timed call starts a new one.  Synchronises on the
+ * recorded events.  RING_ERR_INVALID_ARG when no timed call was recorded. */
 RINGATTN_API int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float* wait_ms, float* pack_ms);
 
-/* The other side of the overlap check of the last timed ring_attn_fwd
+/* The other side of the overlap check of the timed ring_attn_fwd calls
  * ([RA-CN] "如何判断通信是否真的被覆盖": besides compute waiting for the
  * communication, record how long the communication waits for the buffer to
  * be released): release_wait_ms[s] (P entries, ms) is the time the side
  * stream spent, before the copy that feeds step s, waiting for step s - 2 to
- * release the buffer it fills (0 where no copy fed step s).  Needs
- * RING_OPT_TIMING; synchronises on the recorded events. */
+ * release the buffer it fills (0 where no copy fed step s), the mean over the
+ * same calls as ring_attn_get_timing.  Needs RING_OPT_TIMING; synchronises
+ * on the recorded events. */
 RINGATTN_API int ring_attn_get_release_wait(ring_attn_t h, float* release_wait_ms);
 
 /* Synchronise `stream` and report any device-side error recorded by this

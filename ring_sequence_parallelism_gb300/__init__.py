@@ -306,6 +306,8 @@ class RingAttention:
         return out, lse
 
     def timing(self):
+        """Per-step means over the forwards timed since the previous read
+        (RING_OPT_TIMING); reading does not clear them."""
         P = self.P
         k, c, w = (ctypes.c_float * P)(), (ctypes.c_float * P)(), (ctypes.c_float * P)()
         pk = ctypes.c_float()

@@ -135,6 +135,19 @@ struct HostPipe {
   bool have_done = false;  // ev_done recorded by an earlier call
 };
 
+// Events of one timed ring_attn_fwd (RING_OPT_TIMING).
+struct FwdTiming {
+  std::vector<cudaEvent_t> k0, k1;  // [s]: around the step kernel (lap: the launch, entry 0)
+  std::vector<cudaEvent_t> c0, c1;  // [s]: around the side-stream copy that feeds step s
+  std::vector<cudaEvent_t> w0, w1;  // [s]: around the compute stream's wait for that copy
+  std::vector<cudaEvent_t> r0;      // [s]: side stream, before its wait for the buffer (then c0)
+  cudaEvent_t p0 = nullptr, p1 = nullptr;  // around the pack
+  std::vector<char> copied;         // [s]: a copy fed step s
+};
+// The timing getters average over the timed forwards since the previous
+// read, the latest kTimedCalls of them.
+constexpr int kTimedCalls = 64;
+
 struct ring_attn {
   Plan plan;
   int rotation = 2;
@@ -149,15 +162,15 @@ struct ring_attn {
   cudaStream_t side = nullptr;
   cudaEvent_t packed = nullptr;
   std::vector<cudaEvent_t> landed, released;
-  std::vector<cudaEvent_t> tk0, tk1, tc0, tc1, tw0, tw1;
-  std::vector<cudaEvent_t> tr0;  // side stream, before its wait for released[s-1] (then tc0)
+  std::vector<FwdTiming> tsets;  // event sets of timed forwards, used in turn
+  int t_next = 0;                // set of the next timed forward
+  int t_count = 0;               // timed forwards recorded (at most kTimedCalls)
+  bool t_read = false;           // a getter has read them: the next timed forward starts anew
   std::vector<cudaEvent_t> tbk0, tbk1, tbq0, tbq1;  // backward: dK/dV and dQ kernels per step
   cudaEvent_t tbp0 = nullptr, tbp1 = nullptr;          // backward preprocessing
   bool bwd_timed_valid = false;
   bool bwd_timed_lap = false;  // the timed backward ran in lap mode (one launch each)
-  std::vector<char> copied;  // [s]: the side stream filled slots for step s (timing)
-  cudaEvent_t tp0 = nullptr, tp1 = nullptr;
-  bool timed_valid = false;
+  std::vector<char> copied;  // [s]: the side stream filled slots for step s (this forward)
   int* d_err = nullptr;  // [0] flags, [1] first failing site
   int* d_seg = nullptr;  // segments: first / one-past-last position of each position's document, [2][N]
   long long d_seg_n = 0;
@@ -194,6 +207,33 @@ int make_events(std::vector<cudaEvent_t>& v, int n, unsigned flags) {
   return RING_OK;
 }
 
+// The event set for the next timed forward (made on first use).
+int begin_timed_call(ring_attn* h, FwdTiming** out) {
+  if (h->t_read) {
+    h->t_count = 0;
+    h->t_next = 0;
+    h->t_read = false;
+  }
+  if ((int)h->tsets.size() <= h->t_next) {
+    h->tsets.emplace_back();
+    FwdTiming& T = h->tsets.back();
+    const int P = h->plan.P;
+    int rc;
+    for (auto* v : {&T.k0, &T.k1, &T.c0, &T.c1, &T.w0, &T.w1, &T.r0})
+      if ((rc = make_events(*v, P, cudaEventDefault))) return rc;
+    RA_CUDA(cudaEventCreate(&T.p0), "cudaEventCreate");
+    RA_CUDA(cudaEventCreate(&T.p1), "cudaEventCreate");
+  }
+  *out = &h->tsets[h->t_next];
+  return RING_OK;
+}
+
+void end_timed_call(ring_attn* h) {
+  h->tsets[h->t_next].copied = h->copied;
+  h->t_next = (h->t_next + 1) % kTimedCalls;
+  if (h->t_count < kTimedCalls) ++h->t_count;
+}
+
 int ensure_device(ring_attn* h) {
   int dev = -1;
   RA_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
@@ -219,11 +259,8 @@ int ensure_device(ring_attn* h) {
   RA_CUDA(cudaEventCreateWithFlags(&h->packed, cudaEventDisableTiming), "cudaEventCreate");
   if ((rc = make_events(h->landed, P, cudaEventDisableTiming))) return rc;
   if ((rc = make_events(h->released, P, cudaEventDisableTiming))) return rc;
-  for (auto* v : {&h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1, &h->tr0, &h->tbk0, &h->tbk1, &h->tbq0,
-                  &h->tbq1})
+  for (auto* v : {&h->tbk0, &h->tbk1, &h->tbq0, &h->tbq1})
     if ((rc = make_events(*v, P, cudaEventDefault))) return rc;
-  RA_CUDA(cudaEventCreate(&h->tp0), "cudaEventCreate");
-  RA_CUDA(cudaEventCreate(&h->tp1), "cudaEventCreate");
   RA_CUDA(cudaEventCreate(&h->tbp0), "cudaEventCreate");
   RA_CUDA(cudaEventCreate(&h->tbp1), "cudaEventCreate");
   RA_CUDA(cudaMalloc(&h->d_err, 2 * sizeof(int)), "cudaMalloc(error word)");
@@ -341,15 +378,19 @@ int ring_attn_destroy(ring_attn_t h) {
     int prev = -1;
     cudaGetDevice(&prev);
     if (prev != h->device) cudaSetDevice(h->device);
-    for (auto* v : {&h->landed, &h->released, &h->tk0, &h->tk1, &h->tc0, &h->tc1, &h->tw0, &h->tw1, &h->tbk0,
-                    &h->tbk1, &h->tbq0, &h->tbq1})
+    for (auto* v : {&h->landed, &h->released, &h->tbk0, &h->tbk1, &h->tbq0, &h->tbq1})
       for (auto e : *v)
         if (e) cudaEventDestroy(e);
+    for (FwdTiming& T : h->tsets) {
+      for (auto* v : {&T.k0, &T.k1, &T.c0, &T.c1, &T.w0, &T.w1, &T.r0})
+        for (auto e : *v)
+          if (e) cudaEventDestroy(e);
+      for (cudaEvent_t e : {T.p0, T.p1})
+        if (e) cudaEventDestroy(e);
+    }
     if (h->tbp0) cudaEventDestroy(h->tbp0);
     if (h->tbp1) cudaEventDestroy(h->tbp1);
     if (h->packed) cudaEventDestroy(h->packed);
-    if (h->tp0) cudaEventDestroy(h->tp0);
-    if (h->tp1) cudaEventDestroy(h->tp1);
     if (h->side) cudaStreamDestroy(h->side);
     if (h->d_err) cudaFree(h->d_err);
     if (h->d_seg) cudaFree(h->d_seg);
@@ -639,10 +680,12 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
   }
 
   const bool timing = h->timing != 0;
-  if (timing) RA_CUDA(cudaEventRecord(h->tp0, cs), "cudaEventRecord");
+  FwdTiming* T = nullptr;
+  if (timing && (rc = begin_timed_call(h, &T))) return rc;
+  if (timing) RA_CUDA(cudaEventRecord(T->p0, cs), "cudaEventRecord");
   if (!in_place)
     RA_CUDA((cudaError_t)launch_pack_kv(k, v, kbuf[0], vbuf[0], BHkv, p.n, p.d, P, p.layout, cs), "pack launch");
-  if (timing) RA_CUDA(cudaEventRecord(h->tp1, cs), "cudaEventRecord");
+  if (timing) RA_CUDA(cudaEventRecord(T->p1, cs), "cudaEventRecord");
   if (rotate) RA_CUDA(cudaEventRecord(h->packed, cs), "cudaEventRecord");
 
   const size_t slot_bytes = (size_t)BHkv * (size_t)p.n * p.d * 2;
@@ -666,16 +709,16 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     a.kv_mode = kKvSlotJ;
     a.finalize = 1;
     a.n_active = P;
-    if (timing) RA_CUDA(cudaEventRecord(h->tk0[0], cs), "cudaEventRecord");
+    if (timing) RA_CUDA(cudaEventRecord(T->k0[0], cs), "cudaEventRecord");
     RA_CUDA((cudaError_t)launch_fwd_lap(a, &qm, in_place ? &kn_map : &km[0], in_place ? &vn_map : &vm[0], p.d, cs),
             "lap kernel launch");
     if (timing) {
       for (int s = 0; s < P; ++s) {
-        if (s > 0) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
-        RA_CUDA(cudaEventRecord(h->tk1[s], cs), "cudaEventRecord");
+        if (s > 0) RA_CUDA(cudaEventRecord(T->k0[s], cs), "cudaEventRecord");
+        RA_CUDA(cudaEventRecord(T->k1[s], cs), "cudaEventRecord");
       }
+      end_timed_call(h);
     }
-    h->timed_valid = timing;
     return RING_OK;
   }
 
@@ -694,9 +737,9 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
   for (int s = 0; s < P; ++s) {
     const int cur = rotate ? (s & 1) : 0;
     if (rotate && s >= 1 && h->copied[s]) {
-      if (timing) RA_CUDA(cudaEventRecord(h->tw0[s], cs), "cudaEventRecord");
+      if (timing) RA_CUDA(cudaEventRecord(T->w0[s], cs), "cudaEventRecord");
       RA_CUDA(cudaStreamWaitEvent(cs, h->landed[s], 0), "cudaStreamWaitEvent");
-      if (timing) RA_CUDA(cudaEventRecord(h->tw1[s], cs), "cudaEventRecord");
+      if (timing) RA_CUDA(cudaEventRecord(T->w1[s], cs), "cudaEventRecord");
     }
     const auto& act = p.active[s];
     a.step = s;
@@ -706,11 +749,11 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     a.n_active = (int)act.size();
     for (size_t x = 0; x < act.size(); ++x) a.active[x] = act[x];
     const int grid = block_partial_grid(p.T, a.n_active, BH);
-    if (timing) RA_CUDA(cudaEventRecord(h->tk0[s], cs), "cudaEventRecord");
+    if (timing) RA_CUDA(cudaEventRecord(T->k0[s], cs), "cudaEventRecord");
     RA_CUDA((cudaError_t)launch_block_partial(a, &qm, &km[cur], &vm[cur], p.d, grid, cs, &km[cur ^ 1],
                                               &vm[cur ^ 1]),
             "step kernel launch");
-    if (timing) RA_CUDA(cudaEventRecord(h->tk1[s], cs), "cudaEventRecord");
+    if (timing) RA_CUDA(cudaEventRecord(T->k1[s], cs), "cudaEventRecord");
     if (rotate) RA_CUDA(cudaEventRecord(h->released[s], cs), "cudaEventRecord");
     if (!rotate || s + 1 >= P) continue;
     // slots the side stream moves for step s+1: all of them (mode 1), or
@@ -725,9 +768,9 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
     for (int r = 0; r < P; ++r) any = any || send[r];
     if (!any) continue;
     // fill the other buffer once step s-1 has released it (and written it)
-    if (timing) RA_CUDA(cudaEventRecord(h->tr0[s + 1], h->side), "cudaEventRecord");
+    if (timing) RA_CUDA(cudaEventRecord(T->r0[s + 1], h->side), "cudaEventRecord");
     RA_CUDA(cudaStreamWaitEvent(h->side, s == 0 ? h->packed : h->released[s - 1], 0), "cudaStreamWaitEvent");
-    if (timing) RA_CUDA(cudaEventRecord(h->tc0[s + 1], h->side), "cudaEventRecord");
+    if (timing) RA_CUDA(cudaEventRecord(T->c0[s + 1], h->side), "cudaEventRecord");
     // runs of consecutive slots r0..r1 (r1 < P-1) go to r0+1..r1+1; slot P-1 goes to 0
     for (int r = 0; r < P - 1;) {
       if (!send[r]) { ++r; continue; }
@@ -737,11 +780,11 @@ int ring_attn_fwd(ring_attn_t h, const void* q, const void* k, const void* v, fl
       r = r1 + 1;
     }
     if (send[P - 1] && (rc = copy_slots(cur, P - 1, 0, 1))) return rc;
-    if (timing) RA_CUDA(cudaEventRecord(h->tc1[s + 1], h->side), "cudaEventRecord");
+    if (timing) RA_CUDA(cudaEventRecord(T->c1[s + 1], h->side), "cudaEventRecord");
     RA_CUDA(cudaEventRecord(h->landed[s + 1], h->side), "cudaEventRecord");
     h->copied[s + 1] = 1;
   }
-  h->timed_valid = timing;
+  if (timing) end_timed_call(h);
   return RING_OK;
 }
 
@@ -1227,53 +1270,70 @@ int ring_attn_decode(ring_attn_t h, const void* q, const void* k, const void* v,
 
 int ring_attn_get_timing(ring_attn_t h, float* kernel_ms, float* copy_ms, float* wait_ms, float* pack_ms) {
   if (!h) return fail(RING_ERR_INVALID_ARG, "NULL handle");
-  if (!h->timed_valid) return fail(RING_ERR_INVALID_ARG, "no timed ring_attn_fwd recorded (set RING_OPT_TIMING)");
+  const int n = h->t_count;
+  if (n == 0) return fail(RING_ERR_INVALID_ARG, "no timed ring_attn_fwd recorded (set RING_OPT_TIMING)");
   const int P = h->plan.P;
+  // elapsed time between two events of one set, synchronising on the later one
+  auto elapsed = [](cudaEvent_t e0, cudaEvent_t e1, float* ms) -> int {
+    RA_CUDA(cudaEventSynchronize(e1), "cudaEventSynchronize");
+    RA_CUDA(cudaEventElapsedTime(ms, e0, e1), "cudaEventElapsedTime");
+    return RING_OK;
+  };
+  int rc;
   for (int s = 0; s < P; ++s) {
-    const bool copied = s < (int)h->copied.size() && h->copied[s];
-    float ms = 0.f;
-    if (kernel_ms) {
-      RA_CUDA(cudaEventSynchronize(h->tk1[s]), "cudaEventSynchronize");
-      RA_CUDA(cudaEventElapsedTime(&ms, h->tk0[s], h->tk1[s]), "cudaEventElapsedTime");
-      kernel_ms[s] = ms;
-    }
-    if (copy_ms) {
-      ms = 0.f;
-      if (copied) {
-        RA_CUDA(cudaEventSynchronize(h->tc1[s]), "cudaEventSynchronize");
-        RA_CUDA(cudaEventElapsedTime(&ms, h->tc0[s], h->tc1[s]), "cudaEventElapsedTime");
+    double k = 0, c = 0, w = 0;
+    for (int x = 0; x < n; ++x) {
+      const FwdTiming& T = h->tsets[x];
+      const bool copied = s < (int)T.copied.size() && T.copied[s];
+      float ms = 0.f;
+      if (kernel_ms) {
+        if ((rc = elapsed(T.k0[s], T.k1[s], &ms))) return rc;
+        k += ms;
       }
-      copy_ms[s] = ms;
-    }
-    if (wait_ms) {
-      ms = 0.f;
-      if (copied) {
-        RA_CUDA(cudaEventSynchronize(h->tw1[s]), "cudaEventSynchronize");
-        RA_CUDA(cudaEventElapsedTime(&ms, h->tw0[s], h->tw1[s]), "cudaEventElapsedTime");
+      if (copy_ms && copied) {
+        if ((rc = elapsed(T.c0[s], T.c1[s], &ms))) return rc;
+        c += ms;
       }
-      wait_ms[s] = ms;
+      if (wait_ms && copied) {
+        if ((rc = elapsed(T.w0[s], T.w1[s], &ms))) return rc;
+        w += ms;
+      }
     }
+    if (kernel_ms) kernel_ms[s] = (float)(k / n);
+    if (copy_ms) copy_ms[s] = (float)(c / n);
+    if (wait_ms) wait_ms[s] = (float)(w / n);
   }
   if (pack_ms) {
-    float ms = 0.f;
-    RA_CUDA(cudaEventSynchronize(h->tp1), "cudaEventSynchronize");
-    RA_CUDA(cudaEventElapsedTime(&ms, h->tp0, h->tp1), "cudaEventElapsedTime");
-    *pack_ms = ms;
+    double pk = 0;
+    for (int x = 0; x < n; ++x) {
+      float ms = 0.f;
+      if ((rc = elapsed(h->tsets[x].p0, h->tsets[x].p1, &ms))) return rc;
+      pk += ms;
+    }
+    *pack_ms = (float)(pk / n);
   }
+  h->t_read = true;
   return RING_OK;
 }
 
 int ring_attn_get_release_wait(ring_attn_t h, float* release_wait_ms) {
   if (!h || !release_wait_ms) return fail(RING_ERR_INVALID_ARG, "NULL argument");
-  if (!h->timed_valid) return fail(RING_ERR_INVALID_ARG, "no timed ring_attn_fwd recorded (set RING_OPT_TIMING)");
+  const int n = h->t_count;
+  if (n == 0) return fail(RING_ERR_INVALID_ARG, "no timed ring_attn_fwd recorded (set RING_OPT_TIMING)");
   for (int s = 0; s < h->plan.P; ++s) {
-    float ms = 0.f;
-    if (s < (int)h->copied.size() && h->copied[s]) {
-      RA_CUDA(cudaEventSynchronize(h->tc0[s]), "cudaEventSynchronize");
-      RA_CUDA(cudaEventElapsedTime(&ms, h->tr0[s], h->tc0[s]), "cudaEventElapsedTime");
+    double sum = 0;
+    for (int x = 0; x < n; ++x) {
+      const FwdTiming& T = h->tsets[x];
+      if (s < (int)T.copied.size() && T.copied[s]) {
+        float ms = 0.f;
+        RA_CUDA(cudaEventSynchronize(T.c0[s]), "cudaEventSynchronize");
+        RA_CUDA(cudaEventElapsedTime(&ms, T.r0[s], T.c0[s]), "cudaEventElapsedTime");
+        sum += ms;
+      }
     }
-    release_wait_ms[s] = ms;
+    release_wait_ms[s] = (float)(sum / n);
   }
+  h->t_read = true;
   return RING_OK;
 }
 

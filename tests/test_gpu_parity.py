@@ -538,3 +538,35 @@ def test_bad_alignment_is_rejected():
         ra.ring_attn_fwd(att.handle, q, q, q, out, lse, att.workspace())
     assert e.value.status == ra._lib.RING_ERR_INVALID_ARG
     att.close()
+
+
+def test_timing_means_over_calls():
+    """The timings are means over the forwards timed since the previous read:
+    reading does not clear them, and the first timed call after a read starts
+    a new record."""
+    B, H, N, d, P = 1, 2, 8 * 512, 128, 8
+    q, k, v = (x.cuda() for x in make_qkv(B, H, N, d, seed=9))
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout="striped")
+    att.set_option(ra.RING_OPT_TIMING, 1)
+    for _ in range(3):
+        att.fwd(q, k, v)
+    t1 = att.timing()
+    t2 = att.timing()
+    att.check()
+    assert t1 == t2 and all(x > 0 for x in t1["kernel_ms"])
+    # one call with side-stream copies (mode 1), then one with the kernels
+    # sending (striped: every shard has work every step, so no copies): the
+    # first call's copies are in the means
+    att.set_option(ra.RING_OPT_ROTATION, 1)
+    att.fwd(q, k, v)
+    att.set_option(ra.RING_OPT_ROTATION, 2)
+    att.fwd(q, k, v)
+    t3 = att.timing()
+    assert t3["copy_ms"][0] == 0 and all(x > 0 for x in t3["copy_ms"][1:])
+    # after the read, a new record holds the last call alone
+    att.fwd(q, k, v)
+    t4 = att.timing()
+    att.check()
+    assert all(x == 0 for x in t4["copy_ms"]) and all(x == 0 for x in t4["wait_ms"])
+    assert all(x > 0 for x in t4["kernel_ms"]) and t4["pack_ms"] > 0
+    att.close()
