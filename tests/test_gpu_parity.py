@@ -570,3 +570,22 @@ def test_timing_means_over_calls():
     assert all(x == 0 for x in t4["copy_ms"]) and all(x == 0 for x in t4["wait_ms"])
     assert all(x > 0 for x in t4["kernel_ms"]) and t4["pack_ms"] > 0
     att.close()
+
+
+def test_fwd_heads_beyond_one_grid_dimension():
+    """B*H = 65537, an odd count: the step kernel's grid holds at most 65535
+    head groups in y (one head each when B*H is odd), so the launch is split
+    by heads; heads on both sides of the split match the oracle."""
+    B, H, N, d, P = 1, 65537, 128, 64, 1
+    q, k, v = make_qkv(B, H, N, d, seed=21)
+    att = ra.RingAttention(B, H, N, d, P, causal=True, layout="contiguous")
+    out, lse = att.fwd(q.cuda(), k.cuda(), v.cuda())
+    att.check()
+    torch.cuda.synchronize()
+    heads = [0, 65533, 65534, 65535, 65536]
+    got_out = out[0, heads].cpu().double().numpy()
+    got_lse = lse[0, heads].cpu().double().numpy()
+    att.close()
+    ref_out, ref_lse = oracle.default().dense(q[0, heads], k[0, heads], v[0, heads], True)
+    d_out, d_lse = report("65537 heads", got_out, got_lse, ref_out, ref_lse)
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE
