@@ -186,21 +186,39 @@ __global__ void finalize_kernel(const float* __restrict__ m, const float* __rest
 }
 
 // Pack natural-order K and V into the shard-major rotation buffer:
-// buf[r][bh][k][:] = src[bh][pos(r, k)][:]  (blockIdx.y: 0 = K, 1 = V).
-__global__ void pack_kv_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ kb,
-                               uint4* __restrict__ vb, int BH, long long n, int u16, int P, int layout) {
-  const uint4* src = blockIdx.y == 0 ? k : v;
-  uint4* dst = blockIdx.y == 0 ? kb : vb;
+// buf[r][bh][k][:] = src[bh][pos(r, k)][:].  A row is u16 16-byte chunks; a
+// 256-thread block copies kPackRows consecutive rows k of one (shard, head)
+// of K or V, a chunk per thread and pass, all its loads issued before its
+// stores.  Grid (ceil(n / kPackRows) * BH, P, 2): the (head, row block) pair,
+// the shard, K or V; the index arithmetic is per block, not per chunk.
+constexpr int kPackRows = 64;
+constexpr int kPackThreads = 256;
+__global__ void __launch_bounds__(kPackThreads) pack_kv_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                                               uint4* __restrict__ kb, uint4* __restrict__ vb, int BH,
+                                                               long long n, int u16, int P, int layout) {
+  const uint4* src = blockIdx.z == 0 ? k : v;
+  uint4* dst = blockIdx.z == 0 ? kb : vb;
+  const int nblk = (int)((n + kPackRows - 1) / kPackRows);
+  const int bh = (int)(blockIdx.x / nblk);
+  const long long k0 = (long long)(blockIdx.x % nblk) * kPackRows;
+  const int r = blockIdx.y;
   const long long N = n * P;
-  const long long total = (long long)P * BH * n * u16;
-  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < total;
-       x += (long long)gridDim.x * blockDim.x) {
-    const long long row = x / u16;  // destination row: (r, bh, kk)
-    const int c = (int)(x % u16);
-    const long long kk = row % n;
-    const long long bh = (row / n) % BH;
-    const long long r = row / (n * BH);
-    dst[x] = src[(bh * N + natural_pos(layout, n, P, r, kk)) * u16 + c];
+  const int per_pass = kPackThreads / u16;  // rows per pass: 16 (d = 128) or 32 (d = 64)
+  const int passes = kPackRows / per_pass;  // 4 or 2
+  const int c = threadIdx.x % u16;
+  const int kr = threadIdx.x / u16;
+  const uint4* s_head = src + (long long)bh * N * u16 + c;
+  uint4* d_rows = dst + ((long long)r * BH + bh) * n * u16 + c;
+  uint4 buf[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const long long kk = k0 + p * per_pass + kr;
+    if (p < passes && kk < n) buf[p] = s_head[natural_pos(layout, n, P, r, kk) * u16];
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const long long kk = k0 + p * per_pass + kr;
+    if (p < passes && kk < n) d_rows[kk * u16] = buf[p];
   }
 }
 
@@ -336,11 +354,12 @@ int launch_finalize(const float* m, const float* l, const float* o, float* out, 
 
 int launch_pack_kv(const void* k, const void* v, void* kbuf, void* vbuf, int BH, long long n, int d, int P,
                    int layout, void* stream) {
-  const int u16 = d * 2 / 16;
-  const long long total = (long long)P * BH * n * u16;
-  if (total <= 0) return 0;
-  dim3 grid(grid_for(total, 256), 2);
-  pack_kv_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  const int u16 = d * 2 / 16;  // 8 or 16: kPackThreads is a multiple, kPackRows * u16 of kPackThreads
+  if ((long long)P * BH * n <= 0) return 0;
+  const long long blocks = (n + kPackRows - 1) / kPackRows * BH;
+  if (blocks > 0x7fffffffLL || P > 65535) return (int)cudaErrorInvalidValue;
+  dim3 grid((unsigned)blocks, (unsigned)P, 2);
+  pack_kv_kernel<<<grid, kPackThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(kbuf),
       static_cast<uint4*>(vbuf), BH, n, u16, P, layout);
   return (int)cudaGetLastError();
