@@ -215,14 +215,22 @@ int begin_timed_call(ring_attn* h, FwdTiming** out) {
     h->t_read = false;
   }
   if ((int)h->tsets.size() <= h->t_next) {
-    h->tsets.emplace_back();
-    FwdTiming& T = h->tsets.back();
+    FwdTiming T;
     const int P = h->plan.P;
-    int rc;
+    int rc = RING_OK;
     for (auto* v : {&T.k0, &T.k1, &T.c0, &T.c1, &T.w0, &T.w1, &T.r0})
-      if ((rc = make_events(*v, P, cudaEventDefault))) return rc;
-    RA_CUDA(cudaEventCreate(&T.p0), "cudaEventCreate");
-    RA_CUDA(cudaEventCreate(&T.p1), "cudaEventCreate");
+      if (!rc) rc = make_events(*v, P, cudaEventDefault);
+    if (!rc && cudaEventCreate(&T.p0) != cudaSuccess) rc = fail(RING_ERR_CUDA, "cudaEventCreate");
+    if (!rc && cudaEventCreate(&T.p1) != cudaSuccess) rc = fail(RING_ERR_CUDA, "cudaEventCreate");
+    if (rc) {  // release what was made; the set is not kept
+      for (auto* v : {&T.k0, &T.k1, &T.c0, &T.c1, &T.w0, &T.w1, &T.r0})
+        for (auto e : *v)
+          if (e) cudaEventDestroy(e);
+      for (cudaEvent_t e : {T.p0, T.p1})
+        if (e) cudaEventDestroy(e);
+      return rc;
+    }
+    h->tsets.push_back(std::move(T));
   }
   *out = &h->tsets[h->t_next];
   return RING_OK;
