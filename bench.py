@@ -369,7 +369,7 @@ def measure_imbalance(names=("contiguous-8k", "striped-8k", "zigzag-8k"), reps=5
         ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(w.P)]
               for _ in range(w.P)]
         samples = [[[] for _ in range(w.P)] for _ in range(w.P)]  # [s][r]
-        for rep in range(reps + 1):  # round 0 warms up
+        for rep in range(reps + 1):  # repetition 0 warms up
             for s in range(w.P):
                 for r in range(w.P):
                     j = (r - s) % w.P
